@@ -1,0 +1,98 @@
+// pkv_internal.h -- descriptors and kernel launchers shared by the host core
+// (pkv_host.cpp) and the kernels (pkv_kernels.cu).  Not part of the C ABI.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace pkv {
+
+// One batch row: a sequence appending and attending n_q consecutive rows.
+struct RowDesc {
+    int32_t slot;      // page-table row of the sequence on the device
+    int32_t past_len;  // tokens committed before this call (seq_len)
+    int32_t n_q;       // rows appended and attended by this call
+    int32_t q_row0;    // first of this row's rows in Q / K_new / V_new / out
+};
+
+// One split-K work unit: query qi of row `row`, keys [split*S, (split+1)*S)
+// clipped to the visible range.  part >= 0 indexes this unit's partial record
+// (the query has several splits); part < 0 means the unit writes out directly.
+struct UnitDesc {
+    int32_t row, qi, split, part;
+};
+
+// One query whose splits are combined by the merge kernel.
+struct MergeDesc {
+    int32_t row, qi, part0, n_split;
+};
+
+// One appended token row: position `pos` of sequence page-table row `slot`
+// receives row `src_row` of K_new / V_new.
+struct AppendDesc {
+    int32_t slot, pos, src_row, pad;
+};
+
+// A run of page-table entries to upload: pt[slot][start .. start+count) =
+// vals[voff .. voff+count).
+struct PtRun {
+    int32_t slot, start, count, voff;
+};
+
+// One copy-on-append block copy (every layer, K and V).
+struct CopyDesc {
+    int32_t src, dst;
+};
+
+// Address of a key/value row in the paged pool:
+//   pool[pt[slot][pos / bs]][layer][pos % bs][kv_head*hd ...]
+struct PagedAddr {
+    float *k, *v;
+    const int32_t *pt;
+    int64_t block_stride;  // floats per block: n_layers * bs * kv_dim
+    int64_t layer_off;     // floats to the layer: layer * bs * kv_dim
+    int32_t kv_dim, bs, bs_shift, max_blocks, n_blocks;
+};
+
+// Address of a key/value row in a contiguous history: base[pos][kv_head*hd ...]
+struct ContigAddr {
+    const float *k, *v;
+    int32_t kv_dim;
+};
+
+struct AttnArgs {
+    const float *Q;
+    float *out;
+    const RowDesc *rows;
+    const UnitDesc *units;
+    int32_t n_units;
+    float *pm, *pl, *pacc;  // partials: [n_part][n_heads], [n_part][n_heads], [n_part][n_heads][hd]
+    int32_t n_heads, n_kv, hd, group, causal, split_keys;
+    float scale_log2;       // scale * log2(e): scores are kept in base-2 units
+    int32_t *err;
+};
+
+struct MergeArgs {
+    const float *pm, *pl, *pacc;
+    float *out;
+    const RowDesc *rows;
+    const MergeDesc *items;
+    int32_t n_items, n_heads, hd;
+};
+
+// Kernel launchers (pkv_kernels.cu).  Each enqueues exactly one kernel.
+cudaError_t launch_pt_apply(int32_t *pt_dev, int32_t max_blocks, const PtRun *runs, int32_t n_runs,
+                            const int32_t *vals, cudaStream_t s);
+cudaError_t launch_append(const float *K_new, const float *V_new, const AppendDesc *items,
+                          int32_t n_items, const PagedAddr &addr, int32_t *err, cudaStream_t s);
+cudaError_t launch_copy_blocks(float *k, float *v, const CopyDesc *items, int32_t n_items,
+                               int64_t block_floats, int32_t n_blocks, int32_t *err,
+                               cudaStream_t s);
+cudaError_t launch_decode_paged(const AttnArgs &a, const PagedAddr &addr, cudaStream_t s);
+cudaError_t launch_decode_contig(const AttnArgs &a, const ContigAddr &addr, cudaStream_t s);
+cudaError_t launch_merge(const MergeArgs &a, cudaStream_t s);
+
+// Largest head_dim the decode kernels accept.
+constexpr int kMaxHeadDim = 256;
+
+}  // namespace pkv
