@@ -37,6 +37,12 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#if defined(__GNUC__)
+#define PKV_API __attribute__((visibility("default")))
+#else
+#define PKV_API
+#endif
+
 #ifdef __cplusplus
 extern "C" {
 #endif
@@ -74,68 +80,68 @@ typedef void *pkv_stream_t; /* cudaStream_t */
  * one page table.  The free list is a LIFO stack whose first pops are 0,1,2,...
  * Returns NULL on failure (bad sizes, out of memory).  With PKV_POOL_HOST_ONLY
  * the pool keeps metadata only and the device pointers / stream are ignored. */
-pkv_pool *pkv_pool_new(int32_t n_blocks, int32_t n_layers, int32_t kv_dim, int32_t block_size,
+PKV_API pkv_pool *pkv_pool_new(int32_t n_blocks, int32_t n_layers, int32_t kv_dim, int32_t block_size,
                        float *k_pool_dev, float *v_pool_dev, int32_t max_seqs,
                        int32_t max_blocks_per_seq, pkv_stream_t stream, uint32_t flags);
 
 /* Release the pool, every sequence still alive in it, and library-owned memory.
  * Waits for the pool stream first. */
-void pkv_pool_free(pkv_pool *pool);
+PKV_API void pkv_pool_free(pkv_pool *pool);
 
 /* Rebind the pool stream.  The caller orders the old stream's work before the
  * new stream's (e.g. by synchronising).  Returns PKV_OK or PKV_ERR_ARG. */
-int pkv_pool_set_stream(pkv_pool *pool, pkv_stream_t stream);
+PKV_API int pkv_pool_set_stream(pkv_pool *pool, pkv_stream_t stream);
 
 /* Device base addresses of the K and V pools (NULL for a host-only pool). */
-float *pkv_pool_k_data(const pkv_pool *pool);
-float *pkv_pool_v_data(const pkv_pool *pool);
+PKV_API float *pkv_pool_k_data(const pkv_pool *pool);
+PKV_API float *pkv_pool_v_data(const pkv_pool *pool);
 
 /* Number of blocks on the free list, or -1 for NULL. */
-int32_t pkv_pool_free_blocks(const pkv_pool *pool);
+PKV_API int32_t pkv_pool_free_blocks(const pkv_pool *pool);
 
 /* Allocate one block: its id (refcount 1), or -1 when the pool is exhausted
  * ("nx_paged_kv_gate.nx source", KAT section: ids 0,1,2 then -1). */
-int64_t pkv_alloc_block(pkv_pool *pool);
+PKV_API int64_t pkv_alloc_block(pkv_pool *pool);
 
 /* Drop one reference; at zero the id returns to the free list and is the next
  * one handed out (KAT section: a freed id recycles).  PKV_ERR_ARG for an id
  * out of range or not allocated. */
-int pkv_unref_block(pkv_pool *pool, int64_t id);
+PKV_API int pkv_unref_block(pkv_pool *pool, int64_t id);
 
 /* Refcount of a block (0 when free), or -1 for an id out of range
  * ("nx_paged_kv_gate.nx source", FORK section reads pool.refcnt[id]). */
-int32_t pkv_refcnt(const pkv_pool *pool, int64_t id);
+PKV_API int32_t pkv_refcnt(const pkv_pool *pool, int64_t id);
 
 /* ------------------------------------------------------------ sequences ---- */
 
 /* New empty sequence with room for max_tokens tokens ("nx_paged_kv_gate.nx
  * source", EQUIV section: seq_new(pool, 64)).  NULL if max_tokens <= 0, if
  * ceil(max_tokens / block_size) > max_blocks_per_seq, or if max_seqs are live. */
-pkv_seq *pkv_seq_new(pkv_pool *pool, int32_t max_tokens);
+PKV_API pkv_seq *pkv_seq_new(pkv_pool *pool, int32_t max_tokens);
 
 /* Fork: a new sequence sharing every block of the parent (refcount + 1 each)
  * with the same length ("nx_paged_kv_gate.nx source", FORK section).  Writes
  * into a shared block are preceded by a private copy (copy-on-append, see
  * pkv_ensure_append).  NULL on failure. */
-pkv_seq *pkv_seq_fork(pkv_seq *parent);
+PKV_API pkv_seq *pkv_seq_fork(pkv_seq *parent);
 
 /* Release a sequence: unreference its blocks, last block first. */
-int pkv_seq_free(pkv_seq *seq);
+PKV_API int pkv_seq_free(pkv_seq *seq);
 
 /* Speculative-decode rewind ("nx_paged_kv_gate.nx source", REWIND section):
  * len := new_len, blocks with index >= ceil(new_len / block_size) are
  * unreferenced (last first).  PKV_ERR_ARG unless 0 <= new_len <= len. */
-int pkv_seq_truncate(pkv_seq *seq, int32_t new_len);
+PKV_API int pkv_seq_truncate(pkv_seq *seq, int32_t new_len);
 
 /* Current length (tokens already committed by pkv_advance), or -1 for NULL. */
-int32_t pkv_seq_len(const pkv_seq *seq);
+PKV_API int32_t pkv_seq_len(const pkv_seq *seq);
 
 /* Copy up to cap page-table entries (block ids, in position order) to out (host).
  * Returns the number of entries the table holds, or -1 for NULL seq. */
-int32_t pkv_seq_page_table(const pkv_seq *seq, int32_t *out, int32_t cap);
+PKV_API int32_t pkv_seq_page_table(const pkv_seq *seq, int32_t *out, int32_t cap);
 
 /* Pool slot of the sequence's page-table row on the device (0..max_seqs-1), or -1. */
-int32_t pkv_seq_slot(const pkv_seq *seq);
+PKV_API int32_t pkv_seq_slot(const pkv_seq *seq);
 
 /* Make positions [len, len+n) writable, once per step before layer 0
  * ("nx_f32_attn_paged.nx source", caller contract; "nx_f32_llama_v4b.nx
@@ -145,19 +151,19 @@ int32_t pkv_seq_slot(const pkv_seq *seq);
  * tail blocks are allocated, both in ascending block index.  All-or-nothing:
  * PKV_ERR_CAPACITY if len+n > max_tokens, PKV_ERR_EXHAUSTED if the pool has
  * too few free blocks -- nothing changes in either case.  PKV_ERR_ARG if n <= 0. */
-int pkv_ensure_append(pkv_seq *seq, int32_t n);
+PKV_API int pkv_ensure_append(pkv_seq *seq, int32_t n);
 
 /* pkv_ensure_append for M sequences, all-or-nothing over the whole batch;
  * n is a host array of M counts.  Duplicate sequences -> PKV_ERR_ARG. */
-int pkv_ensure_append_batch(pkv_seq *const *seqs, int32_t M, const int32_t *n);
+PKV_API int pkv_ensure_append_batch(pkv_seq *const *seqs, int32_t M, const int32_t *n);
 
 /* Commit n appended tokens, once per step after the last layer
  * ("nx_f32_attn_paged.nx source", caller contract).  PKV_ERR_SEQ if no block
  * covers the new length, PKV_ERR_CAPACITY past max_tokens, PKV_ERR_ARG if n <= 0. */
-int pkv_advance(pkv_seq *seq, int32_t n);
+PKV_API int pkv_advance(pkv_seq *seq, int32_t n);
 
 /* pkv_advance for M sequences (validated as a whole, then applied). */
-int pkv_advance_batch(pkv_seq *const *seqs, int32_t M, const int32_t *n);
+PKV_API int pkv_advance_batch(pkv_seq *const *seqs, int32_t M, const int32_t *n);
 
 /* ------------------------------------------------------------ per layer ---- */
 
@@ -165,7 +171,7 @@ int pkv_advance_batch(pkv_seq *const *seqs, int32_t M, const int32_t *n);
  * at positions len..len+n_tokens-1 of layer `layer` through the page table
  * (the append step of "nx_f32_attn_paged.nx source": blocks pre-ensured).
  * PKV_ERR_SEQ if those rows are not in existing private blocks. */
-int pkv_append_layer(pkv_seq *seq, int32_t layer, const float *K_new, const float *V_new,
+PKV_API int pkv_append_layer(pkv_seq *seq, int32_t layer, const float *K_new, const float *V_new,
                      int32_t n_tokens);
 
 /* Append + attend for one sequence and one layer (nx_f32_attn_with_paged,
@@ -177,7 +183,7 @@ int pkv_append_layer(pkv_seq *seq, int32_t layer, const float *K_new, const floa
  * [n_tokens, n_kv_heads*head_dim]; n_kv_heads*head_dim must equal the pool's
  * kv_dim, head_dim <= 256.  Checks, in order: sizes <= 0 -> PKV_ERR_BAD_DIM;
  * grouping -> PKV_ERR_BAD_GQA; NULL seq or rows not ensured -> PKV_ERR_SEQ. */
-int pkv_attn_with_paged(const float *Q, const float *K_new, const float *V_new,
+PKV_API int pkv_attn_with_paged(const float *Q, const float *K_new, const float *V_new,
                         int32_t n_tokens, int32_t n_heads, int32_t n_kv_heads, int32_t head_dim,
                         pkv_seq *seq, int32_t layer, int32_t causal, float scale, float *out);
 
@@ -188,14 +194,14 @@ int pkv_attn_with_paged(const float *Q, const float *K_new, const float *V_new,
  * (offset-causal).  n_q is a host array.  Each row's result equals the M = 1
  * call on that row bit for bit.  Errors as pkv_attn_with_paged; duplicate
  * sequences -> PKV_ERR_ARG. */
-int pkv_attn_batch(pkv_seq *const *seqs, int32_t M, const int32_t *n_q, const float *Q,
+PKV_API int pkv_attn_batch(pkv_seq *const *seqs, int32_t M, const int32_t *n_q, const float *Q,
                    const float *K_new, const float *V_new, int32_t n_heads, int32_t n_kv_heads,
                    int32_t head_dim, int32_t layer, int32_t causal, float scale, float *out);
 
 /* pkv_attn_batch taking HOST buffers for Q, K_new, V_new and out: copies the
  * inputs to device staging, runs the batch, copies out back, and returns when
  * out is filled (pinned host memory makes the copies asynchronous DMA). */
-int pkv_attn_batch_host(pkv_seq *const *seqs, int32_t M, const int32_t *n_q, const float *Q_host,
+PKV_API int pkv_attn_batch_host(pkv_seq *const *seqs, int32_t M, const int32_t *n_q, const float *Q_host,
                         const float *K_new_host, const float *V_new_host, int32_t n_heads,
                         int32_t n_kv_heads, int32_t head_dim, int32_t layer, int32_t causal,
                         float scale, float *out_host);
@@ -205,7 +211,7 @@ int pkv_attn_batch_host(pkv_seq *const *seqs, int32_t M, const int32_t *n_q, con
  * history.  Kc, Vc: device [total_k, n_kv_heads*head_dim], already holding the
  * n_q new rows at the end; Q, out: device [n_q, n_heads*head_dim].  For the
  * same history it returns the paged path's output bit for bit. */
-int pkv_attn_contiguous(const float *Q, const float *Kc, const float *Vc, int32_t n_q,
+PKV_API int pkv_attn_contiguous(const float *Q, const float *Kc, const float *Vc, int32_t n_q,
                         int32_t total_k, int32_t n_heads, int32_t n_kv_heads, int32_t head_dim,
                         int32_t causal, float scale, float *out, pkv_stream_t stream);
 
@@ -214,17 +220,17 @@ int pkv_attn_contiguous(const float *Q, const float *Kc, const float *Vc, int32_
 /* Wait for the pool stream, then return and clear the pool's device error
  * flag: PKV_OK, PKV_ERR_DEVICE_BOUNDS (a kernel met a block id or page index
  * out of range and skipped that access), or PKV_ERR_CUDA. */
-int pkv_sync_error(pkv_pool *pool);
+PKV_API int pkv_sync_error(pkv_pool *pool);
 
 /* Upload pending page-table changes now (they are otherwise uploaded by the
  * next device call on the pool). */
-int pkv_pool_flush(pkv_pool *pool);
+PKV_API int pkv_pool_flush(pkv_pool *pool);
 
 /* Keys per split-K work unit of the decode kernels (default 512, a multiple of
  * 32 in [32, 65536]).  Process-wide; every call uses the value current at the
  * call, so results stay bit-exact between calls made under one setting. */
-int pkv_set_split_keys(int32_t keys);
-int32_t pkv_get_split_keys(void);
+PKV_API int pkv_set_split_keys(int32_t keys);
+PKV_API int32_t pkv_get_split_keys(void);
 
 /* Kernel launch accounting.  pkv_launch_count: kernels launched by the library
  * so far (all kinds).  When profiling is on, every launch is bracketed by CUDA
@@ -240,13 +246,13 @@ enum pkv_kernel_kind {
     PKV_KERNEL_PAGETABLE = 5,
     PKV_KERNEL_KINDS = 6
 };
-int64_t pkv_launch_count(void);
-int pkv_profile_enable(int32_t on);
-int pkv_profile_reset(void);
-int pkv_profile_read(int32_t kind, double *ms, int64_t *launches);
+PKV_API int64_t pkv_launch_count(void);
+PKV_API int pkv_profile_enable(int32_t on);
+PKV_API int pkv_profile_reset(void);
+PKV_API int pkv_profile_read(int32_t kind, double *ms, int64_t *launches);
 
 /* Description of the calling thread's last failure ("" if none). */
-const char *pkv_last_error(void);
+PKV_API const char *pkv_last_error(void);
 
 #ifdef __cplusplus
 }

@@ -1,0 +1,1071 @@
+// pkv_host.cpp -- host core and C ABI of libpkv.
+//
+// Host side of the paged KV cache: the refcounted block pool (LIFO free
+// stack, refcounts), sequences with their page tables, ensure_append with
+// copy-on-append, advance, fork, truncate; and the per-layer calls that build
+// one descriptor blob per call (page-table changes, batch rows, append rows,
+// split-K work units, merge items), upload it through a pinned staging ring
+// and launch the kernels on the pool stream.
+//
+// Call contract: "nx_f32_attn_paged.nx source" (header comment: ensure_append
+// once per step, append + attend per layer, advance once after all layers);
+// pool behaviour: "nx_paged_kv_gate.nx source" (KAT, FORK, REWIND sections).
+#include "../../include/pkv.h"
+#include "pkv_internal.h"
+
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <atomic>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <unordered_map>
+#include <vector>
+
+using namespace pkv;
+
+// ------------------------------------------------------------------ state ----
+namespace {
+
+thread_local std::string g_last_error;
+
+int fail(int code, const char *fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return code;
+}
+
+int cuda_fail(cudaError_t e, const char *what) {
+    return fail(PKV_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+std::atomic<int32_t> g_split_keys{512};
+std::atomic<int64_t> g_launches{0};
+
+// Optional per-launch CUDA-event timing.
+struct Profiler {
+    std::mutex mu;
+    bool on = false;
+    struct Rec {
+        int kind;
+        cudaEvent_t a, b;
+    };
+    std::vector<Rec> recs;
+    std::vector<cudaEvent_t> spare;
+    double ms[PKV_KERNEL_KINDS] = {};
+    int64_t n[PKV_KERNEL_KINDS] = {};
+
+    cudaEvent_t get() {
+        if (!spare.empty()) {
+            cudaEvent_t e = spare.back();
+            spare.pop_back();
+            return e;
+        }
+        cudaEvent_t e = nullptr;
+        cudaEventCreate(&e);
+        return e;
+    }
+    // Fold finished records into the totals (caller holds mu).
+    void drain() {
+        for (auto &r : recs) {
+            cudaEventSynchronize(r.b);
+            float t = 0.f;
+            if (cudaEventElapsedTime(&t, r.a, r.b) == cudaSuccess) {
+                ms[r.kind] += t;
+                n[r.kind] += 1;
+            }
+            spare.push_back(r.a);
+            spare.push_back(r.b);
+        }
+        recs.clear();
+    }
+};
+Profiler g_prof;
+
+// Enqueue one kernel through `f`, counting it and (when profiling) timing it.
+template <class F>
+cudaError_t launch(int kind, cudaStream_t s, F &&f) {
+    cudaEvent_t a = nullptr, b = nullptr;
+    bool on;
+    {
+        std::lock_guard<std::mutex> lk(g_prof.mu);
+        on = g_prof.on;
+        if (on) {
+            a = g_prof.get();
+            b = g_prof.get();
+        }
+    }
+    if (on) cudaEventRecord(a, s);
+    cudaError_t e = f();
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    if (on) {
+        cudaEventRecord(b, s);
+        std::lock_guard<std::mutex> lk(g_prof.mu);
+        g_prof.recs.push_back({kind, a, b});
+    }
+    return e;
+}
+
+// The library's stream-ordered memory pool, one per device; memory is kept
+// (release threshold = max) so steady-state calls reuse it without the OS.
+std::mutex g_mempool_mu;
+cudaMemPool_t g_mempool[64] = {};
+
+cudaError_t mempool_for(int dev, cudaMemPool_t *out) {
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lk(g_mempool_mu);
+    if (!g_mempool[dev]) {
+        cudaMemPoolProps props = {};
+        props.allocType = cudaMemAllocationTypePinned;
+        props.handleTypes = cudaMemHandleTypeNone;
+        props.location.type = cudaMemLocationTypeDevice;
+        props.location.id = dev;
+        cudaMemPool_t mp = nullptr;
+        cudaError_t e = cudaMemPoolCreate(&mp, &props);
+        if (e != cudaSuccess) return e;
+        uint64_t thr = ~0ull;
+        cudaMemPoolSetAttribute(mp, cudaMemPoolAttrReleaseThreshold, &thr);
+        g_mempool[dev] = mp;
+    }
+    *out = g_mempool[dev];
+    return cudaSuccess;
+}
+
+// Growable stream-ordered device buffer.
+struct DevBuf {
+    void *p = nullptr;
+    size_t cap = 0;
+    cudaError_t ensure(size_t n, cudaStream_t s, int dev) {
+        if (n <= cap) return cudaSuccess;
+        cudaMemPool_t mp;
+        cudaError_t e = mempool_for(dev, &mp);
+        if (e != cudaSuccess) return e;
+        if (p) cudaFreeAsync(p, s);
+        p = nullptr;
+        cap = 0;
+        size_t nc = std::max<size_t>(n, 4096);
+        e = cudaMallocFromPoolAsync(&p, nc, mp, s);
+        if (e != cudaSuccess) {
+            p = nullptr;
+            return e;
+        }
+        cap = nc;
+        return cudaSuccess;
+    }
+    void release(cudaStream_t s) {
+        if (p) cudaFreeAsync(p, s);
+        p = nullptr;
+        cap = 0;
+    }
+};
+
+// Pinned staging ring for host->device descriptor uploads.  A slot is reused
+// only after the copy that last read it has completed.
+struct Stager {
+    static constexpr int N = 8;
+    struct Slot {
+        void *h = nullptr;
+        size_t cap = 0;
+        cudaEvent_t ev = nullptr;
+        bool pending = false;
+    };
+    Slot slots[N];
+    int next = 0;
+
+    cudaError_t upload(void *dst, const void *src, size_t n, cudaStream_t s) {
+        Slot &sl = slots[next];
+        next = (next + 1) % N;
+        if (sl.pending) {
+            cudaEventSynchronize(sl.ev);
+            sl.pending = false;
+        }
+        if (sl.cap < n) {
+            if (sl.h) cudaFreeHost(sl.h);
+            sl.h = nullptr;
+            sl.cap = 0;
+            size_t nc = std::max<size_t>(n, 64 * 1024);
+            cudaError_t e = cudaMallocHost(&sl.h, nc);
+            if (e != cudaSuccess) return e;
+            sl.cap = nc;
+        }
+        if (!sl.ev) {
+            cudaError_t e = cudaEventCreateWithFlags(&sl.ev, cudaEventDisableTiming);
+            if (e != cudaSuccess) return e;
+        }
+        std::memcpy(sl.h, src, n);
+        cudaError_t e = cudaMemcpyAsync(dst, sl.h, n, cudaMemcpyHostToDevice, s);
+        if (e != cudaSuccess) return e;
+        e = cudaEventRecord(sl.ev, s);
+        if (e != cudaSuccess) return e;
+        sl.pending = true;
+        return cudaSuccess;
+    }
+    void destroy() {
+        for (auto &sl : slots) {
+            if (sl.pending) cudaEventSynchronize(sl.ev);
+            if (sl.ev) cudaEventDestroy(sl.ev);
+            if (sl.h) cudaFreeHost(sl.h);
+            sl = Slot{};
+        }
+    }
+};
+
+// Host-side descriptor blob; sections start on 16-byte boundaries.
+struct Blob {
+    std::vector<unsigned char> b;
+    void clear() { b.clear(); }
+    template <class T>
+    size_t put(const T *data, size_t count) {
+        size_t off = (b.size() + 15) & ~static_cast<size_t>(15);
+        b.resize(off + count * sizeof(T));
+        if (count) std::memcpy(b.data() + off, data, count * sizeof(T));
+        return off;
+    }
+    size_t size() const { return std::max<size_t>(b.size(), 16); }
+};
+
+struct DevGuard {
+    int prev = -1;
+    explicit DevGuard(int dev) {
+        if (cudaGetDevice(&prev) == cudaSuccess && prev != dev) cudaSetDevice(dev);
+    }
+    ~DevGuard() {
+        int cur = -1;
+        if (prev >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != prev) cudaSetDevice(prev);
+    }
+};
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+int32_t ceil_div(int64_t a, int64_t b) { return static_cast<int32_t>((a + b - 1) / b); }
+
+}  // namespace
+
+// ------------------------------------------------------------- pool, seq ----
+
+struct pkv_seq;
+
+struct pkv_pool {
+    int32_t n_blocks = 0, n_layers = 0, kv_dim = 0, bs = 0, bs_shift = -1;
+    int32_t max_seqs = 0, max_blocks = 0;
+    bool host_only = false;
+    float *k = nullptr, *v = nullptr;
+    bool owns_kv = false;
+    int32_t *pt_dev = nullptr;
+    int32_t *err_dev = nullptr;
+    cudaStream_t stream = nullptr;
+    int device = 0;
+
+    std::vector<int32_t> free_stack;   // top = back
+    std::vector<int32_t> refcnt;
+    std::vector<int32_t> free_slots;   // top = back
+    std::vector<pkv_seq *> slot_owner;
+    std::vector<pkv_seq *> dirty;      // sequences with page-table entries not yet uploaded
+
+    Stager stager;
+    DevBuf desc, part, io_in, io_out;
+    Blob blob;
+
+    int64_t block_floats() const { return static_cast<int64_t>(n_layers) * bs * kv_dim; }
+};
+
+struct pkv_seq {
+    pkv_pool *pool = nullptr;
+    int32_t slot = -1, len = 0, max_tokens = 0;
+    std::vector<int32_t> pt;
+    int32_t dlo = 0, dhi = 0;
+    bool dirty = false;
+};
+
+namespace {
+
+void mark_dirty(pkv_seq *s, int32_t lo, int32_t hi) {
+    pkv_pool *p = s->pool;
+    if (p->host_only || hi <= lo) return;
+    if (!s->dirty) {
+        s->dirty = true;
+        s->dlo = lo;
+        s->dhi = hi;
+        p->dirty.push_back(s);
+    } else {
+        s->dlo = std::min(s->dlo, lo);
+        s->dhi = std::max(s->dhi, hi);
+    }
+}
+
+int32_t pop_block(pkv_pool *p) {
+    if (p->free_stack.empty()) return -1;
+    int32_t b = p->free_stack.back();
+    p->free_stack.pop_back();
+    p->refcnt[b] = 1;
+    return b;
+}
+
+void unref(pkv_pool *p, int32_t b) {
+    if (--p->refcnt[b] == 0) p->free_stack.push_back(b);
+}
+
+// Page-table changes since the last upload, as runs into the blob.
+void put_pt_runs(pkv_pool *p, Blob &blob, size_t *runs_off, int32_t *n_runs, size_t *vals_off) {
+    std::vector<PtRun> runs;
+    std::vector<int32_t> vals;
+    for (pkv_seq *s : p->dirty) {
+        const int32_t hi = std::min<int32_t>(s->dhi, static_cast<int32_t>(s->pt.size()));
+        if (hi > s->dlo) {
+            runs.push_back({s->slot, s->dlo, hi - s->dlo, static_cast<int32_t>(vals.size())});
+            vals.insert(vals.end(), s->pt.begin() + s->dlo, s->pt.begin() + hi);
+        }
+        s->dirty = false;
+    }
+    p->dirty.clear();
+    *runs_off = blob.put(runs.data(), runs.size());
+    *vals_off = blob.put(vals.data(), vals.size());
+    *n_runs = static_cast<int32_t>(runs.size());
+}
+
+PagedAddr paged_addr(const pkv_pool *p, int32_t layer) {
+    PagedAddr a;
+    a.k = p->k;
+    a.v = p->v;
+    a.pt = p->pt_dev;
+    a.block_stride = p->block_floats();
+    a.layer_off = static_cast<int64_t>(layer) * p->bs * p->kv_dim;
+    a.kv_dim = p->kv_dim;
+    a.bs = p->bs;
+    a.bs_shift = p->bs_shift;
+    a.max_blocks = p->max_blocks;
+    a.n_blocks = p->n_blocks;
+    return a;
+}
+
+// Rows [len, len+n) lie in existing blocks of refcount 1.
+bool can_append(const pkv_seq *s, int32_t n) {
+    const pkv_pool *p = s->pool;
+    if (static_cast<int64_t>(s->len) + n > static_cast<int64_t>(s->pt.size()) * p->bs) return false;
+    for (int32_t k = s->len / p->bs; k <= (s->len + n - 1) / p->bs; ++k)
+        if (p->refcnt[s->pt[k]] != 1) return false;
+    return true;
+}
+
+// Split-K work list for a set of rows.  Units with a full split of S keys come
+// first (the heavy ones), each query's last (ragged) split after them.
+struct WorkList {
+    std::vector<UnitDesc> units;
+    std::vector<MergeDesc> merges;
+    int64_t n_part = 0;
+};
+
+void build_work(const std::vector<RowDesc> &rows, int causal, int32_t S, WorkList &w) {
+    std::vector<UnitDesc> tail;
+    w.units.clear();
+    w.merges.clear();
+    w.n_part = 0;
+    for (int32_t r = 0; r < static_cast<int32_t>(rows.size()); ++r) {
+        const RowDesc &rd = rows[r];
+        const int32_t total_k = rd.past_len + rd.n_q;
+        for (int32_t i = 0; i < rd.n_q; ++i) {
+            const int32_t q_pos = total_k - rd.n_q + i;
+            const int32_t nk = causal ? q_pos + 1 : total_k;
+            const int32_t ns = ceil_div(nk, S);
+            if (ns == 1) {
+                tail.push_back({r, i, 0, -1});
+            } else {
+                const int32_t part0 = static_cast<int32_t>(w.n_part);
+                w.n_part += ns;
+                w.merges.push_back({r, i, part0, ns});
+                for (int32_t s = 0; s + 1 < ns; ++s) w.units.push_back({r, i, s, part0 + s});
+                tail.push_back({r, i, ns - 1, part0 + ns - 1});
+            }
+        }
+    }
+    w.units.insert(w.units.end(), tail.begin(), tail.end());
+}
+
+int check_heads(int32_t n_heads, int32_t n_kv_heads, int32_t head_dim) {
+    if (n_heads <= 0 || n_kv_heads <= 0 || head_dim <= 0)
+        return fail(PKV_ERR_BAD_DIM, "n_heads, n_kv_heads and head_dim must be positive");
+    if (n_heads % n_kv_heads != 0)
+        return fail(PKV_ERR_BAD_GQA, "n_heads (%d) is not a multiple of n_kv_heads (%d)", n_heads,
+                    n_kv_heads);
+    return PKV_OK;
+}
+
+int check_dup(const pkv_pool *p, pkv_seq *const *seqs, int32_t M) {
+    std::vector<char> seen(p->max_seqs, 0);
+    for (int32_t r = 0; r < M; ++r) {
+        if (seen[seqs[r]->slot]) return fail(PKV_ERR_ARG, "sequence appears twice in the batch");
+        seen[seqs[r]->slot] = 1;
+    }
+    return PKV_OK;
+}
+
+// Upload the blob to the pool's descriptor buffer.
+cudaError_t upload_blob(pkv_pool *p) {
+    cudaError_t e = p->desc.ensure(p->blob.size(), p->stream, p->device);
+    if (e != cudaSuccess) return e;
+    return p->stager.upload(p->desc.p, p->blob.b.data(), p->blob.b.size(), p->stream);
+}
+
+template <class T>
+const T *dptr(const pkv_pool *p, size_t off) {
+    return reinterpret_cast<const T *>(static_cast<unsigned char *>(p->desc.p) + off);
+}
+
+// Shared body of pkv_attn_batch / pkv_attn_with_paged / pkv_attn_batch_host /
+// pkv_append_layer.  `attend` = false stops after the append.
+int run_layer(pkv_seq *const *seqs, int32_t M, const int32_t *n_q, const float *Q,
+              const float *K_new, const float *V_new, int32_t n_heads, int32_t n_kv_heads,
+              int32_t head_dim, int32_t layer, int32_t causal, float scale, float *out,
+              bool host_io, bool attend) {
+    // checks in the order of nx_f32_attn_with_paged: sizes, grouping, sequence
+    if (M <= 0 || !n_q) return fail(PKV_ERR_BAD_DIM, "M must be positive and n_q non-NULL");
+    for (int32_t r = 0; r < M; ++r)
+        if (n_q[r] <= 0) return fail(PKV_ERR_BAD_DIM, "n_q[%d] = %d must be positive", r, n_q[r]);
+    if (attend) {
+        int rc = check_heads(n_heads, n_kv_heads, head_dim);
+        if (rc) return rc;
+    }
+    if (!seqs) return fail(PKV_ERR_SEQ, "seqs is NULL");
+    for (int32_t r = 0; r < M; ++r)
+        if (!seqs[r] || !seqs[r]->pool) return fail(PKV_ERR_SEQ, "sequence %d is NULL", r);
+    pkv_pool *p = seqs[0]->pool;
+    for (int32_t r = 1; r < M; ++r)
+        if (seqs[r]->pool != p) return fail(PKV_ERR_ARG, "sequences of different pools in one batch");
+    if (p->host_only) return fail(PKV_ERR_ARG, "host-only pool has no device storage");
+    if (attend) {
+        if (static_cast<int64_t>(n_kv_heads) * head_dim != p->kv_dim)
+            return fail(PKV_ERR_BAD_DIM, "n_kv_heads*head_dim = %d differs from the pool's kv_dim %d",
+                        n_kv_heads * head_dim, p->kv_dim);
+        if (head_dim > kMaxHeadDim)
+            return fail(PKV_ERR_BAD_DIM, "head_dim %d > %d is not supported", head_dim, kMaxHeadDim);
+    }
+    if (layer < 0 || layer >= p->n_layers)
+        return fail(PKV_ERR_ARG, "layer %d outside [0, %d)", layer, p->n_layers);
+    if (!K_new || !V_new || (attend && (!Q || !out)))
+        return fail(PKV_ERR_ARG, "NULL data pointer");
+    if (!host_io && (!aligned16(K_new) || !aligned16(V_new) || (attend && (!aligned16(Q) || !aligned16(out)))))
+        return fail(PKV_ERR_ARG, "device pointers must be 16-byte aligned");
+    {
+        int rc = check_dup(p, seqs, M);
+        if (rc) return rc;
+    }
+    for (int32_t r = 0; r < M; ++r)
+        if (!can_append(seqs[r], n_q[r]))
+            return fail(PKV_ERR_SEQ, "rows [%d, %d) of batch row %d are not ensured (call pkv_ensure_append)",
+                        seqs[r]->len, seqs[r]->len + n_q[r], r);
+
+    DevGuard dg(p->device);
+    cudaStream_t st = p->stream;
+    const int32_t q_dim = n_heads * head_dim;
+    const int32_t kv_dim = p->kv_dim;
+
+    std::vector<RowDesc> rows(M);
+    std::vector<AppendDesc> app;
+    int64_t T = 0;
+    for (int32_t r = 0; r < M; ++r) {
+        rows[r] = {seqs[r]->slot, seqs[r]->len, n_q[r], static_cast<int32_t>(T)};
+        for (int32_t t = 0; t < n_q[r]; ++t)
+            app.push_back({seqs[r]->slot, seqs[r]->len + t, static_cast<int32_t>(T + t), 0});
+        T += n_q[r];
+    }
+    if (T > 0x7fffffffLL / std::max(q_dim, kv_dim)) return fail(PKV_ERR_BAD_DIM, "batch too large");
+
+    WorkList w;
+    const int32_t S = g_split_keys.load();
+    if (attend) build_work(rows, causal, S, w);
+
+    Blob &blob = p->blob;
+    blob.clear();
+    size_t runs_off, vals_off;
+    int32_t n_runs;
+    put_pt_runs(p, blob, &runs_off, &n_runs, &vals_off);
+    const size_t rows_off = blob.put(rows.data(), rows.size());
+    const size_t app_off = blob.put(app.data(), app.size());
+    const size_t units_off = blob.put(w.units.data(), w.units.size());
+    const size_t merges_off = blob.put(w.merges.data(), w.merges.size());
+
+    cudaError_t e = upload_blob(p);
+    if (e != cudaSuccess) return cuda_fail(e, "descriptor upload");
+
+    const float *Qd = Q, *Kd = K_new, *Vd = V_new;
+    float *Od = out;
+    if (host_io) {
+        const size_t in_bytes = static_cast<size_t>(T) * (q_dim + 2 * kv_dim) * sizeof(float);
+        e = p->io_in.ensure(in_bytes, st, p->device);
+        if (e == cudaSuccess) e = p->io_out.ensure(static_cast<size_t>(T) * q_dim * sizeof(float), st, p->device);
+        if (e != cudaSuccess) return cuda_fail(e, "staging buffers");
+        float *base = static_cast<float *>(p->io_in.p);
+        float *qd = base, *kd = base + T * q_dim, *vd = kd + T * kv_dim;
+        e = cudaMemcpyAsync(qd, Q, sizeof(float) * T * q_dim, cudaMemcpyHostToDevice, st);
+        if (e == cudaSuccess) e = cudaMemcpyAsync(kd, K_new, sizeof(float) * T * kv_dim, cudaMemcpyHostToDevice, st);
+        if (e == cudaSuccess) e = cudaMemcpyAsync(vd, V_new, sizeof(float) * T * kv_dim, cudaMemcpyHostToDevice, st);
+        if (e != cudaSuccess) return cuda_fail(e, "input copy");
+        Qd = qd;
+        Kd = kd;
+        Vd = vd;
+        Od = static_cast<float *>(p->io_out.p);
+    }
+
+    if (n_runs > 0) {
+        e = launch(PKV_KERNEL_PAGETABLE, st, [&] {
+            return launch_pt_apply(p->pt_dev, p->max_blocks, dptr<PtRun>(p, runs_off), n_runs,
+                                   dptr<int32_t>(p, vals_off), st);
+        });
+        if (e != cudaSuccess) return cuda_fail(e, "page-table upload kernel");
+    }
+    const PagedAddr addr = paged_addr(p, layer);
+    e = launch(PKV_KERNEL_APPEND, st, [&] {
+        return launch_append(Kd, Vd, dptr<AppendDesc>(p, app_off), static_cast<int32_t>(T), addr,
+                             p->err_dev, st);
+    });
+    if (e != cudaSuccess) return cuda_fail(e, "append kernel");
+    if (!attend) return PKV_OK;
+
+    AttnArgs a{};
+    a.Q = Qd;
+    a.out = Od;
+    a.rows = dptr<RowDesc>(p, rows_off);
+    a.units = dptr<UnitDesc>(p, units_off);
+    a.n_units = static_cast<int32_t>(w.units.size());
+    a.n_heads = n_heads;
+    a.n_kv = n_kv_heads;
+    a.hd = head_dim;
+    a.group = n_heads / n_kv_heads;
+    a.causal = causal ? 1 : 0;
+    a.split_keys = S;
+    a.scale_log2 = scale * 1.4426950408889634f;
+    a.err = p->err_dev;
+    if (w.n_part > 0) {
+        const size_t pf = static_cast<size_t>(w.n_part) * n_heads;
+        e = p->part.ensure(pf * (2 + head_dim) * sizeof(float), st, p->device);
+        if (e != cudaSuccess) return cuda_fail(e, "partials buffer");
+        a.pm = static_cast<float *>(p->part.p);
+        a.pl = a.pm + pf;
+        a.pacc = a.pl + pf;
+    }
+    e = launch(PKV_KERNEL_DECODE, st, [&] { return launch_decode_paged(a, addr, st); });
+    if (e != cudaSuccess) return cuda_fail(e, "decode kernel");
+    if (!w.merges.empty()) {
+        MergeArgs m{a.pm, a.pl, a.pacc, Od, a.rows, dptr<MergeDesc>(p, merges_off),
+                    static_cast<int32_t>(w.merges.size()), n_heads, head_dim};
+        e = launch(PKV_KERNEL_MERGE, st, [&] { return launch_merge(m, st); });
+        if (e != cudaSuccess) return cuda_fail(e, "merge kernel");
+    }
+    if (host_io) {
+        e = cudaMemcpyAsync(out, Od, sizeof(float) * T * q_dim, cudaMemcpyDeviceToHost, st);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+        if (e != cudaSuccess) return cuda_fail(e, "output copy");
+    }
+    return PKV_OK;
+}
+
+// Contiguous-path globals: one staging ring and error word per device.
+std::mutex g_contig_mu;
+Stager g_contig_stager[64];
+int32_t *g_contig_err[64] = {};
+
+}  // namespace
+
+// ================================================================== C ABI ====
+extern "C" {
+
+const char *pkv_last_error(void) { return g_last_error.c_str(); }
+
+pkv_pool *pkv_pool_new(int32_t n_blocks, int32_t n_layers, int32_t kv_dim, int32_t block_size,
+                       float *k_pool_dev, float *v_pool_dev, int32_t max_seqs,
+                       int32_t max_blocks_per_seq, pkv_stream_t stream, uint32_t flags) {
+    if (n_blocks <= 0 || n_layers <= 0 || kv_dim <= 0 || block_size <= 0 || max_seqs <= 0 ||
+        max_blocks_per_seq <= 0) {
+        fail(PKV_ERR_BAD_DIM, "pool sizes must be positive");
+        return nullptr;
+    }
+    if (static_cast<int64_t>(max_seqs) * max_blocks_per_seq > (1LL << 31)) {
+        fail(PKV_ERR_BAD_DIM, "max_seqs * max_blocks_per_seq too large");
+        return nullptr;
+    }
+    auto *p = new pkv_pool();
+    p->n_blocks = n_blocks;
+    p->n_layers = n_layers;
+    p->kv_dim = kv_dim;
+    p->bs = block_size;
+    p->bs_shift = (block_size & (block_size - 1)) == 0 ? __builtin_ctz(block_size) : -1;
+    p->max_seqs = max_seqs;
+    p->max_blocks = max_blocks_per_seq;
+    p->host_only = (flags & PKV_POOL_HOST_ONLY) != 0;
+    p->free_stack.resize(n_blocks);
+    for (int32_t i = 0; i < n_blocks; ++i) p->free_stack[i] = n_blocks - 1 - i;
+    p->refcnt.assign(n_blocks, 0);
+    p->free_slots.resize(max_seqs);
+    for (int32_t i = 0; i < max_seqs; ++i) p->free_slots[i] = max_seqs - 1 - i;
+    p->slot_owner.assign(max_seqs, nullptr);
+    if (p->host_only) return p;
+
+    p->stream = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaGetDevice(&p->device);
+    if (e != cudaSuccess) {
+        cuda_fail(e, "cudaGetDevice");
+        delete p;
+        return nullptr;
+    }
+    if ((k_pool_dev == nullptr) != (v_pool_dev == nullptr)) {
+        fail(PKV_ERR_ARG, "pass both K and V pool buffers or neither");
+        delete p;
+        return nullptr;
+    }
+    const size_t pool_bytes = static_cast<size_t>(n_blocks) * p->block_floats() * sizeof(float);
+    if (k_pool_dev) {
+        if (!aligned16(k_pool_dev) || !aligned16(v_pool_dev)) {
+            fail(PKV_ERR_ARG, "pool buffers must be 16-byte aligned");
+            delete p;
+            return nullptr;
+        }
+        p->k = k_pool_dev;
+        p->v = v_pool_dev;
+    } else {
+        e = cudaMalloc(&p->k, pool_bytes);
+        if (e == cudaSuccess) e = cudaMalloc(&p->v, pool_bytes);
+        if (e != cudaSuccess) {
+            cuda_fail(e, "pool allocation");
+            cudaFree(p->k);
+            delete p;
+            return nullptr;
+        }
+        p->owns_kv = true;
+    }
+    e = cudaMalloc(&p->pt_dev, static_cast<size_t>(max_seqs) * max_blocks_per_seq * sizeof(int32_t));
+    if (e == cudaSuccess) e = cudaMalloc(&p->err_dev, sizeof(int32_t));
+    if (e == cudaSuccess)
+        e = cudaMemsetAsync(p->pt_dev, 0xff, static_cast<size_t>(max_seqs) * max_blocks_per_seq * sizeof(int32_t),
+                            p->stream);
+    if (e == cudaSuccess) e = cudaMemsetAsync(p->err_dev, 0, sizeof(int32_t), p->stream);
+    if (e != cudaSuccess) {
+        cuda_fail(e, "pool metadata allocation");
+        pkv_pool_free(p);
+        return nullptr;
+    }
+    return p;
+}
+
+void pkv_pool_free(pkv_pool *p) {
+    if (!p) return;
+    for (pkv_seq *s : p->slot_owner) delete s;
+    p->slot_owner.clear();
+    if (!p->host_only) {
+        DevGuard dg(p->device);
+        p->desc.release(p->stream);
+        p->part.release(p->stream);
+        p->io_in.release(p->stream);
+        p->io_out.release(p->stream);
+        cudaStreamSynchronize(p->stream);
+        p->stager.destroy();
+        if (p->owns_kv) {
+            cudaFree(p->k);
+            cudaFree(p->v);
+        }
+        cudaFree(p->pt_dev);
+        cudaFree(p->err_dev);
+    }
+    delete p;
+}
+
+int pkv_pool_set_stream(pkv_pool *p, pkv_stream_t stream) {
+    if (!p) return fail(PKV_ERR_ARG, "NULL pool");
+    p->stream = static_cast<cudaStream_t>(stream);
+    return PKV_OK;
+}
+
+float *pkv_pool_k_data(const pkv_pool *p) { return p ? p->k : nullptr; }
+float *pkv_pool_v_data(const pkv_pool *p) { return p ? p->v : nullptr; }
+int32_t pkv_pool_free_blocks(const pkv_pool *p) {
+    return p ? static_cast<int32_t>(p->free_stack.size()) : -1;
+}
+
+int64_t pkv_alloc_block(pkv_pool *p) {
+    if (!p) {
+        fail(PKV_ERR_ARG, "NULL pool");
+        return -1;
+    }
+    int32_t b = pop_block(p);
+    if (b < 0) fail(PKV_ERR_EXHAUSTED, "pool exhausted");
+    return b;
+}
+
+int pkv_unref_block(pkv_pool *p, int64_t id) {
+    if (!p) return fail(PKV_ERR_ARG, "NULL pool");
+    if (id < 0 || id >= p->n_blocks || p->refcnt[id] <= 0)
+        return fail(PKV_ERR_ARG, "block %lld is not allocated", static_cast<long long>(id));
+    unref(p, static_cast<int32_t>(id));
+    return PKV_OK;
+}
+
+int32_t pkv_refcnt(const pkv_pool *p, int64_t id) {
+    if (!p || id < 0 || id >= p->n_blocks) return -1;
+    return p->refcnt[id];
+}
+
+pkv_seq *pkv_seq_new(pkv_pool *p, int32_t max_tokens) {
+    if (!p) {
+        fail(PKV_ERR_ARG, "NULL pool");
+        return nullptr;
+    }
+    if (max_tokens <= 0 || ceil_div(max_tokens, p->bs) > p->max_blocks) {
+        fail(PKV_ERR_CAPACITY, "max_tokens %d outside (0, %lld]", max_tokens,
+             static_cast<long long>(p->max_blocks) * p->bs);
+        return nullptr;
+    }
+    if (p->free_slots.empty()) {
+        fail(PKV_ERR_CAPACITY, "max_seqs sequences are live");
+        return nullptr;
+    }
+    auto *s = new pkv_seq();
+    s->pool = p;
+    s->slot = p->free_slots.back();
+    p->free_slots.pop_back();
+    s->max_tokens = max_tokens;
+    p->slot_owner[s->slot] = s;
+    return s;
+}
+
+pkv_seq *pkv_seq_fork(pkv_seq *parent) {
+    if (!parent) {
+        fail(PKV_ERR_SEQ, "NULL sequence");
+        return nullptr;
+    }
+    pkv_pool *p = parent->pool;
+    if (p->free_slots.empty()) {
+        fail(PKV_ERR_CAPACITY, "max_seqs sequences are live");
+        return nullptr;
+    }
+    auto *s = new pkv_seq();
+    s->pool = p;
+    s->slot = p->free_slots.back();
+    p->free_slots.pop_back();
+    s->max_tokens = parent->max_tokens;
+    s->len = parent->len;
+    s->pt = parent->pt;
+    for (int32_t b : s->pt) p->refcnt[b] += 1;
+    p->slot_owner[s->slot] = s;
+    mark_dirty(s, 0, static_cast<int32_t>(s->pt.size()));
+    return s;
+}
+
+int pkv_seq_free(pkv_seq *s) {
+    if (!s) return fail(PKV_ERR_ARG, "NULL sequence");
+    pkv_pool *p = s->pool;
+    for (auto it = s->pt.rbegin(); it != s->pt.rend(); ++it) unref(p, *it);
+    if (s->dirty) p->dirty.erase(std::remove(p->dirty.begin(), p->dirty.end(), s), p->dirty.end());
+    p->slot_owner[s->slot] = nullptr;
+    p->free_slots.push_back(s->slot);
+    delete s;
+    return PKV_OK;
+}
+
+int pkv_seq_truncate(pkv_seq *s, int32_t new_len) {
+    if (!s) return fail(PKV_ERR_ARG, "NULL sequence");
+    if (new_len < 0 || new_len > s->len)
+        return fail(PKV_ERR_ARG, "truncate to %d outside [0, %d]", new_len, s->len);
+    pkv_pool *p = s->pool;
+    const int32_t keep = ceil_div(new_len, p->bs);
+    for (int32_t k = static_cast<int32_t>(s->pt.size()) - 1; k >= keep; --k) unref(p, s->pt[k]);
+    if (static_cast<int32_t>(s->pt.size()) > keep) s->pt.resize(keep);
+    s->len = new_len;
+    return PKV_OK;
+}
+
+int32_t pkv_seq_len(const pkv_seq *s) { return s ? s->len : -1; }
+int32_t pkv_seq_slot(const pkv_seq *s) { return s ? s->slot : -1; }
+
+int32_t pkv_seq_page_table(const pkv_seq *s, int32_t *out, int32_t cap) {
+    if (!s) return -1;
+    const int32_t n = static_cast<int32_t>(s->pt.size());
+    if (out)
+        for (int32_t i = 0; i < std::min(n, cap); ++i) out[i] = s->pt[i];
+    return n;
+}
+
+int pkv_ensure_append_batch(pkv_seq *const *seqs, int32_t M, const int32_t *n) {
+    if (M <= 0 || !seqs || !n) return fail(PKV_ERR_ARG, "empty batch");
+    for (int32_t r = 0; r < M; ++r)
+        if (!seqs[r]) return fail(PKV_ERR_ARG, "sequence %d is NULL", r);
+    pkv_pool *p = seqs[0]->pool;
+    for (int32_t r = 1; r < M; ++r)
+        if (seqs[r]->pool != p) return fail(PKV_ERR_ARG, "sequences of different pools in one batch");
+    {
+        int rc = check_dup(p, seqs, M);
+        if (rc) return rc;
+    }
+    // pass 1: validate row by row and count blocks, as the rows would consume
+    // them in order (a block shared by two rows is copied by the first only)
+    std::unordered_map<int32_t, int32_t> dec;
+    int64_t needed = 0;
+    const int64_t avail = static_cast<int64_t>(p->free_stack.size());
+    for (int32_t r = 0; r < M; ++r) {
+        const pkv_seq *s = seqs[r];
+        if (n[r] <= 0) return fail(PKV_ERR_ARG, "n[%d] = %d must be positive", r, n[r]);
+        if (static_cast<int64_t>(s->len) + n[r] > s->max_tokens)
+            return fail(PKV_ERR_CAPACITY, "row %d: len %d + %d exceeds max_tokens %d", r, s->len, n[r],
+                        s->max_tokens);
+        const int32_t first = s->len / p->bs;
+        const int32_t last = (s->len + n[r] - 1) / p->bs;
+        const int32_t have = static_cast<int32_t>(s->pt.size());
+        for (int32_t k = first; k <= last && k < have; ++k) {
+            const int32_t b = s->pt[k];
+            auto it = dec.find(b);
+            const int32_t eff = p->refcnt[b] - (it == dec.end() ? 0 : it->second);
+            if (eff > 1) {
+                ++needed;
+                ++dec[b];
+            }
+        }
+        needed += std::max(0, last + 1 - have);
+        if (needed > avail)
+            return fail(PKV_ERR_EXHAUSTED, "pool exhausted (%lld blocks needed, %lld free)",
+                        static_cast<long long>(needed), static_cast<long long>(avail));
+    }
+    // pass 2: apply
+    std::vector<CopyDesc> copies;
+    for (int32_t r = 0; r < M; ++r) {
+        pkv_seq *s = seqs[r];
+        const int32_t first = s->len / p->bs;
+        const int32_t last = (s->len + n[r] - 1) / p->bs;
+        const int32_t have = static_cast<int32_t>(s->pt.size());
+        for (int32_t k = first; k <= last && k < have; ++k) {
+            const int32_t b = s->pt[k];
+            if (p->refcnt[b] > 1) {
+                const int32_t nb = pop_block(p);
+                copies.push_back({b, nb});
+                unref(p, b);
+                s->pt[k] = nb;
+                mark_dirty(s, k, k + 1);
+            }
+        }
+        for (int32_t k = have; k <= last; ++k) s->pt.push_back(pop_block(p));
+        mark_dirty(s, have, last + 1);
+    }
+    if (copies.empty() || p->host_only) return PKV_OK;
+
+    DevGuard dg(p->device);
+    p->blob.clear();
+    const size_t off = p->blob.put(copies.data(), copies.size());
+    cudaError_t e = upload_blob(p);
+    if (e != cudaSuccess) return cuda_fail(e, "copy list upload");
+    e = launch(PKV_KERNEL_COPY, p->stream, [&] {
+        return launch_copy_blocks(p->k, p->v, dptr<CopyDesc>(p, off), static_cast<int32_t>(copies.size()),
+                                  p->block_floats(), p->n_blocks, p->err_dev, p->stream);
+    });
+    if (e != cudaSuccess) return cuda_fail(e, "copy-on-append kernel");
+    return PKV_OK;
+}
+
+int pkv_ensure_append(pkv_seq *s, int32_t n) { return pkv_ensure_append_batch(&s, 1, &n); }
+
+int pkv_advance_batch(pkv_seq *const *seqs, int32_t M, const int32_t *n) {
+    if (M <= 0 || !seqs || !n) return fail(PKV_ERR_ARG, "empty batch");
+    for (int32_t r = 0; r < M; ++r)
+        if (!seqs[r]) return fail(PKV_ERR_ARG, "sequence %d is NULL", r);
+    pkv_pool *p = seqs[0]->pool;
+    for (int32_t r = 1; r < M; ++r)
+        if (seqs[r]->pool != p) return fail(PKV_ERR_ARG, "sequences of different pools in one batch");
+    {
+        int rc = check_dup(p, seqs, M);
+        if (rc) return rc;
+    }
+    for (int32_t r = 0; r < M; ++r) {
+        const pkv_seq *s = seqs[r];
+        if (n[r] <= 0) return fail(PKV_ERR_ARG, "n[%d] = %d must be positive", r, n[r]);
+        if (static_cast<int64_t>(s->len) + n[r] > s->max_tokens)
+            return fail(PKV_ERR_CAPACITY, "row %d: advance past max_tokens", r);
+        if (static_cast<int64_t>(s->len) + n[r] > static_cast<int64_t>(s->pt.size()) * p->bs)
+            return fail(PKV_ERR_SEQ, "row %d: advance past the ensured blocks", r);
+    }
+    for (int32_t r = 0; r < M; ++r) seqs[r]->len += n[r];
+    return PKV_OK;
+}
+
+int pkv_advance(pkv_seq *s, int32_t n) { return pkv_advance_batch(&s, 1, &n); }
+
+int pkv_append_layer(pkv_seq *seq, int32_t layer, const float *K_new, const float *V_new,
+                     int32_t n_tokens) {
+    return run_layer(&seq, 1, &n_tokens, nullptr, K_new, V_new, 0, 0, 0, layer, 0, 0.f, nullptr,
+                     false, false);
+}
+
+int pkv_attn_with_paged(const float *Q, const float *K_new, const float *V_new, int32_t n_tokens,
+                        int32_t n_heads, int32_t n_kv_heads, int32_t head_dim, pkv_seq *seq,
+                        int32_t layer, int32_t causal, float scale, float *out) {
+    if (n_tokens <= 0) return fail(PKV_ERR_BAD_DIM, "n_tokens must be positive");
+    return run_layer(&seq, 1, &n_tokens, Q, K_new, V_new, n_heads, n_kv_heads, head_dim, layer,
+                     causal, scale, out, false, true);
+}
+
+int pkv_attn_batch(pkv_seq *const *seqs, int32_t M, const int32_t *n_q, const float *Q,
+                   const float *K_new, const float *V_new, int32_t n_heads, int32_t n_kv_heads,
+                   int32_t head_dim, int32_t layer, int32_t causal, float scale, float *out) {
+    return run_layer(seqs, M, n_q, Q, K_new, V_new, n_heads, n_kv_heads, head_dim, layer, causal,
+                     scale, out, false, true);
+}
+
+int pkv_attn_batch_host(pkv_seq *const *seqs, int32_t M, const int32_t *n_q, const float *Q_host,
+                        const float *K_new_host, const float *V_new_host, int32_t n_heads,
+                        int32_t n_kv_heads, int32_t head_dim, int32_t layer, int32_t causal,
+                        float scale, float *out_host) {
+    return run_layer(seqs, M, n_q, Q_host, K_new_host, V_new_host, n_heads, n_kv_heads, head_dim,
+                     layer, causal, scale, out_host, true, true);
+}
+
+int pkv_attn_contiguous(const float *Q, const float *Kc, const float *Vc, int32_t n_q,
+                        int32_t total_k, int32_t n_heads, int32_t n_kv_heads, int32_t head_dim,
+                        int32_t causal, float scale, float *out, pkv_stream_t stream) {
+    if (n_q <= 0) return fail(PKV_ERR_BAD_DIM, "n_q must be positive");
+    int rc = check_heads(n_heads, n_kv_heads, head_dim);
+    if (rc) return rc;
+    if (total_k < n_q) return fail(PKV_ERR_BAD_DIM, "total_k %d < n_q %d", total_k, n_q);
+    if (head_dim > kMaxHeadDim)
+        return fail(PKV_ERR_BAD_DIM, "head_dim %d > %d is not supported", head_dim, kMaxHeadDim);
+    if (!Q || !Kc || !Vc || !out) return fail(PKV_ERR_ARG, "NULL data pointer");
+    if (!aligned16(Q) || !aligned16(Kc) || !aligned16(Vc) || !aligned16(out))
+        return fail(PKV_ERR_ARG, "device pointers must be 16-byte aligned");
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= 64) return fail(PKV_ERR_ARG, "device index out of range");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+    std::vector<RowDesc> rows{{0, total_k - n_q, n_q, 0}};
+    WorkList w;
+    const int32_t S = g_split_keys.load();
+    build_work(rows, causal, S, w);
+    Blob blob;
+    const size_t rows_off = blob.put(rows.data(), 1);
+    const size_t units_off = blob.put(w.units.data(), w.units.size());
+    const size_t merges_off = blob.put(w.merges.data(), w.merges.size());
+    const size_t desc_bytes = (blob.size() + 255) & ~static_cast<size_t>(255);
+    const size_t pf = static_cast<size_t>(w.n_part) * n_heads;
+    const size_t total = desc_bytes + pf * (2 + head_dim) * sizeof(float);
+
+    std::lock_guard<std::mutex> lk(g_contig_mu);
+    if (!g_contig_err[dev]) {
+        e = cudaMalloc(&g_contig_err[dev], sizeof(int32_t));
+        if (e == cudaSuccess) e = cudaMemset(g_contig_err[dev], 0, sizeof(int32_t));
+        if (e != cudaSuccess) return cuda_fail(e, "error word");
+    }
+    cudaMemPool_t mp;
+    e = mempool_for(dev, &mp);
+    if (e != cudaSuccess) return cuda_fail(e, "memory pool");
+    void *mem = nullptr;
+    e = cudaMallocFromPoolAsync(&mem, total, mp, st);
+    if (e != cudaSuccess) return cuda_fail(e, "scratch allocation");
+    unsigned char *base = static_cast<unsigned char *>(mem);
+    e = g_contig_stager[dev].upload(base, blob.b.data(), blob.b.size(), st);
+    if (e != cudaSuccess) {
+        cudaFreeAsync(mem, st);
+        return cuda_fail(e, "descriptor upload");
+    }
+    AttnArgs a{};
+    a.Q = Q;
+    a.out = out;
+    a.rows = reinterpret_cast<const RowDesc *>(base + rows_off);
+    a.units = reinterpret_cast<const UnitDesc *>(base + units_off);
+    a.n_units = static_cast<int32_t>(w.units.size());
+    a.n_heads = n_heads;
+    a.n_kv = n_kv_heads;
+    a.hd = head_dim;
+    a.group = n_heads / n_kv_heads;
+    a.causal = causal ? 1 : 0;
+    a.split_keys = S;
+    a.scale_log2 = scale * 1.4426950408889634f;
+    a.err = g_contig_err[dev];
+    if (pf > 0) {
+        a.pm = reinterpret_cast<float *>(base + desc_bytes);
+        a.pl = a.pm + pf;
+        a.pacc = a.pl + pf;
+    }
+    const ContigAddr addr{Kc, Vc, n_kv_heads * head_dim};
+    e = launch(PKV_KERNEL_DECODE, st, [&] { return launch_decode_contig(a, addr, st); });
+    if (e == cudaSuccess && !w.merges.empty()) {
+        MergeArgs m{a.pm, a.pl, a.pacc, out, a.rows,
+                    reinterpret_cast<const MergeDesc *>(base + merges_off),
+                    static_cast<int32_t>(w.merges.size()), n_heads, head_dim};
+        e = launch(PKV_KERNEL_MERGE, st, [&] { return launch_merge(m, st); });
+    }
+    cudaFreeAsync(mem, st);
+    if (e != cudaSuccess) return cuda_fail(e, "contiguous attention kernels");
+    return PKV_OK;
+}
+
+int pkv_sync_error(pkv_pool *p) {
+    if (!p) return fail(PKV_ERR_ARG, "NULL pool");
+    if (p->host_only) return PKV_OK;
+    DevGuard dg(p->device);
+    cudaError_t e = cudaStreamSynchronize(p->stream);
+    if (e != cudaSuccess) return cuda_fail(e, "stream synchronize");
+    int32_t h = 0;
+    e = cudaMemcpy(&h, p->err_dev, sizeof h, cudaMemcpyDeviceToHost);
+    if (e == cudaSuccess && h) e = cudaMemset(p->err_dev, 0, sizeof h);
+    if (e != cudaSuccess) return cuda_fail(e, "error word");
+    if (h) return fail(PKV_ERR_DEVICE_BOUNDS, "a kernel met a page-table entry out of range");
+    return PKV_OK;
+}
+
+int pkv_pool_flush(pkv_pool *p) {
+    if (!p) return fail(PKV_ERR_ARG, "NULL pool");
+    if (p->host_only || p->dirty.empty()) return PKV_OK;
+    DevGuard dg(p->device);
+    p->blob.clear();
+    size_t runs_off, vals_off;
+    int32_t n_runs;
+    put_pt_runs(p, p->blob, &runs_off, &n_runs, &vals_off);
+    if (n_runs == 0) return PKV_OK;
+    cudaError_t e = upload_blob(p);
+    if (e != cudaSuccess) return cuda_fail(e, "page-table upload");
+    e = launch(PKV_KERNEL_PAGETABLE, p->stream, [&] {
+        return launch_pt_apply(p->pt_dev, p->max_blocks, dptr<PtRun>(p, runs_off), n_runs,
+                               dptr<int32_t>(p, vals_off), p->stream);
+    });
+    if (e != cudaSuccess) return cuda_fail(e, "page-table upload kernel");
+    return PKV_OK;
+}
+
+int pkv_set_split_keys(int32_t keys) {
+    if (keys < 32 || keys > 65536 || (keys % 32) != 0)
+        return fail(PKV_ERR_ARG, "split keys %d: need a multiple of 32 in [32, 65536]", keys);
+    g_split_keys.store(keys);
+    return PKV_OK;
+}
+int32_t pkv_get_split_keys(void) { return g_split_keys.load(); }
+
+int64_t pkv_launch_count(void) { return g_launches.load(); }
+
+int pkv_profile_enable(int32_t on) {
+    std::lock_guard<std::mutex> lk(g_prof.mu);
+    g_prof.on = on != 0;
+    return PKV_OK;
+}
+
+int pkv_profile_reset(void) {
+    std::lock_guard<std::mutex> lk(g_prof.mu);
+    g_prof.drain();
+    for (int k = 0; k < PKV_KERNEL_KINDS; ++k) {
+        g_prof.ms[k] = 0;
+        g_prof.n[k] = 0;
+    }
+    return PKV_OK;
+}
+
+int pkv_profile_read(int32_t kind, double *ms, int64_t *launches) {
+    if (kind < 0 || kind >= PKV_KERNEL_KINDS) return fail(PKV_ERR_ARG, "kernel kind %d", kind);
+    std::lock_guard<std::mutex> lk(g_prof.mu);
+    g_prof.drain();
+    if (ms) *ms = g_prof.ms[kind];
+    if (launches) *launches = g_prof.n[kind];
+    return PKV_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,666 @@
+// pkv_kernels.cu -- sm_103a kernels of libpkv.
+//
+//   pt_apply      upload page-table entries changed on the host
+//   append_rows   scatter each layer's K_new / V_new rows into their blocks
+//                 (the append step of "nx_f32_attn_paged.nx source")
+//   copy_blocks   copy-on-append: duplicate shared blocks (every layer, K and V)
+//   decode_fast   split-K attention, head_dim 128, query group 1/2/4: one CTA
+//                 per (work unit, kv head); the whole GQA group of query heads
+//                 reuses every K/V row ("nx_f32_attn_paged.nx source", step 3:
+//                 query head h reads kv head h / group)
+//   decode_generic the same computation for any head_dim <= 256 and group
+//   merge_splits  log-sum-exp merge of the split partials
+//
+// The attention kernels are templates over an address functor: PagedAddr
+// reads rows through the page table, ContigAddr from a contiguous history.
+// Everything else -- the split boundaries (multiples of S keys), the tile
+// order, every reduction tree -- depends only on token positions, so the paged
+// and the contiguous instantiations return the same bits, and a batch row
+// returns the same bits as the same row launched alone.
+#include "pkv_internal.h"
+
+#include <cstdio>
+
+namespace pkv {
+namespace {
+
+constexpr unsigned kFull = 0xffffffffu;
+
+__device__ __forceinline__ void cp_async16(void *smem, const void *gmem) {
+    const unsigned s = static_cast<unsigned>(__cvta_generic_to_shared(smem));
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(s), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
+}
+
+__device__ __forceinline__ void flag_error(int32_t *err, int code) {
+    if (err) atomicOr(err, code);
+}
+
+// ------------------------------------------------------------ addressing ----
+
+struct PagedRows {
+    PagedAddr a;
+    // Row of (slot, pos) for kv head `kvh`; false (and the error flag) when the
+    // page index or the block id is out of range -- the access is skipped.
+    __device__ __forceinline__ bool row(int slot, int pos, int kvh, int hd, const float *&kr,
+                                        const float *&vr, int32_t *err) const {
+        const int bi = a.bs_shift >= 0 ? (pos >> a.bs_shift) : (pos / a.bs);
+        const int off = pos - bi * a.bs;
+        if (bi >= a.max_blocks) {
+            flag_error(err, 1);
+            return false;
+        }
+        const int blk = __ldg(a.pt + static_cast<size_t>(slot) * a.max_blocks + bi);
+        if (static_cast<unsigned>(blk) >= static_cast<unsigned>(a.n_blocks)) {
+            flag_error(err, 1);
+            return false;
+        }
+        const size_t o = static_cast<size_t>(blk) * a.block_stride + a.layer_off +
+                         static_cast<size_t>(off) * a.kv_dim + static_cast<size_t>(kvh) * hd;
+        kr = a.k + o;
+        vr = a.v + o;
+        return true;
+    }
+};
+
+struct ContigRows {
+    ContigAddr a;
+    __device__ __forceinline__ bool row(int, int pos, int kvh, int hd, const float *&kr,
+                                        const float *&vr, int32_t *) const {
+        const size_t o = static_cast<size_t>(pos) * a.kv_dim + static_cast<size_t>(kvh) * hd;
+        kr = a.k + o;
+        vr = a.v + o;
+        return true;
+    }
+};
+
+// The key range of one work unit.
+struct UnitRange {
+    int kbeg, kend;
+};
+__device__ __forceinline__ UnitRange unit_range(const UnitDesc &u, const RowDesc &rd, int causal,
+                                                int split_keys) {
+    const int total_k = rd.past_len + rd.n_q;
+    const int q_pos = total_k - rd.n_q + u.qi;  // offset-causal query position
+    const int lim = causal ? q_pos + 1 : total_k;
+    const int kbeg = u.split * split_keys;
+    const int kend = min(kbeg + split_keys, lim);
+    return {kbeg, kend};
+}
+
+// ------------------------------------------------------------- page table ----
+
+__global__ void pt_apply_kernel(int32_t *pt, int32_t max_blocks, const PtRun *runs,
+                                const int32_t *vals) {
+    const PtRun r = runs[blockIdx.x];
+    int32_t *dst = pt + static_cast<size_t>(r.slot) * max_blocks + r.start;
+    for (int i = threadIdx.x; i < r.count; i += blockDim.x) dst[i] = vals[r.voff + i];
+}
+
+// ----------------------------------------------------------------- append ----
+
+// One warp per (token row, K or V).
+__global__ void append_rows_kernel(const float *__restrict__ K_new, const float *__restrict__ V_new,
+                                   const AppendDesc *__restrict__ items, int32_t n_items,
+                                   PagedAddr a, int32_t *err) {
+    const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (gw >= 2 * n_items) return;
+    const AppendDesc d = items[gw >> 1];
+    const bool is_v = gw & 1;
+    const int bi = a.bs_shift >= 0 ? (d.pos >> a.bs_shift) : (d.pos / a.bs);
+    const int off = d.pos - bi * a.bs;
+    if (bi >= a.max_blocks) {
+        if (lane == 0) flag_error(err, 1);
+        return;
+    }
+    const int blk = a.pt[static_cast<size_t>(d.slot) * a.max_blocks + bi];
+    if (static_cast<unsigned>(blk) >= static_cast<unsigned>(a.n_blocks)) {
+        if (lane == 0) flag_error(err, 1);
+        return;
+    }
+    float *dst = (is_v ? a.v : a.k) + static_cast<size_t>(blk) * a.block_stride + a.layer_off +
+                 static_cast<size_t>(off) * a.kv_dim;
+    const float *src = (is_v ? V_new : K_new) + static_cast<size_t>(d.src_row) * a.kv_dim;
+    if ((a.kv_dim & 3) == 0) {
+        const float4 *s4 = reinterpret_cast<const float4 *>(src);
+        float4 *d4 = reinterpret_cast<float4 *>(dst);
+        for (int i = lane; i < (a.kv_dim >> 2); i += 32) d4[i] = __ldg(s4 + i);
+    } else {
+        for (int i = lane; i < a.kv_dim; i += 32) dst[i] = src[i];
+    }
+}
+
+// ------------------------------------------------------------- block copy ----
+
+__global__ void copy_blocks_kernel(float *k, float *v, const CopyDesc *__restrict__ items,
+                                   int64_t block_floats, int32_t n_blocks, int32_t *err) {
+    const CopyDesc c = items[blockIdx.y];
+    if (static_cast<unsigned>(c.src) >= static_cast<unsigned>(n_blocks) ||
+        static_cast<unsigned>(c.dst) >= static_cast<unsigned>(n_blocks)) {
+        if (threadIdx.x == 0 && blockIdx.x == 0) flag_error(err, 1);
+        return;
+    }
+    const size_t so = static_cast<size_t>(c.src) * block_floats;
+    const size_t dO = static_cast<size_t>(c.dst) * block_floats;
+    const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
+    if ((block_floats & 3) == 0) {
+        const size_t n4 = static_cast<size_t>(block_floats) >> 2;
+        const float4 *ks = reinterpret_cast<const float4 *>(k + so);
+        const float4 *vs = reinterpret_cast<const float4 *>(v + so);
+        float4 *kd = reinterpret_cast<float4 *>(k + dO);
+        float4 *vd = reinterpret_cast<float4 *>(v + dO);
+        for (size_t i = blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += stride) {
+            kd[i] = ks[i];
+            vd[i] = vs[i];
+        }
+    } else {
+        for (size_t i = blockIdx.x * blockDim.x + threadIdx.x; i < static_cast<size_t>(block_floats);
+             i += stride) {
+            k[dO + i] = k[so + i];
+            v[dO + i] = v[so + i];
+        }
+    }
+}
+
+// ------------------------------------------------- fast decode, hd = 128 ----
+//
+// CTA = 4 warps = one (unit, kv head).  The unit's keys are cut into tiles of
+// T = 8 positions; warp w takes tiles w, w+4, w+8, ... and runs its own
+// NST-stage cp.async pipeline and its own online softmax over them (no block
+// barrier in the main loop).  The four warps' (max, sum, acc) are combined at
+// the end in warp order.
+//
+// Lane layout for Q.K: lane = 8*kg + c.  Lane group kg handles key kg (and
+// kg + 4) of a tile; lane c holds dims {4c + 32i + e : i < 4, e < 4} of every
+// query head of the group (16 dims x G heads, pre-scaled by scale*log2(e)).
+// The 8 lanes of a group reduce their G partial dot products with a
+// reduce-scatter butterfly (xor 4, 2, 1); afterwards lane c holds the full
+// score of head c / (8 / G).  Lane layout for P.V: lane owns dims
+// 4*lane .. 4*lane+3 of every head.
+
+template <int G>
+struct FastCfg {
+    static constexpr int HD = 128;
+    static constexpr int T = 8;   // keys per tile
+    static constexpr int W = 4;   // warps per CTA
+    static constexpr int LPH = 8 / G;  // lanes of a group holding one head's score
+};
+
+template <int G>
+__device__ __forceinline__ float reduce_scatter8(const float (&p)[G], int c);
+
+template <>
+__device__ __forceinline__ float reduce_scatter8<4>(const float (&p)[4], int c) {
+    const bool hi4 = (c & 4) != 0;
+    const float s0 = hi4 ? p[0] : p[2], s1 = hi4 ? p[1] : p[3];
+    float k0 = hi4 ? p[2] : p[0], k1 = hi4 ? p[3] : p[1];
+    k0 += __shfl_xor_sync(kFull, s0, 4);
+    k1 += __shfl_xor_sync(kFull, s1, 4);
+    const bool hi2 = (c & 2) != 0;
+    const float s = hi2 ? k0 : k1;
+    float k = hi2 ? k1 : k0;
+    k += __shfl_xor_sync(kFull, s, 2);
+    k += __shfl_xor_sync(kFull, k, 1);
+    return k;  // head c >> 1
+}
+template <>
+__device__ __forceinline__ float reduce_scatter8<2>(const float (&p)[2], int c) {
+    const bool hi4 = (c & 4) != 0;
+    const float s = hi4 ? p[0] : p[1];
+    float k = hi4 ? p[1] : p[0];
+    k += __shfl_xor_sync(kFull, s, 4);
+    k += __shfl_xor_sync(kFull, k, 2);
+    k += __shfl_xor_sync(kFull, k, 1);
+    return k;  // head c >> 2
+}
+template <>
+__device__ __forceinline__ float reduce_scatter8<1>(const float (&p)[1], int) {
+    float k = p[0];
+    k += __shfl_xor_sync(kFull, k, 4);
+    k += __shfl_xor_sync(kFull, k, 2);
+    k += __shfl_xor_sync(kFull, k, 1);
+    return k;
+}
+
+__device__ __forceinline__ float comp(const float4 &v, int i) {
+    return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
+}
+__device__ __forceinline__ float4 fma4(float s, const float4 &v, const float4 &acc) {
+    return make_float4(fmaf(s, v.x, acc.x), fmaf(s, v.y, acc.y), fmaf(s, v.z, acc.z),
+                       fmaf(s, v.w, acc.w));
+}
+
+template <int G, int NST>
+constexpr size_t fast_smem_bytes() {
+    using C = FastCfg<G>;
+    return static_cast<size_t>(C::W) * NST * C::T * C::HD * 2 * sizeof(float) +
+           static_cast<size_t>(C::W) * (C::T + 1) * 4 * sizeof(float);
+}
+
+template <int G, int NST, class Rows>
+__global__ void __launch_bounds__(128) decode_fast_kernel(AttnArgs a, Rows rows_of) {
+    using C = FastCfg<G>;
+    constexpr int HD = C::HD, T = C::T, W = C::W;
+    constexpr int STAGE = T * HD * 2;          // floats: K rows then V rows
+    constexpr int WARP_FLOATS = NST * STAGE;
+    extern __shared__ __align__(16) float sm[];
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int kg = lane >> 3, c = lane & 7;
+    const int ui = blockIdx.x / a.n_kv;
+    const int kvh = blockIdx.x - ui * a.n_kv;
+    const UnitDesc u = a.units[ui];
+    const RowDesc rd = a.rows[u.row];
+    const UnitRange ur = unit_range(u, rd, a.causal, a.split_keys);
+    const int n_tiles = (ur.kend - ur.kbeg + T - 1) / T;
+    const int my_n = warp < n_tiles ? (n_tiles - warp + W - 1) / W : 0;
+
+    float *wbase = sm + warp * WARP_FLOATS;
+    float *P = sm + W * WARP_FLOATS + warp * (T + 1) * 4;
+
+    // query slice of the group, pre-scaled to base-2 units
+    const float *qrow = a.Q + static_cast<size_t>(rd.q_row0 + u.qi) * (a.n_heads * HD) +
+                        static_cast<size_t>(kvh) * G * HD;
+    float4 q[G][4];
+#pragma unroll
+    for (int g = 0; g < G; ++g)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            float4 t = __ldg(reinterpret_cast<const float4 *>(qrow + g * HD + 4 * c + 32 * i));
+            q[g][i] = make_float4(t.x * a.scale_log2, t.y * a.scale_log2, t.z * a.scale_log2,
+                                  t.w * a.scale_log2);
+        }
+
+    auto load_tile = [&](int k_local, int stage) {
+        const int pos0 = ur.kbeg + (warp + k_local * W) * T;
+        float *Ks = wbase + stage * STAGE;
+        float *Vs = Ks + T * HD;
+#pragma unroll
+        for (int j = 0; j < T; ++j) {
+            const int pos = pos0 + j;
+            if (pos < ur.kend) {
+                const float *kr, *vr;
+                if (rows_of.row(rd.slot, pos, kvh, HD, kr, vr, a.err)) {
+                    cp_async16(Ks + j * HD + lane * 4, kr + lane * 4);
+                    cp_async16(Vs + j * HD + lane * 4, vr + lane * 4);
+                }
+            }
+        }
+    };
+
+#pragma unroll
+    for (int s = 0; s < NST - 1; ++s) {
+        if (s < my_n) load_tile(s, s);
+        cp_async_commit();
+    }
+
+    constexpr int LPH = C::LPH;
+    const int hh = c / LPH;  // the head whose score this lane holds
+    float m_run = -INFINITY, l_run = 0.f;
+    float4 acc[G];
+#pragma unroll
+    for (int g = 0; g < G; ++g) acc[g] = make_float4(0.f, 0.f, 0.f, 0.f);
+
+    for (int k = 0; k < my_n; ++k) {
+        const int kn = k + NST - 1;
+        if (kn < my_n) load_tile(kn, kn % NST);
+        cp_async_commit();
+        cp_async_wait<NST - 1>();
+        __syncwarp();
+
+        const int pos0 = ur.kbeg + (warp + k * W) * T;
+        const int n_valid = min(T, ur.kend - pos0);
+        const float *Ks = wbase + (k % NST) * STAGE;
+        const float *Vs = Ks + T * HD;
+
+        float sc[2];
+#pragma unroll
+        for (int it = 0; it < 2; ++it) {
+            const int j = it * 4 + kg;
+            const float4 *K4 = reinterpret_cast<const float4 *>(Ks + j * HD);
+            float4 kk[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) kk[i] = K4[c + 8 * i];
+            float part[G];
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                float acc_d = 0.f;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    acc_d = fmaf(q[g][i].x, kk[i].x, acc_d);
+                    acc_d = fmaf(q[g][i].y, kk[i].y, acc_d);
+                    acc_d = fmaf(q[g][i].z, kk[i].z, acc_d);
+                    acc_d = fmaf(q[g][i].w, kk[i].w, acc_d);
+                }
+                part[g] = acc_d;
+            }
+            const float s = reduce_scatter8<G>(part, c);
+            sc[it] = (j < n_valid) ? s : -INFINITY;
+        }
+
+        // online softmax for this lane's head over the tile's 8 keys
+        float tmax = fmaxf(sc[0], sc[1]);
+        tmax = fmaxf(tmax, __shfl_xor_sync(kFull, tmax, 8));
+        tmax = fmaxf(tmax, __shfl_xor_sync(kFull, tmax, 16));
+        const float m_new = fmaxf(m_run, tmax);
+        const float alpha = exp2f(m_run - m_new);
+        const float p0 = exp2f(sc[0] - m_new);
+        const float p1 = exp2f(sc[1] - m_new);
+        float ps = p0 + p1;
+        ps += __shfl_xor_sync(kFull, ps, 8);
+        ps += __shfl_xor_sync(kFull, ps, 16);
+        l_run = fmaf(l_run, alpha, ps);
+        m_run = m_new;
+        if ((c % LPH) == 0) {
+            P[kg * 4 + hh] = p0;
+            P[(4 + kg) * 4 + hh] = p1;
+            if (kg == 0) P[T * 4 + hh] = alpha;
+        }
+        __syncwarp();
+
+        const float4 *P4 = reinterpret_cast<const float4 *>(P);
+        const float4 al = P4[T];
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+            const float s = comp(al, g);
+            acc[g] = make_float4(acc[g].x * s, acc[g].y * s, acc[g].z * s, acc[g].w * s);
+        }
+        const float4 *V4 = reinterpret_cast<const float4 *>(Vs);
+#pragma unroll
+        for (int j = 0; j < T; ++j) {
+            if (j < n_valid) {
+                const float4 v = V4[j * 32 + lane];
+                const float4 pj = P4[j];
+#pragma unroll
+                for (int g = 0; g < G; ++g) acc[g] = fma4(comp(pj, g), v, acc[g]);
+            }
+        }
+        __syncwarp();
+    }
+    cp_async_wait<0>();
+    __syncwarp();
+
+    // publish this warp's state in its own (now idle) stage memory
+    float *R = wbase;
+#pragma unroll
+    for (int g = 0; g < G; ++g) reinterpret_cast<float4 *>(R + g * HD)[lane] = acc[g];
+    if (kg == 0 && (c % LPH) == 0) {
+        R[G * HD + hh] = m_run;
+        R[G * HD + G + hh] = l_run;
+    }
+    __syncthreads();
+
+    const int d = threadIdx.x;  // 128 threads <-> 128 dims
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+        float mw[W];
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < W; ++w) {
+            mw[w] = sm[w * WARP_FLOATS + G * HD + g];
+            M = fmaxf(M, mw[w]);
+        }
+        float num = 0.f, den = 0.f;
+#pragma unroll
+        for (int w = 0; w < W; ++w) {
+            if (mw[w] != -INFINITY) {
+                const float wt = exp2f(mw[w] - M);
+                num = fmaf(wt, sm[w * WARP_FLOATS + g * HD + d], num);
+                den = fmaf(wt, sm[w * WARP_FLOATS + G * HD + G + g], den);
+            }
+        }
+        const int h = kvh * G + g;
+        if (u.part < 0) {
+            a.out[static_cast<size_t>(rd.q_row0 + u.qi) * (a.n_heads * HD) +
+                  static_cast<size_t>(h) * HD + d] = num / den;
+        } else {
+            const size_t ph = static_cast<size_t>(u.part) * a.n_heads + h;
+            a.pacc[ph * HD + d] = num;
+            if (d == 0) {
+                a.pm[ph] = M;
+                a.pl[ph] = den;
+            }
+        }
+    }
+}
+
+// --------------------------------------------------------- generic decode ----
+//
+// CTA = 4 warps = one (unit, kv head, chunk of up to 16 query heads).  Warp w
+// takes the unit's keys w, w+4, ...; for each key and head the warp forms the
+// dot product over lanes (d = lane, lane+32, ...) and a butterfly sum, then
+// updates its online softmax; the accumulators live in shared memory.
+
+constexpr int kGenW = 4;
+constexpr int kGenMaxHeads = 16;
+
+__host__ __device__ constexpr size_t generic_smem_floats(int hpc, int hd) {
+    return static_cast<size_t>(hpc) * hd * (1 + kGenW) + 2 * kGenW * hpc;
+}
+
+template <class Rows>
+__global__ void __launch_bounds__(128) decode_generic_kernel(AttnArgs a, Rows rows_of, int hpc) {
+    extern __shared__ __align__(16) float sm[];
+    const int n_chunks = (a.group + hpc - 1) / hpc;
+    int b = blockIdx.x;
+    const int chunk = b % n_chunks;
+    b /= n_chunks;
+    const int kvh = b % a.n_kv;
+    const int ui = b / a.n_kv;
+    const UnitDesc u = a.units[ui];
+    const RowDesc rd = a.rows[u.row];
+    const UnitRange ur = unit_range(u, rd, a.causal, a.split_keys);
+    const int hd = a.hd;
+    const int h0 = kvh * a.group + chunk * hpc;
+    const int nh = min(hpc, a.group - chunk * hpc);
+
+    float *qs = sm;                                // [hpc][hd]
+    float *accs = qs + hpc * hd;                   // [W][hpc][hd]
+    float *ms = accs + kGenW * hpc * hd;           // [W][hpc]
+    float *ls = ms + kGenW * hpc;                  // [W][hpc]
+    const float *qrow = a.Q + static_cast<size_t>(rd.q_row0 + u.qi) * (a.n_heads * hd) +
+                        static_cast<size_t>(h0) * hd;
+    for (int t = threadIdx.x; t < nh * hd; t += blockDim.x) qs[t] = qrow[t] * a.scale_log2;
+    for (int t = threadIdx.x; t < kGenW * hpc * hd; t += blockDim.x) accs[t] = 0.f;
+    __syncthreads();
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    float m[kGenMaxHeads], l[kGenMaxHeads];
+#pragma unroll
+    for (int g = 0; g < kGenMaxHeads; ++g) {
+        m[g] = -INFINITY;
+        l[g] = 0.f;
+    }
+    float *acc = accs + warp * hpc * hd;
+    for (int j = ur.kbeg + warp; j < ur.kend; j += kGenW) {
+        const float *kr, *vr;
+        if (!rows_of.row(rd.slot, j, kvh, hd, kr, vr, a.err)) continue;
+#pragma unroll
+        for (int g = 0; g < kGenMaxHeads; ++g) {
+            if (g < nh) {
+                float part = 0.f;
+                for (int d = lane; d < hd; d += 32) part = fmaf(qs[g * hd + d], kr[d], part);
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(kFull, part, o);
+                const float mn = fmaxf(m[g], part);
+                const float alpha = exp2f(m[g] - mn);
+                const float p = exp2f(part - mn);
+                l[g] = fmaf(l[g], alpha, p);
+                m[g] = mn;
+                for (int d = lane; d < hd; d += 32)
+                    acc[g * hd + d] = fmaf(p, vr[d], acc[g * hd + d] * alpha);
+            }
+        }
+    }
+    if (lane == 0) {
+#pragma unroll
+        for (int g = 0; g < kGenMaxHeads; ++g)
+            if (g < nh) {
+                ms[warp * hpc + g] = m[g];
+                ls[warp * hpc + g] = l[g];
+            }
+    }
+    __syncthreads();
+
+    for (int t = threadIdx.x; t < nh * hd; t += blockDim.x) {
+        const int g = t / hd, d = t - g * hd;
+        float M = -INFINITY;
+        for (int w = 0; w < kGenW; ++w) M = fmaxf(M, ms[w * hpc + g]);
+        float num = 0.f, den = 0.f;
+        for (int w = 0; w < kGenW; ++w) {
+            const float mw = ms[w * hpc + g];
+            if (mw != -INFINITY) {
+                const float wt = exp2f(mw - M);
+                num = fmaf(wt, accs[(w * hpc + g) * hd + d], num);
+                den = fmaf(wt, ls[w * hpc + g], den);
+            }
+        }
+        const int h = h0 + g;
+        if (u.part < 0) {
+            a.out[static_cast<size_t>(rd.q_row0 + u.qi) * (a.n_heads * hd) +
+                  static_cast<size_t>(h) * hd + d] = num / den;
+        } else {
+            const size_t ph = static_cast<size_t>(u.part) * a.n_heads + h;
+            a.pacc[ph * hd + d] = num;
+            if (d == 0) {
+                a.pm[ph] = M;
+                a.pl[ph] = den;
+            }
+        }
+    }
+}
+
+// ------------------------------------------------------------------ merge ----
+
+// One warp per (query, head): out = sum_s 2^(m_s - M) acc_s / sum_s 2^(m_s - M) l_s,
+// splits taken in ascending order.
+__global__ void merge_splits_kernel(MergeArgs a) {
+    const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (gw >= a.n_items * a.n_heads) return;
+    const int it = gw / a.n_heads, h = gw - it * a.n_heads;
+    const MergeDesc md = a.items[it];
+    const RowDesc rd = a.rows[md.row];
+    float M = -INFINITY;
+    for (int s = 0; s < md.n_split; ++s)
+        M = fmaxf(M, a.pm[static_cast<size_t>(md.part0 + s) * a.n_heads + h]);
+    float den = 0.f;
+    for (int s = 0; s < md.n_split; ++s) {
+        const size_t ph = static_cast<size_t>(md.part0 + s) * a.n_heads + h;
+        den = fmaf(exp2f(a.pm[ph] - M), a.pl[ph], den);
+    }
+    float *o = a.out + static_cast<size_t>(rd.q_row0 + md.qi) * (a.n_heads * a.hd) +
+               static_cast<size_t>(h) * a.hd;
+    for (int d = lane; d < a.hd; d += 32) {
+        float num = 0.f;
+        for (int s = 0; s < md.n_split; ++s) {
+            const size_t ph = static_cast<size_t>(md.part0 + s) * a.n_heads + h;
+            num = fmaf(exp2f(a.pm[ph] - M), a.pacc[ph * a.hd + d], num);
+        }
+        o[d] = num / den;
+    }
+}
+
+// -------------------------------------------------------------- dispatch ----
+
+constexpr int kFastStages = 3;
+
+template <int G, class Rows>
+cudaError_t launch_fast(const AttnArgs &a, const Rows &r, cudaStream_t s) {
+    constexpr size_t smem = fast_smem_bytes<G, kFastStages>();
+    static bool configured = false;  // per process; the attribute is per function
+    if (!configured) {
+        cudaError_t e = cudaFuncSetAttribute(decode_fast_kernel<G, kFastStages, Rows>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(smem));
+        if (e != cudaSuccess) return e;
+        configured = true;
+    }
+    const long long grid = static_cast<long long>(a.n_units) * a.n_kv;
+    if (grid <= 0 || grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    decode_fast_kernel<G, kFastStages, Rows><<<static_cast<unsigned>(grid), 128, smem, s>>>(a, r);
+    return cudaGetLastError();
+}
+
+template <class Rows>
+cudaError_t launch_generic(const AttnArgs &a, const Rows &r, cudaStream_t s) {
+    const int hpc = a.group < kGenMaxHeads ? a.group : kGenMaxHeads;
+    const size_t smem = generic_smem_floats(hpc, a.hd) * sizeof(float);
+    static bool configured = false;
+    if (!configured) {
+        cudaError_t e = cudaFuncSetAttribute(decode_generic_kernel<Rows>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(generic_smem_floats(kGenMaxHeads, kMaxHeadDim) * sizeof(float)));
+        if (e != cudaSuccess) return e;
+        configured = true;
+    }
+    const int n_chunks = (a.group + hpc - 1) / hpc;
+    const long long grid = static_cast<long long>(a.n_units) * a.n_kv * n_chunks;
+    if (grid <= 0 || grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    decode_generic_kernel<Rows><<<static_cast<unsigned>(grid), 128, smem, s>>>(a, r, hpc);
+    return cudaGetLastError();
+}
+
+template <class Rows>
+cudaError_t launch_decode(const AttnArgs &a, const Rows &r, cudaStream_t s) {
+    if (a.hd == 128) {
+        if (a.group == 4) return launch_fast<4>(a, r, s);
+        if (a.group == 2) return launch_fast<2>(a, r, s);
+        if (a.group == 1) return launch_fast<1>(a, r, s);
+    }
+    return launch_generic(a, r, s);
+}
+
+}  // namespace
+
+cudaError_t launch_pt_apply(int32_t *pt_dev, int32_t max_blocks, const PtRun *runs, int32_t n_runs,
+                            const int32_t *vals, cudaStream_t s) {
+    if (n_runs <= 0) return cudaSuccess;
+    pt_apply_kernel<<<n_runs, 128, 0, s>>>(pt_dev, max_blocks, runs, vals);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_append(const float *K_new, const float *V_new, const AppendDesc *items,
+                          int32_t n_items, const PagedAddr &addr, int32_t *err, cudaStream_t s) {
+    if (n_items <= 0) return cudaSuccess;
+    const long long warps = 2LL * n_items;
+    const unsigned blocks = static_cast<unsigned>((warps + 7) / 8);
+    append_rows_kernel<<<blocks, 256, 0, s>>>(K_new, V_new, items, n_items, addr, err);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_copy_blocks(float *k, float *v, const CopyDesc *items, int32_t n_items,
+                               int64_t block_floats, int32_t n_blocks, int32_t *err,
+                               cudaStream_t s) {
+    if (n_items <= 0) return cudaSuccess;
+    const long long per = (block_floats + 3) / 4;
+    unsigned bx = static_cast<unsigned>((per + 255) / 256);
+    if (bx > 64) bx = 64;
+    if (bx == 0) bx = 1;
+    dim3 grid(bx, static_cast<unsigned>(n_items));
+    copy_blocks_kernel<<<grid, 256, 0, s>>>(k, v, items, block_floats, n_blocks, err);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_decode_paged(const AttnArgs &a, const PagedAddr &addr, cudaStream_t s) {
+    return launch_decode(a, PagedRows{addr}, s);
+}
+
+cudaError_t launch_decode_contig(const AttnArgs &a, const ContigAddr &addr, cudaStream_t s) {
+    return launch_decode(a, ContigRows{addr}, s);
+}
+
+cudaError_t launch_merge(const MergeArgs &a, cudaStream_t s) {
+    if (a.n_items <= 0) return cudaSuccess;
+    const long long warps = static_cast<long long>(a.n_items) * a.n_heads;
+    const unsigned blocks = static_cast<unsigned>((warps + 7) / 8);
+    merge_splits_kernel<<<blocks, 256, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace pkv

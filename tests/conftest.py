@@ -27,3 +27,15 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+def _ensure_built():
+    """Build the product library and the oracle's C core when missing or stale
+    (compiling is not running: no test here depends on a GPU to build)."""
+    from paged_kv_gqa_nx_gb300 import build as pkv_build
+    pkv_build.build()
+    import oracle
+    oracle.build()
+
+
+_ensure_built()
