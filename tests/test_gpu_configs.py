@@ -1,0 +1,214 @@
+"""Parity at the full workload sizes, through the same entry point and launch
+configuration the benchmark times (pkv_attn_batch, default split size).
+
+* batched decode, M = 64, Qwen3-4B attention shape: every row vs the oracle.
+* continuous-batching decode, M = 256, log-uniform lengths, 600 000-block
+  shuffled pool: a sample of rows (the shortest, the longest, and a seeded
+  draw) vs the oracle, and the contiguous twin bit for bit on two of them.
+* chunked prefill, 8 x (2048 + 512) over 4 layers: sampled queries per layer.
+* shared-prefix forks: 128 forks of an 8192-token prefix, divergent chunks,
+  a batched decode step, truncation of half the forks and re-append; and the
+  same with an unaligned 8200-token prefix, where copy-on-append fires.
+
+Histories are drawn with seeded torch generators and written into the pool
+with torch indexing; the oracle receives host copies of those draws.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_gqa_nx_gb300 as pkv
+from synth import workloads as wl
+from gpu_helpers import GpuPool, assert_close, bits_equal, contiguous_attend
+
+
+def _oracle_row(Qr, Kf, Vf, n, tk, w, causal=1):
+    rc, ref = oracle.attend(Qr, Kf, Vf, n, tk, w.n_heads, w.n_kv_heads, w.head_dim, causal, w.scale)
+    assert rc == 0
+    return ref
+
+
+def build_decode(w, keep_rows, seed_base):
+    """Pool + sequences holding each row's history (layer 0); returns host
+    copies of the histories of the rows in keep_rows."""
+    pool = GpuPool(w.n_blocks, w.n_layers, w.kv_dim, w.block_size, max_seqs=w.M + 4,
+                   max_blocks=-(-(w.max_tokens() + 1) // w.block_size) + 1, shuffle_seed=w.seed)
+    seqs, kept = [], {}
+    for r in range(w.M):
+        L = int(w.past_len[r])
+        s = pool.new_seq(L + int(w.n_q[r]) + 1)
+        pool.grow(s, L)
+        Kh = wl.normal((L, w.kv_dim), seed_base + 2 * r, "cuda")
+        Vh = wl.normal((L, w.kv_dim), seed_base + 2 * r + 1, "cuda")
+        pool.write_history(s, 0, Kh, Vh)
+        if r in keep_rows:
+            kept[r] = (Kh.cpu().numpy(), Vh.cpu().numpy())
+        del Kh, Vh
+        seqs.append(s)
+    torch.cuda.synchronize()
+    return pool, seqs, kept
+
+
+def decode_step_and_check(w, rows_to_check, contig_rows=()):
+    pool, seqs, kept = build_decode(w, set(rows_to_check), w.seed * 1000)
+    try:
+        T = int(w.n_q.sum())
+        Q = wl.normal((T, w.q_dim), w.seed + 101, "cuda")
+        Kn = wl.normal((T, w.kv_dim), w.seed + 102, "cuda")
+        Vn = wl.normal((T, w.kv_dim), w.seed + 103, "cuda")
+        nq = [int(x) for x in w.n_q]
+        pkv.check(pkv.pkv_ensure_append_batch(seqs, nq))
+        out = torch.empty(T, w.q_dim, device="cuda")
+        pkv.check(pkv.pkv_attn_batch(seqs, nq, Q, Kn, Vn, w.n_heads, w.n_kv_heads, w.head_dim, 0, 1,
+                                     w.scale, out))
+        pool.check_no_device_error()
+        offs = np.concatenate([[0], np.cumsum(w.n_q)])
+        Qh, Knh, Vnh, outh = Q.cpu().numpy(), Kn.cpu().numpy(), Vn.cpu().numpy(), out.cpu().numpy()
+        for r in rows_to_check:
+            o, n, L = int(offs[r]), nq[r], int(w.past_len[r])
+            Kf = np.concatenate([kept[r][0], Knh[o:o + n]])
+            Vf = np.concatenate([kept[r][1], Vnh[o:o + n]])
+            ref = _oracle_row(Qh[o:o + n], Kf, Vf, n, L + n, w)
+            assert_close(outh[o:o + n], ref, np.abs(Vf).max(), "%s row %d (len %d)" % (w.name, r, L))
+            if r in contig_rows:
+                oc = contiguous_attend(Q[o:o + n], torch.from_numpy(Kf).cuda(), torch.from_numpy(Vf).cuda(),
+                                       n, L + n, w.n_heads, w.n_kv_heads, w.head_dim, 1, w.scale)
+                assert bits_equal(out[o:o + n], oc)
+    finally:
+        pool.close()
+
+
+@pytest.mark.gpu
+def test_batched_decode_m64_all_rows():
+    w = wl.batched_decode_m64()
+    decode_step_and_check(w, list(range(w.M)), contig_rows=(0, 1))
+
+
+@pytest.mark.gpu
+def test_continuous_batching_m256_sampled():
+    w = wl.continuous_batching_m256()
+    free, _ = torch.cuda.mem_get_info()
+    need = 2 * w.n_blocks * w.block_size * w.kv_dim * 4
+    if free < need + (8 << 30):
+        pytest.skip("needs %.1f GB of device memory" % (need / 1e9))
+    rng = np.random.default_rng(w.seed + 7)
+    rows = sorted(set([int(np.argmin(w.past_len)), int(np.argmax(w.past_len))] +
+                      [int(x) for x in rng.choice(w.M, 10, replace=False)]))
+    decode_step_and_check(w, rows, contig_rows=(rows[0], int(np.argmax(w.past_len))))
+
+
+@pytest.mark.gpu
+def test_chunked_prefill_sampled_queries():
+    w = wl.chunked_prefill()
+    bs = w.block_size
+    pool = GpuPool(w.n_blocks, w.n_layers, w.kv_dim, bs, max_seqs=w.M + 2,
+                   max_blocks=-(-w.max_tokens() // bs) + 1, shuffle_seed=w.seed)
+    try:
+        past, n = int(w.past_len[0]), int(w.n_q[0])
+        seqs, hist = [], {}
+        for r in range(w.M):
+            s = pool.new_seq(past + n)
+            pool.grow(s, past)
+            for layer in range(w.n_layers):
+                Kh = wl.normal((past, w.kv_dim), w.seed * 100 + 10 * r + 2 * layer, "cuda")
+                Vh = wl.normal((past, w.kv_dim), w.seed * 100 + 10 * r + 2 * layer + 1, "cuda")
+                pool.write_history(s, layer, Kh, Vh)
+                if r in (0, w.M - 1):
+                    hist[(r, layer)] = (Kh.cpu().numpy(), Vh.cpu().numpy())
+            seqs.append(s)
+        T = w.M * n
+        nq = [n] * w.M
+        pkv.check(pkv.pkv_ensure_append_batch(seqs, nq))
+        results = []
+        for layer in range(w.n_layers):
+            Q = wl.normal((T, w.q_dim), w.seed + 200 + layer, "cuda")
+            Kn = wl.normal((T, w.kv_dim), w.seed + 300 + layer, "cuda")
+            Vn = wl.normal((T, w.kv_dim), w.seed + 400 + layer, "cuda")
+            out = torch.empty(T, w.q_dim, device="cuda")
+            pkv.check(pkv.pkv_attn_batch(seqs, nq, Q, Kn, Vn, w.n_heads, w.n_kv_heads, w.head_dim,
+                                         layer, 1, w.scale, out))
+            results.append((Q.cpu().numpy(), Kn.cpu().numpy(), Vn.cpu().numpy(), out.cpu().numpy()))
+        pkv.check(pkv.pkv_advance_batch(seqs, nq))
+        pool.check_no_device_error()
+        for layer in (0, w.n_layers - 1):
+            Qh, Knh, Vnh, outh = results[layer]
+            for r in (0, w.M - 1):
+                Kf = np.concatenate([hist[(r, layer)][0], Knh[r * n:(r + 1) * n]])
+                Vf = np.concatenate([hist[(r, layer)][1], Vnh[r * n:(r + 1) * n]])
+                for i in (0, 1, 255, n - 1):
+                    row = r * n + i
+                    ref = _oracle_row(Qh[row:row + 1], Kf, Vf, 1, past + i + 1, w)
+                    assert_close(outh[row:row + 1], ref, np.abs(Vf).max(),
+                                 "layer %d row %d query %d" % (layer, r, i))
+    finally:
+        pool.close()
+
+
+def _shared_prefix(prefix, n_forks, seed):
+    w = wl.shared_prefix_forks(prefix=prefix, n_forks=n_forks)
+    bs = w.block_size
+    div = [int(x) for x in w.n_q]
+    pool = GpuPool(w.n_blocks, 1, w.kv_dim, bs, max_seqs=n_forks + 4,
+                   max_blocks=-(-(prefix + 2 * 256 + 2) // bs) + 1, shuffle_seed=w.seed)
+    try:
+        root = pool.new_seq(prefix + 2 * 256 + 2)
+        pool.grow(root, prefix)
+        Kp = wl.normal((prefix, w.kv_dim), seed, "cuda")
+        Vp = wl.normal((prefix, w.kv_dim), seed + 1, "cuda")
+        pool.write_history(root, 0, Kp, Vp)
+        Kp_h, Vp_h = Kp.cpu().numpy(), Vp.cpu().numpy()
+        forks = [pkv.pkv_seq_fork(root) for _ in range(n_forks)]
+        assert all(forks)
+        pt_root = pkv.pkv_seq_page_table(root)
+        assert pkv.pkv_refcnt(pool.p, pt_root[0]) == n_forks + 1
+        check = sorted({0, n_forks // 2, n_forks - 1, int(np.argmax(div))})
+
+        def chunk_round(seqs, ns, tag, hist):
+            T = sum(ns)
+            Q = wl.normal((T, w.q_dim), seed + tag, "cuda")
+            K = wl.normal((T, w.kv_dim), seed + tag + 1, "cuda")
+            V = wl.normal((T, w.kv_dim), seed + tag + 2, "cuda")
+            pkv.check(pkv.pkv_ensure_append_batch(seqs, ns))
+            out = torch.empty(T, w.q_dim, device="cuda")
+            pkv.check(pkv.pkv_attn_batch(seqs, ns, Q, K, V, w.n_heads, w.n_kv_heads, w.head_dim, 0, 1,
+                                         w.scale, out))
+            pkv.check(pkv.pkv_advance_batch(seqs, ns))
+            Qh, Kh, Vh, oh = Q.cpu().numpy(), K.cpu().numpy(), V.cpu().numpy(), out.cpu().numpy()
+            o = 0
+            for j, (s, n) in enumerate(zip(seqs, ns)):
+                kh, vh = hist[s]
+                hist[s] = (np.concatenate([kh, Kh[o:o + n]]), np.concatenate([vh, Vh[o:o + n]]))
+                if j in check:
+                    Kf, Vf = hist[s]
+                    ref = _oracle_row(Qh[o:o + n], Kf, Vf, n, Kf.shape[0], w)
+                    assert_close(oh[o:o + n], ref, np.abs(Vf).max(), "fork %d tag %d" % (j, tag))
+                o += n
+
+        hist = {f: (Kp_h, Vp_h) for f in forks}
+        chunk_round(forks, div, 10, hist)                      # divergent chunks (copy-on-append)
+        for f in forks:
+            pt = pkv.pkv_seq_page_table(f)
+            assert pt[:prefix // bs] == pt_root[:prefix // bs]  # full prefix blocks stay shared
+        chunk_round(forks, [1] * n_forks, 20, hist)             # batched decode step of all forks
+        half = forks[: n_forks // 2]
+        for f in half:
+            pkv.check(pkv.pkv_seq_truncate(f, prefix))
+            hist[f] = (Kp_h, Vp_h)
+        chunk_round(half, div[: n_forks // 2], 30, hist)        # re-append fresh divergent chunks
+        assert pkv.pkv_seq_len(root) == prefix
+        pool.check_no_device_error()
+    finally:
+        pool.close()
+
+
+@pytest.mark.gpu
+def test_shared_prefix_forks_aligned():
+    _shared_prefix(8192, 128, 77)
+
+
+@pytest.mark.gpu
+def test_shared_prefix_forks_unaligned_cow():
+    _shared_prefix(8200, 16, 88)

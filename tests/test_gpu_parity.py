@@ -1,0 +1,252 @@
+"""GPU parity on seeded shapes that span several tiles and splits with ragged
+tails: the batched paged path against the oracle (within tolerance), against
+the contiguous twin (bit for bit), against the same row launched alone (bit
+for bit), and under a permutation of the physical blocks (bit for bit).
+
+Shapes cover the head_dim-128 fast kernel (query groups 1, 2, 4) and the
+generic kernel (head_dim 5..256, groups 1..32, block sizes 1..16 including
+non-powers of two), decode rows (n_q = 1), chunked-prefill rows (n_q > 1,
+offset-causal), non-causal rows, a first token (total_k = 1) and rows whose
+length sits on and next to block and split boundaries.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_gqa_nx_gb300 as pkv
+from gpu_helpers import GpuPool, assert_close, bits_equal, contiguous_attend
+
+
+@pytest.fixture
+def split_keys():
+    old = pkv.pkv_get_split_keys()
+    yield lambda k: pkv.check(pkv.pkv_set_split_keys(k))
+    pkv.check(pkv.pkv_set_split_keys(old))
+
+
+def run_case(H, KV, hd, bs, past, nq, causal=1, seed=0, n_layers=1, layer=0, shuffle=True,
+             check_m1=True, check_contig=True):
+    rng = np.random.default_rng(seed)
+    M = len(past)
+    kv_dim, q_dim = KV * hd, H * hd
+    scale = float(np.float32(1.0 / math.sqrt(hd)))
+    need = sum(-(-(p + n) // bs) for p, n in zip(past, nq))
+    max_blocks = max(-(-(p + n) // bs) for p, n in zip(past, nq)) + 1
+    pool = GpuPool(need + 8, n_layers, kv_dim, bs, max_seqs=M + 2, max_blocks=max_blocks,
+                   shuffle_seed=(seed + 11) if shuffle else None)
+    try:
+        seqs, hk, hv = [], [], []
+        for p, n in zip(past, nq):
+            s = pool.new_seq(p + n)
+            Kh = rng.standard_normal((p, kv_dim)).astype(np.float32)
+            Vh = rng.standard_normal((p, kv_dim)).astype(np.float32)
+            if p:
+                pool.grow(s, p)
+                pool.write_history(s, layer, torch.from_numpy(Kh), torch.from_numpy(Vh))
+            seqs.append(s)
+            hk.append(Kh)
+            hv.append(Vh)
+        T = int(sum(nq))
+        Q = rng.standard_normal((T, q_dim)).astype(np.float32)
+        Kn = rng.standard_normal((T, kv_dim)).astype(np.float32)
+        Vn = rng.standard_normal((T, kv_dim)).astype(np.float32)
+        Qd, Kd, Vd = (torch.from_numpy(a).cuda() for a in (Q, Kn, Vn))
+        pkv.check(pkv.pkv_ensure_append_batch(seqs, nq))
+        out = torch.empty(T, q_dim, device="cuda")
+        pkv.check(pkv.pkv_attn_batch(seqs, nq, Qd, Kd, Vd, H, KV, hd, layer, causal, scale, out))
+        pool.check_no_device_error()
+        o = 0
+        for r, (p, n) in enumerate(zip(past, nq)):
+            Kf = np.concatenate([hk[r], Kn[o:o + n]])
+            Vf = np.concatenate([hv[r], Vn[o:o + n]])
+            rc, ref = oracle.attend(Q[o:o + n], Kf, Vf, n, p + n, H, KV, hd, causal, scale)
+            assert rc == 0
+            assert_close(out[o:o + n].cpu().numpy(), ref, np.abs(Vf).max(), "row %d" % r)
+            if check_contig:
+                oc = contiguous_attend(Qd[o:o + n], torch.from_numpy(Kf).cuda(),
+                                       torch.from_numpy(Vf).cuda(), n, p + n, H, KV, hd, causal,
+                                       scale)
+                assert bits_equal(out[o:o + n], oc), "row %d: paged != contiguous" % r
+            if check_m1:
+                # the same row alone (re-appending the same rows at the same positions)
+                o1 = torch.empty(n, q_dim, device="cuda")
+                pkv.check(pkv.pkv_attn_with_paged(Qd[o:o + n], Kd[o:o + n], Vd[o:o + n], n, H, KV,
+                                                  hd, seqs[r], layer, causal, scale, o1))
+                assert bits_equal(out[o:o + n], o1), "row %d: batched != M=1" % r
+            o += n
+        pool.check_no_device_error()
+        return out
+    finally:
+        pool.close()
+
+
+EDGE_LENS = [0, 1, 7, 8, 15, 16, 17, 63, 64, 65, 511, 512, 513, 1000]
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("H,KV", [(32, 8), (16, 8), (8, 8)], ids=["g4", "g2", "g1"])
+def test_fast_kernel_decode(H, KV, split_keys):
+    split_keys(512)
+    run_case(H, KV, 128, 16, EDGE_LENS, [1] * len(EDGE_LENS), seed=H)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("split", [32, 64, 96])
+def test_fast_kernel_many_splits(split, split_keys):
+    split_keys(split)
+    run_case(32, 8, 128, 16, [31, 32, 33, 200, 777, 1300], [1] * 6, seed=split)
+
+
+@pytest.mark.gpu
+def test_fast_kernel_prefill_rows(split_keys):
+    split_keys(64)
+    run_case(32, 8, 128, 16, [0, 5, 100, 64, 300], [1, 3, 17, 40, 70], seed=7)
+
+
+@pytest.mark.gpu
+def test_fast_kernel_noncausal(split_keys):
+    split_keys(64)
+    run_case(32, 8, 128, 16, [10, 90], [5, 33], causal=0, seed=8)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("H,KV,hd,bs", [
+    (4, 2, 8, 4),        # the gate's shape
+    (12, 3, 64, 5),      # non-power-of-two block size
+    (32, 1, 64, 16),     # group 32 -> two head chunks
+    (8, 2, 256, 16),     # largest head_dim
+    (6, 2, 96, 3),
+    (3, 1, 5, 4),        # kv_dim not a multiple of 4 (scalar append)
+    (8, 8, 32, 1),       # block size 1
+    (16, 2, 128, 16),    # head_dim 128 with group 8 -> generic kernel
+], ids=["gate", "bs5", "g32", "hd256", "hd96", "hd5", "bs1", "g8"])
+def test_generic_kernel(H, KV, hd, bs, split_keys):
+    split_keys(64)
+    lens = [0, 1, bs - 1, bs, 63, 64, 65, 200]
+    lens = [max(0, x) for x in lens]
+    run_case(H, KV, hd, bs, lens, [1, 2, 1, 5, 1, 1, 9, 1], seed=hd + bs)
+
+
+@pytest.mark.gpu
+def test_first_token_is_its_value_row():
+    """total_k = 1: the only key gets weight 1, so out equals the new V row
+    exactly (the single-key closed form)."""
+    H, KV, hd = 32, 8, 128
+    pool = GpuPool(4, 1, KV * hd, 16, max_seqs=2, max_blocks=2)
+    try:
+        s = pool.new_seq(16)
+        Q = torch.randn(1, H * hd, device="cuda")
+        K = torch.randn(1, KV * hd, device="cuda")
+        V = torch.randn(1, KV * hd, device="cuda")
+        pkv.check(pkv.pkv_ensure_append(s, 1))
+        out = torch.empty(1, H * hd, device="cuda")
+        pkv.check(pkv.pkv_attn_with_paged(Q, K, V, 1, H, KV, hd, s, 0, 1, 0.1, out))
+        exp = V.view(KV, 1, hd).expand(KV, H // KV, hd).reshape(1, H * hd)
+        assert bits_equal(out, exp)
+    finally:
+        pool.close()
+
+
+@pytest.mark.gpu
+def test_block_permutation_invariance(split_keys):
+    """Paging is storage only: the same histories in a shuffled and in an
+    ordered pool give the same bits."""
+    split_keys(128)
+    a = run_case(32, 8, 128, 16, [40, 300, 999], [1, 1, 4], seed=3, shuffle=True,
+                 check_m1=False, check_contig=False)
+    b = run_case(32, 8, 128, 16, [40, 300, 999], [1, 1, 4], seed=3, shuffle=False,
+                 check_m1=False, check_contig=False)
+    assert bits_equal(a, b)
+
+
+@pytest.mark.gpu
+def test_multilayer_pool_layer_offsets(split_keys):
+    split_keys(64)
+    run_case(32, 8, 128, 16, [100, 17], [1, 2], n_layers=3, layer=2, seed=5)
+    run_case(4, 2, 8, 4, [9, 3], [1, 3], n_layers=2, layer=1, seed=6)
+
+
+@pytest.mark.gpu
+def test_host_buffer_entry_point_matches_device_path():
+    H, KV, hd, bs = 32, 8, 128, 16
+    pool = GpuPool(64, 1, KV * hd, bs, max_seqs=4, max_blocks=32)
+    try:
+        seqs = [pool.new_seq(400) for _ in range(3)]
+        for s, p in zip(seqs, [10, 100, 300]):
+            pool.grow(s, p)
+            pool.write_history(s, 0, torch.randn(p, KV * hd), torch.randn(p, KV * hd))
+        nq = [1, 1, 2]
+        Q = torch.randn(4, H * hd).pin_memory()
+        K = torch.randn(4, KV * hd).pin_memory()
+        V = torch.randn(4, KV * hd).pin_memory()
+        pkv.check(pkv.pkv_ensure_append_batch(seqs, nq))
+        out_h = torch.empty(4, H * hd).pin_memory()
+        pkv.check(pkv.pkv_attn_batch_host(seqs, nq, Q, K, V, H, KV, hd, 0, 1, 0.088, out_h))
+        out_d = torch.empty(4, H * hd, device="cuda")
+        pkv.check(pkv.pkv_attn_batch(seqs, nq, Q.cuda(), K.cuda(), V.cuda(), H, KV, hd, 0, 1, 0.088,
+                                     out_d))
+        assert bits_equal(out_h.cuda(), out_d)
+    finally:
+        pool.close()
+
+
+@pytest.mark.gpu
+def test_error_paths_change_nothing():
+    H, KV, hd, bs = 32, 8, 128, 16
+    pool = GpuPool(8, 1, KV * hd, bs, max_seqs=4, max_blocks=8)
+    try:
+        a = pool.new_seq(64)
+        Q = torch.randn(2, H * hd, device="cuda")
+        K = torch.randn(2, KV * hd, device="cuda")
+        out = torch.empty(2, H * hd, device="cuda")
+        # rows not ensured
+        assert pkv.pkv_attn_with_paged(Q, K, K, 1, H, KV, hd, a, 0, 1, 1.0, out) == pkv.PKV_ERR_SEQ
+        pkv.check(pkv.pkv_ensure_append(a, 1))
+        assert pkv.pkv_attn_with_paged(Q, K, K, 0, H, KV, hd, a, 0, 1, 1.0, out) == pkv.PKV_ERR_BAD_DIM
+        assert pkv.pkv_attn_with_paged(Q, K, K, 1, 30, KV, hd, a, 0, 1, 1.0, out) == pkv.PKV_ERR_BAD_GQA
+        assert pkv.pkv_attn_with_paged(Q, K, K, 1, H, KV, hd, None, 0, 1, 1.0, out) == pkv.PKV_ERR_SEQ
+        assert pkv.pkv_attn_with_paged(Q, K, K, 1, H, KV, 64, a, 0, 1, 1.0, out) == pkv.PKV_ERR_BAD_DIM
+        assert pkv.pkv_attn_with_paged(Q, K, K, 1, H, KV, hd, a, 1, 1, 1.0, out) == pkv.PKV_ERR_ARG
+        assert pkv.pkv_attn_batch([a, a], [1, 1], Q, K, K, H, KV, hd, 0, 1, 1.0, out) == pkv.PKV_ERR_ARG
+        mis = torch.empty(H * hd + 1, device="cuda")[1:].view(1, H * hd)
+        assert pkv.pkv_attn_with_paged(mis, K, K, 1, H, KV, hd, a, 0, 1, 1.0, out) == pkv.PKV_ERR_ARG
+        # shared block not privatised -> refused, not written
+        pkv.check(pkv.pkv_attn_with_paged(Q[:1], K[:1], K[:1], 1, H, KV, hd, a, 0, 1, 1.0, out))
+        pkv.check(pkv.pkv_advance(a, 1))
+        b = pkv.pkv_seq_fork(a)
+        assert pkv.pkv_attn_with_paged(Q[:1], K[:1], K[:1], 1, H, KV, hd, b, 0, 1, 1.0, out) == pkv.PKV_ERR_SEQ
+        pool.check_no_device_error()
+    finally:
+        pool.close()
+
+
+@pytest.mark.gpu
+def test_launch_accounting_and_profiling():
+    H, KV, hd = 32, 8, 128
+    pool = GpuPool(64, 1, KV * hd, 16, max_seqs=4, max_blocks=64)
+    try:
+        s = pool.new_seq(1024)
+        pool.grow(s, 900)
+        pool.write_history(s, 0, torch.randn(900, KV * hd), torch.randn(900, KV * hd))
+        pkv.check(pkv.pkv_ensure_append(s, 1))
+        Q = torch.randn(1, H * hd, device="cuda")
+        K = torch.randn(1, KV * hd, device="cuda")
+        out = torch.empty(1, H * hd, device="cuda")
+        pkv.pkv_profile_reset()
+        pkv.pkv_profile_enable(True)
+        n0 = pkv.pkv_launch_count()
+        pkv.check(pkv.pkv_attn_with_paged(Q, K, K, 1, H, KV, hd, s, 0, 1, 0.1, out))
+        torch.cuda.synchronize()
+        pkv.pkv_profile_enable(False)
+        n = pkv.pkv_launch_count() - n0
+        kinds = {k: pkv.pkv_profile_read(k) for k in range(pkv.PKV_KERNEL_KINDS)}
+        assert sum(v[1] for v in kinds.values()) == n
+        assert kinds[pkv.PKV_KERNEL_DECODE][1] == 1 and kinds[pkv.PKV_KERNEL_DECODE][0] > 0
+        assert kinds[pkv.PKV_KERNEL_APPEND][1] == 1
+        assert kinds[pkv.PKV_KERNEL_MERGE][1] == (1 if 901 > pkv.pkv_get_split_keys() else 0)
+    finally:
+        pkv.pkv_profile_reset()
+        pool.close()
