@@ -7,7 +7,7 @@ or CPU tensors; streams are ``torch.cuda.Stream`` objects, raw ``cudaStream_t``
 integers or None.  Constructors return an opaque handle or None (check
 ``pkv_last_error()``); the rest return the library's status code.
 
-The library must be built first (``python -m paged_kv_gqa_nx_gb300.build`` or
+The library must be built first (``python paged_kv_gqa_nx_gb300/build.py`` or
 ``__graft_entry__.build()``); importing this package without it raises.
 """
 from __future__ import annotations
@@ -47,7 +47,7 @@ class PkvError(RuntimeError):
 
 
 if not os.path.exists(LIB_PATH):
-    raise ImportError("libpkv.so is not built (%s); run `python -m paged_kv_gqa_nx_gb300.build`"
+    raise ImportError("libpkv.so is not built (%s); run `python paged_kv_gqa_nx_gb300/build.py`"
                       % LIB_PATH)
 
 _lib = ctypes.CDLL(LIB_PATH)

@@ -4,7 +4,9 @@ Each translation unit under ``csrc/`` compiles in parallel to an object in
 ``_build/``; the objects link into ``paged_kv_gqa_nx_gb300/libpkv.so``
 (CUDA runtime linked statically, only the ``pkv_*`` C ABI exported).
 
-    python -m paged_kv_gqa_nx_gb300.build [--force] [--verbose]
+    python paged_kv_gqa_nx_gb300/build.py [--force] [--verbose]
+
+(Run by path: importing the package itself needs the built library.)
 """
 from __future__ import annotations
 
@@ -39,6 +41,7 @@ def _stale(target: str, deps) -> bool:
         return True
     t = os.path.getmtime(target)
     return any(os.path.getmtime(d) > t for d in deps)
+
 
 
 def build(force: bool = False, verbose: bool = False) -> str:

@@ -32,8 +32,12 @@ def pytest_collection_modifyitems(config, items):
 def _ensure_built():
     """Build the product library and the oracle's C core when missing or stale
     (compiling is not running: no test here depends on a GPU to build)."""
-    from paged_kv_gqa_nx_gb300 import build as pkv_build
-    pkv_build.build()
+    import importlib.util
+    spec = importlib.util.spec_from_file_location(
+        "pkv_build", os.path.join(ROOT, "paged_kv_gqa_nx_gb300", "build.py"))
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    mod.build()
     import oracle
     oracle.build()
 
