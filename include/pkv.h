@@ -17,8 +17,9 @@
  *   - All float data are IEEE f32, row-major.  Q and out are [rows, n_heads*head_dim];
  *     K_new and V_new are [rows, n_kv_heads*head_dim] ("nx_f32_gqa_attention.nx
  *     source", header).  Query head h reads kv head h / (n_heads / n_kv_heads).
- *   - Device pointers are CUDA device addresses and must be 16-byte aligned;
- *     host pointers are plain host memory.  The caller owns every pointer it
+ *   - Device pointers are CUDA device addresses, 16-byte aligned when head_dim
+ *     is a multiple of 4 (vector access) and 4-byte aligned otherwise; host
+ *     pointers are plain host memory.  The caller owns every pointer it
  *     passes; the library never frees them.
  *   - A stream argument is a cudaStream_t passed as void* (NULL = legacy default
  *     stream).  A pool binds one stream: every device operation on the pool and

@@ -243,6 +243,7 @@ struct DevGuard {
 };
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3) == 0; }
 
 int32_t ceil_div(int64_t a, int64_t b) { return static_cast<int32_t>((a + b - 1) / b); }
 
@@ -450,8 +451,15 @@ int run_layer(pkv_seq *const *seqs, int32_t M, const int32_t *n_q, const float *
         return fail(PKV_ERR_ARG, "layer %d outside [0, %d)", layer, p->n_layers);
     if (!K_new || !V_new || (attend && (!Q || !out)))
         return fail(PKV_ERR_ARG, "NULL data pointer");
-    if (!host_io && (!aligned16(K_new) || !aligned16(V_new) || (attend && (!aligned16(Q) || !aligned16(out)))))
-        return fail(PKV_ERR_ARG, "device pointers must be 16-byte aligned");
+    if (!host_io) {
+        // 16-byte alignment where the kernels use vector access (head_dim % 4 == 0),
+        // element alignment otherwise
+        const bool vec = attend && (head_dim % 4) == 0;
+        auto ok = [&](const void *q) { return vec ? aligned16(q) : aligned4(q); };
+        if (!ok(K_new) || !ok(V_new) || (attend && (!ok(Q) || !ok(out))))
+            return fail(PKV_ERR_ARG, vec ? "device pointers must be 16-byte aligned"
+                                         : "device pointers must be 4-byte aligned");
+    }
     {
         int rc = check_dup(p, seqs, M);
         if (rc) return rc;
@@ -523,7 +531,7 @@ int run_layer(pkv_seq *const *seqs, int32_t M, const int32_t *n_q, const float *
     const PagedAddr addr = paged_addr(p, layer);
     e = launch(PKV_KERNEL_APPEND, st, [&] {
         return launch_append(Kd, Vd, dptr<AppendDesc>(p, app_off), static_cast<int32_t>(T), addr,
-                             p->err_dev, st);
+                             (kv_dim % 4) == 0 && aligned16(Kd) && aligned16(Vd), p->err_dev, st);
     });
     if (e != cudaSuccess) return cuda_fail(e, "append kernel");
     if (!attend) return PKV_OK;
@@ -930,8 +938,9 @@ int pkv_attn_contiguous(const float *Q, const float *Kc, const float *Vc, int32_
     if (head_dim > kMaxHeadDim)
         return fail(PKV_ERR_BAD_DIM, "head_dim %d > %d is not supported", head_dim, kMaxHeadDim);
     if (!Q || !Kc || !Vc || !out) return fail(PKV_ERR_ARG, "NULL data pointer");
-    if (!aligned16(Q) || !aligned16(Kc) || !aligned16(Vc) || !aligned16(out))
-        return fail(PKV_ERR_ARG, "device pointers must be 16-byte aligned");
+    if ((head_dim % 4) == 0 ? (!aligned16(Q) || !aligned16(Kc) || !aligned16(Vc) || !aligned16(out))
+                            : (!aligned4(Q) || !aligned4(Kc) || !aligned4(Vc) || !aligned4(out)))
+        return fail(PKV_ERR_ARG, "device pointers must be 16-byte aligned (4-byte if head_dim %% 4 != 0)");
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");

@@ -83,8 +83,10 @@ struct MergeArgs {
 // Kernel launchers (pkv_kernels.cu).  Each enqueues exactly one kernel.
 cudaError_t launch_pt_apply(int32_t *pt_dev, int32_t max_blocks, const PtRun *runs, int32_t n_runs,
                             const int32_t *vals, cudaStream_t s);
+// vec4: rows are copied as float4 (kv_dim % 4 == 0 and K_new / V_new 16-byte aligned)
 cudaError_t launch_append(const float *K_new, const float *V_new, const AppendDesc *items,
-                          int32_t n_items, const PagedAddr &addr, int32_t *err, cudaStream_t s);
+                          int32_t n_items, const PagedAddr &addr, bool vec4, int32_t *err,
+                          cudaStream_t s);
 cudaError_t launch_copy_blocks(float *k, float *v, const CopyDesc *items, int32_t n_items,
                                int64_t block_floats, int32_t n_blocks, int32_t *err,
                                cudaStream_t s);

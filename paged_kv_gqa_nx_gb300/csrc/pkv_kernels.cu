@@ -106,7 +106,7 @@ __global__ void pt_apply_kernel(int32_t *pt, int32_t max_blocks, const PtRun *ru
 // One warp per (token row, K or V).
 __global__ void append_rows_kernel(const float *__restrict__ K_new, const float *__restrict__ V_new,
                                    const AppendDesc *__restrict__ items, int32_t n_items,
-                                   PagedAddr a, int32_t *err) {
+                                   PagedAddr a, bool vec4, int32_t *err) {
     const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
     if (gw >= 2 * n_items) return;
@@ -126,7 +126,7 @@ __global__ void append_rows_kernel(const float *__restrict__ K_new, const float 
     float *dst = (is_v ? a.v : a.k) + static_cast<size_t>(blk) * a.block_stride + a.layer_off +
                  static_cast<size_t>(off) * a.kv_dim;
     const float *src = (is_v ? V_new : K_new) + static_cast<size_t>(d.src_row) * a.kv_dim;
-    if ((a.kv_dim & 3) == 0) {
+    if (vec4) {
         const float4 *s4 = reinterpret_cast<const float4 *>(src);
         float4 *d4 = reinterpret_cast<float4 *>(dst);
         for (int i = lane; i < (a.kv_dim >> 2); i += 32) d4[i] = __ldg(s4 + i);
@@ -626,11 +626,12 @@ cudaError_t launch_pt_apply(int32_t *pt_dev, int32_t max_blocks, const PtRun *ru
 }
 
 cudaError_t launch_append(const float *K_new, const float *V_new, const AppendDesc *items,
-                          int32_t n_items, const PagedAddr &addr, int32_t *err, cudaStream_t s) {
+                          int32_t n_items, const PagedAddr &addr, bool vec4, int32_t *err,
+                          cudaStream_t s) {
     if (n_items <= 0) return cudaSuccess;
     const long long warps = 2LL * n_items;
     const unsigned blocks = static_cast<unsigned>((warps + 7) / 8);
-    append_rows_kernel<<<blocks, 256, 0, s>>>(K_new, V_new, items, n_items, addr, err);
+    append_rows_kernel<<<blocks, 256, 0, s>>>(K_new, V_new, items, n_items, addr, vec4, err);
     return cudaGetLastError();
 }
 
