@@ -136,6 +136,7 @@ def get_workload(name):
     from synth import workloads as wl
     table = {
         "continuous_batching_m256": wl.continuous_batching_m256,
+        "continuous_batching_small": wl.continuous_batching_small,
         "batched_decode_m64": wl.batched_decode_m64,
         "chunked_prefill": wl.chunked_prefill,
         "shared_prefix_forks": wl.shared_prefix_forks,

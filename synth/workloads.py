@@ -91,6 +91,17 @@ def continuous_batching_m256(seed: int = BASE_SEED + 3, n_blocks: int = 600_000)
                     past, n_q, seed)
 
 
+def continuous_batching_small(seed: int = BASE_SEED + 3) -> Workload:
+    """A smaller draw of the continuous-batching mix for profiler captures:
+    M=64, lengths log-uniform in [128, 8192], a 32 768-block pool (4.3 GB);
+    each step still reads ~0.8 GB of K/V, well above the L2."""
+    rng = np.random.default_rng(seed)
+    u = rng.uniform(math.log(128.0), math.log(8192.0), size=64)
+    past = np.clip(np.rint(np.exp(u)), 128, 8192).astype(np.int64)
+    return Workload("continuous_batching_small", 32, 8, 128, 1, 16, 32768, past,
+                    np.ones(64, dtype=np.int64), seed)
+
+
 def shared_prefix_forks(seed: int = BASE_SEED + 4, prefix: int = 8192,
                         n_forks: int = 128) -> Workload:
     rng = np.random.default_rng(seed)
