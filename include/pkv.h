@@ -216,6 +216,30 @@ PKV_API int pkv_attn_contiguous(const float *Q, const float *Kc, const float *Vc
                         int32_t total_k, int32_t n_heads, int32_t n_kv_heads, int32_t head_dim,
                         int32_t causal, float scale, float *out, pkv_stream_t stream);
 
+/* No counterpart in the paper: an addition of this library.
+ * pkv_attn_contiguous for callers that cannot let a library allocate device
+ * memory -- a serving engine that has reserved its whole device-memory budget
+ * (a further cudaMalloc would fail or break its accounting), code running
+ * inside an allocator or memory-pressure callback (allocating again would
+ * re-enter that allocator), and latency-critical loops where cudaMalloc /
+ * cudaFree may synchronise the device.  Same arguments, same kernels and the
+ * same result as pkv_attn_contiguous, but it calls no cudaMalloc, cudaFree or
+ * other allocating routine: its scratch (work list and split-K partials) is one
+ * static device array of PKV_NOALLOC_SCRATCH_BYTES, held by every GPU that loads
+ * the library until the process exits.  The caller still passes the inputs and
+ * the output.  Requests whose scratch would exceed the array are rejected with
+ * PKV_ERR_CAPACITY before any work is enqueued (pkv_last_error() names the sizes).
+ * The first call on a device looks up the array's device address (a one-time
+ * set-up with that device current); make that first call before any stream
+ * capture.  Every call shares the array and finds the previous call's contents
+ * in it: calls whose GPU work overlaps (different streams, or threads without
+ * ordering between their streams) race; calls on one stream are ordered. */
+#define PKV_NOALLOC_SCRATCH_BYTES (16u << 20)
+PKV_API int pkv_attn_contiguous_noalloc(const float *Q, const float *Kc, const float *Vc,
+                                        int32_t n_q, int32_t total_k, int32_t n_heads,
+                                        int32_t n_kv_heads, int32_t head_dim, int32_t causal,
+                                        float scale, float *out, pkv_stream_t stream);
+
 /* ---------------------------------------------------------- diagnostics ---- */
 
 /* Wait for the pool stream, then return and clear the pool's device error

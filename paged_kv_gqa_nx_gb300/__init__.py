@@ -29,6 +29,7 @@ PKV_ERR_CUDA = 7
 PKV_ERR_DEVICE_BOUNDS = 8
 
 PKV_POOL_HOST_ONLY = 1
+PKV_NOALLOC_SCRATCH_BYTES = 16 << 20
 
 PKV_KERNEL_APPEND = 0
 PKV_KERNEL_DECODE = 1
@@ -86,6 +87,7 @@ _SIGS = {
     "pkv_attn_batch": (_int, [_vp, _i32, _pi32, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _f32, _vp]),
     "pkv_attn_batch_host": (_int, [_vp, _i32, _pi32, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _f32, _vp]),
     "pkv_attn_contiguous": (_int, [_vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _f32, _vp, _vp]),
+    "pkv_attn_contiguous_noalloc": (_int, [_vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _f32, _vp, _vp]),
     "pkv_sync_error": (_int, [_vp]),
     "pkv_pool_flush": (_int, [_vp]),
     "pkv_set_split_keys": (_int, [_i32]),
@@ -282,6 +284,15 @@ def pkv_attn_contiguous(Q, Kc, Vc, n_q, total_k, n_heads, n_kv_heads, head_dim, 
     return _lib.pkv_attn_contiguous(_dev(Q, "Q"), _dev(Kc, "Kc"), _dev(Vc, "Vc"), n_q, total_k,
                                     n_heads, n_kv_heads, head_dim, causal, scale, _dev(out, "out"),
                                     _stream(stream))
+
+
+def pkv_attn_contiguous_noalloc(Q, Kc, Vc, n_q, total_k, n_heads, n_kv_heads, head_dim, causal,
+                                scale, out, stream=None):
+    """pkv_attn_contiguous without any device allocation (static scratch of
+    PKV_NOALLOC_SCRATCH_BYTES; see include/pkv.h)."""
+    return _lib.pkv_attn_contiguous_noalloc(_dev(Q, "Q"), _dev(Kc, "Kc"), _dev(Vc, "Vc"), n_q,
+                                            total_k, n_heads, n_kv_heads, head_dim, causal, scale,
+                                            _dev(out, "out"), _stream(stream))
 
 
 def pkv_sync_error(pool):

@@ -1078,3 +1078,26 @@ int pkv_profile_read(int32_t kind, double *ms, int64_t *launches) {
 }
 
 }  // extern "C"
+
+// ------------------------------------------- helpers for other entry points ----
+namespace pkv {
+
+void build_contig_work(int32_t n_q, int32_t total_k, int32_t causal, int32_t split_keys,
+                       std::vector<UnitDesc> &units, std::vector<MergeDesc> &merges,
+                       int64_t *n_part) {
+    WorkList w;
+    build_work(std::vector<RowDesc>{{0, total_k - n_q, n_q, 0}}, causal, split_keys, w);
+    units.swap(w.units);
+    merges.swap(w.merges);
+    *n_part = w.n_part;
+}
+
+cudaError_t launch_counted(int kind, cudaStream_t s, cudaError_t (*fn)(void *), void *ctx) {
+    return launch(kind, s, [&] { return fn(ctx); });
+}
+
+int32_t current_split_keys() { return g_split_keys.load(); }
+
+int report_error(int code, const char *msg) { return fail(code, "%s", msg); }
+
+}  // namespace pkv

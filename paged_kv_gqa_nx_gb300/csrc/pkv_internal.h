@@ -3,6 +3,8 @@
 #pragma once
 
 #include <cstdint>
+#include <vector>
+
 #include <cuda_runtime.h>
 
 namespace pkv {
@@ -93,6 +95,18 @@ cudaError_t launch_copy_blocks(float *k, float *v, const CopyDesc *items, int32_
 cudaError_t launch_decode_paged(const AttnArgs &a, const PagedAddr &addr, cudaStream_t s);
 cudaError_t launch_decode_contig(const AttnArgs &a, const ContigAddr &addr, cudaStream_t s);
 cudaError_t launch_merge(const MergeArgs &a, cudaStream_t s);
+
+// Host-core helpers for entry points defined in other translation units
+// (pkv_host.cpp).  build_contig_work: the split-K work list of one contiguous
+// row, as pkv_attn_contiguous builds it.  launch_counted: enqueue fn(ctx) with
+// the library's launch accounting and optional event timing.  report_error:
+// record the calling thread's last error message and return code.
+void build_contig_work(int32_t n_q, int32_t total_k, int32_t causal, int32_t split_keys,
+                       std::vector<UnitDesc> &units, std::vector<MergeDesc> &merges,
+                       int64_t *n_part);
+cudaError_t launch_counted(int kind, cudaStream_t s, cudaError_t (*fn)(void *), void *ctx);
+int32_t current_split_keys();
+int report_error(int code, const char *msg);
 
 // Largest head_dim the decode kernels accept.
 constexpr int kMaxHeadDim = 256;
