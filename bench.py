@@ -354,6 +354,8 @@ def run_pkv(args):
     import torch
     import paged_kv_gqa_nx_gb300 as pkv
     rank, world, dist = dist_setup(args.gpus)
+    if args.split_keys:
+        pkv.check(pkv.pkv_set_split_keys(args.split_keys))
     w = get_workload(args.workload)
     run = DeviceRun(w, rank)
     peak, peak_kind = measured_hbm_peak()
@@ -528,6 +530,7 @@ def main():
     ap.add_argument("--workload", default="continuous_batching_m256")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time")
+    ap.add_argument("--split-keys", type=int, default=0, help="keys per split-K unit (0: library default)")
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)

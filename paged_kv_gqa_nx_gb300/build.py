@@ -45,7 +45,10 @@ def _stale(target: str, deps) -> bool:
 
 
 def build(force: bool = False, verbose: bool = False) -> str:
+    """Compile and link.  Extra nvcc flags (e.g. -DPKV_FAST_STAGES=3) may be
+    given in the PKV_NVCC_FLAGS environment variable."""
     nvcc = _nvcc()
+    extra = os.environ.get("PKV_NVCC_FLAGS", "").split()
     os.makedirs(BUILD, exist_ok=True)
     jobs = []
     objs = []
@@ -54,7 +57,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
         obj = os.path.join(BUILD, src + ".o")
         objs.append(obj)
         if force or _stale(obj, [path] + HEADERS):
-            cmd = [nvcc] + ARCH + COMMON + ["-c", path, "-o", obj]
+            cmd = [nvcc] + ARCH + COMMON + extra + ["-c", path, "-o", obj]
             if src.endswith(".cu"):
                 cmd += ["-Xptxas", "-v"] if verbose else []
             else:

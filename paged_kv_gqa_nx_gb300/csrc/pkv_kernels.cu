@@ -65,6 +65,11 @@ struct PagedRows {
         vr = a.v + o;
         return true;
     }
+    // Tiles of T positions starting at a multiple of T stay inside one block
+    // when the block size is a multiple of T: row pos0 + j is then row pos0
+    // plus j * kv_dim.
+    __device__ __forceinline__ bool whole_tiles(int T) const { return (a.bs % T) == 0; }
+    __device__ __forceinline__ size_t row_stride() const { return static_cast<size_t>(a.kv_dim); }
 };
 
 struct ContigRows {
@@ -76,6 +81,8 @@ struct ContigRows {
         vr = a.v + o;
         return true;
     }
+    __device__ __forceinline__ bool whole_tiles(int) const { return true; }
+    __device__ __forceinline__ size_t row_stride() const { return static_cast<size_t>(a.kv_dim); }
 };
 
 // The key range of one work unit.
@@ -243,7 +250,7 @@ constexpr size_t fast_smem_bytes() {
 }
 
 template <int G, int NST, class Rows>
-__global__ void __launch_bounds__(128) decode_fast_kernel(AttnArgs a, Rows rows_of) {
+__global__ void __launch_bounds__(128, 3) decode_fast_kernel(AttnArgs a, Rows rows_of) {
     using C = FastCfg<G>;
     constexpr int HD = C::HD, T = C::T, W = C::W;
     constexpr int STAGE = T * HD * 2;          // floats: K rows then V rows
@@ -276,18 +283,34 @@ __global__ void __launch_bounds__(128) decode_fast_kernel(AttnArgs a, Rows rows_
                                   t.w * a.scale_log2);
         }
 
+    const bool whole = rows_of.whole_tiles(T);
+    const size_t rstride = rows_of.row_stride();
     auto load_tile = [&](int k_local, int stage) {
         const int pos0 = ur.kbeg + (warp + k_local * W) * T;
+        const int nv = min(T, ur.kend - pos0);
         float *Ks = wbase + stage * STAGE;
         float *Vs = Ks + T * HD;
+        if (whole) {
+            // one page-table lookup per tile
+            const float *kb, *vb;
+            if (rows_of.row(rd.slot, pos0, kvh, HD, kb, vb, a.err)) {
 #pragma unroll
-        for (int j = 0; j < T; ++j) {
-            const int pos = pos0 + j;
-            if (pos < ur.kend) {
-                const float *kr, *vr;
-                if (rows_of.row(rd.slot, pos, kvh, HD, kr, vr, a.err)) {
-                    cp_async16(Ks + j * HD + lane * 4, kr + lane * 4);
-                    cp_async16(Vs + j * HD + lane * 4, vr + lane * 4);
+                for (int j = 0; j < T; ++j) {
+                    if (j < nv) {
+                        cp_async16(Ks + j * HD + lane * 4, kb + j * rstride + lane * 4);
+                        cp_async16(Vs + j * HD + lane * 4, vb + j * rstride + lane * 4);
+                    }
+                }
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < T; ++j) {
+                if (j < nv) {
+                    const float *kr, *vr;
+                    if (rows_of.row(rd.slot, pos0 + j, kvh, HD, kr, vr, a.err)) {
+                        cp_async16(Ks + j * HD + lane * 4, kr + lane * 4);
+                        cp_async16(Vs + j * HD + lane * 4, vr + lane * 4);
+                    }
                 }
             }
         }
@@ -568,7 +591,10 @@ __global__ void merge_splits_kernel(MergeArgs a) {
 
 // -------------------------------------------------------------- dispatch ----
 
-constexpr int kFastStages = 3;
+#ifndef PKV_FAST_STAGES
+#define PKV_FAST_STAGES 2
+#endif
+constexpr int kFastStages = PKV_FAST_STAGES;
 
 template <int G, class Rows>
 cudaError_t launch_fast(const AttnArgs &a, const Rows &r, cudaStream_t s) {
