@@ -190,6 +190,9 @@ class DeviceRun:
                 self.seqs.append(s)
             self.n_q = [int(x) for x in w.n_q]
         self.base_len = [pkv.pkv_seq_len(s) for s in self.seqs]
+        self.c_seqs = pkv.seq_array(self.seqs)
+        self.c_nq = pkv.i32_array(self.n_q)
+        self.c_base = pkv.i32_array(self.base_len)
         self.T = sum(self.n_q)
         self.inputs = []
         for layer in range(w.n_layers):
@@ -235,19 +238,19 @@ class DeviceRun:
         """One pass of the hot path.  host = (Qh, Kh, Vh, outh) pinned buffers
         to run it through the host-buffer entry point instead."""
         pkv, w = self.pkv, self.w
-        pkv.check(pkv.pkv_ensure_append_batch(self.seqs, self.n_q))
+        seqs, nq = self.c_seqs, self.c_nq
+        pkv.check(pkv.pkv_ensure_append_batch(seqs, nq))
         for layer in range(w.n_layers):
             if host is None:
                 Q, K, V = self.inputs[layer]
-                pkv.check(pkv.pkv_attn_batch(self.seqs, self.n_q, Q, K, V, w.n_heads, w.n_kv_heads,
+                pkv.check(pkv.pkv_attn_batch(seqs, nq, Q, K, V, w.n_heads, w.n_kv_heads,
                                              w.head_dim, layer, 1, w.scale, self.out))
             else:
                 Qh, Kh, Vh, oh = host[layer]
-                pkv.check(pkv.pkv_attn_batch_host(self.seqs, self.n_q, Qh, Kh, Vh, w.n_heads,
+                pkv.check(pkv.pkv_attn_batch_host(seqs, nq, Qh, Kh, Vh, w.n_heads,
                                                   w.n_kv_heads, w.head_dim, layer, 1, w.scale, oh))
-        pkv.check(pkv.pkv_advance_batch(self.seqs, self.n_q))
-        for s, L in zip(self.seqs, self.base_len):
-            pkv.check(pkv.pkv_seq_truncate(s, L))
+        pkv.check(pkv.pkv_advance_batch(seqs, nq))
+        pkv.check(pkv.pkv_seq_truncate_batch(seqs, self.c_base))
 
     def host_buffers(self):
         bufs = []

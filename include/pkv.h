@@ -134,6 +134,11 @@ PKV_API int pkv_seq_free(pkv_seq *seq);
  * unreferenced (last first).  PKV_ERR_ARG unless 0 <= new_len <= len. */
 PKV_API int pkv_seq_truncate(pkv_seq *seq, int32_t new_len);
 
+/* pkv_seq_truncate for M sequences of one pool: new_len is a host array of M
+ * lengths; all are validated (PKV_ERR_ARG, duplicates included) before any
+ * sequence changes, then applied in batch order. */
+PKV_API int pkv_seq_truncate_batch(pkv_seq *const *seqs, int32_t M, const int32_t *new_len);
+
 /* Current length (tokens already committed by pkv_advance), or -1 for NULL. */
 PKV_API int32_t pkv_seq_len(const pkv_seq *seq);
 

@@ -140,6 +140,19 @@ class PoolModel:
         s.len = new_len
         return OK
 
+    def seq_truncate_batch(self, seqs, new_lens) -> int:
+        """Truncate several sequences: every row is validated before any changes."""
+        if len(seqs) != len(new_lens) or len(seqs) == 0:
+            return ERR_ARG
+        if len({id(s) for s in seqs}) != len(seqs):
+            return ERR_ARG
+        for s, n in zip(seqs, new_lens):
+            if s is None or not s.alive or not 0 <= n <= s.len:
+                return ERR_ARG
+        for s, n in zip(seqs, new_lens):
+            self.seq_truncate(s, n)
+        return OK
+
     # ---- step calls (caller contract) ------------------------------------------
     def _ensure_one(self, s: SeqModel, n: int) -> int:
         if s is None or not s.alive or n <= 0:

@@ -75,6 +75,7 @@ _SIGS = {
     "pkv_seq_fork": (_vp, [_vp]),
     "pkv_seq_free": (_int, [_vp]),
     "pkv_seq_truncate": (_int, [_vp, _i32]),
+    "pkv_seq_truncate_batch": (_int, [_vp, _i32, _pi32]),
     "pkv_seq_len": (_i32, [_vp]),
     "pkv_seq_page_table": (_i32, [_vp, _pi32, _i32]),
     "pkv_seq_slot": (_i32, [_vp]),
@@ -150,13 +151,27 @@ def _host(a, name="array"):
 
 
 def _seq_array(seqs):
-    arr = (_vp * len(seqs))(*seqs)
-    return arr
+    if isinstance(seqs, ctypes.Array):
+        return seqs
+    return (_vp * len(seqs))(*seqs)
 
 
 def _i32_array(vals):
+    if isinstance(vals, ctypes.Array):
+        return vals
     vals = [int(v) for v in vals]
     return (_i32 * max(1, len(vals)))(*vals)
+
+
+def seq_array(seqs):
+    """A reusable ctypes array of sequence handles (saves re-marshalling a
+    batch on every call)."""
+    return (_vp * len(seqs))(*seqs)
+
+
+def i32_array(vals):
+    """A reusable ctypes int32 array (per-row counts or lengths)."""
+    return (_i32 * max(1, len(vals)))(*[int(v) for v in vals])
 
 
 # ------------------------------------------------------------ entry points ----
@@ -218,6 +233,10 @@ def pkv_seq_free(seq):
 
 def pkv_seq_truncate(seq, new_len):
     return _lib.pkv_seq_truncate(seq, new_len)
+
+
+def pkv_seq_truncate_batch(seqs, new_len):
+    return _lib.pkv_seq_truncate_batch(_seq_array(seqs), len(seqs), _i32_array(new_len))
 
 
 def pkv_seq_len(seq):

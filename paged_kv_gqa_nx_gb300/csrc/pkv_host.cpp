@@ -787,6 +787,24 @@ int pkv_seq_truncate(pkv_seq *s, int32_t new_len) {
     return PKV_OK;
 }
 
+int pkv_seq_truncate_batch(pkv_seq *const *seqs, int32_t M, const int32_t *new_len) {
+    if (M <= 0 || !seqs || !new_len) return fail(PKV_ERR_ARG, "empty batch");
+    for (int32_t r = 0; r < M; ++r)
+        if (!seqs[r]) return fail(PKV_ERR_ARG, "sequence %d is NULL", r);
+    pkv_pool *p = seqs[0]->pool;
+    for (int32_t r = 1; r < M; ++r)
+        if (seqs[r]->pool != p) return fail(PKV_ERR_ARG, "sequences of different pools in one batch");
+    {
+        int rc = check_dup(p, seqs, M);
+        if (rc) return rc;
+    }
+    for (int32_t r = 0; r < M; ++r)
+        if (new_len[r] < 0 || new_len[r] > seqs[r]->len)
+            return fail(PKV_ERR_ARG, "row %d: truncate to %d outside [0, %d]", r, new_len[r], seqs[r]->len);
+    for (int32_t r = 0; r < M; ++r) pkv_seq_truncate(seqs[r], new_len[r]);
+    return PKV_OK;
+}
+
 int32_t pkv_seq_len(const pkv_seq *s) { return s ? s->len : -1; }
 int32_t pkv_seq_slot(const pkv_seq *s) { return s ? s->slot : -1; }
 

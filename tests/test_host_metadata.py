@@ -129,6 +129,12 @@ def test_random_ops_bit_exact_vs_model(seed):
                     rc_c = pkv.pkv_advance_batch([b[0] for b in batch], ns)
                     rc_m = t.m.advance_batch([b[1] for b in batch], ns)
                     assert rc_c == rc_m == 0
+            elif op == 7 and t.pairs and rng.random() < 0.3:
+                k = rng.randrange(1, min(4, len(t.pairs)) + 1)
+                batch = rng.sample(t.pairs, k)
+                nls = [rng.randrange(-1, b[1].len + 2) for b in batch]
+                assert pkv.pkv_seq_truncate_batch([b[0] for b in batch], nls) == \
+                    t.m.seq_truncate_batch([b[1] for b in batch], nls)
             elif op == 7 and t.pairs:
                 hc, sm = rng.choice(t.pairs)
                 n = rng.randrange(-1, 6)
