@@ -355,22 +355,47 @@ bool can_append(const pkv_seq *s, int32_t n) {
     return true;
 }
 
-// Split-K work list for a set of rows.  Units with a full split of S keys come
-// first (the heavy ones), each query's last (ragged) split after them.
+// Work list for a set of rows.  Rows with many queries (and a supported
+// shape) become tensor-core prefill tiles; every other query becomes split-K
+// decode units.  Decode units with a full split of S keys come first (the heavy
+// ones), each query's last (ragged) split after them; prefill tiles are listed
+// latest-first (the latest queries see the most keys).
 struct WorkList {
     std::vector<UnitDesc> units;
+    std::vector<PrefillTile> tiles;
     std::vector<MergeDesc> merges;
     int64_t n_part = 0;
 };
 
-void build_work(const std::vector<RowDesc> &rows, int causal, int32_t S, WorkList &w) {
+void build_work(const std::vector<RowDesc> &rows, int causal, int32_t S, int32_t head_dim,
+                int32_t group, WorkList &w) {
     std::vector<UnitDesc> tail;
     w.units.clear();
+    w.tiles.clear();
     w.merges.clear();
     w.n_part = 0;
+    const bool tc_shape = prefill_shape(head_dim, group);
+    const int32_t TQ = tc_shape ? 128 / group : 0;
+    const int32_t Sp = S * kPrefillSplitFactor;
     for (int32_t r = 0; r < static_cast<int32_t>(rows.size()); ++r) {
         const RowDesc &rd = rows[r];
         const int32_t total_k = rd.past_len + rd.n_q;
+        if (tc_shape && rd.n_q >= kPrefillMinQueries) {
+            for (int32_t q0 = ((rd.n_q - 1) / TQ) * TQ; q0 >= 0; q0 -= TQ) {
+                const int32_t nv = std::min(TQ, rd.n_q - q0);
+                const int32_t kend = causal ? total_k - rd.n_q + q0 + nv : total_k;
+                const int32_t ns = ceil_div(kend, Sp);
+                if (ns == 1) {
+                    w.tiles.push_back({r, q0, 0, -1});
+                } else {
+                    const int32_t part0 = static_cast<int32_t>(w.n_part);
+                    w.n_part += static_cast<int64_t>(nv) * ns;
+                    for (int32_t s = 0; s < ns; ++s) w.tiles.push_back({r, q0, s, part0});
+                    for (int32_t t = 0; t < nv; ++t) w.merges.push_back({r, q0 + t, part0 + t * ns, ns});
+                }
+            }
+            continue;
+        }
         for (int32_t i = 0; i < rd.n_q; ++i) {
             const int32_t q_pos = total_k - rd.n_q + i;
             const int32_t nk = causal ? q_pos + 1 : total_k;
@@ -487,7 +512,7 @@ int run_layer(pkv_seq *const *seqs, int32_t M, const int32_t *n_q, const float *
 
     WorkList w;
     const int32_t S = g_split_keys.load();
-    if (attend) build_work(rows, causal, S, w);
+    if (attend) build_work(rows, causal, S, head_dim, n_heads / n_kv_heads, w);
 
     Blob &blob = p->blob;
     blob.clear();
@@ -497,6 +522,7 @@ int run_layer(pkv_seq *const *seqs, int32_t M, const int32_t *n_q, const float *
     const size_t rows_off = blob.put(rows.data(), rows.size());
     const size_t app_off = blob.put(app.data(), app.size());
     const size_t units_off = blob.put(w.units.data(), w.units.size());
+    const size_t tiles_off = blob.put(w.tiles.data(), w.tiles.size());
     const size_t merges_off = blob.put(w.merges.data(), w.merges.size());
 
     cudaError_t e = upload_blob(p);
@@ -558,8 +584,18 @@ int run_layer(pkv_seq *const *seqs, int32_t M, const int32_t *n_q, const float *
         a.pl = a.pm + pf;
         a.pacc = a.pl + pf;
     }
-    e = launch(PKV_KERNEL_DECODE, st, [&] { return launch_decode_paged(a, addr, st); });
-    if (e != cudaSuccess) return cuda_fail(e, "decode kernel");
+    if (!w.tiles.empty()) {
+        const PrefillArgs pa{Qd, Od, a.rows, dptr<PrefillTile>(p, tiles_off),
+                             static_cast<int32_t>(w.tiles.size()), a.pm, a.pl, a.pacc, n_heads,
+                             n_kv_heads, a.group, a.causal, S * kPrefillSplitFactor, a.scale_log2,
+                             p->err_dev};
+        e = launch(PKV_KERNEL_PREFILL, st, [&] { return launch_prefill_paged(pa, addr, st); });
+        if (e != cudaSuccess) return cuda_fail(e, "prefill kernel");
+    }
+    if (!w.units.empty()) {
+        e = launch(PKV_KERNEL_DECODE, st, [&] { return launch_decode_paged(a, addr, st); });
+        if (e != cudaSuccess) return cuda_fail(e, "decode kernel");
+    }
     if (!w.merges.empty()) {
         MergeArgs m{a.pm, a.pl, a.pacc, Od, a.rows, dptr<MergeDesc>(p, merges_off),
                     static_cast<int32_t>(w.merges.size()), n_heads, head_dim};
@@ -968,10 +1004,11 @@ int pkv_attn_contiguous(const float *Q, const float *Kc, const float *Vc, int32_
     std::vector<RowDesc> rows{{0, total_k - n_q, n_q, 0}};
     WorkList w;
     const int32_t S = g_split_keys.load();
-    build_work(rows, causal, S, w);
+    build_work(rows, causal, S, head_dim, n_heads / n_kv_heads, w);
     Blob blob;
     const size_t rows_off = blob.put(rows.data(), 1);
     const size_t units_off = blob.put(w.units.data(), w.units.size());
+    const size_t tiles_off = blob.put(w.tiles.data(), w.tiles.size());
     const size_t merges_off = blob.put(w.merges.data(), w.merges.size());
     const size_t desc_bytes = (blob.size() + 255) & ~static_cast<size_t>(255);
     const size_t pf = static_cast<size_t>(w.n_part) * n_heads;
@@ -1015,7 +1052,15 @@ int pkv_attn_contiguous(const float *Q, const float *Kc, const float *Vc, int32_
         a.pacc = a.pl + pf;
     }
     const ContigAddr addr{Kc, Vc, n_kv_heads * head_dim};
-    e = launch(PKV_KERNEL_DECODE, st, [&] { return launch_decode_contig(a, addr, st); });
+    if (!w.tiles.empty()) {
+        const PrefillArgs pa{Q, out, a.rows, reinterpret_cast<const PrefillTile *>(base + tiles_off),
+                             static_cast<int32_t>(w.tiles.size()), a.pm, a.pl, a.pacc, n_heads,
+                             n_kv_heads, a.group, a.causal, S * kPrefillSplitFactor, a.scale_log2,
+                             a.err};
+        e = launch(PKV_KERNEL_PREFILL, st, [&] { return launch_prefill_contig(pa, addr, st); });
+    }
+    if (e == cudaSuccess && !w.units.empty())
+        e = launch(PKV_KERNEL_DECODE, st, [&] { return launch_decode_contig(a, addr, st); });
     if (e == cudaSuccess && !w.merges.empty()) {
         MergeArgs m{a.pm, a.pl, a.pacc, out, a.rows,
                     reinterpret_cast<const MergeDesc *>(base + merges_off),
@@ -1101,11 +1146,14 @@ int pkv_profile_read(int32_t kind, double *ms, int64_t *launches) {
 namespace pkv {
 
 void build_contig_work(int32_t n_q, int32_t total_k, int32_t causal, int32_t split_keys,
-                       std::vector<UnitDesc> &units, std::vector<MergeDesc> &merges,
+                       int32_t head_dim, int32_t group, std::vector<UnitDesc> &units,
+                       std::vector<PrefillTile> &tiles, std::vector<MergeDesc> &merges,
                        int64_t *n_part) {
     WorkList w;
-    build_work(std::vector<RowDesc>{{0, total_k - n_q, n_q, 0}}, causal, split_keys, w);
+    build_work(std::vector<RowDesc>{{0, total_k - n_q, n_q, 0}}, causal, split_keys, head_dim,
+               group, w);
     units.swap(w.units);
+    tiles.swap(w.tiles);
     merges.swap(w.merges);
     *n_part = w.n_part;
 }

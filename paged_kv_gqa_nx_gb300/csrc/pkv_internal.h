@@ -74,6 +74,26 @@ struct AttnArgs {
     int32_t *err;
 };
 
+// One tensor-core prefill tile: queries q0 .. q0 + 128/G - 1 of row `row`
+// (clipped to n_q), key split `split` of size PrefillArgs::split_keys.
+// part0 < 0: the tile's queries have one split and write out directly;
+// otherwise query q0 + t's partial for split s is record part0 + t*n_split + s.
+struct PrefillTile {
+    int32_t row, q0, split, part0;
+};
+
+struct PrefillArgs {
+    const float *Q;
+    float *out;
+    const RowDesc *rows;
+    const PrefillTile *tiles;
+    int32_t n_tiles;
+    float *pm, *pl, *pacc;  // same partial layout as AttnArgs
+    int32_t n_heads, n_kv, group, causal, split_keys;
+    float scale_log2;
+    int32_t *err;
+};
+
 struct MergeArgs {
     const float *pm, *pl, *pacc;
     float *out;
@@ -95,6 +115,18 @@ cudaError_t launch_copy_blocks(float *k, float *v, const CopyDesc *items, int32_
 cudaError_t launch_decode_paged(const AttnArgs &a, const PagedAddr &addr, cudaStream_t s);
 cudaError_t launch_decode_contig(const AttnArgs &a, const ContigAddr &addr, cudaStream_t s);
 cudaError_t launch_merge(const MergeArgs &a, cudaStream_t s);
+// Tensor-core prefill (pkv_prefill.cu): head_dim 128, group 1, 2, 4 or 8.
+cudaError_t launch_prefill_paged(const PrefillArgs &a, const PagedAddr &addr, cudaStream_t s);
+cudaError_t launch_prefill_contig(const PrefillArgs &a, const ContigAddr &addr, cudaStream_t s);
+
+// Rows with at least this many queries take the tensor-core prefill kernel
+// (when head_dim is 128 and the group is 1, 2, 4 or 8); its key split is
+// kPrefillSplitFactor times the decode split.  Both depend only on the row.
+constexpr int kPrefillMinQueries = 32;
+constexpr int kPrefillSplitFactor = 16;
+__host__ __device__ constexpr bool prefill_shape(int head_dim, int group) {
+    return head_dim == 128 && (group == 1 || group == 2 || group == 4 || group == 8);
+}
 
 // Host-core helpers for entry points defined in other translation units
 // (pkv_host.cpp).  build_contig_work: the split-K work list of one contiguous
@@ -102,7 +134,8 @@ cudaError_t launch_merge(const MergeArgs &a, cudaStream_t s);
 // the library's launch accounting and optional event timing.  report_error:
 // record the calling thread's last error message and return code.
 void build_contig_work(int32_t n_q, int32_t total_k, int32_t causal, int32_t split_keys,
-                       std::vector<UnitDesc> &units, std::vector<MergeDesc> &merges,
+                       int32_t head_dim, int32_t group, std::vector<UnitDesc> &units,
+                       std::vector<PrefillTile> &tiles, std::vector<MergeDesc> &merges,
                        int64_t *n_part);
 cudaError_t launch_counted(int kind, cudaStream_t s, cudaError_t (*fn)(void *), void *ctx);
 int32_t current_split_keys();

@@ -48,6 +48,15 @@ cudaError_t run_decode(void *p) {
     auto *c = static_cast<DecodeCtx *>(p);
     return launch_decode_contig(*c->a, *c->addr, c->s);
 }
+struct PrefillCtx {
+    const PrefillArgs *a;
+    const ContigAddr *addr;
+    cudaStream_t s;
+};
+cudaError_t run_prefill(void *p) {
+    auto *c = static_cast<PrefillCtx *>(p);
+    return launch_prefill_contig(*c->a, *c->addr, c->s);
+}
 struct MergeCtx {
     const MergeArgs *m;
     cudaStream_t s;
@@ -81,13 +90,16 @@ extern "C" int pkv_attn_contiguous_noalloc(const float *Q, const float *Kc, cons
     // work list and the scratch layout: [error word][rows][units][merges][partials]
     const int32_t S = current_split_keys();
     std::vector<UnitDesc> units;
+    std::vector<PrefillTile> tiles;
     std::vector<MergeDesc> merges;
     int64_t n_part = 0;
-    build_contig_work(n_q, total_k, causal, S, units, merges, &n_part);
+    build_contig_work(n_q, total_k, causal, S, head_dim, n_heads / n_kv_heads, units, tiles,
+                      merges, &n_part);
     const RowDesc row{0, total_k - n_q, n_q, 0};
     const size_t rows_off = 256;
     const size_t units_off = round256(rows_off + sizeof(RowDesc));
-    const size_t merges_off = round256(units_off + units.size() * sizeof(UnitDesc));
+    const size_t tiles_off = round256(units_off + units.size() * sizeof(UnitDesc));
+    const size_t merges_off = round256(tiles_off + tiles.size() * sizeof(PrefillTile));
     const size_t desc_end = round256(merges_off + merges.size() * sizeof(MergeDesc));
     const size_t pf = static_cast<size_t>(n_part) * n_heads;
     const size_t total = desc_end + pf * (2 + static_cast<size_t>(head_dim)) * sizeof(float);
@@ -127,6 +139,8 @@ extern "C" int pkv_attn_contiguous_noalloc(const float *Q, const float *Kc, cons
     std::memcpy(blob.data(), &row, sizeof row);
     if (!units.empty())
         std::memcpy(blob.data() + (units_off - rows_off), units.data(), units.size() * sizeof(UnitDesc));
+    if (!tiles.empty())
+        std::memcpy(blob.data() + (tiles_off - rows_off), tiles.data(), tiles.size() * sizeof(PrefillTile));
     if (!merges.empty())
         std::memcpy(blob.data() + (merges_off - rows_off), merges.data(), merges.size() * sizeof(MergeDesc));
     e = cudaMemsetAsync(base, 0, sizeof(int32_t), st);
@@ -154,8 +168,16 @@ extern "C" int pkv_attn_contiguous_noalloc(const float *Q, const float *Kc, cons
         a.pacc = a.pl + pf;
     }
     const ContigAddr addr{Kc, Vc, n_kv_heads * head_dim};
+    if (!tiles.empty()) {
+        const PrefillArgs pa{Q, out, a.rows, reinterpret_cast<const PrefillTile *>(base + tiles_off),
+                             static_cast<int32_t>(tiles.size()), a.pm, a.pl, a.pacc, n_heads,
+                             n_kv_heads, a.group, a.causal, S * kPrefillSplitFactor, a.scale_log2,
+                             a.err};
+        PrefillCtx pc{&pa, &addr, st};
+        e = launch_counted(PKV_KERNEL_PREFILL, st, run_prefill, &pc);
+    }
     DecodeCtx dc{&a, &addr, st};
-    e = launch_counted(PKV_KERNEL_DECODE, st, run_decode, &dc);
+    if (e == cudaSuccess && !units.empty()) e = launch_counted(PKV_KERNEL_DECODE, st, run_decode, &dc);
     if (e == cudaSuccess && !merges.empty()) {
         MergeArgs m{a.pm, a.pl, a.pacc, out, a.rows,
                     reinterpret_cast<const MergeDesc *>(base + merges_off),

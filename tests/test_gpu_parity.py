@@ -250,3 +250,28 @@ def test_launch_accounting_and_profiling():
     finally:
         pkv.pkv_profile_reset()
         pool.close()
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("H,KV", [(32, 8), (16, 8), (8, 8), (64, 8)], ids=["g4", "g2", "g1", "g8"])
+def test_prefill_tensor_core_rows(H, KV, split_keys):
+    """Rows with n_q >= 32 take the tcgen05 3xTF32 kernel: tiles of 128/G
+    tokens, ragged last tiles, an empty history, and rows long enough to be
+    cut into several key splits (split size 16 x 32 = 512 keys) and merged."""
+    split_keys(32)
+    run_case(H, KV, 128, 16, [0, 5, 31, 600, 1100], [32, 33, 100, 64, 47], seed=H + 1)
+
+
+@pytest.mark.gpu
+def test_prefill_noncausal_and_odd_blocks(split_keys):
+    split_keys(512)
+    run_case(32, 8, 128, 5, [0, 77, 300], [40, 96, 33], causal=0, seed=21)
+    run_case(32, 8, 128, 4, [13, 250], [64, 50], causal=1, seed=22)
+
+
+@pytest.mark.gpu
+def test_prefill_and_decode_rows_in_one_batch(split_keys):
+    """A batch mixing decode rows, short chunks (decode kernel) and long
+    chunks (tensor-core kernel); every row equals its M = 1 launch."""
+    split_keys(128)
+    run_case(32, 8, 128, 16, [3000, 10, 257, 0, 999, 64], [1, 31, 32, 200, 1, 130], seed=23)
