@@ -50,7 +50,10 @@ def test_no_alloc_matches_allocating_entry_point_on_two_calls():
 
 @pytest.mark.gpu
 def test_no_alloc_rejects_requests_beyond_its_scratch():
-    Q, Kc, Vc, n_q, tk, H, KV, hd, causal, scale = _case(512, 4000, 32, 8, 128, 1, 3)
+    # 31 queries (the split-K decode path) over a 70 000-key history need about
+    # 70 MB of split partials, far beyond the static array; the buffers are
+    # full size so that nothing could be read out of bounds in any case
+    Q, Kc, Vc, n_q, tk, H, KV, hd, causal, scale = _case(31, 70000, 32, 8, 128, 1, 3)
     out = torch.empty(n_q, H * hd, device="cuda")
     rc = pkv.pkv_attn_contiguous_noalloc(Q, Kc, Vc, n_q, tk, H, KV, hd, causal, scale, out,
                                          torch.cuda.current_stream())
