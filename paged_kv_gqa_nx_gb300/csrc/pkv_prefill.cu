@@ -6,25 +6,30 @@
 // into a tf32 part and its exact f32 rest (x = hi + lo) and every product is
 // formed as hi*hi + hi*lo + lo*hi; the dropped lo*lo term is ~2^-20 relative.
 //
-// One CTA (128 threads) = one tile of 128 query rows -- (128 / G) consecutive
-// tokens x the G query heads that share kv head `kvh` -- and one key split.
-// Row m of the tile is token m / G, head m % G, and TMEM lane m; thread m owns
-// that row's online softmax.  Per key tile of 32 positions:
-//   1. K and V rows (through the page table or a contiguous history) are
-//      split into hi/lo and written to shared memory as the K-major B operand
-//      of Q.K^T and, transposed, of P.V;
-//   2. S[128 x 32] = Q.K^T into TMEM (48 MMAs of K = 8);
-//   3. each thread reads its row of S, applies the offset-causal mask
-//      (key j visible iff j <= q_pos = total_k - n_q + i), updates (max, sum)
-//      and writes p (hi/lo) as the A operand of P.V;
-//   4. D[128 x 128] = P.V into TMEM (12 MMAs); each thread adds its row of D
-//      to its register accumulator after rescaling.
-// The next tile's K/V rows are loaded into registers while the MMAs run.
-// Shared memory: Q hi/lo 128 KiB, K hi/lo (aliased by P hi/lo) 32 KiB, V^T
-// hi/lo 32 KiB.  TMEM: 256 columns (D at 0, S at 128).
+// One CTA = one tile of 128 query rows -- (128 / G) consecutive tokens x the G
+// query heads that share kv head `kvh` -- and one key split; 256 threads.
+// Row m of the tile is token m / G, head m % G and TMEM lane m; the two
+// threads that share TMEM lane m (warps w and w + 4) each own 32 of a key
+// tile's scores and half of the row's output columns, and exchange the row
+// max and sum through shared memory.  Two threads issue the MMAs (QK and PV
+// concurrently, each committing to its own mbarrier).  Key tiles are 64
+// positions:
+//   QK(j):  S[128 x 64]  = Q.K_j^T     A = Q hi (TMEM) / Q lo (smem), B = K_j (smem)
+//   PV(j):  D[128 x 128] = P_j.V_j     A = P hi/lo (TMEM),            B = V_j^T (smem)
+// Loop j: wait S_j -> online softmax (offset-causal mask: key p visible iff
+// p <= q_pos = total_k - n_q + i) -> wait PV(j-1) -> write P_j, V_j, K_{j+1}
+// -> QK(j+1) and PV(j) are issued, PV adding into the TMEM
+// accumulator D; the softmax of tile j+1 runs while PV(j) executes.  p is
+// relative to a reference max that moves (and D is rescaled) only when a
+// tile's max exceeds it by more than 2^8, which keeps every p below 256.
+// K/V rows for the next tiles are loaded into registers while the MMAs run.
+// Shared memory: Q lo 64 KiB, K hi/lo 64 KiB, V^T hi/lo 64 KiB.
+// TMEM (512 columns): Q hi [0,128), S [128,192), P hi [256,320), P lo
+// [320,384), D [384,512).
 //
-// The address functor is the decode kernels' (PagedRows / ContigRows), so the
-// paged and contiguous instantiations return the same bits.
+// The address functors mirror the decode kernels' (paged through the page
+// table, or contiguous), so the paged and contiguous instantiations return the
+// same bits.
 #include "pkv_internal.h"
 #include "pkv_tcgen05.h"
 
@@ -34,8 +39,11 @@ namespace {
 using namespace tc;
 
 constexpr int kHD = 128;
-constexpr int kKT = 32;          // keys per tile
-constexpr uint32_t kTmemCols = 256;
+constexpr int kKT = 64;  // keys per tile
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColQhi = 0, kColS = 128, kColPhi = 256, kColPlo = 320, kColD = 384;
+constexpr int kThreads = 256;                 // two threads per tile row
+constexpr float kRescale = 8.f;               // lazy-rescale threshold (base 2)
 
 struct PagedRowsP {
     PagedAddr a;
@@ -58,6 +66,9 @@ struct PagedRowsP {
         vr = a.v + o;
         return true;
     }
+    // groups of 8 positions starting at a multiple of 8 lie in one block
+    __device__ __forceinline__ bool whole8() const { return (a.bs & 7) == 0; }
+    __device__ __forceinline__ size_t row_stride() const { return static_cast<size_t>(a.kv_dim); }
 };
 
 struct ContigRowsP {
@@ -69,12 +80,14 @@ struct ContigRowsP {
         vr = a.v + o;
         return true;
     }
+    __device__ __forceinline__ bool whole8() const { return true; }
+    __device__ __forceinline__ size_t row_stride() const { return static_cast<size_t>(a.kv_dim); }
 };
 
-constexpr size_t kSmemQ = 64 * 1024;       // one of Q hi / Q lo
-constexpr size_t kSmemK = 16 * 1024;       // one of K hi / K lo (and P hi / P lo)
-constexpr size_t kSmemV = 16 * 1024;       // one of V^T hi / V^T lo
-constexpr size_t kSmemBytes = 2 * kSmemQ + 2 * kSmemK + 2 * kSmemV + 1024;  // + alignment slack
+constexpr uint32_t kSmemQlo = 64 * 1024;  // 4 k-blocks of 128 rows
+constexpr uint32_t kSmemK = 32 * 1024;    // one of K hi / lo: 4 k-blocks of 64 rows
+constexpr uint32_t kSmemV = 32 * 1024;    // one of V^T hi / lo: 2 k-blocks of 128 rows
+constexpr size_t kSmemBytes = kSmemQlo + 2 * kSmemK + 2 * kSmemV + 1024;  // + alignment slack
 
 __device__ __forceinline__ void split4(const float4 &x, float4 &h, float4 &l) {
     split_tf32(x.x, h.x, l.x);
@@ -84,35 +97,35 @@ __device__ __forceinline__ void split4(const float4 &x, float4 &h, float4 &l) {
 }
 
 template <int G, class Rows>
-__global__ void __launch_bounds__(128, 1) prefill_tc_kernel(PrefillArgs a, Rows rows_of) {
+__global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs a, Rows rows_of) {
     constexpr int TQ = 128 / G;  // tokens per tile
     extern __shared__ __align__(1024) unsigned char smraw[];
     unsigned char *sm = reinterpret_cast<unsigned char *>(
         (reinterpret_cast<uintptr_t>(smraw) + 1023) & ~static_cast<uintptr_t>(1023));
-    unsigned char *Qhi = sm;
-    unsigned char *Qlo = Qhi + kSmemQ;
-    unsigned char *Khi = Qlo + kSmemQ;   // also P hi
-    unsigned char *Klo = Khi + kSmemK;   // also P lo
+    unsigned char *Qlo = sm;
+    unsigned char *Khi = Qlo + kSmemQlo;
+    unsigned char *Klo = Khi + kSmemK;
     unsigned char *Vhi = Klo + kSmemK;
     unsigned char *Vlo = Vhi + kSmemV;
-    __shared__ uint64_t mbar;
+    __shared__ uint64_t bar_qk, bar_pv;
     __shared__ uint32_t tslot;
+    __shared__ float red[2][kThreads];
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int wq = warp & 3, half = (warp >> 2) & 1;  // TMEM lane quadrant, key / column half
+    const int m = 32 * wq + lane;                      // this thread's row of the tile
     const int ti = blockIdx.x / a.n_kv;
     const int kvh = blockIdx.x - ti * a.n_kv;
     const PrefillTile tile = a.tiles[ti];
     const RowDesc rd = a.rows[tile.row];
     const int total_k = rd.past_len + rd.n_q;
 
-    // this thread's row of the tile
-    const int tq = tid / G, g = tid - (tid / G) * G;
+    const int tq = m / G, g = m - (m / G) * G;
     const int qi = tile.q0 + tq;
     const bool valid = qi < rd.n_q;
     const int q_pos = total_k - rd.n_q + qi;
     const int kend_row = valid ? (a.causal ? min(q_pos + 1, total_k) : total_k) : 1;
 
-    // key range of this split
     const int n_valid_q = min(TQ, rd.n_q - tile.q0);
     const int kend_tile =
         a.causal ? min(total_k, total_k - rd.n_q + tile.q0 + n_valid_q) : total_k;
@@ -120,203 +133,277 @@ __global__ void __launch_bounds__(128, 1) prefill_tc_kernel(PrefillArgs a, Rows 
     const int kend = min(kbeg + a.split_keys, kend_tile);
     const int kt0 = kbeg / kKT, kt1 = (kend + kKT - 1) / kKT;
 
-    // Q row (pre-scaled to base-2 units), split into the A operand
-    {
-        const float *qrow = a.Q + static_cast<size_t>(rd.q_row0 + (valid ? qi : 0)) * (a.n_heads * kHD) +
-                            static_cast<size_t>(kvh * G + g) * kHD;
-#pragma unroll 4
-        for (int j = 0; j < 32; ++j) {
-            float4 x = valid ? __ldg(reinterpret_cast<const float4 *>(qrow) + j) : make_float4(0.f, 0.f, 0.f, 0.f);
-            x.x *= a.scale_log2;
-            x.y *= a.scale_log2;
-            x.z *= a.scale_log2;
-            x.w *= a.scale_log2;
-            float4 h, l;
-            split4(x, h, l);
-            const uint32_t off = (j >> 3) * 16384u + sw128_chunk(tid, j & 7);
-            *reinterpret_cast<float4 *>(Qhi + off) = h;
-            *reinterpret_cast<float4 *>(Qlo + off) = l;
-        }
-    }
-    if (tid == 0) mbar_init(smem_u32(&mbar), 1);
     if (warp == 0) {
         tmem_alloc(smem_u32(&tslot), kTmemCols);
         tmem_relinquish();
     }
-
-    // register prefetch of one key tile: K rows key-major (8 keys per warp,
-    // one 512-byte row per instruction), V rows key-per-lane (for the transpose)
-    float4 kreg[8], vreg[8];
-    auto prefetch = [&](int kt) {
-        const int base = kt * kKT;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const int pos = base + warp * 8 + i;
-            kreg[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-            const float *kr, *vr;
-            if (pos < kend && rows_of.row(rd.slot, pos, kvh, kr, vr, a.err))
-                kreg[i] = __ldg(reinterpret_cast<const float4 *>(kr) + lane);
-        }
-        const int vpos = base + lane;
-        const float *kr, *vr;
-        const bool vok = vpos < kend && rows_of.row(rd.slot, vpos, kvh, kr, vr, a.err);
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-            vreg[i] = vok ? __ldg(reinterpret_cast<const float4 *>(vr) + warp + 4 * i)
-                          : make_float4(0.f, 0.f, 0.f, 0.f);
-    };
-    if (kt0 < kt1) prefetch(kt0);
-
-    fence_proxy_async();
+    if (tid == 0) {
+        mbar_init(smem_u32(&bar_qk), 1);
+        mbar_init(smem_u32(&bar_pv), 1);
+    }
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
     const uint32_t tbase = tslot;
-    const uint32_t tlane = static_cast<uint32_t>(32 * warp) << 16;
-    const uint32_t tS = tbase + 128, tD = tbase;
-    const uint32_t idesc_s = idesc_tf32(128, kKT), idesc_o = idesc_tf32(128, kHD);
-
-    float o[kHD];
-#pragma unroll
-    for (int d = 0; d < kHD; ++d) o[d] = 0.f;
-    float m_run = -INFINITY, l_run = 0.f;
-    uint32_t phase = 0;
     bool ok = true;
 
-    for (int kt = kt0; kt < kt1 && ok; ++kt) {
-        // 1. K (B operand of Q.K^T) and V^T (B operand of P.V), hi and lo
+    {
+        // ---- compute warps ----
+        const uint32_t tlane = static_cast<uint32_t>(32 * wq) << 16;
+        // Q row (pre-scaled to base-2 units): hi -> TMEM, lo -> smem (A operands)
+        {
+            const float *qrow = a.Q + static_cast<size_t>(rd.q_row0 + (valid ? qi : 0)) * (a.n_heads * kHD) +
+                                static_cast<size_t>(kvh * G + g) * kHD + 64 * half;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const int key = warp * 8 + i;
-            float4 h, l;
-            split4(kreg[i], h, l);
-            const uint32_t off = (lane >> 3) * 4096u + sw128_chunk(key, lane & 7);
-            *reinterpret_cast<float4 *>(Khi + off) = h;
-            *reinterpret_cast<float4 *>(Klo + off) = l;
-        }
+            for (int c = 0; c < 2; ++c) {
+                float hv[32];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const int d0 = 4 * (warp + 4 * i);
-            const float v4[4] = {vreg[i].x, vreg[i].y, vreg[i].z, vreg[i].w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                float h, l;
-                split_tf32(v4[e], h, l);
-                const uint32_t off = sw128_offset(d0 + e, lane);
-                *reinterpret_cast<float *>(Vhi + off) = h;
-                *reinterpret_cast<float *>(Vlo + off) = l;
+                for (int j4 = 0; j4 < 8; ++j4) {
+                    float4 x = valid ? __ldg(reinterpret_cast<const float4 *>(qrow + 32 * c) + j4)
+                                     : make_float4(0.f, 0.f, 0.f, 0.f);
+                    x.x *= a.scale_log2;
+                    x.y *= a.scale_log2;
+                    x.z *= a.scale_log2;
+                    x.w *= a.scale_log2;
+                    float4 h, l;
+                    split4(x, h, l);
+                    hv[4 * j4] = h.x;
+                    hv[4 * j4 + 1] = h.y;
+                    hv[4 * j4 + 2] = h.z;
+                    hv[4 * j4 + 3] = h.w;
+                    const uint32_t off = (2 * half + c) * 16384u + sw128_chunk(m, j4);
+                    *reinterpret_cast<float4 *>(Qlo + off) = l;
+                }
+                tmem_st32(tbase + tlane + kColQhi + 64 * half + 32 * c, hv);
             }
         }
-        fence_proxy_async();
-        fence_before_sync();
-        __syncthreads();
-        fence_after_sync();
 
-        // 2. S = Q.K^T
-        if (tid == 0) {
-#pragma unroll 1
+        // K rows key-major (8 keys per warp, one 512-byte row per instruction;
+        // one page-table lookup per warp when a block holds whole 8-key groups),
+        // V rows key-per-lane for the transposed store
+        float4 kreg[8], vreg[8];
+        const bool k_whole = rows_of.whole8();
+        const size_t rstride = rows_of.row_stride();
+        auto prefetch_k = [&](int kt) {
+            const int pos0 = kt * kKT + warp * 8;
+            if (k_whole) {
+                const float *kr, *vr;
+                const bool have = pos0 < kend && rows_of.row(rd.slot, pos0, kvh, kr, vr, a.err);
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    kreg[i] = (have && pos0 + i < kend)
+                                  ? __ldg(reinterpret_cast<const float4 *>(kr + i * rstride) + lane)
+                                  : make_float4(0.f, 0.f, 0.f, 0.f);
+            } else {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const float *kr, *vr;
+                    const bool have = pos0 + i < kend && rows_of.row(rd.slot, pos0 + i, kvh, kr, vr, a.err);
+                    kreg[i] = have ? __ldg(reinterpret_cast<const float4 *>(kr) + lane)
+                                   : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+            }
+        };
+        auto prefetch_v = [&](int kt) {
+            const int pos = kt * kKT + 32 * half + lane;
+            const float *kr, *vr;
+            const bool have = pos < kend && rows_of.row(rd.slot, pos, kvh, kr, vr, a.err);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                vreg[i] = have ? __ldg(reinterpret_cast<const float4 *>(vr) + wq + 4 * i)
+                               : make_float4(0.f, 0.f, 0.f, 0.f);
+        };
+        auto store_k = [&]() {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                float4 h, l;
+                split4(kreg[i], h, l);
+                const uint32_t off = (lane >> 3) * 8192u + sw128_chunk(warp * 8 + i, lane & 7);
+                *reinterpret_cast<float4 *>(Khi + off) = h;
+                *reinterpret_cast<float4 *>(Klo + off) = l;
+            }
+        };
+        auto store_v = [&]() {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int d0 = 4 * (wq + 4 * i);
+                const float v4[4] = {vreg[i].x, vreg[i].y, vreg[i].z, vreg[i].w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    float h, l;
+                    split_tf32(v4[e], h, l);
+                    const uint32_t off = half * 16384u + sw128_offset(d0 + e, lane);
+                    *reinterpret_cast<float *>(Vhi + off) = h;
+                    *reinterpret_cast<float *>(Vlo + off) = l;
+                }
+            }
+        };
+        // MMA issue: after the operand barrier, lane 0 of warp 0 issues QK (and
+        // commits it to bar_qk) while lane 0 of warp 4 issues PV (bar_pv); each
+        // commit tracks only its own thread's MMAs.
+        const uint64_t dKhi = desc_sw128(smem_u32(Khi)), dKlo = desc_sw128(smem_u32(Klo));
+        const uint64_t dQlo = desc_sw128(smem_u32(Qlo));
+        const uint64_t dVhi = desc_sw128(smem_u32(Vhi)), dVlo = desc_sw128(smem_u32(Vlo));
+        auto issue_qk = [&]() {
+            const uint32_t tS = tbase + kColS, tQ = tbase + kColQhi;
+            const uint32_t idesc_s = idesc_tf32(128, kKT);
+#pragma unroll
             for (int s = 0; s < 16; ++s) {
-                const uint32_t ao = (s >> 2) * 16384u + (s & 3) * 32u;
-                const uint32_t bo = (s >> 2) * 4096u + (s & 3) * 32u;
-                const uint64_t qh = desc_sw128(smem_u32(Qhi + ao)), ql = desc_sw128(smem_u32(Qlo + ao));
-                const uint64_t kh = desc_sw128(smem_u32(Khi + bo)), kl = desc_sw128(smem_u32(Klo + bo));
-                mma_tf32(tS, qh, kh, idesc_s, s > 0);
-                mma_tf32(tS, qh, kl, idesc_s, 1);
-                mma_tf32(tS, ql, kh, idesc_s, 1);
+                const uint64_t ko = ((s >> 2) * 8192u + (s & 3) * 32u) >> 4;
+                const uint64_t qo = ((s >> 2) * 16384u + (s & 3) * 32u) >> 4;
+                mma_tf32_ts(tS, tQ + 8 * s, dKhi + ko, idesc_s, s > 0);
+                mma_tf32_ts(tS, tQ + 8 * s, dKlo + ko, idesc_s, 1);
+                mma_tf32(tS, dQlo + qo, dKhi + ko, idesc_s, 1);
             }
-            mma_commit(smem_u32(&mbar));
-        }
-        if (kt + 1 < kt1) prefetch(kt + 1);
-        ok = __syncthreads_and(mbar_wait(smem_u32(&mbar), phase));
-        phase ^= 1;
-        if (!ok) break;
-        fence_after_sync();
-
-        // 3. online softmax of this row over the tile's 32 keys
-        float s[32];
-        tmem_ld32(tS + tlane, s);
-        const int base = kt * kKT;
-        float tmax = -INFINITY;
+            mma_commit(smem_u32(&bar_qk));
+        };
+        auto issue_pv = [&](bool first) {
+            const uint32_t tD = tbase + kColD, tPh = tbase + kColPhi, tPl = tbase + kColPlo;
+            const uint32_t idesc_o = idesc_tf32(128, kHD);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-            const bool vis = base + i < kend_row && base + i < kend;
-            s[i] = vis ? s[i] : -INFINITY;
-            tmax = fmaxf(tmax, s[i]);
-        }
-        const float m_new = fmaxf(m_run, tmax);
-        const float alpha = (m_new == -INFINITY) ? 1.f : exp2f(m_run - m_new);
-        float psum = 0.f;
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-            s[i] = (s[i] == -INFINITY) ? 0.f : exp2f(s[i] - m_new);
-            psum += s[i];
-        }
-        l_run = fmaf(l_run, alpha, psum);
-        m_run = m_new;
-        // p (A operand of P.V) over the K hi/lo space, row tid
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-            float4 p = make_float4(s[4 * c], s[4 * c + 1], s[4 * c + 2], s[4 * c + 3]);
-            float4 h, l;
-            split4(p, h, l);
-            const uint32_t off = sw128_chunk(tid, c);
-            *reinterpret_cast<float4 *>(Khi + off) = h;
-            *reinterpret_cast<float4 *>(Klo + off) = l;
-        }
-        fence_proxy_async();
-        fence_before_sync();
-        __syncthreads();
-        fence_after_sync();
-
-        // 4. D = P.V
-        if (tid == 0) {
-#pragma unroll 1
-            for (int st = 0; st < 4; ++st) {
-                const uint32_t off = st * 32u;
-                const uint64_t ph = desc_sw128(smem_u32(Khi + off)), pl = desc_sw128(smem_u32(Klo + off));
-                const uint64_t vh = desc_sw128(smem_u32(Vhi + off)), vl = desc_sw128(smem_u32(Vlo + off));
-                mma_tf32(tD, ph, vh, idesc_o, st > 0);
-                mma_tf32(tD, ph, vl, idesc_o, 1);
-                mma_tf32(tD, pl, vh, idesc_o, 1);
+            for (int s = 0; s < 8; ++s) {
+                const uint64_t vo = ((s >> 2) * 16384u + (s & 3) * 32u) >> 4;
+                mma_tf32_ts(tD, tPh + 8 * s, dVhi + vo, idesc_o, !first || s > 0);
+                mma_tf32_ts(tD, tPh + 8 * s, dVlo + vo, idesc_o, 1);
+                mma_tf32_ts(tD, tPl + 8 * s, dVhi + vo, idesc_o, 1);
             }
-            mma_commit(smem_u32(&mbar));
-        }
-        ok = __syncthreads_and(mbar_wait(smem_u32(&mbar), phase));
-        phase ^= 1;
-        if (!ok) break;
-        fence_after_sync();
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            float dv[32];
-            tmem_ld32(tD + tlane + 32 * c, dv);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) o[32 * c + i] = fmaf(o[32 * c + i], alpha, dv[i]);
-        }
-        fence_before_sync();
-        __syncthreads();
-    }
+            mma_commit(smem_u32(&bar_pv));
+        };
+        auto operands_ready = [&](bool qk, bool pv, bool pv_first) {
+            tmem_st_wait();
+            fence_proxy_async();
+            fence_before_sync();
+            __syncthreads();
+            fence_after_sync();
+            if (qk && tid == 0) issue_qk();
+            if (pv && tid == 128) issue_pv(pv_first);
+        };
 
-    if (!ok) {
-        if (tid == 0 && a.err) atomicOr(a.err, 2);
-    } else if (valid) {
-        const int h = kvh * G + g;
-        if (tile.part0 < 0) {
-            float *orow = a.out + static_cast<size_t>(rd.q_row0 + qi) * (a.n_heads * kHD) +
-                          static_cast<size_t>(h) * kHD;
-            const float inv = 1.f / l_run;
+        // The output accumulator lives in TMEM (D) and the P.V MMAs add into it.
+        // p is taken relative to a reference max m_ref that moves only when a
+        // tile's max exceeds it by more than kRescale (base-2 units); then D and
+        // l are rescaled once.  Both threads of a row take the same decisions.
+        float m_ref = -INFINITY, l_run = 0.f;
+        uint32_t ph_qk = 0, ph_pv = 0;
+
+        // prologue: K of the first tile; V of the first tile and K of the second in registers
+        prefetch_k(kt0);
+        prefetch_v(kt0);
+        store_k();
+        if (kt0 + 1 < kt1) prefetch_k(kt0 + 1);
+        operands_ready(kt0 < kt1, false, false);
+
+        for (int kt = kt0; kt < kt1; ++kt) {
+            ok = __syncthreads_and(mbar_wait(smem_u32(&bar_qk), ph_qk));
+            ph_qk ^= 1;
+            if (!ok) break;
+            fence_after_sync();
+
+            // this thread's 32 scores; row max and sum shared with the partner
+            // thread of the same row (tid ^ 128)
+            float s[32];
+            tmem_ld32(tbase + tlane + kColS + 32 * half, s);
+            const int base = kt * kKT + 32 * half;
+            float tmax = -INFINITY;
 #pragma unroll
-            for (int d = 0; d < kHD; d += 4)
-                *reinterpret_cast<float4 *>(orow + d) =
-                    make_float4(o[d] * inv, o[d + 1] * inv, o[d + 2] * inv, o[d + 3] * inv);
+            for (int i = 0; i < 32; ++i) {
+                const bool vis = base + i < kend_row && base + i < kend;
+                s[i] = vis ? s[i] : -INFINITY;
+                tmax = fmaxf(tmax, s[i]);
+            }
+            red[0][tid] = tmax;
+            __syncthreads();
+            const float row_max = fmaxf(tmax, red[0][tid ^ 128]);
+            const bool rescale = m_ref != -INFINITY && row_max > m_ref + kRescale;
+            const float m_use = (m_ref == -INFINITY || rescale) ? row_max : m_ref;
+            float psum = 0.f;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                s[i] = (s[i] == -INFINITY) ? 0.f : exp2f(s[i] - m_use);
+                psum += s[i];
+            }
+            red[1][tid] = psum;
+            __syncthreads();
+            const float rowsum = half ? red[1][tid ^ 128] + psum : psum + red[1][tid ^ 128];
+
+            // PV(kt-1) complete: D is quiescent (rescale it if the reference moved)
+            if (kt > kt0) {
+                ok = __syncthreads_and(mbar_wait(smem_u32(&bar_pv), ph_pv));
+                ph_pv ^= 1;
+                if (!ok) break;
+                fence_after_sync();
+            }
+            // tcgen05.ld / st are warp-collective: the whole warp takes this branch
+            // when any of its rows rescales (the others multiply by 1)
+            if (__any_sync(0xffffffffu, rescale)) {
+                const float f = rescale ? exp2f(m_ref - m_use) : 1.f;
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    float dv[32];
+                    tmem_ld32(tbase + tlane + kColD + 64 * half + 32 * c, dv);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) dv[i] *= f;
+                    tmem_st32(tbase + tlane + kColD + 64 * half + 32 * c, dv);
+                    tmem_st_wait();
+                }
+                l_run *= f;
+            }
+            l_run += rowsum;
+            m_ref = m_use;
+
+            // P_kt -> TMEM (hi, then lo), V_kt -> smem, K_{kt+1} -> smem
+            {
+                float t[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) t[i] = __uint_as_float(__float_as_uint(s[i]) & 0xFFFFE000u);
+                tmem_st32(tbase + tlane + kColPhi + 32 * half, t);
+                tmem_st_wait();
+#pragma unroll
+                for (int i = 0; i < 32; ++i) t[i] = s[i] - __uint_as_float(__float_as_uint(s[i]) & 0xFFFFE000u);
+                tmem_st32(tbase + tlane + kColPlo + 32 * half, t);
+            }
+            store_v();
+            if (kt + 1 < kt1) {
+                store_k();
+                prefetch_v(kt + 1);
+                if (kt + 2 < kt1) prefetch_k(kt + 2);
+            }
+            operands_ready(kt + 1 < kt1, true, kt == kt0);
+        }
+        // the last PV, then the result
+        if (ok) ok = __syncthreads_and(mbar_wait(smem_u32(&bar_pv), ph_pv));
+        if (!ok) {
+            if (tid == 0 && a.err) atomicOr(a.err, 2);
         } else {
-            const int n_split = (kend_tile + a.split_keys - 1) / a.split_keys;
-            const size_t ph = static_cast<size_t>(tile.part0 + tq * n_split + tile.split) * a.n_heads + h;
-            float *prow = a.pacc + ph * kHD;
+            fence_after_sync();
+            const int h = kvh * G + g;
+            const bool direct = tile.part0 < 0;
+            float *dst = nullptr;
+            size_t ph = 0;
+            if (direct) {
+                dst = a.out + static_cast<size_t>(rd.q_row0 + (valid ? qi : 0)) * (a.n_heads * kHD) +
+                      static_cast<size_t>(h) * kHD + 64 * half;
+            } else {
+                const int n_split = (kend_tile + a.split_keys - 1) / a.split_keys;
+                ph = static_cast<size_t>(tile.part0 + (valid ? tq : 0) * n_split + tile.split) * a.n_heads + h;
+                dst = a.pacc + ph * kHD + 64 * half;
+            }
+            const float scl = direct ? 1.f / l_run : 1.f;
 #pragma unroll
-            for (int d = 0; d < kHD; d += 4)
-                *reinterpret_cast<float4 *>(prow + d) = make_float4(o[d], o[d + 1], o[d + 2], o[d + 3]);
-            a.pm[ph] = m_run;
-            a.pl[ph] = l_run;
+            for (int c = 0; c < 2; ++c) {
+                float dv[32];
+                tmem_ld32(tbase + tlane + kColD + 64 * half + 32 * c, dv);
+                if (valid) {
+#pragma unroll
+                    for (int i = 0; i < 32; i += 4)
+                        *reinterpret_cast<float4 *>(dst + 32 * c + i) =
+                            make_float4(dv[i] * scl, dv[i + 1] * scl, dv[i + 2] * scl, dv[i + 3] * scl);
+                }
+            }
+            if (valid && !direct && half == 0) {
+                a.pm[ph] = m_ref;
+                a.pl[ph] = l_run;
+            }
         }
     }
     fence_before_sync();
@@ -336,7 +423,7 @@ cudaError_t launch_prefill_g(const PrefillArgs &a, const Rows &r, cudaStream_t s
     }
     const long long grid = static_cast<long long>(a.n_tiles) * a.n_kv;
     if (grid <= 0 || grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    prefill_tc_kernel<G, Rows><<<static_cast<unsigned>(grid), 128, kSmemBytes, s>>>(a, r);
+    prefill_tc_kernel<G, Rows><<<static_cast<unsigned>(grid), kThreads, kSmemBytes, s>>>(a, r);
     return cudaGetLastError();
 }
 

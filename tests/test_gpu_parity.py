@@ -28,7 +28,7 @@ def split_keys():
 
 
 def run_case(H, KV, hd, bs, past, nq, causal=1, seed=0, n_layers=1, layer=0, shuffle=True,
-             check_m1=True, check_contig=True):
+             check_m1=True, check_contig=True, shape_data=None):
     rng = np.random.default_rng(seed)
     M = len(past)
     kv_dim, q_dim = KV * hd, H * hd
@@ -43,6 +43,8 @@ def run_case(H, KV, hd, bs, past, nq, causal=1, seed=0, n_layers=1, layer=0, shu
             s = pool.new_seq(p + n)
             Kh = rng.standard_normal((p, kv_dim)).astype(np.float32)
             Vh = rng.standard_normal((p, kv_dim)).astype(np.float32)
+            if shape_data is not None:
+                Kh = shape_data("K", Kh, 0)
             if p:
                 pool.grow(s, p)
                 pool.write_history(s, layer, torch.from_numpy(Kh), torch.from_numpy(Vh))
@@ -53,6 +55,12 @@ def run_case(H, KV, hd, bs, past, nq, causal=1, seed=0, n_layers=1, layer=0, shu
         Q = rng.standard_normal((T, q_dim)).astype(np.float32)
         Kn = rng.standard_normal((T, kv_dim)).astype(np.float32)
         Vn = rng.standard_normal((T, kv_dim)).astype(np.float32)
+        if shape_data is not None:
+            Q = shape_data("Q", Q, 0)
+            o = 0
+            for p, n in zip(past, nq):
+                Kn[o:o + n] = shape_data("K", Kn[o:o + n], p)
+                o += n
         Qd, Kd, Vd = (torch.from_numpy(a).cuda() for a in (Q, Kn, Vn))
         pkv.check(pkv.pkv_ensure_append_batch(seqs, nq))
         out = torch.empty(T, q_dim, device="cuda")
@@ -275,3 +283,25 @@ def test_prefill_and_decode_rows_in_one_batch(split_keys):
     chunks (tensor-core kernel); every row equals its M = 1 launch."""
     split_keys(128)
     run_case(32, 8, 128, 16, [3000, 10, 257, 0, 999, 64], [1, 31, 32, 200, 1, 130], seed=23)
+
+
+@pytest.mark.gpu
+def test_prefill_rescales_diverge_within_a_warp(split_keys):
+    """Scores that jump up by ~9.5 (base 2) at position 400 for half of the
+    query heads and down for the other half: the rising rows move their
+    reference max and rescale the TMEM accumulator while their neighbours in
+    the same warp do not."""
+    split_keys(512)
+    H, KV, hd = 32, 8, 128
+
+    def shape(kind, a, start):
+        a = a.copy()
+        if kind == "K":
+            pos = start + np.arange(a.shape[0])
+            step = np.where(pos < 400, -0.3, 0.28).astype(np.float32)[:, None]
+            return (0.1 * a + step).astype(np.float32)
+        q = a.reshape(a.shape[0], H, hd)
+        sign = np.where(np.arange(H) % 2 == 0, 1.0, -1.0).astype(np.float32)[None, :, None]
+        return (0.1 * q + sign).reshape(a.shape).astype(np.float32)
+
+    run_case(H, KV, hd, 16, [900, 300], [64, 40], seed=31, shape_data=shape)
