@@ -256,7 +256,7 @@ PKV_API int pkv_sync_error(pkv_pool *pool);
  * next device call on the pool). */
 PKV_API int pkv_pool_flush(pkv_pool *pool);
 
-/* Keys per split-K work unit of the decode kernels (default 512, a multiple of
+/* Keys per split-K work unit of the decode kernels (default 1024, a multiple of
  * 32 in [32, 65536]).  Process-wide; every call uses the value current at the
  * call, so results stay bit-exact between calls made under one setting. */
 PKV_API int pkv_set_split_keys(int32_t keys);

@@ -46,7 +46,7 @@ int cuda_fail(cudaError_t e, const char *what) {
     return fail(PKV_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
 }
 
-std::atomic<int32_t> g_split_keys{512};
+std::atomic<int32_t> g_split_keys{1024};
 std::atomic<int64_t> g_launches{0};
 
 // Optional per-launch CUDA-event timing.
