@@ -363,7 +363,8 @@ bool can_append(const pkv_seq *s, int32_t n) {
 struct WorkList {
     std::vector<UnitDesc> units;
     std::vector<PrefillTile> tiles;
-    std::vector<MergeDesc> merges;
+    std::vector<MergeDesc> merges;   // queries with several splits (decode first, then prefill)
+    std::vector<MergeDesc> pmerges;  // prefill items while building
     int64_t n_part = 0;
 };
 
@@ -373,6 +374,7 @@ void build_work(const std::vector<RowDesc> &rows, int causal, int32_t S, int32_t
     w.units.clear();
     w.tiles.clear();
     w.merges.clear();
+    w.pmerges.clear();
     w.n_part = 0;
     const bool tc_shape = prefill_shape(head_dim, group);
     const int32_t TQ = tc_shape ? 128 / group : 0;
@@ -391,7 +393,7 @@ void build_work(const std::vector<RowDesc> &rows, int causal, int32_t S, int32_t
                     const int32_t part0 = static_cast<int32_t>(w.n_part);
                     w.n_part += static_cast<int64_t>(nv) * ns;
                     for (int32_t s = 0; s < ns; ++s) w.tiles.push_back({r, q0, s, part0});
-                    for (int32_t t = 0; t < nv; ++t) w.merges.push_back({r, q0 + t, part0 + t * ns, ns});
+                    for (int32_t t = 0; t < nv; ++t) w.pmerges.push_back({r, q0 + t, part0 + t * ns, ns});
                 }
             }
             continue;
@@ -404,14 +406,18 @@ void build_work(const std::vector<RowDesc> &rows, int causal, int32_t S, int32_t
                 tail.push_back({r, i, 0, -1});
             } else {
                 const int32_t part0 = static_cast<int32_t>(w.n_part);
+                const int32_t item = static_cast<int32_t>(w.merges.size());
                 w.n_part += ns;
                 w.merges.push_back({r, i, part0, ns});
-                for (int32_t s = 0; s + 1 < ns; ++s) w.units.push_back({r, i, s, part0 + s});
-                tail.push_back({r, i, ns - 1, part0 + ns - 1});
+                for (int32_t s = 0; s + 1 < ns; ++s) w.units.push_back({r, i, s, item});
+                tail.push_back({r, i, ns - 1, item});
             }
         }
     }
     w.units.insert(w.units.end(), tail.begin(), tail.end());
+    // one merge list: decode items first (units refer to them by index), then prefill items
+    w.merges.insert(w.merges.end(), w.pmerges.begin(), w.pmerges.end());
+    w.pmerges.clear();
 }
 
 int check_heads(int32_t n_heads, int32_t n_kv_heads, int32_t head_dim) {
@@ -504,8 +510,10 @@ int run_layer(pkv_seq *const *seqs, int32_t M, const int32_t *n_q, const float *
     int64_t T = 0;
     for (int32_t r = 0; r < M; ++r) {
         rows[r] = {seqs[r]->slot, seqs[r]->len, n_q[r], static_cast<int32_t>(T)};
-        for (int32_t t = 0; t < n_q[r]; ++t)
-            app.push_back({seqs[r]->slot, seqs[r]->len + t, static_cast<int32_t>(T + t), 0});
+        for (int32_t t = 0; t < n_q[r]; ++t) {
+            const int32_t pos = seqs[r]->len + t;
+            app.push_back({seqs[r]->slot, pos, static_cast<int32_t>(T + t), seqs[r]->pt[pos / p->bs]});
+        }
         T += n_q[r];
     }
     if (T > 0x7fffffffLL / std::max(q_dim, kv_dim)) return fail(PKV_ERR_BAD_DIM, "batch too large");
@@ -547,19 +555,21 @@ int run_layer(pkv_seq *const *seqs, int32_t M, const int32_t *n_q, const float *
         Od = static_cast<float *>(p->io_out.p);
     }
 
-    if (n_runs > 0) {
-        e = launch(PKV_KERNEL_PAGETABLE, st, [&] {
-            return launch_pt_apply(p->pt_dev, p->max_blocks, dptr<PtRun>(p, runs_off), n_runs,
-                                   dptr<int32_t>(p, vals_off), st);
-        });
-        if (e != cudaSuccess) return cuda_fail(e, "page-table upload kernel");
-    }
     const PagedAddr addr = paged_addr(p, layer);
-    e = launch(PKV_KERNEL_APPEND, st, [&] {
-        return launch_append(Kd, Vd, dptr<AppendDesc>(p, app_off), static_cast<int32_t>(T), addr,
-                             (kv_dim % 4) == 0 && aligned16(Kd) && aligned16(Vd), p->err_dev, st);
-    });
-    if (e != cudaSuccess) return cuda_fail(e, "append kernel");
+    PrepArgs pr{};
+    pr.pt = p->pt_dev;
+    pr.max_blocks = p->max_blocks;
+    pr.runs = dptr<PtRun>(p, runs_off);
+    pr.vals = dptr<int32_t>(p, vals_off);
+    pr.n_runs = n_runs;
+    pr.app = dptr<AppendDesc>(p, app_off);
+    pr.n_app = static_cast<int32_t>(T);
+    pr.K_new = Kd;
+    pr.V_new = Vd;
+    pr.vec4 = (kv_dim % 4) == 0 && aligned16(Kd) && aligned16(Vd);
+    pr.err = p->err_dev;
+    e = launch(PKV_KERNEL_APPEND, st, [&] { return launch_prep(pr, addr, st); });
+    if (e != cudaSuccess) return cuda_fail(e, "prep kernel");
     if (!attend) return PKV_OK;
 
     AttnArgs a{};
@@ -567,6 +577,7 @@ int run_layer(pkv_seq *const *seqs, int32_t M, const int32_t *n_q, const float *
     a.out = Od;
     a.rows = dptr<RowDesc>(p, rows_off);
     a.units = dptr<UnitDesc>(p, units_off);
+    a.merges = dptr<MergeDesc>(p, merges_off);
     a.n_units = static_cast<int32_t>(w.units.size());
     a.n_heads = n_heads;
     a.n_kv = n_kv_heads;
@@ -1037,6 +1048,7 @@ int pkv_attn_contiguous(const float *Q, const float *Kc, const float *Vc, int32_
     a.out = out;
     a.rows = reinterpret_cast<const RowDesc *>(base + rows_off);
     a.units = reinterpret_cast<const UnitDesc *>(base + units_off);
+    a.merges = reinterpret_cast<const MergeDesc *>(base + merges_off);
     a.n_units = static_cast<int32_t>(w.units.size());
     a.n_heads = n_heads;
     a.n_kv = n_kv_heads;

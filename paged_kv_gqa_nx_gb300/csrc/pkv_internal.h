@@ -18,10 +18,11 @@ struct RowDesc {
 };
 
 // One split-K work unit: query qi of row `row`, keys [split*S, (split+1)*S)
-// clipped to the visible range.  part >= 0 indexes this unit's partial record
-// (the query has several splits); part < 0 means the unit writes out directly.
+// clipped to the visible range.  item >= 0: the query has several splits and
+// MergeDesc `item` describes them (this unit's partial record is
+// part0 + split); item < 0: the unit writes out directly.
 struct UnitDesc {
-    int32_t row, qi, split, part;
+    int32_t row, qi, split, item;
 };
 
 // One query whose splits are combined by the merge kernel.
@@ -29,10 +30,10 @@ struct MergeDesc {
     int32_t row, qi, part0, n_split;
 };
 
-// One appended token row: position `pos` of sequence page-table row `slot`
-// receives row `src_row` of K_new / V_new.
+// One appended token row: position `pos` (in block `blk` of the host page
+// table) receives row `src_row` of K_new / V_new.
 struct AppendDesc {
-    int32_t slot, pos, src_row, pad;
+    int32_t slot, pos, src_row, blk;
 };
 
 // A run of page-table entries to upload: pt[slot][start .. start+count) =
@@ -67,6 +68,7 @@ struct AttnArgs {
     float *out;
     const RowDesc *rows;
     const UnitDesc *units;
+    const MergeDesc *merges;  // merge items of the units with several splits
     int32_t n_units;
     float *pm, *pl, *pacc;  // partials: [n_part][n_heads], [n_part][n_heads], [n_part][n_heads][hd]
     int32_t n_heads, n_kv, hd, group, causal, split_keys;
@@ -102,7 +104,22 @@ struct MergeArgs {
     int32_t n_items, n_heads, hd;
 };
 
+// One launch before attention: upload page-table runs, append the new rows.
+struct PrepArgs {
+    int32_t *pt;
+    int32_t max_blocks;
+    const PtRun *runs;
+    const int32_t *vals;
+    int32_t n_runs;
+    const AppendDesc *app;
+    int32_t n_app;
+    const float *K_new, *V_new;
+    bool vec4;
+    int32_t *err;
+};
+
 // Kernel launchers (pkv_kernels.cu).  Each enqueues exactly one kernel.
+cudaError_t launch_prep(const PrepArgs &a, const PagedAddr &addr, cudaStream_t s);
 cudaError_t launch_pt_apply(int32_t *pt_dev, int32_t max_blocks, const PtRun *runs, int32_t n_runs,
                             const int32_t *vals, cudaStream_t s);
 // vec4: rows are copied as float4 (kv_dim % 4 == 0 and K_new / V_new 16-byte aligned)

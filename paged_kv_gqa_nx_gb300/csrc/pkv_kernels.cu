@@ -1,8 +1,10 @@
 // pkv_kernels.cu -- sm_103a kernels of libpkv.
 //
-//   pt_apply      upload page-table entries changed on the host
-//   append_rows   scatter each layer's K_new / V_new rows into their blocks
+//   prep          one launch per layer call: upload changed page-table entries
+//                 and scatter the layer's K_new / V_new rows into their blocks
 //                 (the append step of "nx_f32_attn_paged.nx source")
+//   pt_apply      page-table upload alone (pkv_pool_flush)
+//   append_rows   append alone
 //   copy_blocks   copy-on-append: duplicate shared blocks (every layer, K and V)
 //   decode_fast   split-K attention, head_dim 128, query group 1/2/4: one CTA
 //                 per (work unit, kv head); the whole GQA group of query heads
@@ -139,6 +141,46 @@ __global__ void append_rows_kernel(const float *__restrict__ K_new, const float 
         for (int i = lane; i < (a.kv_dim >> 2); i += 32) d4[i] = __ldg(s4 + i);
     } else {
         for (int i = lane; i < a.kv_dim; i += 32) dst[i] = src[i];
+    }
+}
+
+// ------------------------------------------------------------------- prep ----
+//
+// One launch before attention: blocks [0, n_runs) upload page-table runs, the
+// other blocks append the new rows (8 warps per block, one warp per row and K
+// or V; the destination block comes from the host's page table).
+
+__global__ void prep_kernel(PrepArgs p, PagedAddr a) {
+    int b = blockIdx.x;
+    if (b < p.n_runs) {
+        const PtRun r = p.runs[b];
+        int32_t *dst = p.pt + static_cast<size_t>(r.slot) * p.max_blocks + r.start;
+        for (int i = threadIdx.x; i < r.count; i += blockDim.x) dst[i] = p.vals[r.voff + i];
+        return;
+    }
+    b -= p.n_runs;
+    const int app_blocks = (2 * p.n_app + 7) / 8;
+    if (b < app_blocks) {
+        const int gw = b * 8 + (threadIdx.x >> 5);
+        const int lane = threadIdx.x & 31;
+        if (gw >= 2 * p.n_app) return;
+        const AppendDesc d = p.app[gw >> 1];
+        const bool is_v = gw & 1;
+        if (static_cast<unsigned>(d.blk) >= static_cast<unsigned>(a.n_blocks)) {
+            if (lane == 0) flag_error(p.err, 1);
+            return;
+        }
+        const int off = a.bs_shift >= 0 ? (d.pos & (a.bs - 1)) : (d.pos % a.bs);
+        float *dst = (is_v ? a.v : a.k) + static_cast<size_t>(d.blk) * a.block_stride + a.layer_off +
+                     static_cast<size_t>(off) * a.kv_dim;
+        const float *src = (is_v ? p.V_new : p.K_new) + static_cast<size_t>(d.src_row) * a.kv_dim;
+        if (p.vec4) {
+            const float4 *s4 = reinterpret_cast<const float4 *>(src);
+            float4 *d4 = reinterpret_cast<float4 *>(dst);
+            for (int i = lane; i < (a.kv_dim >> 2); i += 32) d4[i] = __ldg(s4 + i);
+        } else {
+            for (int i = lane; i < a.kv_dim; i += 32) dst[i] = src[i];
+        }
     }
 }
 
@@ -438,11 +480,11 @@ __global__ void __launch_bounds__(128, 3) decode_fast_kernel(AttnArgs a, Rows ro
             }
         }
         const int h = kvh * G + g;
-        if (u.part < 0) {
+        if (u.item < 0) {
             a.out[static_cast<size_t>(rd.q_row0 + u.qi) * (a.n_heads * HD) +
                   static_cast<size_t>(h) * HD + d] = num / den;
         } else {
-            const size_t ph = static_cast<size_t>(u.part) * a.n_heads + h;
+            const size_t ph = static_cast<size_t>(a.merges[u.item].part0 + u.split) * a.n_heads + h;
             a.pacc[ph * HD + d] = num;
             if (d == 0) {
                 a.pm[ph] = M;
@@ -544,11 +586,11 @@ __global__ void __launch_bounds__(128) decode_generic_kernel(AttnArgs a, Rows ro
             }
         }
         const int h = h0 + g;
-        if (u.part < 0) {
+        if (u.item < 0) {
             a.out[static_cast<size_t>(rd.q_row0 + u.qi) * (a.n_heads * hd) +
                   static_cast<size_t>(h) * hd + d] = num / den;
         } else {
-            const size_t ph = static_cast<size_t>(u.part) * a.n_heads + h;
+            const size_t ph = static_cast<size_t>(a.merges[u.item].part0 + u.split) * a.n_heads + h;
             a.pacc[ph * hd + d] = num;
             if (d == 0) {
                 a.pm[ph] = M;
@@ -648,6 +690,15 @@ cudaError_t launch_pt_apply(int32_t *pt_dev, int32_t max_blocks, const PtRun *ru
                             const int32_t *vals, cudaStream_t s) {
     if (n_runs <= 0) return cudaSuccess;
     pt_apply_kernel<<<n_runs, 128, 0, s>>>(pt_dev, max_blocks, runs, vals);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_prep(const PrepArgs &p, const PagedAddr &addr, cudaStream_t s) {
+    const long long app_blocks = (2LL * p.n_app + 7) / 8;
+    const long long grid = p.n_runs + app_blocks;
+    if (grid <= 0) return cudaSuccess;
+    if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    prep_kernel<<<static_cast<unsigned>(grid), 256, 0, s>>>(p, addr);
     return cudaGetLastError();
 }
 

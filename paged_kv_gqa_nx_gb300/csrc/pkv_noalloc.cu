@@ -87,7 +87,8 @@ extern "C" int pkv_attn_contiguous_noalloc(const float *Q, const float *Kc, cons
           reinterpret_cast<uintptr_t>(Vc) | reinterpret_cast<uintptr_t>(out)) & mask) != 0)
         return err_arg(PKV_ERR_ARG, "device pointers must be 16-byte aligned (4-byte if head_dim % 4 != 0)");
 
-    // work list and the scratch layout: [error word][rows][units][merges][partials]
+    // work list and the scratch layout:
+    // [error word][rows][units][tiles][merges][partials]
     const int32_t S = current_split_keys();
     std::vector<UnitDesc> units;
     std::vector<PrefillTile> tiles;
@@ -101,8 +102,9 @@ extern "C" int pkv_attn_contiguous_noalloc(const float *Q, const float *Kc, cons
     const size_t tiles_off = round256(units_off + units.size() * sizeof(UnitDesc));
     const size_t merges_off = round256(tiles_off + tiles.size() * sizeof(PrefillTile));
     const size_t desc_end = round256(merges_off + merges.size() * sizeof(MergeDesc));
+    const size_t part_off = desc_end;
     const size_t pf = static_cast<size_t>(n_part) * n_heads;
-    const size_t total = desc_end + pf * (2 + static_cast<size_t>(head_dim)) * sizeof(float);
+    const size_t total = part_off + pf * (2 + static_cast<size_t>(head_dim)) * sizeof(float);
     if (total > kScratchBytes) {
         char msg[256];
         snprintf(msg, sizeof msg,
@@ -143,6 +145,7 @@ extern "C" int pkv_attn_contiguous_noalloc(const float *Q, const float *Kc, cons
         std::memcpy(blob.data() + (tiles_off - rows_off), tiles.data(), tiles.size() * sizeof(PrefillTile));
     if (!merges.empty())
         std::memcpy(blob.data() + (merges_off - rows_off), merges.data(), merges.size() * sizeof(MergeDesc));
+    // the error word must start at zero
     e = cudaMemsetAsync(base, 0, sizeof(int32_t), st);
     if (e == cudaSuccess)
         e = cudaMemcpyAsync(base + rows_off, blob.data(), blob.size(), cudaMemcpyHostToDevice, st);
@@ -153,6 +156,7 @@ extern "C" int pkv_attn_contiguous_noalloc(const float *Q, const float *Kc, cons
     a.out = out;
     a.rows = reinterpret_cast<const RowDesc *>(base + rows_off);
     a.units = reinterpret_cast<const UnitDesc *>(base + units_off);
+    a.merges = reinterpret_cast<const MergeDesc *>(base + merges_off);
     a.n_units = static_cast<int32_t>(units.size());
     a.n_heads = n_heads;
     a.n_kv = n_kv_heads;
@@ -163,7 +167,7 @@ extern "C" int pkv_attn_contiguous_noalloc(const float *Q, const float *Kc, cons
     a.scale_log2 = scale * 1.4426950408889634f;
     a.err = reinterpret_cast<int32_t *>(base);
     if (pf > 0) {
-        a.pm = reinterpret_cast<float *>(base + desc_end);
+        a.pm = reinterpret_cast<float *>(base + part_off);
         a.pl = a.pm + pf;
         a.pacc = a.pl + pf;
     }
