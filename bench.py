@@ -331,9 +331,9 @@ def dist_setup(n_gpus):
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local = int(os.environ.get("LOCAL_RANK", str(rank)))
-    if torch.cuda.is_available():
+    backend = os.environ.get("PKV_DIST_BACKEND") or ("nccl" if torch.cuda.is_available() else "gloo")
+    if backend == "nccl":
         torch.cuda.set_device(local)
-    backend = "nccl" if torch.cuda.is_available() else "gloo"
     dist.init_process_group(backend=backend)
     return rank, world, dist
 
@@ -342,7 +342,8 @@ def max_over_ranks(value, dist):
     if dist is None:
         return value
     import torch
-    dev = torch.device("cuda", torch.cuda.current_device()) if torch.cuda.is_available() else "cpu"
+    dev = (torch.device("cuda", torch.cuda.current_device()) if dist.get_backend() == "nccl"
+           else torch.device("cpu"))
     t = torch.tensor([float(value)], device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
