@@ -7,19 +7,20 @@
 // formed as hi*hi + hi*lo + lo*hi; the dropped lo*lo term is ~2^-20 relative.
 //
 // One CTA = one tile of 128 query rows -- (128 / G) consecutive tokens x the G
-// query heads that share kv head `kvh` -- and one key split; 256 threads.
-// Row m of the tile is token m / G, head m % G and TMEM lane m; the two
-// threads that share TMEM lane m (warps w and w + 4) each own 32 of a key
-// tile's scores and half of the row's output columns, and exchange the row
-// max and sum through shared memory.  Two threads issue the MMAs (QK and PV
-// concurrently, each committing to its own mbarrier).  Key tiles are 64
-// positions:
+// query heads that share kv head `kvh` -- and one key split.  16 compute
+// warps and one MMA-issue warp.  Row m of the tile is token m / G, head m % G
+// and TMEM lane m; the four compute threads that share TMEM lane m (warps w,
+// w + 4, w + 8, w + 12) each own 16 of a key tile's scores and 32 of the row's
+// output columns, and combine the row max and sum through shared memory.  The
+// compute warps arrive on an mbarrier when the operands of QK or PV are in
+// place; the issue warp waits on it, issues, and commits to the mbarrier the
+// compute warps wait on.  Key tiles are 64 positions:
 //   QK(j):  S[128 x 64]  = Q.K_j^T     A = Q hi (TMEM) / Q lo (smem), B = K_j (smem)
 //   PV(j):  D[128 x 128] = P_j.V_j     A = P hi/lo (TMEM),            B = V_j^T (smem)
-// Loop j: wait S_j -> online softmax (offset-causal mask: key p visible iff
-// p <= q_pos = total_k - n_q + i) -> wait PV(j-1) -> write P_j, V_j, K_{j+1}
-// -> QK(j+1) and PV(j) are issued, PV adding into the TMEM
-// accumulator D; the softmax of tile j+1 runs while PV(j) executes.  p is
+// Loop j: wait S_j -> write K_{j+1} (QK(j+1) starts) -> online softmax
+// (offset-causal mask: key p visible iff p <= q_pos = total_k - n_q + i) ->
+// wait PV(j-1) -> write P_j, V_j (PV(j) starts, adding into the TMEM
+// accumulator D); QK(j+1) runs during the softmax of tile j.  p is
 // relative to a reference max that moves (and D is rescaled) only when a
 // tile's max exceeds it by more than 2^8, which keeps every p below 256.
 // K/V rows for the next tiles are loaded into registers while the MMAs run.
@@ -42,46 +43,83 @@ constexpr int kHD = 128;
 constexpr int kKT = 64;  // keys per tile
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColQhi = 0, kColS = 128, kColPhi = 256, kColPlo = 320, kColD = 384;
-constexpr int kThreads = 256;                 // two threads per tile row
+#ifndef PKV_PREFILL_COMPUTE_WARPS
+#define PKV_PREFILL_COMPUTE_WARPS 16
+#endif
+constexpr int kComputeWarps = PKV_PREFILL_COMPUTE_WARPS;  // 8: two threads per tile row, 16: four
+constexpr int kCompute = 32 * kComputeWarps;
+constexpr int kThreads = kCompute + 32;                     // + the MMA-issue warp
+constexpr int kTPR = kComputeWarps / 4;                     // threads per tile row
+constexpr int kSCols = kKT / kTPR;                          // scores per thread per key tile
+constexpr int kDCols = kHD / kTPR;                          // output columns per thread
+constexpr int kKPW = kKT / kComputeWarps;                   // K rows per warp per key tile
+constexpr int kVF = 32 / (kComputeWarps / 2);               // V float4 per thread per key tile
+static_assert(kComputeWarps == 8 || kComputeWarps == 16, "8 or 16 compute warps");
 constexpr float kRescale = 8.f;               // lazy-rescale threshold (base 2)
 
 struct PagedRowsP {
     PagedAddr a;
-    __device__ __forceinline__ bool row(int slot, int pos, int kvh, const float *&kr,
-                                        const float *&vr, int32_t *err) const {
+    // Block id of (slot, pos), or -1 (and the error flag) when the page index
+    // or the id is out of range.
+    __device__ __forceinline__ int block(int slot, int pos, int32_t *err) const {
         const int bi = a.bs_shift >= 0 ? (pos >> a.bs_shift) : (pos / a.bs);
-        const int off = pos - bi * a.bs;
         if (bi >= a.max_blocks) {
             if (err) atomicOr(err, 1);
-            return false;
+            return -1;
         }
         const int blk = __ldg(a.pt + static_cast<size_t>(slot) * a.max_blocks + bi);
         if (static_cast<unsigned>(blk) >= static_cast<unsigned>(a.n_blocks)) {
             if (err) atomicOr(err, 1);
-            return false;
+            return -1;
         }
-        const size_t o = static_cast<size_t>(blk) * a.block_stride + a.layer_off +
-                         static_cast<size_t>(off) * a.kv_dim + static_cast<size_t>(kvh) * kHD;
-        kr = a.k + o;
-        vr = a.v + o;
-        return true;
+        return blk;
     }
-    // groups of 8 positions starting at a multiple of 8 lie in one block
-    __device__ __forceinline__ bool whole8() const { return (a.bs & 7) == 0; }
-    __device__ __forceinline__ size_t row_stride() const { return static_cast<size_t>(a.kv_dim); }
+    // The page-table entry of (slot, pos) without waiting for it: -1 when the
+    // page index is out of range (error flag set), else the raw entry, which
+    // checked() validates where it is used, a tile later, so the lookup's
+    // latency stays off the critical path.
+    __device__ __forceinline__ int entry(int slot, int pos, int32_t *err) const {
+        const int bi = a.bs_shift >= 0 ? (pos >> a.bs_shift) : (pos / a.bs);
+        if (bi >= a.max_blocks) {
+            if (err) atomicOr(err, 1);
+            return -1;
+        }
+        return __ldg(a.pt + static_cast<size_t>(slot) * a.max_blocks + bi);
+    }
+    __device__ __forceinline__ int checked(int blk, int32_t *err) const {
+        if (static_cast<unsigned>(blk) >= static_cast<unsigned>(a.n_blocks)) {
+            if (err) atomicOr(err, 1);
+            return -1;
+        }
+        return blk;
+    }
+    __device__ __forceinline__ size_t offset(int blk, int pos, int kvh) const {
+        const int off = a.bs_shift >= 0 ? (pos & (a.bs - 1)) : (pos % a.bs);
+        return static_cast<size_t>(blk) * a.block_stride + a.layer_off +
+               static_cast<size_t>(off) * a.kv_dim + static_cast<size_t>(kvh) * kHD;
+    }
+    __device__ __forceinline__ const float *k_row(int blk, int pos, int kvh) const {
+        return a.k + offset(blk, pos, kvh);
+    }
+    __device__ __forceinline__ const float *v_row(int blk, int pos, int kvh) const {
+        return a.v + offset(blk, pos, kvh);
+    }
+    // groups of n positions starting at a multiple of n lie in one block
+    __device__ __forceinline__ bool whole(int n) const { return (a.bs % n) == 0; }
 };
 
 struct ContigRowsP {
     ContigAddr a;
-    __device__ __forceinline__ bool row(int, int pos, int kvh, const float *&kr, const float *&vr,
-                                        int32_t *) const {
-        const size_t o = static_cast<size_t>(pos) * a.kv_dim + static_cast<size_t>(kvh) * kHD;
-        kr = a.k + o;
-        vr = a.v + o;
-        return true;
+    __device__ __forceinline__ int block(int, int, int32_t *) const { return 0; }
+    __device__ __forceinline__ int entry(int, int, int32_t *) const { return 0; }
+    __device__ __forceinline__ int checked(int blk, int32_t *) const { return blk; }
+    __device__ __forceinline__ const float *k_row(int, int pos, int kvh) const {
+        return a.k + static_cast<size_t>(pos) * a.kv_dim + static_cast<size_t>(kvh) * kHD;
     }
-    __device__ __forceinline__ bool whole8() const { return true; }
-    __device__ __forceinline__ size_t row_stride() const { return static_cast<size_t>(a.kv_dim); }
+    __device__ __forceinline__ const float *v_row(int, int pos, int kvh) const {
+        return a.v + static_cast<size_t>(pos) * a.kv_dim + static_cast<size_t>(kvh) * kHD;
+    }
+    __device__ __forceinline__ bool whole(int) const { return true; }
 };
 
 constexpr uint32_t kSmemQlo = 64 * 1024;  // 4 k-blocks of 128 rows
@@ -107,25 +145,19 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs a, 
     unsigned char *Klo = Khi + kSmemK;
     unsigned char *Vhi = Klo + kSmemK;
     unsigned char *Vlo = Vhi + kSmemV;
-    __shared__ uint64_t bar_qk, bar_pv;
+    // bar_qk / bar_pv: the MMAs of QK / PV completed (tcgen05.commit);
+    // bar_k / bar_p: the compute warps put the operands of QK / PV in place
+    __shared__ uint64_t bar_qk, bar_pv, bar_k, bar_p;
     __shared__ uint32_t tslot;
-    __shared__ float red[2][kThreads];
+    __shared__ float red[2][kCompute];
+    static_assert(kSCols == 16 || kSCols == 32, "");
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int wq = warp & 3, half = (warp >> 2) & 1;  // TMEM lane quadrant, key / column half
-    const int m = 32 * wq + lane;                      // this thread's row of the tile
     const int ti = blockIdx.x / a.n_kv;
     const int kvh = blockIdx.x - ti * a.n_kv;
     const PrefillTile tile = a.tiles[ti];
     const RowDesc rd = a.rows[tile.row];
     const int total_k = rd.past_len + rd.n_q;
-
-    const int tq = m / G, g = m - (m / G) * G;
-    const int qi = tile.q0 + tq;
-    const bool valid = qi < rd.n_q;
-    const int q_pos = total_k - rd.n_q + qi;
-    const int kend_row = valid ? (a.causal ? min(q_pos + 1, total_k) : total_k) : 1;
-
     const int n_valid_q = min(TQ, rd.n_q - tile.q0);
     const int kend_tile =
         a.causal ? min(total_k, total_k - rd.n_q + tile.q0 + n_valid_q) : total_k;
@@ -140,6 +172,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs a, 
     if (tid == 0) {
         mbar_init(smem_u32(&bar_qk), 1);
         mbar_init(smem_u32(&bar_pv), 1);
+        mbar_init(smem_u32(&bar_k), kComputeWarps);
+        mbar_init(smem_u32(&bar_p), kComputeWarps);
     }
     fence_before_sync();
     __syncthreads();
@@ -147,20 +181,84 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs a, 
     const uint32_t tbase = tslot;
     bool ok = true;
 
-    {
-        // ---- compute warps ----
+    if (warp == kComputeWarps) {
+        // ---------------- MMA issue warp (lane 0 issues) ----------------
+        const uint64_t dKhi = desc_sw128(smem_u32(Khi)), dKlo = desc_sw128(smem_u32(Klo));
+        const uint64_t dQlo = desc_sw128(smem_u32(Qlo));
+        const uint64_t dVhi = desc_sw128(smem_u32(Vhi)), dVlo = desc_sw128(smem_u32(Vlo));
+        const uint32_t tS = tbase + kColS, tQ = tbase + kColQhi, tD = tbase + kColD;
+        const uint32_t tPh = tbase + kColPhi, tPl = tbase + kColPlo;
+        const uint32_t idesc_s = idesc_tf32(128, kKT), idesc_o = idesc_tf32(128, kHD);
+        uint32_t ph_k = 0, ph_p = 0;
+        auto issue_qk = [&]() {
+            // operands: K of the tile (and, the first time, Q) in place
+            ok = mbar_wait(smem_u32(&bar_k), ph_k);
+            ph_k ^= 1;
+            if (!ok) return;
+            fence_after_sync();
+            if (lane == 0) {
+#pragma unroll
+                for (int s = 0; s < 16; ++s) {
+                    const uint64_t ko = ((s >> 2) * 8192u + (s & 3) * 32u) >> 4;
+                    const uint64_t qo = ((s >> 2) * 16384u + (s & 3) * 32u) >> 4;
+                    mma_tf32_ts(tS, tQ + 8 * s, dKhi + ko, idesc_s, s > 0);
+                    mma_tf32_ts(tS, tQ + 8 * s, dKlo + ko, idesc_s, 1);
+                    mma_tf32(tS, dQlo + qo, dKhi + ko, idesc_s, 1);
+                }
+                mma_commit(smem_u32(&bar_qk));
+            }
+            __syncwarp();
+        };
+        auto issue_pv = [&](bool first) {
+            // operands: P and V of the tile in place
+            ok = mbar_wait(smem_u32(&bar_p), ph_p);
+            ph_p ^= 1;
+            if (!ok) return;
+            fence_after_sync();
+            if (lane == 0) {
+#pragma unroll
+                for (int s = 0; s < 8; ++s) {
+                    const uint64_t vo = ((s >> 2) * 16384u + (s & 3) * 32u) >> 4;
+                    mma_tf32_ts(tD, tPh + 8 * s, dVhi + vo, idesc_o, !first || s > 0);
+                    mma_tf32_ts(tD, tPh + 8 * s, dVlo + vo, idesc_o, 1);
+                    mma_tf32_ts(tD, tPl + 8 * s, dVhi + vo, idesc_o, 1);
+                }
+                mma_commit(smem_u32(&bar_pv));
+            }
+            __syncwarp();
+        };
+        // order on the tensor core: QK(kt0), then per tile QK(kt+1) before PV(kt),
+        // so QK(kt+1) runs while the compute warps do the softmax of tile kt
+        if (kt0 < kt1) issue_qk();
+        for (int kt = kt0; kt < kt1 && ok; ++kt) {
+            if (kt + 1 < kt1) issue_qk();
+            if (ok) issue_pv(kt == kt0);
+        }
+        if (!ok && lane == 0 && a.err) atomicOr(a.err, 2);
+    } else {
+        // ---------------- compute warps: 4 threads per tile row ----------------
+        const int wq = warp & 3;               // TMEM lane quadrant
+        const int qp = warp >> 2;              // which quarter of the row this thread owns
+        const int m = 32 * wq + lane;          // this thread's row of the tile
+        const int tq = m / G, g = m - (m / G) * G;
+        const int qi = tile.q0 + tq;
+        const bool valid = qi < rd.n_q;
+        const int q_pos = total_k - rd.n_q + qi;
+        const int kend_row = valid ? (a.causal ? min(q_pos + 1, total_k) : total_k) : 1;
         const uint32_t tlane = static_cast<uint32_t>(32 * wq) << 16;
-        // Q row (pre-scaled to base-2 units): hi -> TMEM, lo -> smem (A operands)
+
+        // Q row (pre-scaled to base-2 units): this thread's kDCols dims, hi -> TMEM,
+        // lo -> shared memory (one k-block per 32 dims)
         {
             const float *qrow = a.Q + static_cast<size_t>(rd.q_row0 + (valid ? qi : 0)) * (a.n_heads * kHD) +
-                                static_cast<size_t>(kvh * G + g) * kHD + 64 * half;
+                                static_cast<size_t>(kvh * G + g) * kHD + kDCols * qp;
 #pragma unroll
-            for (int c = 0; c < 2; ++c) {
+            for (int c = 0; c < kDCols / 32; ++c) {
                 float hv[32];
 #pragma unroll
                 for (int j4 = 0; j4 < 8; ++j4) {
-                    float4 x = valid ? __ldg(reinterpret_cast<const float4 *>(qrow + 32 * c) + j4)
-                                     : make_float4(0.f, 0.f, 0.f, 0.f);
+                    float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+                    if (valid) x = __ldg(reinterpret_cast<const float4 *>(qrow + 32 * c) + j4);
                     x.x *= a.scale_log2;
                     x.y *= a.scale_log2;
                     x.z *= a.scale_log2;
@@ -171,164 +269,162 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs a, 
                     hv[4 * j4 + 1] = h.y;
                     hv[4 * j4 + 2] = h.z;
                     hv[4 * j4 + 3] = h.w;
-                    const uint32_t off = (2 * half + c) * 16384u + sw128_chunk(m, j4);
-                    *reinterpret_cast<float4 *>(Qlo + off) = l;
+                    const uint32_t kb = static_cast<uint32_t>(kDCols / 32 * qp + c);
+                    *reinterpret_cast<float4 *>(Qlo + kb * 16384u + sw128_chunk(m, j4)) = l;
                 }
-                tmem_st32(tbase + tlane + kColQhi + 64 * half + 32 * c, hv);
+                tmem_st32(tbase + tlane + kColQhi + kDCols * qp + 32 * c, hv);
             }
         }
 
-        // K rows key-major (8 keys per warp, one 512-byte row per instruction;
-        // one page-table lookup per warp when a block holds whole 8-key groups),
-        // V rows key-per-lane for the transposed store
-        float4 kreg[8], vreg[8];
-        const bool k_whole = rows_of.whole8();
-        const size_t rstride = rows_of.row_stride();
-        auto prefetch_k = [&](int kt) {
-            const int pos0 = kt * kKT + warp * 8;
-            if (k_whole) {
-                const float *kr, *vr;
-                const bool have = pos0 < kend && rows_of.row(rd.slot, pos0, kvh, kr, vr, a.err);
+        // Key rows of a tile: warp w owns keys kKPW*w .. kKPW*w + kKPW-1 for K (one
+        // 512-byte row per instruction; one page-table lookup per warp when a
+        // block holds whole kKPW-key groups) and key 32*(w & 1) + lane, float4
+        // columns (w >> 1) + (kComputeWarps/2) i, for V (the transposed store).
+        // Page-table lookups are issued one phase before the loads that use them.
+        float4 kreg[kKPW], vreg[kVF];
+        const bool k_whole = rows_of.whole(kKPW);
+        auto k_pos = [&](int kt) { return kt * kKT + warp * kKPW; };
+        auto v_pos = [&](int kt) { return kt * kKT + 32 * (warp & 1) + lane; };
+        auto load_k = [&](int kt, int blk0) {
+            const int pos0 = k_pos(kt);
+            if (k_whole && pos0 < kend) blk0 = rows_of.checked(blk0, a.err);
 #pragma unroll
-                for (int i = 0; i < 8; ++i)
-                    kreg[i] = (have && pos0 + i < kend)
-                                  ? __ldg(reinterpret_cast<const float4 *>(kr + i * rstride) + lane)
-                                  : make_float4(0.f, 0.f, 0.f, 0.f);
-            } else {
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const float *kr, *vr;
-                    const bool have = pos0 + i < kend && rows_of.row(rd.slot, pos0 + i, kvh, kr, vr, a.err);
-                    kreg[i] = have ? __ldg(reinterpret_cast<const float4 *>(kr) + lane)
-                                   : make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int i = 0; i < kKPW; ++i) {
+                kreg[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+                const int pos = pos0 + i;
+                if (pos < kend) {
+                    const float *kr = nullptr;
+                    if (k_whole) {
+                        if (blk0 >= 0) kr = rows_of.k_row(blk0, pos, kvh);
+                    } else {
+                        const int b = rows_of.block(rd.slot, pos, a.err);
+                        kr = b >= 0 ? rows_of.k_row(b, pos, kvh) : nullptr;
+                    }
+                    if (kr) kreg[i] = __ldg(reinterpret_cast<const float4 *>(kr) + lane);
                 }
             }
         };
-        auto prefetch_v = [&](int kt) {
-            const int pos = kt * kKT + 32 * half + lane;
-            const float *kr, *vr;
-            const bool have = pos < kend && rows_of.row(rd.slot, pos, kvh, kr, vr, a.err);
+        auto load_v = [&](int kt, int vblk) {
+            const int pos = v_pos(kt);
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-                vreg[i] = have ? __ldg(reinterpret_cast<const float4 *>(vr) + wq + 4 * i)
-                               : make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int i = 0; i < kVF; ++i) vreg[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (pos < kend) vblk = rows_of.checked(vblk, a.err);
+            if (pos < kend && vblk >= 0) {
+                const float *vr = rows_of.v_row(vblk, pos, kvh);
+#pragma unroll
+                for (int i = 0; i < kVF; ++i)
+                    vreg[i] = __ldg(reinterpret_cast<const float4 *>(vr) + (warp >> 1) + (kComputeWarps / 2) * i);
+            }
+        };
+        auto lookup_k = [&](int kt) {
+            const int pos0 = k_pos(kt);
+            return (k_whole && pos0 < kend) ? rows_of.entry(rd.slot, pos0, a.err) : -1;
+        };
+        auto lookup_v = [&](int kt) {
+            const int pos = v_pos(kt);
+            return pos < kend ? rows_of.entry(rd.slot, pos, a.err) : -1;
         };
         auto store_k = [&]() {
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
+            for (int i = 0; i < kKPW; ++i) {
                 float4 h, l;
                 split4(kreg[i], h, l);
-                const uint32_t off = (lane >> 3) * 8192u + sw128_chunk(warp * 8 + i, lane & 7);
+                const uint32_t off = (lane >> 3) * 8192u + sw128_chunk(warp * kKPW + i, lane & 7);
                 *reinterpret_cast<float4 *>(Khi + off) = h;
                 *reinterpret_cast<float4 *>(Klo + off) = l;
             }
         };
         auto store_v = [&]() {
+            const uint32_t kb = static_cast<uint32_t>(warp & 1) * 16384u;
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const int d0 = 4 * (wq + 4 * i);
+            for (int i = 0; i < kVF; ++i) {
+                const int d0 = 4 * ((warp >> 1) + (kComputeWarps / 2) * i);
                 const float v4[4] = {vreg[i].x, vreg[i].y, vreg[i].z, vreg[i].w};
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     float h, l;
                     split_tf32(v4[e], h, l);
-                    const uint32_t off = half * 16384u + sw128_offset(d0 + e, lane);
+                    const uint32_t off = kb + sw128_offset(d0 + e, lane);
                     *reinterpret_cast<float *>(Vhi + off) = h;
                     *reinterpret_cast<float *>(Vlo + off) = l;
                 }
             }
         };
-        // MMA issue: after the operand barrier, lane 0 of warp 0 issues QK (and
-        // commits it to bar_qk) while lane 0 of warp 4 issues PV (bar_pv); each
-        // commit tracks only its own thread's MMAs.
-        const uint64_t dKhi = desc_sw128(smem_u32(Khi)), dKlo = desc_sw128(smem_u32(Klo));
-        const uint64_t dQlo = desc_sw128(smem_u32(Qlo));
-        const uint64_t dVhi = desc_sw128(smem_u32(Vhi)), dVlo = desc_sw128(smem_u32(Vlo));
-        auto issue_qk = [&]() {
-            const uint32_t tS = tbase + kColS, tQ = tbase + kColQhi;
-            const uint32_t idesc_s = idesc_tf32(128, kKT);
-#pragma unroll
-            for (int s = 0; s < 16; ++s) {
-                const uint64_t ko = ((s >> 2) * 8192u + (s & 3) * 32u) >> 4;
-                const uint64_t qo = ((s >> 2) * 16384u + (s & 3) * 32u) >> 4;
-                mma_tf32_ts(tS, tQ + 8 * s, dKhi + ko, idesc_s, s > 0);
-                mma_tf32_ts(tS, tQ + 8 * s, dKlo + ko, idesc_s, 1);
-                mma_tf32(tS, dQlo + qo, dKhi + ko, idesc_s, 1);
-            }
-            mma_commit(smem_u32(&bar_qk));
-        };
-        auto issue_pv = [&](bool first) {
-            const uint32_t tD = tbase + kColD, tPh = tbase + kColPhi, tPl = tbase + kColPlo;
-            const uint32_t idesc_o = idesc_tf32(128, kHD);
-#pragma unroll
-            for (int s = 0; s < 8; ++s) {
-                const uint64_t vo = ((s >> 2) * 16384u + (s & 3) * 32u) >> 4;
-                mma_tf32_ts(tD, tPh + 8 * s, dVhi + vo, idesc_o, !first || s > 0);
-                mma_tf32_ts(tD, tPh + 8 * s, dVlo + vo, idesc_o, 1);
-                mma_tf32_ts(tD, tPl + 8 * s, dVhi + vo, idesc_o, 1);
-            }
-            mma_commit(smem_u32(&bar_pv));
-        };
-        auto operands_ready = [&](bool qk, bool pv, bool pv_first) {
+        // operands written: make them visible to the tensor core, then one lane
+        // per warp arrives on the barrier the issue warp waits on
+        auto arrive = [&](uint64_t *bar) {
             tmem_st_wait();
             fence_proxy_async();
             fence_before_sync();
-            __syncthreads();
-            fence_after_sync();
-            if (qk && tid == 0) issue_qk();
-            if (pv && tid == 128) issue_pv(pv_first);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(bar));
         };
 
         // The output accumulator lives in TMEM (D) and the P.V MMAs add into it.
         // p is taken relative to a reference max m_ref that moves only when a
         // tile's max exceeds it by more than kRescale (base-2 units); then D and
-        // l are rescaled once.  Both threads of a row take the same decisions.
+        // l are rescaled once.  The four threads of a row take the same decisions.
         float m_ref = -INFINITY, l_run = 0.f;
         uint32_t ph_qk = 0, ph_pv = 0;
 
-        // prologue: K of the first tile; V of the first tile and K of the second in registers
-        prefetch_k(kt0);
-        prefetch_v(kt0);
+        // prologue: K_kt0 in place (QK(kt0) may start), V_kt0 and K_kt0+1 in registers
+        load_k(kt0, lookup_k(kt0));
+        int vblk = lookup_v(kt0);
+        load_v(kt0, vblk);
         store_k();
-        if (kt0 + 1 < kt1) prefetch_k(kt0 + 1);
-        operands_ready(kt0 < kt1, false, false);
+        int kblk = kt0 + 1 < kt1 ? lookup_k(kt0 + 1) : -1;
+        arrive(&bar_k);
+        if (kt0 + 1 < kt1) load_k(kt0 + 1, kblk);
+        vblk = kt0 + 1 < kt1 ? lookup_v(kt0 + 1) : -1;
 
         for (int kt = kt0; kt < kt1; ++kt) {
-            ok = __syncthreads_and(mbar_wait(smem_u32(&bar_qk), ph_qk));
+            // S_kt ready (QK(kt) done: the K buffer is free again)
+            ok = named_sync_and(1, kCompute, mbar_wait(smem_u32(&bar_qk), ph_qk));
             ph_qk ^= 1;
             if (!ok) break;
             fence_after_sync();
+            float s[kSCols];
+            tmem_ldn<kSCols>(tbase + tlane + kColS + kSCols * qp, s);
+            // K_{kt+1} -> smem; the issue warp starts QK(kt+1) while we do the softmax
+            if (kt + 1 < kt1) {
+                store_k();
+                kblk = kt + 2 < kt1 ? lookup_k(kt + 2) : -1;
+                arrive(&bar_k);
+            }
 
-            // this thread's 32 scores; row max and sum shared with the partner
-            // thread of the same row (tid ^ 128)
-            float s[32];
-            tmem_ld32(tbase + tlane + kColS + 32 * half, s);
-            const int base = kt * kKT + 32 * half;
+            // online softmax: this thread's kSCols scores; max and sum combined over
+            // the row's threads (tid + 128 k), in order of k
+            const int base = kt * kKT + kSCols * qp;
             float tmax = -INFINITY;
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
+            for (int i = 0; i < kSCols; ++i) {
                 const bool vis = base + i < kend_row && base + i < kend;
                 s[i] = vis ? s[i] : -INFINITY;
                 tmax = fmaxf(tmax, s[i]);
             }
             red[0][tid] = tmax;
-            __syncthreads();
-            const float row_max = fmaxf(tmax, red[0][tid ^ 128]);
+            named_sync(1, kCompute);
+            const int r0 = tid & 127;
+            float row_max = red[0][r0];
+#pragma unroll
+            for (int k = 1; k < kTPR; ++k) row_max = fmaxf(row_max, red[0][r0 + 128 * k]);
             const bool rescale = m_ref != -INFINITY && row_max > m_ref + kRescale;
             const float m_use = (m_ref == -INFINITY || rescale) ? row_max : m_ref;
             float psum = 0.f;
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
+            for (int i = 0; i < kSCols; ++i) {
                 s[i] = (s[i] == -INFINITY) ? 0.f : exp2f(s[i] - m_use);
                 psum += s[i];
             }
             red[1][tid] = psum;
-            __syncthreads();
-            const float rowsum = half ? red[1][tid ^ 128] + psum : psum + red[1][tid ^ 128];
+            named_sync(1, kCompute);
+            float rowsum = red[1][r0];
+#pragma unroll
+            for (int k = 1; k < kTPR; ++k) rowsum += red[1][r0 + 128 * k];
 
-            // PV(kt-1) complete: D is quiescent (rescale it if the reference moved)
+            // PV(kt-1) done: D, the P columns and the V buffer are free
             if (kt > kt0) {
-                ok = __syncthreads_and(mbar_wait(smem_u32(&bar_pv), ph_pv));
+                ok = named_sync_and(1, kCompute, mbar_wait(smem_u32(&bar_pv), ph_pv));
                 ph_pv ^= 1;
                 if (!ok) break;
                 fence_after_sync();
@@ -338,12 +434,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs a, 
             if (__any_sync(0xffffffffu, rescale)) {
                 const float f = rescale ? exp2f(m_ref - m_use) : 1.f;
 #pragma unroll
-                for (int c = 0; c < 2; ++c) {
+                for (int c = 0; c < kDCols / 32; ++c) {
                     float dv[32];
-                    tmem_ld32(tbase + tlane + kColD + 64 * half + 32 * c, dv);
+                    tmem_ld32(tbase + tlane + kColD + kDCols * qp + 32 * c, dv);
 #pragma unroll
                     for (int i = 0; i < 32; ++i) dv[i] *= f;
-                    tmem_st32(tbase + tlane + kColD + 64 * half + 32 * c, dv);
+                    tmem_st32(tbase + tlane + kColD + kDCols * qp + 32 * c, dv);
                     tmem_st_wait();
                 }
                 l_run *= f;
@@ -351,27 +447,29 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs a, 
             l_run += rowsum;
             m_ref = m_use;
 
-            // P_kt -> TMEM (hi, then lo), V_kt -> smem, K_{kt+1} -> smem
+            // P_kt -> TMEM (hi, then lo), V_kt -> smem; the issue warp starts PV(kt)
             {
-                float t[32];
+                float t[kSCols];
 #pragma unroll
-                for (int i = 0; i < 32; ++i) t[i] = __uint_as_float(__float_as_uint(s[i]) & 0xFFFFE000u);
-                tmem_st32(tbase + tlane + kColPhi + 32 * half, t);
+                for (int i = 0; i < kSCols; ++i) t[i] = __uint_as_float(__float_as_uint(s[i]) & 0xFFFFE000u);
+                tmem_stn<kSCols>(tbase + tlane + kColPhi + kSCols * qp, t);
                 tmem_st_wait();
 #pragma unroll
-                for (int i = 0; i < 32; ++i) t[i] = s[i] - __uint_as_float(__float_as_uint(s[i]) & 0xFFFFE000u);
-                tmem_st32(tbase + tlane + kColPlo + 32 * half, t);
+                for (int i = 0; i < kSCols; ++i) t[i] = s[i] - __uint_as_float(__float_as_uint(s[i]) & 0xFFFFE000u);
+                tmem_stn<kSCols>(tbase + tlane + kColPlo + kSCols * qp, t);
             }
             store_v();
+            arrive(&bar_p);
+
+            // registers for the next tiles: V_{kt+1}, K_{kt+2}
             if (kt + 1 < kt1) {
-                store_k();
-                prefetch_v(kt + 1);
-                if (kt + 2 < kt1) prefetch_k(kt + 2);
+                load_v(kt + 1, vblk);
+                vblk = kt + 2 < kt1 ? lookup_v(kt + 2) : -1;
             }
-            operands_ready(kt + 1 < kt1, true, kt == kt0);
+            if (kt + 2 < kt1) load_k(kt + 2, kblk);
         }
         // the last PV, then the result
-        if (ok) ok = __syncthreads_and(mbar_wait(smem_u32(&bar_pv), ph_pv));
+        if (ok) ok = named_sync_and(1, kCompute, mbar_wait(smem_u32(&bar_pv), ph_pv));
         if (!ok) {
             if (tid == 0 && a.err) atomicOr(a.err, 2);
         } else {
@@ -382,17 +480,17 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs a, 
             size_t ph = 0;
             if (direct) {
                 dst = a.out + static_cast<size_t>(rd.q_row0 + (valid ? qi : 0)) * (a.n_heads * kHD) +
-                      static_cast<size_t>(h) * kHD + 64 * half;
+                      static_cast<size_t>(h) * kHD + kDCols * qp;
             } else {
                 const int n_split = (kend_tile + a.split_keys - 1) / a.split_keys;
                 ph = static_cast<size_t>(tile.part0 + (valid ? tq : 0) * n_split + tile.split) * a.n_heads + h;
-                dst = a.pacc + ph * kHD + 64 * half;
+                dst = a.pacc + ph * kHD + kDCols * qp;
             }
             const float scl = direct ? 1.f / l_run : 1.f;
 #pragma unroll
-            for (int c = 0; c < 2; ++c) {
+            for (int c = 0; c < kDCols / 32; ++c) {
                 float dv[32];
-                tmem_ld32(tbase + tlane + kColD + 64 * half + 32 * c, dv);
+                tmem_ld32(tbase + tlane + kColD + kDCols * qp + 32 * c, dv);
                 if (valid) {
 #pragma unroll
                     for (int i = 0; i < 32; i += 4)
@@ -400,9 +498,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs a, 
                             make_float4(dv[i] * scl, dv[i + 1] * scl, dv[i + 2] * scl, dv[i + 3] * scl);
                 }
             }
-            if (valid && !direct && half == 0) {
-                a.pm[ph] = m_ref;
-                a.pl[ph] = l_run;
+            if (valid) {
+                if (!direct && qp == 0) {
+                    a.pm[ph] = m_ref;
+                    a.pl[ph] = l_run;
+                }
             }
         }
     }
