@@ -51,24 +51,41 @@ def measured_hbm_peak():
         return HBM_FALLBACK_GBS, "fallback"
 
 
-def kernel_source_digest():
+KERNEL_SOURCES = {"decode": "paged_kv_gqa_nx_gb300/csrc/pkv_kernels.cu",
+                  "prefill": "paged_kv_gqa_nx_gb300/csrc/pkv_prefill.cu"}
+PROFILE_FILES = {"decode": "decode_%s.md", "prefill": "prefill_tc_%s.md"}
+
+
+def measured_tensor_peak():
+    """f32 peak of the 3xTF32 prefill contraction: the measured bf16 dense
+    rate times the nominal TF32/BF16 ratio (1.1 / 2.25 PFLOP/s), divided by the
+    three TF32 products each f32 product takes."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            bf16, kind = float(json.load(f)["bf16_tflops"]), "measured"
+    except Exception:
+        bf16, kind = 1900.0, "fallback"
+    return bf16 * (1.1 / 2.25) / 3.0, kind
+
+
+def kernel_source_digest(kernel: str = "decode"):
     h = hashlib.sha256()
-    for rel in ("paged_kv_gqa_nx_gb300/csrc/pkv_kernels.cu",):
-        with open(os.path.join(ROOT, rel), "rb") as f:
-            h.update(f.read())
+    with open(os.path.join(ROOT, KERNEL_SOURCES[kernel]), "rb") as f:
+        h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(workload: str):
-    """DRAM bytes per decode launch from the committed ncu summary for this
-    workload, if it was taken on the current kernel source; else None."""
-    path = os.path.join(ROOT, "profiles", "decode_%s.md" % workload)
+def profiled_traffic(workload: str, kernel: str = "decode"):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary for
+    this workload, if it was taken on the current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", PROFILE_FILES[kernel] % workload)
     if not os.path.exists(path):
         return None
     text = open(path).read()
     m_src = re.search(r"kernel_source_sha256:\s*([0-9a-f]+)", text)
     m_tr = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
-    if not m_src or not m_tr or m_src.group(1) != kernel_source_digest():
+    if not m_src or not m_tr or m_src.group(1) != kernel_source_digest(kernel):
         return None
     return float(m_tr.group(1))
 
@@ -204,6 +221,11 @@ class DeviceRun:
         self.kv_bytes_per_layer = float(sum(tk)) * w.kv_dim * 4 * 2
         self.kv_bytes = self.kv_bytes_per_layer * w.n_layers
         self.q_out_bytes = float(self.T) * w.q_dim * 4 * 2 * w.n_layers
+        # algorithmic flops of the rows the tensor-core prefill kernel takes
+        # (n_q >= 32): 2 for q.k and 2 for p.v per visible (query, key, dim)
+        self.prefill_flops_per_layer = float(sum(
+            4.0 * w.head_dim * w.n_heads * (n * b + n * (n + 1) // 2)
+            for b, n in zip(self.base_len, self.n_q) if n >= 32))
         torch.cuda.synchronize()
 
     def _grow_and_fill(self, s, L, seed):
@@ -417,11 +439,32 @@ def run_pkv(args):
     h2d = run.T * (w.q_dim + 2 * w.kv_dim) * 4 * w.n_layers
     d2h = run.T * w.q_dim * 4 * w.n_layers
 
+    # the roofline of the kernel that takes most of the step
     dec_ms, dec_n = kern["decode"]
-    dec_avg_s = dec_ms * 1e-3 / max(dec_n, 1)
-    alg_bytes = run.kv_bytes_per_layer + run.T * w.q_dim * 4 * 2
-    achieved = alg_bytes / dec_avg_s / 1e9 if dec_n else None
-    traffic = profiled_traffic(args.workload)
+    pre_ms, pre_n = kern["prefill"]
+    if pre_ms > dec_ms and pre_n:
+        pre_avg_s = pre_ms * 1e-3 / pre_n
+        tpeak, tkind = measured_tensor_peak()
+        achieved = run.prefill_flops_per_layer / pre_avg_s / 1e12
+        roofline = {"bound": "tensor", "kernel": "prefill (tcgen05 3xTF32 chunked prefill)",
+                    "achieved": round(achieved, 1), "peak": round(tpeak, 1),
+                    "peak_source": ("%s bf16_tflops x 1.1/2.25 (nominal TF32/BF16) / 3 (TF32 products "
+                                    "per f32 product)" % tkind),
+                    "unit": "TFLOP/s", "frac": round(achieved / tpeak, 4),
+                    "traffic": profiled_traffic(args.workload, "prefill"),
+                    "alg_flops_per_launch": run.prefill_flops_per_layer,
+                    "avg_launch_ms": round(pre_avg_s * 1e3, 4)}
+    else:
+        dec_avg_s = dec_ms * 1e-3 / max(dec_n, 1)
+        alg_bytes = run.kv_bytes_per_layer + run.T * w.q_dim * 4 * 2
+        achieved = alg_bytes / dec_avg_s / 1e9 if dec_n else None
+        roofline = {"bound": "hbm", "kernel": "decode (split-K paged attention)",
+                    "achieved": round(achieved, 1) if achieved else None, "peak": peak,
+                    "peak_source": peak_kind + " (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
+                    else "fallback", "unit": "GB/s",
+                    "frac": round(achieved / peak, 4) if achieved else None,
+                    "traffic": profiled_traffic(args.workload), "alg_bytes_per_launch": alg_bytes,
+                    "avg_launch_ms": round(dec_avg_s * 1e3, 4)}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -463,13 +506,7 @@ def run_pkv(args):
         "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps},
         "gpu_launches": launches,
-        "roofline": {"bound": "hbm", "kernel": "decode (split-K paged attention)",
-                     "achieved": round(achieved, 1) if achieved else None, "peak": peak,
-                     "peak_source": peak_kind + " (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
-                     else "fallback", "unit": "GB/s",
-                     "frac": round(achieved / peak, 4) if achieved else None,
-                     "traffic": traffic, "alg_bytes_per_launch": alg_bytes,
-                     "avg_launch_ms": round(dec_avg_s * 1e3, 4)},
+        "roofline": roofline,
         "cpu_baseline": cpu,
         "clocks": clk,
     }

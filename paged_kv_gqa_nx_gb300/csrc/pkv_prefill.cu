@@ -8,7 +8,10 @@
 //
 // One CTA = one tile of 128 query rows -- (128 / G) consecutive tokens x the G
 // query heads that share kv head `kvh` -- and one key split.  16 compute
-// warps and one MMA-issue warp.  Row m of the tile is token m / G, head m % G
+// warps and one more warpgroup whose first warp issues the MMAs; that
+// warpgroup hands most of its registers to the compute warps (setmaxnreg),
+// which keeps the compute warps' prefetch registers from spilling.  Row m of
+// the tile is token m / G, head m % G
 // and TMEM lane m; the four compute threads that share TMEM lane m (warps w,
 // w + 4, w + 8, w + 12) each own 16 of a key tile's scores and 32 of the row's
 // output columns, and combine the row max and sum through shared memory.  The
@@ -48,12 +51,20 @@ constexpr uint32_t kColQhi = 0, kColS = 128, kColPhi = 256, kColPlo = 320, kColD
 #endif
 constexpr int kComputeWarps = PKV_PREFILL_COMPUTE_WARPS;  // 8: two threads per tile row, 16: four
 constexpr int kCompute = 32 * kComputeWarps;
-constexpr int kThreads = kCompute + 32;                     // + the MMA-issue warp
+// + one warpgroup whose first warp issues the MMAs; it gives registers back
+// (setmaxnreg) so that the compute warps can hold more
+constexpr int kThreads = kCompute + 128;
+// per thread at launch: 65536 registers over the CTA, and 16384 over the at
+// most kThreads/128 warps of one SM sub-partition
+constexpr int kLaunchRegs = kComputeWarps == 16 ? 96 : 168;
+constexpr int kIssueRegs = 32;                                 // issue warpgroup after .dec
+constexpr int kComputeRegs = kComputeWarps == 16 ? 112 : 232;  // compute warps after .inc
+static_assert(kCompute * kComputeRegs + 128 * kIssueRegs <= kThreads * kLaunchRegs,
+              "register split exceeds the launch's registers");
 constexpr int kTPR = kComputeWarps / 4;                     // threads per tile row
 constexpr int kSCols = kKT / kTPR;                          // scores per thread per key tile
 constexpr int kDCols = kHD / kTPR;                          // output columns per thread
 constexpr int kKPW = kKT / kComputeWarps;                   // K rows per warp per key tile
-constexpr int kVF = 32 / (kComputeWarps / 2);               // V float4 per thread per key tile
 static_assert(kComputeWarps == 8 || kComputeWarps == 16, "8 or 16 compute warps");
 constexpr float kRescale = 8.f;               // lazy-rescale threshold (base 2)
 
@@ -181,7 +192,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs a, 
     const uint32_t tbase = tslot;
     bool ok = true;
 
-    if (warp == kComputeWarps) {
+    if (warp >= kComputeWarps) {
+        // the issue warpgroup: its first warp issues, the other three only give
+        // their registers back
+        setmaxnreg_dec<kIssueRegs>();
+        if (warp == kComputeWarps) {
         // ---------------- MMA issue warp (lane 0 issues) ----------------
         const uint64_t dKhi = desc_sw128(smem_u32(Khi)), dKlo = desc_sw128(smem_u32(Klo));
         const uint64_t dQlo = desc_sw128(smem_u32(Qlo));
@@ -192,12 +207,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs a, 
         uint32_t ph_k = 0, ph_p = 0;
         auto issue_qk = [&]() {
             // operands: K of the tile (and, the first time, Q) in place
-            ok = mbar_wait(smem_u32(&bar_k), ph_k);
+            ok = __shfl_sync(0xffffffffu, lane == 0 ? mbar_wait(smem_u32(&bar_k), ph_k) : true, 0);
             ph_k ^= 1;
             if (!ok) return;
             fence_after_sync();
             if (lane == 0) {
-#pragma unroll
+#pragma unroll 1
                 for (int s = 0; s < 16; ++s) {
                     const uint64_t ko = ((s >> 2) * 8192u + (s & 3) * 32u) >> 4;
                     const uint64_t qo = ((s >> 2) * 16384u + (s & 3) * 32u) >> 4;
@@ -211,12 +226,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs a, 
         };
         auto issue_pv = [&](bool first) {
             // operands: P and V of the tile in place
-            ok = mbar_wait(smem_u32(&bar_p), ph_p);
+            ok = __shfl_sync(0xffffffffu, lane == 0 ? mbar_wait(smem_u32(&bar_p), ph_p) : true, 0);
             ph_p ^= 1;
             if (!ok) return;
             fence_after_sync();
             if (lane == 0) {
-#pragma unroll
+#pragma unroll 1
                 for (int s = 0; s < 8; ++s) {
                     const uint64_t vo = ((s >> 2) * 16384u + (s & 3) * 32u) >> 4;
                     mma_tf32_ts(tD, tPh + 8 * s, dVhi + vo, idesc_o, !first || s > 0);
@@ -235,7 +250,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs a, 
             if (ok) issue_pv(kt == kt0);
         }
         if (!ok && lane == 0 && a.err) atomicOr(a.err, 2);
+        }
     } else {
+        setmaxnreg_inc<kComputeRegs>();
         // ---------------- compute warps: 4 threads per tile row ----------------
         const int wq = warp & 3;               // TMEM lane quadrant
         const int qp = warp >> 2;              // which quarter of the row this thread owns
@@ -276,54 +293,55 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs a, 
             }
         }
 
-        // Key rows of a tile: warp w owns keys kKPW*w .. kKPW*w + kKPW-1 for K (one
-        // 512-byte row per instruction; one page-table lookup per warp when a
-        // block holds whole kKPW-key groups) and key 32*(w & 1) + lane, float4
-        // columns (w >> 1) + (kComputeWarps/2) i, for V (the transposed store).
+        // Key rows of a tile: warp w owns keys kKPW*w .. kKPW*w + kKPW-1 of both K
+        // and V, so one page-table lookup per warp serves a tile when a block
+        // holds whole kKPW-key groups.  K: one 512-byte row per instruction,
+        // stored as 16-byte chunks of the K-major layout.  V: lane l loads dims
+        // l + 32c (c < 4) of each row (128-byte coalesced loads) and writes
+        // 16-byte runs of 4 keys into rows d = l + 32c of V^T; the 32 rows of one
+        // store fall in all 8 swizzle phases, so the store is conflict-free.
         // Page-table lookups are issued one phase before the loads that use them.
-        float4 kreg[kKPW], vreg[kVF];
+        float4 kreg[kKPW], vq[kKPW / 4][4];
         const bool k_whole = rows_of.whole(kKPW);
         auto k_pos = [&](int kt) { return kt * kKT + warp * kKPW; };
-        auto v_pos = [&](int kt) { return kt * kKT + 32 * (warp & 1) + lane; };
+        // row pointer of key pos (nullptr beyond the split or on a bad entry)
+        auto row_of = [&](int pos, int blk0, bool is_v) -> const float * {
+            if (pos >= kend) return nullptr;
+            int b = blk0;
+            if (!k_whole) b = rows_of.block(rd.slot, pos, a.err);
+            if (b < 0) return nullptr;
+            return is_v ? rows_of.v_row(b, pos, kvh) : rows_of.k_row(b, pos, kvh);
+        };
         auto load_k = [&](int kt, int blk0) {
             const int pos0 = k_pos(kt);
             if (k_whole && pos0 < kend) blk0 = rows_of.checked(blk0, a.err);
 #pragma unroll
             for (int i = 0; i < kKPW; ++i) {
-                kreg[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-                const int pos = pos0 + i;
-                if (pos < kend) {
-                    const float *kr = nullptr;
-                    if (k_whole) {
-                        if (blk0 >= 0) kr = rows_of.k_row(blk0, pos, kvh);
-                    } else {
-                        const int b = rows_of.block(rd.slot, pos, a.err);
-                        kr = b >= 0 ? rows_of.k_row(b, pos, kvh) : nullptr;
-                    }
-                    if (kr) kreg[i] = __ldg(reinterpret_cast<const float4 *>(kr) + lane);
-                }
+                const float *kr = row_of(pos0 + i, blk0, false);
+                kreg[i] = kr ? __ldg(reinterpret_cast<const float4 *>(kr) + lane) : make_float4(0.f, 0.f, 0.f, 0.f);
             }
         };
-        auto load_v = [&](int kt, int vblk) {
-            const int pos = v_pos(kt);
+        auto load_v = [&](int kt, int blk0) {
+            const int pos0 = k_pos(kt);
+            if (k_whole && pos0 < kend) blk0 = rows_of.checked(blk0, a.err);
 #pragma unroll
-            for (int i = 0; i < kVF; ++i) vreg[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (pos < kend) vblk = rows_of.checked(vblk, a.err);
-            if (pos < kend && vblk >= 0) {
-                const float *vr = rows_of.v_row(vblk, pos, kvh);
+            for (int g4 = 0; g4 < kKPW / 4; ++g4) {
+                float v[4][4];  // [key][c]
 #pragma unroll
-                for (int i = 0; i < kVF; ++i)
-                    vreg[i] = __ldg(reinterpret_cast<const float4 *>(vr) + (warp >> 1) + (kComputeWarps / 2) * i);
+                for (int i = 0; i < 4; ++i) {
+                    const float *vr = row_of(pos0 + 4 * g4 + i, blk0, true);
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) v[i][c] = vr ? __ldg(vr + lane + 32 * c) : 0.f;
+                }
+#pragma unroll
+                for (int c = 0; c < 4; ++c) vq[g4][c] = make_float4(v[0][c], v[1][c], v[2][c], v[3][c]);
             }
         };
         auto lookup_k = [&](int kt) {
             const int pos0 = k_pos(kt);
             return (k_whole && pos0 < kend) ? rows_of.entry(rd.slot, pos0, a.err) : -1;
         };
-        auto lookup_v = [&](int kt) {
-            const int pos = v_pos(kt);
-            return pos < kend ? rows_of.entry(rd.slot, pos, a.err) : -1;
-        };
+        auto lookup_v = lookup_k;
         auto store_k = [&]() {
 #pragma unroll
             for (int i = 0; i < kKPW; ++i) {
@@ -335,20 +353,28 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs a, 
             }
         };
         auto store_v = [&]() {
-            const uint32_t kb = static_cast<uint32_t>(warp & 1) * 16384u;
 #pragma unroll
-            for (int i = 0; i < kVF; ++i) {
-                const int d0 = 4 * ((warp >> 1) + (kComputeWarps / 2) * i);
-                const float v4[4] = {vreg[i].x, vreg[i].y, vreg[i].z, vreg[i].w};
+            for (int g4 = 0; g4 < kKPW / 4; ++g4) {
+                const int key0 = warp * kKPW + 4 * g4;
+                const uint32_t kb = static_cast<uint32_t>(key0 >> 5) * 16384u;
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    float h, l;
-                    split_tf32(v4[e], h, l);
-                    const uint32_t off = kb + sw128_offset(d0 + e, lane);
-                    *reinterpret_cast<float *>(Vhi + off) = h;
-                    *reinterpret_cast<float *>(Vlo + off) = l;
+                for (int c = 0; c < 4; ++c) {
+                    float4 h, l;
+                    split4(vq[g4][c], h, l);
+                    const uint32_t off = kb + sw128_chunk(lane + 32 * c, (key0 & 31) >> 2);
+                    *reinterpret_cast<float4 *>(Vhi + off) = h;
+                    *reinterpret_cast<float4 *>(Vlo + off) = l;
                 }
             }
+        };
+        // Wait for an MMA commit: one thread polls the mbarrier and the others
+        // wait in the named barrier, so the polling takes no shared-memory
+        // bandwidth from the tensor core's operand reads.
+        auto wait_one = [&](uint64_t *bar, uint32_t ph) {
+            bool w = true;
+            if (tid == 0) w = mbar_wait(smem_u32(bar), ph);
+            __syncwarp();
+            return named_sync_and(1, kCompute, w);
         };
         // operands written: make them visible to the tensor core, then one lane
         // per warp arrives on the barrier the issue warp waits on
@@ -367,7 +393,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs a, 
         float m_ref = -INFINITY, l_run = 0.f;
         uint32_t ph_qk = 0, ph_pv = 0;
 
-        // prologue: K_kt0 in place (QK(kt0) may start), V_kt0 and K_kt0+1 in registers
+        // prologue: K_kt0 in place (QK(kt0) may start), V_kt0 and K_kt0+1 in
+        // registers, the page-table entries of K_kt0+2 and V_kt0+1 on their way
         load_k(kt0, lookup_k(kt0));
         int vblk = lookup_v(kt0);
         load_v(kt0, vblk);
@@ -379,13 +406,14 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs a, 
 
         for (int kt = kt0; kt < kt1; ++kt) {
             // S_kt ready (QK(kt) done: the K buffer is free again)
-            ok = named_sync_and(1, kCompute, mbar_wait(smem_u32(&bar_qk), ph_qk));
+            ok = wait_one(&bar_qk, ph_qk);
             ph_qk ^= 1;
             if (!ok) break;
             fence_after_sync();
             float s[kSCols];
             tmem_ldn<kSCols>(tbase + tlane + kColS + kSCols * qp, s);
-            // K_{kt+1} -> smem; the issue warp starts QK(kt+1) while we do the softmax
+            // K_{kt+1} -> smem; the issue warp starts QK(kt+1) while we do the
+            // softmax, and the K_{kt+2} loads overlap it too
             if (kt + 1 < kt1) {
                 store_k();
                 kblk = kt + 2 < kt1 ? lookup_k(kt + 2) : -1;
@@ -424,7 +452,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs a, 
 
             // PV(kt-1) done: D, the P columns and the V buffer are free
             if (kt > kt0) {
-                ok = named_sync_and(1, kCompute, mbar_wait(smem_u32(&bar_pv), ph_pv));
+                ok = wait_one(&bar_pv, ph_pv);
                 ph_pv ^= 1;
                 if (!ok) break;
                 fence_after_sync();
@@ -449,19 +477,20 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs a, 
 
             // P_kt -> TMEM (hi, then lo), V_kt -> smem; the issue warp starts PV(kt)
             {
+                // hi from a copy, then lo in place (s is dead after this)
                 float t[kSCols];
 #pragma unroll
                 for (int i = 0; i < kSCols; ++i) t[i] = __uint_as_float(__float_as_uint(s[i]) & 0xFFFFE000u);
                 tmem_stn<kSCols>(tbase + tlane + kColPhi + kSCols * qp, t);
-                tmem_st_wait();
 #pragma unroll
-                for (int i = 0; i < kSCols; ++i) t[i] = s[i] - __uint_as_float(__float_as_uint(s[i]) & 0xFFFFE000u);
-                tmem_stn<kSCols>(tbase + tlane + kColPlo + kSCols * qp, t);
+                for (int i = 0; i < kSCols; ++i) s[i] -= t[i];
+                tmem_st_wait();
+                tmem_stn<kSCols>(tbase + tlane + kColPlo + kSCols * qp, s);
             }
             store_v();
             arrive(&bar_p);
 
-            // registers for the next tiles: V_{kt+1}, K_{kt+2}
+            // registers for the next tile: V_{kt+1}
             if (kt + 1 < kt1) {
                 load_v(kt + 1, vblk);
                 vblk = kt + 2 < kt1 ? lookup_v(kt + 2) : -1;
@@ -469,7 +498,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs a, 
             if (kt + 2 < kt1) load_k(kt + 2, kblk);
         }
         // the last PV, then the result
-        if (ok) ok = named_sync_and(1, kCompute, mbar_wait(smem_u32(&bar_pv), ph_pv));
+        if (ok) ok = wait_one(&bar_pv, ph_pv);
         if (!ok) {
             if (tid == 0 && a.err) atomicOr(a.err, 2);
         } else {
@@ -515,9 +544,17 @@ template <int G, class Rows>
 cudaError_t launch_prefill_g(const PrefillArgs &a, const Rows &r, cudaStream_t s) {
     static bool configured = false;
     if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<G, Rows>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(kSmemBytes));
+        // setmaxnreg.inc waits until the CTA's pool holds the registers it asks
+        // for, so launch only if the compiled kernel starts with the registers
+        // the split was sized for
+        cudaFuncAttributes fa{};
+        cudaError_t e = cudaFuncGetAttributes(&fa, prefill_tc_kernel<G, Rows>);
+        if (e != cudaSuccess) return e;
+        if (fa.numRegs < kLaunchRegs || fa.maxThreadsPerBlock < kThreads)
+            return cudaErrorInvalidConfiguration;
+        e = cudaFuncSetAttribute(prefill_tc_kernel<G, Rows>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(kSmemBytes));
         if (e != cudaSuccess) return e;
         configured = true;
     }

@@ -109,7 +109,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t mbar, uint32_t parity) {
         uint32_t ok;
         asm volatile(
             "{\n\t.reg .pred p;\n\t"
-            "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+            "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
             "selp.u32 %0, 1, 0, p;\n\t}\n"
             : "=r"(ok)
             : "r"(mbar), "r"(parity)
@@ -240,6 +240,20 @@ __device__ __forceinline__ void tmem_stn(uint32_t taddr, const float (&v)[N]) {
 }
 __device__ __forceinline__ void tmem_st_wait() {
     asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory");
+}
+
+// Register reallocation between warpgroups: every warp of a warpgroup executes
+// the same call.  .dec returns registers to the CTA's pool, .inc waits until the
+// pool holds enough; the launch's registers must cover the sum of the targets.
+template <int N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+    static_assert(N % 8 == 0 && N >= 24 && N <= 256, "setmaxnreg target");
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+    static_assert(N % 8 == 0 && N >= 24 && N <= 256, "setmaxnreg target");
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;\n" ::"n"(N));
 }
 
 // Split x into a tf32 value (low 13 mantissa bits cleared) and the exact f32 rest.
