@@ -262,6 +262,20 @@ PKV_API int pkv_pool_flush(pkv_pool *pool);
 PKV_API int pkv_set_split_keys(int32_t keys);
 PKV_API int32_t pkv_get_split_keys(void);
 
+/* Fused append (default on).  The per-layer step is "append the new K/V rows
+ * into their pages, then attend over the sequence" ("nx_f32_kvcache_paged"
+ * page, the attend-with-paged call contract).  With fusion on, a decode call
+ * -- no row takes the tensor-core prefill path, head_dim 128, group size 1, 2
+ * or 4 -- whose pending page-table changes all lie in pages that hold only
+ * this call's new positions (fresh pages; not a copy-on-append tail, a fork or
+ * a truncate) runs as the decode kernel alone: it reads the new rows from
+ * K_new / V_new, stores them into the pool and enters the new pages into the
+ * device page table, with no separate append launch.  Every other call takes
+ * the unfused path.  Results, pool contents and page tables are bit-identical
+ * either way.  on != 0 enables; process-wide. */
+PKV_API int pkv_set_fused_append(int32_t on);
+PKV_API int32_t pkv_get_fused_append(void);
+
 /* Kernel launch accounting.  pkv_launch_count: kernels launched by the library
  * so far (all kinds).  When profiling is on, every launch is bracketed by CUDA
  * events on its stream; pkv_profile_read synchronises those events and

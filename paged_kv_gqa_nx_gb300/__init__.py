@@ -93,6 +93,8 @@ _SIGS = {
     "pkv_pool_flush": (_int, [_vp]),
     "pkv_set_split_keys": (_int, [_i32]),
     "pkv_get_split_keys": (_i32, []),
+    "pkv_set_fused_append": (_int, [_i32]),
+    "pkv_get_fused_append": (_i32, []),
     "pkv_launch_count": (_i64, []),
     "pkv_profile_enable": (_int, [_i32]),
     "pkv_profile_reset": (_int, []),
@@ -328,6 +330,14 @@ def pkv_set_split_keys(keys):
 
 def pkv_get_split_keys():
     return _lib.pkv_get_split_keys()
+
+
+def pkv_set_fused_append(on):
+    return _lib.pkv_set_fused_append(1 if on else 0)
+
+
+def pkv_get_fused_append():
+    return bool(_lib.pkv_get_fused_append())
 
 
 def pkv_launch_count():

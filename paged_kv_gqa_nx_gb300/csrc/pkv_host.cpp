@@ -47,6 +47,7 @@ int cuda_fail(cudaError_t e, const char *what) {
 }
 
 std::atomic<int32_t> g_split_keys{1024};
+std::atomic<int32_t> g_fused_append{1};
 std::atomic<int64_t> g_launches{0};
 
 // Optional per-launch CUDA-event timing.
@@ -420,6 +421,37 @@ void build_work(const std::vector<RowDesc> &rows, int causal, int32_t S, int32_t
     w.pmerges.clear();
 }
 
+// The fused append may replace the page-table upload when every pending
+// change belongs to a sequence of this batch and lies in pages that hold none
+// of its past positions and only positions this call appends: nothing in the
+// launch reads those entries (new positions come from K_new / V_new), and the
+// kernel enters them itself.
+bool dirty_within_appends(const pkv_pool *p, pkv_seq *const *seqs, int32_t M, const int32_t *n_q) {
+    std::unordered_map<const pkv_seq *, int32_t> row_of;
+    for (int32_t r = 0; r < M; ++r) row_of[seqs[r]] = r;
+    for (const pkv_seq *s : p->dirty) {
+        const auto it = row_of.find(s);
+        if (it == row_of.end()) return false;
+        const int32_t hi = std::min<int32_t>(s->dhi, static_cast<int32_t>(s->pt.size()));
+        if (hi <= s->dlo) continue;
+        const int32_t first_new = ceil_div(s->len, p->bs);
+        const int32_t end_new = ceil_div(s->len + n_q[it->second], p->bs);
+        if (s->dlo < first_new || hi > end_new) return false;
+    }
+    return true;
+}
+
+// Mark every pending page-table change as uploaded; true if there was one.
+bool clear_dirty(pkv_pool *p) {
+    bool any = false;
+    for (pkv_seq *s : p->dirty) {
+        any = any || s->dhi > s->dlo;
+        s->dirty = false;
+    }
+    p->dirty.clear();
+    return any;
+}
+
 int check_heads(int32_t n_heads, int32_t n_kv_heads, int32_t head_dim) {
     if (n_heads <= 0 || n_kv_heads <= 0 || head_dim <= 0)
         return fail(PKV_ERR_BAD_DIM, "n_heads, n_kv_heads and head_dim must be positive");
@@ -521,12 +553,18 @@ int run_layer(pkv_seq *const *seqs, int32_t M, const int32_t *n_q, const float *
     WorkList w;
     const int32_t S = g_split_keys.load();
     if (attend) build_work(rows, causal, S, head_dim, n_heads / n_kv_heads, w);
+    const int32_t group = attend ? n_heads / n_kv_heads : 0;
+    const bool fuse = attend && g_fused_append.load() != 0 && w.tiles.empty() && !w.units.empty() &&
+                      head_dim == 128 && (group == 1 || group == 2 || group == 4) &&
+                      dirty_within_appends(p, seqs, M, n_q);
 
     Blob &blob = p->blob;
     blob.clear();
-    size_t runs_off, vals_off;
-    int32_t n_runs;
-    put_pt_runs(p, blob, &runs_off, &n_runs, &vals_off);
+    size_t runs_off = 0, vals_off = 0;
+    int32_t n_runs = 0;
+    bool pt_write = false;
+    if (fuse) pt_write = clear_dirty(p);
+    else put_pt_runs(p, blob, &runs_off, &n_runs, &vals_off);
     const size_t rows_off = blob.put(rows.data(), rows.size());
     const size_t app_off = blob.put(app.data(), app.size());
     const size_t units_off = blob.put(w.units.data(), w.units.size());
@@ -568,8 +606,10 @@ int run_layer(pkv_seq *const *seqs, int32_t M, const int32_t *n_q, const float *
     pr.V_new = Vd;
     pr.vec4 = (kv_dim % 4) == 0 && aligned16(Kd) && aligned16(Vd);
     pr.err = p->err_dev;
-    e = launch(PKV_KERNEL_APPEND, st, [&] { return launch_prep(pr, addr, st); });
-    if (e != cudaSuccess) return cuda_fail(e, "prep kernel");
+    if (!fuse) {
+        e = launch(PKV_KERNEL_APPEND, st, [&] { return launch_prep(pr, addr, st); });
+        if (e != cudaSuccess) return cuda_fail(e, "prep kernel");
+    }
     if (!attend) return PKV_OK;
 
     AttnArgs a{};
@@ -587,6 +627,12 @@ int run_layer(pkv_seq *const *seqs, int32_t M, const int32_t *n_q, const float *
     a.split_keys = S;
     a.scale_log2 = scale * 1.4426950408889634f;
     a.err = p->err_dev;
+    if (fuse) {
+        a.K_new = Kd;
+        a.V_new = Vd;
+        a.app = pr.app;
+        a.pt_write = pt_write ? 1 : 0;
+    }
     if (w.n_part > 0) {
         const size_t pf = static_cast<size_t>(w.n_part) * n_heads;
         e = p->part.ensure(pf * (2 + head_dim) * sizeof(float), st, p->device);
@@ -1124,6 +1170,12 @@ int pkv_set_split_keys(int32_t keys) {
     return PKV_OK;
 }
 int32_t pkv_get_split_keys(void) { return g_split_keys.load(); }
+
+int pkv_set_fused_append(int32_t on) {
+    g_fused_append.store(on ? 1 : 0);
+    return PKV_OK;
+}
+int32_t pkv_get_fused_append(void) { return g_fused_append.load(); }
 
 int64_t pkv_launch_count(void) { return g_launches.load(); }
 

@@ -51,7 +51,7 @@ struct CopyDesc {
 //   pool[pt[slot][pos / bs]][layer][pos % bs][kv_head*hd ...]
 struct PagedAddr {
     float *k, *v;
-    const int32_t *pt;
+    int32_t *pt;           // written only by the fused append, for pages no reader of that launch uses
     int64_t block_stride;  // floats per block: n_layers * bs * kv_dim
     int64_t layer_off;     // floats to the layer: layer * bs * kv_dim
     int32_t kv_dim, bs, bs_shift, max_blocks, n_blocks;
@@ -74,6 +74,15 @@ struct AttnArgs {
     int32_t n_heads, n_kv, hd, group, causal, split_keys;
     float scale_log2;       // scale * log2(e): scores are kept in base-2 units
     int32_t *err;
+    // Fused append (paged decode, K_new != nullptr): a row's positions
+    // past_len .. past_len + n_q - 1 are read from K_new / V_new row
+    // q_row0 + (pos - past_len) instead of the pool, and the unit of query
+    // n_q - 1 whose split holds them also stores them into the pool (block id
+    // app[q_row0 + t].blk) and, when pt_write is set, enters each new block
+    // (a position at a block boundary) into the device page table.
+    const float *K_new = nullptr, *V_new = nullptr;
+    const AppendDesc *app = nullptr;
+    int32_t pt_write = 0;
 };
 
 // One tensor-core prefill tile: queries q0 .. q0 + 128/G - 1 of row `row`

@@ -72,6 +72,30 @@ struct PagedRows {
     // plus j * kv_dim.
     __device__ __forceinline__ bool whole_tiles(int T) const { return (a.bs % T) == 0; }
     __device__ __forceinline__ size_t row_stride() const { return static_cast<size_t>(a.kv_dim); }
+    __device__ __forceinline__ bool block_start(int pos) const {
+        return (a.bs_shift >= 0 ? (pos & (a.bs - 1)) : (pos % a.bs)) == 0;
+    }
+    // Fused append: store head kvh's hd floats of one new row (K and V) at
+    // position pos of block blk, one float4 per lane of the calling warp;
+    // with set_pt, also enter blk as the page of pos.  False (and the error
+    // flag) on an out-of-range block id or page index.
+    __device__ __forceinline__ bool store_row(int slot, int blk, int pos, int kvh, int hd,
+                                              const float *ks, const float *vs, bool set_pt,
+                                              int lane, int32_t *err) const {
+        const int bi = a.bs_shift >= 0 ? (pos >> a.bs_shift) : (pos / a.bs);
+        if (static_cast<unsigned>(blk) >= static_cast<unsigned>(a.n_blocks) || bi >= a.max_blocks) {
+            if (lane == 0) flag_error(err, 1);
+            return false;
+        }
+        const size_t o = static_cast<size_t>(blk) * a.block_stride + a.layer_off +
+                         static_cast<size_t>(pos - bi * a.bs) * a.kv_dim + static_cast<size_t>(kvh) * hd;
+        for (int i = lane; 4 * i < hd; i += 32) {
+            reinterpret_cast<float4 *>(a.k + o)[i] = __ldg(reinterpret_cast<const float4 *>(ks) + i);
+            reinterpret_cast<float4 *>(a.v + o)[i] = __ldg(reinterpret_cast<const float4 *>(vs) + i);
+        }
+        if (set_pt && lane == 0) a.pt[static_cast<size_t>(slot) * a.max_blocks + bi] = blk;
+        return true;
+    }
 };
 
 struct ContigRows {
@@ -85,6 +109,12 @@ struct ContigRows {
     }
     __device__ __forceinline__ bool whole_tiles(int) const { return true; }
     __device__ __forceinline__ size_t row_stride() const { return static_cast<size_t>(a.kv_dim); }
+    // contiguous histories are caller-owned: there is no fused append
+    __device__ __forceinline__ bool block_start(int) const { return false; }
+    __device__ __forceinline__ bool store_row(int, int, int, int, int, const float *, const float *,
+                                              bool, int, int32_t *) const {
+        return false;
+    }
 };
 
 // The key range of one work unit.
@@ -327,12 +357,25 @@ __global__ void __launch_bounds__(128, 3) decode_fast_kernel(AttnArgs a, Rows ro
 
     const bool whole = rows_of.whole_tiles(T);
     const size_t rstride = rows_of.row_stride();
+    // fused append: positions from past_len on come from K_new / V_new
+    const bool fused = a.K_new != nullptr;
+    const int new0 = fused ? rd.past_len : 0x7fffffff;
+    auto row_ptrs = [&](int pos, const float *&kr, const float *&vr) {
+        if (pos >= new0) {
+            const size_t o = static_cast<size_t>(rd.q_row0 + (pos - new0)) * rstride +
+                             static_cast<size_t>(kvh) * HD;
+            kr = a.K_new + o;
+            vr = a.V_new + o;
+            return true;
+        }
+        return rows_of.row(rd.slot, pos, kvh, HD, kr, vr, a.err);
+    };
     auto load_tile = [&](int k_local, int stage) {
         const int pos0 = ur.kbeg + (warp + k_local * W) * T;
         const int nv = min(T, ur.kend - pos0);
         float *Ks = wbase + stage * STAGE;
         float *Vs = Ks + T * HD;
-        if (whole) {
+        if (whole && pos0 + T <= new0) {
             // one page-table lookup per tile
             const float *kb, *vb;
             if (rows_of.row(rd.slot, pos0, kvh, HD, kb, vb, a.err)) {
@@ -349,7 +392,7 @@ __global__ void __launch_bounds__(128, 3) decode_fast_kernel(AttnArgs a, Rows ro
             for (int j = 0; j < T; ++j) {
                 if (j < nv) {
                     const float *kr, *vr;
-                    if (rows_of.row(rd.slot, pos0 + j, kvh, HD, kr, vr, a.err)) {
+                    if (row_ptrs(pos0 + j, kr, vr)) {
                         cp_async16(Ks + j * HD + lane * 4, kr + lane * 4);
                         cp_async16(Vs + j * HD + lane * 4, vr + lane * 4);
                     }
@@ -357,6 +400,18 @@ __global__ void __launch_bounds__(128, 3) decode_fast_kernel(AttnArgs a, Rows ro
             }
         }
     };
+
+    // fused append: the unit of the row's last query stores the new rows of
+    // its split into the pool (nothing in this launch reads them from there)
+    if (fused && u.qi == rd.n_q - 1) {
+        for (int pos = max(ur.kbeg, new0) + warp; pos < ur.kend; pos += W) {
+            const int t = pos - new0;
+            const AppendDesc ad = a.app[rd.q_row0 + t];
+            const size_t o = static_cast<size_t>(rd.q_row0 + t) * rstride + static_cast<size_t>(kvh) * HD;
+            const bool set_pt = a.pt_write && kvh == 0 && (pos == 0 || rows_of.block_start(pos));
+            rows_of.store_row(rd.slot, ad.blk, pos, kvh, HD, a.K_new + o, a.V_new + o, set_pt, lane, a.err);
+        }
+    }
 
 #pragma unroll
     for (int s = 0; s < NST - 1; ++s) {
