@@ -221,11 +221,6 @@ class DeviceRun:
         self.kv_bytes_per_layer = float(sum(tk)) * w.kv_dim * 4 * 2
         self.kv_bytes = self.kv_bytes_per_layer * w.n_layers
         self.q_out_bytes = float(self.T) * w.q_dim * 4 * 2 * w.n_layers
-        # algorithmic flops of the rows the tensor-core prefill kernel takes
-        # (n_q >= 32): 2 for q.k and 2 for p.v per visible (query, key, dim)
-        self.prefill_flops_per_layer = float(sum(
-            4.0 * w.head_dim * w.n_heads * (n * b + n * (n + 1) // 2)
-            for b, n in zip(self.base_len, self.n_q) if n >= 32))
         torch.cuda.synchronize()
 
     def _grow_and_fill(self, s, L, seed):
@@ -389,6 +384,11 @@ def run_pkv(args):
     for _ in range(args.warmup):
         run.step()
     torch.cuda.synchronize()
+    # tensor-core work of one layer call as the library laid it out: the
+    # visible (query, key) pairs of the prefill rows and of the shared-prefix
+    # pass, 2 flops each for q.k and for p.v per head dimension
+    work = pkv.pkv_pool_last_work(run.pool)
+    tensor_flops_per_layer = 4.0 * w.head_dim * w.n_heads * (work["prefill_pairs"] + work["prefix_pairs"])
 
     uuid = None
     try:
@@ -443,16 +443,19 @@ def run_pkv(args):
     dec_ms, dec_n = kern["decode"]
     pre_ms, pre_n = kern["prefill"]
     if pre_ms > dec_ms and pre_n:
+        # flops per launch: one layer call's tensor-core work over its prefill launches
+        pre_per_layer = pre_n / (args.steps * w.n_layers)
         pre_avg_s = pre_ms * 1e-3 / pre_n
+        flops_per_launch = tensor_flops_per_layer / max(pre_per_layer, 1e-9)
         tpeak, tkind = measured_tensor_peak()
-        achieved = run.prefill_flops_per_layer / pre_avg_s / 1e12
+        achieved = flops_per_launch / pre_avg_s / 1e12
         roofline = {"bound": "tensor", "kernel": "prefill (tcgen05 3xTF32 chunked prefill)",
                     "achieved": round(achieved, 1), "peak": round(tpeak, 1),
                     "peak_source": ("%s bf16_tflops x 1.1/2.25 (nominal TF32/BF16) / 3 (TF32 products "
                                     "per f32 product)" % tkind),
                     "unit": "TFLOP/s", "frac": round(achieved / tpeak, 4),
                     "traffic": profiled_traffic(args.workload, "prefill"),
-                    "alg_flops_per_launch": run.prefill_flops_per_layer,
+                    "alg_flops_per_launch": flops_per_launch,
                     "avg_launch_ms": round(pre_avg_s * 1e3, 4)}
     else:
         dec_avg_s = dec_ms * 1e-3 / max(dec_n, 1)

@@ -100,6 +100,17 @@ PKV_API float *pkv_pool_v_data(const pkv_pool *pool);
 /* Number of blocks on the free list, or -1 for NULL. */
 PKV_API int32_t pkv_pool_free_blocks(const pkv_pool *pool);
 
+/* Work list of the pool's last attend call (diagnostics and measurement; no
+ * counterpart on the pages).  Writes min(cap, PKV_WORK_FIELDS) values into
+ * the caller's host array `out`; returns PKV_OK, or PKV_ERR_ARG for a NULL
+ * pool or array or a negative cap:
+ *   [0] split-K decode units, [1] tensor-core prefill tiles, [2] shared-prefix
+ *   tiles, [3] merge items, [4] visible (query, key) pairs of the prefill rows,
+ *   [5] (query, key) pairs of the shared-prefix pass, [6] 1 if the call ran
+ *   with the fused append. */
+#define PKV_WORK_FIELDS 7
+PKV_API int pkv_pool_last_work(const pkv_pool *pool, int64_t *out, int32_t cap);
+
 /* Allocate one block: its id (refcount 1), or -1 when the pool is exhausted
  * ("nx_paged_kv_gate.nx source", KAT section: ids 0,1,2 then -1). */
 PKV_API int64_t pkv_alloc_block(pkv_pool *pool);
@@ -275,6 +286,20 @@ PKV_API int32_t pkv_get_split_keys(void);
  * either way.  on != 0 enables; process-wide. */
 PKV_API int pkv_set_fused_append(int32_t on);
 PKV_API int32_t pkv_get_fused_append(void);
+
+/* Shared-prefix (cascade) decode (default on).  Forks share their prefix
+ * pages by reference ("nx_f32_kvcache_paged" page, fork: the child's page
+ * table copies the parent's and every page's reference count goes up).  When
+ * a batch holds 16 or more consecutive rows with one query each whose first
+ * 2048 or more keys lie in the same whole pages (head_dim 128, group size 1,
+ * 2, 4 or 8), those keys are attended once for the whole run by a tensor-core
+ * pass over the stacked queries, and each row's remaining keys by the decode
+ * kernel; the two parts are combined by the log-sum-exp merge.  The result is
+ * the same attention within f32 rounding (the split boundaries differ from
+ * the non-cascade path, so it is not bit-identical to it).  on != 0 enables;
+ * process-wide. */
+PKV_API int pkv_set_cascade(int32_t on);
+PKV_API int32_t pkv_get_cascade(void);
 
 /* Kernel launch accounting.  pkv_launch_count: kernels launched by the library
  * so far (all kinds).  When profiling is on, every launch is bracketed by CUDA

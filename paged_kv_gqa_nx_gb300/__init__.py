@@ -95,6 +95,9 @@ _SIGS = {
     "pkv_get_split_keys": (_i32, []),
     "pkv_set_fused_append": (_int, [_i32]),
     "pkv_get_fused_append": (_i32, []),
+    "pkv_set_cascade": (_int, [_i32]),
+    "pkv_pool_last_work": (_int, [_vp, ctypes.POINTER(ctypes.c_int64), _i32]),
+    "pkv_get_cascade": (_i32, []),
     "pkv_launch_count": (_i64, []),
     "pkv_profile_enable": (_int, [_i32]),
     "pkv_profile_reset": (_int, []),
@@ -338,6 +341,26 @@ def pkv_set_fused_append(on):
 
 def pkv_get_fused_append():
     return bool(_lib.pkv_get_fused_append())
+
+
+PKV_WORK_FIELDS = 7
+WORK_FIELD_NAMES = ("decode_units", "prefill_tiles", "prefix_tiles", "merge_items",
+                    "prefill_pairs", "prefix_pairs", "fused_append")
+
+
+def pkv_pool_last_work(pool):
+    """The pool's last attend call's work list as a dict (see WORK_FIELD_NAMES)."""
+    buf = (ctypes.c_int64 * PKV_WORK_FIELDS)()
+    check(_lib.pkv_pool_last_work(pool, buf, PKV_WORK_FIELDS))
+    return dict(zip(WORK_FIELD_NAMES, list(buf)))
+
+
+def pkv_set_cascade(on):
+    return _lib.pkv_set_cascade(1 if on else 0)
+
+
+def pkv_get_cascade():
+    return bool(_lib.pkv_get_cascade())
 
 
 def pkv_launch_count():

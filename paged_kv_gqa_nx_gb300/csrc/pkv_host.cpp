@@ -48,6 +48,7 @@ int cuda_fail(cudaError_t e, const char *what) {
 
 std::atomic<int32_t> g_split_keys{1024};
 std::atomic<int32_t> g_fused_append{1};
+std::atomic<int32_t> g_cascade{1};
 std::atomic<int64_t> g_launches{0};
 
 // Optional per-launch CUDA-event timing.
@@ -265,6 +266,8 @@ struct pkv_pool {
     cudaStream_t stream = nullptr;
     int device = 0;
 
+    int64_t last_work[PKV_WORK_FIELDS] = {};  // work list of the last attend call
+
     std::vector<int32_t> free_stack;   // top = back
     std::vector<int32_t> refcnt;
     std::vector<int32_t> free_slots;   // top = back
@@ -364,23 +367,121 @@ bool can_append(const pkv_seq *s, int32_t n) {
 struct WorkList {
     std::vector<UnitDesc> units;
     std::vector<PrefillTile> tiles;
+    std::vector<PrefillTile> ctiles;  // shared-prefix pass (non-causal, split S)
     std::vector<MergeDesc> merges;   // queries with several splits (decode first, then prefill)
     std::vector<MergeDesc> pmerges;  // prefill items while building
     int64_t n_part = 0;
 };
 
-void build_work(const std::vector<RowDesc> &rows, int causal, int32_t S, int32_t head_dim,
-                int32_t group, WorkList &w) {
+// A run of consecutive single-query rows whose page tables start with the
+// same Lp / bs pages (shared through forks: a page id common to two live
+// sequences is one physical page, so those keys are identical).
+struct Cascade {
+    int32_t r0, n, Lp;
+};
+
+// Shared-prefix groups of a decode batch: at least kCascadeMinRows
+// consecutive rows with one query each whose first kCascadeMinKeys or more
+// keys lie in common whole pages.  The group's common page count is fixed by
+// its first two rows; later rows join while they share all of those pages.
+constexpr int32_t kCascadeMinRows = 16;
+constexpr int32_t kCascadeMinKeys = 2048;
+
+std::vector<Cascade> find_cascades(pkv_seq *const *seqs, int32_t M, const int32_t *n_q,
+                                   int32_t bs) {
+    std::vector<Cascade> out;
+    auto eligible = [&](int32_t r) { return n_q[r] == 1 && seqs[r]->len >= kCascadeMinKeys; };
+    auto shares = [&](int32_t a, int32_t b, int32_t pages) {
+        const std::vector<int32_t> &x = seqs[a]->pt, &y = seqs[b]->pt;
+        return seqs[b]->len / bs >= pages &&
+               std::equal(x.begin(), x.begin() + pages, y.begin());
+    };
+    int32_t r = 0;
+    while (r + 1 < M) {
+        if (!eligible(r) || !eligible(r + 1)) {
+            ++r;
+            continue;
+        }
+        const std::vector<int32_t> &x = seqs[r]->pt, &y = seqs[r + 1]->pt;
+        int32_t lim = std::min(seqs[r]->len, seqs[r + 1]->len) / bs;
+        int32_t pages = 0;
+        while (pages < lim && x[pages] == y[pages]) ++pages;
+        if (static_cast<int64_t>(pages) * bs < kCascadeMinKeys) {
+            ++r;
+            continue;
+        }
+        int32_t e = r + 2;
+        while (e < M && eligible(e) && shares(r, e, pages)) ++e;
+        const int32_t n = e - r, Lp = pages * bs;
+        if (n >= kCascadeMinRows && Lp >= n) {
+            out.push_back({r, n, Lp});
+            r = e;
+        } else {
+            ++r;
+        }
+    }
+    return out;
+}
+
+// Work of the cascade groups: per group one virtual row (the members' queries,
+// consecutive in Q, over keys [0, Lp), non-causal) cut into tensor-core tiles
+// of split S, and per member the decode units of keys [Lp, total_k) and a
+// merge item whose records are the prefix splits followed by the suffix
+// splits.  Members get k0 = Lp, s0 = the prefix split count; virtual rows are
+// appended to `rows`.  Returns the member mask.
+std::vector<char> add_cascades(std::vector<RowDesc> &rows, const std::vector<Cascade> &cas,
+                               int32_t S, int32_t group, WorkList &w,
+                               std::vector<UnitDesc> &tail) {
+    std::vector<char> member(rows.size(), 0);
+    const int32_t TQ = 128 / group;
+    for (const Cascade &c : cas) {
+        const int32_t n_pref = ceil_div(c.Lp, S);
+        int32_t max_suf = 0;
+        for (int32_t t = 0; t < c.n; ++t) {
+            const RowDesc &rd = rows[c.r0 + t];
+            max_suf = std::max(max_suf, ceil_div(rd.past_len + rd.n_q - c.Lp, S));
+        }
+        const int32_t stride = n_pref + max_suf;
+        const int32_t part0 = static_cast<int32_t>(w.n_part);
+        w.n_part += static_cast<int64_t>(c.n) * stride;
+        RowDesc vr{rows[c.r0].slot, c.Lp - c.n, c.n, rows[c.r0].q_row0};
+        const int32_t vi = static_cast<int32_t>(rows.size());
+        rows.push_back(vr);
+        for (int32_t q0 = 0; q0 < c.n; q0 += TQ)
+            for (int32_t sp = 0; sp < n_pref; ++sp)
+                w.ctiles.push_back({vi, q0, sp, part0 + q0 * stride, stride});
+        for (int32_t t = 0; t < c.n; ++t) {
+            const int32_t r = c.r0 + t;
+            RowDesc &rd = rows[r];
+            const int32_t n_suf = ceil_div(rd.past_len + rd.n_q - c.Lp, S);
+            rd.k0 = c.Lp;
+            rd.s0 = n_pref;
+            const int32_t item = static_cast<int32_t>(w.merges.size());
+            w.merges.push_back({r, 0, part0 + t * stride, n_pref + n_suf});
+            for (int32_t j = 0; j + 1 < n_suf; ++j) w.units.push_back({r, 0, n_pref + j, item});
+            tail.push_back({r, 0, n_pref + n_suf - 1, item});
+            member[r] = 1;
+        }
+    }
+    return member;
+}
+
+void build_work(std::vector<RowDesc> &rows, int causal, int32_t S, int32_t head_dim,
+                int32_t group, WorkList &w, const std::vector<Cascade> &cas = {}) {
     std::vector<UnitDesc> tail;
     w.units.clear();
     w.tiles.clear();
+    w.ctiles.clear();
     w.merges.clear();
     w.pmerges.clear();
     w.n_part = 0;
+    const int32_t n_real = static_cast<int32_t>(rows.size());
+    const std::vector<char> member = add_cascades(rows, cas, S, group, w, tail);
     const bool tc_shape = prefill_shape(head_dim, group);
     const int32_t TQ = tc_shape ? 128 / group : 0;
     const int32_t Sp = S * kPrefillSplitFactor;
-    for (int32_t r = 0; r < static_cast<int32_t>(rows.size()); ++r) {
+    for (int32_t r = 0; r < n_real; ++r) {
+        if (member[r]) continue;
         const RowDesc &rd = rows[r];
         const int32_t total_k = rd.past_len + rd.n_q;
         if (tc_shape && rd.n_q >= kPrefillMinQueries) {
@@ -552,11 +653,32 @@ int run_layer(pkv_seq *const *seqs, int32_t M, const int32_t *n_q, const float *
 
     WorkList w;
     const int32_t S = g_split_keys.load();
-    if (attend) build_work(rows, causal, S, head_dim, n_heads / n_kv_heads, w);
     const int32_t group = attend ? n_heads / n_kv_heads : 0;
-    const bool fuse = attend && g_fused_append.load() != 0 && w.tiles.empty() && !w.units.empty() &&
+    std::vector<Cascade> cas;
+    if (attend && g_cascade.load() != 0 && prefill_shape(head_dim, group))
+        cas = find_cascades(seqs, M, n_q, p->bs);
+    if (attend) build_work(rows, causal, S, head_dim, group, w, cas);
+    const bool fuse = attend && g_fused_append.load() != 0 && w.tiles.empty() && w.ctiles.empty() &&
+                      !w.units.empty() &&
                       head_dim == 128 && (group == 1 || group == 2 || group == 4) &&
                       dirty_within_appends(p, seqs, M, n_q);
+
+    if (attend) {
+        int64_t pairs = 0, ppairs = 0;
+        for (int32_t r = 0; r < M; ++r) {
+            const RowDesc &rd = rows[r];
+            if (rd.n_q < kPrefillMinQueries || !prefill_shape(head_dim, group)) continue;
+            const int64_t n = rd.n_q, b = rd.past_len;
+            pairs += causal ? n * b + n * (n + 1) / 2 : n * (b + n);
+        }
+        for (const Cascade &c : cas) ppairs += static_cast<int64_t>(c.n) * c.Lp;
+        const int64_t vals[PKV_WORK_FIELDS] = {static_cast<int64_t>(w.units.size()),
+                                               static_cast<int64_t>(w.tiles.size()),
+                                               static_cast<int64_t>(w.ctiles.size()),
+                                               static_cast<int64_t>(w.merges.size()),
+                                               pairs, ppairs, fuse ? 1 : 0};
+        std::copy(vals, vals + PKV_WORK_FIELDS, p->last_work);
+    }
 
     Blob &blob = p->blob;
     blob.clear();
@@ -569,6 +691,7 @@ int run_layer(pkv_seq *const *seqs, int32_t M, const int32_t *n_q, const float *
     const size_t app_off = blob.put(app.data(), app.size());
     const size_t units_off = blob.put(w.units.data(), w.units.size());
     const size_t tiles_off = blob.put(w.tiles.data(), w.tiles.size());
+    const size_t ctiles_off = blob.put(w.ctiles.data(), w.ctiles.size());
     const size_t merges_off = blob.put(w.merges.data(), w.merges.size());
 
     cudaError_t e = upload_blob(p);
@@ -648,6 +771,14 @@ int run_layer(pkv_seq *const *seqs, int32_t M, const int32_t *n_q, const float *
                              p->err_dev};
         e = launch(PKV_KERNEL_PREFILL, st, [&] { return launch_prefill_paged(pa, addr, st); });
         if (e != cudaSuccess) return cuda_fail(e, "prefill kernel");
+    }
+    if (!w.ctiles.empty()) {
+        // shared prefixes: every member query sees all Lp prefix keys
+        const PrefillArgs pa{Qd, Od, a.rows, dptr<PrefillTile>(p, ctiles_off),
+                             static_cast<int32_t>(w.ctiles.size()), a.pm, a.pl, a.pacc, n_heads,
+                             n_kv_heads, a.group, 0, S, a.scale_log2, p->err_dev};
+        e = launch(PKV_KERNEL_PREFILL, st, [&] { return launch_prefill_paged(pa, addr, st); });
+        if (e != cudaSuccess) return cuda_fail(e, "shared-prefix kernel");
     }
     if (!w.units.empty()) {
         e = launch(PKV_KERNEL_DECODE, st, [&] { return launch_decode_paged(a, addr, st); });
@@ -784,6 +915,13 @@ int pkv_pool_set_stream(pkv_pool *p, pkv_stream_t stream) {
 
 float *pkv_pool_k_data(const pkv_pool *p) { return p ? p->k : nullptr; }
 float *pkv_pool_v_data(const pkv_pool *p) { return p ? p->v : nullptr; }
+int pkv_pool_last_work(const pkv_pool *p, int64_t *out, int32_t cap) {
+    if (!p || !out || cap < 0) return fail(PKV_ERR_ARG, "NULL pool or output");
+    const int32_t n = std::min<int32_t>(cap, PKV_WORK_FIELDS);
+    std::copy(p->last_work, p->last_work + n, out);
+    return PKV_OK;
+}
+
 int32_t pkv_pool_free_blocks(const pkv_pool *p) {
     return p ? static_cast<int32_t>(p->free_stack.size()) : -1;
 }
@@ -1177,6 +1315,12 @@ int pkv_set_fused_append(int32_t on) {
 }
 int32_t pkv_get_fused_append(void) { return g_fused_append.load(); }
 
+int pkv_set_cascade(int32_t on) {
+    g_cascade.store(on ? 1 : 0);
+    return PKV_OK;
+}
+int32_t pkv_get_cascade(void) { return g_cascade.load(); }
+
 int64_t pkv_launch_count(void) { return g_launches.load(); }
 
 int pkv_profile_enable(int32_t on) {
@@ -1214,8 +1358,8 @@ void build_contig_work(int32_t n_q, int32_t total_k, int32_t causal, int32_t spl
                        std::vector<PrefillTile> &tiles, std::vector<MergeDesc> &merges,
                        int64_t *n_part) {
     WorkList w;
-    build_work(std::vector<RowDesc>{{0, total_k - n_q, n_q, 0}}, causal, split_keys, head_dim,
-               group, w);
+    std::vector<RowDesc> rows{{0, total_k - n_q, n_q, 0}};
+    build_work(rows, causal, split_keys, head_dim, group, w);
     units.swap(w.units);
     tiles.swap(w.tiles);
     merges.swap(w.merges);

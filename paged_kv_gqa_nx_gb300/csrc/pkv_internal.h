@@ -15,6 +15,11 @@ struct RowDesc {
     int32_t past_len;  // tokens committed before this call (seq_len)
     int32_t n_q;       // rows appended and attended by this call
     int32_t q_row0;    // first of this row's rows in Q / K_new / V_new / out
+    // Shared-prefix (cascade) rows: keys [0, k0) were attended by a prefix
+    // pass whose partials are the first s0 records of the query's merge item;
+    // the row's decode unit of split s covers k0 + (s - s0) * S .. (S keys).
+    // 0, 0 for every other row.
+    int32_t k0 = 0, s0 = 0;
 };
 
 // One split-K work unit: query qi of row `row`, keys [split*S, (split+1)*S)
@@ -88,9 +93,12 @@ struct AttnArgs {
 // One tensor-core prefill tile: queries q0 .. q0 + 128/G - 1 of row `row`
 // (clipped to n_q), key split `split` of size PrefillArgs::split_keys.
 // part0 < 0: the tile's queries have one split and write out directly;
-// otherwise query q0 + t's partial for split s is record part0 + t*n_split + s.
+// otherwise query q0 + t's partial for split s is record
+// part0 + t*stride + s, stride = n_split unless the tile sets it (a prefix
+// pass leaves room for the decode splits that follow each query's prefix).
 struct PrefillTile {
     int32_t row, q0, split, part0;
+    int32_t stride = 0;
 };
 
 struct PrefillArgs {

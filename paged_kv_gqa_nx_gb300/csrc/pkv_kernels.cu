@@ -126,7 +126,7 @@ __device__ __forceinline__ UnitRange unit_range(const UnitDesc &u, const RowDesc
     const int total_k = rd.past_len + rd.n_q;
     const int q_pos = total_k - rd.n_q + u.qi;  // offset-causal query position
     const int lim = causal ? q_pos + 1 : total_k;
-    const int kbeg = u.split * split_keys;
+    const int kbeg = rd.k0 + (u.split - rd.s0) * split_keys;
     const int kend = min(kbeg + split_keys, lim);
     return {kbeg, kend};
 }

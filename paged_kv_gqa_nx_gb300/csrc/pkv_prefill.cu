@@ -512,7 +512,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs a, 
                       static_cast<size_t>(h) * kHD + kDCols * qp;
             } else {
                 const int n_split = (kend_tile + a.split_keys - 1) / a.split_keys;
-                ph = static_cast<size_t>(tile.part0 + (valid ? tq : 0) * n_split + tile.split) * a.n_heads + h;
+                const int stride = tile.stride > 0 ? tile.stride : n_split;
+                ph = static_cast<size_t>(tile.part0 + (valid ? tq : 0) * stride + tile.split) * a.n_heads + h;
                 dst = a.pacc + ph * kHD + kDCols * qp;
             }
             const float scl = direct ? 1.f / l_run : 1.f;

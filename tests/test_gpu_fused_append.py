@@ -74,6 +74,7 @@ def _run(fused, lens, n_q, steps, n_layers=2, bs=16, seed=7, fork_tail=False, sp
         torch.cuda.synchronize()
         pkv.pkv_profile_enable(False)
         counts = {k: pkv.pkv_profile_read(k)[1] for k in range(pkv.PKV_KERNEL_KINDS)}
+        counts["work"] = pkv.pkv_pool_last_work(pool.p)
         pkv.check(pkv.pkv_sync_error(pool.p))
         # the device page table is checked through the steps themselves: every
         # page a step enters is read back through it by the next step
@@ -107,6 +108,7 @@ def test_fused_append_is_bit_exact_across_pages_and_splits(fused_mode):
     assert fused[4][pkv.PKV_KERNEL_APPEND] == 0
     assert plain[4][pkv.PKV_KERNEL_APPEND] == 3 * 2
     assert fused[4][pkv.PKV_KERNEL_DECODE] == plain[4][pkv.PKV_KERNEL_DECODE] == 3 * 2
+    assert fused[4]["work"]["fused_append"] == 1 and plain[4]["work"]["fused_append"] == 0
 
 
 @pytest.mark.gpu
