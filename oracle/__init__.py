@@ -15,6 +15,8 @@ Contents
                       (``contiguous_cache.py``).
 ``PoolModel``         the pool / page-table / refcount metadata model
                       (``pool_model.py``).
+``rope_neox``         rotary position embedding, NeoX pairing, float64
+                      (``rope.py``).
 
 Every function cites the passage of the pages it follows; the pages are the
 source listings "nx_f32_attn_paged.nx source", "nx_f32_gqa_attention.nx
@@ -112,6 +114,7 @@ def attend(Q, K, V, n_q: int, total_k: int, n_heads: int, n_kv_heads: int,
 from .contiguous_cache import ContiguousCache  # noqa: E402
 from .pool_model import PoolModel, SeqModel  # noqa: E402
 from . import pool_model  # noqa: E402
+from .rope import rope_neox  # noqa: E402
 
 __all__ = ["attend", "build", "ContiguousCache", "PoolModel", "SeqModel", "pool_model",
            "OK", "ERR_BAD_DIM", "ERR_BAD_GQA"]
