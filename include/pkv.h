@@ -209,11 +209,30 @@ PKV_API int pkv_attn_with_paged(const float *Q, const float *K_new, const float 
  * row r owns n_q[r] consecutive rows of Q / K_new / V_new / out, in batch
  * order.  n_q[r] = 1 for decode rows; n_q[r] > 1 is a chunked-prefill row
  * (offset-causal).  n_q is a host array.  Each row's result equals the M = 1
- * call on that row bit for bit.  Errors as pkv_attn_with_paged; duplicate
- * sequences -> PKV_ERR_ARG. */
+ * call on that row bit for bit, except rows of a shared-prefix group (see
+ * pkv_set_cascade), which agree with it within f32 rounding.  Errors as
+ * pkv_attn_with_paged; duplicate sequences -> PKV_ERR_ARG. */
 PKV_API int pkv_attn_batch(pkv_seq *const *seqs, int32_t M, const int32_t *n_q, const float *Q,
                    const float *K_new, const float *V_new, int32_t n_heads, int32_t n_kv_heads,
                    int32_t head_dim, int32_t layer, int32_t causal, float scale, float *out);
+
+/* pkv_attn_batch with rotary position embedding on append ("nx_f32_llama_v4b.nx
+ * source", Block section, RoPE step: each row's position is its sequence's
+ * length, the build-cs / apply-cs-neox pair applied to every query head and
+ * every new key head before the attend call).  Row t of batch row r sits at
+ * position p = len(r) + t; for every head and i < head_dim/2 the pair
+ * (x[i], x[i + head_dim/2]) turns by the angle p * rope_base^(-2i/head_dim):
+ *   x'[i] = x[i] cos - x[i+h/2] sin,  x'[i+h/2] = x[i] sin + x[i+h/2] cos,
+ * with cos and sin of the angle computed in double precision and rounded to
+ * f32.  The rotated keys go into the pool (V is not rotated); the rotated
+ * queries are library scratch; the caller's Q and K_new are left unchanged.
+ * rope_base must be > 0 (PKV_ERR_ARG) and head_dim even (PKV_ERR_BAD_DIM);
+ * the pages pass the base as an integer (rope_log_base).  Calls with RoPE keep
+ * the separate append launch (no fused append). */
+PKV_API int pkv_attn_batch_rope(pkv_seq *const *seqs, int32_t M, const int32_t *n_q, const float *Q,
+                        const float *K_new, const float *V_new, int32_t n_heads,
+                        int32_t n_kv_heads, int32_t head_dim, int32_t layer, int32_t causal,
+                        float scale, double rope_base, float *out);
 
 /* pkv_attn_batch taking HOST buffers for Q, K_new, V_new and out: copies the
  * inputs to device staging, runs the batch, copies out back, and returns when

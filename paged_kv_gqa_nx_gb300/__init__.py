@@ -87,6 +87,8 @@ _SIGS = {
     "pkv_attn_with_paged": (_int, [_vp, _vp, _vp, _i32, _i32, _i32, _i32, _vp, _i32, _i32, _f32, _vp]),
     "pkv_attn_batch": (_int, [_vp, _i32, _pi32, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _f32, _vp]),
     "pkv_attn_batch_host": (_int, [_vp, _i32, _pi32, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _f32, _vp]),
+    "pkv_attn_batch_rope": (_int, [_vp, _i32, _pi32, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _f32,
+                                   ctypes.c_double, _vp]),
     "pkv_attn_contiguous": (_int, [_vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _f32, _vp, _vp]),
     "pkv_attn_contiguous_noalloc": (_int, [_vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _f32, _vp, _vp]),
     "pkv_sync_error": (_int, [_vp]),
@@ -294,6 +296,14 @@ def pkv_attn_batch(seqs, n_q, Q, K_new, V_new, n_heads, n_kv_heads, head_dim, la
     return _lib.pkv_attn_batch(_seq_array(seqs), len(seqs), _i32_array(n_q), _dev(Q, "Q"),
                                _dev(K_new, "K_new"), _dev(V_new, "V_new"), n_heads, n_kv_heads,
                                head_dim, layer, causal, scale, _dev(out, "out"))
+
+
+def pkv_attn_batch_rope(seqs, n_q, Q, K_new, V_new, n_heads, n_kv_heads, head_dim, layer, causal,
+                        scale, rope_base, out):
+    return _lib.pkv_attn_batch_rope(_seq_array(seqs), len(seqs), _i32_array(n_q), _dev(Q, "Q"),
+                                    _dev(K_new, "K_new"), _dev(V_new, "V_new"), n_heads,
+                                    n_kv_heads, head_dim, layer, causal, scale, float(rope_base),
+                                    _dev(out, "out"))
 
 
 def pkv_attn_batch_host(seqs, n_q, Q, K_new, V_new, n_heads, n_kv_heads, head_dim, layer, causal,

@@ -275,7 +275,7 @@ struct pkv_pool {
     std::vector<pkv_seq *> dirty;      // sequences with page-table entries not yet uploaded
 
     Stager stager;
-    DevBuf desc, part, io_in, io_out;
+    DevBuf desc, part, io_in, io_out, qrot;
     Blob blob;
 
     int64_t block_floats() const { return static_cast<int64_t>(n_layers) * bs * kv_dim; }
@@ -588,7 +588,7 @@ const T *dptr(const pkv_pool *p, size_t off) {
 int run_layer(pkv_seq *const *seqs, int32_t M, const int32_t *n_q, const float *Q,
               const float *K_new, const float *V_new, int32_t n_heads, int32_t n_kv_heads,
               int32_t head_dim, int32_t layer, int32_t causal, float scale, float *out,
-              bool host_io, bool attend) {
+              bool host_io, bool attend, double rope_base = 0.0) {
     // checks in the order of nx_f32_attn_with_paged: sizes, grouping, sequence
     if (M <= 0 || !n_q) return fail(PKV_ERR_BAD_DIM, "M must be positive and n_q non-NULL");
     for (int32_t r = 0; r < M; ++r)
@@ -596,6 +596,9 @@ int run_layer(pkv_seq *const *seqs, int32_t M, const int32_t *n_q, const float *
     if (attend) {
         int rc = check_heads(n_heads, n_kv_heads, head_dim);
         if (rc) return rc;
+        if (rope_base < 0.0 || (rope_base > 0.0 && (head_dim % 2) != 0))
+            return fail(rope_base < 0.0 ? PKV_ERR_ARG : PKV_ERR_BAD_DIM,
+                        "RoPE needs a positive base and an even head_dim");
     }
     if (!seqs) return fail(PKV_ERR_SEQ, "seqs is NULL");
     for (int32_t r = 0; r < M; ++r)
@@ -658,8 +661,8 @@ int run_layer(pkv_seq *const *seqs, int32_t M, const int32_t *n_q, const float *
     if (attend && g_cascade.load() != 0 && prefill_shape(head_dim, group))
         cas = find_cascades(seqs, M, n_q, p->bs);
     if (attend) build_work(rows, causal, S, head_dim, group, w, cas);
-    const bool fuse = attend && g_fused_append.load() != 0 && w.tiles.empty() && w.ctiles.empty() &&
-                      !w.units.empty() &&
+    const bool fuse = attend && rope_base == 0.0 && g_fused_append.load() != 0 && w.tiles.empty() &&
+                      w.ctiles.empty() && !w.units.empty() &&
                       head_dim == 128 && (group == 1 || group == 2 || group == 4) &&
                       dirty_within_appends(p, seqs, M, n_q);
 
@@ -729,6 +732,16 @@ int run_layer(pkv_seq *const *seqs, int32_t M, const int32_t *n_q, const float *
     pr.V_new = Vd;
     pr.vec4 = (kv_dim % 4) == 0 && aligned16(Kd) && aligned16(Vd);
     pr.err = p->err_dev;
+    if (attend && rope_base > 0.0) {
+        e = p->qrot.ensure(static_cast<size_t>(T) * q_dim * sizeof(float), st, p->device);
+        if (e != cudaSuccess) return cuda_fail(e, "rotated-query buffer");
+        pr.rope_base = rope_base;
+        pr.Q = Qd;
+        pr.Q_rot = static_cast<float *>(p->qrot.p);
+        pr.q_dim = q_dim;
+        pr.hd = head_dim;
+        Qd = pr.Q_rot;  // the attention kernels read the rotated queries
+    }
     if (!fuse) {
         e = launch(PKV_KERNEL_APPEND, st, [&] { return launch_prep(pr, addr, st); });
         if (e != cudaSuccess) return cuda_fail(e, "prep kernel");
@@ -1167,6 +1180,15 @@ int pkv_attn_batch(pkv_seq *const *seqs, int32_t M, const int32_t *n_q, const fl
                    int32_t head_dim, int32_t layer, int32_t causal, float scale, float *out) {
     return run_layer(seqs, M, n_q, Q, K_new, V_new, n_heads, n_kv_heads, head_dim, layer, causal,
                      scale, out, false, true);
+}
+
+int pkv_attn_batch_rope(pkv_seq *const *seqs, int32_t M, const int32_t *n_q, const float *Q,
+                        const float *K_new, const float *V_new, int32_t n_heads, int32_t n_kv_heads,
+                        int32_t head_dim, int32_t layer, int32_t causal, float scale,
+                        double rope_base, float *out) {
+    if (!(rope_base > 0.0)) return fail(PKV_ERR_ARG, "RoPE base must be positive");
+    return run_layer(seqs, M, n_q, Q, K_new, V_new, n_heads, n_kv_heads, head_dim, layer, causal,
+                     scale, out, false, true, rope_base);
 }
 
 int pkv_attn_batch_host(pkv_seq *const *seqs, int32_t M, const int32_t *n_q, const float *Q_host,

@@ -133,6 +133,13 @@ struct PrepArgs {
     const float *K_new, *V_new;
     bool vec4;
     int32_t *err;
+    // RoPE on append (rope_base > 0): K rows are rotated on their way into
+    // the pool and Q rows into Q_rot, at position AppendDesc::pos; pairs
+    // (i, i + hd/2) turn by pos * rope_base^(-2i/hd).
+    double rope_base = 0.0;
+    const float *Q = nullptr;
+    float *Q_rot = nullptr;
+    int32_t q_dim = 0, hd = 0;
 };
 
 // Kernel launchers (pkv_kernels.cu).  Each enqueues exactly one kernel.

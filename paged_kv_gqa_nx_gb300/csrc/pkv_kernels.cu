@@ -180,6 +180,45 @@ __global__ void append_rows_kernel(const float *__restrict__ K_new, const float 
 // other blocks append the new rows (8 warps per block, one warp per row and K
 // or V; the destination block comes from the host's page table).
 
+// RoPE (NeoX pairing) of one appended row, all heads: K into its pool row,
+// or Q into Q_rot.  Lane l takes the pairs (i, i + hd/2) for i = l, l + 32,
+// ..., the angle pos * base^(-2i/hd) and its cosine and sine computed in
+// double precision and rounded to f32 once.
+__device__ void rope_row(const PrepArgs &p, const PagedAddr &a, const AppendDesc &d, bool is_q,
+                         int lane) {
+    const int half = p.hd >> 1;
+    const float *src;
+    float *dst;
+    int n_heads;
+    if (is_q) {
+        src = p.Q + static_cast<size_t>(d.src_row) * p.q_dim;
+        dst = p.Q_rot + static_cast<size_t>(d.src_row) * p.q_dim;
+        n_heads = p.q_dim / p.hd;
+    } else {
+        if (static_cast<unsigned>(d.blk) >= static_cast<unsigned>(a.n_blocks)) {
+            if (lane == 0) flag_error(p.err, 1);
+            return;
+        }
+        const int off = a.bs_shift >= 0 ? (d.pos & (a.bs - 1)) : (d.pos % a.bs);
+        src = p.K_new + static_cast<size_t>(d.src_row) * a.kv_dim;
+        dst = a.k + static_cast<size_t>(d.blk) * a.block_stride + a.layer_off +
+              static_cast<size_t>(off) * a.kv_dim;
+        n_heads = a.kv_dim / p.hd;
+    }
+    const double lb = log(p.rope_base);
+    for (int i = lane; i < half; i += 32) {
+        const double ang = static_cast<double>(d.pos) * exp(-2.0 * i / p.hd * lb);
+        double sd, cd;
+        sincos(ang, &sd, &cd);
+        const float c = static_cast<float>(cd), sn = static_cast<float>(sd);
+        for (int h = 0; h < n_heads; ++h) {
+            const float x0 = src[h * p.hd + i], x1 = src[h * p.hd + i + half];
+            dst[h * p.hd + i] = x0 * c - x1 * sn;
+            dst[h * p.hd + i + half] = x0 * sn + x1 * c;
+        }
+    }
+}
+
 __global__ void prep_kernel(PrepArgs p, PagedAddr a) {
     int b = blockIdx.x;
     if (b < p.n_runs) {
@@ -189,13 +228,20 @@ __global__ void prep_kernel(PrepArgs p, PagedAddr a) {
         return;
     }
     b -= p.n_runs;
-    const int app_blocks = (2 * p.n_app + 7) / 8;
+    const bool rope = p.rope_base > 0.0;
+    const int per_row = rope ? 3 : 2;  // warps per appended row: K, V (, Q)
+    const int app_blocks = (per_row * p.n_app + 7) / 8;
     if (b < app_blocks) {
         const int gw = b * 8 + (threadIdx.x >> 5);
         const int lane = threadIdx.x & 31;
-        if (gw >= 2 * p.n_app) return;
-        const AppendDesc d = p.app[gw >> 1];
-        const bool is_v = gw & 1;
+        if (gw >= per_row * p.n_app) return;
+        const AppendDesc d = p.app[gw / per_row];
+        const int role = gw - (gw / per_row) * per_row;  // 0 K, 1 V, 2 Q
+        if (rope && role != 1) {
+            rope_row(p, a, d, role == 2, lane);
+            return;
+        }
+        const bool is_v = role == 1;
         if (static_cast<unsigned>(d.blk) >= static_cast<unsigned>(a.n_blocks)) {
             if (lane == 0) flag_error(p.err, 1);
             return;
@@ -749,7 +795,7 @@ cudaError_t launch_pt_apply(int32_t *pt_dev, int32_t max_blocks, const PtRun *ru
 }
 
 cudaError_t launch_prep(const PrepArgs &p, const PagedAddr &addr, cudaStream_t s) {
-    const long long app_blocks = (2LL * p.n_app + 7) / 8;
+    const long long app_blocks = ((p.rope_base > 0.0 ? 3LL : 2LL) * p.n_app + 7) / 8;
     const long long grid = p.n_runs + app_blocks;
     if (grid <= 0) return cudaSuccess;
     if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
