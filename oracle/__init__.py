@@ -17,6 +17,8 @@ Contents
                       (``pool_model.py``).
 ``rope_neox``         rotary position embedding, NeoX pairing, float64
                       (``rope.py``).
+``round_bf16``        the bf16 pool's rounding of stored rows (nearest,
+                      ties to even; ``kv_format.py``).
 
 Every function cites the passage of the pages it follows; the pages are the
 source listings "nx_f32_attn_paged.nx source", "nx_f32_gqa_attention.nx
@@ -115,6 +117,7 @@ from .contiguous_cache import ContiguousCache  # noqa: E402
 from .pool_model import PoolModel, SeqModel  # noqa: E402
 from . import pool_model  # noqa: E402
 from .rope import rope_neox  # noqa: E402
+from .kv_format import round_bf16  # noqa: E402
 
 __all__ = ["attend", "build", "ContiguousCache", "PoolModel", "SeqModel", "pool_model",
            "OK", "ERR_BAD_DIM", "ERR_BAD_GQA"]
