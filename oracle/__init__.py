@@ -116,7 +116,7 @@ def attend(Q, K, V, n_q: int, total_k: int, n_heads: int, n_kv_heads: int,
 from .contiguous_cache import ContiguousCache  # noqa: E402
 from .pool_model import PoolModel, SeqModel  # noqa: E402
 from . import pool_model  # noqa: E402
-from .rope import rope_neox  # noqa: E402
+from .rope import rope_neox, rope_neox_f32  # noqa: E402
 from .kv_format import round_bf16  # noqa: E402
 
 __all__ = ["attend", "build", "ContiguousCache", "PoolModel", "SeqModel", "pool_model",

@@ -40,3 +40,27 @@ def rope_neox(x, positions, head_dim: int, base: float) -> np.ndarray:
     y[..., :half] = a * c[:, None, :] - b * s[:, None, :]
     y[..., half:] = a * s[:, None, :] + b * c[:, None, :]
     return y.reshape(T, D)
+
+
+def rope_neox_f32(x, positions, head_dim: int, base: float) -> np.ndarray:
+    """The same rotation carried out in float32 the way the library's kernel
+    does it -- cos and sin of the float64 angle rounded to float32, each
+    product and each sum rounded to float32 -- for tests that must take the
+    same rounding decision downstream (a bf16 pool rounds the rotated keys).
+    Returns float32."""
+    x = np.asarray(x, dtype=np.float32)
+    T, D = x.shape
+    if head_dim % 2 != 0 or D % head_dim != 0:
+        raise ValueError("head_dim must be even and divide the row width")
+    half = head_dim // 2
+    i = np.arange(half, dtype=np.float64)
+    theta = float(base) ** (-2.0 * i / head_dim)
+    ang = np.asarray(positions, dtype=np.float64)[:, None] * theta[None, :]
+    c = np.cos(ang).astype(np.float32)[:, None, :]
+    s = np.sin(ang).astype(np.float32)[:, None, :]
+    xh = x.reshape(T, D // head_dim, head_dim)
+    a, b = xh[..., :half], xh[..., half:]
+    y = np.empty_like(xh)
+    y[..., :half] = (a * c) - (b * s)      # float32 operations, each rounded
+    y[..., half:] = (a * s) + (b * c)
+    return y.reshape(T, D)

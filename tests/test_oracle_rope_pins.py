@@ -90,3 +90,22 @@ def test_attention_over_rotated_rows_is_shift_invariant():
         assert rc == 0
         outs.append(o)
     np.testing.assert_allclose(outs[0], outs[1], atol=2e-6)
+
+
+def test_float32_form_agrees_with_the_definition():
+    # the float32 carrying-out differs from the float64 definition only by
+    # float32 rounding (a few ulps of the pair's magnitude), and is exact at
+    # position 0
+    rng = np.random.default_rng(5)
+    x = rng.standard_normal((6, 128)).astype(np.float32)
+    pos = np.array([0, 1, 17, 999, 12345, 30000])
+    y64 = oracle.rope_neox(x, pos, 64, 10000.0)
+    y32 = oracle.rope_neox_f32(x, pos, 64, 10000.0)
+    assert y32.dtype == np.float32
+    mag = np.abs(x).max()
+    assert np.max(np.abs(y32 - y64)) <= 4 * 2.0 ** -24 * 2 * mag
+    np.testing.assert_array_equal(y32[0], x[0])
+    # and a wrong pairing in the float32 form would not pass the worked values
+    e = np.eye(4, dtype=np.float32)
+    y = oracle.rope_neox_f32(e, [1] * 4, 4, 10000.0)
+    np.testing.assert_allclose(y[0], [np.cos(1.0), 0, np.sin(1.0), 0], atol=1e-7)
