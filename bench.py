@@ -167,7 +167,7 @@ class DeviceRun:
     """The workload resident on one GPU: pool, sequences with histories, and
     the per-layer step inputs."""
 
-    def __init__(self, w, rank=0):
+    def __init__(self, w, rank=0, kv_dtype="f32"):
         import torch
         import paged_kv_gqa_nx_gb300 as pkv
         from synth import workloads as wl
@@ -178,10 +178,14 @@ class DeviceRun:
         max_tok = w.max_tokens() + 2
         if w.name == "shared_prefix_forks":
             max_tok = int(w.extra["prefix"]) + 2 * 256 + 2
-        self.K = torch.empty((w.n_blocks, w.n_layers, bs, w.kv_dim), device=dev, dtype=torch.float32)
+        self.bf16 = kv_dtype == "bf16"
+        self.elem = 2 if self.bf16 else 4
+        self.K = torch.empty((w.n_blocks, w.n_layers, bs, w.kv_dim), device=dev,
+                             dtype=torch.bfloat16 if self.bf16 else torch.float32)
         self.V = torch.empty_like(self.K)
         self.pool = pkv.pkv_pool_new(w.n_blocks, w.n_layers, w.kv_dim, bs, self.K, self.V,
-                                     w.M + 8, -(-max_tok // bs) + 1, self.stream)
+                                     w.M + 8, -(-max_tok // bs) + 1, self.stream,
+                                     flags=pkv.PKV_POOL_BF16 if self.bf16 else 0)
         assert self.pool, pkv.pkv_last_error()
         # shuffle the free list through the public API
         ids = [pkv.pkv_alloc_block(self.pool) for _ in range(w.n_blocks)]
@@ -218,7 +222,7 @@ class DeviceRun:
         self.out = torch.empty((self.T, w.q_dim), device=dev, dtype=torch.float32)
         # algorithmic bytes: every visible K and V row read once per row and layer
         tk = [b + n for b, n in zip(self.base_len, self.n_q)]
-        self.kv_bytes_per_layer = float(sum(tk)) * w.kv_dim * 4 * 2
+        self.kv_bytes_per_layer = float(sum(tk)) * w.kv_dim * self.elem * 2
         self.kv_bytes = self.kv_bytes_per_layer * w.n_layers
         self.q_out_bytes = float(self.T) * w.q_dim * 4 * 2 * w.n_layers
         torch.cuda.synchronize()
@@ -234,9 +238,9 @@ class DeviceRun:
         pos = torch.arange(L, device=self.K.device)
         for layer in range(w.n_layers):
             self.K[pt[pos // w.block_size], layer, pos % w.block_size] = wl.normal(
-                (L, w.kv_dim), seed + 2 * layer, self.K.device)
+                (L, w.kv_dim), seed + 2 * layer, self.K.device).to(self.K.dtype)
             self.V[pt[pos // w.block_size], layer, pos % w.block_size] = wl.normal(
-                (L, w.kv_dim), seed + 2 * layer + 1, self.K.device)
+                (L, w.kv_dim), seed + 2 * layer + 1, self.K.device).to(self.V.dtype)
 
     def _chunk(self, seqs, ns, seed):
         from synth import workloads as wl
@@ -288,8 +292,8 @@ class DeviceRun:
             pt = torch.tensor(pkv.pkv_seq_page_table(self.seqs[r]), device=self.K.device,
                               dtype=torch.long)
             pos = torch.arange(L, device=self.K.device)
-            Kh = self.K[pt[pos // w.block_size], 0, pos % w.block_size].cpu().numpy()
-            Vh = self.V[pt[pos // w.block_size], 0, pos % w.block_size].cpu().numpy()
+            Kh = self.K[pt[pos // w.block_size], 0, pos % w.block_size].float().cpu().numpy()
+            Vh = self.V[pt[pos // w.block_size], 0, pos % w.block_size].float().cpu().numpy()
             o, n = int(offs[r]), self.n_q[r]
             res.append((Q[o:o + n], np.concatenate([Kh, K[o:o + n]]), np.concatenate([Vh, V[o:o + n]]),
                         n, L + n))
@@ -378,7 +382,7 @@ def run_pkv(args):
     if args.split_keys:
         pkv.check(pkv.pkv_set_split_keys(args.split_keys))
     w = get_workload(args.workload)
-    run = DeviceRun(w, rank)
+    run = DeviceRun(w, rank, args.kv_dtype)
     peak, peak_kind = measured_hbm_peak()
 
     for _ in range(args.warmup):
@@ -491,7 +495,7 @@ def run_pkv(args):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "f32",
+        "dtype": "f32" if not run.bf16 else "f32 math, bf16 K/V storage",
         "data": "synthetic (seeded N(0,1) K/V/Q, seeded length draws)",
         "config": {
             "workload": w.name,
@@ -575,6 +579,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time")
     ap.add_argument("--split-keys", type=int, default=0, help="keys per split-K unit (0: library default)")
+    ap.add_argument("--kv-dtype", choices=["f32", "bf16"], default="f32",
+                    help="K/V pool storage (bf16: rows rounded on write, f32 math)")
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)

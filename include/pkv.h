@@ -69,20 +69,26 @@ typedef void *pkv_stream_t; /* cudaStream_t */
 
 /* pkv_pool_new flags */
 #define PKV_POOL_HOST_ONLY 1u /* metadata only: no device memory, no device work */
+/* bf16 storage (no counterpart on the pages, which store f32): every K/V row
+ * is rounded to the nearest bfloat16 (ties to even) when it is written and
+ * widened to f32 when it is read; all arithmetic stays f32.  Halves the pool's
+ * bytes and the decode traffic.  Needs an even kv_dim.  The fused append is
+ * not used on such pools, and the contiguous twin stays f32. */
+#define PKV_POOL_BF16 2u
 
 /* ---------------------------------------------------------------- pool ---- */
 
 /* Create a refcounted block pool ("nx_paged_kv_gate.nx source", KAT section:
  * pool_new(n_blocks, n_layers, kv_dim)).  Device layout of each of the K and V
- * pools: f32 [n_blocks][n_layers][block_size][kv_dim]; a block holds block_size
- * consecutive token rows of every layer.  k_pool_dev / v_pool_dev: caller-owned
- * device buffers of that size (both non-NULL), or both NULL to let the library
- * allocate them.  max_seqs bounds the live sequences; max_blocks_per_seq bounds
+ * pools: [n_blocks][n_layers][block_size][kv_dim] elements, f32 (or bf16 with
+ * PKV_POOL_BF16); a block holds block_size consecutive token rows of every
+ * layer.  k_pool_dev / v_pool_dev: caller-owned 16-byte-aligned device buffers
+ * of that size (both non-NULL), or both NULL to let the library allocate them.  max_seqs bounds the live sequences; max_blocks_per_seq bounds
  * one page table.  The free list is a LIFO stack whose first pops are 0,1,2,...
  * Returns NULL on failure (bad sizes, out of memory).  With PKV_POOL_HOST_ONLY
  * the pool keeps metadata only and the device pointers / stream are ignored. */
 PKV_API pkv_pool *pkv_pool_new(int32_t n_blocks, int32_t n_layers, int32_t kv_dim, int32_t block_size,
-                       float *k_pool_dev, float *v_pool_dev, int32_t max_seqs,
+                       void *k_pool_dev, void *v_pool_dev, int32_t max_seqs,
                        int32_t max_blocks_per_seq, pkv_stream_t stream, uint32_t flags);
 
 /* Release the pool, every sequence still alive in it, and library-owned memory.
@@ -93,9 +99,10 @@ PKV_API void pkv_pool_free(pkv_pool *pool);
  * new stream's (e.g. by synchronising).  Returns PKV_OK or PKV_ERR_ARG. */
 PKV_API int pkv_pool_set_stream(pkv_pool *pool, pkv_stream_t stream);
 
-/* Device base addresses of the K and V pools (NULL for a host-only pool). */
-PKV_API float *pkv_pool_k_data(const pkv_pool *pool);
-PKV_API float *pkv_pool_v_data(const pkv_pool *pool);
+/* Device base addresses of the K and V pools (NULL for a host-only pool);
+ * f32 or bf16 elements as the pool was created. */
+PKV_API void *pkv_pool_k_data(const pkv_pool *pool);
+PKV_API void *pkv_pool_v_data(const pkv_pool *pool);
 
 /* Number of blocks on the free list, or -1 for NULL. */
 PKV_API int32_t pkv_pool_free_blocks(const pkv_pool *pool);
@@ -224,7 +231,7 @@ PKV_API int pkv_attn_batch(pkv_seq *const *seqs, int32_t M, const int32_t *n_q, 
  * (x[i], x[i + head_dim/2]) turns by the angle p * rope_base^(-2i/head_dim):
  *   x'[i] = x[i] cos - x[i+h/2] sin,  x'[i+h/2] = x[i] sin + x[i+h/2] cos,
  * with cos and sin of the angle computed in double precision and rounded to
- * f32.  The rotated keys go into the pool (V is not rotated); the rotated
+ * f32, and each product and sum rounded to f32 (no fused multiply-add).  The rotated keys go into the pool (V is not rotated); the rotated
  * queries are library scratch; the caller's Q and K_new are left unchanged.
  * rope_base must be > 0 (PKV_ERR_ARG) and head_dim even (PKV_ERR_BAD_DIM);
  * the pages pass the base as an integer (rope_log_base).  Calls with RoPE keep

@@ -29,6 +29,7 @@ PKV_ERR_CUDA = 7
 PKV_ERR_DEVICE_BOUNDS = 8
 
 PKV_POOL_HOST_ONLY = 1
+PKV_POOL_BF16 = 2
 PKV_NOALLOC_SCRATCH_BYTES = 16 << 20
 
 PKV_KERNEL_APPEND = 0
@@ -123,8 +124,9 @@ def _stream(s):
     return int(s.cuda_stream)
 
 
-def _dev(t, name="tensor"):
-    """Device address of a contiguous f32 CUDA tensor (or a raw int address)."""
+def _dev(t, name="tensor", dtypes=("float32",)):
+    """Device address of a contiguous CUDA tensor of one of `dtypes` (default
+    f32), or a raw int address."""
     if t is None:
         return None
     if isinstance(t, int):
@@ -132,8 +134,8 @@ def _dev(t, name="tensor"):
     import torch
     if not isinstance(t, torch.Tensor) or not t.is_cuda:
         raise TypeError("%s must be a CUDA tensor" % name)
-    if t.dtype != torch.float32 or not t.is_contiguous():
-        raise TypeError("%s must be a contiguous float32 tensor" % name)
+    if str(t.dtype).replace("torch.", "") not in dtypes or not t.is_contiguous():
+        raise TypeError("%s must be a contiguous %s tensor" % (name, " or ".join(dtypes)))
     return t.data_ptr()
 
 
@@ -189,8 +191,10 @@ def pkv_last_error() -> str:
 
 def pkv_pool_new(n_blocks, n_layers, kv_dim, block_size, k_pool=None, v_pool=None,
                  max_seqs=1024, max_blocks_per_seq=4096, stream=None, flags=0):
-    return _lib.pkv_pool_new(n_blocks, n_layers, kv_dim, block_size, _dev(k_pool, "k_pool"),
-                             _dev(v_pool, "v_pool"), max_seqs, max_blocks_per_seq,
+    """k_pool / v_pool: float32 tensors, or bfloat16 with flags |= PKV_POOL_BF16."""
+    want = ("bfloat16",) if flags & PKV_POOL_BF16 else ("float32",)
+    return _lib.pkv_pool_new(n_blocks, n_layers, kv_dim, block_size, _dev(k_pool, "k_pool", want),
+                             _dev(v_pool, "v_pool", want), max_seqs, max_blocks_per_seq,
                              _stream(stream), flags)
 
 

@@ -259,8 +259,9 @@ struct pkv_pool {
     int32_t n_blocks = 0, n_layers = 0, kv_dim = 0, bs = 0, bs_shift = -1;
     int32_t max_seqs = 0, max_blocks = 0;
     bool host_only = false;
-    float *k = nullptr, *v = nullptr;
+    void *k = nullptr, *v = nullptr;
     bool owns_kv = false;
+    bool bf16 = false;  // storage element: f32, or bf16 (PKV_POOL_BF16)
     int32_t *pt_dev = nullptr;
     int32_t *err_dev = nullptr;
     cudaStream_t stream = nullptr;
@@ -278,7 +279,8 @@ struct pkv_pool {
     DevBuf desc, part, io_in, io_out, qrot;
     Blob blob;
 
-    int64_t block_floats() const { return static_cast<int64_t>(n_layers) * bs * kv_dim; }
+    int64_t block_floats() const { return static_cast<int64_t>(n_layers) * bs * kv_dim; }  // elements
+    size_t elem_bytes() const { return bf16 ? 2 : 4; }
 };
 
 struct pkv_seq {
@@ -339,6 +341,7 @@ PagedAddr paged_addr(const pkv_pool *p, int32_t layer) {
     PagedAddr a;
     a.k = p->k;
     a.v = p->v;
+    a.bf16 = p->bf16 ? 1 : 0;
     a.pt = p->pt_dev;
     a.block_stride = p->block_floats();
     a.layer_off = static_cast<int64_t>(layer) * p->bs * p->kv_dim;
@@ -661,7 +664,7 @@ int run_layer(pkv_seq *const *seqs, int32_t M, const int32_t *n_q, const float *
     if (attend && g_cascade.load() != 0 && prefill_shape(head_dim, group))
         cas = find_cascades(seqs, M, n_q, p->bs);
     if (attend) build_work(rows, causal, S, head_dim, group, w, cas);
-    const bool fuse = attend && rope_base == 0.0 && g_fused_append.load() != 0 && w.tiles.empty() &&
+    const bool fuse = attend && rope_base == 0.0 && !p->bf16 && g_fused_append.load() != 0 && w.tiles.empty() &&
                       w.ctiles.empty() && !w.units.empty() &&
                       head_dim == 128 && (group == 1 || group == 2 || group == 4) &&
                       dirty_within_appends(p, seqs, M, n_q);
@@ -824,7 +827,7 @@ extern "C" {
 const char *pkv_last_error(void) { return g_last_error.c_str(); }
 
 pkv_pool *pkv_pool_new(int32_t n_blocks, int32_t n_layers, int32_t kv_dim, int32_t block_size,
-                       float *k_pool_dev, float *v_pool_dev, int32_t max_seqs,
+                       void *k_pool_dev, void *v_pool_dev, int32_t max_seqs,
                        int32_t max_blocks_per_seq, pkv_stream_t stream, uint32_t flags) {
     if (n_blocks <= 0 || n_layers <= 0 || kv_dim <= 0 || block_size <= 0 || max_seqs <= 0 ||
         max_blocks_per_seq <= 0) {
@@ -844,6 +847,12 @@ pkv_pool *pkv_pool_new(int32_t n_blocks, int32_t n_layers, int32_t kv_dim, int32
     p->max_seqs = max_seqs;
     p->max_blocks = max_blocks_per_seq;
     p->host_only = (flags & PKV_POOL_HOST_ONLY) != 0;
+    p->bf16 = (flags & PKV_POOL_BF16) != 0;
+    if (p->bf16 && (kv_dim % 2) != 0) {
+        fail(PKV_ERR_BAD_DIM, "a bf16 pool needs an even kv_dim");
+        delete p;
+        return nullptr;
+    }
     p->free_stack.resize(n_blocks);
     for (int32_t i = 0; i < n_blocks; ++i) p->free_stack[i] = n_blocks - 1 - i;
     p->refcnt.assign(n_blocks, 0);
@@ -864,7 +873,7 @@ pkv_pool *pkv_pool_new(int32_t n_blocks, int32_t n_layers, int32_t kv_dim, int32
         delete p;
         return nullptr;
     }
-    const size_t pool_bytes = static_cast<size_t>(n_blocks) * p->block_floats() * sizeof(float);
+    const size_t pool_bytes = static_cast<size_t>(n_blocks) * p->block_floats() * p->elem_bytes();
     if (k_pool_dev) {
         if (!aligned16(k_pool_dev) || !aligned16(v_pool_dev)) {
             fail(PKV_ERR_ARG, "pool buffers must be 16-byte aligned");
@@ -926,8 +935,8 @@ int pkv_pool_set_stream(pkv_pool *p, pkv_stream_t stream) {
     return PKV_OK;
 }
 
-float *pkv_pool_k_data(const pkv_pool *p) { return p ? p->k : nullptr; }
-float *pkv_pool_v_data(const pkv_pool *p) { return p ? p->v : nullptr; }
+void *pkv_pool_k_data(const pkv_pool *p) { return p ? p->k : nullptr; }
+void *pkv_pool_v_data(const pkv_pool *p) { return p ? p->v : nullptr; }
 int pkv_pool_last_work(const pkv_pool *p, int64_t *out, int32_t cap) {
     if (!p || !out || cap < 0) return fail(PKV_ERR_ARG, "NULL pool or output");
     const int32_t n = std::min<int32_t>(cap, PKV_WORK_FIELDS);
@@ -1128,7 +1137,8 @@ int pkv_ensure_append_batch(pkv_seq *const *seqs, int32_t M, const int32_t *n) {
     if (e != cudaSuccess) return cuda_fail(e, "copy list upload");
     e = launch(PKV_KERNEL_COPY, p->stream, [&] {
         return launch_copy_blocks(p->k, p->v, dptr<CopyDesc>(p, off), static_cast<int32_t>(copies.size()),
-                                  p->block_floats(), p->n_blocks, p->err_dev, p->stream);
+                                  p->block_floats() * static_cast<int64_t>(p->elem_bytes()) / 4,
+                                  p->n_blocks, p->err_dev, p->stream);
     });
     if (e != cudaSuccess) return cuda_fail(e, "copy-on-append kernel");
     return PKV_OK;

@@ -55,11 +55,12 @@ struct CopyDesc {
 // Address of a key/value row in the paged pool:
 //   pool[pt[slot][pos / bs]][layer][pos % bs][kv_head*hd ...]
 struct PagedAddr {
-    float *k, *v;
+    void *k, *v;           // pool storage: f32 elements, or bf16 when bf16 != 0
     int32_t *pt;           // written only by the fused append, for pages no reader of that launch uses
-    int64_t block_stride;  // floats per block: n_layers * bs * kv_dim
-    int64_t layer_off;     // floats to the layer: layer * bs * kv_dim
+    int64_t block_stride;  // elements per block: n_layers * bs * kv_dim
+    int64_t layer_off;     // elements to the layer: layer * bs * kv_dim
     int32_t kv_dim, bs, bs_shift, max_blocks, n_blocks;
+    int32_t bf16 = 0;      // storage element: 0 f32, 1 bf16 (rounded to nearest even on write)
 };
 
 // Address of a key/value row in a contiguous history: base[pos][kv_head*hd ...]
@@ -146,12 +147,9 @@ struct PrepArgs {
 cudaError_t launch_prep(const PrepArgs &a, const PagedAddr &addr, cudaStream_t s);
 cudaError_t launch_pt_apply(int32_t *pt_dev, int32_t max_blocks, const PtRun *runs, int32_t n_runs,
                             const int32_t *vals, cudaStream_t s);
-// vec4: rows are copied as float4 (kv_dim % 4 == 0 and K_new / V_new 16-byte aligned)
-cudaError_t launch_append(const float *K_new, const float *V_new, const AppendDesc *items,
-                          int32_t n_items, const PagedAddr &addr, bool vec4, int32_t *err,
-                          cudaStream_t s);
-cudaError_t launch_copy_blocks(float *k, float *v, const CopyDesc *items, int32_t n_items,
-                               int64_t block_floats, int32_t n_blocks, int32_t *err,
+// block_words: one block's K (or V) storage in 4-byte words
+cudaError_t launch_copy_blocks(void *k, void *v, const CopyDesc *items, int32_t n_items,
+                               int64_t block_words, int32_t n_blocks, int32_t *err,
                                cudaStream_t s);
 cudaError_t launch_decode_paged(const AttnArgs &a, const PagedAddr &addr, cudaStream_t s);
 cudaError_t launch_decode_contig(const AttnArgs &a, const ContigAddr &addr, cudaStream_t s);

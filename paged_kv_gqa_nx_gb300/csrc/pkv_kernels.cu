@@ -4,7 +4,6 @@
 //                 and scatter the layer's K_new / V_new rows into their blocks
 //                 (the append step of "nx_f32_attn_paged.nx source")
 //   pt_apply      page-table upload alone (pkv_pool_flush)
-//   append_rows   append alone
 //   copy_blocks   copy-on-append: duplicate shared blocks (every layer, K and V)
 //   decode_fast   split-K attention, head_dim 128, query group 1/2/4: one CTA
 //                 per (work unit, kv head); the whole GQA group of query heads
@@ -14,14 +13,17 @@
 //   merge_splits  log-sum-exp merge of the split partials
 //
 // The attention kernels are templates over an address functor: PagedAddr
-// reads rows through the page table, ContigAddr from a contiguous history.
+// reads rows through the page table (f32 or bf16 pool elements, widened to
+// f32 on load), ContigAddr from a contiguous f32 history.
 // Everything else -- the split boundaries (multiples of S keys), the tile
 // order, every reduction tree -- depends only on token positions, so the paged
 // and the contiguous instantiations return the same bits, and a batch row
 // returns the same bits as the same row launched alone.
+#include "pkv_elem.h"
 #include "pkv_internal.h"
 
 #include <cstdio>
+#include <type_traits>
 
 namespace pkv {
 namespace {
@@ -44,12 +46,14 @@ __device__ __forceinline__ void flag_error(int32_t *err, int code) {
 
 // ------------------------------------------------------------ addressing ----
 
+template <class E>
 struct PagedRows {
+    using Elem = E;
     PagedAddr a;
     // Row of (slot, pos) for kv head `kvh`; false (and the error flag) when the
     // page index or the block id is out of range -- the access is skipped.
-    __device__ __forceinline__ bool row(int slot, int pos, int kvh, int hd, const float *&kr,
-                                        const float *&vr, int32_t *err) const {
+    __device__ __forceinline__ bool row(int slot, int pos, int kvh, int hd, const E *&kr,
+                                        const E *&vr, int32_t *err) const {
         const int bi = a.bs_shift >= 0 ? (pos >> a.bs_shift) : (pos / a.bs);
         const int off = pos - bi * a.bs;
         if (bi >= a.max_blocks) {
@@ -63,8 +67,8 @@ struct PagedRows {
         }
         const size_t o = static_cast<size_t>(blk) * a.block_stride + a.layer_off +
                          static_cast<size_t>(off) * a.kv_dim + static_cast<size_t>(kvh) * hd;
-        kr = a.k + o;
-        vr = a.v + o;
+        kr = static_cast<const E *>(a.k) + o;
+        vr = static_cast<const E *>(a.v) + o;
         return true;
     }
     // Tiles of T positions starting at a multiple of T stay inside one block
@@ -90,8 +94,8 @@ struct PagedRows {
         const size_t o = static_cast<size_t>(blk) * a.block_stride + a.layer_off +
                          static_cast<size_t>(pos - bi * a.bs) * a.kv_dim + static_cast<size_t>(kvh) * hd;
         for (int i = lane; 4 * i < hd; i += 32) {
-            reinterpret_cast<float4 *>(a.k + o)[i] = __ldg(reinterpret_cast<const float4 *>(ks) + i);
-            reinterpret_cast<float4 *>(a.v + o)[i] = __ldg(reinterpret_cast<const float4 *>(vs) + i);
+            store4(static_cast<E *>(a.k) + o + 4 * i, ldg4(ks + 4 * i));
+            store4(static_cast<E *>(a.v) + o + 4 * i, ldg4(vs + 4 * i));
         }
         if (set_pt && lane == 0) a.pt[static_cast<size_t>(slot) * a.max_blocks + bi] = blk;
         return true;
@@ -99,6 +103,7 @@ struct PagedRows {
 };
 
 struct ContigRows {
+    using Elem = float;
     ContigAddr a;
     __device__ __forceinline__ bool row(int, int pos, int kvh, int hd, const float *&kr,
                                         const float *&vr, int32_t *) const {
@@ -142,37 +147,6 @@ __global__ void pt_apply_kernel(int32_t *pt, int32_t max_blocks, const PtRun *ru
 
 // ----------------------------------------------------------------- append ----
 
-// One warp per (token row, K or V).
-__global__ void append_rows_kernel(const float *__restrict__ K_new, const float *__restrict__ V_new,
-                                   const AppendDesc *__restrict__ items, int32_t n_items,
-                                   PagedAddr a, bool vec4, int32_t *err) {
-    const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    const int lane = threadIdx.x & 31;
-    if (gw >= 2 * n_items) return;
-    const AppendDesc d = items[gw >> 1];
-    const bool is_v = gw & 1;
-    const int bi = a.bs_shift >= 0 ? (d.pos >> a.bs_shift) : (d.pos / a.bs);
-    const int off = d.pos - bi * a.bs;
-    if (bi >= a.max_blocks) {
-        if (lane == 0) flag_error(err, 1);
-        return;
-    }
-    const int blk = a.pt[static_cast<size_t>(d.slot) * a.max_blocks + bi];
-    if (static_cast<unsigned>(blk) >= static_cast<unsigned>(a.n_blocks)) {
-        if (lane == 0) flag_error(err, 1);
-        return;
-    }
-    float *dst = (is_v ? a.v : a.k) + static_cast<size_t>(blk) * a.block_stride + a.layer_off +
-                 static_cast<size_t>(off) * a.kv_dim;
-    const float *src = (is_v ? V_new : K_new) + static_cast<size_t>(d.src_row) * a.kv_dim;
-    if (vec4) {
-        const float4 *s4 = reinterpret_cast<const float4 *>(src);
-        float4 *d4 = reinterpret_cast<float4 *>(dst);
-        for (int i = lane; i < (a.kv_dim >> 2); i += 32) d4[i] = __ldg(s4 + i);
-    } else {
-        for (int i = lane; i < a.kv_dim; i += 32) dst[i] = src[i];
-    }
-}
 
 // ------------------------------------------------------------------- prep ----
 //
@@ -183,12 +157,13 @@ __global__ void append_rows_kernel(const float *__restrict__ K_new, const float 
 // RoPE (NeoX pairing) of one appended row, all heads: K into its pool row,
 // or Q into Q_rot.  Lane l takes the pairs (i, i + hd/2) for i = l, l + 32,
 // ..., the angle pos * base^(-2i/hd) and its cosine and sine computed in
-// double precision and rounded to f32 once.
+// double precision and rounded to f32 once; the rotation is f32.
 __device__ void rope_row(const PrepArgs &p, const PagedAddr &a, const AppendDesc &d, bool is_q,
                          int lane) {
     const int half = p.hd >> 1;
     const float *src;
-    float *dst;
+    float *dst = nullptr;       // the rotated queries
+    size_t dst_off = 0;         // or the key row in the pool (f32 or bf16 elements)
     int n_heads;
     if (is_q) {
         src = p.Q + static_cast<size_t>(d.src_row) * p.q_dim;
@@ -201,8 +176,8 @@ __device__ void rope_row(const PrepArgs &p, const PagedAddr &a, const AppendDesc
         }
         const int off = a.bs_shift >= 0 ? (d.pos & (a.bs - 1)) : (d.pos % a.bs);
         src = p.K_new + static_cast<size_t>(d.src_row) * a.kv_dim;
-        dst = a.k + static_cast<size_t>(d.blk) * a.block_stride + a.layer_off +
-              static_cast<size_t>(off) * a.kv_dim;
+        dst_off = static_cast<size_t>(d.blk) * a.block_stride + a.layer_off +
+                  static_cast<size_t>(off) * a.kv_dim;
         n_heads = a.kv_dim / p.hd;
     }
     const double lb = log(p.rope_base);
@@ -213,8 +188,21 @@ __device__ void rope_row(const PrepArgs &p, const PagedAddr &a, const AppendDesc
         const float c = static_cast<float>(cd), sn = static_cast<float>(sd);
         for (int h = 0; h < n_heads; ++h) {
             const float x0 = src[h * p.hd + i], x1 = src[h * p.hd + i + half];
-            dst[h * p.hd + i] = x0 * c - x1 * sn;
-            dst[h * p.hd + i + half] = x0 * sn + x1 * c;
+            // products and sums each rounded to f32 (no contraction), so the
+            // value that a bf16 pool rounds is reproducible
+            const float y0 = __fsub_rn(__fmul_rn(x0, c), __fmul_rn(x1, sn));
+            const float y1 = __fadd_rn(__fmul_rn(x0, sn), __fmul_rn(x1, c));
+            const size_t o0 = static_cast<size_t>(h) * p.hd + i, o1 = o0 + half;
+            if (dst) {
+                dst[o0] = y0;
+                dst[o1] = y1;
+            } else if (a.bf16) {
+                store1(static_cast<bf16 *>(a.k) + dst_off + o0, y0);
+                store1(static_cast<bf16 *>(a.k) + dst_off + o1, y1);
+            } else {
+                store1(static_cast<float *>(a.k) + dst_off + o0, y0);
+                store1(static_cast<float *>(a.k) + dst_off + o1, y1);
+            }
         }
     }
 }
@@ -247,21 +235,29 @@ __global__ void prep_kernel(PrepArgs p, PagedAddr a) {
             return;
         }
         const int off = a.bs_shift >= 0 ? (d.pos & (a.bs - 1)) : (d.pos % a.bs);
-        float *dst = (is_v ? a.v : a.k) + static_cast<size_t>(d.blk) * a.block_stride + a.layer_off +
-                     static_cast<size_t>(off) * a.kv_dim;
+        const size_t o = static_cast<size_t>(d.blk) * a.block_stride + a.layer_off +
+                         static_cast<size_t>(off) * a.kv_dim;
         const float *src = (is_v ? p.V_new : p.K_new) + static_cast<size_t>(d.src_row) * a.kv_dim;
-        if (p.vec4) {
-            const float4 *s4 = reinterpret_cast<const float4 *>(src);
-            float4 *d4 = reinterpret_cast<float4 *>(dst);
-            for (int i = lane; i < (a.kv_dim >> 2); i += 32) d4[i] = __ldg(s4 + i);
+        void *base = is_v ? a.v : a.k;
+        if (a.bf16) {
+            bf16 *dst = static_cast<bf16 *>(base) + o;
+            if (p.vec4)
+                for (int i = lane; i < (a.kv_dim >> 2); i += 32) store4(dst + 4 * i, ldg4(src + 4 * i));
+            else
+                for (int i = lane; i < a.kv_dim; i += 32) store1(dst + i, src[i]);
         } else {
-            for (int i = lane; i < a.kv_dim; i += 32) dst[i] = src[i];
+            float *dst = static_cast<float *>(base) + o;
+            if (p.vec4)
+                for (int i = lane; i < (a.kv_dim >> 2); i += 32) store4(dst + 4 * i, ldg4(src + 4 * i));
+            else
+                for (int i = lane; i < a.kv_dim; i += 32) dst[i] = src[i];
         }
     }
 }
 
 // ------------------------------------------------------------- block copy ----
 
+// Blocks are copied as 4-byte words (block_floats = the block's size in words).
 __global__ void copy_blocks_kernel(float *k, float *v, const CopyDesc *__restrict__ items,
                                    int64_t block_floats, int32_t n_blocks, int32_t *err) {
     const CopyDesc c = items[blockIdx.y];
@@ -360,20 +356,26 @@ __device__ __forceinline__ float4 fma4(float s, const float4 &v, const float4 &a
                        fmaf(s, v.w, acc.w));
 }
 
-template <int G, int NST>
+template <int G, int NST, class E>
 constexpr size_t fast_smem_bytes() {
     using C = FastCfg<G>;
-    return static_cast<size_t>(C::W) * NST * C::T * C::HD * 2 * sizeof(float) +
+    return static_cast<size_t>(C::W) * NST * C::T * C::HD * 2 * sizeof(E) +
            static_cast<size_t>(C::W) * (C::T + 1) * 4 * sizeof(float);
 }
 
 template <int G, int NST, class Rows>
 __global__ void __launch_bounds__(128, 3) decode_fast_kernel(AttnArgs a, Rows rows_of) {
     using C = FastCfg<G>;
+    using E = typename Rows::Elem;             // pool element (f32 or bf16)
     constexpr int HD = C::HD, T = C::T, W = C::W;
-    constexpr int STAGE = T * HD * 2;          // floats: K rows then V rows
-    constexpr int WARP_FLOATS = NST * STAGE;
-    extern __shared__ __align__(16) float sm[];
+    constexpr int EPC = 16 / static_cast<int>(sizeof(E));  // elements per 16-byte chunk
+    constexpr int CPR = HD / EPC;              // chunks per row: 32 (f32), 16 (bf16)
+    constexpr int STAGE = T * HD * 2;          // elements: K rows then V rows
+    constexpr int WARP_ELEMS = NST * STAGE;
+    static_assert(NST * STAGE * sizeof(E) >= (G * HD + 2 * G) * sizeof(float),
+                  "a warp's stage memory holds its (acc, m, l)");
+    extern __shared__ __align__(16) unsigned char smraw[];
+    E *sm = reinterpret_cast<E *>(smraw);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int kg = lane >> 3, c = lane & 7;
@@ -385,8 +387,8 @@ __global__ void __launch_bounds__(128, 3) decode_fast_kernel(AttnArgs a, Rows ro
     const int n_tiles = (ur.kend - ur.kbeg + T - 1) / T;
     const int my_n = warp < n_tiles ? (n_tiles - warp + W - 1) / W : 0;
 
-    float *wbase = sm + warp * WARP_FLOATS;
-    float *P = sm + W * WARP_FLOATS + warp * (T + 1) * 4;
+    E *wbase = sm + warp * WARP_ELEMS;
+    float *P = reinterpret_cast<float *>(sm + W * WARP_ELEMS) + warp * (T + 1) * 4;
 
     // query slice of the group, pre-scaled to base-2 units
     const float *qrow = a.Q + static_cast<size_t>(rd.q_row0 + u.qi) * (a.n_heads * HD) +
@@ -403,45 +405,49 @@ __global__ void __launch_bounds__(128, 3) decode_fast_kernel(AttnArgs a, Rows ro
 
     const bool whole = rows_of.whole_tiles(T);
     const size_t rstride = rows_of.row_stride();
-    // fused append: positions from past_len on come from K_new / V_new
-    const bool fused = a.K_new != nullptr;
+    // fused append (f32 pools): positions from past_len on come from K_new / V_new
+    constexpr bool kF32 = std::is_same<E, float>::value;
+    const bool fused = kF32 && a.K_new != nullptr;
     const int new0 = fused ? rd.past_len : 0x7fffffff;
-    auto row_ptrs = [&](int pos, const float *&kr, const float *&vr) {
-        if (pos >= new0) {
-            const size_t o = static_cast<size_t>(rd.q_row0 + (pos - new0)) * rstride +
-                             static_cast<size_t>(kvh) * HD;
-            kr = a.K_new + o;
-            vr = a.V_new + o;
-            return true;
+    auto row_ptrs = [&](int pos, const E *&kr, const E *&vr) {
+        if constexpr (kF32) {
+            if (pos >= new0) {
+                const size_t o = static_cast<size_t>(rd.q_row0 + (pos - new0)) * rstride +
+                                 static_cast<size_t>(kvh) * HD;
+                kr = a.K_new + o;
+                vr = a.V_new + o;
+                return true;
+            }
         }
         return rows_of.row(rd.slot, pos, kvh, HD, kr, vr, a.err);
+    };
+    // one key's K and V rows into the stage: 2 * CPR 16-byte chunks over the lanes
+    auto copy_rows = [&](E *Kd, E *Vd, const E *kr, const E *vr) {
+#pragma unroll
+        for (int ci = lane; ci < 2 * CPR; ci += 32) {
+            if (ci < CPR) cp_async16(Kd + ci * EPC, kr + ci * EPC);
+            else cp_async16(Vd + (ci - CPR) * EPC, vr + (ci - CPR) * EPC);
+        }
     };
     auto load_tile = [&](int k_local, int stage) {
         const int pos0 = ur.kbeg + (warp + k_local * W) * T;
         const int nv = min(T, ur.kend - pos0);
-        float *Ks = wbase + stage * STAGE;
-        float *Vs = Ks + T * HD;
+        E *Ks = wbase + stage * STAGE;
+        E *Vs = Ks + T * HD;
         if (whole && pos0 + T <= new0) {
             // one page-table lookup per tile
-            const float *kb, *vb;
+            const E *kb, *vb;
             if (rows_of.row(rd.slot, pos0, kvh, HD, kb, vb, a.err)) {
 #pragma unroll
-                for (int j = 0; j < T; ++j) {
-                    if (j < nv) {
-                        cp_async16(Ks + j * HD + lane * 4, kb + j * rstride + lane * 4);
-                        cp_async16(Vs + j * HD + lane * 4, vb + j * rstride + lane * 4);
-                    }
-                }
+                for (int j = 0; j < T; ++j)
+                    if (j < nv) copy_rows(Ks + j * HD, Vs + j * HD, kb + j * rstride, vb + j * rstride);
             }
         } else {
 #pragma unroll
             for (int j = 0; j < T; ++j) {
                 if (j < nv) {
-                    const float *kr, *vr;
-                    if (row_ptrs(pos0 + j, kr, vr)) {
-                        cp_async16(Ks + j * HD + lane * 4, kr + lane * 4);
-                        cp_async16(Vs + j * HD + lane * 4, vr + lane * 4);
-                    }
+                    const E *kr, *vr;
+                    if (row_ptrs(pos0 + j, kr, vr)) copy_rows(Ks + j * HD, Vs + j * HD, kr, vr);
                 }
             }
         }
@@ -449,7 +455,7 @@ __global__ void __launch_bounds__(128, 3) decode_fast_kernel(AttnArgs a, Rows ro
 
     // fused append: the unit of the row's last query stores the new rows of
     // its split into the pool (nothing in this launch reads them from there)
-    if (fused && u.qi == rd.n_q - 1) {
+    if (kF32 && fused && u.qi == rd.n_q - 1) {
         for (int pos = max(ur.kbeg, new0) + warp; pos < ur.kend; pos += W) {
             const int t = pos - new0;
             const AppendDesc ad = a.app[rd.q_row0 + t];
@@ -481,17 +487,16 @@ __global__ void __launch_bounds__(128, 3) decode_fast_kernel(AttnArgs a, Rows ro
 
         const int pos0 = ur.kbeg + (warp + k * W) * T;
         const int n_valid = min(T, ur.kend - pos0);
-        const float *Ks = wbase + (k % NST) * STAGE;
-        const float *Vs = Ks + T * HD;
+        const E *Ks = wbase + (k % NST) * STAGE;
+        const E *Vs = Ks + T * HD;
 
         float sc[2];
 #pragma unroll
         for (int it = 0; it < 2; ++it) {
             const int j = it * 4 + kg;
-            const float4 *K4 = reinterpret_cast<const float4 *>(Ks + j * HD);
             float4 kk[4];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) kk[i] = K4[c + 8 * i];
+            for (int i = 0; i < 4; ++i) kk[i] = load4(Ks + j * HD + 4 * (c + 8 * i));
             float part[G];
 #pragma unroll
             for (int g = 0; g < G; ++g) {
@@ -536,11 +541,10 @@ __global__ void __launch_bounds__(128, 3) decode_fast_kernel(AttnArgs a, Rows ro
             const float s = comp(al, g);
             acc[g] = make_float4(acc[g].x * s, acc[g].y * s, acc[g].z * s, acc[g].w * s);
         }
-        const float4 *V4 = reinterpret_cast<const float4 *>(Vs);
 #pragma unroll
         for (int j = 0; j < T; ++j) {
             if (j < n_valid) {
-                const float4 v = V4[j * 32 + lane];
+                const float4 v = load4(Vs + j * HD + 4 * lane);
                 const float4 pj = P4[j];
 #pragma unroll
                 for (int g = 0; g < G; ++g) acc[g] = fma4(comp(pj, g), v, acc[g]);
@@ -552,7 +556,8 @@ __global__ void __launch_bounds__(128, 3) decode_fast_kernel(AttnArgs a, Rows ro
     __syncwarp();
 
     // publish this warp's state in its own (now idle) stage memory
-    float *R = wbase;
+    float *R = reinterpret_cast<float *>(wbase);
+    auto Rw = [&](int w) { return reinterpret_cast<const float *>(sm + w * WARP_ELEMS); };
 #pragma unroll
     for (int g = 0; g < G; ++g) reinterpret_cast<float4 *>(R + g * HD)[lane] = acc[g];
     if (kg == 0 && (c % LPH) == 0) {
@@ -568,7 +573,7 @@ __global__ void __launch_bounds__(128, 3) decode_fast_kernel(AttnArgs a, Rows ro
         float M = -INFINITY;
 #pragma unroll
         for (int w = 0; w < W; ++w) {
-            mw[w] = sm[w * WARP_FLOATS + G * HD + g];
+            mw[w] = Rw(w)[G * HD + g];
             M = fmaxf(M, mw[w]);
         }
         float num = 0.f, den = 0.f;
@@ -576,8 +581,8 @@ __global__ void __launch_bounds__(128, 3) decode_fast_kernel(AttnArgs a, Rows ro
         for (int w = 0; w < W; ++w) {
             if (mw[w] != -INFINITY) {
                 const float wt = exp2f(mw[w] - M);
-                num = fmaf(wt, sm[w * WARP_FLOATS + g * HD + d], num);
-                den = fmaf(wt, sm[w * WARP_FLOATS + G * HD + G + g], den);
+                num = fmaf(wt, Rw(w)[g * HD + d], num);
+                den = fmaf(wt, Rw(w)[G * HD + G + g], den);
             }
         }
         const int h = kvh * G + g;
@@ -644,13 +649,13 @@ __global__ void __launch_bounds__(128) decode_generic_kernel(AttnArgs a, Rows ro
     }
     float *acc = accs + warp * hpc * hd;
     for (int j = ur.kbeg + warp; j < ur.kend; j += kGenW) {
-        const float *kr, *vr;
+        const typename Rows::Elem *kr, *vr;
         if (!rows_of.row(rd.slot, j, kvh, hd, kr, vr, a.err)) continue;
 #pragma unroll
         for (int g = 0; g < kGenMaxHeads; ++g) {
             if (g < nh) {
                 float part = 0.f;
-                for (int d = lane; d < hd; d += 32) part = fmaf(qs[g * hd + d], kr[d], part);
+                for (int d = lane; d < hd; d += 32) part = fmaf(qs[g * hd + d], to_f32(kr[d]), part);
 #pragma unroll
                 for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(kFull, part, o);
                 const float mn = fmaxf(m[g], part);
@@ -659,7 +664,7 @@ __global__ void __launch_bounds__(128) decode_generic_kernel(AttnArgs a, Rows ro
                 l[g] = fmaf(l[g], alpha, p);
                 m[g] = mn;
                 for (int d = lane; d < hd; d += 32)
-                    acc[g * hd + d] = fmaf(p, vr[d], acc[g * hd + d] * alpha);
+                    acc[g * hd + d] = fmaf(p, to_f32(vr[d]), acc[g * hd + d] * alpha);
             }
         }
     }
@@ -741,7 +746,7 @@ constexpr int kFastStages = PKV_FAST_STAGES;
 
 template <int G, class Rows>
 cudaError_t launch_fast(const AttnArgs &a, const Rows &r, cudaStream_t s) {
-    constexpr size_t smem = fast_smem_bytes<G, kFastStages>();
+    constexpr size_t smem = fast_smem_bytes<G, kFastStages, typename Rows::Elem>();
     static bool configured = false;  // per process; the attribute is per function
     if (!configured) {
         cudaError_t e = cudaFuncSetAttribute(decode_fast_kernel<G, kFastStages, Rows>,
@@ -803,19 +808,10 @@ cudaError_t launch_prep(const PrepArgs &p, const PagedAddr &addr, cudaStream_t s
     return cudaGetLastError();
 }
 
-cudaError_t launch_append(const float *K_new, const float *V_new, const AppendDesc *items,
-                          int32_t n_items, const PagedAddr &addr, bool vec4, int32_t *err,
-                          cudaStream_t s) {
-    if (n_items <= 0) return cudaSuccess;
-    const long long warps = 2LL * n_items;
-    const unsigned blocks = static_cast<unsigned>((warps + 7) / 8);
-    append_rows_kernel<<<blocks, 256, 0, s>>>(K_new, V_new, items, n_items, addr, vec4, err);
-    return cudaGetLastError();
-}
-
-cudaError_t launch_copy_blocks(float *k, float *v, const CopyDesc *items, int32_t n_items,
+cudaError_t launch_copy_blocks(void *kp, void *vp, const CopyDesc *items, int32_t n_items,
                                int64_t block_floats, int32_t n_blocks, int32_t *err,
                                cudaStream_t s) {
+    float *k = static_cast<float *>(kp), *v = static_cast<float *>(vp);
     if (n_items <= 0) return cudaSuccess;
     const long long per = (block_floats + 3) / 4;
     unsigned bx = static_cast<unsigned>((per + 255) / 256);
@@ -827,7 +823,8 @@ cudaError_t launch_copy_blocks(float *k, float *v, const CopyDesc *items, int32_
 }
 
 cudaError_t launch_decode_paged(const AttnArgs &a, const PagedAddr &addr, cudaStream_t s) {
-    return launch_decode(a, PagedRows{addr}, s);
+    if (addr.bf16) return launch_decode(a, PagedRows<bf16>{addr}, s);
+    return launch_decode(a, PagedRows<float>{addr}, s);
 }
 
 cudaError_t launch_decode_contig(const AttnArgs &a, const ContigAddr &addr, cudaStream_t s) {

@@ -34,6 +34,7 @@
 // The address functors mirror the decode kernels' (paged through the page
 // table, or contiguous), so the paged and contiguous instantiations return the
 // same bits.
+#include "pkv_elem.h"
 #include "pkv_internal.h"
 #include "pkv_tcgen05.h"
 
@@ -68,7 +69,9 @@ constexpr int kKPW = kKT / kComputeWarps;                   // K rows per warp p
 static_assert(kComputeWarps == 8 || kComputeWarps == 16, "8 or 16 compute warps");
 constexpr float kRescale = 8.f;               // lazy-rescale threshold (base 2)
 
+template <class E>
 struct PagedRowsP {
+    using Elem = E;
     PagedAddr a;
     // Block id of (slot, pos), or -1 (and the error flag) when the page index
     // or the id is out of range.
@@ -109,17 +112,18 @@ struct PagedRowsP {
         return static_cast<size_t>(blk) * a.block_stride + a.layer_off +
                static_cast<size_t>(off) * a.kv_dim + static_cast<size_t>(kvh) * kHD;
     }
-    __device__ __forceinline__ const float *k_row(int blk, int pos, int kvh) const {
-        return a.k + offset(blk, pos, kvh);
+    __device__ __forceinline__ const E *k_row(int blk, int pos, int kvh) const {
+        return static_cast<const E *>(a.k) + offset(blk, pos, kvh);
     }
-    __device__ __forceinline__ const float *v_row(int blk, int pos, int kvh) const {
-        return a.v + offset(blk, pos, kvh);
+    __device__ __forceinline__ const E *v_row(int blk, int pos, int kvh) const {
+        return static_cast<const E *>(a.v) + offset(blk, pos, kvh);
     }
     // groups of n positions starting at a multiple of n lie in one block
     __device__ __forceinline__ bool whole(int n) const { return (a.bs % n) == 0; }
 };
 
 struct ContigRowsP {
+    using Elem = float;
     ContigAddr a;
     __device__ __forceinline__ int block(int, int, int32_t *) const { return 0; }
     __device__ __forceinline__ int entry(int, int, int32_t *) const { return 0; }
@@ -305,7 +309,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs a, 
         const bool k_whole = rows_of.whole(kKPW);
         auto k_pos = [&](int kt) { return kt * kKT + warp * kKPW; };
         // row pointer of key pos (nullptr beyond the split or on a bad entry)
-        auto row_of = [&](int pos, int blk0, bool is_v) -> const float * {
+        using E = typename Rows::Elem;
+        auto row_of = [&](int pos, int blk0, bool is_v) -> const E * {
             if (pos >= kend) return nullptr;
             int b = blk0;
             if (!k_whole) b = rows_of.block(rd.slot, pos, a.err);
@@ -317,8 +322,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs a, 
             if (k_whole && pos0 < kend) blk0 = rows_of.checked(blk0, a.err);
 #pragma unroll
             for (int i = 0; i < kKPW; ++i) {
-                const float *kr = row_of(pos0 + i, blk0, false);
-                kreg[i] = kr ? __ldg(reinterpret_cast<const float4 *>(kr) + lane) : make_float4(0.f, 0.f, 0.f, 0.f);
+                const E *kr = row_of(pos0 + i, blk0, false);
+                kreg[i] = kr ? ldg4(kr + 4 * lane) : make_float4(0.f, 0.f, 0.f, 0.f);
             }
         };
         auto load_v = [&](int kt, int blk0) {
@@ -329,9 +334,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs a, 
                 float v[4][4];  // [key][c]
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
-                    const float *vr = row_of(pos0 + 4 * g4 + i, blk0, true);
+                    const E *vr = row_of(pos0 + 4 * g4 + i, blk0, true);
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) v[i][c] = vr ? __ldg(vr + lane + 32 * c) : 0.f;
+                    for (int c = 0; c < 4; ++c) v[i][c] = vr ? ldg1(vr + lane + 32 * c) : 0.f;
                 }
 #pragma unroll
                 for (int c = 0; c < 4; ++c) vq[g4][c] = make_float4(v[0][c], v[1][c], v[2][c], v[3][c]);
@@ -579,7 +584,8 @@ cudaError_t launch_prefill(const PrefillArgs &a, const Rows &r, cudaStream_t s) 
 }  // namespace
 
 cudaError_t launch_prefill_paged(const PrefillArgs &a, const PagedAddr &addr, cudaStream_t s) {
-    return launch_prefill(a, PagedRowsP{addr}, s);
+    if (addr.bf16) return launch_prefill(a, PagedRowsP<bf16>{addr}, s);
+    return launch_prefill(a, PagedRowsP<float>{addr}, s);
 }
 
 cudaError_t launch_prefill_contig(const PrefillArgs &a, const ContigAddr &addr, cudaStream_t s) {

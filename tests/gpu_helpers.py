@@ -40,13 +40,14 @@ class GpuPool:
     of a row nobody wrote poisons the output."""
 
     def __init__(self, n_blocks, n_layers, kv_dim, bs, max_seqs=64, max_blocks=4096,
-                 shuffle_seed=None, fill=float("nan")):
+                 shuffle_seed=None, fill=float("nan"), dtype=torch.float32):
         self.n_blocks, self.n_layers, self.kv_dim, self.bs = n_blocks, n_layers, kv_dim, bs
-        self.K = torch.full((n_blocks, n_layers, bs, kv_dim), fill, device="cuda", dtype=torch.float32)
+        self.K = torch.full((n_blocks, n_layers, bs, kv_dim), fill, device="cuda", dtype=dtype)
         self.V = torch.full_like(self.K, fill)
         self.stream = torch.cuda.current_stream()
+        flags = pkv.PKV_POOL_BF16 if dtype == torch.bfloat16 else 0
         self.p = pkv.pkv_pool_new(n_blocks, n_layers, kv_dim, bs, self.K, self.V, max_seqs,
-                                  max_blocks, self.stream)
+                                  max_blocks, self.stream, flags)
         assert self.p, pkv.pkv_last_error()
         if shuffle_seed is not None:
             ids = [pkv.pkv_alloc_block(self.p) for _ in range(n_blocks)]
@@ -71,8 +72,9 @@ class GpuPool:
         pos = torch.arange(start, start + L, device="cuda")
         blk = pt[pos // self.bs]
         off = pos % self.bs
-        self.K[blk, layer, off] = K_hist.to(device="cuda", dtype=torch.float32)
-        self.V[blk, layer, off] = V_hist.to(device="cuda", dtype=torch.float32)
+        # a bf16 pool stores torch's float32 -> bfloat16 cast (nearest, ties to even)
+        self.K[blk, layer, off] = K_hist.to(device="cuda", dtype=torch.float32).to(self.K.dtype)
+        self.V[blk, layer, off] = V_hist.to(device="cuda", dtype=torch.float32).to(self.V.dtype)
 
     def read_history(self, seq, layer, L):
         pt = torch.tensor(pkv.pkv_seq_page_table(seq), device="cuda", dtype=torch.long)
