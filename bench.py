@@ -224,6 +224,16 @@ class DeviceRun:
         tk = [b + n for b, n in zip(self.base_len, self.n_q)]
         self.kv_bytes_per_layer = float(sum(tk)) * w.kv_dim * self.elem * 2
         self.kv_bytes = self.kv_bytes_per_layer * w.n_layers
+        # unique bytes: distinct physical rows behind the visible positions
+        # (forks share prefix pages), plus each row's new positions
+        keys = []
+        for s_, L in zip(self.seqs, self.base_len):
+            if L:
+                pt = np.asarray(pkv.pkv_seq_page_table(s_), dtype=np.int64)
+                pos = np.arange(L, dtype=np.int64)
+                keys.append(pt[pos // bs] * bs + pos % bs)
+        n_unique = (np.unique(np.concatenate(keys)).size if keys else 0) + sum(self.n_q)
+        self.unique_kv_bytes = float(n_unique) * w.kv_dim * self.elem * 2 * w.n_layers
         self.q_out_bytes = float(self.T) * w.q_dim * 4 * 2 * w.n_layers
         torch.cuda.synchronize()
 
@@ -507,6 +517,8 @@ def run_pkv(args):
             "l2": "no flush: each step reads %.2f GB of K/V, far above the 129 MB L2" % (run.kv_bytes / 1e9),
         },
         "rows_layers_per_s": round(world * run.T * w.n_layers / (ms_step * 1e-3), 1),
+        "unique_kv_bytes_per_step": run.unique_kv_bytes,
+        "unique_kv_gbs": round(world * run.unique_kv_bytes * args.steps / (ms_total * 1e-3) / 1e9, 2),
         "frac_of_hbm_peak": round(value / world / peak, 4),
         "host_ms_per_step": round(host_s * 1e3 / args.steps, 4),
         "kernels_ms_per_step": {k: round(v[0] / args.steps, 4) for k, v in kern.items() if v[1]},
