@@ -339,7 +339,8 @@ enum pkv_kernel_kind {
     PKV_KERNEL_PREFILL = 3,
     PKV_KERNEL_COPY = 4,
     PKV_KERNEL_PAGETABLE = 5,
-    PKV_KERNEL_KINDS = 6
+    PKV_KERNEL_SPLIT = 6,  /* operand images for the tensor-core launches */
+    PKV_KERNEL_KINDS = 7
 };
 PKV_API int64_t pkv_launch_count(void);
 PKV_API int pkv_profile_enable(int32_t on);

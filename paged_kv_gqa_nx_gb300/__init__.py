@@ -38,8 +38,9 @@ PKV_KERNEL_MERGE = 2
 PKV_KERNEL_PREFILL = 3
 PKV_KERNEL_COPY = 4
 PKV_KERNEL_PAGETABLE = 5
-PKV_KERNEL_KINDS = 6
-KERNEL_NAMES = ["append", "decode", "merge", "prefill", "copy", "pagetable"]
+PKV_KERNEL_SPLIT = 6
+PKV_KERNEL_KINDS = 7
+KERNEL_NAMES = ["append", "decode", "merge", "prefill", "copy", "pagetable", "split"]
 
 
 class PkvError(RuntimeError):

@@ -276,7 +276,7 @@ struct pkv_pool {
     std::vector<pkv_seq *> dirty;      // sequences with page-table entries not yet uploaded
 
     Stager stager;
-    DevBuf desc, part, io_in, io_out, qrot;
+    DevBuf desc, part, io_in, io_out, qrot, img;
     Blob blob;
 
     int64_t block_floats() const { return static_cast<int64_t>(n_layers) * bs * kv_dim; }  // elements
@@ -686,6 +686,24 @@ int run_layer(pkv_seq *const *seqs, int32_t M, const int32_t *n_q, const float *
         std::copy(vals, vals + PKV_WORK_FIELDS, p->last_work);
     }
 
+    // operand images for the tensor-core launches: every 64-key tile of each
+    // row with prefill tiles (real rows and shared-prefix virtual rows)
+    std::vector<int32_t> img_tile0;
+    std::vector<SplitItem> split_items;
+    if (!w.tiles.empty() || !w.ctiles.empty()) {
+        img_tile0.assign(rows.size(), -1);
+        int32_t next = 0;
+        auto need = [&](int32_t r) {
+            if (img_tile0[r] >= 0) return;
+            const int32_t nt = ceil_div(rows[r].past_len + rows[r].n_q, kKeyTile);
+            img_tile0[r] = next;
+            next += nt;
+            for (int32_t kt = 0; kt < nt; ++kt) split_items.push_back({r, kt});
+        };
+        for (const PrefillTile &t : w.tiles) need(t.row);
+        for (const PrefillTile &t : w.ctiles) need(t.row);
+    }
+
     Blob &blob = p->blob;
     blob.clear();
     size_t runs_off = 0, vals_off = 0;
@@ -699,6 +717,8 @@ int run_layer(pkv_seq *const *seqs, int32_t M, const int32_t *n_q, const float *
     const size_t tiles_off = blob.put(w.tiles.data(), w.tiles.size());
     const size_t ctiles_off = blob.put(w.ctiles.data(), w.ctiles.size());
     const size_t merges_off = blob.put(w.merges.data(), w.merges.size());
+    const size_t tile0_off = blob.put(img_tile0.data(), img_tile0.size());
+    const size_t split_off = blob.put(split_items.data(), split_items.size());
 
     cudaError_t e = upload_blob(p);
     if (e != cudaSuccess) return cuda_fail(e, "descriptor upload");
@@ -780,19 +800,35 @@ int run_layer(pkv_seq *const *seqs, int32_t M, const int32_t *n_q, const float *
         a.pl = a.pm + pf;
         a.pacc = a.pl + pf;
     }
+    const unsigned char *img = nullptr;
+    if (!split_items.empty()) {
+        const size_t img_bytes = static_cast<size_t>(split_items.size()) * n_kv_heads * kImageBytes;
+        e = p->img.ensure(img_bytes, st, p->device);
+        if (e != cudaSuccess) return cuda_fail(e, "operand image buffer");
+        const SplitArgs sa{a.rows, dptr<SplitItem>(p, split_off), static_cast<int32_t>(split_items.size()),
+                           n_kv_heads, static_cast<unsigned char *>(p->img.p),
+                           dptr<int32_t>(p, tile0_off), p->err_dev};
+        e = launch(PKV_KERNEL_SPLIT, st, [&] { return launch_split_paged(sa, addr, st); });
+        if (e != cudaSuccess) return cuda_fail(e, "split kernel");
+        img = static_cast<const unsigned char *>(p->img.p);
+    }
     if (!w.tiles.empty()) {
-        const PrefillArgs pa{Qd, Od, a.rows, dptr<PrefillTile>(p, tiles_off),
-                             static_cast<int32_t>(w.tiles.size()), a.pm, a.pl, a.pacc, n_heads,
-                             n_kv_heads, a.group, a.causal, S * kPrefillSplitFactor, a.scale_log2,
-                             p->err_dev};
+        PrefillArgs pa{Qd, Od, a.rows, dptr<PrefillTile>(p, tiles_off),
+                       static_cast<int32_t>(w.tiles.size()), a.pm, a.pl, a.pacc, n_heads,
+                       n_kv_heads, a.group, a.causal, S * kPrefillSplitFactor, a.scale_log2,
+                       p->err_dev};
+        pa.img = img;
+        pa.img_tile0 = dptr<int32_t>(p, tile0_off);
         e = launch(PKV_KERNEL_PREFILL, st, [&] { return launch_prefill_paged(pa, addr, st); });
         if (e != cudaSuccess) return cuda_fail(e, "prefill kernel");
     }
     if (!w.ctiles.empty()) {
         // shared prefixes: every member query sees all Lp prefix keys
-        const PrefillArgs pa{Qd, Od, a.rows, dptr<PrefillTile>(p, ctiles_off),
-                             static_cast<int32_t>(w.ctiles.size()), a.pm, a.pl, a.pacc, n_heads,
-                             n_kv_heads, a.group, 0, S, a.scale_log2, p->err_dev};
+        PrefillArgs pa{Qd, Od, a.rows, dptr<PrefillTile>(p, ctiles_off),
+                       static_cast<int32_t>(w.ctiles.size()), a.pm, a.pl, a.pacc, n_heads,
+                       n_kv_heads, a.group, 0, S, a.scale_log2, p->err_dev};
+        pa.img = img;
+        pa.img_tile0 = dptr<int32_t>(p, tile0_off);
         e = launch(PKV_KERNEL_PREFILL, st, [&] { return launch_prefill_paged(pa, addr, st); });
         if (e != cudaSuccess) return cuda_fail(e, "shared-prefix kernel");
     }

@@ -112,6 +112,32 @@ struct PrefillArgs {
     int32_t n_heads, n_kv, group, causal, split_keys;
     float scale_log2;
     int32_t *err;
+    // Paged launches: the K/V operand images made by the split pass; row r's
+    // key tile kt for kv head h is image (img_tile0[r] + kt) * n_kv + h.
+    const unsigned char *img = nullptr;
+    const int32_t *img_tile0 = nullptr;
+};
+
+// The tensor-core kernel's operands for one (row, 64-key tile, kv head), as
+// they sit in its shared memory: K hi, K lo (K-major, 128-byte swizzle, four
+// k-blocks of 32 dims x 64 keys) and V^T hi, V^T lo (two k-blocks of 32 keys x
+// 128 dims).  f32 x = hi + lo, hi = x with the low 13 mantissa bits cleared.
+constexpr int32_t kKeyTile = 64;  // keys per tensor-core tile (and per image)
+constexpr uint32_t kImagePlane = 32 * 1024;
+constexpr uint32_t kImageBytes = 4 * kImagePlane;
+
+// One image to make: key tile kt of row `row` (all kv heads).
+struct SplitItem {
+    int32_t row, kt;
+};
+
+struct SplitArgs {
+    const RowDesc *rows;
+    const SplitItem *items;
+    int32_t n_items, n_kv;
+    unsigned char *img;
+    const int32_t *img_tile0;
+    int32_t *err;
 };
 
 struct MergeArgs {
@@ -156,6 +182,8 @@ cudaError_t launch_decode_contig(const AttnArgs &a, const ContigAddr &addr, cuda
 cudaError_t launch_merge(const MergeArgs &a, cudaStream_t s);
 // Tensor-core prefill (pkv_prefill.cu): head_dim 128, group 1, 2, 4 or 8.
 cudaError_t launch_prefill_paged(const PrefillArgs &a, const PagedAddr &addr, cudaStream_t s);
+// The split pass of the paged tensor-core launches: one image per item and kv head.
+cudaError_t launch_split_paged(const SplitArgs &a, const PagedAddr &addr, cudaStream_t s);
 cudaError_t launch_prefill_contig(const PrefillArgs &a, const ContigAddr &addr, cudaStream_t s);
 
 // Rows with at least this many queries take the tensor-core prefill kernel

@@ -45,6 +45,7 @@ using namespace tc;
 
 constexpr int kHD = 128;
 constexpr int kKT = 64;  // keys per tile
+static_assert(kKT == kKeyTile, "one image per tile");
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColQhi = 0, kColS = 128, kColPhi = 256, kColPlo = 320, kColD = 384;
 #ifndef PKV_PREFILL_COMPUTE_WARPS
@@ -62,6 +63,14 @@ constexpr int kIssueRegs = 32;                                 // issue warpgrou
 constexpr int kComputeRegs = kComputeWarps == 16 ? 112 : 232;  // compute warps after .inc
 static_assert(kCompute * kComputeRegs + 128 * kIssueRegs <= kThreads * kLaunchRegs,
               "register split exceeds the launch's registers");
+// with operand images the compute warps hold no prefetch registers and the
+// issue thread also runs the copies
+constexpr int kIssueRegsBulk = 80;
+constexpr int kComputeRegsBulk = kComputeWarps == 16 ? 96 : 184;
+static_assert(kCompute * kComputeRegsBulk + 128 * kIssueRegsBulk <= kThreads * kLaunchRegs,
+              "register split exceeds the launch's registers");
+static_assert(kComputeWarps != 16 || 4 * 32 * kComputeRegsBulk + 32 * kIssueRegsBulk <= 16384,
+              "register split exceeds one SM sub-partition");
 constexpr int kTPR = kComputeWarps / 4;                     // threads per tile row
 constexpr int kSCols = kKT / kTPR;                          // scores per thread per key tile
 constexpr int kDCols = kHD / kTPR;                          // output columns per thread
@@ -149,7 +158,9 @@ __device__ __forceinline__ void split4(const float4 &x, float4 &h, float4 &l) {
     split_tf32(x.w, h.w, l.w);
 }
 
-template <int G, class Rows>
+// kBulk: the K/V operands come as images (the split pass) by bulk copy,
+// issued by the MMA thread; otherwise the compute warps load and split them.
+template <int G, class Rows, bool kBulk>
 __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs a, Rows rows_of) {
     constexpr int TQ = 128 / G;  // tokens per tile
     extern __shared__ __align__(1024) unsigned char smraw[];
@@ -161,7 +172,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs a, 
     unsigned char *Vhi = Klo + kSmemK;
     unsigned char *Vlo = Vhi + kSmemV;
     // bar_qk / bar_pv: the MMAs of QK / PV completed (tcgen05.commit);
-    // bar_k / bar_p: the compute warps put the operands of QK / PV in place
+    // bar_k / bar_p: the operands of QK / PV are in place.  Register mode: the
+    // compute warps stored them.  Image mode: the compute warps read S (or, the
+    // first time, wrote Q) / wrote P, and the copy warp's K / V image landed.
     __shared__ uint64_t bar_qk, bar_pv, bar_k, bar_p;
     __shared__ uint32_t tslot;
     __shared__ float red[2][kCompute];
@@ -187,8 +200,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs a, 
     if (tid == 0) {
         mbar_init(smem_u32(&bar_qk), 1);
         mbar_init(smem_u32(&bar_pv), 1);
-        mbar_init(smem_u32(&bar_k), kComputeWarps);
-        mbar_init(smem_u32(&bar_p), kComputeWarps);
+        // with images the copy warp's expect-tx arrival joins each phase
+        mbar_init(smem_u32(&bar_k), kComputeWarps + (kBulk ? 1 : 0));
+        mbar_init(smem_u32(&bar_p), kComputeWarps + (kBulk ? 1 : 0));
     }
     fence_before_sync();
     __syncthreads();
@@ -197,10 +211,70 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs a, 
     bool ok = true;
 
     if (warp >= kComputeWarps) {
-        // the issue warpgroup: its first warp issues, the other three only give
-        // their registers back
-        setmaxnreg_dec<kIssueRegs>();
-        if (warp == kComputeWarps) {
+        // the issue warpgroup: its first warp issues the MMAs, in image mode
+        // its second warp runs the bulk copies; the rest only give their
+        // registers back
+        setmaxnreg_dec<kBulk ? kIssueRegsBulk : kIssueRegs>();
+        if (kBulk && warp == kComputeWarps + 1) {
+            // ---------------- copy warp (lane 0 copies) ----------------
+            // A K / V buffer is refilled as soon as the MMAs that read it are
+            // done, in the order the tensor core completes them: QK(kt0), then
+            // QK(kt+1), PV(kt), ...  Each copy arrives with its byte count on
+            // the operand barrier that the MMA warp waits on.
+            const unsigned char *img0 =
+                a.img + (static_cast<size_t>(a.img_tile0[tile.row]) * a.n_kv + kvh) * kImageBytes;
+            const size_t img_step = static_cast<size_t>(a.n_kv) * kImageBytes;
+            auto copy_k = [&](int kt) {
+                if (lane == 0) {
+                    const unsigned char *src = img0 + static_cast<size_t>(kt) * img_step;
+                    mbar_expect_tx(smem_u32(&bar_k), 2 * kImagePlane);
+                    bulk_g2s(smem_u32(Khi), src, kImagePlane, smem_u32(&bar_k));
+                    bulk_g2s(smem_u32(Klo), src + kImagePlane, kImagePlane, smem_u32(&bar_k));
+                }
+            };
+            auto copy_v = [&](int kt) {
+                if (lane == 0) {
+                    const unsigned char *src = img0 + static_cast<size_t>(kt) * img_step + 2 * kImagePlane;
+                    mbar_expect_tx(smem_u32(&bar_p), 2 * kImagePlane);
+                    bulk_g2s(smem_u32(Vhi), src, kImagePlane, smem_u32(&bar_p));
+                    bulk_g2s(smem_u32(Vlo), src + kImagePlane, kImagePlane, smem_u32(&bar_p));
+                }
+            };
+            auto wait_c = [&](uint64_t *bar, uint32_t &ph) {
+                const bool w = __shfl_sync(0xffffffffu, lane == 0 ? mbar_wait(smem_u32(bar), ph) : true, 0);
+                ph ^= 1;
+                return w;
+            };
+            uint32_t ph_qkd = 0, ph_pvd = 0;
+            bool cok = true;
+            if (kt0 < kt1) {
+                copy_k(kt0);
+                copy_v(kt0);
+                if (kt0 + 1 < kt1) {
+                    cok = wait_c(&bar_qk, ph_qkd);  // QK(kt0) done
+                    if (cok) copy_k(kt0 + 1);
+                }
+            }
+            for (int kt = kt0; kt + 1 < kt1 && cok; ++kt) {
+                if (kt + 2 < kt1) {
+                    cok = wait_c(&bar_qk, ph_qkd);  // QK(kt+1) done: the K buffer is free
+                    if (!cok) break;
+                    copy_k(kt + 2);
+                }
+                cok = wait_c(&bar_pv, ph_pvd);  // PV(kt) done: the V buffer is free
+                if (!cok) break;
+                copy_v(kt + 1);
+            }
+            // let the last copies land before the CTA's shared memory is given
+            // up (their phases also need the compute warps; bounded if those
+            // gave up)
+            if (kt0 < kt1) {
+                uint32_t last = static_cast<uint32_t>(kt1 - 1 - kt0) & 1u;
+                wait_c(&bar_k, last);
+                last = static_cast<uint32_t>(kt1 - 1 - kt0) & 1u;
+                wait_c(&bar_p, last);
+            }
+        } else if (warp == kComputeWarps) {
         // ---------------- MMA issue warp (lane 0 issues) ----------------
         const uint64_t dKhi = desc_sw128(smem_u32(Khi)), dKlo = desc_sw128(smem_u32(Klo));
         const uint64_t dQlo = desc_sw128(smem_u32(Qlo));
@@ -209,54 +283,76 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs a, 
         const uint32_t tPh = tbase + kColPhi, tPl = tbase + kColPlo;
         const uint32_t idesc_s = idesc_tf32(128, kKT), idesc_o = idesc_tf32(128, kHD);
         uint32_t ph_k = 0, ph_p = 0;
-        auto issue_qk = [&]() {
-            // operands: K of the tile (and, the first time, Q) in place
-            ok = __shfl_sync(0xffffffffu, lane == 0 ? mbar_wait(smem_u32(&bar_k), ph_k) : true, 0);
-            ph_k ^= 1;
-            if (!ok) return;
+        // one k-step of QK (8 dims) / PV (8 keys): three products of the split
+        auto qk_step = [&](int s) {
+            const uint64_t ko = ((s >> 2) * 8192u + (s & 3) * 32u) >> 4;
+            const uint64_t qo = ((s >> 2) * 16384u + (s & 3) * 32u) >> 4;
+            mma_tf32_ts(tS, tQ + 8 * s, dKhi + ko, idesc_s, s > 0);
+            mma_tf32_ts(tS, tQ + 8 * s, dKlo + ko, idesc_s, 1);
+            mma_tf32(tS, dQlo + qo, dKhi + ko, idesc_s, 1);
+        };
+        auto pv_step = [&](int s, bool first) {
+            const uint64_t vo = ((s >> 2) * 16384u + (s & 3) * 32u) >> 4;
+            mma_tf32_ts(tD, tPh + 8 * s, dVhi + vo, idesc_o, !first || s > 0);
+            mma_tf32_ts(tD, tPh + 8 * s, dVlo + vo, idesc_o, 1);
+            mma_tf32_ts(tD, tPl + 8 * s, dVhi + vo, idesc_o, 1);
+        };
+        // the MMAs of one tile (lane 0 issues, then commits); unrolled when the
+        // issue warpgroup has the registers for it (image mode)
+        auto mma_qk = [&]() {
             fence_after_sync();
             if (lane == 0) {
+                if constexpr (kBulk) {
+#pragma unroll
+                    for (int s = 0; s < 16; ++s) qk_step(s);
+                } else {
 #pragma unroll 1
-                for (int s = 0; s < 16; ++s) {
-                    const uint64_t ko = ((s >> 2) * 8192u + (s & 3) * 32u) >> 4;
-                    const uint64_t qo = ((s >> 2) * 16384u + (s & 3) * 32u) >> 4;
-                    mma_tf32_ts(tS, tQ + 8 * s, dKhi + ko, idesc_s, s > 0);
-                    mma_tf32_ts(tS, tQ + 8 * s, dKlo + ko, idesc_s, 1);
-                    mma_tf32(tS, dQlo + qo, dKhi + ko, idesc_s, 1);
+                    for (int s = 0; s < 16; ++s) qk_step(s);
                 }
                 mma_commit(smem_u32(&bar_qk));
             }
             __syncwarp();
         };
-        auto issue_pv = [&](bool first) {
-            // operands: P and V of the tile in place
-            ok = __shfl_sync(0xffffffffu, lane == 0 ? mbar_wait(smem_u32(&bar_p), ph_p) : true, 0);
-            ph_p ^= 1;
-            if (!ok) return;
+        auto mma_pv = [&](bool first) {
             fence_after_sync();
             if (lane == 0) {
+                if constexpr (kBulk) {
+#pragma unroll
+                    for (int s = 0; s < 8; ++s) pv_step(s, first);
+                } else {
 #pragma unroll 1
-                for (int s = 0; s < 8; ++s) {
-                    const uint64_t vo = ((s >> 2) * 16384u + (s & 3) * 32u) >> 4;
-                    mma_tf32_ts(tD, tPh + 8 * s, dVhi + vo, idesc_o, !first || s > 0);
-                    mma_tf32_ts(tD, tPh + 8 * s, dVlo + vo, idesc_o, 1);
-                    mma_tf32_ts(tD, tPl + 8 * s, dVhi + vo, idesc_o, 1);
+                    for (int s = 0; s < 8; ++s) pv_step(s, first);
                 }
                 mma_commit(smem_u32(&bar_pv));
             }
             __syncwarp();
         };
-        // order on the tensor core: QK(kt0), then per tile QK(kt+1) before PV(kt),
-        // so QK(kt+1) runs while the compute warps do the softmax of tile kt
-        if (kt0 < kt1) issue_qk();
+        // lane 0 waits (bounded), the warp learns the outcome
+        auto wait1 = [&](uint64_t *bar, uint32_t &ph) {
+            const bool w = __shfl_sync(0xffffffffu, lane == 0 ? mbar_wait(smem_u32(bar), ph) : true, 0);
+            ph ^= 1;
+            return w;
+        };
+        // order on the tensor core: QK(kt0), then per tile QK(kt+1) before
+        // PV(kt), so QK(kt+1) runs while the compute warps do the softmax
+        if (kt0 < kt1) {
+            ok = wait1(&bar_k, ph_k);  // K of the tile (and, the first time, Q) in place
+            if (ok) mma_qk();
+        }
         for (int kt = kt0; kt < kt1 && ok; ++kt) {
-            if (kt + 1 < kt1) issue_qk();
-            if (ok) issue_pv(kt == kt0);
+            if (kt + 1 < kt1) {
+                ok = wait1(&bar_k, ph_k);
+                if (!ok) break;
+                mma_qk();
+            }
+            ok = wait1(&bar_p, ph_p);  // P and V of the tile in place
+            if (!ok) break;
+            mma_pv(kt == kt0);
         }
         if (!ok && lane == 0 && a.err) atomicOr(a.err, 2);
         }
     } else {
-        setmaxnreg_inc<kComputeRegs>();
+        setmaxnreg_inc<kBulk ? kComputeRegsBulk : kComputeRegs>();
         // ---------------- compute warps: 4 threads per tile row ----------------
         const int wq = warp & 3;               // TMEM lane quadrant
         const int qp = warp >> 2;              // which quarter of the row this thread owns
@@ -399,15 +495,21 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs a, 
         uint32_t ph_qk = 0, ph_pv = 0;
 
         // prologue: K_kt0 in place (QK(kt0) may start), V_kt0 and K_kt0+1 in
-        // registers, the page-table entries of K_kt0+2 and V_kt0+1 on their way
-        load_k(kt0, lookup_k(kt0));
-        int vblk = lookup_v(kt0);
-        load_v(kt0, vblk);
-        store_k();
-        int kblk = kt0 + 1 < kt1 ? lookup_k(kt0 + 1) : -1;
+        // registers, the page-table entries of K_kt0+2 and V_kt0+1 on their way.
+        // With images (kBulk) the issue thread brings K and V in: Q only.
+        int vblk = -1, kblk = -1;
+        if constexpr (!kBulk) {
+            load_k(kt0, lookup_k(kt0));
+            vblk = lookup_v(kt0);
+            load_v(kt0, vblk);
+            store_k();
+            kblk = kt0 + 1 < kt1 ? lookup_k(kt0 + 1) : -1;
+        }
         arrive(&bar_k);
-        if (kt0 + 1 < kt1) load_k(kt0 + 1, kblk);
-        vblk = kt0 + 1 < kt1 ? lookup_v(kt0 + 1) : -1;
+        if constexpr (!kBulk) {
+            if (kt0 + 1 < kt1) load_k(kt0 + 1, kblk);
+            vblk = kt0 + 1 < kt1 ? lookup_v(kt0 + 1) : -1;
+        }
 
         for (int kt = kt0; kt < kt1; ++kt) {
             // S_kt ready (QK(kt) done: the K buffer is free again)
@@ -417,9 +519,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs a, 
             fence_after_sync();
             float s[kSCols];
             tmem_ldn<kSCols>(tbase + tlane + kColS + kSCols * qp, s);
-            // K_{kt+1} -> smem; the issue warp starts QK(kt+1) while we do the
-            // softmax, and the K_{kt+2} loads overlap it too
-            if (kt + 1 < kt1) {
+            if constexpr (kBulk) {
+                // S read: QK(kt+1) may overwrite it
+                if (kt + 1 < kt1) arrive(&bar_k);
+            } else if (kt + 1 < kt1) {
+                // K_{kt+1} -> smem; the issue warp starts QK(kt+1) while we do
+                // the softmax, and the K_{kt+2} loads overlap it too
                 store_k();
                 kblk = kt + 2 < kt1 ? lookup_k(kt + 2) : -1;
                 arrive(&bar_k);
@@ -492,15 +597,17 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs a, 
                 tmem_st_wait();
                 tmem_stn<kSCols>(tbase + tlane + kColPlo + kSCols * qp, s);
             }
-            store_v();
+            if constexpr (!kBulk) store_v();
             arrive(&bar_p);
 
             // registers for the next tile: V_{kt+1}
-            if (kt + 1 < kt1) {
-                load_v(kt + 1, vblk);
-                vblk = kt + 2 < kt1 ? lookup_v(kt + 2) : -1;
+            if constexpr (!kBulk) {
+                if (kt + 1 < kt1) {
+                    load_v(kt + 1, vblk);
+                    vblk = kt + 2 < kt1 ? lookup_v(kt + 2) : -1;
+                }
+                if (kt + 2 < kt1) load_k(kt + 2, kblk);
             }
-            if (kt + 2 < kt1) load_k(kt + 2, kblk);
         }
         // the last PV, then the result
         if (ok) ok = wait_one(&bar_pv, ph_pv);
@@ -546,7 +653,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs a, 
     if (warp == 0) tmem_dealloc(tbase, kTmemCols);
 }
 
-template <int G, class Rows>
+template <int G, class Rows, bool kBulk>
 cudaError_t launch_prefill_g(const PrefillArgs &a, const Rows &r, cudaStream_t s) {
     static bool configured = false;
     if (!configured) {
@@ -554,11 +661,11 @@ cudaError_t launch_prefill_g(const PrefillArgs &a, const Rows &r, cudaStream_t s
         // for, so launch only if the compiled kernel starts with the registers
         // the split was sized for
         cudaFuncAttributes fa{};
-        cudaError_t e = cudaFuncGetAttributes(&fa, prefill_tc_kernel<G, Rows>);
+        cudaError_t e = cudaFuncGetAttributes(&fa, prefill_tc_kernel<G, Rows, kBulk>);
         if (e != cudaSuccess) return e;
         if (fa.numRegs < kLaunchRegs || fa.maxThreadsPerBlock < kThreads)
             return cudaErrorInvalidConfiguration;
-        e = cudaFuncSetAttribute(prefill_tc_kernel<G, Rows>,
+        e = cudaFuncSetAttribute(prefill_tc_kernel<G, Rows, kBulk>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(kSmemBytes));
         if (e != cudaSuccess) return e;
@@ -566,30 +673,116 @@ cudaError_t launch_prefill_g(const PrefillArgs &a, const Rows &r, cudaStream_t s
     }
     const long long grid = static_cast<long long>(a.n_tiles) * a.n_kv;
     if (grid <= 0 || grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    prefill_tc_kernel<G, Rows><<<static_cast<unsigned>(grid), kThreads, kSmemBytes, s>>>(a, r);
+    prefill_tc_kernel<G, Rows, kBulk><<<static_cast<unsigned>(grid), kThreads, kSmemBytes, s>>>(a, r);
     return cudaGetLastError();
 }
 
-template <class Rows>
+template <class Rows, bool kBulk>
 cudaError_t launch_prefill(const PrefillArgs &a, const Rows &r, cudaStream_t s) {
     switch (a.group) {
-        case 1: return launch_prefill_g<1>(a, r, s);
-        case 2: return launch_prefill_g<2>(a, r, s);
-        case 4: return launch_prefill_g<4>(a, r, s);
-        case 8: return launch_prefill_g<8>(a, r, s);
+        case 1: return launch_prefill_g<1, Rows, kBulk>(a, r, s);
+        case 2: return launch_prefill_g<2, Rows, kBulk>(a, r, s);
+        case 4: return launch_prefill_g<4, Rows, kBulk>(a, r, s);
+        case 8: return launch_prefill_g<8, Rows, kBulk>(a, r, s);
         default: return cudaErrorInvalidValue;
     }
+}
+
+// ----------------------------------------------------------- split pass ----
+//
+// One CTA per (row, 64-key tile, kv head): the tile's K and V rows (read once
+// through the page table, widened to f32; zero past the row's keys) go to
+// shared memory, then every 16-byte chunk of the four operand planes is split
+// (hi = low 13 mantissa bits cleared, lo = the exact rest) and written in the
+// prefill kernel's shared-memory order, chunk by chunk (coalesced).  The V
+// rows are kept 129 floats apart so that reading them transposed has no bank
+// conflicts.
+constexpr int kSplitRawFloats = kKT * kHD + kKT * (kHD + 1);
+
+template <class E>
+__global__ void __launch_bounds__(256) split_kernel(SplitArgs p, PagedRowsP<E> rows_of) {
+    extern __shared__ __align__(16) float raw[];
+    float *rk = raw;              // [64][128]
+    float *rv = raw + kKT * kHD;  // [64][129]
+    const int it = blockIdx.x / p.n_kv;
+    const int kvh = blockIdx.x - it * p.n_kv;
+    const SplitItem t = p.items[it];
+    const RowDesc rd = p.rows[t.row];
+    const int total_k = rd.past_len + rd.n_q;
+    const int key0 = t.kt * kKT;
+    for (int i = threadIdx.x; i < kKT * (kHD / 4); i += blockDim.x) {
+        const int key = i >> 5, ch = i & 31, pos = key0 + key;
+        float4 kx = make_float4(0.f, 0.f, 0.f, 0.f), vx = kx;
+        if (pos < total_k) {
+            const int b = rows_of.checked(rows_of.entry(rd.slot, pos, p.err), p.err);
+            if (b >= 0) {
+                kx = ldg4(rows_of.k_row(b, pos, kvh) + 4 * ch);
+                vx = ldg4(rows_of.v_row(b, pos, kvh) + 4 * ch);
+            }
+        }
+        *reinterpret_cast<float4 *>(rk + key * kHD + 4 * ch) = kx;
+        float *vd = rv + key * (kHD + 1) + 4 * ch;
+        vd[0] = vx.x;
+        vd[1] = vx.y;
+        vd[2] = vx.z;
+        vd[3] = vx.w;
+    }
+    __syncthreads();
+    unsigned char *out =
+        p.img + (static_cast<size_t>(p.img_tile0[t.row] + t.kt) * p.n_kv + kvh) * kImageBytes;
+    for (int q = threadIdx.x; q < static_cast<int>(kImagePlane / 16); q += blockDim.x) {
+        float4 h, l;
+        {
+            // K: k-block q >> 9 (32 dims), key row (q >> 3) & 63, swizzled chunk q & 7
+            const int kb = q >> 9, r = (q >> 3) & 63, lc = (q & 7) ^ (r & 7);
+            split4(*reinterpret_cast<const float4 *>(rk + r * kHD + kb * 32 + lc * 4), h, l);
+            *reinterpret_cast<float4 *>(out + q * 16) = h;
+            *reinterpret_cast<float4 *>(out + kImagePlane + q * 16) = l;
+        }
+        {
+            // V^T: k-block q >> 10 (32 keys), dim row (q >> 3) & 127, swizzled chunk q & 7
+            const int kb = q >> 10, d = (q >> 3) & 127, lc = (q & 7) ^ (d & 7);
+            const int k0 = kb * 32 + lc * 4;
+            const float4 x = make_float4(rv[k0 * (kHD + 1) + d], rv[(k0 + 1) * (kHD + 1) + d],
+                                         rv[(k0 + 2) * (kHD + 1) + d], rv[(k0 + 3) * (kHD + 1) + d]);
+            split4(x, h, l);
+            *reinterpret_cast<float4 *>(out + 2 * kImagePlane + q * 16) = h;
+            *reinterpret_cast<float4 *>(out + 3 * kImagePlane + q * 16) = l;
+        }
+    }
+}
+
+template <class E>
+cudaError_t launch_split(const SplitArgs &a, const PagedRowsP<E> &r, cudaStream_t s) {
+    constexpr size_t smem = kSplitRawFloats * sizeof(float);
+    static bool configured = false;
+    if (!configured) {
+        cudaError_t e = cudaFuncSetAttribute(split_kernel<E>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(smem));
+        if (e != cudaSuccess) return e;
+        configured = true;
+    }
+    const long long grid = static_cast<long long>(a.n_items) * a.n_kv;
+    if (grid <= 0 || grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    split_kernel<E><<<static_cast<unsigned>(grid), 256, smem, s>>>(a, r);
+    return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_prefill_paged(const PrefillArgs &a, const PagedAddr &addr, cudaStream_t s) {
-    if (addr.bf16) return launch_prefill(a, PagedRowsP<bf16>{addr}, s);
-    return launch_prefill(a, PagedRowsP<float>{addr}, s);
+    // the operands come as images (whatever the pool element): one instantiation
+    if (!a.img || !a.img_tile0) return cudaErrorInvalidValue;
+    return launch_prefill<PagedRowsP<float>, true>(a, PagedRowsP<float>{addr}, s);
 }
 
 cudaError_t launch_prefill_contig(const PrefillArgs &a, const ContigAddr &addr, cudaStream_t s) {
-    return launch_prefill(a, ContigRowsP{addr}, s);
+    return launch_prefill<ContigRowsP, false>(a, ContigRowsP{addr}, s);
+}
+
+cudaError_t launch_split_paged(const SplitArgs &a, const PagedAddr &addr, cudaStream_t s) {
+    if (addr.bf16) return launch_split(a, PagedRowsP<bf16>{addr}, s);
+    return launch_split(a, PagedRowsP<float>{addr}, s);
 }
 
 }  // namespace pkv

@@ -104,6 +104,16 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 // wait is bounded (iterations and ~1 s of wall time); on expiry it returns
 // false and the caller bails out.
 __device__ __forceinline__ bool mbar_wait(uint32_t mbar, uint32_t parity) {
+    // a phase that has already completed costs one non-blocking test
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(done)
+        : "r"(mbar), "r"(parity)
+        : "memory");
+    if (done) return true;
     const uint64_t t0 = globaltimer_ns();
     for (uint32_t it = 0; it < (1u << 26); ++it) {
         uint32_t ok;
@@ -118,6 +128,23 @@ __device__ __forceinline__ bool mbar_wait(uint32_t mbar, uint32_t parity) {
         if ((it & 255u) == 255u && globaltimer_ns() - t0 > 1000000000ull) return false;
     }
     return false;
+}
+
+// Arrive once and add `bytes` to the transaction count the current phase waits
+// for (the bulk copies that complete_tx on this barrier bring them in).
+__device__ __forceinline__ void mbar_expect_tx(uint32_t mbar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(mbar), "r"(bytes)
+                 : "memory");
+}
+
+// Bulk copy (TMA, no tensor map) of `bytes` from global to this CTA's shared
+// memory; completes `bytes` of the barrier's transaction count.  Both
+// addresses 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t mbar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(dst),
+        "l"(src), "r"(bytes), "r"(mbar)
+        : "memory");
 }
 
 // Arrive once on an mbarrier (count-based).
