@@ -819,6 +819,7 @@ int run_layer(pkv_seq *const *seqs, int32_t M, const int32_t *n_q, const float *
                        p->err_dev};
         pa.img = img;
         pa.img_tile0 = dptr<int32_t>(p, tile0_off);
+        pa.lo_zero = p->bf16 ? 1 : 0;
         e = launch(PKV_KERNEL_PREFILL, st, [&] { return launch_prefill_paged(pa, addr, st); });
         if (e != cudaSuccess) return cuda_fail(e, "prefill kernel");
     }
@@ -829,6 +830,7 @@ int run_layer(pkv_seq *const *seqs, int32_t M, const int32_t *n_q, const float *
                        n_kv_heads, a.group, 0, S, a.scale_log2, p->err_dev};
         pa.img = img;
         pa.img_tile0 = dptr<int32_t>(p, tile0_off);
+        pa.lo_zero = p->bf16 ? 1 : 0;
         e = launch(PKV_KERNEL_PREFILL, st, [&] { return launch_prefill_paged(pa, addr, st); });
         if (e != cudaSuccess) return cuda_fail(e, "shared-prefix kernel");
     }

@@ -116,6 +116,9 @@ struct PrefillArgs {
     // key tile kt for kv head h is image (img_tile0[r] + kt) * n_kv + h.
     const unsigned char *img = nullptr;
     const int32_t *img_tile0 = nullptr;
+    // the images' lo planes are zero (a bf16 pool: every K/V value is exact
+    // in tf32), so the products with them and their copies are skipped
+    int32_t lo_zero = 0;
 };
 
 // The tensor-core kernel's operands for one (row, 64-key tile, kv head), as

@@ -38,6 +38,8 @@
 #include "pkv_internal.h"
 #include "pkv_tcgen05.h"
 
+#include <type_traits>
+
 namespace pkv {
 namespace {
 
@@ -158,9 +160,10 @@ __device__ __forceinline__ void split4(const float4 &x, float4 &h, float4 &l) {
     split_tf32(x.w, h.w, l.w);
 }
 
-// kBulk: the K/V operands come as images (the split pass) by bulk copy,
-// issued by the MMA thread; otherwise the compute warps load and split them.
-template <int G, class Rows, bool kBulk>
+// kBulk: the K/V operands come as images (the split pass) by bulk copy;
+// otherwise the compute warps load and split them.  kLoZero (images of a bf16
+// pool): the K / V lo planes are zero, so they are neither copied nor used.
+template <int G, class Rows, bool kBulk, bool kLoZero>
 __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs a, Rows rows_of) {
     constexpr int TQ = 128 / G;  // tokens per tile
     extern __shared__ __align__(1024) unsigned char smraw[];
@@ -224,20 +227,21 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs a, 
             const unsigned char *img0 =
                 a.img + (static_cast<size_t>(a.img_tile0[tile.row]) * a.n_kv + kvh) * kImageBytes;
             const size_t img_step = static_cast<size_t>(a.n_kv) * kImageBytes;
+            constexpr uint32_t planes = kLoZero ? 1u : 2u;  // hi (and lo) of K / V
             auto copy_k = [&](int kt) {
                 if (lane == 0) {
                     const unsigned char *src = img0 + static_cast<size_t>(kt) * img_step;
-                    mbar_expect_tx(smem_u32(&bar_k), 2 * kImagePlane);
+                    mbar_expect_tx(smem_u32(&bar_k), planes * kImagePlane);
                     bulk_g2s(smem_u32(Khi), src, kImagePlane, smem_u32(&bar_k));
-                    bulk_g2s(smem_u32(Klo), src + kImagePlane, kImagePlane, smem_u32(&bar_k));
+                    if constexpr (planes == 2) bulk_g2s(smem_u32(Klo), src + kImagePlane, kImagePlane, smem_u32(&bar_k));
                 }
             };
             auto copy_v = [&](int kt) {
                 if (lane == 0) {
                     const unsigned char *src = img0 + static_cast<size_t>(kt) * img_step + 2 * kImagePlane;
-                    mbar_expect_tx(smem_u32(&bar_p), 2 * kImagePlane);
+                    mbar_expect_tx(smem_u32(&bar_p), planes * kImagePlane);
                     bulk_g2s(smem_u32(Vhi), src, kImagePlane, smem_u32(&bar_p));
-                    bulk_g2s(smem_u32(Vlo), src + kImagePlane, kImagePlane, smem_u32(&bar_p));
+                    if constexpr (planes == 2) bulk_g2s(smem_u32(Vlo), src + kImagePlane, kImagePlane, smem_u32(&bar_p));
                 }
             };
             auto wait_c = [&](uint64_t *bar, uint32_t &ph) {
@@ -284,17 +288,19 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs a, 
         const uint32_t idesc_s = idesc_tf32(128, kKT), idesc_o = idesc_tf32(128, kHD);
         uint32_t ph_k = 0, ph_p = 0;
         // one k-step of QK (8 dims) / PV (8 keys): three products of the split
+        // (products with the K / V lo planes are left out when those are zero)
+        constexpr bool lo = !kLoZero;
         auto qk_step = [&](int s) {
             const uint64_t ko = ((s >> 2) * 8192u + (s & 3) * 32u) >> 4;
             const uint64_t qo = ((s >> 2) * 16384u + (s & 3) * 32u) >> 4;
             mma_tf32_ts(tS, tQ + 8 * s, dKhi + ko, idesc_s, s > 0);
-            mma_tf32_ts(tS, tQ + 8 * s, dKlo + ko, idesc_s, 1);
+            if constexpr (lo) mma_tf32_ts(tS, tQ + 8 * s, dKlo + ko, idesc_s, 1);
             mma_tf32(tS, dQlo + qo, dKhi + ko, idesc_s, 1);
         };
         auto pv_step = [&](int s, bool first) {
             const uint64_t vo = ((s >> 2) * 16384u + (s & 3) * 32u) >> 4;
             mma_tf32_ts(tD, tPh + 8 * s, dVhi + vo, idesc_o, !first || s > 0);
-            mma_tf32_ts(tD, tPh + 8 * s, dVlo + vo, idesc_o, 1);
+            if constexpr (lo) mma_tf32_ts(tD, tPh + 8 * s, dVlo + vo, idesc_o, 1);
             mma_tf32_ts(tD, tPl + 8 * s, dVhi + vo, idesc_o, 1);
         };
         // the MMAs of one tile (lane 0 issues, then commits); unrolled when the
@@ -653,7 +659,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs a, 
     if (warp == 0) tmem_dealloc(tbase, kTmemCols);
 }
 
-template <int G, class Rows, bool kBulk>
+template <int G, class Rows, bool kBulk, bool kLoZero>
 cudaError_t launch_prefill_g(const PrefillArgs &a, const Rows &r, cudaStream_t s) {
     static bool configured = false;
     if (!configured) {
@@ -661,11 +667,11 @@ cudaError_t launch_prefill_g(const PrefillArgs &a, const Rows &r, cudaStream_t s
         // for, so launch only if the compiled kernel starts with the registers
         // the split was sized for
         cudaFuncAttributes fa{};
-        cudaError_t e = cudaFuncGetAttributes(&fa, prefill_tc_kernel<G, Rows, kBulk>);
+        cudaError_t e = cudaFuncGetAttributes(&fa, prefill_tc_kernel<G, Rows, kBulk, kLoZero>);
         if (e != cudaSuccess) return e;
         if (fa.numRegs < kLaunchRegs || fa.maxThreadsPerBlock < kThreads)
             return cudaErrorInvalidConfiguration;
-        e = cudaFuncSetAttribute(prefill_tc_kernel<G, Rows, kBulk>,
+        e = cudaFuncSetAttribute(prefill_tc_kernel<G, Rows, kBulk, kLoZero>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(kSmemBytes));
         if (e != cudaSuccess) return e;
@@ -673,17 +679,17 @@ cudaError_t launch_prefill_g(const PrefillArgs &a, const Rows &r, cudaStream_t s
     }
     const long long grid = static_cast<long long>(a.n_tiles) * a.n_kv;
     if (grid <= 0 || grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    prefill_tc_kernel<G, Rows, kBulk><<<static_cast<unsigned>(grid), kThreads, kSmemBytes, s>>>(a, r);
+    prefill_tc_kernel<G, Rows, kBulk, kLoZero><<<static_cast<unsigned>(grid), kThreads, kSmemBytes, s>>>(a, r);
     return cudaGetLastError();
 }
 
-template <class Rows, bool kBulk>
+template <class Rows, bool kBulk, bool kLoZero = false>
 cudaError_t launch_prefill(const PrefillArgs &a, const Rows &r, cudaStream_t s) {
     switch (a.group) {
-        case 1: return launch_prefill_g<1, Rows, kBulk>(a, r, s);
-        case 2: return launch_prefill_g<2, Rows, kBulk>(a, r, s);
-        case 4: return launch_prefill_g<4, Rows, kBulk>(a, r, s);
-        case 8: return launch_prefill_g<8, Rows, kBulk>(a, r, s);
+        case 1: return launch_prefill_g<1, Rows, kBulk, kLoZero>(a, r, s);
+        case 2: return launch_prefill_g<2, Rows, kBulk, kLoZero>(a, r, s);
+        case 4: return launch_prefill_g<4, Rows, kBulk, kLoZero>(a, r, s);
+        case 8: return launch_prefill_g<8, Rows, kBulk, kLoZero>(a, r, s);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -701,6 +707,8 @@ constexpr int kSplitRawFloats = kKT * kHD + kKT * (kHD + 1);
 
 template <class E>
 __global__ void __launch_bounds__(256) split_kernel(SplitArgs p, PagedRowsP<E> rows_of) {
+    // bf16 values are exact in tf32: their lo planes are zero and not written
+    constexpr bool kLoZero = std::is_same<E, bf16>::value;
     extern __shared__ __align__(16) float raw[];
     float *rk = raw;              // [64][128]
     float *rv = raw + kKT * kHD;  // [64][129]
@@ -737,7 +745,7 @@ __global__ void __launch_bounds__(256) split_kernel(SplitArgs p, PagedRowsP<E> r
             const int kb = q >> 9, r = (q >> 3) & 63, lc = (q & 7) ^ (r & 7);
             split4(*reinterpret_cast<const float4 *>(rk + r * kHD + kb * 32 + lc * 4), h, l);
             *reinterpret_cast<float4 *>(out + q * 16) = h;
-            *reinterpret_cast<float4 *>(out + kImagePlane + q * 16) = l;
+            if constexpr (!kLoZero) *reinterpret_cast<float4 *>(out + kImagePlane + q * 16) = l;
         }
         {
             // V^T: k-block q >> 10 (32 keys), dim row (q >> 3) & 127, swizzled chunk q & 7
@@ -747,7 +755,7 @@ __global__ void __launch_bounds__(256) split_kernel(SplitArgs p, PagedRowsP<E> r
                                          rv[(k0 + 2) * (kHD + 1) + d], rv[(k0 + 3) * (kHD + 1) + d]);
             split4(x, h, l);
             *reinterpret_cast<float4 *>(out + 2 * kImagePlane + q * 16) = h;
-            *reinterpret_cast<float4 *>(out + 3 * kImagePlane + q * 16) = l;
+            if constexpr (!kLoZero) *reinterpret_cast<float4 *>(out + 3 * kImagePlane + q * 16) = l;
         }
     }
 }
@@ -773,7 +781,8 @@ cudaError_t launch_split(const SplitArgs &a, const PagedRowsP<E> &r, cudaStream_
 cudaError_t launch_prefill_paged(const PrefillArgs &a, const PagedAddr &addr, cudaStream_t s) {
     // the operands come as images (whatever the pool element): one instantiation
     if (!a.img || !a.img_tile0) return cudaErrorInvalidValue;
-    return launch_prefill<PagedRowsP<float>, true>(a, PagedRowsP<float>{addr}, s);
+    if (a.lo_zero) return launch_prefill<PagedRowsP<float>, true, true>(a, PagedRowsP<float>{addr}, s);
+    return launch_prefill<PagedRowsP<float>, true, false>(a, PagedRowsP<float>{addr}, s);
 }
 
 cudaError_t launch_prefill_contig(const PrefillArgs &a, const ContigAddr &addr, cudaStream_t s) {
