@@ -19,6 +19,8 @@ Contents
                       (``rope.py``).
 ``round_bf16``        the bf16 pool's rounding of stored rows (nearest,
                       ties to even; ``kv_format.py``).
+``round_e4m3``        the fp8 pool's stored-and-read value (e4m3 of x/scale,
+                      nearest, ties to even, saturating; ``kv_format.py``).
 
 Every function cites the passage of the pages it follows; the pages are the
 source listings "nx_f32_attn_paged.nx source", "nx_f32_gqa_attention.nx
@@ -117,7 +119,7 @@ from .contiguous_cache import ContiguousCache  # noqa: E402
 from .pool_model import PoolModel, SeqModel  # noqa: E402
 from . import pool_model  # noqa: E402
 from .rope import rope_neox, rope_neox_f32  # noqa: E402
-from .kv_format import round_bf16  # noqa: E402
+from .kv_format import round_bf16, round_e4m3  # noqa: E402
 
 __all__ = ["attend", "build", "ContiguousCache", "PoolModel", "SeqModel", "pool_model",
            "OK", "ERR_BAD_DIM", "ERR_BAD_GQA"]
