@@ -179,13 +179,16 @@ class DeviceRun:
         if w.name == "shared_prefix_forks":
             max_tok = int(w.extra["prefix"]) + 2 * 256 + 2
         self.bf16 = kv_dtype == "bf16"
-        self.elem = 2 if self.bf16 else 4
+        self.fp8 = kv_dtype == "fp8"
+        self.elem = 1 if self.fp8 else 2 if self.bf16 else 4
         self.K = torch.empty((w.n_blocks, w.n_layers, bs, w.kv_dim), device=dev,
-                             dtype=torch.bfloat16 if self.bf16 else torch.float32)
+                             dtype=(torch.float8_e4m3fn if self.fp8 else
+                                    torch.bfloat16 if self.bf16 else torch.float32))
         self.V = torch.empty_like(self.K)
         self.pool = pkv.pkv_pool_new(w.n_blocks, w.n_layers, w.kv_dim, bs, self.K, self.V,
                                      w.M + 8, -(-max_tok // bs) + 1, self.stream,
-                                     flags=pkv.PKV_POOL_BF16 if self.bf16 else 0)
+                                     flags=(pkv.PKV_POOL_FP8 if self.fp8 else
+                                            pkv.PKV_POOL_BF16 if self.bf16 else 0))
         assert self.pool, pkv.pkv_last_error()
         # shuffle the free list through the public API
         ids = [pkv.pkv_alloc_block(self.pool) for _ in range(w.n_blocks)]
@@ -505,7 +508,8 @@ def run_pkv(args):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "f32" if not run.bf16 else "f32 math, bf16 K/V storage",
+        "dtype": ("f32 math, fp8 e4m3 K/V storage" if run.fp8 else
+                  "f32 math, bf16 K/V storage" if run.bf16 else "f32"),
         "data": "synthetic (seeded N(0,1) K/V/Q, seeded length draws)",
         "config": {
             "workload": w.name,
@@ -591,8 +595,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time")
     ap.add_argument("--split-keys", type=int, default=0, help="keys per split-K unit (0: library default)")
-    ap.add_argument("--kv-dtype", choices=["f32", "bf16"], default="f32",
-                    help="K/V pool storage (bf16: rows rounded on write, f32 math)")
+    ap.add_argument("--kv-dtype", choices=["f32", "bf16", "fp8"], default="f32",
+                    help="K/V pool storage (bf16 / fp8 e4m3: rows rounded on write, f32 math)")
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)

@@ -75,14 +75,22 @@ typedef void *pkv_stream_t; /* cudaStream_t */
  * bytes and the decode traffic.  Needs an even kv_dim.  The fused append is
  * not used on such pools, and the contiguous twin stays f32. */
 #define PKV_POOL_BF16 2u
+/* fp8 e4m3 storage (no counterpart on the pages): every K/V row is stored as
+ * e4m3(x / scale) -- nearest, ties to even, saturated to +-448 -- and read as
+ * that value times scale; scale is a power of two (pkv_pool_set_kv_scale,
+ * default 1), so the read values are exact in f32 and tf32 and only the
+ * storage rounding differs from f32.  Quarters the pool's bytes.  Needs kv_dim
+ * % 4 == 0 (% 16 with head_dim 128).  As for bf16: no fused append, and the
+ * contiguous twin stays f32. */
+#define PKV_POOL_FP8 4u
 
 /* ---------------------------------------------------------------- pool ---- */
 
 /* Create a refcounted block pool ("nx_paged_kv_gate.nx source", KAT section:
  * pool_new(n_blocks, n_layers, kv_dim)).  Device layout of each of the K and V
  * pools: [n_blocks][n_layers][block_size][kv_dim] elements, f32 (or bf16 with
- * PKV_POOL_BF16); a block holds block_size consecutive token rows of every
- * layer.  k_pool_dev / v_pool_dev: caller-owned 16-byte-aligned device buffers
+ * PKV_POOL_BF16, fp8 e4m3 with PKV_POOL_FP8); a block holds block_size
+ * consecutive token rows of every layer.  k_pool_dev / v_pool_dev: caller-owned 16-byte-aligned device buffers
  * of that size (both non-NULL), or both NULL to let the library allocate them.  max_seqs bounds the live sequences; max_blocks_per_seq bounds
  * one page table.  The free list is a LIFO stack whose first pops are 0,1,2,...
  * Returns NULL on failure (bad sizes, out of memory).  With PKV_POOL_HOST_ONLY
@@ -100,9 +108,15 @@ PKV_API void pkv_pool_free(pkv_pool *pool);
 PKV_API int pkv_pool_set_stream(pkv_pool *pool, pkv_stream_t stream);
 
 /* Device base addresses of the K and V pools (NULL for a host-only pool);
- * f32 or bf16 elements as the pool was created. */
+ * f32, bf16 or fp8 elements as the pool was created. */
 PKV_API void *pkv_pool_k_data(const pkv_pool *pool);
 PKV_API void *pkv_pool_v_data(const pkv_pool *pool);
+
+/* Scale of an fp8 pool (no counterpart on the pages): stored element =
+ * e4m3(x / scale), read value = element * scale.  A power of two in
+ * [2^-20, 2^20]; settable only while every block is free.  PKV_ERR_ARG for a
+ * pool that is not fp8, a bad scale, or blocks in use. */
+PKV_API int pkv_pool_set_kv_scale(pkv_pool *pool, float scale);
 
 /* Number of blocks on the free list, or -1 for NULL. */
 PKV_API int32_t pkv_pool_free_blocks(const pkv_pool *pool);

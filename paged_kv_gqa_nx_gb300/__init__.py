@@ -30,6 +30,7 @@ PKV_ERR_DEVICE_BOUNDS = 8
 
 PKV_POOL_HOST_ONLY = 1
 PKV_POOL_BF16 = 2
+PKV_POOL_FP8 = 4
 PKV_NOALLOC_SCRATCH_BYTES = 16 << 20
 
 PKV_KERNEL_APPEND = 0
@@ -101,6 +102,7 @@ _SIGS = {
     "pkv_get_fused_append": (_i32, []),
     "pkv_set_cascade": (_int, [_i32]),
     "pkv_pool_last_work": (_int, [_vp, ctypes.POINTER(ctypes.c_int64), _i32]),
+    "pkv_pool_set_kv_scale": (_int, [_vp, _f32]),
     "pkv_get_cascade": (_i32, []),
     "pkv_launch_count": (_i64, []),
     "pkv_profile_enable": (_int, [_i32]),
@@ -192,8 +194,10 @@ def pkv_last_error() -> str:
 
 def pkv_pool_new(n_blocks, n_layers, kv_dim, block_size, k_pool=None, v_pool=None,
                  max_seqs=1024, max_blocks_per_seq=4096, stream=None, flags=0):
-    """k_pool / v_pool: float32 tensors, or bfloat16 with flags |= PKV_POOL_BF16."""
-    want = ("bfloat16",) if flags & PKV_POOL_BF16 else ("float32",)
+    """k_pool / v_pool: float32 tensors, bfloat16 with flags |= PKV_POOL_BF16,
+    float8_e4m3fn (or uint8) with flags |= PKV_POOL_FP8."""
+    want = (("bfloat16",) if flags & PKV_POOL_BF16 else
+            ("float8_e4m3fn", "uint8") if flags & PKV_POOL_FP8 else ("float32",))
     return _lib.pkv_pool_new(n_blocks, n_layers, kv_dim, block_size, _dev(k_pool, "k_pool", want),
                              _dev(v_pool, "v_pool", want), max_seqs, max_blocks_per_seq,
                              _stream(stream), flags)
@@ -368,6 +372,10 @@ def pkv_pool_last_work(pool):
     buf = (ctypes.c_int64 * PKV_WORK_FIELDS)()
     check(_lib.pkv_pool_last_work(pool, buf, PKV_WORK_FIELDS))
     return dict(zip(WORK_FIELD_NAMES, list(buf)))
+
+
+def pkv_pool_set_kv_scale(pool, scale):
+    return _lib.pkv_pool_set_kv_scale(pool, float(scale))
 
 
 def pkv_set_cascade(on):

@@ -16,6 +16,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <cmath>
 #include <atomic>
 #include <cstdarg>
 #include <cstdio>
@@ -262,6 +263,8 @@ struct pkv_pool {
     void *k = nullptr, *v = nullptr;
     bool owns_kv = false;
     bool bf16 = false;  // storage element: f32, or bf16 (PKV_POOL_BF16)
+    bool fp8 = false;   // or fp8 e4m3 of x / kv_scale (PKV_POOL_FP8)
+    float kv_scale = 1.f;
     int32_t *pt_dev = nullptr;
     int32_t *err_dev = nullptr;
     cudaStream_t stream = nullptr;
@@ -280,7 +283,8 @@ struct pkv_pool {
     Blob blob;
 
     int64_t block_floats() const { return static_cast<int64_t>(n_layers) * bs * kv_dim; }  // elements
-    size_t elem_bytes() const { return bf16 ? 2 : 4; }
+    size_t elem_bytes() const { return fp8 ? 1 : bf16 ? 2 : 4; }
+    bool narrow() const { return bf16 || fp8; }  // a storage element other than f32
 };
 
 struct pkv_seq {
@@ -342,6 +346,8 @@ PagedAddr paged_addr(const pkv_pool *p, int32_t layer) {
     a.k = p->k;
     a.v = p->v;
     a.bf16 = p->bf16 ? 1 : 0;
+    a.fp8 = p->fp8 ? 1 : 0;
+    a.kv_scale = p->kv_scale;
     a.pt = p->pt_dev;
     a.block_stride = p->block_floats();
     a.layer_off = static_cast<int64_t>(layer) * p->bs * p->kv_dim;
@@ -616,6 +622,8 @@ int run_layer(pkv_seq *const *seqs, int32_t M, const int32_t *n_q, const float *
                         n_kv_heads * head_dim, p->kv_dim);
         if (head_dim > kMaxHeadDim)
             return fail(PKV_ERR_BAD_DIM, "head_dim %d > %d is not supported", head_dim, kMaxHeadDim);
+        if (p->fp8 && head_dim == 128 && (p->kv_dim % 16) != 0)
+            return fail(PKV_ERR_BAD_DIM, "an fp8 pool with head_dim 128 needs kv_dim %% 16 == 0");
     }
     if (layer < 0 || layer >= p->n_layers)
         return fail(PKV_ERR_ARG, "layer %d outside [0, %d)", layer, p->n_layers);
@@ -664,7 +672,7 @@ int run_layer(pkv_seq *const *seqs, int32_t M, const int32_t *n_q, const float *
     if (attend && g_cascade.load() != 0 && prefill_shape(head_dim, group))
         cas = find_cascades(seqs, M, n_q, p->bs);
     if (attend) build_work(rows, causal, S, head_dim, group, w, cas);
-    const bool fuse = attend && rope_base == 0.0 && !p->bf16 && g_fused_append.load() != 0 && w.tiles.empty() &&
+    const bool fuse = attend && rope_base == 0.0 && !p->narrow() && g_fused_append.load() != 0 && w.tiles.empty() &&
                       w.ctiles.empty() && !w.units.empty() &&
                       head_dim == 128 && (group == 1 || group == 2 || group == 4) &&
                       dirty_within_appends(p, seqs, M, n_q);
@@ -819,7 +827,7 @@ int run_layer(pkv_seq *const *seqs, int32_t M, const int32_t *n_q, const float *
                        p->err_dev};
         pa.img = img;
         pa.img_tile0 = dptr<int32_t>(p, tile0_off);
-        pa.lo_zero = p->bf16 ? 1 : 0;
+        pa.lo_zero = p->narrow() ? 1 : 0;
         e = launch(PKV_KERNEL_PREFILL, st, [&] { return launch_prefill_paged(pa, addr, st); });
         if (e != cudaSuccess) return cuda_fail(e, "prefill kernel");
     }
@@ -830,7 +838,7 @@ int run_layer(pkv_seq *const *seqs, int32_t M, const int32_t *n_q, const float *
                        n_kv_heads, a.group, 0, S, a.scale_log2, p->err_dev};
         pa.img = img;
         pa.img_tile0 = dptr<int32_t>(p, tile0_off);
-        pa.lo_zero = p->bf16 ? 1 : 0;
+        pa.lo_zero = p->narrow() ? 1 : 0;
         e = launch(PKV_KERNEL_PREFILL, st, [&] { return launch_prefill_paged(pa, addr, st); });
         if (e != cudaSuccess) return cuda_fail(e, "shared-prefix kernel");
     }
@@ -886,8 +894,19 @@ pkv_pool *pkv_pool_new(int32_t n_blocks, int32_t n_layers, int32_t kv_dim, int32
     p->max_blocks = max_blocks_per_seq;
     p->host_only = (flags & PKV_POOL_HOST_ONLY) != 0;
     p->bf16 = (flags & PKV_POOL_BF16) != 0;
+    p->fp8 = (flags & PKV_POOL_FP8) != 0;
+    if (p->bf16 && p->fp8) {
+        fail(PKV_ERR_ARG, "PKV_POOL_BF16 and PKV_POOL_FP8 exclude each other");
+        delete p;
+        return nullptr;
+    }
     if (p->bf16 && (kv_dim % 2) != 0) {
         fail(PKV_ERR_BAD_DIM, "a bf16 pool needs an even kv_dim");
+        delete p;
+        return nullptr;
+    }
+    if (p->fp8 && (kv_dim % 4) != 0) {
+        fail(PKV_ERR_BAD_DIM, "an fp8 pool needs kv_dim to be a multiple of 4");
         delete p;
         return nullptr;
     }
@@ -975,6 +994,19 @@ int pkv_pool_set_stream(pkv_pool *p, pkv_stream_t stream) {
 
 void *pkv_pool_k_data(const pkv_pool *p) { return p ? p->k : nullptr; }
 void *pkv_pool_v_data(const pkv_pool *p) { return p ? p->v : nullptr; }
+int pkv_pool_set_kv_scale(pkv_pool *p, float scale) {
+    if (!p) return fail(PKV_ERR_ARG, "NULL pool");
+    if (!p->fp8) return fail(PKV_ERR_ARG, "the scale applies to fp8 pools only");
+    int ex = 0;
+    const float m = std::frexp(scale, &ex);
+    if (!(scale > 0.f) || m != 0.5f || ex < -19 || ex > 21)
+        return fail(PKV_ERR_ARG, "the scale must be a power of two in [2^-20, 2^20]");
+    if (static_cast<int32_t>(p->free_stack.size()) != p->n_blocks)
+        return fail(PKV_ERR_ARG, "the scale can only change while no block is in use");
+    p->kv_scale = scale;
+    return PKV_OK;
+}
+
 int pkv_pool_last_work(const pkv_pool *p, int64_t *out, int32_t cap) {
     if (!p || !out || cap < 0) return fail(PKV_ERR_ARG, "NULL pool or output");
     const int32_t n = std::min<int32_t>(cap, PKV_WORK_FIELDS);

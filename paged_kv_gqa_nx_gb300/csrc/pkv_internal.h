@@ -61,6 +61,8 @@ struct PagedAddr {
     int64_t layer_off;     // elements to the layer: layer * bs * kv_dim
     int32_t kv_dim, bs, bs_shift, max_blocks, n_blocks;
     int32_t bf16 = 0;      // storage element: 0 f32, 1 bf16 (rounded to nearest even on write)
+    int32_t fp8 = 0;       // 1: fp8 e4m3 elements holding x / kv_scale (saturating)
+    float kv_scale = 1.f;  // power of two; 1 unless fp8
 };
 
 // Address of a key/value row in a contiguous history: base[pos][kv_head*hd ...]

@@ -76,6 +76,8 @@ struct PagedRows {
     // plus j * kv_dim.
     __device__ __forceinline__ bool whole_tiles(int T) const { return (a.bs % T) == 0; }
     __device__ __forceinline__ size_t row_stride() const { return static_cast<size_t>(a.kv_dim); }
+    // read value = stored element * scale (a power of two; 1 except on fp8 pools)
+    __device__ __forceinline__ float scale() const { return a.kv_scale; }
     __device__ __forceinline__ bool block_start(int pos) const {
         return (a.bs_shift >= 0 ? (pos & (a.bs - 1)) : (pos % a.bs)) == 0;
     }
@@ -114,6 +116,7 @@ struct ContigRows {
     }
     __device__ __forceinline__ bool whole_tiles(int) const { return true; }
     __device__ __forceinline__ size_t row_stride() const { return static_cast<size_t>(a.kv_dim); }
+    __device__ __forceinline__ float scale() const { return 1.f; }
     // contiguous histories are caller-owned: there is no fused append
     __device__ __forceinline__ bool block_start(int) const { return false; }
     __device__ __forceinline__ bool store_row(int, int, int, int, int, const float *, const float *,
@@ -196,6 +199,10 @@ __device__ void rope_row(const PrepArgs &p, const PagedAddr &a, const AppendDesc
             if (dst) {
                 dst[o0] = y0;
                 dst[o1] = y1;
+            } else if (a.fp8) {
+                const float inv = 1.f / a.kv_scale;
+                store1(static_cast<fp8 *>(a.k) + dst_off + o0, y0 * inv);
+                store1(static_cast<fp8 *>(a.k) + dst_off + o1, y1 * inv);
             } else if (a.bf16) {
                 store1(static_cast<bf16 *>(a.k) + dst_off + o0, y0);
                 store1(static_cast<bf16 *>(a.k) + dst_off + o1, y1);
@@ -239,7 +246,17 @@ __global__ void prep_kernel(PrepArgs p, PagedAddr a) {
                          static_cast<size_t>(off) * a.kv_dim;
         const float *src = (is_v ? p.V_new : p.K_new) + static_cast<size_t>(d.src_row) * a.kv_dim;
         void *base = is_v ? a.v : a.k;
-        if (a.bf16) {
+        if (a.fp8) {
+            fp8 *dst = static_cast<fp8 *>(base) + o;
+            const float inv = 1.f / a.kv_scale;  // power of two: exact
+            if (p.vec4)
+                for (int i = lane; i < (a.kv_dim >> 2); i += 32) {
+                    const float4 x = ldg4(src + 4 * i);
+                    store4(dst + 4 * i, make_float4(x.x * inv, x.y * inv, x.z * inv, x.w * inv));
+                }
+            else
+                for (int i = lane; i < a.kv_dim; i += 32) store1(dst + i, src[i] * inv);
+        } else if (a.bf16) {
             bf16 *dst = static_cast<bf16 *>(base) + o;
             if (p.vec4)
                 for (int i = lane; i < (a.kv_dim >> 2); i += 32) store4(dst + 4 * i, ldg4(src + 4 * i));
@@ -393,14 +410,17 @@ __global__ void __launch_bounds__(128, 3) decode_fast_kernel(AttnArgs a, Rows ro
     // query slice of the group, pre-scaled to base-2 units
     const float *qrow = a.Q + static_cast<size_t>(rd.q_row0 + u.qi) * (a.n_heads * HD) +
                         static_cast<size_t>(kvh) * G * HD;
+    // an fp8 pool's power-of-two scale folds into the queries (for K) and the
+    // output (for V), exactly; it is 1 on other pools
+    const float ks = rows_of.scale();
     float4 q[G][4];
 #pragma unroll
     for (int g = 0; g < G; ++g)
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             float4 t = __ldg(reinterpret_cast<const float4 *>(qrow + g * HD + 4 * c + 32 * i));
-            q[g][i] = make_float4(t.x * a.scale_log2, t.y * a.scale_log2, t.z * a.scale_log2,
-                                  t.w * a.scale_log2);
+            q[g][i] = make_float4(t.x * a.scale_log2 * ks, t.y * a.scale_log2 * ks,
+                                  t.z * a.scale_log2 * ks, t.w * a.scale_log2 * ks);
         }
 
     const bool whole = rows_of.whole_tiles(T);
@@ -588,10 +608,10 @@ __global__ void __launch_bounds__(128, 3) decode_fast_kernel(AttnArgs a, Rows ro
         const int h = kvh * G + g;
         if (u.item < 0) {
             a.out[static_cast<size_t>(rd.q_row0 + u.qi) * (a.n_heads * HD) +
-                  static_cast<size_t>(h) * HD + d] = num / den;
+                  static_cast<size_t>(h) * HD + d] = num * ks / den;
         } else {
             const size_t ph = static_cast<size_t>(a.merges[u.item].part0 + u.split) * a.n_heads + h;
-            a.pacc[ph * HD + d] = num;
+            a.pacc[ph * HD + d] = num * ks;
             if (d == 0) {
                 a.pm[ph] = M;
                 a.pl[ph] = den;
@@ -636,7 +656,8 @@ __global__ void __launch_bounds__(128) decode_generic_kernel(AttnArgs a, Rows ro
     float *ls = ms + kGenW * hpc;                  // [W][hpc]
     const float *qrow = a.Q + static_cast<size_t>(rd.q_row0 + u.qi) * (a.n_heads * hd) +
                         static_cast<size_t>(h0) * hd;
-    for (int t = threadIdx.x; t < nh * hd; t += blockDim.x) qs[t] = qrow[t] * a.scale_log2;
+    const float ks = rows_of.scale();  // fp8 scale (power of two) into the queries and the output
+    for (int t = threadIdx.x; t < nh * hd; t += blockDim.x) qs[t] = qrow[t] * a.scale_log2 * ks;
     for (int t = threadIdx.x; t < kGenW * hpc * hd; t += blockDim.x) accs[t] = 0.f;
     __syncthreads();
 
@@ -694,10 +715,10 @@ __global__ void __launch_bounds__(128) decode_generic_kernel(AttnArgs a, Rows ro
         const int h = h0 + g;
         if (u.item < 0) {
             a.out[static_cast<size_t>(rd.q_row0 + u.qi) * (a.n_heads * hd) +
-                  static_cast<size_t>(h) * hd + d] = num / den;
+                  static_cast<size_t>(h) * hd + d] = num * ks / den;
         } else {
             const size_t ph = static_cast<size_t>(a.merges[u.item].part0 + u.split) * a.n_heads + h;
-            a.pacc[ph * hd + d] = num;
+            a.pacc[ph * hd + d] = num * ks;
             if (d == 0) {
                 a.pm[ph] = M;
                 a.pl[ph] = den;
@@ -823,6 +844,7 @@ cudaError_t launch_copy_blocks(void *kp, void *vp, const CopyDesc *items, int32_
 }
 
 cudaError_t launch_decode_paged(const AttnArgs &a, const PagedAddr &addr, cudaStream_t s) {
+    if (addr.fp8) return launch_decode(a, PagedRows<fp8>{addr}, s);
     if (addr.bf16) return launch_decode(a, PagedRows<bf16>{addr}, s);
     return launch_decode(a, PagedRows<float>{addr}, s);
 }

@@ -707,8 +707,10 @@ constexpr int kSplitRawFloats = kKT * kHD + kKT * (kHD + 1);
 
 template <class E>
 __global__ void __launch_bounds__(256) split_kernel(SplitArgs p, PagedRowsP<E> rows_of) {
-    // bf16 values are exact in tf32: their lo planes are zero and not written
-    constexpr bool kLoZero = std::is_same<E, bf16>::value;
+    // bf16 values, and fp8 values times a power of two, are exact in tf32:
+    // their lo planes are zero and not written
+    constexpr bool kLoZero = !std::is_same<E, float>::value;
+    const float p_scale = rows_of.a.kv_scale;
     extern __shared__ __align__(16) float raw[];
     float *rk = raw;              // [64][128]
     float *rv = raw + kKT * kHD;  // [64][129]
@@ -726,6 +728,11 @@ __global__ void __launch_bounds__(256) split_kernel(SplitArgs p, PagedRowsP<E> r
             if (b >= 0) {
                 kx = ldg4(rows_of.k_row(b, pos, kvh) + 4 * ch);
                 vx = ldg4(rows_of.v_row(b, pos, kvh) + 4 * ch);
+                if constexpr (std::is_same<E, fp8>::value) {
+                    const float sc = p_scale;  // power of two: exact
+                    kx = make_float4(kx.x * sc, kx.y * sc, kx.z * sc, kx.w * sc);
+                    vx = make_float4(vx.x * sc, vx.y * sc, vx.z * sc, vx.w * sc);
+                }
             }
         }
         *reinterpret_cast<float4 *>(rk + key * kHD + 4 * ch) = kx;
@@ -790,6 +797,7 @@ cudaError_t launch_prefill_contig(const PrefillArgs &a, const ContigAddr &addr, 
 }
 
 cudaError_t launch_split_paged(const SplitArgs &a, const PagedAddr &addr, cudaStream_t s) {
+    if (addr.fp8) return launch_split(a, PagedRowsP<fp8>{addr}, s);
     if (addr.bf16) return launch_split(a, PagedRowsP<bf16>{addr}, s);
     return launch_split(a, PagedRowsP<float>{addr}, s);
 }

@@ -40,15 +40,20 @@ class GpuPool:
     of a row nobody wrote poisons the output."""
 
     def __init__(self, n_blocks, n_layers, kv_dim, bs, max_seqs=64, max_blocks=4096,
-                 shuffle_seed=None, fill=float("nan"), dtype=torch.float32):
+                 shuffle_seed=None, fill=float("nan"), dtype=torch.float32, kv_scale=1.0):
         self.n_blocks, self.n_layers, self.kv_dim, self.bs = n_blocks, n_layers, kv_dim, bs
-        self.K = torch.full((n_blocks, n_layers, bs, kv_dim), fill, device="cuda", dtype=dtype)
+        self.K = torch.full((n_blocks, n_layers, bs, kv_dim), fill, device="cuda",
+                            dtype=torch.float32).to(dtype)
         self.V = torch.full_like(self.K, fill)
         self.stream = torch.cuda.current_stream()
-        flags = pkv.PKV_POOL_BF16 if dtype == torch.bfloat16 else 0
+        self.kv_scale = float(kv_scale)
+        flags = (pkv.PKV_POOL_BF16 if dtype == torch.bfloat16 else
+                 pkv.PKV_POOL_FP8 if dtype == torch.float8_e4m3fn else 0)
         self.p = pkv.pkv_pool_new(n_blocks, n_layers, kv_dim, bs, self.K, self.V, max_seqs,
                                   max_blocks, self.stream, flags)
         assert self.p, pkv.pkv_last_error()
+        if self.kv_scale != 1.0:
+            pkv.check(pkv.pkv_pool_set_kv_scale(self.p, self.kv_scale))
         if shuffle_seed is not None:
             ids = [pkv.pkv_alloc_block(self.p) for _ in range(n_blocks)]
             assert ids == list(range(n_blocks))
@@ -72,14 +77,22 @@ class GpuPool:
         pos = torch.arange(start, start + L, device="cuda")
         blk = pt[pos // self.bs]
         off = pos % self.bs
-        # a bf16 pool stores torch's float32 -> bfloat16 cast (nearest, ties to even)
-        self.K[blk, layer, off] = K_hist.to(device="cuda", dtype=torch.float32).to(self.K.dtype)
-        self.V[blk, layer, off] = V_hist.to(device="cuda", dtype=torch.float32).to(self.V.dtype)
+        # a bf16 / fp8 pool stores torch's float32 -> bfloat16 / float8_e4m3fn cast
+        # (nearest, ties to even) of x / scale
+        s = self.kv_scale
+        self.K[blk, layer, off] = (K_hist.to(device="cuda", dtype=torch.float32) / s).to(self.K.dtype)
+        self.V[blk, layer, off] = (V_hist.to(device="cuda", dtype=torch.float32) / s).to(self.V.dtype)
 
     def read_history(self, seq, layer, L):
+        """Rows [0, L) as stored (the pool's element type; times kv_scale to read)."""
         pt = torch.tensor(pkv.pkv_seq_page_table(seq), device="cuda", dtype=torch.long)
         pos = torch.arange(L, device="cuda")
         return self.K[pt[pos // self.bs], layer, pos % self.bs], self.V[pt[pos // self.bs], layer, pos % self.bs]
+
+    def read_values(self, seq, layer, L):
+        """Rows [0, L) as the kernels read them: float32, element * kv_scale."""
+        K, V = self.read_history(seq, layer, L)
+        return K.float() * self.kv_scale, V.float() * self.kv_scale
 
     def check_no_device_error(self):
         assert pkv.pkv_sync_error(self.p) == pkv.PKV_OK, pkv.pkv_last_error()

@@ -1,11 +1,13 @@
-"""bf16 K/V pools (PKV_POOL_BF16; not on the pages, which store f32).
+"""bf16 and fp8 K/V pools (PKV_POOL_BF16 / PKV_POOL_FP8; not on the pages,
+which store f32).
 
-Every K/V row is rounded once to the nearest bfloat16 (ties to even) when it
-is written and read back exactly; the attention math stays f32.  So the
-oracle attends, in its usual precision, over the rounded histories: the rows
-written into the pool with torch's bf16 cast (which the oracle's round_bf16
-matches, pinned on the CPU) and the call's new rows rounded by round_bf16.
-The rounded rows the library stores are compared with round_bf16 bit for bit.
+Every K/V row is rounded once when it is written -- to the nearest bfloat16,
+or to e4m3 of x / scale (saturating, scale a power of two) -- and read back
+exactly; the attention math stays f32.  So the oracle attends, in its usual
+precision, over the rounded histories: the rows written into the pool with
+torch's casts (which the oracle's round_bf16 / round_e4m3 match, pinned on
+the CPU) and the call's new rows rounded by the oracle.  The values the
+library stores are compared with the oracle's rounding bit for bit.
 """
 from __future__ import annotations
 
@@ -20,16 +22,22 @@ import paged_kv_gqa_nx_gb300 as pkv
 from gpu_helpers import GpuPool, assert_close, bits_equal
 
 BF = torch.bfloat16
+FMTS = {
+    "bf16": (torch.bfloat16, 1.0, lambda x, s: oracle.round_bf16(x)),
+    "fp8": (torch.float8_e4m3fn, 1.0, lambda x, s: oracle.round_e4m3(x, s)),
+    "fp8s": (torch.float8_e4m3fn, 0.25, lambda x, s: oracle.round_e4m3(x, s)),
+}
 
 
-def _case(H, KV, hd, past, nq, seed=0, bs=16, rope=0.0, check_m1=True):
+def _case(H, KV, hd, past, nq, seed=0, bs=16, rope=0.0, check_m1=True, fmt="bf16"):
+    dtype, kv_scale, rnd = FMTS[fmt]
     rng = np.random.default_rng(seed)
     kv_dim, q_dim = KV * hd, H * hd
     scale = float(np.float32(1.0 / math.sqrt(hd)))
     need = sum(-(-(p + n) // bs) for p, n in zip(past, nq))
     pool = GpuPool(need + 8, 1, kv_dim, bs, max_seqs=len(past) + 2,
                    max_blocks=max(-(-(p + n) // bs) for p, n in zip(past, nq)) + 1,
-                   shuffle_seed=seed + 5, dtype=BF)
+                   shuffle_seed=seed + 5, dtype=dtype, kv_scale=kv_scale)
     try:
         seqs, hk, hv = [], [], []
         for p, n in zip(past, nq):
@@ -40,8 +48,8 @@ def _case(H, KV, hd, past, nq, seed=0, bs=16, rope=0.0, check_m1=True):
                 pool.grow(s, p)
                 pool.write_history(s, 0, torch.from_numpy(Kh), torch.from_numpy(Vh))
             seqs.append(s)
-            hk.append(oracle.round_bf16(Kh))
-            hv.append(oracle.round_bf16(Vh))
+            hk.append(rnd(Kh, kv_scale))
+            hv.append(rnd(Vh, kv_scale))
         T = int(sum(nq))
         Q = rng.standard_normal((T, q_dim)).astype(np.float32)
         Kn = rng.standard_normal((T, kv_dim)).astype(np.float32)
@@ -64,10 +72,10 @@ def _case(H, KV, hd, past, nq, seed=0, bs=16, rope=0.0, check_m1=True):
                 # rounding decision on the same float32 values the kernel rounds
                 Qr = oracle.rope_neox(Qr, pos, hd, rope).astype(np.float32)
                 Kr = oracle.rope_neox_f32(Kr, pos, hd, rope)
-            Kr, Vr = oracle.round_bf16(Kr), oracle.round_bf16(Vn[o:o + n])
-            Kp, Vp = pool.read_history(seqs[r], 0, p + n)
-            stored_k = Kp[p:].float().cpu().numpy()
-            stored_v = Vp[p:].float().cpu().numpy()
+            Kr, Vr = rnd(Kr, kv_scale), rnd(Vn[o:o + n], kv_scale)
+            Kp, Vp = pool.read_values(seqs[r], 0, p + n)
+            stored_k = Kp[p:].cpu().numpy()
+            stored_v = Vp[p:].cpu().numpy()
             assert np.array_equal(stored_k.view(np.uint32), Kr.view(np.uint32)), "row %d K" % r
             assert np.array_equal(stored_v.view(np.uint32), Vr.view(np.uint32)), "row %d V" % r
             Kf = np.concatenate([hk[r], Kr])
@@ -87,22 +95,25 @@ def _case(H, KV, hd, past, nq, seed=0, bs=16, rope=0.0, check_m1=True):
 
 
 @pytest.mark.gpu
+@pytest.mark.parametrize("fmt", ["bf16", "fp8", "fp8s"])
 @pytest.mark.parametrize("H,KV", [(32, 8), (16, 8), (8, 8)], ids=["g4", "g2", "g1"])
-def test_bf16_fast_kernel_decode_and_prefill(H, KV):
+def test_narrow_fast_kernel_decode_and_prefill(H, KV, fmt):
     # decode rows across page and split boundaries, a short multi-token row, a
     # tensor-core prefill row
-    _case(H, KV, 128, [0, 15, 1024, 3000, 777, 2100], [1, 1, 1, 1, 5, 64])
+    _case(H, KV, 128, [0, 15, 1024, 3000, 777, 2100], [1, 1, 1, 1, 5, 64], fmt=fmt)
 
 
 @pytest.mark.gpu
-def test_bf16_generic_kernel():
-    # head_dim 6 (generic kernel), 4-row pages
-    _case(6, 2, 6, [0, 9, 130], [1, 3, 1], seed=2, bs=4)
+@pytest.mark.parametrize("fmt", ["bf16", "fp8s"])
+def test_narrow_generic_kernel(fmt):
+    # head_dim 8 (generic kernel), 4-row pages
+    _case(6, 2, 8, [0, 9, 130], [1, 3, 1], seed=2, bs=4, fmt=fmt)
 
 
 @pytest.mark.gpu
-def test_bf16_rope_on_append():
-    _case(32, 8, 128, [0, 100, 5000], [1, 2, 40], seed=3, rope=10000.0)
+@pytest.mark.parametrize("fmt", ["bf16", "fp8"])
+def test_narrow_rope_on_append(fmt):
+    _case(32, 8, 128, [0, 100, 5000], [1, 2, 40], seed=3, rope=10000.0, fmt=fmt)
 
 
 @pytest.mark.gpu
@@ -163,7 +174,21 @@ def test_bf16_copy_on_append_and_cascade():
 
 
 @pytest.mark.gpu
-def test_bf16_pool_needs_even_kv_dim():
+def test_narrow_pool_argument_checks():
     K = torch.zeros(4, 1, 4, 5, device="cuda", dtype=BF)
     assert not pkv.pkv_pool_new(4, 1, 5, 4, K, K.clone(), 2, 4, None, pkv.PKV_POOL_BF16)
     assert "even kv_dim" in pkv.pkv_last_error()
+    K8 = torch.zeros(4, 1, 4, 6, device="cuda", dtype=torch.float8_e4m3fn)
+    assert not pkv.pkv_pool_new(4, 1, 6, 4, K8, K8.clone(), 2, 4, None, pkv.PKV_POOL_FP8)
+    assert "multiple of 4" in pkv.pkv_last_error()
+    K8 = torch.zeros(4, 1, 4, 8, device="cuda", dtype=torch.float8_e4m3fn)
+    p = pkv.pkv_pool_new(4, 1, 8, 4, K8, K8.clone(), 2, 4, None, pkv.PKV_POOL_FP8)
+    assert p
+    try:
+        for bad in (3.0, 0.0, -2.0, 2.0 ** 30):
+            assert pkv.pkv_pool_set_kv_scale(p, bad) == pkv.PKV_ERR_ARG
+        assert pkv.pkv_pool_set_kv_scale(p, 0.5) == pkv.PKV_OK
+        assert pkv.pkv_alloc_block(p) == 0
+        assert pkv.pkv_pool_set_kv_scale(p, 2.0) == pkv.PKV_ERR_ARG  # a block is in use
+    finally:
+        pkv.pkv_pool_free(p)
