@@ -321,10 +321,13 @@ __global__ void copy_blocks_kernel(float *k, float *v, const CopyDesc *__restric
 // score of head c / (8 / G).  Lane layout for P.V: lane owns dims
 // 4*lane .. 4*lane+3 of every head.
 
-template <int G>
+template <int G, class E = float>
 struct FastCfg {
     static constexpr int HD = 128;
-    static constexpr int T = 8;   // keys per tile
+    // keys per tile: 8 for f32 rows; 16 for bf16 / fp8 rows, whose smaller
+    // stages leave room to spread each tile's softmax over twice the keys
+    static constexpr int T = sizeof(E) == 4 ? 8 : 16;
+    static constexpr int NIT = T / 4;  // keys per lane group and tile
     static constexpr int W = 4;   // warps per CTA
     static constexpr int LPH = 8 / G;  // lanes of a group holding one head's score
 };
@@ -375,16 +378,16 @@ __device__ __forceinline__ float4 fma4(float s, const float4 &v, const float4 &a
 
 template <int G, int NST, class E>
 constexpr size_t fast_smem_bytes() {
-    using C = FastCfg<G>;
+    using C = FastCfg<G, E>;
     return static_cast<size_t>(C::W) * NST * C::T * C::HD * 2 * sizeof(E) +
            static_cast<size_t>(C::W) * (C::T + 1) * 4 * sizeof(float);
 }
 
 template <int G, int NST, class Rows>
 __global__ void __launch_bounds__(128, 3) decode_fast_kernel(AttnArgs a, Rows rows_of) {
-    using C = FastCfg<G>;
-    using E = typename Rows::Elem;             // pool element (f32 or bf16)
-    constexpr int HD = C::HD, T = C::T, W = C::W;
+    using E = typename Rows::Elem;             // pool element (f32, bf16 or fp8)
+    using C = FastCfg<G, E>;
+    constexpr int HD = C::HD, T = C::T, W = C::W, NIT = C::NIT;
     constexpr int EPC = 16 / static_cast<int>(sizeof(E));  // elements per 16-byte chunk
     constexpr int CPR = HD / EPC;              // chunks per row: 32 (f32), 16 (bf16)
     constexpr int STAGE = T * HD * 2;          // elements: K rows then V rows
@@ -510,9 +513,9 @@ __global__ void __launch_bounds__(128, 3) decode_fast_kernel(AttnArgs a, Rows ro
         const E *Ks = wbase + (k % NST) * STAGE;
         const E *Vs = Ks + T * HD;
 
-        float sc[2];
+        float sc[NIT];
 #pragma unroll
-        for (int it = 0; it < 2; ++it) {
+        for (int it = 0; it < NIT; ++it) {
             const int j = it * 4 + kg;
             float4 kk[4];
 #pragma unroll
@@ -534,22 +537,27 @@ __global__ void __launch_bounds__(128, 3) decode_fast_kernel(AttnArgs a, Rows ro
             sc[it] = (j < n_valid) ? s : -INFINITY;
         }
 
-        // online softmax for this lane's head over the tile's 8 keys
+        // online softmax for this lane's head over the tile's T keys
         float tmax = fmaxf(sc[0], sc[1]);
+#pragma unroll
+        for (int it = 2; it < NIT; ++it) tmax = fmaxf(tmax, sc[it]);
         tmax = fmaxf(tmax, __shfl_xor_sync(kFull, tmax, 8));
         tmax = fmaxf(tmax, __shfl_xor_sync(kFull, tmax, 16));
         const float m_new = fmaxf(m_run, tmax);
         const float alpha = exp2f(m_run - m_new);
-        const float p0 = exp2f(sc[0] - m_new);
-        const float p1 = exp2f(sc[1] - m_new);
-        float ps = p0 + p1;
+        float pv[NIT];
+#pragma unroll
+        for (int it = 0; it < NIT; ++it) pv[it] = exp2f(sc[it] - m_new);
+        float ps = pv[0] + pv[1];
+#pragma unroll
+        for (int it = 2; it < NIT; ++it) ps += pv[it];
         ps += __shfl_xor_sync(kFull, ps, 8);
         ps += __shfl_xor_sync(kFull, ps, 16);
         l_run = fmaf(l_run, alpha, ps);
         m_run = m_new;
         if ((c % LPH) == 0) {
-            P[kg * 4 + hh] = p0;
-            P[(4 + kg) * 4 + hh] = p1;
+#pragma unroll
+            for (int it = 0; it < NIT; ++it) P[(it * 4 + kg) * 4 + hh] = pv[it];
             if (kg == 0) P[T * 4 + hh] = alpha;
         }
         __syncwarp();
