@@ -6,7 +6,7 @@ position is its sequence's current length, a cos/sin table is built for that
 position from head_dim and the base, and the "neox" application is made to
 every query head and every new key head before the attend call.  The bodies
 of the table builder and of the application are not printed on the pages;
-this is the plain reading of the NeoX form (readings listed in the design doc):
+this is the plain reading of the NeoX form:
 
     theta_i = base ** (-2 i / head_dim),     i = 0 .. head_dim/2 - 1
     angle   = pos * theta_i
