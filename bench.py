@@ -76,10 +76,12 @@ def kernel_source_digest(kernel: str = "decode"):
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(workload: str, kernel: str = "decode"):
+def profiled_traffic(workload: str, kernel: str = "decode", kv_dtype: str = "f32"):
     """DRAM bytes per launch of `kernel` from the committed ncu summary for
-    this workload, if it was taken on the current kernel source; else None."""
-    path = os.path.join(ROOT, "profiles", PROFILE_FILES[kernel] % workload)
+    this workload and pool element type (f32 summaries carry no suffix), if it
+    was taken on the current kernel source; else None."""
+    name = workload if kv_dtype == "f32" else "%s_%s" % (workload, kv_dtype)
+    path = os.path.join(ROOT, "profiles", PROFILE_FILES[kernel] % name)
     if not os.path.exists(path):
         return None
     text = open(path).read()
@@ -471,7 +473,7 @@ def run_pkv(args):
                     "peak_source": ("%s bf16_tflops x 1.1/2.25 (nominal TF32/BF16) / 3 (TF32 products "
                                     "per f32 product)" % tkind),
                     "unit": "TFLOP/s", "frac": round(achieved / tpeak, 4),
-                    "traffic": profiled_traffic(args.workload, "prefill"),
+                    "traffic": profiled_traffic(args.workload, "prefill", args.kv_dtype),
                     "alg_flops_per_launch": flops_per_launch,
                     "avg_launch_ms": round(pre_avg_s * 1e3, 4)}
     else:
@@ -483,7 +485,7 @@ def run_pkv(args):
                     "peak_source": peak_kind + " (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
                     else "fallback", "unit": "GB/s",
                     "frac": round(achieved / peak, 4) if achieved else None,
-                    "traffic": profiled_traffic(args.workload), "alg_bytes_per_launch": alg_bytes,
+                    "traffic": profiled_traffic(args.workload, "decode", args.kv_dtype), "alg_bytes_per_launch": alg_bytes,
                     "avg_launch_ms": round(dec_avg_s * 1e3, 4)}
 
     cpu = None
