@@ -51,8 +51,17 @@ def measured_hbm_peak():
         return HBM_FALLBACK_GBS, "fallback"
 
 
-KERNEL_SOURCES = {"decode": "paged_kv_gqa_nx_gb300/csrc/pkv_kernels.cu",
-                  "prefill": "paged_kv_gqa_nx_gb300/csrc/pkv_prefill.cu"}
+_CSRC = "paged_kv_gqa_nx_gb300/csrc/"
+# the sources a committed ncu summary was taken on, per (kernel, pool element
+# type): a summary's sha256 prefix covers these files in this order
+KERNEL_SOURCES = {
+    ("decode", "f32"): ["pkv_kernels.cu", "pkv_rows.h"],
+    ("decode", "bf16"): ["pkv_decode_mma.cu", "pkv_rows.h"],
+    ("decode", "fp8"): ["pkv_decode_mma.cu", "pkv_rows.h"],
+    ("prefill", "f32"): ["pkv_prefill.cu", "pkv_tcgen05.h"],
+    ("prefill", "bf16"): ["pkv_prefill.cu", "pkv_tcgen05.h"],
+    ("prefill", "fp8"): ["pkv_prefill.cu", "pkv_tcgen05.h"],
+}
 PROFILE_FILES = {"decode": "decode_%s.md", "prefill": "prefill_tc_%s.md"}
 
 
@@ -69,10 +78,11 @@ def measured_tensor_peak():
     return bf16 * (1.1 / 2.25) / 3.0, kind
 
 
-def kernel_source_digest(kernel: str = "decode"):
+def kernel_source_digest(kernel: str = "decode", kv_dtype: str = "f32"):
     h = hashlib.sha256()
-    with open(os.path.join(ROOT, KERNEL_SOURCES[kernel]), "rb") as f:
-        h.update(f.read())
+    for name in KERNEL_SOURCES[(kernel, kv_dtype)]:
+        with open(os.path.join(ROOT, _CSRC + name), "rb") as f:
+            h.update(f.read())
     return h.hexdigest()[:16]
 
 
@@ -87,7 +97,7 @@ def profiled_traffic(workload: str, kernel: str = "decode", kv_dtype: str = "f32
     text = open(path).read()
     m_src = re.search(r"kernel_source_sha256:\s*([0-9a-f]+)", text)
     m_tr = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
-    if not m_src or not m_tr or m_src.group(1) != kernel_source_digest(kernel):
+    if not m_src or not m_tr or m_src.group(1) != kernel_source_digest(kernel, kv_dtype):
         return None
     return float(m_tr.group(1))
 

@@ -184,6 +184,14 @@ cudaError_t launch_copy_blocks(void *k, void *v, const CopyDesc *items, int32_t 
                                cudaStream_t s);
 cudaError_t launch_decode_paged(const AttnArgs &a, const PagedAddr &addr, cudaStream_t s);
 cudaError_t launch_decode_contig(const AttnArgs &a, const ContigAddr &addr, cudaStream_t s);
+// Decode over a bf16 or fp8 pool on the tensor cores (pkv_decode_mma.cu), for
+// the shapes decode_mma_shape accepts; no fused append.
+cudaError_t launch_decode_mma_paged(const AttnArgs &a, const PagedAddr &addr, cudaStream_t s);
+__host__ __device__ constexpr bool decode_mma_shape(int head_dim, int group, bool bf16, bool fp8) {
+    return head_dim == 128 &&
+           ((fp8 && (group == 1 || group == 2 || group == 4 || group == 8)) ||
+            (!fp8 && bf16 && (group == 1 || group == 2 || group == 4)));
+}
 cudaError_t launch_merge(const MergeArgs &a, cudaStream_t s);
 // Tensor-core prefill (pkv_prefill.cu): head_dim 128, group 1, 2, 4 or 8.
 cudaError_t launch_prefill_paged(const PrefillArgs &a, const PagedAddr &addr, cudaStream_t s);

@@ -29,7 +29,7 @@ FMTS = {
 }
 
 
-def _case(H, KV, hd, past, nq, seed=0, bs=16, rope=0.0, check_m1=True, fmt="bf16"):
+def _case(H, KV, hd, past, nq, seed=0, bs=16, rope=0.0, check_m1=True, fmt="bf16", q_head_scale=None):
     dtype, kv_scale, rnd = FMTS[fmt]
     rng = np.random.default_rng(seed)
     kv_dim, q_dim = KV * hd, H * hd
@@ -52,6 +52,8 @@ def _case(H, KV, hd, past, nq, seed=0, bs=16, rope=0.0, check_m1=True, fmt="bf16
             hv.append(rnd(Vh, kv_scale))
         T = int(sum(nq))
         Q = rng.standard_normal((T, q_dim)).astype(np.float32)
+        if q_head_scale is not None:  # per query head magnitudes
+            Q = (Q.reshape(T, H, hd) * np.asarray(q_head_scale, np.float32)[None, :, None]).reshape(T, q_dim)
         Kn = rng.standard_normal((T, kv_dim)).astype(np.float32)
         Vn = rng.standard_normal((T, kv_dim)).astype(np.float32)
         Qd, Kd, Vd = (torch.from_numpy(a).cuda() for a in (Q, Kn, Vn))
@@ -97,10 +99,37 @@ def _case(H, KV, hd, past, nq, seed=0, bs=16, rope=0.0, check_m1=True, fmt="bf16
 @pytest.mark.gpu
 @pytest.mark.parametrize("fmt", ["bf16", "fp8", "fp8s"])
 @pytest.mark.parametrize("H,KV", [(32, 8), (16, 8), (8, 8)], ids=["g4", "g2", "g1"])
-def test_narrow_fast_kernel_decode_and_prefill(H, KV, fmt):
+def test_narrow_decode_and_prefill(H, KV, fmt):
     # decode rows across page and split boundaries, a short multi-token row, a
     # tensor-core prefill row
     _case(H, KV, 128, [0, 15, 1024, 3000, 777, 2100], [1, 1, 1, 1, 5, 64], fmt=fmt)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("fmt", ["fp8", "fp8s"])
+def test_fp8_group8(fmt):
+    # 64 query heads on 8 kv heads: the fp8 tensor-core kernel carries all 8
+    # heads of a group in one MMA tile
+    _case(64, 8, 128, [0, 31, 1024, 2500, 100], [1, 1, 1, 1, 7], seed=4, fmt=fmt)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("fmt", ["bf16", "fp8"])
+def test_narrow_small_pages(fmt):
+    # 8-row pages: every key of a tile is looked up on its own
+    _case(32, 8, 128, [0, 13, 1030, 333], [1, 1, 3, 1], seed=5, bs=8, fmt=fmt)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("fmt", ["bf16", "fp8", "fp8s"])
+def test_narrow_query_magnitudes(fmt):
+    # query heads from 1e-4 to 8 in size (scores from nearly uniform to
+    # sharply peaked; larger scores would put the f32 rounding of the scores
+    # themselves above the tolerance); the f16 pieces of an fp8 pool are
+    # scaled per head
+    H = 32
+    sc = [1e-4 * (8e4 ** (i / (H - 1))) for i in range(H)]
+    _case(H, 8, 128, [5, 700, 2049], [1, 1, 2], seed=6, fmt=fmt, q_head_scale=sc)
 
 
 @pytest.mark.gpu
@@ -117,17 +146,21 @@ def test_narrow_rope_on_append(fmt):
 
 
 @pytest.mark.gpu
-def test_bf16_copy_on_append_and_cascade():
-    # forks of a bf16 prefix ending inside a page: the first append copies the
-    # tail page (2-byte elements); then a batched decode step of 20 forks takes
-    # the shared-prefix path.  Every fork is checked against the oracle.
+@pytest.mark.parametrize("fmt", ["bf16", "fp8s"])
+def test_narrow_copy_on_append_and_cascade(fmt):
+    # forks of a narrow-pool prefix ending inside a page: the first append
+    # copies the tail page (2- or 1-byte elements); then a batched decode step
+    # of 20 forks takes the shared-prefix path.  Every fork is checked against
+    # the oracle.
+    dtype, kv_scale, rnd0 = FMTS[fmt]
+    rnd = lambda x: rnd0(x, kv_scale)  # noqa: E731
     H, KV, hd, bs = 32, 8, 128, 16
     kv_dim, q_dim = KV * hd, H * hd
     scale = float(np.float32(1.0 / math.sqrt(hd)))
     rng = np.random.default_rng(9)
     prefix, n_f = 2500, 20
     pool = GpuPool(prefix // bs + 4 * n_f + 16, 1, kv_dim, bs, max_seqs=n_f + 4,
-                   max_blocks=prefix // bs + 8, shuffle_seed=4, dtype=BF)
+                   max_blocks=prefix // bs + 8, shuffle_seed=4, dtype=dtype, kv_scale=kv_scale)
     try:
         root = pool.new_seq(prefix + 40)
         Kp = rng.standard_normal((prefix, kv_dim)).astype(np.float32)
@@ -135,7 +168,7 @@ def test_bf16_copy_on_append_and_cascade():
         pool.grow(root, prefix)
         pool.write_history(root, 0, torch.from_numpy(Kp), torch.from_numpy(Vp))
         forks = [pkv.pkv_seq_fork(root) for _ in range(n_f)]
-        hist = {f: (oracle.round_bf16(Kp), oracle.round_bf16(Vp)) for f in forks}
+        hist = {f: (rnd(Kp), rnd(Vp)) for f in forks}
         for tag, n in ((1, 3), (2, 1)):
             M = len(forks)
             Q = rng.standard_normal((M * n, q_dim)).astype(np.float32)
@@ -157,8 +190,8 @@ def test_bf16_copy_on_append_and_cascade():
             got = out.cpu().numpy()
             for j, f in enumerate(forks):
                 kh, vh = hist[f]
-                kh = np.concatenate([kh, oracle.round_bf16(Kn[j * n:(j + 1) * n])])
-                vh = np.concatenate([vh, oracle.round_bf16(Vn[j * n:(j + 1) * n])])
+                kh = np.concatenate([kh, rnd(Kn[j * n:(j + 1) * n])])
+                vh = np.concatenate([vh, rnd(Vn[j * n:(j + 1) * n])])
                 hist[f] = (kh, vh)
                 rc, ref = oracle.attend(Q[j * n:(j + 1) * n], kh, vh, n, kh.shape[0], H, KV, hd, 1, scale)
                 assert rc == 0
@@ -166,9 +199,8 @@ def test_bf16_copy_on_append_and_cascade():
             if tag == 2:
                 assert n_pre == 1, "the decode step should take the shared-prefix pass"
         # the root still sees its own prefix, untouched by the forks' copies
-        Kr, _ = pool.read_history(root, 0, prefix)
-        assert np.array_equal(Kr.float().cpu().numpy().view(np.uint32),
-                              oracle.round_bf16(Kp).view(np.uint32))
+        Kr, _ = pool.read_values(root, 0, prefix)
+        assert np.array_equal(Kr.cpu().numpy().view(np.uint32), rnd(Kp).view(np.uint32))
     finally:
         pool.close()
 
