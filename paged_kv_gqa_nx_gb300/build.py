@@ -62,7 +62,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
             if src.endswith(".cu"):
                 cmd += ["-Xptxas", "-v"] if verbose else []
             else:
-                cmd = [nvcc] + COMMON + ["-x", "c++", "-c", path, "-o", obj]
+                cmd = [nvcc] + COMMON + extra + ["-x", "c++", "-c", path, "-o", obj]
             jobs.append(cmd)
     with cf.ThreadPoolExecutor(max_workers=max(1, len(jobs))) as ex:
         results = list(ex.map(lambda c: subprocess.run(c, capture_output=True, text=True), jobs))

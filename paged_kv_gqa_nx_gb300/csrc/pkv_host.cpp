@@ -974,6 +974,8 @@ void pkv_pool_free(pkv_pool *p) {
         p->part.release(p->stream);
         p->io_in.release(p->stream);
         p->io_out.release(p->stream);
+        p->qrot.release(p->stream);
+        p->img.release(p->stream);
         cudaStreamSynchronize(p->stream);
         p->stager.destroy();
         if (p->owns_kv) {
