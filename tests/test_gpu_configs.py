@@ -4,7 +4,9 @@ configuration the benchmark times (pkv_attn_batch, default split size).
 * batched decode, M = 64, Qwen3-4B attention shape: every row vs the oracle.
 * continuous-batching decode, M = 256, log-uniform lengths, 600 000-block
   shuffled pool: a sample of rows (the shortest, the longest, and a seeded
-  draw) vs the oracle, and the contiguous twin bit for bit on two of them.
+  draw) vs the oracle, and the contiguous twin bit for bit on two of them;
+  the same step on bf16 and fp8 pools (the benchmark's --kv-dtype runs) vs
+  the oracle over the rounded histories.
 * chunked prefill, 8 x (2048 + 512) over 4 layers: sampled queries per layer.
 * shared-prefix forks: 128 forks of an 8192-token prefix, divergent chunks,
   a batched decode step, truncation of half the forks and re-append; and the
@@ -31,11 +33,21 @@ def _oracle_row(Qr, Kf, Vf, n, tk, w, causal=1):
     return ref
 
 
-def build_decode(w, keep_rows, seed_base):
+# pool element -> (torch dtype, the oracle's rounding of the values a row reads back)
+FORMATS = {
+    "f32": (torch.float32, lambda x: x),
+    "bf16": (torch.bfloat16, oracle.round_bf16),
+    "fp8": (torch.float8_e4m3fn, lambda x: oracle.round_e4m3(x, 1.0)),
+}
+
+
+def build_decode(w, keep_rows, seed_base, fmt="f32"):
     """Pool + sequences holding each row's history (layer 0); returns host
-    copies of the histories of the rows in keep_rows."""
+    copies of the histories of the rows in keep_rows, as the pool stores them."""
+    dtype, rnd = FORMATS[fmt]
     pool = GpuPool(w.n_blocks, w.n_layers, w.kv_dim, w.block_size, max_seqs=w.M + 4,
-                   max_blocks=-(-(w.max_tokens() + 1) // w.block_size) + 1, shuffle_seed=w.seed)
+                   max_blocks=-(-(w.max_tokens() + 1) // w.block_size) + 1, shuffle_seed=w.seed,
+                   dtype=dtype)
     seqs, kept = [], {}
     for r in range(w.M):
         L = int(w.past_len[r])
@@ -45,15 +57,16 @@ def build_decode(w, keep_rows, seed_base):
         Vh = wl.normal((L, w.kv_dim), seed_base + 2 * r + 1, "cuda")
         pool.write_history(s, 0, Kh, Vh)
         if r in keep_rows:
-            kept[r] = (Kh.cpu().numpy(), Vh.cpu().numpy())
+            kept[r] = (rnd(Kh.cpu().numpy()), rnd(Vh.cpu().numpy()))
         del Kh, Vh
         seqs.append(s)
     torch.cuda.synchronize()
     return pool, seqs, kept
 
 
-def decode_step_and_check(w, rows_to_check, contig_rows=()):
-    pool, seqs, kept = build_decode(w, set(rows_to_check), w.seed * 1000)
+def decode_step_and_check(w, rows_to_check, contig_rows=(), fmt="f32"):
+    rnd = FORMATS[fmt][1]
+    pool, seqs, kept = build_decode(w, set(rows_to_check), w.seed * 1000, fmt)
     try:
         T = int(w.n_q.sum())
         Q = wl.normal((T, w.q_dim), w.seed + 101, "cuda")
@@ -69,8 +82,8 @@ def decode_step_and_check(w, rows_to_check, contig_rows=()):
         Qh, Knh, Vnh, outh = Q.cpu().numpy(), Kn.cpu().numpy(), Vn.cpu().numpy(), out.cpu().numpy()
         for r in rows_to_check:
             o, n, L = int(offs[r]), nq[r], int(w.past_len[r])
-            Kf = np.concatenate([kept[r][0], Knh[o:o + n]])
-            Vf = np.concatenate([kept[r][1], Vnh[o:o + n]])
+            Kf = np.concatenate([kept[r][0], rnd(Knh[o:o + n])])
+            Vf = np.concatenate([kept[r][1], rnd(Vnh[o:o + n])])
             ref = _oracle_row(Qh[o:o + n], Kf, Vf, n, L + n, w)
             assert_close(outh[o:o + n], ref, np.abs(Vf).max(), "%s row %d (len %d)" % (w.name, r, L))
             if r in contig_rows:
@@ -101,11 +114,27 @@ def test_continuous_batching_m256_sampled():
 
 
 @pytest.mark.gpu
-def test_chunked_prefill_sampled_queries():
+@pytest.mark.parametrize("fmt", ["bf16", "fp8"])
+def test_continuous_batching_m256_narrow_pool_sampled(fmt):
+    w = wl.continuous_batching_m256()
+    free, _ = torch.cuda.mem_get_info()
+    need = 2 * w.n_blocks * w.block_size * w.kv_dim * (2 if fmt == "bf16" else 1)
+    if free < need + (8 << 30):
+        pytest.skip("needs %.1f GB of device memory" % (need / 1e9))
+    rng = np.random.default_rng(w.seed + 8)
+    rows = sorted(set([int(np.argmin(w.past_len)), int(np.argmax(w.past_len))] +
+                      [int(x) for x in rng.choice(w.M, 8, replace=False)]))
+    decode_step_and_check(w, rows, fmt=fmt)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("fmt", ["f32", "bf16"])
+def test_chunked_prefill_sampled_queries(fmt):
     w = wl.chunked_prefill()
     bs = w.block_size
+    dtype, rnd = FORMATS[fmt]
     pool = GpuPool(w.n_blocks, w.n_layers, w.kv_dim, bs, max_seqs=w.M + 2,
-                   max_blocks=-(-w.max_tokens() // bs) + 1, shuffle_seed=w.seed)
+                   max_blocks=-(-w.max_tokens() // bs) + 1, shuffle_seed=w.seed, dtype=dtype)
     try:
         past, n = int(w.past_len[0]), int(w.n_q[0])
         seqs, hist = [], {}
@@ -117,7 +146,7 @@ def test_chunked_prefill_sampled_queries():
                 Vh = wl.normal((past, w.kv_dim), w.seed * 100 + 10 * r + 2 * layer + 1, "cuda")
                 pool.write_history(s, layer, Kh, Vh)
                 if r in (0, w.M - 1):
-                    hist[(r, layer)] = (Kh.cpu().numpy(), Vh.cpu().numpy())
+                    hist[(r, layer)] = (rnd(Kh.cpu().numpy()), rnd(Vh.cpu().numpy()))
             seqs.append(s)
         T = w.M * n
         nq = [n] * w.M
@@ -136,8 +165,8 @@ def test_chunked_prefill_sampled_queries():
         for layer in (0, w.n_layers - 1):
             Qh, Knh, Vnh, outh = results[layer]
             for r in (0, w.M - 1):
-                Kf = np.concatenate([hist[(r, layer)][0], Knh[r * n:(r + 1) * n]])
-                Vf = np.concatenate([hist[(r, layer)][1], Vnh[r * n:(r + 1) * n]])
+                Kf = np.concatenate([hist[(r, layer)][0], rnd(Knh[r * n:(r + 1) * n])])
+                Vf = np.concatenate([hist[(r, layer)][1], rnd(Vnh[r * n:(r + 1) * n])])
                 for i in (0, 1, 255, n - 1):
                     row = r * n + i
                     ref = _oracle_row(Qh[row:row + 1], Kf, Vf, 1, past + i + 1, w)
