@@ -408,6 +408,8 @@ def run_pkv(args):
         pkv.check(pkv.pkv_set_split_keys(args.split_keys))
     w = get_workload(args.workload)
     run = DeviceRun(w, rank, args.kv_dtype)
+    if args.image_cache_mb:
+        pkv.check(pkv.pkv_pool_set_image_cache(run.pool, args.image_cache_mb << 20))
     peak, peak_kind = measured_hbm_peak()
 
     for _ in range(args.warmup):
@@ -530,6 +532,7 @@ def run_pkv(args):
             "block_size": w.block_size, "n_blocks": w.n_blocks,
             "kv_bytes_per_step": run.kv_bytes, "split_keys": pkv.pkv_get_split_keys(),
             "parallelism": "replicas" if world > 1 else "single GPU",
+            "image_cache_mb": args.image_cache_mb,
             "l2": "no flush: each step reads %.2f GB of K/V, far above the 129 MB L2" % (run.kv_bytes / 1e9),
         },
         "rows_layers_per_s": round(world * run.T * w.n_layers / (ms_step * 1e-3), 1),
@@ -609,6 +612,9 @@ def main():
     ap.add_argument("--split-keys", type=int, default=0, help="keys per split-K unit (0: library default)")
     ap.add_argument("--kv-dtype", choices=["f32", "bf16", "fp8"], default="f32",
                     help="K/V pool storage (bf16 / fp8 e4m3: rows rounded on write, f32 math)")
+    ap.add_argument("--image-cache-mb", type=int, default=0,
+                    help="keep tensor-core operand images of unchanged pages across steps "
+                         "(pkv_pool_set_image_cache), up to this many MiB; 0 = off")
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)

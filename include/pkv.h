@@ -128,9 +128,30 @@ PKV_API int32_t pkv_pool_free_blocks(const pkv_pool *pool);
  *   [0] split-K decode units, [1] tensor-core prefill tiles, [2] shared-prefix
  *   tiles, [3] merge items, [4] visible (query, key) pairs of the prefill rows,
  *   [5] (query, key) pairs of the shared-prefix pass, [6] 1 if the call ran
- *   with the fused append. */
-#define PKV_WORK_FIELDS 7
+ *   with the fused append, [7] operand images (64-key tile x kv heads) the
+ *   call took from the image cache, [8] operand images it built. */
+#define PKV_WORK_FIELDS 9
 PKV_API int pkv_pool_last_work(const pkv_pool *pool, int64_t *out, int32_t cap);
+
+/* Operand-image cache (no counterpart on the pages; off by default).  The
+ * tensor-core launches read every 64-key tile they attend as an image of
+ * tf32 hi/lo planes (n_kv_heads x 128 KiB per tile, head_dim 128), which a
+ * split pass builds from the pool.  With the cache on, images of tiles whose
+ * pages have not been written since are kept across calls in up to
+ * max_bytes of device memory (least recently used first out) instead of
+ * being rebuilt: a chunked prefill then splits each key tile once rather
+ * than once per later chunk, and the pages of a shared prefix once rather
+ * than once per decode step.  A tile is identified by its layer, its length
+ * and the pages holding it with their write generations; the library bumps a
+ * page's generation whenever it writes the page (append, copy-on-append,
+ * allocation).  Writes into caller-owned pool storage that bypass the
+ * library are not seen: call this function again after them, which forgets
+ * every cached image.  A call that needs more tiles than the cache holds
+ * builds its images as without the cache.  max_bytes = 0 turns the cache off
+ * and frees it.  Returns PKV_OK; PKV_ERR_ARG for a NULL or host-only pool or a
+ * negative size; PKV_ERR_CUDA if the buffer cannot be allocated (the cache is
+ * then off). */
+PKV_API int pkv_pool_set_image_cache(pkv_pool *pool, int64_t max_bytes);
 
 /* Allocate one block: its id (refcount 1), or -1 when the pool is exhausted
  * ("nx_paged_kv_gate.nx source", KAT section: ids 0,1,2 then -1). */

@@ -102,6 +102,7 @@ _SIGS = {
     "pkv_get_fused_append": (_i32, []),
     "pkv_set_cascade": (_int, [_i32]),
     "pkv_pool_last_work": (_int, [_vp, ctypes.POINTER(ctypes.c_int64), _i32]),
+    "pkv_pool_set_image_cache": (_int, [_vp, ctypes.c_int64]),
     "pkv_pool_set_kv_scale": (_int, [_vp, _f32]),
     "pkv_get_cascade": (_i32, []),
     "pkv_launch_count": (_i64, []),
@@ -362,9 +363,9 @@ def pkv_get_fused_append():
     return bool(_lib.pkv_get_fused_append())
 
 
-PKV_WORK_FIELDS = 7
+PKV_WORK_FIELDS = 9
 WORK_FIELD_NAMES = ("decode_units", "prefill_tiles", "prefix_tiles", "merge_items",
-                    "prefill_pairs", "prefix_pairs", "fused_append")
+                    "prefill_pairs", "prefix_pairs", "fused_append", "image_hits", "image_builds")
 
 
 def pkv_pool_last_work(pool):
@@ -372,6 +373,10 @@ def pkv_pool_last_work(pool):
     buf = (ctypes.c_int64 * PKV_WORK_FIELDS)()
     check(_lib.pkv_pool_last_work(pool, buf, PKV_WORK_FIELDS))
     return dict(zip(WORK_FIELD_NAMES, list(buf)))
+
+
+def pkv_pool_set_image_cache(pool, max_bytes):
+    return _lib.pkv_pool_set_image_cache(pool, int(max_bytes))
 
 
 def pkv_pool_set_kv_scale(pool, scale):

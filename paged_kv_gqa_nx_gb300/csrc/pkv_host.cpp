@@ -21,6 +21,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <list>
 #include <mutex>
 #include <string>
 #include <unordered_map>
@@ -256,6 +257,61 @@ int32_t ceil_div(int64_t a, int64_t b) { return static_cast<int32_t>((a + b - 1)
 
 struct pkv_seq;
 
+// Operand images kept across calls (pkv_pool_set_image_cache).  A slot
+// holds one 64-key tile's images for every kv head; `map` finds the slot of a
+// tile key (layer, length, offset in the first page, and each covering page
+// with its write generation), `lru` orders the occupied slots, most recently
+// used first.
+struct ImageCache {
+    int32_t n_slots = 0;  // 0: off
+    size_t slot_bytes = 0;
+    DevBuf buf;
+    std::unordered_map<std::string, int32_t> map;
+    std::vector<std::string> key_of;
+    std::list<int32_t> lru;
+    std::vector<std::list<int32_t>::iterator> where;
+    std::vector<char> in_lru;
+    std::vector<int32_t> free_slots;
+
+    void reset(int32_t n) {
+        n_slots = n;
+        map.clear();
+        lru.clear();
+        key_of.assign(n, std::string());
+        where.assign(n, lru.end());
+        in_lru.assign(n, 0);
+        free_slots.clear();
+        for (int32_t i = n - 1; i >= 0; --i) free_slots.push_back(i);
+    }
+    // The slot of `key`; `hit` tells whether it already holds the images.  A
+    // miss takes a free slot or the least recently used one.
+    int32_t get(const std::string &key, bool &hit) {
+        auto it = map.find(key);
+        int32_t slot;
+        if (it != map.end()) {
+            hit = true;
+            slot = it->second;
+            lru.erase(where[slot]);
+        } else {
+            hit = false;
+            if (!free_slots.empty()) {
+                slot = free_slots.back();
+                free_slots.pop_back();
+            } else {
+                slot = lru.back();
+                lru.pop_back();
+                map.erase(key_of[slot]);
+            }
+            key_of[slot] = key;
+            map.emplace(key, slot);
+        }
+        lru.push_front(slot);
+        where[slot] = lru.begin();
+        in_lru[slot] = 1;
+        return slot;
+    }
+};
+
 struct pkv_pool {
     int32_t n_blocks = 0, n_layers = 0, kv_dim = 0, bs = 0, bs_shift = -1;
     int32_t max_seqs = 0, max_blocks = 0;
@@ -271,6 +327,8 @@ struct pkv_pool {
     int device = 0;
 
     int64_t last_work[PKV_WORK_FIELDS] = {};  // work list of the last attend call
+    std::vector<uint32_t> gen;  // write generation per (block, layer)
+    ImageCache icache;
 
     std::vector<int32_t> free_stack;   // top = back
     std::vector<int32_t> refcnt;
@@ -311,11 +369,23 @@ void mark_dirty(pkv_seq *s, int32_t lo, int32_t hi) {
     }
 }
 
+// A page about to receive new contents (a fresh block, a copy-on-append
+// target, appended rows): images made from its old contents are stale.
+void bump_gen(pkv_pool *p, int32_t b, int32_t layer) {
+    if (p->gen.empty()) return;
+    if (layer >= 0) {
+        ++p->gen[static_cast<size_t>(b) * p->n_layers + layer];
+    } else {
+        for (int32_t l = 0; l < p->n_layers; ++l) ++p->gen[static_cast<size_t>(b) * p->n_layers + l];
+    }
+}
+
 int32_t pop_block(pkv_pool *p) {
     if (p->free_stack.empty()) return -1;
     int32_t b = p->free_stack.back();
     p->free_stack.pop_back();
     p->refcnt[b] = 1;
+    bump_gen(p, b, -1);
     return b;
 }
 
@@ -694,22 +764,69 @@ int run_layer(pkv_seq *const *seqs, int32_t M, const int32_t *n_q, const float *
         std::copy(vals, vals + PKV_WORK_FIELDS, p->last_work);
     }
 
+    // the pages this call writes get new generations
+    for (const AppendDesc &ad : app) bump_gen(p, ad.blk, layer);
+
     // operand images for the tensor-core launches: every 64-key tile of each
-    // row with prefill tiles (real rows and shared-prefix virtual rows)
-    std::vector<int32_t> img_tile0;
+    // row with prefill tiles (real rows and shared-prefix virtual rows).  Tile
+    // kt of row r is image img_slot[img_tile0[r] + kt]; the split pass builds
+    // the ones listed in split_items.  With the image cache, a tile whose
+    // pages are unchanged since an earlier call keeps that call's image.
+    std::vector<int32_t> img_tile0, img_slot;
     std::vector<SplitItem> split_items;
+    bool cached = false;
+    int64_t img_hits = 0;
     if (!w.tiles.empty() || !w.ctiles.empty()) {
         img_tile0.assign(rows.size(), -1);
+        std::vector<int32_t> order;  // rows needing images, first use first
         int32_t next = 0;
         auto need = [&](int32_t r) {
             if (img_tile0[r] >= 0) return;
-            const int32_t nt = ceil_div(rows[r].past_len + rows[r].n_q, kKeyTile);
             img_tile0[r] = next;
-            next += nt;
-            for (int32_t kt = 0; kt < nt; ++kt) split_items.push_back({r, kt});
+            next += ceil_div(rows[r].past_len + rows[r].n_q, kKeyTile);
+            order.push_back(r);
         };
         for (const PrefillTile &t : w.tiles) need(t.row);
         for (const PrefillTile &t : w.ctiles) need(t.row);
+        img_slot.resize(next);
+        ImageCache &ic = p->icache;
+        cached = ic.n_slots >= next && ic.slot_bytes == static_cast<size_t>(n_kv_heads) * kImageBytes;
+        // the host page table of each row: a shared-prefix virtual row reads
+        // its first member's (add_cascades appends them in cascade order)
+        auto row_seq = [&](int32_t r) { return r < M ? seqs[r] : seqs[cas[r - M].r0]; };
+        std::string key;
+        for (int32_t r : order) {
+            const int32_t tk = rows[r].past_len + rows[r].n_q, nt = ceil_div(tk, kKeyTile);
+            const pkv_seq *sq = row_seq(r);
+            for (int32_t kt = 0; kt < nt; ++kt) {
+                const int32_t i = img_tile0[r] + kt;
+                if (!cached) {
+                    img_slot[i] = i;
+                    split_items.push_back({r, kt, i});
+                    continue;
+                }
+                const int32_t k0 = kt * kKeyTile, nv = std::min(kKeyTile, tk - k0);
+                const int32_t g0 = k0 / p->bs, g1 = (k0 + nv - 1) / p->bs;
+                key.clear();
+                auto put = [&](int32_t v) { key.append(reinterpret_cast<const char *>(&v), sizeof v); };
+                put(layer);
+                put(nv);
+                put(k0 % p->bs);
+                for (int32_t g = g0; g <= g1; ++g) {
+                    const int32_t b = sq->pt[g];
+                    put(b);
+                    put(static_cast<int32_t>(p->gen[static_cast<size_t>(b) * p->n_layers + layer]));
+                }
+                bool hit = false;
+                img_slot[i] = ic.get(key, hit);
+                if (hit) ++img_hits;
+                else split_items.push_back({r, kt, img_slot[i]});
+            }
+        }
+    }
+    if (attend) {
+        p->last_work[7] = img_hits;
+        p->last_work[8] = static_cast<int64_t>(split_items.size());
     }
 
     Blob &blob = p->blob;
@@ -726,6 +843,7 @@ int run_layer(pkv_seq *const *seqs, int32_t M, const int32_t *n_q, const float *
     const size_t ctiles_off = blob.put(w.ctiles.data(), w.ctiles.size());
     const size_t merges_off = blob.put(w.merges.data(), w.merges.size());
     const size_t tile0_off = blob.put(img_tile0.data(), img_tile0.size());
+    const size_t slot_off = blob.put(img_slot.data(), img_slot.size());
     const size_t split_off = blob.put(split_items.data(), split_items.size());
 
     cudaError_t e = upload_blob(p);
@@ -808,17 +926,24 @@ int run_layer(pkv_seq *const *seqs, int32_t M, const int32_t *n_q, const float *
         a.pl = a.pm + pf;
         a.pacc = a.pl + pf;
     }
-    const unsigned char *img = nullptr;
+    unsigned char *img = nullptr;
+    if (!img_slot.empty()) {
+        if (cached) {
+            img = static_cast<unsigned char *>(p->icache.buf.p);
+        } else {
+            e = p->img.ensure(img_slot.size() * n_kv_heads * kImageBytes, st, p->device);
+            if (e != cudaSuccess) return cuda_fail(e, "operand image buffer");
+            img = static_cast<unsigned char *>(p->img.p);
+        }
+    }
     if (!split_items.empty()) {
-        const size_t img_bytes = static_cast<size_t>(split_items.size()) * n_kv_heads * kImageBytes;
-        e = p->img.ensure(img_bytes, st, p->device);
-        if (e != cudaSuccess) return cuda_fail(e, "operand image buffer");
         const SplitArgs sa{a.rows, dptr<SplitItem>(p, split_off), static_cast<int32_t>(split_items.size()),
-                           n_kv_heads, static_cast<unsigned char *>(p->img.p),
-                           dptr<int32_t>(p, tile0_off), p->err_dev};
+                           n_kv_heads, img, p->err_dev};
         e = launch(PKV_KERNEL_SPLIT, st, [&] { return launch_split_paged(sa, addr, st); });
-        if (e != cudaSuccess) return cuda_fail(e, "split kernel");
-        img = static_cast<const unsigned char *>(p->img.p);
+        if (e != cudaSuccess) {
+            if (cached) p->icache.reset(p->icache.n_slots);  // the missed images were not made
+            return cuda_fail(e, "split kernel");
+        }
     }
     if (!w.tiles.empty()) {
         PrefillArgs pa{Qd, Od, a.rows, dptr<PrefillTile>(p, tiles_off),
@@ -827,6 +952,7 @@ int run_layer(pkv_seq *const *seqs, int32_t M, const int32_t *n_q, const float *
                        p->err_dev};
         pa.img = img;
         pa.img_tile0 = dptr<int32_t>(p, tile0_off);
+        pa.img_slot = dptr<int32_t>(p, slot_off);
         pa.lo_zero = p->narrow() ? 1 : 0;
         e = launch(PKV_KERNEL_PREFILL, st, [&] { return launch_prefill_paged(pa, addr, st); });
         if (e != cudaSuccess) return cuda_fail(e, "prefill kernel");
@@ -838,6 +964,7 @@ int run_layer(pkv_seq *const *seqs, int32_t M, const int32_t *n_q, const float *
                        n_kv_heads, a.group, 0, S, a.scale_log2, p->err_dev};
         pa.img = img;
         pa.img_tile0 = dptr<int32_t>(p, tile0_off);
+        pa.img_slot = dptr<int32_t>(p, slot_off);
         pa.lo_zero = p->narrow() ? 1 : 0;
         e = launch(PKV_KERNEL_PREFILL, st, [&] { return launch_prefill_paged(pa, addr, st); });
         if (e != cudaSuccess) return cuda_fail(e, "shared-prefix kernel");
@@ -976,6 +1103,7 @@ void pkv_pool_free(pkv_pool *p) {
         p->io_out.release(p->stream);
         p->qrot.release(p->stream);
         p->img.release(p->stream);
+        p->icache.buf.release(p->stream);
         cudaStreamSynchronize(p->stream);
         p->stager.destroy();
         if (p->owns_kv) {
@@ -986,6 +1114,34 @@ void pkv_pool_free(pkv_pool *p) {
         cudaFree(p->err_dev);
     }
     delete p;
+}
+
+int pkv_pool_set_image_cache(pkv_pool *p, int64_t max_bytes) {
+    if (!p || p->host_only) return fail(PKV_ERR_ARG, "image cache needs a device pool");
+    if (max_bytes < 0) return fail(PKV_ERR_ARG, "negative image cache size");
+    DevGuard dg(p->device);
+    ImageCache &ic = p->icache;
+    // one slot: a 64-key tile's images for every kv head of head_dim 128
+    const size_t slot_bytes = static_cast<size_t>(ceil_div(p->kv_dim, 128)) * kImageBytes;
+    const int64_t n = max_bytes / static_cast<int64_t>(slot_bytes);
+    ic.reset(0);
+    ic.buf.release(p->stream);
+    if (n <= 0) {
+        p->gen.clear();
+        p->gen.shrink_to_fit();
+        return PKV_OK;
+    }
+    if (n > 0x7fffffffLL) return fail(PKV_ERR_ARG, "image cache too large");
+    cudaError_t e = ic.buf.ensure(static_cast<size_t>(n) * slot_bytes, p->stream, p->device);
+    if (e != cudaSuccess) {
+        ic.buf.release(p->stream);
+        return cuda_fail(e, "image cache buffer");
+    }
+    // generations start over: nothing cached depends on earlier ones
+    p->gen.assign(static_cast<size_t>(p->n_blocks) * p->n_layers, 0u);
+    ic.slot_bytes = slot_bytes;
+    ic.reset(static_cast<int32_t>(n));
+    return PKV_OK;
 }
 
 int pkv_pool_set_stream(pkv_pool *p, pkv_stream_t stream) {

@@ -114,10 +114,12 @@ struct PrefillArgs {
     int32_t n_heads, n_kv, group, causal, split_keys;
     float scale_log2;
     int32_t *err;
-    // Paged launches: the K/V operand images made by the split pass; row r's
-    // key tile kt for kv head h is image (img_tile0[r] + kt) * n_kv + h.
+    // Paged launches: the K/V operand images made by the split pass (or kept
+    // from earlier calls); row r's key tile kt for kv head h is image
+    // img_slot[img_tile0[r] + kt] * n_kv + h.
     const unsigned char *img = nullptr;
     const int32_t *img_tile0 = nullptr;
+    const int32_t *img_slot = nullptr;
     // the images' lo planes are zero (a bf16 pool: every K/V value is exact
     // in tf32), so the products with them and their copies are skipped
     int32_t lo_zero = 0;
@@ -131,9 +133,10 @@ constexpr int32_t kKeyTile = 64;  // keys per tensor-core tile (and per image)
 constexpr uint32_t kImagePlane = 32 * 1024;
 constexpr uint32_t kImageBytes = 4 * kImagePlane;
 
-// One image to make: key tile kt of row `row` (all kv heads).
+// One image to make: key tile kt of row `row` (all kv heads), into image
+// slot `slot` (images slot * n_kv + h).
 struct SplitItem {
-    int32_t row, kt;
+    int32_t row, kt, slot;
 };
 
 struct SplitArgs {
@@ -141,7 +144,6 @@ struct SplitArgs {
     const SplitItem *items;
     int32_t n_items, n_kv;
     unsigned char *img;
-    const int32_t *img_tile0;
     int32_t *err;
 };
 

@@ -224,21 +224,25 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs a, 
             // done, in the order the tensor core completes them: QK(kt0), then
             // QK(kt+1), PV(kt), ...  Each copy arrives with its byte count on
             // the operand barrier that the MMA warp waits on.
-            const unsigned char *img0 =
-                a.img + (static_cast<size_t>(a.img_tile0[tile.row]) * a.n_kv + kvh) * kImageBytes;
-            const size_t img_step = static_cast<size_t>(a.n_kv) * kImageBytes;
+            // tile kt's image slot; read a copy ahead of its use (slot_at is
+            // called only by lane 0)
+            const int32_t *slots = a.img_slot + a.img_tile0[tile.row];
+            auto slot_at = [&](int kt) { return kt < kt1 ? __ldg(slots + kt) : 0; };
+            auto image = [&](int32_t slot) {
+                return a.img + (static_cast<size_t>(slot) * a.n_kv + kvh) * kImageBytes;
+            };
             constexpr uint32_t planes = kLoZero ? 1u : 2u;  // hi (and lo) of K / V
-            auto copy_k = [&](int kt) {
+            auto copy_k = [&](int32_t slot) {
                 if (lane == 0) {
-                    const unsigned char *src = img0 + static_cast<size_t>(kt) * img_step;
+                    const unsigned char *src = image(slot);
                     mbar_expect_tx(smem_u32(&bar_k), planes * kImagePlane);
                     bulk_g2s(smem_u32(Khi), src, kImagePlane, smem_u32(&bar_k));
                     if constexpr (planes == 2) bulk_g2s(smem_u32(Klo), src + kImagePlane, kImagePlane, smem_u32(&bar_k));
                 }
             };
-            auto copy_v = [&](int kt) {
+            auto copy_v = [&](int32_t slot) {
                 if (lane == 0) {
-                    const unsigned char *src = img0 + static_cast<size_t>(kt) * img_step + 2 * kImagePlane;
+                    const unsigned char *src = image(slot) + 2 * kImagePlane;
                     mbar_expect_tx(smem_u32(&bar_p), planes * kImagePlane);
                     bulk_g2s(smem_u32(Vhi), src, kImagePlane, smem_u32(&bar_p));
                     if constexpr (planes == 2) bulk_g2s(smem_u32(Vlo), src + kImagePlane, kImagePlane, smem_u32(&bar_p));
@@ -251,23 +255,31 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs a, 
             };
             uint32_t ph_qkd = 0, ph_pvd = 0;
             bool cok = true;
-            if (kt0 < kt1) {
-                copy_k(kt0);
-                copy_v(kt0);
-                if (kt0 + 1 < kt1) {
-                    cok = wait_c(&bar_qk, ph_qkd);  // QK(kt0) done
-                    if (cok) copy_k(kt0 + 1);
-                }
+            int32_t s_v = 0, s_k = 0;  // slots of the next V copy (kt + 1) and K copy (kt + 2)
+            if (lane == 0 && kt0 < kt1) {
+                const int32_t s0 = slot_at(kt0);
+                s_v = slot_at(kt0 + 1);
+                s_k = slot_at(kt0 + 2);
+                copy_k(s0);
+                copy_v(s0);
+            }
+            if (kt0 + 1 < kt1) {
+                cok = wait_c(&bar_qk, ph_qkd);  // QK(kt0) done
+                if (cok) copy_k(s_v);
             }
             for (int kt = kt0; kt + 1 < kt1 && cok; ++kt) {
                 if (kt + 2 < kt1) {
                     cok = wait_c(&bar_qk, ph_qkd);  // QK(kt+1) done: the K buffer is free
                     if (!cok) break;
-                    copy_k(kt + 2);
+                    copy_k(s_k);
                 }
                 cok = wait_c(&bar_pv, ph_pvd);  // PV(kt) done: the V buffer is free
                 if (!cok) break;
-                copy_v(kt + 1);
+                copy_v(s_v);
+                if (lane == 0) {
+                    s_v = s_k;
+                    s_k = slot_at(kt + 3);
+                }
             }
             // let the last copies land before the CTA's shared memory is given
             // up (their phases also need the compute warps; bounded if those
@@ -743,8 +755,7 @@ __global__ void __launch_bounds__(256) split_kernel(SplitArgs p, PagedRowsP<E> r
         vd[3] = vx.w;
     }
     __syncthreads();
-    unsigned char *out =
-        p.img + (static_cast<size_t>(p.img_tile0[t.row] + t.kt) * p.n_kv + kvh) * kImageBytes;
+    unsigned char *out = p.img + (static_cast<size_t>(t.slot) * p.n_kv + kvh) * kImageBytes;
     for (int q = threadIdx.x; q < static_cast<int>(kImagePlane / 16); q += blockDim.x) {
         float4 h, l;
         {
