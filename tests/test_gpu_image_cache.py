@@ -190,3 +190,47 @@ def test_image_cache_argument_checks():
         assert pkv.pkv_pool_set_image_cache(pool.p, 1 << 20) == pkv.PKV_OK
     finally:
         pool.close()
+
+
+@pytest.mark.gpu
+def test_two_layers_and_copy_on_append():
+    # forks of an unaligned prefix: the first append copies the shared tail
+    # page (a new block, new generation) in each fork; two layers keep
+    # separate images of the same pages
+    prefix, n_f, chunk, L = 1000, 3, 80, 2
+    g = torch.Generator(device="cuda").manual_seed(6)
+    pools = [GpuPool(prefix // BS + 24 * n_f + 16, L, KV_DIM, BS, max_seqs=n_f + 4,
+                     max_blocks=(prefix + 3 * chunk) // BS + 2, shuffle_seed=7) for _ in range(2)]
+    try:
+        pkv.check(pkv.pkv_pool_set_image_cache(pools[0].p, CACHE_BYTES))
+        hist = [(_rand(prefix, KV_DIM, g), _rand(prefix, KV_DIM, g)) for _ in range(L)]
+        forks = []
+        for p in pools:
+            root = p.new_seq(prefix + 3 * chunk)
+            p.grow(root, prefix)
+            for layer in range(L):
+                p.write_history(root, layer, *hist[layer])
+            forks.append([pkv.pkv_seq_fork(root) for _ in range(n_f)])
+        for c in range(3):
+            nq = [chunk] * n_f
+            for p, ff in zip(pools, forks):
+                pkv.check(pkv.pkv_ensure_append_batch(ff, nq))
+            for layer in range(L):
+                Q = _rand(n_f * chunk, Q_DIM, g)
+                K, V = _rand(n_f * chunk, KV_DIM, g), _rand(n_f * chunk, KV_DIM, g)
+                outs = []
+                for p, ff in zip(pools, forks):
+                    out = torch.empty(n_f * chunk, Q_DIM, device="cuda")
+                    pkv.check(pkv.pkv_attn_batch(ff, nq, Q, K, V, H, KV, HD, layer, 1, SCALE, out))
+                    p.check_no_device_error()
+                    outs.append(out)
+                torch.cuda.synchronize()
+                assert bits_equal(outs[0], outs[1]), "chunk %d layer %d" % (c, layer)
+                wk = pkv.pkv_pool_last_work(pools[0].p)
+                if c > 0:
+                    assert wk["image_hits"] > 0, (c, layer, wk)
+            for p, ff in zip(pools, forks):
+                pkv.check(pkv.pkv_advance_batch(ff, nq))
+    finally:
+        for p in pools:
+            p.close()
