@@ -732,7 +732,12 @@ __global__ void __launch_bounds__(256) split_kernel(SplitArgs p, PagedRowsP<E> r
     const RowDesc rd = p.rows[t.row];
     const int total_k = rd.past_len + rd.n_q;
     const int key0 = t.kt * kKT;
-    for (int i = threadIdx.x; i < kKT * (kHD / 4); i += blockDim.x) {
+    // 256 threads x 8 passes = 64 keys x 32 float4 chunks; unrolled, so that
+    // a thread's 16 row loads are in flight together
+    static_assert(kKT * (kHD / 4) == 256 * 8, "one tile per 8 passes of 256 threads");
+#pragma unroll
+    for (int pass = 0; pass < 8; ++pass) {
+        const int i = threadIdx.x + 256 * pass;
         const int key = i >> 5, ch = i & 31, pos = key0 + key;
         float4 kx = make_float4(0.f, 0.f, 0.f, 0.f), vx = kx;
         if (pos < total_k) {
