@@ -185,3 +185,17 @@ def test_capacity_errors_match():
         t.compare()
     finally:
         t.close()
+
+
+def test_image_cache_needs_a_device_pool():
+    # the operand-image cache lives in device memory: a host-only pool, a NULL
+    # pool and a negative size are argument errors, and nothing is allocated
+    p = host_pool(8, 1, 16, 4, 2, 4)
+    try:
+        assert pkv.pkv_pool_set_image_cache(p, 1 << 20) == pkv.PKV_ERR_ARG
+        assert pkv.pkv_pool_set_image_cache(p, 0) == pkv.PKV_ERR_ARG
+        assert pkv.pkv_pool_set_image_cache(None, 1 << 20) == pkv.PKV_ERR_ARG
+        assert "device pool" in pkv.pkv_last_error()
+        assert pkv.pkv_alloc_block(p) == 0   # the pool itself is untouched
+    finally:
+        pkv.pkv_pool_free(p)
