@@ -9,7 +9,8 @@ Contents
 --------
 ``attend``            dense offset-causal GQA attention over a contiguous
                       K/V history (C core in ``attention.c``, double
-                      accumulation, rounded once to f32).
+                      accumulation, rounded once to f32; ``set_threads``
+                      spreads its (query, head) pairs over host cores).
 ``ContiguousCache``   the contiguous per-layer K/V history a sequence would
                       have, with append / advance / truncate / fork
                       (``contiguous_cache.py``).
@@ -47,14 +48,19 @@ ERR_BAD_GQA = 2
 
 
 def build(force: bool = False) -> str:
-    """Compile ``attention.c`` into ``liboracle.so`` with gcc (plain -O2, no
-    fast-math, no host-specific flags) when it is missing or stale."""
+    """Compile ``attention.c`` into ``liboracle.so`` with gcc when it is
+    missing or stale: -O3, OpenMP over (query, head) pairs, no fast-math, no
+    contraction into fused multiply-adds, no host-specific flags.  Without
+    OpenMP support the same source builds single-threaded."""
     if (not force and os.path.exists(_LIB)
             and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC)):
         return _LIB
     tmp = _LIB + ".tmp.%d" % os.getpid()
-    subprocess.check_call(["gcc", "-O2", "-std=c11", "-fPIC", "-shared",
-                           "-o", tmp, _SRC, "-lm"])
+    base = ["gcc", "-O3", "-std=c11", "-ffp-contract=off", "-fPIC", "-shared", "-o", tmp, _SRC]
+    try:
+        subprocess.check_call(base + ["-fopenmp", "-lm"], stderr=subprocess.DEVNULL)
+    except subprocess.CalledProcessError:
+        subprocess.check_call(base + ["-lm"])
     os.replace(tmp, _LIB)
     return _LIB
 
@@ -69,8 +75,18 @@ def _load():
                                           ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                           ctypes.c_int, ctypes.c_float, fp]
             lib.oracle_attend.restype = ctypes.c_int
+            lib.oracle_set_threads.argtypes = [ctypes.c_int]
+            lib.oracle_set_threads.restype = ctypes.c_int
+            lib.oracle_set_threads(0)
             _lib = lib
     return _lib
+
+
+def set_threads(n: int) -> int:
+    """Threads for ``attend`` from now on (n < 1: every core the host offers;
+    the default).  Returns the count in effect (1 when the C core was built
+    without OpenMP).  The result does not depend on it."""
+    return int(_load().oracle_set_threads(int(n)))
 
 
 def _padded(a: np.ndarray, n: int) -> np.ndarray:
@@ -121,5 +137,5 @@ from . import pool_model  # noqa: E402
 from .rope import rope_neox, rope_neox_f32  # noqa: E402
 from .kv_format import round_bf16, round_e4m3  # noqa: E402
 
-__all__ = ["attend", "build", "ContiguousCache", "PoolModel", "SeqModel", "pool_model",
+__all__ = ["attend", "build", "set_threads", "ContiguousCache", "PoolModel", "SeqModel", "pool_model",
            "OK", "ERR_BAD_DIM", "ERR_BAD_GQA"]

@@ -261,3 +261,22 @@ def test_mutations_are_caught(name, tmp_path):
         except (AssertionError, ValueError, TypeError, FloatingPointError):
             failures += 1
     assert failures > 0, "planted mistake %s passed every pin" % name
+
+
+def test_thread_count_does_not_change_bits():
+    """Each (query, head) pair is computed by one thread in a fixed order, so
+    the oracle gives the same bits on one thread and on every core."""
+    rng = np.random.default_rng(11)
+    n_q, tk, H, KV, hd = 7, 300, 8, 2, 16
+    Q = rng.standard_normal((n_q, H * hd)).astype(np.float32)
+    K = rng.standard_normal((tk, KV * hd)).astype(np.float32)
+    V = rng.standard_normal((tk, KV * hd)).astype(np.float32)
+    try:
+        oracle.set_threads(1)
+        rc1, o1 = oracle.attend(Q, K, V, n_q, tk, H, KV, hd, 1, 0.25)
+        n = oracle.set_threads(0)
+        rcn, on = oracle.attend(Q, K, V, n_q, tk, H, KV, hd, 1, 0.25)
+    finally:
+        oracle.set_threads(0)
+    assert rc1 == rcn == 0 and n >= 1
+    assert np.array_equal(o1, on)
