@@ -60,8 +60,16 @@ enum pkv_status {
     PKV_ERR_CAPACITY = 5,      /* len + n exceeds the sequence's max_tokens        */
     PKV_ERR_ARG = 6,           /* any other bad argument (NULL, alignment, dup)    */
     PKV_ERR_CUDA = 7,          /* a CUDA call failed                               */
-    PKV_ERR_DEVICE_BOUNDS = 8  /* a kernel met a page-table entry out of range     */
+    PKV_ERR_DEVICE_BOUNDS = 8, /* a kernel met a block id or page index out of range
+                                  and skipped that access                          */
+    PKV_ERR_DEVICE_TIMEOUT = 9 /* a kernel's bounded wait ran out; the tile it was
+                                  working on was not written                       */
 };
+
+/* Bits of a device error word (the kernels OR them in; the sync calls below
+ * read, clear and map them to PKV_ERR_DEVICE_BOUNDS / PKV_ERR_DEVICE_TIMEOUT). */
+#define PKV_DEVERR_BOUNDS 1u
+#define PKV_DEVERR_TIMEOUT 2u
 
 typedef struct pkv_pool pkv_pool;
 typedef struct pkv_seq pkv_seq;
@@ -288,7 +296,8 @@ PKV_API int pkv_attn_batch_host(pkv_seq *const *seqs, int32_t M, const int32_t *
  * gate in "nx_paged_kv_gate.nx source"): the same kernels over a contiguous
  * history.  Kc, Vc: device [total_k, n_kv_heads*head_dim], already holding the
  * n_q new rows at the end; Q, out: device [n_q, n_heads*head_dim].  For the
- * same history it returns the paged path's output bit for bit. */
+ * same history it returns the paged path's output bit for bit.  Failures the
+ * kernels find on the device are read by pkv_contiguous_sync_error. */
 PKV_API int pkv_attn_contiguous(const float *Q, const float *Kc, const float *Vc, int32_t n_q,
                         int32_t total_k, int32_t n_heads, int32_t n_kv_heads, int32_t head_dim,
                         int32_t causal, float scale, float *out, pkv_stream_t stream);
@@ -306,11 +315,15 @@ PKV_API int pkv_attn_contiguous(const float *Q, const float *Kc, const float *Vc
  * the library until the process exits.  The caller still passes the inputs and
  * the output.  Requests whose scratch would exceed the array are rejected with
  * PKV_ERR_CAPACITY before any work is enqueued (pkv_last_error() names the sizes).
- * The first call on a device looks up the array's device address (a one-time
- * set-up with that device current); make that first call before any stream
- * capture.  Every call shares the array and finds the previous call's contents
- * in it: calls whose GPU work overlaps (different streams, or threads without
- * ordering between their streams) race; calls on one stream are ordered. */
+ * The first call on a device does a one-time set-up with that device current:
+ * it looks up the array's device address and clears the array's error word
+ * (waiting for the device to finish the clear); make that first call before
+ * any stream capture.  Every call shares the array and finds the previous
+ * call's contents in it: calls whose GPU work overlaps (different streams, or
+ * threads without ordering between their streams) race; calls on one stream
+ * are ordered.  Failures the kernels find on the device (PKV_DEVERR_*)
+ * gather in the array's error word until pkv_contiguous_sync_error reads
+ * them. */
 #define PKV_NOALLOC_SCRATCH_BYTES (16u << 20)
 PKV_API int pkv_attn_contiguous_noalloc(const float *Q, const float *Kc, const float *Vc,
                                         int32_t n_q, int32_t total_k, int32_t n_heads,
@@ -320,9 +333,37 @@ PKV_API int pkv_attn_contiguous_noalloc(const float *Q, const float *Kc, const f
 /* ---------------------------------------------------------- diagnostics ---- */
 
 /* Wait for the pool stream, then return and clear the pool's device error
- * flag: PKV_OK, PKV_ERR_DEVICE_BOUNDS (a kernel met a block id or page index
- * out of range and skipped that access), or PKV_ERR_CUDA. */
+ * word (the fail-fast return codes of "nx_f32_attn_paged.nx source", applied
+ * to failures found on the device after a call has returned): PKV_OK;
+ * PKV_ERR_DEVICE_TIMEOUT if a kernel's bounded wait ran out (the tile it was
+ * working on left its output unwritten); PKV_ERR_DEVICE_BOUNDS if a kernel
+ * met a block id or page index out of range and skipped that access; or
+ * PKV_ERR_CUDA.  When both happened the timeout is reported and
+ * pkv_last_error() names both. */
 PKV_API int pkv_sync_error(pkv_pool *pool);
+
+/* The same for the contiguous entry points, which have no pool: wait for
+ * `stream`, then read and clear the current device's error words of
+ * pkv_attn_contiguous and pkv_attn_contiguous_noalloc (each word gathers the
+ * bits of every call on that device since it was last read).  Returns
+ * PKV_OK, PKV_ERR_DEVICE_TIMEOUT, PKV_ERR_DEVICE_BOUNDS or PKV_ERR_CUDA as
+ * pkv_sync_error does. */
+PKV_API int pkv_contiguous_sync_error(pkv_stream_t stream);
+
+/* Tests of the status mapping (no counterpart on the pages): OR `bits`
+ * (PKV_DEVERR_*) into a device error word with a host-to-device copy, as a
+ * kernel that met the condition would, so that the sync calls can be checked
+ * without making any kernel fail.  which = PKV_ERRWORD_POOL: the pool's word
+ * (waits for the pool stream first); PKV_ERRWORD_CONTIGUOUS /
+ * PKV_ERRWORD_NOALLOC: the current device's word of pkv_attn_contiguous /
+ * pkv_attn_contiguous_noalloc (pool ignored; the first use on a device sets
+ * the word up as the first call of that entry point would).  Returns PKV_OK,
+ * PKV_ERR_ARG (NULL or host-only pool, unknown `which`, bits outside
+ * PKV_DEVERR_*) or PKV_ERR_CUDA. */
+#define PKV_ERRWORD_POOL 0
+#define PKV_ERRWORD_CONTIGUOUS 1
+#define PKV_ERRWORD_NOALLOC 2
+PKV_API int pkv_debug_or_error_bits(pkv_pool *pool, int32_t which, uint32_t bits);
 
 /* Upload pending page-table changes now (they are otherwise uploaded by the
  * next device call on the pool). */
@@ -334,9 +375,9 @@ PKV_API int pkv_pool_flush(pkv_pool *pool);
 PKV_API int pkv_set_split_keys(int32_t keys);
 PKV_API int32_t pkv_get_split_keys(void);
 
-/* Fused append (default on).  The per-layer step is "append the new K/V rows
- * into their pages, then attend over the sequence" ("nx_f32_kvcache_paged"
- * page, the attend-with-paged call contract).  With fusion on, a decode call
+/* Fused append (default on).  The per-layer step appends the new K/V rows
+ * into their pages and then attends over the sequence ("nx_f32_attn_paged.nx
+ * source", header comment and step 1 of nx_f32_attn_with_paged).  With fusion on, a decode call
  * -- no row takes the tensor-core prefill path, head_dim 128, group size 1, 2
  * or 4 -- whose pending page-table changes all lie in pages that hold only
  * this call's new positions (fresh pages; not a copy-on-append tail, a fork or
@@ -349,8 +390,8 @@ PKV_API int pkv_set_fused_append(int32_t on);
 PKV_API int32_t pkv_get_fused_append(void);
 
 /* Shared-prefix (cascade) decode (default on).  Forks share their prefix
- * pages by reference ("nx_f32_kvcache_paged" page, fork: the child's page
- * table copies the parent's and every page's reference count goes up).  When
+ * pages by reference ("nx_paged_kv_gate.nx source", FORK section: the fork
+ * holds the parent's pages and each shared page's refcount reads 2).  When
  * a batch holds 16 or more consecutive rows with one query each whose first
  * 2048 or more keys lie in the same whole pages (head_dim 128, group size 1,
  * 2, 4 or 8), those keys are attended once for the whole run by a tensor-core

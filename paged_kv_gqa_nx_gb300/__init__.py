@@ -27,6 +27,13 @@ PKV_ERR_CAPACITY = 5
 PKV_ERR_ARG = 6
 PKV_ERR_CUDA = 7
 PKV_ERR_DEVICE_BOUNDS = 8
+PKV_ERR_DEVICE_TIMEOUT = 9
+
+PKV_DEVERR_BOUNDS = 1
+PKV_DEVERR_TIMEOUT = 2
+PKV_ERRWORD_POOL = 0
+PKV_ERRWORD_CONTIGUOUS = 1
+PKV_ERRWORD_NOALLOC = 2
 
 PKV_POOL_HOST_ONLY = 1
 PKV_POOL_BF16 = 2
@@ -95,6 +102,8 @@ _SIGS = {
     "pkv_attn_contiguous": (_int, [_vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _f32, _vp, _vp]),
     "pkv_attn_contiguous_noalloc": (_int, [_vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _f32, _vp, _vp]),
     "pkv_sync_error": (_int, [_vp]),
+    "pkv_contiguous_sync_error": (_int, [_vp]),
+    "pkv_debug_or_error_bits": (_int, [_vp, _i32, _u32]),
     "pkv_pool_flush": (_int, [_vp]),
     "pkv_set_split_keys": (_int, [_i32]),
     "pkv_get_split_keys": (_i32, []),
@@ -341,6 +350,14 @@ def pkv_attn_contiguous_noalloc(Q, Kc, Vc, n_q, total_k, n_heads, n_kv_heads, he
 
 def pkv_sync_error(pool):
     return _lib.pkv_sync_error(pool)
+
+
+def pkv_contiguous_sync_error(stream=None):
+    return _lib.pkv_contiguous_sync_error(_stream(stream))
+
+
+def pkv_debug_or_error_bits(pool, which, bits):
+    return _lib.pkv_debug_or_error_bits(pool, which, bits)
 
 
 def pkv_pool_flush(pool):

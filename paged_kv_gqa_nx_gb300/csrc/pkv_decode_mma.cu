@@ -504,13 +504,14 @@ __global__ void __launch_bounds__(128, 3) decode_mma_kernel(AttnArgs a, PagedRow
 template <int G, class E>
 cudaError_t launch_mma(const AttnArgs &a, const PagedAddr &addr, cudaStream_t s) {
     constexpr size_t smem = mma_smem_bytes<E>();
-    static bool configured = false;  // per process; the attribute is per function
-    if (!configured) {
+    static PerDeviceOnce configured;  // the attribute is per function and device
+    const cudaError_t ce = configured.run([&]() -> cudaError_t {
         cudaError_t e = cudaFuncSetAttribute(decode_mma_kernel<G, E>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              static_cast<int>(smem));
         if (e != cudaSuccess) return e;
-        configured = true;
-    }
+        return cudaSuccess;
+    });
+    if (ce != cudaSuccess) return ce;
     const long long grid = static_cast<long long>(a.n_units) * a.n_kv;
     if (grid <= 0 || grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     decode_mma_kernel<G, E><<<static_cast<unsigned>(grid), 128, smem, s>>>(a, PagedRows<E>{addr});

@@ -992,6 +992,60 @@ std::mutex g_contig_mu;
 Stager g_contig_stager[64];
 int32_t *g_contig_err[64] = {};
 
+// The error word of pkv_attn_contiguous on device `dev` (current), made and
+// cleared on first use.  Call with g_contig_mu held.
+cudaError_t contig_error_word(int dev, int32_t **out) {
+    if (!g_contig_err[dev]) {
+        int32_t *w = nullptr;
+        cudaError_t e = cudaMalloc(&w, sizeof(int32_t));
+        if (e == cudaSuccess) e = cudaMemset(w, 0, sizeof(int32_t));
+        if (e == cudaSuccess) e = cudaDeviceSynchronize();
+        if (e != cudaSuccess) {
+            if (w) cudaFree(w);
+            return e;
+        }
+        g_contig_err[dev] = w;
+    }
+    *out = g_contig_err[dev];
+    return cudaSuccess;
+}
+
+// Read and clear a device error word (nothing to read when it does not exist
+// yet).  The caller has waited for the work that may set it.
+cudaError_t take_error_word(int32_t *word, uint32_t *bits) {
+    *bits = 0;
+    if (!word) return cudaSuccess;
+    int32_t h = 0;
+    cudaError_t e = cudaMemcpy(&h, word, sizeof h, cudaMemcpyDeviceToHost);
+    if (e == cudaSuccess && h) e = cudaMemset(word, 0, sizeof h);
+    if (e == cudaSuccess && h) e = cudaDeviceSynchronize();
+    *bits = static_cast<uint32_t>(h);
+    return e;
+}
+
+// OR bits into a device error word from the host, as a kernel would.
+cudaError_t or_error_word(int32_t *word, uint32_t bits) {
+    int32_t h = 0;
+    cudaError_t e = cudaMemcpy(&h, word, sizeof h, cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return e;
+    h |= static_cast<int32_t>(bits);
+    e = cudaMemcpy(word, &h, sizeof h, cudaMemcpyHostToDevice);
+    return e;
+}
+
+// The status of an error word's bits: a timeout leaves a tile's output
+// unwritten, so it is reported first; the message names every bit set.
+int error_status(uint32_t bits, const char *who) {
+    if (bits == 0) return PKV_OK;
+    const bool t = (bits & PKV_DEVERR_TIMEOUT) != 0, b = (bits & PKV_DEVERR_BOUNDS) != 0;
+    if (t)
+        return fail(PKV_ERR_DEVICE_TIMEOUT,
+                    "%s gave up a bounded wait and left its tile unwritten%s", who,
+                    b ? "; a kernel also met a block id or page index out of range" : "");
+    return fail(PKV_ERR_DEVICE_BOUNDS, "%s met a block id or page index out of range and skipped it",
+                who);
+}
+
 }  // namespace
 
 // ================================================================== C ABI ====
@@ -1470,11 +1524,9 @@ int pkv_attn_contiguous(const float *Q, const float *Kc, const float *Vc, int32_
     const size_t total = desc_bytes + pf * (2 + head_dim) * sizeof(float);
 
     std::lock_guard<std::mutex> lk(g_contig_mu);
-    if (!g_contig_err[dev]) {
-        e = cudaMalloc(&g_contig_err[dev], sizeof(int32_t));
-        if (e == cudaSuccess) e = cudaMemset(g_contig_err[dev], 0, sizeof(int32_t));
-        if (e != cudaSuccess) return cuda_fail(e, "error word");
-    }
+    int32_t *err_word = nullptr;
+    e = contig_error_word(dev, &err_word);
+    if (e != cudaSuccess) return cuda_fail(e, "error word");
     cudaMemPool_t mp;
     e = mempool_for(dev, &mp);
     if (e != cudaSuccess) return cuda_fail(e, "memory pool");
@@ -1501,7 +1553,7 @@ int pkv_attn_contiguous(const float *Q, const float *Kc, const float *Vc, int32_
     a.causal = causal ? 1 : 0;
     a.split_keys = S;
     a.scale_log2 = scale * 1.4426950408889634f;
-    a.err = g_contig_err[dev];
+    a.err = err_word;
     if (pf > 0) {
         a.pm = reinterpret_cast<float *>(base + desc_bytes);
         a.pl = a.pm + pf;
@@ -1534,11 +1586,57 @@ int pkv_sync_error(pkv_pool *p) {
     DevGuard dg(p->device);
     cudaError_t e = cudaStreamSynchronize(p->stream);
     if (e != cudaSuccess) return cuda_fail(e, "stream synchronize");
-    int32_t h = 0;
-    e = cudaMemcpy(&h, p->err_dev, sizeof h, cudaMemcpyDeviceToHost);
-    if (e == cudaSuccess && h) e = cudaMemset(p->err_dev, 0, sizeof h);
+    uint32_t h = 0;
+    e = take_error_word(p->err_dev, &h);
     if (e != cudaSuccess) return cuda_fail(e, "error word");
-    if (h) return fail(PKV_ERR_DEVICE_BOUNDS, "a kernel met a page-table entry out of range");
+    return error_status(h, "a pool kernel");
+}
+
+int pkv_contiguous_sync_error(pkv_stream_t stream) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= 64) return fail(PKV_ERR_ARG, "device index out of range");
+    e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "stream synchronize");
+    uint32_t h = 0, hn = 0;
+    {
+        std::lock_guard<std::mutex> lk(g_contig_mu);
+        e = take_error_word(g_contig_err[dev], &h);
+    }
+    if (e == cudaSuccess) e = take_error_word(noalloc_error_word(dev, false, nullptr), &hn);
+    if (e != cudaSuccess) return cuda_fail(e, "error word");
+    return error_status(h | hn, "a contiguous-path kernel");
+}
+
+int pkv_debug_or_error_bits(pkv_pool *p, int32_t which, uint32_t bits) {
+    if ((bits & ~(PKV_DEVERR_BOUNDS | PKV_DEVERR_TIMEOUT)) != 0)
+        return fail(PKV_ERR_ARG, "bits 0x%x outside PKV_DEVERR_*", bits);
+    int32_t *word = nullptr;
+    cudaError_t e = cudaSuccess;
+    if (which == PKV_ERRWORD_POOL) {
+        if (!p || p->host_only) return fail(PKV_ERR_ARG, "a device pool is needed");
+        DevGuard dg(p->device);
+        e = cudaStreamSynchronize(p->stream);
+        if (e == cudaSuccess) e = or_error_word(p->err_dev, bits);
+        if (e != cudaSuccess) return cuda_fail(e, "error word");
+        return PKV_OK;
+    }
+    int dev = 0;
+    e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= 64) return fail(PKV_ERR_ARG, "device index out of range");
+    if (which == PKV_ERRWORD_CONTIGUOUS) {
+        std::lock_guard<std::mutex> lk(g_contig_mu);
+        e = contig_error_word(dev, &word);
+        if (e == cudaSuccess) e = or_error_word(word, bits);
+    } else if (which == PKV_ERRWORD_NOALLOC) {
+        word = noalloc_error_word(dev, true, &e);
+        if (e == cudaSuccess) e = or_error_word(word, bits);
+    } else {
+        return fail(PKV_ERR_ARG, "unknown error word %d", which);
+    }
+    if (e != cudaSuccess) return cuda_fail(e, "error word");
     return PKV_OK;
 }
 

@@ -2,6 +2,7 @@
 // (pkv_host.cpp) and the kernels (pkv_kernels.cu).  Not part of the C ABI.
 #pragma once
 
+#include <atomic>
 #include <cstdint>
 #include <vector>
 
@@ -176,6 +177,25 @@ struct PrepArgs {
     int32_t q_dim = 0, hd = 0;
 };
 
+// Set-up done once per device: a kernel's function attributes (its dynamic
+// shared-memory opt-in) belong to the current device's context, so a process
+// that drives several GPUs sets them on each.  Setting an attribute is
+// idempotent, so threads that race here all set the same value.
+struct PerDeviceOnce {
+    std::atomic<uint64_t> done{0};  // bit d: device d is set up
+    template <class F>
+    cudaError_t run(F &&f) {
+        int dev = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e != cudaSuccess) return e;
+        const uint64_t bit = (dev >= 0 && dev < 64) ? (uint64_t{1} << dev) : 0;
+        if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+        e = f();
+        if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_release);
+        return e;
+    }
+};
+
 // Kernel launchers (pkv_kernels.cu).  Each enqueues exactly one kernel.
 cudaError_t launch_prep(const PrepArgs &a, const PagedAddr &addr, cudaStream_t s);
 cudaError_t launch_pt_apply(int32_t *pt_dev, int32_t max_blocks, const PtRun *runs, int32_t n_runs,
@@ -222,6 +242,11 @@ void build_contig_work(int32_t n_q, int32_t total_k, int32_t causal, int32_t spl
 cudaError_t launch_counted(int kind, cudaStream_t s, cudaError_t (*fn)(void *), void *ctx);
 int32_t current_split_keys();
 int report_error(int code, const char *msg);
+// The error word of pkv_attn_contiguous_noalloc on device `dev` (current): its
+// device address, or nullptr when no call has set it up yet and `setup` is
+// false; with `setup`, the first use on the device sets it up (*e reports a
+// failure).  Defined in pkv_noalloc.cu.
+int32_t *noalloc_error_word(int dev, bool setup, cudaError_t *e);
 
 // Largest head_dim the decode kernels accept.
 constexpr int kMaxHeadDim = 256;

@@ -666,14 +666,15 @@ constexpr int kFastStages = PKV_FAST_STAGES;
 template <int G, class Rows>
 cudaError_t launch_fast(const AttnArgs &a, const Rows &r, cudaStream_t s) {
     constexpr size_t smem = fast_smem_bytes<G, kFastStages, typename Rows::Elem>();
-    static bool configured = false;  // per process; the attribute is per function
-    if (!configured) {
+    static PerDeviceOnce configured;  // the attribute is per function and device
+    const cudaError_t ce = configured.run([&]() -> cudaError_t {
         cudaError_t e = cudaFuncSetAttribute(decode_fast_kernel<G, kFastStages, Rows>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              static_cast<int>(smem));
         if (e != cudaSuccess) return e;
-        configured = true;
-    }
+        return cudaSuccess;
+    });
+    if (ce != cudaSuccess) return ce;
     const long long grid = static_cast<long long>(a.n_units) * a.n_kv;
     if (grid <= 0 || grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     decode_fast_kernel<G, kFastStages, Rows><<<static_cast<unsigned>(grid), 128, smem, s>>>(a, r);
@@ -684,14 +685,15 @@ template <class Rows>
 cudaError_t launch_generic(const AttnArgs &a, const Rows &r, cudaStream_t s) {
     const int hpc = a.group < kGenMaxHeads ? a.group : kGenMaxHeads;
     const size_t smem = generic_smem_floats(hpc, a.hd) * sizeof(float);
-    static bool configured = false;
-    if (!configured) {
+    static PerDeviceOnce configured;  // the attribute is per function and device
+    const cudaError_t ce = configured.run([&]() -> cudaError_t {
         cudaError_t e = cudaFuncSetAttribute(decode_generic_kernel<Rows>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              static_cast<int>(generic_smem_floats(kGenMaxHeads, kMaxHeadDim) * sizeof(float)));
         if (e != cudaSuccess) return e;
-        configured = true;
-    }
+        return cudaSuccess;
+    });
+    if (ce != cudaSuccess) return ce;
     const int n_chunks = (a.group + hpc - 1) / hpc;
     const long long grid = static_cast<long long>(a.n_units) * a.n_kv * n_chunks;
     if (grid <= 0 || grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;

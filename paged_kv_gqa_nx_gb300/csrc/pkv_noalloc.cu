@@ -15,8 +15,10 @@
 // address, so the entry point looks the address up once per device with
 // cudaGetSymbolAddress (with that device current) and passes it to the
 // kernels.  Every call shares the array and it keeps the previous call's
-// contents; the one word that must start at zero (the kernels' error word) is
-// cleared by each call, everything else is fully written before it is read.
+// contents.  Its first word is the kernels' error word: cleared once, when
+// the device is set up, it gathers the bits of every call until
+// pkv_contiguous_sync_error reads and clears it; everything else is fully
+// written by a call before that call reads it.
 #include "../../include/pkv.h"
 #include "pkv_internal.h"
 
@@ -68,7 +70,40 @@ cudaError_t run_merge(void *p) {
 
 int err_arg(int code, const char *msg) { return report_error(code, msg); }
 
+// First use on device `dev` (current; g_mu held): look up the array's device
+// address and clear its error word.  The clear is finished before this
+// returns, so no stream needs ordering after it.
+cudaError_t set_up(int dev) {
+    if (g_scratch_dev[dev]) return cudaSuccess;
+    void *p = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e == cudaSuccess && !p) e = cudaErrorInvalidSymbol;
+    if (e == cudaSuccess) e = cudaMemset(p, 0, sizeof(int32_t));
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return e;
+    g_scratch_dev[dev] = p;
+    return cudaSuccess;
+}
+
 }  // namespace
+
+namespace pkv {
+
+int32_t *noalloc_error_word(int dev, bool setup, cudaError_t *e) {
+    if (e) *e = cudaSuccess;
+    if (dev < 0 || dev >= 64) return nullptr;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_scratch_dev[dev] && setup) {
+        const cudaError_t r = set_up(dev);
+        if (r != cudaSuccess) {
+            if (e) *e = r;
+            return nullptr;
+        }
+    }
+    return static_cast<int32_t *>(g_scratch_dev[dev]);
+}
+
+}  // namespace pkv
 
 extern "C" int pkv_attn_contiguous_noalloc(const float *Q, const float *Kc, const float *Vc,
                                            int32_t n_q, int32_t total_k, int32_t n_heads,
@@ -121,17 +156,11 @@ extern "C" int pkv_attn_contiguous_noalloc(const float *Q, const float *Kc, cons
     cudaStream_t st = static_cast<cudaStream_t>(stream);
 
     std::lock_guard<std::mutex> lk(g_mu);
-    if (!g_scratch_dev[dev]) {
-        // first call on this device: look up the array's device address
-        void *p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-        if (e != cudaSuccess || !p) {
-            char msg[256];
-            snprintf(msg, sizeof msg, "cudaGetSymbolAddress of the static scratch: %s",
-                     cudaGetErrorString(e));
-            return err_arg(PKV_ERR_CUDA, msg);
-        }
-        g_scratch_dev[dev] = p;
+    e = set_up(dev);
+    if (e != cudaSuccess) {
+        char msg[256];
+        snprintf(msg, sizeof msg, "set-up of the static scratch: %s", cudaGetErrorString(e));
+        return err_arg(PKV_ERR_CUDA, msg);
     }
     unsigned char *base = static_cast<unsigned char *>(g_scratch_dev[dev]);
 
@@ -145,10 +174,7 @@ extern "C" int pkv_attn_contiguous_noalloc(const float *Q, const float *Kc, cons
         std::memcpy(blob.data() + (tiles_off - rows_off), tiles.data(), tiles.size() * sizeof(PrefillTile));
     if (!merges.empty())
         std::memcpy(blob.data() + (merges_off - rows_off), merges.data(), merges.size() * sizeof(MergeDesc));
-    // the error word must start at zero
-    e = cudaMemsetAsync(base, 0, sizeof(int32_t), st);
-    if (e == cudaSuccess)
-        e = cudaMemcpyAsync(base + rows_off, blob.data(), blob.size(), cudaMemcpyHostToDevice, st);
+    e = cudaMemcpyAsync(base + rows_off, blob.data(), blob.size(), cudaMemcpyHostToDevice, st);
     if (e != cudaSuccess) return err_arg(PKV_ERR_CUDA, cudaGetErrorString(e));
 
     AttnArgs a{};

@@ -673,8 +673,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs a, 
 
 template <int G, class Rows, bool kBulk, bool kLoZero>
 cudaError_t launch_prefill_g(const PrefillArgs &a, const Rows &r, cudaStream_t s) {
-    static bool configured = false;
-    if (!configured) {
+    static PerDeviceOnce configured;  // the attribute is per function and device
+    const cudaError_t ce = configured.run([&]() -> cudaError_t {
         // setmaxnreg.inc waits until the CTA's pool holds the registers it asks
         // for, so launch only if the compiled kernel starts with the registers
         // the split was sized for
@@ -687,8 +687,9 @@ cudaError_t launch_prefill_g(const PrefillArgs &a, const Rows &r, cudaStream_t s
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(kSmemBytes));
         if (e != cudaSuccess) return e;
-        configured = true;
-    }
+        return cudaSuccess;
+    });
+    if (ce != cudaSuccess) return ce;
     const long long grid = static_cast<long long>(a.n_tiles) * a.n_kv;
     if (grid <= 0 || grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     prefill_tc_kernel<G, Rows, kBulk, kLoZero><<<static_cast<unsigned>(grid), kThreads, kSmemBytes, s>>>(a, r);
@@ -786,13 +787,14 @@ __global__ void __launch_bounds__(256) split_kernel(SplitArgs p, PagedRowsP<E> r
 template <class E>
 cudaError_t launch_split(const SplitArgs &a, const PagedRowsP<E> &r, cudaStream_t s) {
     constexpr size_t smem = kSplitRawFloats * sizeof(float);
-    static bool configured = false;
-    if (!configured) {
+    static PerDeviceOnce configured;  // the attribute is per function and device
+    const cudaError_t ce = configured.run([&]() -> cudaError_t {
         cudaError_t e = cudaFuncSetAttribute(split_kernel<E>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              static_cast<int>(smem));
         if (e != cudaSuccess) return e;
-        configured = true;
-    }
+        return cudaSuccess;
+    });
+    if (ce != cudaSuccess) return ce;
     const long long grid = static_cast<long long>(a.n_items) * a.n_kv;
     if (grid <= 0 || grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     split_kernel<E><<<static_cast<unsigned>(grid), 256, smem, s>>>(a, r);

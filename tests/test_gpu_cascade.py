@@ -1,7 +1,7 @@
 """Shared-prefix (cascade) decode against the oracle.
 
-Forks share their prefix pages ("nx_f32_kvcache_paged": fork copies the page
-table and raises each page's reference count).  A batch with a run of 16 or
+Forks share their prefix pages ("nx_paged_kv_gate.nx source", FORK section:
+the fork holds its parent's pages and each shared page's refcount reads 2).  A batch with a run of 16 or
 more one-query rows over common prefix pages attends those keys once for the
 run (a tensor-core pass over the stacked queries) and each row's own keys in
 the decode kernel, then merges the two.  Every row is checked against the

@@ -1,8 +1,8 @@
 """Fused append + decode vs the unfused path (append kernel, then attend).
 
 The per-layer step appends the new K/V rows into their pages and then attends
-over the sequence ("nx_f32_kvcache_paged": the attend-with-paged call
-contract).  With fusion the decode kernel reads the new rows from K_new /
+over the sequence ("nx_f32_attn_paged.nx source", header comment and step 1
+of nx_f32_attn_with_paged).  With fusion the decode kernel reads the new rows from K_new /
 V_new, stores them into the pool and enters fresh pages into the device page
 table.  Both paths must give the same bits: outputs, pool contents, page
 tables.  Each case runs twice on identically built pools (same shuffled free

@@ -3,8 +3,13 @@ let a library allocate device memory (an engine that has reserved its whole
 device-memory budget, code inside an allocator callback, loops where
 cudaMalloc/cudaFree could synchronise the device).  Its scratch is one static
 device array, so its output must match pkv_attn_contiguous -- the entry point
-that allocates its scratch per call -- within the tests' tolerance, on two
-calls in a row (the second finds the first call's contents in the array).
+that allocates its scratch per call -- within the tests' tolerance, on calls
+in a row (each finds the previous call's contents in the array), and the
+oracle within the same tolerance.  The calls cover both kernels the entry
+point dispatches: split-K decode (with split partials and their merge in the
+array) and the tensor-core kernel for rows of 32 or more queries (its tiles'
+descriptors and, past 16 384 keys, its split partials in the array), the
+latter both before and after a call that left other partials behind.
 
 This file is collected last so that a run stopping at the first failure has
 run every other test before it; it also passes alone in a fresh process.
@@ -15,6 +20,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 import paged_kv_gqa_nx_gb300 as pkv
 from gpu_helpers import assert_close
 
@@ -34,8 +40,10 @@ def _case(n_q, past, H, KV, hd, causal, seed):
 def test_no_alloc_matches_allocating_entry_point_on_two_calls():
     stream = torch.cuda.current_stream()
     cases = [
-        _case(1, 3000, 32, 8, 128, 1, 1),   # several splits + merge on the head_dim-128 kernel
-        _case(3, 40, 4, 2, 8, 1, 2),        # one split, generic kernel, stale scratch from call 1
+        _case(32, 16500, 32, 8, 128, 1, 4),  # tensor-core kernel, 2 key splits + merge
+        _case(1, 3000, 32, 8, 128, 1, 1),    # several splits + merge on the head_dim-128 kernel
+        _case(64, 1024, 32, 8, 128, 1, 5),   # tensor-core kernel after stale decode partials
+        _case(3, 40, 4, 2, 8, 1, 2),         # one split, generic kernel, stale scratch from call 1
     ]
     for i, (Q, Kc, Vc, n_q, tk, H, KV, hd, causal, scale) in enumerate(cases):
         ref = torch.empty(n_q, H * hd, device="cuda")
@@ -45,7 +53,13 @@ def test_no_alloc_matches_allocating_entry_point_on_two_calls():
         assert pkv.pkv_attn_contiguous_noalloc(Q, Kc, Vc, n_q, tk, H, KV, hd, causal, scale, got,
                                                stream) == pkv.PKV_OK, pkv.pkv_last_error()
         torch.cuda.synchronize()
-        assert_close(got.cpu().numpy(), ref.cpu().numpy(), Vc.abs().max().item(), "call %d" % i)
+        vmax = Vc.abs().max().item()
+        assert_close(got.cpu().numpy(), ref.cpu().numpy(), vmax, "call %d" % i)
+        rc, exp = oracle.attend(Q.cpu().numpy(), Kc.cpu().numpy(), Vc.cpu().numpy(), n_q, tk, H,
+                                KV, hd, causal, scale)
+        assert rc == 0
+        assert_close(got.cpu().numpy(), exp, vmax, "call %d vs the oracle" % i)
+    assert pkv.pkv_contiguous_sync_error(stream) == pkv.PKV_OK, pkv.pkv_last_error()
 
 
 @pytest.mark.gpu
