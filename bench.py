@@ -65,17 +65,61 @@ KERNEL_SOURCES = {
 PROFILE_FILES = {"decode": "decode_%s.md", "prefill": "prefill_tc_%s.md"}
 
 
-def measured_tensor_peak():
-    """f32 peak of the 3xTF32 prefill contraction: the measured bf16 dense
-    rate times the nominal TF32/BF16 ratio (1.1 / 2.25 PFLOP/s), divided by the
-    three TF32 products each f32 product takes."""
+def measured_bf16_peak():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
         with open(path) as f:
-            bf16, kind = float(json.load(f)["bf16_tflops"]), "measured"
+            return float(json.load(f)["bf16_tflops"]), "measured"
     except Exception:
-        bf16, kind = 1900.0, "fallback"
-    return bf16 * (1.1 / 2.25) / 3.0, kind
+        return 1900.0, "fallback"
+
+
+_TF32_CACHE = {}
+
+
+def measured_tf32_tflops(n=8192, reps=10):
+    """cuBLAS TF32 dense matmul throughput on this GPU, measured the way the
+    bf16 figure in MEASURED_PEAKS.json is: torch.matmul of two n x n f32
+    matrices with TF32 tensor cores allowed, 2 n^3 flops, best of `reps`
+    launches timed with CUDA events.  Cached per process."""
+    if "v" in _TF32_CACHE:
+        return _TF32_CACHE["v"]
+    import torch
+    prev = torch.backends.cuda.matmul.allow_tf32
+    torch.backends.cuda.matmul.allow_tf32 = True
+    try:
+        a = torch.randn(n, n, device="cuda")
+        b = torch.randn(n, n, device="cuda")
+        c = torch.empty(n, n, device="cuda")
+        for _ in range(3):
+            torch.matmul(a, b, out=c)
+        torch.cuda.synchronize()
+        best = float("inf")
+        for _ in range(reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            torch.matmul(a, b, out=c)
+            e1.record()
+            e1.synchronize()
+            best = min(best, e0.elapsed_time(e1) * 1e-3)
+        del a, b, c
+        torch.cuda.empty_cache()
+    finally:
+        torch.backends.cuda.matmul.allow_tf32 = prev
+    _TF32_CACHE["v"] = 2.0 * n ** 3 / best / 1e12
+    return _TF32_CACHE["v"]
+
+
+def tensor_peak():
+    """f32-accurate peak of the 3xTF32 prefill contraction: the measured TF32
+    rate (cuBLAS, this GPU, live) divided by the three TF32 products each f32
+    product takes.  Also returns the nominal-ratio figure (measured bf16 x
+    1.1/2.25 / 3) for context."""
+    tf32 = measured_tf32_tflops()
+    bf16, kind = measured_bf16_peak()
+    return tf32 / 3.0, {"tf32_tflops_cublas": round(tf32, 1),
+                        "from_bf16_nominal_ratio": round(bf16 * (1.1 / 2.25) / 3.0, 1),
+                        "bf16_source": kind}
 
 
 def kernel_source_digest(kernel: str = "decode", kv_dtype: str = "f32"):
@@ -331,19 +375,24 @@ class DeviceRun:
 
 # ---------------------------------------------------------- oracle timing ----
 
-def oracle_sample(w, lengths, budget_s, rng_seed=0, n_q=None):
-    """Choose rows of the workload for a bounded oracle run: rows in seeded
-    order until their estimated time reaches the budget."""
+def oracle_sample(w, lengths, budget_s, rng_seed=0, n_q=None, threads=1):
+    """Choose rows of the workload for a bounded oracle run on `threads` host
+    threads (0: all cores): rows in seeded order until their estimated time
+    reaches the budget."""
     import oracle
     rng = np.random.default_rng(rng_seed)
     order = rng.permutation(len(lengths))
-    # calibrate on a small synthetic row
+    # calibrate on a small synthetic row, on the thread count that will run
     L = 2048
     Q = np.ones((1, w.q_dim), np.float32)
     K = np.ones((L, w.kv_dim), np.float32)
-    t0 = time.perf_counter()
-    oracle.attend(Q, K, K, 1, L, w.n_heads, w.n_kv_heads, w.head_dim, 1, w.scale)
-    per_key = (time.perf_counter() - t0) / L
+    oracle.set_threads(threads)
+    try:
+        t0 = time.perf_counter()
+        oracle.attend(Q, K, K, 1, L, w.n_heads, w.n_kv_heads, w.head_dim, 1, w.scale)
+        per_key = (time.perf_counter() - t0) / L
+    finally:
+        oracle.set_threads(0)
     rows, est = [], 0.0
     for r in order:
         cost = per_key * lengths[r] * (1 if n_q is None else n_q[r])
@@ -356,15 +405,21 @@ def oracle_sample(w, lengths, budget_s, rng_seed=0, n_q=None):
     return sorted(rows)
 
 
-def time_oracle(samples, w):
+def time_oracle(samples, w, threads=1):
+    """Seconds the oracle takes over `samples` on `threads` host threads (0:
+    all cores), the K/V bytes it read, and the thread count in effect."""
     import oracle
-    t0 = time.perf_counter()
-    for (Q, K, V, n, tk) in samples:
-        rc, _ = oracle.attend(Q, K, V, n, tk, w.n_heads, w.n_kv_heads, w.head_dim, 1, w.scale)
-        assert rc == 0
-    dt = time.perf_counter() - t0
+    used = oracle.set_threads(threads)
+    try:
+        t0 = time.perf_counter()
+        for (Q, K, V, n, tk) in samples:
+            rc, _ = oracle.attend(Q, K, V, n, tk, w.n_heads, w.n_kv_heads, w.head_dim, 1, w.scale)
+            assert rc == 0
+        dt = time.perf_counter() - t0
+    finally:
+        oracle.set_threads(0)
     nbytes = sum(float(tk) * w.kv_dim * 8 for (_, _, _, _, tk) in samples)
-    return dt, nbytes
+    return dt, nbytes, used
 
 
 # ------------------------------------------------------------------- arms ----
@@ -400,6 +455,106 @@ def barrier(dist):
         dist.barrier()
 
 
+def timed_steps(run, steps, stream_sync=True):
+    """Run `steps` steps between CUDA events on the pool stream with the
+    library's per-launch profiling on; returns (device ms, host s, launches,
+    per-kernel (ms, launches))."""
+    import torch
+    pkv = run.pkv
+    pkv.pkv_profile_reset()
+    pkv.pkv_profile_enable(True)
+    torch.cuda.synchronize()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    launches0 = pkv.pkv_launch_count()
+    h0 = time.perf_counter()
+    ev0.record(run.stream)
+    for _ in range(steps):
+        run.step()
+    ev1.record(run.stream)
+    host_s = time.perf_counter() - h0
+    torch.cuda.synchronize()
+    launches = pkv.pkv_launch_count() - launches0
+    pkv.pkv_profile_enable(False)
+    kern = {pkv.KERNEL_NAMES[k]: pkv.pkv_profile_read(k) for k in range(pkv.PKV_KERNEL_KINDS)}
+    return ev0.elapsed_time(ev1), host_s, launches, kern
+
+
+def roofline_of(run, w, kern, steps, workload, kv_dtype, tensor_flops_per_layer):
+    """The roofline entry of the kernel that takes most of the step."""
+    dec_ms, dec_n = kern["decode"]
+    pre_ms, pre_n = kern["prefill"]
+    if pre_ms > dec_ms and pre_n:
+        # flops per launch: one layer call's tensor-core work over its prefill launches
+        pre_per_layer = pre_n / (steps * w.n_layers)
+        pre_avg_s = pre_ms * 1e-3 / pre_n
+        flops_per_launch = tensor_flops_per_layer / max(pre_per_layer, 1e-9)
+        tpeak, detail = tensor_peak()
+        achieved = flops_per_launch / pre_avg_s / 1e12
+        return {"bound": "tensor", "kernel": "prefill (tcgen05 3xTF32 chunked prefill)",
+                "achieved": round(achieved, 1), "peak": round(tpeak, 1),
+                "peak_source": ("measured cuBLAS TF32 dense matmul on this GPU (%.1f TFLOP/s) / 3 "
+                                "(TF32 products per f32 product)" % detail["tf32_tflops_cublas"]),
+                "peak_detail": detail,
+                "unit": "TFLOP/s", "frac": round(achieved / tpeak, 4),
+                "traffic": profiled_traffic(workload, "prefill", kv_dtype),
+                "alg_flops_per_launch": flops_per_launch,
+                "avg_launch_ms": round(pre_avg_s * 1e3, 4)}
+    peak, peak_kind = measured_hbm_peak()
+    dec_avg_s = dec_ms * 1e-3 / max(dec_n, 1)
+    alg_bytes = run.kv_bytes_per_layer + run.T * w.q_dim * 4 * 2
+    achieved = alg_bytes / dec_avg_s / 1e9 if dec_n else None
+    return {"bound": "hbm", "kernel": "decode (split-K paged attention)",
+            "achieved": round(achieved, 1) if achieved else None, "peak": peak,
+            "peak_source": (peak_kind + " (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
+                            else "fallback"), "unit": "GB/s",
+            "frac": round(achieved / peak, 4) if achieved else None,
+            "traffic": profiled_traffic(workload, "decode", kv_dtype), "alg_bytes_per_launch": alg_bytes,
+            "avg_launch_ms": round(dec_avg_s * 1e3, 4)}
+
+
+def tensor_flops(run, w):
+    """Tensor-core work of one layer call as the library laid it out: the
+    visible (query, key) pairs of the prefill rows and of the shared-prefix
+    pass, 2 flops each for q.k and for p.v per head dimension."""
+    work = run.pkv.pkv_pool_last_work(run.pool)
+    return 4.0 * w.head_dim * w.n_heads * (work["prefill_pairs"] + work["prefix_pairs"])
+
+
+# the other workloads the default run measures beside the headline one
+EXTRA_WORKLOADS = ("batched_decode_m64", "chunked_prefill", "shared_prefix_forks")
+
+
+def measure_extra(name, args, rank):
+    """One more workload through the same step and timing: ms/step, KV GB/s
+    and the dominant kernel's roofline."""
+    import torch
+    w = get_workload(name)
+    run = DeviceRun(w, rank, "f32")
+    try:
+        for _ in range(max(3, args.warmup)):
+            run.step()
+        torch.cuda.synchronize()
+        tfl = tensor_flops(run, w)
+        steps = max(5, min(args.steps, 30))
+        ms_total, host_s, launches, kern = timed_steps(run, steps)
+        ms_step = ms_total / steps
+        peak, _ = measured_hbm_peak()
+        value = run.kv_bytes / (ms_step * 1e-3) / 1e9
+        return {"ms_per_step": round(ms_step, 4), "kv_gbs": round(value, 2),
+                "frac_of_hbm_peak": round(value / peak, 4),
+                "unique_kv_gbs": round(run.unique_kv_bytes / (ms_step * 1e-3) / 1e9, 2),
+                "rows_layers_per_s": round(run.T * w.n_layers / (ms_step * 1e-3), 1),
+                "kv_bytes_per_step": run.kv_bytes, "steps": steps,
+                "gpu_launches": launches,
+                "kernels_ms_per_step": {k: round(v[0] / steps, 4) for k, v in kern.items() if v[1]},
+                "roofline": roofline_of(run, w, kern, steps, name, "f32", tfl)}
+    finally:
+        run.close()
+        del run
+        torch.cuda.empty_cache()
+
+
 def run_pkv(args):
     import torch
     import paged_kv_gqa_nx_gb300 as pkv
@@ -415,11 +570,7 @@ def run_pkv(args):
     for _ in range(args.warmup):
         run.step()
     torch.cuda.synchronize()
-    # tensor-core work of one layer call as the library laid it out: the
-    # visible (query, key) pairs of the prefill rows and of the shared-prefix
-    # pass, 2 flops each for q.k and for p.v per head dimension
-    work = pkv.pkv_pool_last_work(run.pool)
-    tensor_flops_per_layer = 4.0 * w.head_dim * w.n_heads * (work["prefill_pairs"] + work["prefix_pairs"])
+    tensor_flops_per_layer = tensor_flops(run, w)
 
     uuid = None
     try:
@@ -429,26 +580,9 @@ def run_pkv(args):
     clocks = ClockSampler(uuid)
     clocks.start()
     time.sleep(0.3)
-
-    pkv.pkv_profile_reset()
-    pkv.pkv_profile_enable(True)
     barrier(dist)
-    torch.cuda.synchronize()
-    ev0 = torch.cuda.Event(enable_timing=True)
-    ev1 = torch.cuda.Event(enable_timing=True)
-    launches0 = pkv.pkv_launch_count()
-    h0 = time.perf_counter()
-    ev0.record(run.stream)
-    for _ in range(args.steps):
-        run.step()
-    ev1.record(run.stream)
-    host_s = time.perf_counter() - h0
-    torch.cuda.synchronize()
+    ms_total, host_s, launches, kern = timed_steps(run, args.steps)
     barrier(dist)
-    launches = pkv.pkv_launch_count() - launches0
-    pkv.pkv_profile_enable(False)
-    ms_total = ev0.elapsed_time(ev1)
-    kern = {pkv.KERNEL_NAMES[k]: pkv.pkv_profile_read(k) for k in range(pkv.PKV_KERNEL_KINDS)}
     clk = clocks.stop()
     ms_total = max_over_ranks(ms_total, dist)
     ms_step = ms_total / args.steps
@@ -469,47 +603,27 @@ def run_pkv(args):
     e2e_value = world * run.kv_bytes * e2e_steps / e2e_s / 1e9
     h2d = run.T * (w.q_dim + 2 * w.kv_dim) * 4 * w.n_layers
     d2h = run.T * w.q_dim * 4 * w.n_layers
+    del bufs
 
-    # the roofline of the kernel that takes most of the step
-    dec_ms, dec_n = kern["decode"]
-    pre_ms, pre_n = kern["prefill"]
-    if pre_ms > dec_ms and pre_n:
-        # flops per launch: one layer call's tensor-core work over its prefill launches
-        pre_per_layer = pre_n / (args.steps * w.n_layers)
-        pre_avg_s = pre_ms * 1e-3 / pre_n
-        flops_per_launch = tensor_flops_per_layer / max(pre_per_layer, 1e-9)
-        tpeak, tkind = measured_tensor_peak()
-        achieved = flops_per_launch / pre_avg_s / 1e12
-        roofline = {"bound": "tensor", "kernel": "prefill (tcgen05 3xTF32 chunked prefill)",
-                    "achieved": round(achieved, 1), "peak": round(tpeak, 1),
-                    "peak_source": ("%s bf16_tflops x 1.1/2.25 (nominal TF32/BF16) / 3 (TF32 products "
-                                    "per f32 product)" % tkind),
-                    "unit": "TFLOP/s", "frac": round(achieved / tpeak, 4),
-                    "traffic": profiled_traffic(args.workload, "prefill", args.kv_dtype),
-                    "alg_flops_per_launch": flops_per_launch,
-                    "avg_launch_ms": round(pre_avg_s * 1e3, 4)}
-    else:
-        dec_avg_s = dec_ms * 1e-3 / max(dec_n, 1)
-        alg_bytes = run.kv_bytes_per_layer + run.T * w.q_dim * 4 * 2
-        achieved = alg_bytes / dec_avg_s / 1e9 if dec_n else None
-        roofline = {"bound": "hbm", "kernel": "decode (split-K paged attention)",
-                    "achieved": round(achieved, 1) if achieved else None, "peak": peak,
-                    "peak_source": peak_kind + " (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
-                    else "fallback", "unit": "GB/s",
-                    "frac": round(achieved / peak, 4) if achieved else None,
-                    "traffic": profiled_traffic(args.workload, "decode", args.kv_dtype), "alg_bytes_per_launch": alg_bytes,
-                    "avg_launch_ms": round(dec_avg_s * 1e3, 4)}
+    roofline = roofline_of(run, w, kern, args.steps, args.workload, args.kv_dtype,
+                           tensor_flops_per_layer)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        # the oracle on a bounded sample of the same rows: on one thread, then
+        # on every host core (same arithmetic, same bits)
         lens = [b + n for b, n in zip(run.base_len, run.n_q)]
         rows = oracle_sample(w, lens, args.cpu_budget, n_q=run.n_q)
         samples = run.histories_for(rows)
-        dt, nbytes = time_oracle(samples, w)
-        cpu = {"value": nbytes / dt / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
-               "sample": "%d of %d rows (%d keys, layer 0) of the same workload, C oracle, "
-                         "double accumulation, one thread, %.1f s" % (
-                             len(rows), len(lens), sum(lens[r] for r in rows), dt)}
+        dt1, nbytes, _ = time_oracle(samples, w, threads=1)
+        dtn, _, cores = time_oracle(samples, w, threads=0)
+        what = "%d of %d rows (%d keys, layer 0) of the same workload, C oracle, double accumulation" % (
+            len(rows), len(lens), sum(lens[r] for r in rows))
+        cpu = {"value": round(nbytes / dtn / 1e9, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+               "sample": "%s, %d threads, %.2f s" % (what, cores, dtn),
+               "one_thread": {"value": round(nbytes / dt1 / 1e9, 4), "unit": "GB/s", "cores": 1,
+                              "sample": "%s, one thread, %.1f s" % (what, dt1)}}
+        del samples
 
     line = {
         "metric": METRIC,
@@ -548,9 +662,24 @@ def run_pkv(args):
         "cpu_baseline": cpu,
         "clocks": clk,
     }
+    run.close()
+    del run
+    torch.cuda.empty_cache()
+
+    # the other configurations, measured the same way after the headline one
+    # (its 78.6 GB pool freed first): decode M = 64, chunked prefill,
+    # shared-prefix forks
+    if (not args.no_extra and args.workload == "continuous_batching_m256" and args.kv_dtype == "f32"
+            and not args.split_keys and not args.image_cache_mb):
+        extra = {}
+        for name in EXTRA_WORKLOADS:
+            try:
+                extra[name] = measure_extra(name, args, rank)
+            except Exception as exc:  # keep the headline line whatever happens here
+                extra[name] = {"error": "%s: %s" % (type(exc).__name__, exc)}
+        line["extra_workloads"] = extra
     if rank == 0:
         print(json.dumps(line), flush=True)
-    run.close()
     if dist is not None:
         dist.destroy_process_group()
 
@@ -566,7 +695,7 @@ def run_reference(args):
     lens = [int(p + n) for p, n in zip(w.past_len, w.n_q)]
     total_s = max(20.0, min(150.0, 6.0 * (args.steps + args.warmup)))
     per_step = total_s / (args.steps + args.warmup)
-    rows = oracle_sample(w, lens, per_step, rng_seed=1, n_q=[int(x) for x in w.n_q])
+    rows = oracle_sample(w, lens, per_step, rng_seed=1, n_q=[int(x) for x in w.n_q], threads=0)
     rng = np.random.default_rng(w.seed)
     samples = []
     for r in rows:
@@ -575,15 +704,15 @@ def run_reference(args):
                         rng.standard_normal((tk, w.kv_dim)).astype(np.float32),
                         rng.standard_normal((tk, w.kv_dim)).astype(np.float32), n, tk))
     for _ in range(args.warmup):
-        time_oracle(samples, w)
-    dts, nbytes = [], 0.0
+        time_oracle(samples, w, threads=0)
+    dts, nbytes, cores = [], 0.0, 1
     for _ in range(args.steps):
-        dt, nbytes = time_oracle(samples, w)
+        dt, nbytes, cores = time_oracle(samples, w, threads=0)
         dts.append(dt)
     t = sum(dts)
     value = nbytes * args.steps / t / 1e9
-    sample = "%d of %d rows (%d keys) per step, C oracle, double accumulation, one thread" % (
-        len(rows), len(lens), sum(lens[r] for r in rows))
+    sample = "%d of %d rows (%d keys) per step, C oracle, double accumulation, %d threads" % (
+        len(rows), len(lens), sum(lens[r] for r in rows), cores)
     line = {
         "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t * 1e3 / args.steps, 3),
@@ -592,7 +721,7 @@ def run_reference(args):
         "config": {"workload": w.name, "M": w.M, "n_heads": w.n_heads, "n_kv_heads": w.n_kv_heads,
                    "head_dim": w.head_dim, "block_size": w.block_size, "n_layers": w.n_layers},
         "impl": "reference",
-        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
@@ -608,6 +737,8 @@ def main():
     ap.add_argument("--impl", choices=["pkv", "reference"], default="pkv")
     ap.add_argument("--workload", default="continuous_batching_m256")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="measure only --workload (the default run also measures %s)" % ", ".join(EXTRA_WORKLOADS))
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time")
     ap.add_argument("--split-keys", type=int, default=0, help="keys per split-K unit (0: library default)")
     ap.add_argument("--kv-dtype", choices=["f32", "bf16", "fp8"], default="f32",
