@@ -440,9 +440,8 @@ bool can_append(const pkv_seq *s, int32_t n) {
 
 // Work list for a set of rows.  Rows with many queries (and a supported
 // shape) become tensor-core prefill tiles; every other query becomes split-K
-// decode units.  Decode units with a full split of S keys come first (the heavy
-// ones), each query's last (ragged) split after them; prefill tiles are listed
-// latest-first (the latest queries see the most keys).
+// decode units, listed longest first; prefill tiles are listed latest-first
+// (the latest queries see the most keys).
 struct WorkList {
     std::vector<UnitDesc> units;
     std::vector<PrefillTile> tiles;
@@ -545,6 +544,14 @@ std::vector<char> add_cascades(std::vector<RowDesc> &rows, const std::vector<Cas
     return member;
 }
 
+// Keys of one decode unit (the host's copy of the kernels' unit_range).
+int32_t unit_keys(const UnitDesc &u, const RowDesc &rd, int causal, int32_t S) {
+    const int32_t total_k = rd.past_len + rd.n_q;
+    const int32_t lim = causal ? total_k - rd.n_q + u.qi + 1 : total_k;
+    const int32_t kbeg = rd.k0 + (u.split - rd.s0) * S;
+    return std::max(0, std::min(kbeg + S, lim) - kbeg);
+}
+
 void build_work(std::vector<RowDesc> &rows, int causal, int32_t S, int32_t head_dim,
                 int32_t group, WorkList &w, const std::vector<Cascade> &cas = {}) {
     std::vector<UnitDesc> tail;
@@ -596,6 +603,17 @@ void build_work(std::vector<RowDesc> &rows, int causal, int32_t S, int32_t head_
         }
     }
     w.units.insert(w.units.end(), tail.begin(), tail.end());
+    // longest units first, so that the grid's last CTAs are its shortest and
+    // the launch drains quickly (the order changes no result)
+    {
+        std::vector<std::pair<int32_t, int32_t>> key(w.units.size());
+        for (size_t i = 0; i < w.units.size(); ++i)
+            key[i] = {-unit_keys(w.units[i], rows[w.units[i].row], causal, S), static_cast<int32_t>(i)};
+        std::sort(key.begin(), key.end());
+        std::vector<UnitDesc> sorted(w.units.size());
+        for (size_t i = 0; i < key.size(); ++i) sorted[i] = w.units[key[i].second];
+        w.units.swap(sorted);
+    }
     // one merge list: decode items first (units refer to them by index), then prefill items
     w.merges.insert(w.merges.end(), w.pmerges.begin(), w.pmerges.end());
     w.pmerges.clear();

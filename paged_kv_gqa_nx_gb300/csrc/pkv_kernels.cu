@@ -646,6 +646,23 @@ __global__ void merge_splits_kernel(MergeArgs a) {
     }
     float *o = a.out + static_cast<size_t>(rd.q_row0 + md.qi) * (a.n_heads * a.hd) +
                static_cast<size_t>(h) * a.hd;
+    const bool vec = (a.hd & 3) == 0 && ((reinterpret_cast<uintptr_t>(a.pacc) |
+                                           reinterpret_cast<uintptr_t>(o)) & 15) == 0;
+    if (vec) {
+        // lane owns 4 consecutive dims: the splits' float4 loads are
+        // independent and in flight together (same sums, same order)
+        for (int d4 = lane; 4 * d4 < a.hd; d4 += 32) {
+            float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+            for (int s = 0; s < md.n_split; ++s) {
+                const size_t ph = static_cast<size_t>(md.part0 + s) * a.n_heads + h;
+                num = fma4(exp2f(a.pm[ph] - M), ldg4(a.pacc + ph * a.hd + 4 * d4), num);
+            }
+            reinterpret_cast<float4 *>(o)[d4] = make_float4(num.x / den, num.y / den, num.z / den,
+                                                            num.w / den);
+        }
+        return;
+    }
     for (int d = lane; d < a.hd; d += 32) {
         float num = 0.f;
         for (int s = 0; s < md.n_split; ++s) {
