@@ -284,9 +284,14 @@ PKV_API int pkv_attn_batch_rope(pkv_seq *const *seqs, int32_t M, const int32_t *
                         int32_t n_kv_heads, int32_t head_dim, int32_t layer, int32_t causal,
                         float scale, double rope_base, float *out);
 
-/* pkv_attn_batch taking HOST buffers for Q, K_new, V_new and out: copies the
- * inputs to device staging, runs the batch, copies out back, and returns when
- * out is filled (pinned host memory makes the copies asynchronous DMA). */
+/* pkv_attn_batch taking HOST buffers for Q, K_new, V_new and out; returns
+ * when out is filled, with the same result as pkv_attn_batch.  When Q and out
+ * are page-locked host memory the device can address (cudaHostAlloc /
+ * cudaMallocHost, or registered, under unified addressing; 16-byte aligned
+ * when head_dim % 4 == 0), the kernels read Q and write out in host memory
+ * directly, so those transfers overlap the attention work; K_new and V_new
+ * are copied to device staging first.  Other host memory is copied to device
+ * staging before the launches and back after them. */
 PKV_API int pkv_attn_batch_host(pkv_seq *const *seqs, int32_t M, const int32_t *n_q, const float *Q_host,
                         const float *K_new_host, const float *V_new_host, int32_t n_heads,
                         int32_t n_kv_heads, int32_t head_dim, int32_t layer, int32_t causal,

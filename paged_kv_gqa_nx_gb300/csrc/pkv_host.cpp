@@ -680,13 +680,12 @@ const T *dptr(const pkv_pool *p, size_t off) {
     return reinterpret_cast<const T *>(static_cast<unsigned char *>(p->desc.p) + off);
 }
 
-// Shared body of pkv_attn_batch / pkv_attn_with_paged / pkv_attn_batch_host /
-// pkv_append_layer.  `attend` = false stops after the append.
-int run_layer(pkv_seq *const *seqs, int32_t M, const int32_t *n_q, const float *Q,
-              const float *K_new, const float *V_new, int32_t n_heads, int32_t n_kv_heads,
-              int32_t head_dim, int32_t layer, int32_t causal, float scale, float *out,
-              bool host_io, bool attend, double rope_base = 0.0) {
-    // checks in the order of nx_f32_attn_with_paged: sizes, grouping, sequence
+// Argument checks of a layer call, before it changes anything, in the order
+// of nx_f32_attn_with_paged: sizes, grouping, sequence.
+int validate_layer(pkv_seq *const *seqs, int32_t M, const int32_t *n_q, const float *Q,
+                   const float *K_new, const float *V_new, int32_t n_heads, int32_t n_kv_heads,
+                   int32_t head_dim, int32_t layer, const float *out, bool host_io, bool attend,
+                   double rope_base) {
     if (M <= 0 || !n_q) return fail(PKV_ERR_BAD_DIM, "M must be positive and n_q non-NULL");
     for (int32_t r = 0; r < M; ++r)
         if (n_q[r] <= 0) return fail(PKV_ERR_BAD_DIM, "n_q[%d] = %d must be positive", r, n_q[r]);
@@ -734,7 +733,21 @@ int run_layer(pkv_seq *const *seqs, int32_t M, const int32_t *n_q, const float *
         if (!can_append(seqs[r], n_q[r]))
             return fail(PKV_ERR_SEQ, "rows [%d, %d) of batch row %d are not ensured (call pkv_ensure_append)",
                         seqs[r]->len, seqs[r]->len + n_q[r], r);
+    return PKV_OK;
+}
 
+// Shared body of pkv_attn_batch / pkv_attn_with_paged / pkv_attn_batch_host /
+// pkv_append_layer.  `attend` = false stops after the append.
+int run_layer(pkv_seq *const *seqs, int32_t M, const int32_t *n_q, const float *Q,
+              const float *K_new, const float *V_new, int32_t n_heads, int32_t n_kv_heads,
+              int32_t head_dim, int32_t layer, int32_t causal, float scale, float *out,
+              bool host_io, bool attend, double rope_base = 0.0) {
+    {
+        const int rc = validate_layer(seqs, M, n_q, Q, K_new, V_new, n_heads, n_kv_heads, head_dim,
+                                      layer, out, host_io, attend, rope_base);
+        if (rc) return rc;
+    }
+    pkv_pool *p = seqs[0]->pool;
     DevGuard dg(p->device);
     cudaStream_t st = p->stream;
     const int32_t q_dim = n_heads * head_dim;
@@ -1005,6 +1018,72 @@ int run_layer(pkv_seq *const *seqs, int32_t M, const int32_t *n_q, const float *
     return PKV_OK;
 }
 
+// The device address of host memory the kernels may read and write directly
+// (page-locked memory under unified addressing), or nullptr.
+void *device_view(const void *h) {
+    cudaPointerAttributes at{};
+    if (cudaPointerGetAttributes(&at, h) != cudaSuccess) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    return at.type == cudaMemoryTypeHost ? at.devicePointer : nullptr;
+}
+
+// Host buffers.  Page-locked host memory the device can address is read and
+// written by the kernels in place, so those transfers overlap the attention
+// work instead of preceding or following it -- where that pays (measured):
+//   calls with tensor-core prefill rows: staged copies of everything before
+//     and after the launches (a prefill CTA reads 64 KiB of queries before
+//     its first MMA and writes 64 KiB of output at its end; over the host
+//     link that stalls whole waves, costing more than the copies);
+//   decode calls with shared-prefix runs: out written in place (the merge
+//     kernel writes it), Q staged (the prefix pass reads it like a prefill);
+//   other decode calls: Q read and out written in place;
+//   K_new, V_new: always staged (the append reads them once).
+// Other host memory takes staged copies before and after the launches.
+int run_layer_host(pkv_seq *const *seqs, int32_t M, const int32_t *n_q, const float *Qh,
+                   const float *Kh, const float *Vh, int32_t n_heads, int32_t n_kv_heads,
+                   int32_t head_dim, int32_t layer, int32_t causal, float scale, float *outh) {
+    int rc = validate_layer(seqs, M, n_q, Qh, Kh, Vh, n_heads, n_kv_heads, head_dim, layer, outh,
+                            true, true, 0.0);
+    if (rc) return rc;
+    pkv_pool *p = seqs[0]->pool;
+    DevGuard dg(p->device);
+    const bool vec = (head_dim % 4) == 0;
+    auto usable = [&](const void *q) { return q && (vec ? aligned16(q) : aligned4(q)); };
+    const int32_t group = n_heads / n_kv_heads;
+    bool prefill = false, cascade = false;
+    if (prefill_shape(head_dim, group)) {
+        for (int32_t r = 0; r < M && !prefill; ++r) prefill = n_q[r] >= kPrefillMinQueries;
+        if (!prefill && g_cascade.load() != 0) cascade = !find_cascades(seqs, M, n_q, p->bs).empty();
+    }
+    float *Ov = prefill ? nullptr : static_cast<float *>(device_view(outh));
+    if (!usable(Ov))
+        return run_layer(seqs, M, n_q, Qh, Kh, Vh, n_heads, n_kv_heads, head_dim, layer, causal, scale,
+                         outh, true, true);
+    const float *Qv = cascade ? nullptr : static_cast<const float *>(device_view(Qh));
+    if (!usable(Qv)) Qv = nullptr;
+    int64_t T = 0;
+    for (int32_t r = 0; r < M; ++r) T += n_q[r];
+    const int32_t kv_dim = p->kv_dim, q_dim = n_heads * head_dim;
+    cudaStream_t st = p->stream;
+    const size_t in_floats = static_cast<size_t>(T) * (2 * kv_dim + (Qv ? 0 : q_dim));
+    cudaError_t e = p->io_in.ensure(in_floats * sizeof(float), st, p->device);
+    if (e != cudaSuccess) return cuda_fail(e, "staging buffers");
+    float *kd = static_cast<float *>(p->io_in.p), *vd = kd + T * kv_dim, *qd = vd + T * kv_dim;
+    e = cudaMemcpyAsync(kd, Kh, sizeof(float) * T * kv_dim, cudaMemcpyHostToDevice, st);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(vd, Vh, sizeof(float) * T * kv_dim, cudaMemcpyHostToDevice, st);
+    if (e == cudaSuccess && !Qv)
+        e = cudaMemcpyAsync(qd, Qh, sizeof(float) * T * q_dim, cudaMemcpyHostToDevice, st);
+    if (e != cudaSuccess) return cuda_fail(e, "input copy");
+    rc = run_layer(seqs, M, n_q, Qv ? Qv : qd, kd, vd, n_heads, n_kv_heads, head_dim, layer, causal,
+                   scale, Ov, false, true);
+    if (rc != PKV_OK) return rc;
+    e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return cuda_fail(e, "host-buffer call");
+    return PKV_OK;
+}
+
 // Contiguous-path globals: one staging ring and error word per device.
 std::mutex g_contig_mu;
 Stager g_contig_stager[64];
@@ -1178,6 +1257,7 @@ void pkv_pool_free(pkv_pool *p) {
         p->icache.buf.release(p->stream);
         cudaStreamSynchronize(p->stream);
         p->stager.destroy();
+
         if (p->owns_kv) {
             cudaFree(p->k);
             cudaFree(p->v);
@@ -1505,8 +1585,8 @@ int pkv_attn_batch_host(pkv_seq *const *seqs, int32_t M, const int32_t *n_q, con
                         const float *K_new_host, const float *V_new_host, int32_t n_heads,
                         int32_t n_kv_heads, int32_t head_dim, int32_t layer, int32_t causal,
                         float scale, float *out_host) {
-    return run_layer(seqs, M, n_q, Q_host, K_new_host, V_new_host, n_heads, n_kv_heads, head_dim,
-                     layer, causal, scale, out_host, true, true);
+    return run_layer_host(seqs, M, n_q, Q_host, K_new_host, V_new_host, n_heads, n_kv_heads,
+                          head_dim, layer, causal, scale, out_host);
 }
 
 int pkv_attn_contiguous(const float *Q, const float *Kc, const float *Vc, int32_t n_q,

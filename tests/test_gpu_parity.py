@@ -202,6 +202,60 @@ def test_host_buffer_entry_point_matches_device_path():
 
 
 @pytest.mark.gpu
+@pytest.mark.parametrize("pinned,decode_only", [(True, False), (False, False), (True, True)],
+                         ids=["pinned", "pageable", "pinned-decode"])
+def test_host_buffers_match_device_path_large_batch(pinned, decode_only):
+    """Host-buffer calls: a ~75 MB batch of chunked-prefill rows and a run of
+    20 forks that share a 2048-token prefix (one shared-prefix pass), or the
+    forks and the other sequences' decode rows alone.  Page-locked buffers
+    let the kernels use Q and out in host memory for decode calls (out only
+    with a shared-prefix run); pageable ones, and calls with prefill rows,
+    copy through device staging.  Every row equals the device-path call, bit
+    for bit."""
+    H, KV, hd, bs = 32, 8, 128, 16
+    q_dim, kv_dim = H * hd, KV * hd
+    g = torch.Generator().manual_seed(21)
+    pool = GpuPool(1024, 1, kv_dim, bs, max_seqs=32, max_blocks=160, shuffle_seed=5)
+    try:
+        a = pool.new_seq(1024 + 256)
+        pool.grow(a, 256)
+        pool.write_history(a, 0, torch.randn(256, kv_dim, generator=g), torch.randn(256, kv_dim, generator=g))
+        root = pool.new_seq(2048 + 8)
+        pool.grow(root, 2048)
+        pool.write_history(root, 0, torch.randn(2048, kv_dim, generator=g), torch.randn(2048, kv_dim, generator=g))
+        forks = [pkv.pkv_seq_fork(root) for _ in range(20)]
+        assert all(forks)
+        b = pool.new_seq(1024 + 512)
+        pool.grow(b, 512)
+        pool.write_history(b, 0, torch.randn(512, kv_dim, generator=g), torch.randn(512, kv_dim, generator=g))
+        c = pool.new_seq(1024)
+        seqs = [a] + forks + [b, c]
+        nq = [1] * 23 if decode_only else [1024] + [1] * 20 + [1024, 1024]
+        T = sum(nq)
+        Q = torch.randn(T, q_dim, generator=g)
+        K = torch.randn(T, kv_dim, generator=g)
+        V = torch.randn(T, kv_dim, generator=g)
+        out_h = torch.full((T, q_dim), float("nan"))
+        if pinned:
+            Q, K, V, out_h = Q.pin_memory(), K.pin_memory(), V.pin_memory(), out_h.pin_memory()
+            args = (Q, K, V, out_h)
+        else:
+            args = tuple(np.ascontiguousarray(t.numpy()) for t in (Q, K, V, out_h))
+        pkv.check(pkv.pkv_ensure_append_batch(seqs, nq))
+        pkv.check(pkv.pkv_attn_batch_host(seqs, nq, args[0], args[1], args[2], H, KV, hd, 0, 1, 0.088,
+                                          args[3]))
+        got = torch.from_numpy(args[3]) if not pinned else out_h
+        out_d = torch.empty(T, q_dim, device="cuda")
+        pkv.check(pkv.pkv_attn_batch(seqs, nq, Q.cuda(), K.cuda(), V.cuda(), H, KV, hd, 0, 1, 0.088,
+                                     out_d))
+        assert pkv.pkv_pool_last_work(pool.p)["prefix_tiles"] > 0     # the forks ran as one run
+        pool.check_no_device_error()
+        assert bits_equal(got.cuda(), out_d)
+    finally:
+        pool.close()
+
+
+@pytest.mark.gpu
 def test_error_paths_change_nothing():
     H, KV, hd, bs = 32, 8, 128, 16
     pool = GpuPool(8, 1, KV * hd, bs, max_seqs=4, max_blocks=8)
