@@ -80,16 +80,17 @@ typedef void *pkv_stream_t; /* cudaStream_t */
 /* bf16 storage (no counterpart on the pages, which store f32): every K/V row
  * is rounded to the nearest bfloat16 (ties to even) when it is written and
  * widened to f32 when it is read; all arithmetic stays f32.  Halves the pool's
- * bytes and the decode traffic.  Needs an even kv_dim.  The fused append is
- * not used on such pools, and the contiguous twin stays f32. */
+ * bytes and the decode traffic.  Needs an even kv_dim.  The fused append
+ * (pkv_set_fused_append) rounds the new rows the same way; the contiguous
+ * twin stays f32. */
 #define PKV_POOL_BF16 2u
 /* fp8 e4m3 storage (no counterpart on the pages): every K/V row is stored as
  * e4m3(x / scale) -- nearest, ties to even, saturated to +-448 -- and read as
  * that value times scale; scale is a power of two (pkv_pool_set_kv_scale,
  * default 1), so the read values are exact in f32 and tf32 and only the
  * storage rounding differs from f32.  Quarters the pool's bytes.  Needs kv_dim
- * % 4 == 0 (% 16 with head_dim 128).  As for bf16: no fused append, and the
- * contiguous twin stays f32. */
+ * % 4 == 0 (% 16 with head_dim 128).  As for bf16, the fused append rounds
+ * the new rows the same way, and the contiguous twin stays f32. */
 #define PKV_POOL_FP8 4u
 
 /* ---------------------------------------------------------------- pool ---- */
@@ -382,14 +383,16 @@ PKV_API int32_t pkv_get_split_keys(void);
 
 /* Fused append (default on).  The per-layer step appends the new K/V rows
  * into their pages and then attends over the sequence ("nx_f32_attn_paged.nx
- * source", header comment and step 1 of nx_f32_attn_with_paged).  With fusion on, a decode call
- * -- no row takes the tensor-core prefill path, head_dim 128, group size 1, 2
- * or 4 -- whose pending page-table changes all lie in pages that hold only
- * this call's new positions (fresh pages; not a copy-on-append tail, a fork or
- * a truncate) runs as the decode kernel alone: it reads the new rows from
- * K_new / V_new, stores them into the pool and enters the new pages into the
- * device page table, with no separate append launch.  Every other call takes
- * the unfused path.  Results, pool contents and page tables are bit-identical
+ * source", header comment and step 1 of nx_f32_attn_with_paged).  With
+ * fusion on, a decode call -- no row takes the tensor-core prefill path,
+ * head_dim 128, group size 1, 2 or 4 (8 too on an fp8 pool), no RoPE -- whose
+ * pending page-table changes all lie in pages that hold only this call's new
+ * positions (fresh pages; not a copy-on-append tail, a fork or a truncate)
+ * runs as the decode kernel alone: it reads the new rows from K_new / V_new
+ * (rounded to the pool element as the append rounds them, on bf16 / fp8
+ * pools), stores them into the pool and enters the new pages into the device
+ * page table, with no separate append launch.  Every other call takes the
+ * unfused path.  Results, pool contents and page tables are bit-identical
  * either way.  on != 0 enables; process-wide. */
 PKV_API int pkv_set_fused_append(int32_t on);
 PKV_API int32_t pkv_get_fused_append(void);

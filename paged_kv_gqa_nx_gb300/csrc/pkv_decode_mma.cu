@@ -200,10 +200,50 @@ __global__ void __launch_bounds__(128, 3) decode_mma_kernel(AttnArgs a, PagedRow
     const size_t rstride = rows_of.row_stride();
     const bool pages16 = rows_of.whole_tiles(16) && (ur.kbeg & 15) == 0;
     const E *const zsrc = static_cast<const E *>(cv ? rows_of.a.v : rows_of.a.k);  // read by no copy
-    auto load_tile = [&](int kl, int st) {
-        const int pos0 = ur.kbeg + (warp + kl * W) * T;
-        const int nv = min(T, ur.kend - pos0);
+    // fused append: positions from past_len on are this call's new rows; they
+    // come from K_new / V_new (f32), rounded as the append rounds them
+    const bool fused = a.K_new != nullptr;
+    const int new0 = fused ? rd.past_len : 0x7fffffff;
+    const float inv_scale = 1.f / rows_of.a.kv_scale;  // power of two: exact
+    // New row `key` of the tile (position pos) -> the stage, in the layout the
+    // copies use (chunk c of key j at j * RB + ((c ^ (j & 7)) << 4)): lane l <
+    // 2 * CPR converts chunk l % CPR of K (l < CPR) or V with the append's
+    // rounding (store4's conversions) and stores its 16 bytes.
+    auto put_new = [&](uint32_t stage, int key, int pos) {
+        if (lane >= 2 * CPR) return;
+        const int half = lane / CPR, c = lane - half * CPR;
+        const float *src = (half ? a.V_new : a.K_new) +
+                           static_cast<size_t>(rd.q_row0 + (pos - new0)) * rstride +
+                           static_cast<size_t>(kvh) * kHD + c * EPC;
+        uint32_t w[4];
+#pragma unroll
+        for (int i = 0; i < EPC / 4; ++i) {
+            float4 x = __ldg(reinterpret_cast<const float4 *>(src) + i);
+            if constexpr (kF8) {
+                x = make_float4(x.x * inv_scale, x.y * inv_scale, x.z * inv_scale, x.w * inv_scale);
+                const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(x.x, x.y), __NV_SATFINITE, __NV_E4M3);
+                const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(x.z, x.w), __NV_SATFINITE, __NV_E4M3);
+                w[i] = lo | (hi << 16);
+            } else {
+                const __nv_bfloat162 lo = __floats2bfloat162_rn(x.x, x.y);
+                const __nv_bfloat162 hi = __floats2bfloat162_rn(x.z, x.w);
+                w[2 * i] = *reinterpret_cast<const uint32_t *>(&lo);
+                w[2 * i + 1] = *reinterpret_cast<const uint32_t *>(&hi);
+            }
+        }
+        const uint32_t dst = stage + (half ? T * RB : 0) + key * RB + ((c ^ (key & 7)) << 4);
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};\n" ::"r"(dst), "r"(w[0]), "r"(w[1]),
+                     "r"(w[2]), "r"(w[3])
+                     : "memory");
+    };
+    // One tile's copies.  kNew (a tile that holds this call's new rows): a key
+    // slot is written once, by a copy (pool rows; zero past the unit) or, for
+    // a new row, by put_new; every other tile takes the copies alone, with no
+    // per-key test (this kernel is bound by the instructions it issues).
+    auto copy_tile = [&](int pos0, int st, int nv, int nall, auto new_rows) {
+        constexpr bool kNew = decltype(new_rows)::value;
         const uint32_t dst0 = cdst + st * STAGE;
+        auto skip = [&](int j) { return kNew && j >= nv && j < nall; };
         if (pages16) {
             // 16 positions from a multiple of 16 share one page
 #pragma unroll
@@ -214,6 +254,7 @@ __global__ void __launch_bounds__(128, 3) decode_mma_kernel(AttnArgs a, PagedRow
 #pragma unroll
                 for (int i = 0; i < 16 / KPP; ++i) {
                     const int jj = 16 * g + i * KPP;
+                    if (skip(jj + cj)) continue;
                     const bool ok = okg && jj + cj < nv;
                     cp_async16_n(dst0 + jj * RB + ((csw ^ ((i * KPP) & 7)) << 4),
                                  ok ? b + static_cast<size_t>(i * KPP) * rstride : zsrc, ok ? 16u : 0u);
@@ -223,12 +264,25 @@ __global__ void __launch_bounds__(128, 3) decode_mma_kernel(AttnArgs a, PagedRow
 #pragma unroll 1
             for (int jj = 0; jj < T; jj += KPP) {
                 const int j = jj + cj;
+                if (skip(j)) continue;
                 const E *kr, *vr;
                 const bool ok = j < nv && rows_of.row(rd.slot, pos0 + j, kvh, kHD, kr, vr, a.err);
                 cp_async16_n(cdst - cj * RB + st * STAGE + j * RB + ((cch ^ (j & 7)) << 4),
                              ok ? (cv ? vr : kr) + cch * EPC : zsrc, ok ? 16u : 0u);
             }
         }
+        if constexpr (kNew) {
+            const uint32_t stage = wbase_s + st * STAGE;
+            for (int j = max(nv, 0); j < nall; ++j) put_new(stage, j, pos0 + j);
+        }
+    };
+    auto load_tile = [&](int kl, int st) {
+        const int pos0 = ur.kbeg + (warp + kl * W) * T;
+        const int nall = min(T, ur.kend - pos0);  // keys of the unit in this tile
+        if (pos0 + T > new0)
+            copy_tile(pos0, st, min(nall, new0 - pos0), nall, std::true_type{});
+        else
+            copy_tile(pos0, st, nall, nall, std::false_type{});
     };
 
     // the first tiles are in flight while the queries are prepared
@@ -236,6 +290,20 @@ __global__ void __launch_bounds__(128, 3) decode_mma_kernel(AttnArgs a, PagedRow
     for (int s = 0; s < NST - 1; ++s) {
         if (s < my_n) load_tile(s, s);
         cp_async_commit();
+    }
+
+    // fused append: the unit of the row's last query stores the new rows of
+    // its split into the pool (nothing in this launch reads them from there;
+    // the first tiles' copies are already in flight), and enters each new
+    // page into the device page table
+    if (fused && u.qi == rd.n_q - 1) {
+        for (int pos = max(ur.kbeg, new0) + warp; pos < ur.kend; pos += W) {
+            const int t = pos - new0;
+            const AppendDesc ad = a.app[rd.q_row0 + t];
+            const size_t o = static_cast<size_t>(rd.q_row0 + t) * rstride + static_cast<size_t>(kvh) * kHD;
+            const bool set_pt = a.pt_write && kvh == 0 && (pos == 0 || rows_of.block_start(pos));
+            rows_of.store_row(rd.slot, ad.blk, pos, kvh, kHD, a.K_new + o, a.V_new + o, set_pt, lane, a.err);
+        }
     }
 
     // this lane's query head; for bf16, lanes gid >= 4 carry the third piece
@@ -521,8 +589,7 @@ cudaError_t launch_mma(const AttnArgs &a, const PagedAddr &addr, cudaStream_t s)
 }  // namespace
 
 cudaError_t launch_decode_mma_paged(const AttnArgs &a, const PagedAddr &addr, cudaStream_t s) {
-    if (!decode_mma_shape(a.hd, a.group, addr.bf16 != 0, addr.fp8 != 0) || a.K_new != nullptr)
-        return cudaErrorInvalidValue;
+    if (!decode_mma_shape(a.hd, a.group, addr.bf16 != 0, addr.fp8 != 0)) return cudaErrorInvalidValue;
     if (addr.fp8) {
         switch (a.group) {
             case 1: return launch_mma<1, fp8>(a, addr, s);

@@ -525,8 +525,11 @@ std::vector<char> add_cascades(std::vector<RowDesc> &rows, const std::vector<Cas
         RowDesc vr{rows[c.r0].slot, c.Lp - c.n, c.n, rows[c.r0].q_row0};
         const int32_t vi = static_cast<int32_t>(rows.size());
         rows.push_back(vr);
-        for (int32_t q0 = 0; q0 < c.n; q0 += TQ)
-            for (int32_t sp = 0; sp < n_pref; ++sp)
+        // split-major: the query tiles that read the same prefix keys (the
+        // same operand images) are neighbours in the grid, so they run
+        // together and share those images in L2
+        for (int32_t sp = 0; sp < n_pref; ++sp)
+            for (int32_t q0 = 0; q0 < c.n; q0 += TQ)
                 w.ctiles.push_back({vi, q0, sp, part0 + q0 * stride, stride});
         for (int32_t t = 0; t < c.n; ++t) {
             const int32_t r = c.r0 + t;
@@ -773,9 +776,13 @@ int run_layer(pkv_seq *const *seqs, int32_t M, const int32_t *n_q, const float *
     if (attend && g_cascade.load() != 0 && prefill_shape(head_dim, group))
         cas = find_cascades(seqs, M, n_q, p->bs);
     if (attend) build_work(rows, causal, S, head_dim, group, w, cas);
-    const bool fuse = attend && rope_base == 0.0 && !p->narrow() && g_fused_append.load() != 0 && w.tiles.empty() &&
-                      w.ctiles.empty() && !w.units.empty() &&
-                      head_dim == 128 && (group == 1 || group == 2 || group == 4) &&
+    // the decode kernels that take the append themselves: the f32 kernel for
+    // groups 1, 2, 4 and the narrow-pool kernel for its shapes (head_dim 128)
+    const bool fuse_shape = head_dim == 128 &&
+                            (p->narrow() ? decode_mma_shape(head_dim, group, p->bf16, p->fp8)
+                                         : (group == 1 || group == 2 || group == 4));
+    const bool fuse = attend && rope_base == 0.0 && g_fused_append.load() != 0 && w.tiles.empty() &&
+                      w.ctiles.empty() && !w.units.empty() && fuse_shape &&
                       dirty_within_appends(p, seqs, M, n_q);
 
     if (attend) {

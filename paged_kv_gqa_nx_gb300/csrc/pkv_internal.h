@@ -207,7 +207,8 @@ cudaError_t launch_copy_blocks(void *k, void *v, const CopyDesc *items, int32_t 
 cudaError_t launch_decode_paged(const AttnArgs &a, const PagedAddr &addr, cudaStream_t s);
 cudaError_t launch_decode_contig(const AttnArgs &a, const ContigAddr &addr, cudaStream_t s);
 // Decode over a bf16 or fp8 pool on the tensor cores (pkv_decode_mma.cu), for
-// the shapes decode_mma_shape accepts; no fused append.
+// the shapes decode_mma_shape accepts; with AttnArgs::K_new it also takes the
+// fused append (the new rows rounded to the pool element as the append does).
 cudaError_t launch_decode_mma_paged(const AttnArgs &a, const PagedAddr &addr, cudaStream_t s);
 __host__ __device__ constexpr bool decode_mma_shape(int head_dim, int group, bool bf16, bool fp8) {
     return head_dim == 128 &&

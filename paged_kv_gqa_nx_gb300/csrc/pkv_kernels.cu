@@ -366,8 +366,15 @@ __global__ void __launch_bounds__(128, 3) decode_fast_kernel(AttnArgs a, Rows ro
         }
     };
 
+#pragma unroll
+    for (int s = 0; s < NST - 1; ++s) {
+        if (s < my_n) load_tile(s, s);
+        cp_async_commit();
+    }
+
     // fused append: the unit of the row's last query stores the new rows of
-    // its split into the pool (nothing in this launch reads them from there)
+    // its split into the pool (nothing in this launch reads them from there;
+    // the first tiles' copies are already in flight)
     if (kF32 && fused && u.qi == rd.n_q - 1) {
         for (int pos = max(ur.kbeg, new0) + warp; pos < ur.kend; pos += W) {
             const int t = pos - new0;
@@ -376,12 +383,6 @@ __global__ void __launch_bounds__(128, 3) decode_fast_kernel(AttnArgs a, Rows ro
             const bool set_pt = a.pt_write && kvh == 0 && (pos == 0 || rows_of.block_start(pos));
             rows_of.store_row(rd.slot, ad.blk, pos, kvh, HD, a.K_new + o, a.V_new + o, set_pt, lane, a.err);
         }
-    }
-
-#pragma unroll
-    for (int s = 0; s < NST - 1; ++s) {
-        if (s < my_n) load_tile(s, s);
-        cp_async_commit();
     }
 
     constexpr int LPH = C::LPH;
@@ -766,9 +767,10 @@ cudaError_t launch_copy_blocks(void *kp, void *vp, const CopyDesc *items, int32_
 
 cudaError_t launch_decode_paged(const AttnArgs &a, const PagedAddr &addr, cudaStream_t s) {
     // bf16 / fp8 pools: the tensor-core decode kernel where it has the shape
-    if (PKV_NARROW_MMA && a.K_new == nullptr &&
-        decode_mma_shape(a.hd, a.group, addr.bf16 != 0, addr.fp8 != 0))
+    // (the only narrow-pool kernel that takes a fused append)
+    if (PKV_NARROW_MMA && decode_mma_shape(a.hd, a.group, addr.bf16 != 0, addr.fp8 != 0))
         return launch_decode_mma_paged(a, addr, s);
+    if ((addr.bf16 || addr.fp8) && a.K_new != nullptr) return cudaErrorInvalidValue;
     if (addr.fp8) return launch_decode(a, PagedRows<fp8>{addr}, s);
     if (addr.bf16) return launch_decode(a, PagedRows<bf16>{addr}, s);
     return launch_decode(a, PagedRows<float>{addr}, s);

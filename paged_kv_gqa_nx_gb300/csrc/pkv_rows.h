@@ -7,6 +7,7 @@
 #pragma once
 
 #include "pkv_elem.h"
+#include <type_traits>
 #include "pkv_internal.h"
 
 namespace pkv {
@@ -66,7 +67,8 @@ struct PagedRows {
         return (a.bs_shift >= 0 ? (pos & (a.bs - 1)) : (pos % a.bs)) == 0;
     }
     // Fused append: store head kvh's hd floats of one new row (K and V) at
-    // position pos of block blk, one float4 per lane of the calling warp;
+    // position pos of block blk, one float4 per lane of the calling warp,
+    // rounded to the pool element as the append kernel rounds them;
     // with set_pt, also enter blk as the page of pos.  False (and the error
     // flag) on an out-of-range block id or page index.
     __device__ __forceinline__ bool store_row(int slot, int blk, int pos, int kvh, int hd,
@@ -80,8 +82,15 @@ struct PagedRows {
         const size_t o = static_cast<size_t>(blk) * a.block_stride + a.layer_off +
                          static_cast<size_t>(pos - bi * a.bs) * a.kv_dim + static_cast<size_t>(kvh) * hd;
         for (int i = lane; 4 * i < hd; i += 32) {
-            store4(static_cast<E *>(a.k) + o + 4 * i, ldg4(ks + 4 * i));
-            store4(static_cast<E *>(a.v) + o + 4 * i, ldg4(vs + 4 * i));
+            float4 k4 = ldg4(ks + 4 * i), v4 = ldg4(vs + 4 * i);
+            if constexpr (std::is_same<E, fp8>::value) {
+                // e4m3 of x / scale, as the append kernel stores it (a power of two: exact)
+                const float inv = 1.f / a.kv_scale;
+                k4 = make_float4(k4.x * inv, k4.y * inv, k4.z * inv, k4.w * inv);
+                v4 = make_float4(v4.x * inv, v4.y * inv, v4.z * inv, v4.w * inv);
+            }
+            store4(static_cast<E *>(a.k) + o + 4 * i, k4);
+            store4(static_cast<E *>(a.v) + o + 4 * i, v4);
         }
         if (set_pt && lane == 0) a.pt[static_cast<size_t>(slot) * a.max_blocks + bi] = blk;
         return true;

@@ -27,10 +27,15 @@ def fused_mode():
     pkv.pkv_set_fused_append(old)
 
 
-def _run(fused, lens, n_q, steps, n_layers=2, bs=16, seed=7, fork_tail=False, split=None):
+DTYPES = {"f32": torch.float32, "bf16": torch.bfloat16, "fp8": torch.float8_e4m3fn}
+
+
+def _run(fused, lens, n_q, steps, n_layers=2, bs=16, seed=7, fork_tail=False, split=None,
+         dtype="f32", kv_scale=1.0, heads=(H, KV)):
     """Build a pool, write seeded histories, then `steps` decode steps of n_q
     tokens per row.  Returns the per-(step, layer) outputs, the pool tensors,
     the host page tables and the launch counts of the steps per kind."""
+    H, KV = heads
     pkv.pkv_set_fused_append(fused)
     old_split = pkv.pkv_get_split_keys()
     if split:
@@ -39,7 +44,8 @@ def _run(fused, lens, n_q, steps, n_layers=2, bs=16, seed=7, fork_tail=False, sp
     max_tok = max(lens) + n_q * steps + 8
     n_blocks = sum((L + n_q * steps + bs) // bs + 2 for L in lens) + 16
     pool = GpuPool(n_blocks, n_layers, kv_dim, bs, max_seqs=2 * len(lens) + 2,
-                   max_blocks=(max_tok + bs - 1) // bs + 1, shuffle_seed=seed)
+                   max_blocks=(max_tok + bs - 1) // bs + 1, shuffle_seed=seed,
+                   dtype=DTYPES[dtype], kv_scale=kv_scale)
     try:
         seqs = []
         for r, L in enumerate(lens):
@@ -94,7 +100,9 @@ def _compare(a, b):
         assert bits_equal(x, y), "output %d differs between fused and unfused" % i
     assert pta == ptb
     # NaN-filled pools: compare bit patterns, so untouched rows match too
-    assert bits_equal(Ka, Kb) and bits_equal(Va, Vb), "pool contents differ"
+    as_bytes = lambda t: t.contiguous().view(torch.uint8)  # noqa: E731
+    assert torch.equal(as_bytes(Ka), as_bytes(Kb)) and torch.equal(as_bytes(Va), as_bytes(Vb)), \
+        "pool contents differ"
 
 
 @pytest.mark.gpu
@@ -144,3 +152,35 @@ def test_fused_append_falls_back_on_copy_on_append(fused_mode):
     _compare(fused, plain)
     assert fused[4][pkv.PKV_KERNEL_APPEND] == 1
     assert plain[4][pkv.PKV_KERNEL_APPEND] == 3 * 2
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("dtype,kv_scale,heads", [("bf16", 1.0, (32, 8)), ("bf16", 1.0, (16, 8)),
+                                                  ("fp8", 1.0, (32, 8)), ("fp8", 2.0, (64, 8))],
+                         ids=["bf16-g4", "bf16-g2", "fp8-g4", "fp8-scale2-g8"])
+def test_fused_append_narrow_pools(dtype, kv_scale, heads, fused_mode):
+    """bf16 and fp8 pools: the narrow-pool decode kernel takes the append
+    itself, rounding the new rows exactly as the append kernel does (fp8:
+    e4m3 of x / scale, saturating); outputs, pool bytes and page tables equal
+    the unfused path's."""
+    lens = [15, 16, 31, 1023, 1024, 2047, 100, 5]
+    fused = _run(True, lens, 1, steps=3, dtype=dtype, kv_scale=kv_scale, heads=heads)
+    plain = _run(False, lens, 1, steps=3, dtype=dtype, kv_scale=kv_scale, heads=heads)
+    _compare(fused, plain)
+    assert fused[4][pkv.PKV_KERNEL_APPEND] == 0
+    assert plain[4][pkv.PKV_KERNEL_APPEND] == 3 * 2
+    assert fused[4]["work"]["fused_append"] == 1
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("dtype", ["bf16", "fp8"])
+def test_fused_append_narrow_pools_multi_query_and_small_pages(dtype, fused_mode):
+    # 3 new tokens per row on both sides of a split boundary; then block
+    # size 4, where a 16- or 32-key tile spans several pages
+    for kw in (dict(lens=[1022, 2046, 40, 7], n_q=3, steps=2),
+               dict(lens=[3, 8, 33, 300], n_q=1, steps=3, bs=4, split=64)):
+        lens, n_q, steps = kw.pop("lens"), kw.pop("n_q"), kw.pop("steps")
+        fused = _run(True, lens, n_q, steps, dtype=dtype, **kw)
+        plain = _run(False, lens, n_q, steps, dtype=dtype, **kw)
+        _compare(fused, plain)
+        assert fused[4][pkv.PKV_KERNEL_APPEND] == 0
