@@ -117,9 +117,27 @@ def tensor_peak():
     1.1/2.25 / 3) for context."""
     tf32 = measured_tf32_tflops()
     bf16, kind = measured_bf16_peak()
-    return tf32 / 3.0, {"tf32_tflops_cublas": round(tf32, 1),
-                        "from_bf16_nominal_ratio": round(bf16 * (1.1 / 2.25) / 3.0, 1),
-                        "bf16_source": kind}
+    detail = {"tf32_tflops_cublas": round(tf32, 1),
+              "from_bf16_nominal_ratio": round(bf16 * (1.1 / 2.25) / 3.0, 1),
+              "bf16_source": kind}
+    detail.update(tcgen05_tf32_rates())
+    return tf32 / 3.0, detail
+
+
+def tcgen05_tf32_rates():
+    """The issue rate of the prefill kernel's own instruction, measured by the
+    library's probe (pkv_probe_tf32_mma): tcgen05.mma kind::tf32, M = 128, A
+    in tensor memory, at N = 64 (its QK^T products) and N = 128 (its PV
+    products)."""
+    if "probe" in _TF32_CACHE:
+        return _TF32_CACHE["probe"]
+    import paged_kv_gqa_nx_gb300 as pkv
+    out = {}
+    for n in (64, 128):
+        clk, tf = pkv.pkv_probe_tf32_mma(n, True, 4096)
+        out["tcgen05_tf32_n%d" % n] = {"clk_per_mma": round(clk, 2), "tflops": round(tf, 1)}
+    _TF32_CACHE["probe"] = out
+    return out
 
 
 def kernel_source_digest(kernel: str = "decode", kv_dtype: str = "f32"):

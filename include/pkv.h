@@ -431,6 +431,20 @@ PKV_API int pkv_profile_enable(int32_t on);
 PKV_API int pkv_profile_reset(void);
 PKV_API int pkv_profile_read(int32_t kind, double *ms, int64_t *launches);
 
+/* Measured issue rate of tcgen05.mma kind::tf32 (diagnostic for the roofline
+ * of the tensor-core kernels; no counterpart on the pages).  On the current
+ * device, one CTA per SM has one thread issue `iters` MMAs of M = 128, N =
+ * n_cols, K = 8 back to back into one accumulator (A from tensor memory when
+ * a_in_tmem != 0, else from shared memory; B from shared memory; zero
+ * operands).  Writes the SM clocks per MMA (SM 0's CTA) and the GPU's TF32
+ * rate in TFLOP/s (2 * 128 * n_cols * 8 flops per MMA, over the launch's
+ * CUDA-event time).  n_cols 64, 128 or 256; iters a multiple of 16 in
+ * [16, 1048576].  Synchronous; allocates a few bytes of device memory.
+ * PKV_ERR_ARG, PKV_ERR_CUDA, or PKV_ERR_DEVICE_TIMEOUT if the bounded wait for
+ * the MMAs ran out. */
+PKV_API int pkv_probe_tf32_mma(int32_t n_cols, int32_t a_in_tmem, int32_t iters, double *clk_per_mma,
+                               double *tflops);
+
 /* Description of the calling thread's last failure ("" if none). */
 PKV_API const char *pkv_last_error(void);
 

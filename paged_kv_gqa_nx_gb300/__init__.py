@@ -118,6 +118,8 @@ _SIGS = {
     "pkv_profile_enable": (_int, [_i32]),
     "pkv_profile_reset": (_int, []),
     "pkv_profile_read": (_int, [_i32, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int64)]),
+    "pkv_probe_tf32_mma": (_int, [_i32, _i32, _i32, ctypes.POINTER(ctypes.c_double),
+                                  ctypes.POINTER(ctypes.c_double)]),
     "pkv_last_error": (ctypes.c_char_p, []),
 }
 
@@ -428,6 +430,16 @@ def pkv_profile_read(kind):
     if rc != PKV_OK:
         raise PkvError(rc)
     return ms.value, n.value
+
+
+def pkv_probe_tf32_mma(n_cols, a_in_tmem=True, iters=4096):
+    """(SM clocks per MMA, TFLOP/s) of back-to-back tcgen05.mma kind::tf32,
+    M = 128, N = n_cols (see include/pkv.h)."""
+    clk = ctypes.c_double()
+    tf = ctypes.c_double()
+    check(_lib.pkv_probe_tf32_mma(int(n_cols), 1 if a_in_tmem else 0, int(iters), ctypes.byref(clk),
+                                  ctypes.byref(tf)))
+    return clk.value, tf.value
 
 
 def check(rc: int, what: str = "") -> None:

@@ -23,7 +23,8 @@ BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(HERE, "libpkv.so")
 HEADERS = [os.path.join(ROOT, "include", "pkv.h"), os.path.join(CSRC, "pkv_internal.h"),
            os.path.join(CSRC, "pkv_tcgen05.h")]
-SOURCES = ["pkv_kernels.cu", "pkv_decode_mma.cu", "pkv_prefill.cu", "pkv_host.cpp", "pkv_noalloc.cu"]
+SOURCES = ["pkv_kernels.cu", "pkv_decode_mma.cu", "pkv_prefill.cu", "pkv_host.cpp", "pkv_noalloc.cu",
+           "pkv_probe.cu"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 COMMON = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC",

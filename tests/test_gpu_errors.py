@@ -89,3 +89,19 @@ def test_error_bits_arguments_are_checked():
         assert pkv.pkv_debug_or_error_bits(host, pkv.PKV_ERRWORD_POOL, 1) == pkv.PKV_ERR_ARG
     finally:
         pkv.pkv_pool_free(host)
+
+
+@pytest.mark.gpu
+def test_tf32_probe_reports_rates_and_checks_arguments():
+    """The tcgen05 TF32 issue-rate probe: positive clocks per MMA and rate for
+    both operand sources, wider MMAs no cheaper per flop than N = 64 pays in
+    clocks, and bad arguments rejected before any launch."""
+    for n, ts in ((64, True), (128, True), (64, False)):
+        clk, tf = pkv.pkv_probe_tf32_mma(n, ts, 256)
+        assert clk > 0 and tf > 0, (n, ts, clk, tf)
+    c64, _ = pkv.pkv_probe_tf32_mma(64, True, 1024)
+    c128, _ = pkv.pkv_probe_tf32_mma(128, True, 1024)
+    assert c128 >= c64 * 0.9          # twice the work per MMA never costs less time
+    for args in ((96, 1, 256), (64, 1, 100), (64, 1, 0)):
+        with pytest.raises(pkv.PkvError):
+            pkv.pkv_probe_tf32_mma(*args)
