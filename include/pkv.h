@@ -138,8 +138,9 @@ PKV_API int32_t pkv_pool_free_blocks(const pkv_pool *pool);
  *   tiles, [3] merge items, [4] visible (query, key) pairs of the prefill rows,
  *   [5] (query, key) pairs of the shared-prefix pass, [6] 1 if the call ran
  *   with the fused append, [7] operand images (64-key tile x kv heads) the
- *   call took from the image cache, [8] operand images it built. */
-#define PKV_WORK_FIELDS 9
+ *   call took from the image cache, [8] operand images it built, [9] keys per
+ *   split of the shared-prefix pass (0 without one). */
+#define PKV_WORK_FIELDS 10
 PKV_API int pkv_pool_last_work(const pkv_pool *pool, int64_t *out, int32_t cap);
 
 /* Operand-image cache (no counterpart on the pages; off by default).  The

@@ -382,9 +382,10 @@ def pkv_get_fused_append():
     return bool(_lib.pkv_get_fused_append())
 
 
-PKV_WORK_FIELDS = 9
+PKV_WORK_FIELDS = 10
 WORK_FIELD_NAMES = ("decode_units", "prefill_tiles", "prefix_tiles", "merge_items",
-                    "prefill_pairs", "prefix_pairs", "fused_append", "image_hits", "image_builds")
+                    "prefill_pairs", "prefix_pairs", "fused_append", "image_hits", "image_builds",
+                    "prefix_split_keys")
 
 
 def pkv_pool_last_work(pool):

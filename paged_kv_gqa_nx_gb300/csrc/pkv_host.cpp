@@ -325,6 +325,7 @@ struct pkv_pool {
     int32_t *err_dev = nullptr;
     cudaStream_t stream = nullptr;
     int device = 0;
+    int n_sm = 0;  // the device's SM count (sizes the shared-prefix pass)
 
     int64_t last_work[PKV_WORK_FIELDS] = {};  // work list of the last attend call
     std::vector<uint32_t> gen;  // write generation per (block, layer)
@@ -501,19 +502,50 @@ std::vector<Cascade> find_cascades(pkv_seq *const *seqs, int32_t M, const int32_
     return out;
 }
 
+// Keys per split of the shared-prefix pass.  Its CTAs (query tile x kv head
+// x split) each pay a fixed cost -- loading and splitting 128 query rows,
+// writing 128 partial rows -- worth about kPrefixCtaTiles 64-key tiles of
+// work, so the split count of the longest prefix is the one that minimises
+// rounds x (tiles per CTA + that cost) on the device's SMs: for 128 forks of
+// an 8192-token prefix (32 CTAs per split on 152 SMs), 4 splits of 2048 keys
+// in one round rather than 8 of 1024 in 1.7.
+constexpr int32_t kPrefixCtaTiles = 7;
+int32_t prefix_split_keys(const std::vector<Cascade> &cas, int32_t group, int32_t n_kv, int32_t n_sm) {
+    const int32_t TQ = 128 / group;
+    int64_t per_split = 0;  // CTAs per split, all runs
+    int32_t lp = 0;
+    for (const Cascade &c : cas) {
+        per_split += static_cast<int64_t>(ceil_div(c.n, TQ)) * n_kv;
+        lp = std::max(lp, c.Lp);
+    }
+    const int32_t tiles = ceil_div(lp, kKeyTile);
+    const int64_t sms = std::max(1, n_sm);
+    int32_t best_ns = 1;
+    int64_t best = -1;
+    for (int32_t ns = 1; ns <= tiles; ++ns) {
+        const int64_t rounds = (ns * per_split + sms - 1) / sms;
+        const int64_t cost = rounds * (ceil_div(tiles, ns) + kPrefixCtaTiles);
+        if (best < 0 || cost < best) {
+            best = cost;
+            best_ns = ns;
+        }
+    }
+    return ceil_div(tiles, best_ns) * kKeyTile;
+}
+
 // Work of the cascade groups: per group one virtual row (the members' queries,
 // consecutive in Q, over keys [0, Lp), non-causal) cut into tensor-core tiles
-// of split S, and per member the decode units of keys [Lp, total_k) and a
+// of split Sp, and per member the decode units of keys [Lp, total_k) and a
 // merge item whose records are the prefix splits followed by the suffix
 // splits.  Members get k0 = Lp, s0 = the prefix split count; virtual rows are
 // appended to `rows`.  Returns the member mask.
 std::vector<char> add_cascades(std::vector<RowDesc> &rows, const std::vector<Cascade> &cas,
-                               int32_t S, int32_t group, WorkList &w,
+                               int32_t S, int32_t Sp, int32_t group, WorkList &w,
                                std::vector<UnitDesc> &tail) {
     std::vector<char> member(rows.size(), 0);
     const int32_t TQ = 128 / group;
     for (const Cascade &c : cas) {
-        const int32_t n_pref = ceil_div(c.Lp, S);
+        const int32_t n_pref = ceil_div(c.Lp, Sp);
         int32_t max_suf = 0;
         for (int32_t t = 0; t < c.n; ++t) {
             const RowDesc &rd = rows[c.r0 + t];
@@ -556,7 +588,8 @@ int32_t unit_keys(const UnitDesc &u, const RowDesc &rd, int causal, int32_t S) {
 }
 
 void build_work(std::vector<RowDesc> &rows, int causal, int32_t S, int32_t head_dim,
-                int32_t group, WorkList &w, const std::vector<Cascade> &cas = {}) {
+                int32_t group, WorkList &w, const std::vector<Cascade> &cas = {},
+                int32_t prefix_split = 0) {
     std::vector<UnitDesc> tail;
     w.units.clear();
     w.tiles.clear();
@@ -565,7 +598,8 @@ void build_work(std::vector<RowDesc> &rows, int causal, int32_t S, int32_t head_
     w.pmerges.clear();
     w.n_part = 0;
     const int32_t n_real = static_cast<int32_t>(rows.size());
-    const std::vector<char> member = add_cascades(rows, cas, S, group, w, tail);
+    const std::vector<char> member =
+        add_cascades(rows, cas, S, prefix_split > 0 ? prefix_split : S, group, w, tail);
     const bool tc_shape = prefill_shape(head_dim, group);
     const int32_t TQ = tc_shape ? 128 / group : 0;
     const int32_t Sp = S * kPrefillSplitFactor;
@@ -775,7 +809,8 @@ int run_layer(pkv_seq *const *seqs, int32_t M, const int32_t *n_q, const float *
     std::vector<Cascade> cas;
     if (attend && g_cascade.load() != 0 && prefill_shape(head_dim, group))
         cas = find_cascades(seqs, M, n_q, p->bs);
-    if (attend) build_work(rows, causal, S, head_dim, group, w, cas);
+    const int32_t Sp = cas.empty() ? 0 : prefix_split_keys(cas, group, n_kv_heads, p->n_sm);
+    if (attend) build_work(rows, causal, S, head_dim, group, w, cas, Sp);
     // the decode kernels that take the append themselves: the f32 kernel for
     // groups 1, 2, 4 and the narrow-pool kernel for its shapes (head_dim 128)
     const bool fuse_shape = head_dim == 128 &&
@@ -798,7 +833,7 @@ int run_layer(pkv_seq *const *seqs, int32_t M, const int32_t *n_q, const float *
                                                static_cast<int64_t>(w.tiles.size()),
                                                static_cast<int64_t>(w.ctiles.size()),
                                                static_cast<int64_t>(w.merges.size()),
-                                               pairs, ppairs, fuse ? 1 : 0};
+                                               pairs, ppairs, fuse ? 1 : 0, 0, 0, Sp};
         std::copy(vals, vals + PKV_WORK_FIELDS, p->last_work);
     }
 
@@ -999,7 +1034,7 @@ int run_layer(pkv_seq *const *seqs, int32_t M, const int32_t *n_q, const float *
         // shared prefixes: every member query sees all Lp prefix keys
         PrefillArgs pa{Qd, Od, a.rows, dptr<PrefillTile>(p, ctiles_off),
                        static_cast<int32_t>(w.ctiles.size()), a.pm, a.pl, a.pacc, n_heads,
-                       n_kv_heads, a.group, 0, S, a.scale_log2, p->err_dev};
+                       n_kv_heads, a.group, 0, Sp, a.scale_log2, p->err_dev};
         pa.img = img;
         pa.img_tile0 = dptr<int32_t>(p, tile0_off);
         pa.img_slot = dptr<int32_t>(p, slot_off);
@@ -1205,6 +1240,7 @@ pkv_pool *pkv_pool_new(int32_t n_blocks, int32_t n_layers, int32_t kv_dim, int32
 
     p->stream = static_cast<cudaStream_t>(stream);
     cudaError_t e = cudaGetDevice(&p->device);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&p->n_sm, cudaDevAttrMultiProcessorCount, p->device);
     if (e != cudaSuccess) {
         cuda_fail(e, "cudaGetDevice");
         delete p;

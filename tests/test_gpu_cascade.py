@@ -129,7 +129,9 @@ def test_cascade_every_fork_matches_oracle(H, KV, cascade_mode):
     work = counts["work"]
     assert work["prefix_pairs"] == len(div) * Lp
     tq = 128 // (H // KV)
-    assert work["prefix_tiles"] == -(-len(div) // tq) * -(-Lp // pkv.pkv_get_split_keys())
+    sp = work["prefix_split_keys"]
+    assert sp > 0 and sp % 64 == 0 and sp <= -(-Lp // 64) * 64
+    assert work["prefix_tiles"] == -(-len(div) // tq) * -(-Lp // sp)
     assert work["decode_units"] == len(div) and work["merge_items"] == len(div)
     off, exp2, counts2, _ = _forks_then_decode(H, KV, 3000, div, cascade=False)
     assert counts2[pkv.PKV_KERNEL_PREFILL] == 0
