@@ -564,6 +564,7 @@ def measure_extra(name, args, rank):
                 "unique_kv_gbs": round(run.unique_kv_bytes / (ms_step * 1e-3) / 1e9, 2),
                 "rows_layers_per_s": round(run.T * w.n_layers / (ms_step * 1e-3), 1),
                 "kv_bytes_per_step": run.kv_bytes, "steps": steps,
+                "host_ms_per_step": round(host_s * 1e3 / steps, 4),
                 "gpu_launches": launches,
                 "kernels_ms_per_step": {k: round(v[0] / steps, 4) for k, v in kern.items() if v[1]},
                 "roofline": roofline_of(run, w, kern, steps, name, "f32", tfl)}
