@@ -297,6 +297,9 @@ class DeviceRun:
             self.inputs.append(tuple(wl.normal(shape, seed + 1000 * layer + k, dev) for k, shape in
                                      enumerate([(self.T, w.q_dim), (self.T, w.kv_dim), (self.T, w.kv_dim)])))
         self.out = torch.empty((self.T, w.q_dim), device=dev, dtype=torch.float32)
+        # device addresses, marshalled once (the binding takes raw addresses)
+        self.input_ptrs = [tuple(t.data_ptr() for t in qkv) for qkv in self.inputs]
+        self.out_ptr = self.out.data_ptr()
         # algorithmic bytes: every visible K and V row read once per row and layer
         tk = [b + n for b, n in zip(self.base_len, self.n_q)]
         self.kv_bytes_per_layer = float(sum(tk)) * w.kv_dim * self.elem * 2
@@ -350,9 +353,9 @@ class DeviceRun:
         pkv.check(pkv.pkv_ensure_append_batch(seqs, nq))
         for layer in range(w.n_layers):
             if host is None:
-                Q, K, V = self.inputs[layer]
+                Q, K, V = self.input_ptrs[layer]
                 pkv.check(pkv.pkv_attn_batch(seqs, nq, Q, K, V, w.n_heads, w.n_kv_heads,
-                                             w.head_dim, layer, 1, w.scale, self.out))
+                                             w.head_dim, layer, 1, w.scale, self.out_ptr))
             else:
                 Qh, Kh, Vh, oh = host[layer]
                 pkv.check(pkv.pkv_attn_batch_host(seqs, nq, Qh, Kh, Vh, w.n_heads,
