@@ -362,3 +362,49 @@ def test_prefill_rescales_diverge_within_a_warp(split_keys):
         return (0.1 * q + sign).reshape(a.shape).astype(np.float32)
 
     run_case(H, KV, hd, 16, [900, 300], [64, 40], seed=31, shape_data=shape)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float8_e4m3fn], ids=["bf16", "fp8"])
+def test_host_buffers_narrow_pools(dtype):
+    """Decode rows on bf16 / fp8 pools through page-locked host buffers (the
+    narrow-pool kernel reads Q and writes out in host memory, and takes the
+    fused append) equal the device-path call on an identical pool, bit for
+    bit, pool bytes included."""
+    H, KV, hd, bs = 32, 8, 128, 16
+    q_dim, kv_dim = H * hd, KV * hd
+    lens = [5, 700, 1500, 2100, 33]
+
+    def run(host):
+        g = torch.Generator().manual_seed(8)
+        pool = GpuPool(512, 1, kv_dim, bs, max_seqs=8, max_blocks=160, shuffle_seed=4, dtype=dtype)
+        try:
+            seqs = []
+            for L in lens:
+                s = pool.new_seq(L + 4)
+                pool.grow(s, L)
+                pool.write_history(s, 0, torch.randn(L, kv_dim, generator=g), torch.randn(L, kv_dim, generator=g))
+                seqs.append(s)
+            nq = [1] * len(lens)
+            T = len(lens)
+            Q, K, V = (torch.randn(T, d, generator=g) for d in (q_dim, kv_dim, kv_dim))
+            pkv.check(pkv.pkv_ensure_append_batch(seqs, nq))
+            if host:
+                out = torch.full((T, q_dim), float("nan")).pin_memory()
+                pkv.check(pkv.pkv_attn_batch_host(seqs, nq, Q.pin_memory(), K.pin_memory(), V.pin_memory(),
+                                                  H, KV, hd, 0, 1, hd ** -0.5, out))
+                out = out.cuda()
+            else:
+                out = torch.empty(T, q_dim, device="cuda")
+                pkv.check(pkv.pkv_attn_batch(seqs, nq, Q.cuda(), K.cuda(), V.cuda(), H, KV, hd, 0, 1,
+                                             hd ** -0.5, out))
+            pool.check_no_device_error()
+            torch.cuda.synchronize()
+            return out, pool.K.view(torch.uint8).clone(), pool.V.view(torch.uint8).clone()
+        finally:
+            pool.close()
+
+    oh, kh, vh = run(True)
+    od, kd, vd = run(False)
+    assert bits_equal(oh, od)
+    assert torch.equal(kh, kd) and torch.equal(vh, vd)
