@@ -672,6 +672,9 @@ def run_pkv(args):
             "n_kv_heads": w.n_kv_heads, "head_dim": w.head_dim, "n_layers": w.n_layers,
             "block_size": w.block_size, "n_blocks": w.n_blocks,
             "kv_bytes_per_step": run.kv_bytes, "split_keys": pkv.pkv_get_split_keys(),
+            # keys per decode unit on this pool (the library scales the split
+            # to the same bytes on bf16 / fp8 pools)
+            "decode_split_keys": min(65536, pkv.pkv_get_split_keys() * (4 if run.fp8 else 2 if run.bf16 else 1)),
             "parallelism": "replicas" if world > 1 else "single GPU",
             "image_cache_mb": args.image_cache_mb,
             "l2": "no flush: each step reads %.2f GB of K/V, far above the 129 MB L2" % (run.kv_bytes / 1e9),

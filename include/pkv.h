@@ -376,9 +376,11 @@ PKV_API int pkv_debug_or_error_bits(pkv_pool *pool, int32_t which, uint32_t bits
  * next device call on the pool). */
 PKV_API int pkv_pool_flush(pkv_pool *pool);
 
-/* Keys per split-K work unit of the decode kernels (default 1024, a multiple of
- * 32 in [32, 65536]).  Process-wide; every call uses the value current at the
- * call, so results stay bit-exact between calls made under one setting. */
+/* Keys per split-K work unit of the decode kernels on f32 pools (default 1024,
+ * a multiple of 32 in [32, 65536]); units on bf16 / fp8 pools take 2x / 4x as
+ * many keys (the same bytes of K/V), at most 65536.  Tensor-core prefill rows
+ * split every 16 x keys.  Process-wide; every call uses the value current at
+ * the call, so results stay bit-exact between calls made under one setting. */
 PKV_API int pkv_set_split_keys(int32_t keys);
 PKV_API int32_t pkv_get_split_keys(void);
 

@@ -587,9 +587,12 @@ int32_t unit_keys(const UnitDesc &u, const RowDesc &rd, int causal, int32_t S) {
     return std::max(0, std::min(kbeg + S, lim) - kbeg);
 }
 
+// S: keys per split-K decode unit; prefill_split: keys per split of the
+// tensor-core prefill rows (0: kPrefillSplitFactor * S); prefix_split: keys
+// per split of the shared-prefix pass (0: S).
 void build_work(std::vector<RowDesc> &rows, int causal, int32_t S, int32_t head_dim,
                 int32_t group, WorkList &w, const std::vector<Cascade> &cas = {},
-                int32_t prefix_split = 0) {
+                int32_t prefix_split = 0, int32_t prefill_split = 0) {
     std::vector<UnitDesc> tail;
     w.units.clear();
     w.tiles.clear();
@@ -602,7 +605,7 @@ void build_work(std::vector<RowDesc> &rows, int causal, int32_t S, int32_t head_
         add_cascades(rows, cas, S, prefix_split > 0 ? prefix_split : S, group, w, tail);
     const bool tc_shape = prefill_shape(head_dim, group);
     const int32_t TQ = tc_shape ? 128 / group : 0;
-    const int32_t Sp = S * kPrefillSplitFactor;
+    const int32_t Sp = prefill_split > 0 ? prefill_split : S * kPrefillSplitFactor;
     for (int32_t r = 0; r < n_real; ++r) {
         if (member[r]) continue;
         const RowDesc &rd = rows[r];
@@ -805,12 +808,17 @@ int run_layer(pkv_seq *const *seqs, int32_t M, const int32_t *n_q, const float *
 
     WorkList w;
     const int32_t S = g_split_keys.load();
+    // A decode unit covers the same bytes of K/V on every pool: S keys of f32
+    // rows, 2 S of bf16, 4 S of fp8 (so a unit's fixed work -- the query
+    // pieces, the 4-warp merge -- is amortised alike).  It depends on the
+    // pool only, so a row's split boundaries are the same in any batch.
+    const int32_t S_dec = std::min<int32_t>(65536, S * (p->fp8 ? 4 : p->bf16 ? 2 : 1));
     const int32_t group = attend ? n_heads / n_kv_heads : 0;
     std::vector<Cascade> cas;
     if (attend && g_cascade.load() != 0 && prefill_shape(head_dim, group))
         cas = find_cascades(seqs, M, n_q, p->bs);
     const int32_t Sp = cas.empty() ? 0 : prefix_split_keys(cas, group, n_kv_heads, p->n_sm);
-    if (attend) build_work(rows, causal, S, head_dim, group, w, cas, Sp);
+    if (attend) build_work(rows, causal, S_dec, head_dim, group, w, cas, Sp, S * kPrefillSplitFactor);
     // the decode kernels that take the append themselves: the f32 kernel for
     // groups 1, 2, 4 and the narrow-pool kernel for its shapes (head_dim 128)
     const bool fuse_shape = head_dim == 128 &&
@@ -982,7 +990,7 @@ int run_layer(pkv_seq *const *seqs, int32_t M, const int32_t *n_q, const float *
     a.hd = head_dim;
     a.group = n_heads / n_kv_heads;
     a.causal = causal ? 1 : 0;
-    a.split_keys = S;
+    a.split_keys = S_dec;
     a.scale_log2 = scale * 1.4426950408889634f;
     a.err = p->err_dev;
     if (fuse) {
