@@ -110,32 +110,34 @@ def measured_tf32_tflops(n=8192, reps=10):
     return _TF32_CACHE["v"]
 
 
-def tensor_peak():
-    """f32-accurate peak of the 3xTF32 prefill contraction: the measured TF32
-    rate (cuBLAS, this GPU, live) divided by the three TF32 products each f32
-    product takes.  Also returns the nominal-ratio figure (measured bf16 x
-    1.1/2.25 / 3) for context."""
-    tf32 = measured_tf32_tflops()
-    bf16, kind = measured_bf16_peak()
-    detail = {"tf32_tflops_cublas": round(tf32, 1),
-              "from_bf16_nominal_ratio": round(bf16 * (1.1 / 2.25) / 3.0, 1),
-              "bf16_source": kind}
-    detail.update(tcgen05_tf32_rates())
-    return tf32 / 3.0, detail
+def tensor_peak(kv_dtype="f32"):
+    """f32-accurate peak of the prefill contraction: the measured dense f16 /
+    bf16 tensor rate (MEASURED_PEAKS.json, cuBLAS bf16; f16 runs at the same
+    rate) divided by the f16 products each f32-accurate product takes -- three
+    (x0*y0 + x0*y1 + x1*y0) on an f32 pool, two on bf16 / fp8 pools (their K
+    and V are single f16 pieces).  The detail also carries the live cuBLAS
+    TF32 rate and the issue rates of the kernel's own instruction."""
+    f16, kind = measured_bf16_peak()
+    products = 3.0 if kv_dtype == "f32" else 2.0
+    detail = {"f16_tflops": round(f16, 1), "f16_source": kind + " (MEASURED_PEAKS.json bf16_tflops)",
+              "f16_products_per_f32_product": products,
+              "tf32_tflops_cublas": round(measured_tf32_tflops(), 1)}
+    detail.update(tcgen05_rates())
+    return f16 / products, detail
 
 
-def tcgen05_tf32_rates():
+def tcgen05_rates():
     """The issue rate of the prefill kernel's own instruction, measured by the
-    library's probe (pkv_probe_tf32_mma): tcgen05.mma kind::tf32, M = 128, A
-    in tensor memory, at N = 64 (its QK^T products) and N = 128 (its PV
+    library's probe (pkv_probe_f16_mma): tcgen05.mma kind::f16, M = 128, A in
+    tensor memory, at N = 64 (its QK^T products) and N = 128 (its PV
     products)."""
     if "probe" in _TF32_CACHE:
         return _TF32_CACHE["probe"]
     import paged_kv_gqa_nx_gb300 as pkv
     out = {}
     for n in (64, 128):
-        clk, tf = pkv.pkv_probe_tf32_mma(n, True, 4096)
-        out["tcgen05_tf32_n%d" % n] = {"clk_per_mma": round(clk, 2), "tflops": round(tf, 1)}
+        clk, tf = pkv.pkv_probe_f16_mma(n, True, 4096)
+        out["tcgen05_f16_n%d" % n] = {"clk_per_mma": round(clk, 2), "tflops": round(tf, 1)}
     _TF32_CACHE["probe"] = out
     return out
 
@@ -510,12 +512,13 @@ def roofline_of(run, w, kern, steps, workload, kv_dtype, tensor_flops_per_layer)
         pre_per_layer = pre_n / (steps * w.n_layers)
         pre_avg_s = pre_ms * 1e-3 / pre_n
         flops_per_launch = tensor_flops_per_layer / max(pre_per_layer, 1e-9)
-        tpeak, detail = tensor_peak()
+        tpeak, detail = tensor_peak(kv_dtype)
         achieved = flops_per_launch / pre_avg_s / 1e12
-        return {"bound": "tensor", "kernel": "prefill (tcgen05 3xTF32 chunked prefill)",
+        return {"bound": "tensor", "kernel": "prefill (tcgen05 kind::f16, split f32 operands)",
                 "achieved": round(achieved, 1), "peak": round(tpeak, 1),
-                "peak_source": ("measured cuBLAS TF32 dense matmul on this GPU (%.1f TFLOP/s) / 3 "
-                                "(TF32 products per f32 product)" % detail["tf32_tflops_cublas"]),
+                "peak_source": ("measured dense bf16 rate (MEASURED_PEAKS.json, %.1f TFLOP/s; f16 the same) "
+                                "/ %d f16 products per f32 product"
+                                % (detail["f16_tflops"], detail["f16_products_per_f32_product"])),
                 "peak_detail": detail,
                 "unit": "TFLOP/s", "frac": round(achieved / tpeak, 4),
                 "traffic": profiled_traffic(workload, "prefill", kv_dtype),

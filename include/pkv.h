@@ -434,8 +434,8 @@ PKV_API int pkv_profile_enable(int32_t on);
 PKV_API int pkv_profile_reset(void);
 PKV_API int pkv_profile_read(int32_t kind, double *ms, int64_t *launches);
 
-/* Measured issue rate of tcgen05.mma kind::tf32 (diagnostic for the roofline
- * of the tensor-core kernels; no counterpart on the pages).  On the current
+/* Measured issue rate of tcgen05.mma kind::tf32 (a diagnostic for the
+ * roofline of the tensor-core kernels; no counterpart on the pages).  On the current
  * device, one CTA per SM has one thread issue `iters` MMAs of M = 128, N =
  * n_cols, K = 8 back to back into one accumulator (A from tensor memory when
  * a_in_tmem != 0, else from shared memory; B from shared memory; zero
@@ -447,6 +447,13 @@ PKV_API int pkv_profile_read(int32_t kind, double *ms, int64_t *launches);
  * the MMAs ran out. */
 PKV_API int pkv_probe_tf32_mma(int32_t n_cols, int32_t a_in_tmem, int32_t iters, double *clk_per_mma,
                                double *tflops);
+
+/* The same for tcgen05.mma kind::f16 (f16 A and B, f32 accumulator), the
+ * instruction of the tensor-core prefill kernel: K = 16 per MMA, rate over
+ * 2 * 128 * n_cols * 16 flops per MMA.  Arguments, errors and side effects as
+ * pkv_probe_tf32_mma. */
+PKV_API int pkv_probe_f16_mma(int32_t n_cols, int32_t a_in_tmem, int32_t iters, double *clk_per_mma,
+                              double *tflops);
 
 /* Description of the calling thread's last failure ("" if none). */
 PKV_API const char *pkv_last_error(void);

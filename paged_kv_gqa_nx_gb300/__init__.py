@@ -120,6 +120,8 @@ _SIGS = {
     "pkv_profile_read": (_int, [_i32, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int64)]),
     "pkv_probe_tf32_mma": (_int, [_i32, _i32, _i32, ctypes.POINTER(ctypes.c_double),
                                   ctypes.POINTER(ctypes.c_double)]),
+    "pkv_probe_f16_mma": (_int, [_i32, _i32, _i32, ctypes.POINTER(ctypes.c_double),
+                                  ctypes.POINTER(ctypes.c_double)]),
     "pkv_last_error": (ctypes.c_char_p, []),
 }
 
@@ -440,6 +442,16 @@ def pkv_probe_tf32_mma(n_cols, a_in_tmem=True, iters=4096):
     tf = ctypes.c_double()
     check(_lib.pkv_probe_tf32_mma(int(n_cols), 1 if a_in_tmem else 0, int(iters), ctypes.byref(clk),
                                   ctypes.byref(tf)))
+    return clk.value, tf.value
+
+
+def pkv_probe_f16_mma(n_cols, a_in_tmem=True, iters=4096):
+    """(SM clocks per MMA, TFLOP/s) of back-to-back tcgen05.mma kind::f16,
+    M = 128, N = n_cols, K = 16 (see include/pkv.h)."""
+    clk = ctypes.c_double()
+    tf = ctypes.c_double()
+    check(_lib.pkv_probe_f16_mma(int(n_cols), 1 if a_in_tmem else 0, int(iters), ctypes.byref(clk),
+                                 ctypes.byref(tf)))
     return clk.value, tf.value
 
 

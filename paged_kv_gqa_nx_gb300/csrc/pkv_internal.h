@@ -121,18 +121,22 @@ struct PrefillArgs {
     const unsigned char *img = nullptr;
     const int32_t *img_tile0 = nullptr;
     const int32_t *img_slot = nullptr;
-    // the images' lo planes are zero (a bf16 pool: every K/V value is exact
-    // in tf32), so the products with them and their copies are skipped
+    // the images' piece-1 planes are left out (a bf16 or fp8 pool: every K/V
+    // value times the tile's power of two is an f16 value), so the products
+    // with them and their copies are skipped
     int32_t lo_zero = 0;
 };
 
 // The tensor-core kernel's operands for one (row, 64-key tile, kv head), as
-// they sit in its shared memory: K hi, K lo (K-major, 128-byte swizzle, four
-// k-blocks of 32 dims x 64 keys) and V^T hi, V^T lo (two k-blocks of 32 keys x
-// 128 dims).  f32 x = hi + lo, hi = x with the low 13 mantissa bits cleared.
+// they sit in its shared memory: K0, K1 (K-major, 128-byte swizzle, two
+// k-blocks of 64 dims x 64 keys) and V0^T, V1^T (one k-block of 64 keys x
+// 128 dims), f16; then the tile's two exponents (int32 K, V).  Each f32
+// value x of the tile is x * 2^e = x0 + x1, x0 = f16(x * 2^e), x1 = f16 of the
+// exact rest, e the tile's exponent (its largest magnitude into [2^14, 2^15)).
 constexpr int32_t kKeyTile = 64;  // keys per tensor-core tile (and per image)
-constexpr uint32_t kImagePlane = 32 * 1024;
-constexpr uint32_t kImageBytes = 4 * kImagePlane;
+constexpr uint32_t kImagePlane = 16 * 1024;
+constexpr uint32_t kImageExpOff = 4 * kImagePlane;
+constexpr uint32_t kImageBytes = 4 * kImagePlane + 128;  // a multiple of 128 bytes
 
 // One image to make: key tile kt of row `row` (all kv heads), into image
 // slot `slot` (images slot * n_kv + h).

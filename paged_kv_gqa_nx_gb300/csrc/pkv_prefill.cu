@@ -2,38 +2,48 @@
 //
 // For a row with many new tokens, Q.K^T over a tile of queries and keys is a
 // real dense contraction, so it runs on the 5th-generation tensor cores
-// (tcgen05.mma kind::tf32).  To keep f32 accuracy each f32 operand x is split
-// into a tf32 part and its exact f32 rest (x = hi + lo) and every product is
-// formed as hi*hi + hi*lo + lo*hi; the dropped lo*lo term is ~2^-20 relative.
+// (tcgen05.mma kind::f16, f32 accumulators).  To keep f32 accuracy every f32
+// operand is first multiplied by a power of two (exact) that puts its largest
+// magnitude in [2^14, 2^15), then split into two f16 pieces x = x0 + x1 (x0 =
+// x rounded to f16, x1 = the exact rest rounded to f16: 22 significant bits),
+// and every product is formed as x0*y0 + x0*y1 + x1*y0; the dropped x1*y1
+// term is ~2^-22 relative.  The powers of two: one per query row, one per
+// 64-key tile of K and one of V per kv head (the largest magnitude over the
+// tile).  The scores are scaled back exactly before the softmax.  The
+// probabilities p (below 2^8, see the lazy rescale) of a tile whose V
+// exponent is c are multiplied by 2^(C - c), where C is a per-CTA exponent
+// that only decreases and stays at most 7 + c for every tile seen, so they
+// stay below 2^15; the accumulator then holds 2^C x the output's sum, is
+// rescaled exactly when C moves, and is scaled back by 2^-C at the end.
 //
 // One CTA = one tile of 128 query rows -- (128 / G) consecutive tokens x the G
 // query heads that share kv head `kvh` -- and one key split.  16 compute
 // warps and one more warpgroup whose first warp issues the MMAs; that
-// warpgroup hands most of its registers to the compute warps (setmaxnreg),
-// which keeps the compute warps' prefetch registers from spilling.  Row m of
-// the tile is token m / G, head m % G
-// and TMEM lane m; the four compute threads that share TMEM lane m (warps w,
-// w + 4, w + 8, w + 12) each own 16 of a key tile's scores and 32 of the row's
-// output columns, and combine the row max and sum through shared memory.  The
-// compute warps arrive on an mbarrier when the operands of QK or PV are in
-// place; the issue warp waits on it, issues, and commits to the mbarrier the
-// compute warps wait on.  Key tiles are 64 positions:
-//   QK(j):  S[128 x 64]  = Q.K_j^T     A = Q hi (TMEM) / Q lo (smem), B = K_j (smem)
-//   PV(j):  D[128 x 128] = P_j.V_j     A = P hi/lo (TMEM),            B = V_j^T (smem)
-// Loop j: wait S_j -> write K_{j+1} (QK(j+1) starts) -> online softmax
+// warpgroup hands most of its registers to the compute warps (setmaxnreg).
+// Row m of the tile is token m / G, head m % G and TMEM lane m; the four
+// compute threads that share TMEM lane m (warps w, w + 4, w + 8, w + 12) each
+// own 16 of a key tile's scores and 32 of the row's output columns, and
+// combine the row max and sum through shared memory.  The compute warps
+// arrive on an mbarrier when the operands of QK or PV are in place; the issue
+// warp waits on it, issues, and commits to the mbarrier the compute warps
+// wait on.  Key tiles are 64 positions:
+//   QK(j):  S[128 x 64]  = Q.K_j^T     A = Q0 (TMEM) / Q1 (smem), B = K_j (smem)
+//   PV(j):  D[128 x 128] = P_j.V_j     A = P0 / P1 (TMEM),        B = V_j^T (smem)
+// Loop j: wait S_j -> (K_{j+1} in place: QK(j+1) starts) -> online softmax
 // (offset-causal mask: key p visible iff p <= q_pos = total_k - n_q + i) ->
-// wait PV(j-1) -> write P_j, V_j (PV(j) starts, adding into the TMEM
-// accumulator D); QK(j+1) runs during the softmax of tile j.  p is
-// relative to a reference max that moves (and D is rescaled) only when a
-// tile's max exceeds it by more than 2^8, which keeps every p below 256.
-// K/V rows for the next tiles are loaded into registers while the MMAs run.
-// Shared memory: Q lo 64 KiB, K hi/lo 64 KiB, V^T hi/lo 64 KiB.
-// TMEM (512 columns): Q hi [0,128), S [128,192), P hi [256,320), P lo
-// [320,384), D [384,512).
+// wait PV(j-1) -> write P_j (and V_j) (PV(j) starts, adding into the TMEM
+// accumulator D); QK(j+1) runs during the softmax of tile j.  p is relative
+// to a reference max that moves (and D is rescaled) only when a tile's max
+// exceeds it by more than 2^8, which keeps every p at most 256.
+// Shared memory: Q1 32 KiB, K0/K1 16 KiB each, V0^T/V1^T 16 KiB each.
+// TMEM (512 columns; two f16 per column for the A operands): Q0 [0,64),
+// S [64,128), P0 [128,160), P1 [160,192), D [256,384).
 //
-// The address functors mirror the decode kernels' (paged through the page
-// table, or contiguous), so the paged and contiguous instantiations return the
-// same bits.
+// The operands come either as images made by the split pass (paged launches)
+// or are loaded and split by the compute warps (contiguous launches); both
+// take the same tile exponents (over the tile's keys below total_k, zero
+// beyond) and the same pieces, so the paged and contiguous launches return
+// the same bits.
 #include "pkv_elem.h"
 #include "pkv_internal.h"
 #include "pkv_tcgen05.h"
@@ -49,7 +59,7 @@ constexpr int kHD = 128;
 constexpr int kKT = 64;  // keys per tile
 static_assert(kKT == kKeyTile, "one image per tile");
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColQhi = 0, kColS = 128, kColPhi = 256, kColPlo = 320, kColD = 384;
+constexpr uint32_t kColQ0 = 0, kColS = 64, kColP0 = 128, kColP1 = 160, kColD = 256;
 #ifndef PKV_PREFILL_COMPUTE_WARPS
 #define PKV_PREFILL_COMPUTE_WARPS 16
 #endif
@@ -79,6 +89,46 @@ constexpr int kDCols = kHD / kTPR;                          // output columns pe
 constexpr int kKPW = kKT / kComputeWarps;                   // K rows per warp per key tile
 static_assert(kComputeWarps == 8 || kComputeWarps == 16, "8 or 16 compute warps");
 constexpr float kRescale = 8.f;               // lazy-rescale threshold (base 2)
+constexpr int kPExp = 7;                      // C <= kPExp + c: p * 2^(C - c) < 2^(8 + kPExp)
+
+// The power of two that brings a largest magnitude m into [2^14, 2^15):
+// 14 - floor(log2 m), clamped to [-113, 126] (m = 0 or subnormal: 126).
+__device__ __forceinline__ int f16_scale_exp(float m) {
+    const int e = static_cast<int>((__float_as_uint(m) >> 23) & 255u) - 127;
+    return max(-113, min(126, 14 - e));
+}
+// 2^n, n in [-126, 127].
+__device__ __forceinline__ float pow2f(int n) { return __uint_as_float(static_cast<uint32_t>(n + 127) << 23); }
+// x * 2^n, n in [-252, 254], in two exact steps (rounded only where the
+// result is subnormal).
+__device__ __forceinline__ float mul_pow2(float x, int n) {
+    const int n1 = n / 2;
+    return (x * pow2f(n1)) * pow2f(n - n1);
+}
+// Two f32 values (already scaled into f16's range) -> their f16 pieces, packed
+// as f16 pairs (a in the low half): x0 = f16(x), x1 = f16(x - x0).
+__device__ __forceinline__ void split_f16x2(float a, float b, uint32_t &p0, uint32_t &p1) {
+    const __half2 h0 = __floats2half2_rn(a, b);
+    const float2 f0 = __half22float2(h0);
+    const __half2 h1 = __floats2half2_rn(a - f0.x, b - f0.y);
+    p0 = *reinterpret_cast<const uint32_t *>(&h0);
+    p1 = *reinterpret_cast<const uint32_t *>(&h1);
+}
+// Eight consecutive values times 2^e as one 16-byte chunk of each piece.
+__device__ __forceinline__ void split_chunk(const float (&x)[8], float sc, uint4 &c0, uint4 &c1) {
+    split_f16x2(x[0] * sc, x[1] * sc, c0.x, c1.x);
+    split_f16x2(x[2] * sc, x[3] * sc, c0.y, c1.y);
+    split_f16x2(x[4] * sc, x[5] * sc, c0.z, c1.z);
+    split_f16x2(x[6] * sc, x[7] * sc, c0.w, c1.w);
+}
+__device__ __forceinline__ float absmax4(float m, const float4 &x) {
+    return fmaxf(fmaxf(m, fmaxf(fabsf(x.x), fabsf(x.y))), fmaxf(fabsf(x.z), fabsf(x.w)));
+}
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
 
 template <class E>
 struct PagedRowsP {
@@ -148,32 +198,30 @@ struct ContigRowsP {
     __device__ __forceinline__ bool whole(int) const { return true; }
 };
 
-constexpr uint32_t kSmemQlo = 64 * 1024;  // 4 k-blocks of 128 rows
-constexpr uint32_t kSmemK = 32 * 1024;    // one of K hi / lo: 4 k-blocks of 64 rows
-constexpr uint32_t kSmemV = 32 * 1024;    // one of V^T hi / lo: 2 k-blocks of 128 rows
-constexpr size_t kSmemBytes = kSmemQlo + 2 * kSmemK + 2 * kSmemV + 1024;  // + alignment slack
-
-__device__ __forceinline__ void split4(const float4 &x, float4 &h, float4 &l) {
-    split_tf32(x.x, h.x, l.x);
-    split_tf32(x.y, h.y, l.y);
-    split_tf32(x.z, h.z, l.z);
-    split_tf32(x.w, h.w, l.w);
-}
+constexpr uint32_t kSmemQ1 = 32 * 1024;  // Q1: 2 k-blocks of 128 rows x 64 f16
+constexpr uint32_t kSmemK = 16 * 1024;   // one of K0 / K1: 2 k-blocks of 64 rows x 64 f16
+constexpr uint32_t kSmemV = 16 * 1024;   // one of V0^T / V1^T: 1 k-block of 128 rows x 64 f16
+static_assert(kSmemK == kImagePlane && kSmemV == kImagePlane, "one image plane per buffer");
+constexpr size_t kSmemBytes = kSmemQ1 + 2 * kSmemK + 2 * kSmemV + 1024;  // + alignment slack
 
 // kBulk: the K/V operands come as images (the split pass) by bulk copy;
-// otherwise the compute warps load and split them.  kLoZero (images of a bf16
-// pool): the K / V lo planes are zero, so they are neither copied nor used.
+// otherwise the compute warps load and split them.  kLoZero (images of a
+// bf16 or fp8 pool): the K / V piece-1 planes are left out -- a pool value
+// times the tile's power of two is exact in f16 unless it lies more than
+// 2^28 below the tile's largest magnitude, where it is rounded to an f16
+// subnormal (an error below 2^-38 of that magnitude) -- so they are neither
+// copied nor used.
 template <int G, class Rows, bool kBulk, bool kLoZero>
 __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs a, Rows rows_of) {
     constexpr int TQ = 128 / G;  // tokens per tile
     extern __shared__ __align__(1024) unsigned char smraw[];
     unsigned char *sm = reinterpret_cast<unsigned char *>(
         (reinterpret_cast<uintptr_t>(smraw) + 1023) & ~static_cast<uintptr_t>(1023));
-    unsigned char *Qlo = sm;
-    unsigned char *Khi = Qlo + kSmemQlo;
-    unsigned char *Klo = Khi + kSmemK;
-    unsigned char *Vhi = Klo + kSmemK;
-    unsigned char *Vlo = Vhi + kSmemV;
+    unsigned char *Q1 = sm;
+    unsigned char *K0 = Q1 + kSmemQ1;
+    unsigned char *K1 = K0 + kSmemK;
+    unsigned char *V0 = K1 + kSmemK;
+    unsigned char *V1 = V0 + kSmemV;
     // bar_qk / bar_pv: the MMAs of QK / PV completed (tcgen05.commit);
     // bar_k / bar_p: the operands of QK / PV are in place.  Register mode: the
     // compute warps stored them.  Image mode: the compute warps read S (or, the
@@ -181,7 +229,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs a, 
     __shared__ uint64_t bar_qk, bar_pv, bar_k, bar_p;
     __shared__ uint32_t tslot;
     __shared__ float red[2][kCompute];
-    static_assert(kSCols == 16 || kSCols == 32, "");
+    __shared__ float kpart[kComputeWarps], vpart[kComputeWarps];  // register mode: tile maxima
+    static_assert(kSCols == 16, "16 scores per thread");
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int ti = blockIdx.x / a.n_kv;
@@ -212,6 +261,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs a, 
     fence_after_sync();
     const uint32_t tbase = tslot;
     bool ok = true;
+    // image of key tile kt (image mode); slot_at reads the row's slot list
+    const int32_t *slots = kBulk ? a.img_slot + a.img_tile0[tile.row] : nullptr;
+    auto image = [&](int32_t slot) {
+        return a.img + (static_cast<size_t>(slot) * a.n_kv + kvh) * kImageBytes;
+    };
 
     if (warp >= kComputeWarps) {
         // the issue warpgroup: its first warp issues the MMAs, in image mode
@@ -224,28 +278,22 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs a, 
             // done, in the order the tensor core completes them: QK(kt0), then
             // QK(kt+1), PV(kt), ...  Each copy arrives with its byte count on
             // the operand barrier that the MMA warp waits on.
-            // tile kt's image slot; read a copy ahead of its use (slot_at is
-            // called only by lane 0)
-            const int32_t *slots = a.img_slot + a.img_tile0[tile.row];
             auto slot_at = [&](int kt) { return kt < kt1 ? __ldg(slots + kt) : 0; };
-            auto image = [&](int32_t slot) {
-                return a.img + (static_cast<size_t>(slot) * a.n_kv + kvh) * kImageBytes;
-            };
-            constexpr uint32_t planes = kLoZero ? 1u : 2u;  // hi (and lo) of K / V
+            constexpr uint32_t planes = kLoZero ? 1u : 2u;  // pieces 0 (and 1) of K / V
             auto copy_k = [&](int32_t slot) {
                 if (lane == 0) {
                     const unsigned char *src = image(slot);
                     mbar_expect_tx(smem_u32(&bar_k), planes * kImagePlane);
-                    bulk_g2s(smem_u32(Khi), src, kImagePlane, smem_u32(&bar_k));
-                    if constexpr (planes == 2) bulk_g2s(smem_u32(Klo), src + kImagePlane, kImagePlane, smem_u32(&bar_k));
+                    bulk_g2s(smem_u32(K0), src, kImagePlane, smem_u32(&bar_k));
+                    if constexpr (planes == 2) bulk_g2s(smem_u32(K1), src + kImagePlane, kImagePlane, smem_u32(&bar_k));
                 }
             };
             auto copy_v = [&](int32_t slot) {
                 if (lane == 0) {
                     const unsigned char *src = image(slot) + 2 * kImagePlane;
                     mbar_expect_tx(smem_u32(&bar_p), planes * kImagePlane);
-                    bulk_g2s(smem_u32(Vhi), src, kImagePlane, smem_u32(&bar_p));
-                    if constexpr (planes == 2) bulk_g2s(smem_u32(Vlo), src + kImagePlane, kImagePlane, smem_u32(&bar_p));
+                    bulk_g2s(smem_u32(V0), src, kImagePlane, smem_u32(&bar_p));
+                    if constexpr (planes == 2) bulk_g2s(smem_u32(V1), src + kImagePlane, kImagePlane, smem_u32(&bar_p));
                 }
             };
             auto wait_c = [&](uint64_t *bar, uint32_t &ph) {
@@ -292,28 +340,29 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs a, 
             }
         } else if (warp == kComputeWarps) {
         // ---------------- MMA issue warp (lane 0 issues) ----------------
-        const uint64_t dKhi = desc_sw128(smem_u32(Khi)), dKlo = desc_sw128(smem_u32(Klo));
-        const uint64_t dQlo = desc_sw128(smem_u32(Qlo));
-        const uint64_t dVhi = desc_sw128(smem_u32(Vhi)), dVlo = desc_sw128(smem_u32(Vlo));
-        const uint32_t tS = tbase + kColS, tQ = tbase + kColQhi, tD = tbase + kColD;
-        const uint32_t tPh = tbase + kColPhi, tPl = tbase + kColPlo;
-        const uint32_t idesc_s = idesc_tf32(128, kKT), idesc_o = idesc_tf32(128, kHD);
+        const uint64_t dK0 = desc_sw128(smem_u32(K0)), dK1 = desc_sw128(smem_u32(K1));
+        const uint64_t dQ1 = desc_sw128(smem_u32(Q1));
+        const uint64_t dV0 = desc_sw128(smem_u32(V0)), dV1 = desc_sw128(smem_u32(V1));
+        const uint32_t tS = tbase + kColS, tQ = tbase + kColQ0, tD = tbase + kColD;
+        const uint32_t tP0 = tbase + kColP0, tP1 = tbase + kColP1;
+        const uint32_t idesc_s = idesc_f16(128, kKT), idesc_o = idesc_f16(128, kHD);
         uint32_t ph_k = 0, ph_p = 0;
-        // one k-step of QK (8 dims) / PV (8 keys): three products of the split
-        // (products with the K / V lo planes are left out when those are zero)
+        // one k-step of QK (16 dims) / PV (16 keys): three products of the
+        // pieces (products with the K / V piece-1 planes are left out when
+        // those are zero)
         constexpr bool lo = !kLoZero;
         auto qk_step = [&](int s) {
             const uint64_t ko = ((s >> 2) * 8192u + (s & 3) * 32u) >> 4;
             const uint64_t qo = ((s >> 2) * 16384u + (s & 3) * 32u) >> 4;
-            mma_tf32_ts(tS, tQ + 8 * s, dKhi + ko, idesc_s, s > 0);
-            if constexpr (lo) mma_tf32_ts(tS, tQ + 8 * s, dKlo + ko, idesc_s, 1);
-            mma_tf32(tS, dQlo + qo, dKhi + ko, idesc_s, 1);
+            mma_f16_ts(tS, tQ + 8 * s, dK0 + ko, idesc_s, s > 0);
+            if constexpr (lo) mma_f16_ts(tS, tQ + 8 * s, dK1 + ko, idesc_s, 1);
+            mma_f16(tS, dQ1 + qo, dK0 + ko, idesc_s, 1);
         };
         auto pv_step = [&](int s, bool first) {
-            const uint64_t vo = ((s >> 2) * 16384u + (s & 3) * 32u) >> 4;
-            mma_tf32_ts(tD, tPh + 8 * s, dVhi + vo, idesc_o, !first || s > 0);
-            if constexpr (lo) mma_tf32_ts(tD, tPh + 8 * s, dVlo + vo, idesc_o, 1);
-            mma_tf32_ts(tD, tPl + 8 * s, dVhi + vo, idesc_o, 1);
+            const uint64_t vo = (s * 32u) >> 4;
+            mma_f16_ts(tD, tP0 + 8 * s, dV0 + vo, idesc_o, !first || s > 0);
+            if constexpr (lo) mma_f16_ts(tD, tP0 + 8 * s, dV1 + vo, idesc_o, 1);
+            mma_f16_ts(tD, tP1 + 8 * s, dV0 + vo, idesc_o, 1);
         };
         // the MMAs of one tile (lane 0 issues, then commits); unrolled when the
         // issue warpgroup has the registers for it (image mode)
@@ -322,10 +371,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs a, 
             if (lane == 0) {
                 if constexpr (kBulk) {
 #pragma unroll
-                    for (int s = 0; s < 16; ++s) qk_step(s);
+                    for (int s = 0; s < kHD / 16; ++s) qk_step(s);
                 } else {
 #pragma unroll 1
-                    for (int s = 0; s < 16; ++s) qk_step(s);
+                    for (int s = 0; s < kHD / 16; ++s) qk_step(s);
                 }
                 mma_commit(smem_u32(&bar_qk));
             }
@@ -336,10 +385,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs a, 
             if (lane == 0) {
                 if constexpr (kBulk) {
 #pragma unroll
-                    for (int s = 0; s < 8; ++s) pv_step(s, first);
+                    for (int s = 0; s < kKT / 16; ++s) pv_step(s, first);
                 } else {
 #pragma unroll 1
-                    for (int s = 0; s < 8; ++s) pv_step(s, first);
+                    for (int s = 0; s < kKT / 16; ++s) pv_step(s, first);
                 }
                 mma_commit(smem_u32(&bar_pv));
             }
@@ -381,51 +430,68 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs a, 
         const int q_pos = total_k - rd.n_q + qi;
         const int kend_row = valid ? (a.causal ? min(q_pos + 1, total_k) : total_k) : 1;
         const uint32_t tlane = static_cast<uint32_t>(32 * wq) << 16;
+        const int r0 = tid & 127;
 
-        // Q row (pre-scaled to base-2 units): this thread's kDCols dims, hi -> TMEM,
-        // lo -> shared memory (one k-block per 32 dims)
+        // Q row (pre-scaled to base-2 units, then by the row's power of two):
+        // this thread's kDCols dims, piece 0 -> TMEM, piece 1 -> shared memory
+        int qexp;
         {
+            static_assert(kDCols == 32, "32 dims per thread");
             const float *qrow = a.Q + static_cast<size_t>(rd.q_row0 + (valid ? qi : 0)) * (a.n_heads * kHD) +
                                 static_cast<size_t>(kvh * G + g) * kHD + kDCols * qp;
+            float x[32];
+            float mx = 0.f;
 #pragma unroll
-            for (int c = 0; c < kDCols / 32; ++c) {
-                float hv[32];
-#pragma unroll
-                for (int j4 = 0; j4 < 8; ++j4) {
-                    float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-                    if (valid) x = __ldg(reinterpret_cast<const float4 *>(qrow + 32 * c) + j4);
-                    x.x *= a.scale_log2;
-                    x.y *= a.scale_log2;
-                    x.z *= a.scale_log2;
-                    x.w *= a.scale_log2;
-                    float4 h, l;
-                    split4(x, h, l);
-                    hv[4 * j4] = h.x;
-                    hv[4 * j4 + 1] = h.y;
-                    hv[4 * j4 + 2] = h.z;
-                    hv[4 * j4 + 3] = h.w;
-                    const uint32_t kb = static_cast<uint32_t>(kDCols / 32 * qp + c);
-                    *reinterpret_cast<float4 *>(Qlo + kb * 16384u + sw128_chunk(m, j4)) = l;
-                }
-                tmem_st32(tbase + tlane + kColQhi + kDCols * qp + 32 * c, hv);
+            for (int j4 = 0; j4 < 8; ++j4) {
+                float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (valid) v = __ldg(reinterpret_cast<const float4 *>(qrow) + j4);
+                v.x *= a.scale_log2;
+                v.y *= a.scale_log2;
+                v.z *= a.scale_log2;
+                v.w *= a.scale_log2;
+                x[4 * j4] = v.x;
+                x[4 * j4 + 1] = v.y;
+                x[4 * j4 + 2] = v.z;
+                x[4 * j4 + 3] = v.w;
+                mx = absmax4(mx, v);
             }
+            red[0][tid] = mx;
+            named_sync(1, kCompute);
+            float rmax = red[0][r0];
+#pragma unroll
+            for (int k = 1; k < kTPR; ++k) rmax = fmaxf(rmax, red[0][r0 + 128 * k]);
+            qexp = f16_scale_exp(rmax);
+            const float qs = pow2f(qexp);
+            uint32_t h0[16];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                float c8[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) c8[i] = x[8 * j + i];
+                uint4 c0, c1;
+                split_chunk(c8, qs, c0, c1);
+                h0[4 * j] = c0.x;
+                h0[4 * j + 1] = c0.y;
+                h0[4 * j + 2] = c0.z;
+                h0[4 * j + 3] = c0.w;
+                // dims 32 qp + 8 j: k-block qp / 2, chunk 4 (qp % 2) + j of row m
+                *reinterpret_cast<uint4 *>(Q1 + (qp >> 1) * 16384u + sw128_chunk(m, 4 * (qp & 1) + j)) = c1;
+            }
+            tmem_st16u(tbase + tlane + kColQ0 + 16 * qp, h0);
         }
 
-        // Key rows of a tile: warp w owns keys kKPW*w .. kKPW*w + kKPW-1 of both K
-        // and V, so one page-table lookup per warp serves a tile when a block
-        // holds whole kKPW-key groups.  K: one 512-byte row per instruction,
-        // stored as 16-byte chunks of the K-major layout.  V: lane l loads dims
-        // l + 32c (c < 4) of each row (128-byte coalesced loads) and writes
-        // 16-byte runs of 4 keys into rows d = l + 32c of V^T; the 32 rows of one
-        // store fall in all 8 swizzle phases, so the store is conflict-free.
-        // Page-table lookups are issued one phase before the loads that use them.
+        // Register mode.  Key rows of a tile: warp w owns keys kKPW*w ..
+        // kKPW*w + kKPW-1 of both K and V (every key below total_k, zero
+        // beyond, as in an image).  K: lane l holds dims 4l .. 4l+3 of each
+        // row, stored as 8-byte halves of the K-major chunks.  V: lane l holds
+        // dims l + 32c (c < 4) of each row and writes 4 keys of rows
+        // d = l + 32c of V^T.
         float4 kreg[kKPW], vq[kKPW / 4][4];
         const bool k_whole = rows_of.whole(kKPW);
         auto k_pos = [&](int kt) { return kt * kKT + warp * kKPW; };
-        // row pointer of key pos (nullptr beyond the split or on a bad entry)
         using E = typename Rows::Elem;
         auto row_of = [&](int pos, int blk0, bool is_v) -> const E * {
-            if (pos >= kend) return nullptr;
+            if (pos >= total_k) return nullptr;
             int b = blk0;
             if (!k_whole) b = rows_of.block(rd.slot, pos, a.err);
             if (b < 0) return nullptr;
@@ -433,7 +499,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs a, 
         };
         auto load_k = [&](int kt, int blk0) {
             const int pos0 = k_pos(kt);
-            if (k_whole && pos0 < kend) blk0 = rows_of.checked(blk0, a.err);
+            if (k_whole && pos0 < total_k) blk0 = rows_of.checked(blk0, a.err);
 #pragma unroll
             for (int i = 0; i < kKPW; ++i) {
                 const E *kr = row_of(pos0 + i, blk0, false);
@@ -442,7 +508,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs a, 
         };
         auto load_v = [&](int kt, int blk0) {
             const int pos0 = k_pos(kt);
-            if (k_whole && pos0 < kend) blk0 = rows_of.checked(blk0, a.err);
+            if (k_whole && pos0 < total_k) blk0 = rows_of.checked(blk0, a.err);
 #pragma unroll
             for (int g4 = 0; g4 < kKPW / 4; ++g4) {
                 float v[4][4];  // [key][c]
@@ -458,31 +524,61 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs a, 
         };
         auto lookup_k = [&](int kt) {
             const int pos0 = k_pos(kt);
-            return (k_whole && pos0 < kend) ? rows_of.entry(rd.slot, pos0, a.err) : -1;
+            return (k_whole && pos0 < total_k) ? rows_of.entry(rd.slot, pos0, a.err) : -1;
         };
         auto lookup_v = lookup_k;
-        auto store_k = [&]() {
+        // the K tile's exponent: this warp's maximum, then all warps' (a
+        // barrier of the compute warps)
+        auto k_exp = [&]() {
+            float mx = 0.f;
+#pragma unroll
+            for (int i = 0; i < kKPW; ++i) mx = absmax4(mx, kreg[i]);
+            mx = warp_max(mx);
+            if (lane == 0) kpart[warp] = mx;
+            named_sync(2, kCompute);
+            float t = kpart[0];
+#pragma unroll
+            for (int w = 1; w < kComputeWarps; ++w) t = fmaxf(t, kpart[w]);
+            return f16_scale_exp(t);
+        };
+        auto store_k = [&](int kexp) {
+            const float ks = pow2f(kexp);
 #pragma unroll
             for (int i = 0; i < kKPW; ++i) {
-                float4 h, l;
-                split4(kreg[i], h, l);
-                const uint32_t off = (lane >> 3) * 8192u + sw128_chunk(warp * kKPW + i, lane & 7);
-                *reinterpret_cast<float4 *>(Khi + off) = h;
-                *reinterpret_cast<float4 *>(Klo + off) = l;
+                uint32_t a0, a1, b0, b1;
+                split_f16x2(kreg[i].x * ks, kreg[i].y * ks, a0, a1);
+                split_f16x2(kreg[i].z * ks, kreg[i].w * ks, b0, b1);
+                // dims 4 lane .. 4 lane + 3: k-block lane / 16, chunk (lane % 16) / 2, half lane % 2
+                const uint32_t off = (lane >> 4) * 8192u + sw128_chunk(warp * kKPW + i, (lane & 15) >> 1) +
+                                     8u * (lane & 1);
+                *reinterpret_cast<uint2 *>(K0 + off) = make_uint2(a0, b0);
+                *reinterpret_cast<uint2 *>(K1 + off) = make_uint2(a1, b1);
             }
         };
-        auto store_v = [&]() {
+        // this warp's part of the V tile's maximum (read after the next barrier)
+        auto v_part = [&]() {
+            float mx = 0.f;
+#pragma unroll
+            for (int g4 = 0; g4 < kKPW / 4; ++g4)
+#pragma unroll
+                for (int c = 0; c < 4; ++c) mx = absmax4(mx, vq[g4][c]);
+            mx = warp_max(mx);
+            if (lane == 0) vpart[warp] = mx;
+        };
+        auto store_v = [&](int vexp) {
+            const float vs = pow2f(vexp);
 #pragma unroll
             for (int g4 = 0; g4 < kKPW / 4; ++g4) {
                 const int key0 = warp * kKPW + 4 * g4;
-                const uint32_t kb = static_cast<uint32_t>(key0 >> 5) * 16384u;
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
-                    float4 h, l;
-                    split4(vq[g4][c], h, l);
-                    const uint32_t off = kb + sw128_chunk(lane + 32 * c, (key0 & 31) >> 2);
-                    *reinterpret_cast<float4 *>(Vhi + off) = h;
-                    *reinterpret_cast<float4 *>(Vlo + off) = l;
+                    uint32_t a0, a1, b0, b1;
+                    split_f16x2(vq[g4][c].x * vs, vq[g4][c].y * vs, a0, a1);
+                    split_f16x2(vq[g4][c].z * vs, vq[g4][c].w * vs, b0, b1);
+                    // keys key0 .. key0 + 3 of row d: chunk key0 / 8, half (key0 / 4) % 2
+                    const uint32_t off = sw128_chunk(lane + 32 * c, key0 >> 3) + 8u * ((key0 >> 2) & 1);
+                    *reinterpret_cast<uint2 *>(V0 + off) = make_uint2(a0, b0);
+                    *reinterpret_cast<uint2 *>(V1 + off) = make_uint2(a1, b1);
                 }
             }
         };
@@ -510,17 +606,26 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs a, 
         // tile's max exceeds it by more than kRescale (base-2 units); then D and
         // l are rescaled once.  The four threads of a row take the same decisions.
         float m_ref = -INFINITY, l_run = 0.f;
+        int cexp = 0;  // C: D holds 2^C x the output's sum
         uint32_t ph_qk = 0, ph_pv = 0;
 
         // prologue: K_kt0 in place (QK(kt0) may start), V_kt0 and K_kt0+1 in
         // registers, the page-table entries of K_kt0+2 and V_kt0+1 on their way.
-        // With images (kBulk) the issue thread brings K and V in: Q only.
+        // With images (kBulk) the copy warp brings K and V in: Q only, and the
+        // tile exponents are read from the images a tile ahead.
         int vblk = -1, kblk = -1;
-        if constexpr (!kBulk) {
+        int kexp_cur = 0, kexp_next = 0;
+        int2 ex_cur = make_int2(0, 0);
+        int32_t slot_next = 0;
+        if constexpr (kBulk) {
+            if (kt0 < kt1) ex_cur = __ldg(reinterpret_cast<const int2 *>(image(__ldg(slots + kt0)) + kImageExpOff));
+            if (kt0 + 1 < kt1) slot_next = __ldg(slots + kt0 + 1);
+        } else {
             load_k(kt0, lookup_k(kt0));
             vblk = lookup_v(kt0);
             load_v(kt0, vblk);
-            store_k();
+            kexp_cur = k_exp();
+            store_k(kexp_cur);
             kblk = kt0 + 1 < kt1 ? lookup_k(kt0 + 1) : -1;
         }
         arrive(&bar_k);
@@ -537,33 +642,51 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs a, 
             fence_after_sync();
             float s[kSCols];
             tmem_ldn<kSCols>(tbase + tlane + kColS + kSCols * qp, s);
+            int kexp;
             if constexpr (kBulk) {
+                kexp = ex_cur.x;
                 // S read: QK(kt+1) may overwrite it
                 if (kt + 1 < kt1) arrive(&bar_k);
-            } else if (kt + 1 < kt1) {
-                // K_{kt+1} -> smem; the issue warp starts QK(kt+1) while we do
-                // the softmax, and the K_{kt+2} loads overlap it too
-                store_k();
-                kblk = kt + 2 < kt1 ? lookup_k(kt + 2) : -1;
-                arrive(&bar_k);
+            } else {
+                kexp = kexp_cur;
+                if (kt + 1 < kt1) {
+                    // K_{kt+1} -> smem; the issue warp starts QK(kt+1) while we
+                    // do the softmax, and the K_{kt+2} loads overlap it too
+                    kexp_next = k_exp();
+                    store_k(kexp_next);
+                    kblk = kt + 2 < kt1 ? lookup_k(kt + 2) : -1;
+                    arrive(&bar_k);
+                }
+                v_part();
             }
 
-            // online softmax: this thread's kSCols scores; max and sum combined over
-            // the row's threads (tid + 128 k), in order of k
+            // scores back to base-2 units (exact), then the online softmax:
+            // this thread's kSCols scores; max and sum combined over the row's
+            // threads (tid + 128 k), in order of k
+            const int sn = -(qexp + kexp);
+            const float sa = pow2f(sn / 2), sb = pow2f(sn - sn / 2);
             const int base = kt * kKT + kSCols * qp;
             float tmax = -INFINITY;
 #pragma unroll
             for (int i = 0; i < kSCols; ++i) {
                 const bool vis = base + i < kend_row && base + i < kend;
-                s[i] = vis ? s[i] : -INFINITY;
+                s[i] = vis ? (s[i] * sa) * sb : -INFINITY;
                 tmax = fmaxf(tmax, s[i]);
             }
             red[0][tid] = tmax;
             named_sync(1, kCompute);
-            const int r0 = tid & 127;
             float row_max = red[0][r0];
 #pragma unroll
             for (int k = 1; k < kTPR; ++k) row_max = fmaxf(row_max, red[0][r0 + 128 * k]);
+            int vexp;
+            if constexpr (kBulk) {
+                vexp = ex_cur.y;
+            } else {
+                float t = vpart[0];
+#pragma unroll
+                for (int w = 1; w < kComputeWarps; ++w) t = fmaxf(t, vpart[w]);
+                vexp = f16_scale_exp(t);
+            }
             const bool rescale = m_ref != -INFINITY && row_max > m_ref + kRescale;
             const float m_use = (m_ref == -INFINITY || rescale) ? row_max : m_ref;
             float psum = 0.f;
@@ -577,6 +700,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs a, 
             float rowsum = red[1][r0];
 #pragma unroll
             for (int k = 1; k < kTPR; ++k) rowsum += red[1][r0 + 128 * k];
+            // C for this tile (the same in every thread)
+            const int c_new = kt == kt0 ? kPExp + vexp : min(cexp, kPExp + vexp);
 
             // PV(kt-1) done: D, the P columns and the V buffer are free
             if (kt > kt0) {
@@ -586,15 +711,17 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs a, 
                 fence_after_sync();
             }
             // tcgen05.ld / st are warp-collective: the whole warp takes this branch
-            // when any of its rows rescales (the others multiply by 1)
-            if (__any_sync(0xffffffffu, rescale)) {
+            // when any of its rows rescales (the others multiply by 1) or C moves
+            const bool cmove = kt > kt0 && c_new != cexp;
+            if (cmove || __any_sync(0xffffffffu, rescale)) {
                 const float f = rescale ? exp2f(m_ref - m_use) : 1.f;
+                const float fd = mul_pow2(f, c_new - cexp);
 #pragma unroll
                 for (int c = 0; c < kDCols / 32; ++c) {
                     float dv[32];
                     tmem_ld32(tbase + tlane + kColD + kDCols * qp + 32 * c, dv);
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) dv[i] *= f;
+                    for (int i = 0; i < 32; ++i) dv[i] *= fd;
                     tmem_st32(tbase + tlane + kColD + kDCols * qp + 32 * c, dv);
                     tmem_st_wait();
                 }
@@ -602,24 +729,30 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs a, 
             }
             l_run += rowsum;
             m_ref = m_use;
+            cexp = c_new;
 
-            // P_kt -> TMEM (hi, then lo), V_kt -> smem; the issue warp starts PV(kt)
+            // P_kt * 2^(C - c) -> TMEM as two f16 pieces (and V_kt -> smem);
+            // the issue warp starts PV(kt)
             {
-                // hi from a copy, then lo in place (s is dead after this)
-                float t[kSCols];
+                const int pe = cexp - vexp;  // <= kPExp
+                const float pf = pe >= -126 ? pow2f(pe) : 0.f;
+                uint32_t p0[kSCols / 2], p1[kSCols / 2];
 #pragma unroll
-                for (int i = 0; i < kSCols; ++i) t[i] = __uint_as_float(__float_as_uint(s[i]) & 0xFFFFE000u);
-                tmem_stn<kSCols>(tbase + tlane + kColPhi + kSCols * qp, t);
-#pragma unroll
-                for (int i = 0; i < kSCols; ++i) s[i] -= t[i];
-                tmem_st_wait();
-                tmem_stn<kSCols>(tbase + tlane + kColPlo + kSCols * qp, s);
+                for (int i = 0; i < kSCols / 2; ++i) split_f16x2(s[2 * i] * pf, s[2 * i + 1] * pf, p0[i], p1[i]);
+                tmem_st8u(tbase + tlane + kColP0 + (kSCols / 2) * qp, p0);
+                tmem_st8u(tbase + tlane + kColP1 + (kSCols / 2) * qp, p1);
             }
-            if constexpr (!kBulk) store_v();
+            if constexpr (!kBulk) store_v(vexp);
             arrive(&bar_p);
 
-            // registers for the next tile: V_{kt+1}
-            if constexpr (!kBulk) {
+            // the next tile: its exponents (image mode) or its rows (register mode)
+            if constexpr (kBulk) {
+                if (kt + 1 < kt1) {
+                    ex_cur = __ldg(reinterpret_cast<const int2 *>(image(slot_next) + kImageExpOff));
+                    if (kt + 2 < kt1) slot_next = __ldg(slots + kt + 2);
+                }
+            } else {
+                kexp_cur = kexp_next;
                 if (kt + 1 < kt1) {
                     load_v(kt + 1, vblk);
                     vblk = kt + 2 < kt1 ? lookup_v(kt + 2) : -1;
@@ -627,7 +760,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs a, 
                 if (kt + 2 < kt1) load_k(kt + 2, kblk);
             }
         }
-        // the last PV, then the result
+        // the last PV, then the result: D * 2^-C (exact), divided by l
         if (ok) ok = wait_one(&bar_pv, ph_pv);
         if (!ok) {
             if (tid == 0 && a.err) atomicOr(a.err, 2);
@@ -655,7 +788,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs a, 
 #pragma unroll
                     for (int i = 0; i < 32; i += 4)
                         *reinterpret_cast<float4 *>(dst + 32 * c + i) =
-                            make_float4(dv[i] * scl, dv[i + 1] * scl, dv[i + 2] * scl, dv[i + 3] * scl);
+                            make_float4(mul_pow2(dv[i], -cexp) * scl, mul_pow2(dv[i + 1], -cexp) * scl,
+                                        mul_pow2(dv[i + 2], -cexp) * scl, mul_pow2(dv[i + 3], -cexp) * scl);
                 }
             }
             if (valid) {
@@ -710,21 +844,24 @@ cudaError_t launch_prefill(const PrefillArgs &a, const Rows &r, cudaStream_t s) 
 // ----------------------------------------------------------- split pass ----
 //
 // One CTA per (row, 64-key tile, kv head): the tile's K and V rows (read once
-// through the page table, widened to f32; zero past the row's keys) go to
-// shared memory, then every 16-byte chunk of the four operand planes is split
-// (hi = low 13 mantissa bits cleared, lo = the exact rest) and written in the
-// prefill kernel's shared-memory order, chunk by chunk (coalesced).  The V
-// rows are kept 129 floats apart so that reading them transposed has no bank
-// conflicts.
+// through the page table, widened to f32, an fp8 pool's scale applied; zero
+// past the row's keys) go to shared memory, and the block finds the largest
+// magnitude of each; then every 16-byte chunk of the four planes is written in
+// the prefill kernel's shared-memory order, chunk by chunk (coalesced): eight
+// values times the tile's power of two, split into their two f16 pieces.  The
+// two tile exponents (K, V) follow the planes.  The V rows are kept 129
+// floats apart so that reading them transposed has no bank conflicts.
 constexpr int kSplitRawFloats = kKT * kHD + kKT * (kHD + 1);
 
 template <class E>
 __global__ void __launch_bounds__(256) split_kernel(SplitArgs p, PagedRowsP<E> rows_of) {
-    // bf16 values, and fp8 values times a power of two, are exact in tf32:
-    // their lo planes are zero and not written
+    // a bf16 / fp8 value times a power of two is exact in f16 (but for
+    // values more than 2^28 below the tile's largest): the piece-1 planes are
+    // not written
     constexpr bool kLoZero = !std::is_same<E, float>::value;
     const float p_scale = rows_of.a.kv_scale;
     extern __shared__ __align__(16) float raw[];
+    __shared__ float wmax[2][8];
     float *rk = raw;              // [64][128]
     float *rv = raw + kKT * kHD;  // [64][129]
     const int it = blockIdx.x / p.n_kv;
@@ -733,6 +870,7 @@ __global__ void __launch_bounds__(256) split_kernel(SplitArgs p, PagedRowsP<E> r
     const RowDesc rd = p.rows[t.row];
     const int total_k = rd.past_len + rd.n_q;
     const int key0 = t.kt * kKT;
+    float km = 0.f, vm = 0.f;
     // 256 threads x 8 passes = 64 keys x 32 float4 chunks; unrolled, so that
     // a thread's 16 row loads are in flight together
     static_assert(kKT * (kHD / 4) == 256 * 8, "one tile per 8 passes of 256 threads");
@@ -753,6 +891,8 @@ __global__ void __launch_bounds__(256) split_kernel(SplitArgs p, PagedRowsP<E> r
                 }
             }
         }
+        km = absmax4(km, kx);
+        vm = absmax4(vm, vx);
         *reinterpret_cast<float4 *>(rk + key * kHD + 4 * ch) = kx;
         float *vd = rv + key * (kHD + 1) + 4 * ch;
         vd[0] = vx.x;
@@ -760,28 +900,49 @@ __global__ void __launch_bounds__(256) split_kernel(SplitArgs p, PagedRowsP<E> r
         vd[2] = vx.z;
         vd[3] = vx.w;
     }
+    km = warp_max(km);
+    vm = warp_max(vm);
+    if ((threadIdx.x & 31) == 0) {
+        wmax[0][threadIdx.x >> 5] = km;
+        wmax[1][threadIdx.x >> 5] = vm;
+    }
     __syncthreads();
+    km = wmax[0][0];
+    vm = wmax[1][0];
+#pragma unroll
+    for (int w = 1; w < 8; ++w) {
+        km = fmaxf(km, wmax[0][w]);
+        vm = fmaxf(vm, wmax[1][w]);
+    }
+    const int kexp = f16_scale_exp(km), vexp = f16_scale_exp(vm);
+    const float ks = pow2f(kexp), vs = pow2f(vexp);
     unsigned char *out = p.img + (static_cast<size_t>(t.slot) * p.n_kv + kvh) * kImageBytes;
     for (int q = threadIdx.x; q < static_cast<int>(kImagePlane / 16); q += blockDim.x) {
-        float4 h, l;
+        uint4 c0, c1;
+        float x[8];
         {
-            // K: k-block q >> 9 (32 dims), key row (q >> 3) & 63, swizzled chunk q & 7
+            // K: k-block q >> 9 (64 dims), key row (q >> 3) & 63, swizzled chunk q & 7
             const int kb = q >> 9, r = (q >> 3) & 63, lc = (q & 7) ^ (r & 7);
-            split4(*reinterpret_cast<const float4 *>(rk + r * kHD + kb * 32 + lc * 4), h, l);
-            *reinterpret_cast<float4 *>(out + q * 16) = h;
-            if constexpr (!kLoZero) *reinterpret_cast<float4 *>(out + kImagePlane + q * 16) = l;
+            const float *src = rk + r * kHD + kb * 64 + lc * 8;
+            const float4 a0 = *reinterpret_cast<const float4 *>(src);
+            const float4 a1 = *reinterpret_cast<const float4 *>(src + 4);
+            x[0] = a0.x; x[1] = a0.y; x[2] = a0.z; x[3] = a0.w;
+            x[4] = a1.x; x[5] = a1.y; x[6] = a1.z; x[7] = a1.w;
+            split_chunk(x, ks, c0, c1);
+            *reinterpret_cast<uint4 *>(out + q * 16) = c0;
+            if constexpr (!kLoZero) *reinterpret_cast<uint4 *>(out + kImagePlane + q * 16) = c1;
         }
         {
-            // V^T: k-block q >> 10 (32 keys), dim row (q >> 3) & 127, swizzled chunk q & 7
-            const int kb = q >> 10, d = (q >> 3) & 127, lc = (q & 7) ^ (d & 7);
-            const int k0 = kb * 32 + lc * 4;
-            const float4 x = make_float4(rv[k0 * (kHD + 1) + d], rv[(k0 + 1) * (kHD + 1) + d],
-                                         rv[(k0 + 2) * (kHD + 1) + d], rv[(k0 + 3) * (kHD + 1) + d]);
-            split4(x, h, l);
-            *reinterpret_cast<float4 *>(out + 2 * kImagePlane + q * 16) = h;
-            if constexpr (!kLoZero) *reinterpret_cast<float4 *>(out + 3 * kImagePlane + q * 16) = l;
+            // V^T: dim row q >> 3, swizzled chunk q & 7 (8 keys)
+            const int d = q >> 3, k0 = ((q & 7) ^ (d & 7)) * 8;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) x[j] = rv[(k0 + j) * (kHD + 1) + d];
+            split_chunk(x, vs, c0, c1);
+            *reinterpret_cast<uint4 *>(out + 2 * kImagePlane + q * 16) = c0;
+            if constexpr (!kLoZero) *reinterpret_cast<uint4 *>(out + 3 * kImagePlane + q * 16) = c1;
         }
     }
+    if (threadIdx.x == 0) *reinterpret_cast<int2 *>(out + kImageExpOff) = make_int2(kexp, vexp);
 }
 
 template <class E>

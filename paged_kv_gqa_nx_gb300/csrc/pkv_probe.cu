@@ -1,6 +1,6 @@
-// pkv_probe.cu -- measured issue rate of the tensor-core instruction that the
-// chunked-prefill kernel is built on (tcgen05.mma kind::tf32, M = 128), for
-// the roofline of that kernel.  A diagnostic: no counterpart on the pages.
+// pkv_probe.cu -- measured issue rates of tcgen05.mma (kind::f16, which the
+// chunked-prefill kernel is built on, and kind::tf32), M = 128, for the
+// roofline of that kernel.  A diagnostic: no counterpart on the pages.
 //
 // One CTA per SM; one thread issues `iters` MMAs back to back into one TMEM
 // accumulator (zero operands: A from TMEM or shared memory, B from shared
@@ -26,9 +26,9 @@ constexpr size_t kProbeSmem = 120 * 1024;
 constexpr uint32_t kProbeCols = 512;
 constexpr uint32_t kColA = 256;                  // A in TMEM: columns 256 .. 319
 
-template <int N, bool kTS>
-__global__ void __launch_bounds__(kProbeThreads, 1) tf32_rate_kernel(int iters, unsigned long long *cycles,
-                                                                      int32_t *err) {
+template <int N, bool kTS, bool kF16>
+__global__ void __launch_bounds__(kProbeThreads, 1) mma_rate_kernel(int iters, unsigned long long *cycles,
+                                                                     int32_t *err) {
     extern __shared__ __align__(1024) unsigned char smraw[];
     unsigned char *sm = reinterpret_cast<unsigned char *>(
         (reinterpret_cast<uintptr_t>(smraw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -63,14 +63,19 @@ __global__ void __launch_bounds__(kProbeThreads, 1) tf32_rate_kernel(int iters, 
     const unsigned long long c0 = clock64();
     if (t == 0) {
         const uint64_t ad = desc_sw128(smem_u32(sm)), bd = desc_sw128(smem_u32(sm + 16384));
-        const uint32_t id = idesc_tf32(128, N);
+        const uint32_t id = kF16 ? idesc_f16(128, N) : idesc_tf32(128, N);
 #pragma unroll 1
         for (int i = 0; i < iters; i += 16) {
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
                 const uint32_t acc = (i + j) > 0 ? 1u : 0u;
-                if constexpr (kTS) mma_tf32_ts(tb, tb + kColA + 8 * (j & 7), bd, id, acc);
-                else mma_tf32(tb, ad, bd, id, acc);
+                if constexpr (kF16) {
+                    if constexpr (kTS) mma_f16_ts(tb, tb + kColA + 8 * (j & 7), bd, id, acc);
+                    else mma_f16(tb, ad, bd, id, acc);
+                } else {
+                    if constexpr (kTS) mma_tf32_ts(tb, tb + kColA + 8 * (j & 7), bd, id, acc);
+                    else mma_tf32(tb, ad, bd, id, acc);
+                }
             }
         }
         mma_commit(smem_u32(&mbar));
@@ -86,11 +91,11 @@ __global__ void __launch_bounds__(kProbeThreads, 1) tf32_rate_kernel(int iters, 
     if (warp == 0) tmem_dealloc(tb, kProbeCols);
 }
 
-template <int N, bool kTS>
+template <int N, bool kTS, bool kF16>
 cudaError_t run_probe(int nsm, int iters, unsigned long long *dc, int32_t *de, float *ms) {
     static PerDeviceOnce configured;  // the attribute is per function and device
     cudaError_t e = configured.run([&]() -> cudaError_t {
-        return cudaFuncSetAttribute(tf32_rate_kernel<N, kTS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        return cudaFuncSetAttribute(mma_rate_kernel<N, kTS, kF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     static_cast<int>(kProbeSmem));
     });
     if (e != cudaSuccess) return e;
@@ -99,11 +104,11 @@ cudaError_t run_probe(int nsm, int iters, unsigned long long *dc, int32_t *de, f
     if (e == cudaSuccess) e = cudaEventCreate(&e1);
     if (e == cudaSuccess) {
         // warm-up, then the timed launch
-        tf32_rate_kernel<N, kTS><<<nsm, kProbeThreads, kProbeSmem>>>(64, dc, de);
+        mma_rate_kernel<N, kTS, kF16><<<nsm, kProbeThreads, kProbeSmem>>>(64, dc, de);
         e = cudaGetLastError();
         if (e == cudaSuccess) e = cudaEventRecord(e0);
         if (e == cudaSuccess) {
-            tf32_rate_kernel<N, kTS><<<nsm, kProbeThreads, kProbeSmem>>>(iters, dc, de);
+            mma_rate_kernel<N, kTS, kF16><<<nsm, kProbeThreads, kProbeSmem>>>(iters, dc, de);
             e = cudaGetLastError();
         }
         if (e == cudaSuccess) e = cudaEventRecord(e1);
@@ -115,10 +120,9 @@ cudaError_t run_probe(int nsm, int iters, unsigned long long *dc, int32_t *de, f
     return e;
 }
 
-}  // namespace
-
-extern "C" int pkv_probe_tf32_mma(int32_t n_cols, int32_t a_in_tmem, int32_t iters, double *clk_per_mma,
-                                  double *tflops) {
+// Both probes: kind::tf32 (K = 8 per MMA) or kind::f16 (K = 16).
+template <bool kF16>
+int probe_mma(int32_t n_cols, int32_t a_in_tmem, int32_t iters, double *clk_per_mma, double *tflops) {
     if (!clk_per_mma || !tflops) return report_error(PKV_ERR_ARG, "NULL output pointer");
     if (n_cols != 64 && n_cols != 128 && n_cols != 256)
         return report_error(PKV_ERR_ARG, "n_cols must be 64, 128 or 256");
@@ -136,9 +140,12 @@ extern "C" int pkv_probe_tf32_mma(int32_t n_cols, int32_t a_in_tmem, int32_t ite
     float ms = 0.f;
     if (e == cudaSuccess) {
         const bool ts = a_in_tmem != 0;
-        if (n_cols == 64) e = ts ? run_probe<64, true>(nsm, iters, dc, de, &ms) : run_probe<64, false>(nsm, iters, dc, de, &ms);
-        else if (n_cols == 128) e = ts ? run_probe<128, true>(nsm, iters, dc, de, &ms) : run_probe<128, false>(nsm, iters, dc, de, &ms);
-        else e = ts ? run_probe<256, true>(nsm, iters, dc, de, &ms) : run_probe<256, false>(nsm, iters, dc, de, &ms);
+        if (n_cols == 64)
+            e = ts ? run_probe<64, true, kF16>(nsm, iters, dc, de, &ms) : run_probe<64, false, kF16>(nsm, iters, dc, de, &ms);
+        else if (n_cols == 128)
+            e = ts ? run_probe<128, true, kF16>(nsm, iters, dc, de, &ms) : run_probe<128, false, kF16>(nsm, iters, dc, de, &ms);
+        else
+            e = ts ? run_probe<256, true, kF16>(nsm, iters, dc, de, &ms) : run_probe<256, false, kF16>(nsm, iters, dc, de, &ms);
     }
     unsigned long long cyc = 0;
     int32_t he = 0;
@@ -148,7 +155,20 @@ extern "C" int pkv_probe_tf32_mma(int32_t n_cols, int32_t a_in_tmem, int32_t ite
     if (de) cudaFree(de);
     if (e != cudaSuccess) return report_error(PKV_ERR_CUDA, cudaGetErrorString(e));
     if (he) return report_error(PKV_ERR_DEVICE_TIMEOUT, "the probe's wait for its MMAs ran out");
+    const double k = kF16 ? 16.0 : 8.0;
     *clk_per_mma = static_cast<double>(cyc) / iters;
-    *tflops = 2.0 * 128.0 * n_cols * 8.0 * iters * nsm / (static_cast<double>(ms) * 1e-3) / 1e12;
+    *tflops = 2.0 * 128.0 * n_cols * k * iters * nsm / (static_cast<double>(ms) * 1e-3) / 1e12;
     return PKV_OK;
+}
+
+}  // namespace
+
+extern "C" int pkv_probe_tf32_mma(int32_t n_cols, int32_t a_in_tmem, int32_t iters, double *clk_per_mma,
+                                  double *tflops) {
+    return probe_mma<false>(n_cols, a_in_tmem, iters, clk_per_mma, tflops);
+}
+
+extern "C" int pkv_probe_f16_mma(int32_t n_cols, int32_t a_in_tmem, int32_t iters, double *clk_per_mma,
+                                 double *tflops) {
+    return probe_mma<true>(n_cols, a_in_tmem, iters, clk_per_mma, tflops);
 }

@@ -1,13 +1,16 @@
 // pkv_tcgen05.h -- inline-PTX helpers for the sm_103a tensor-core path:
-// tensor memory (TMEM) allocation, tcgen05.mma (kind::tf32), commit to an
-// mbarrier, bounded mbarrier waits, TMEM loads, and the shared-memory matrix
-// descriptors of the K-major 128-byte-swizzled operand layout.
+// tensor memory (TMEM) allocation, tcgen05.mma (kind::tf32 and kind::f16),
+// commit to an mbarrier, bounded mbarrier waits, TMEM loads and stores, and
+// the shared-memory matrix descriptors of the K-major 128-byte-swizzled
+// operand layout.
 //
-// Operand layout ("K-major, 128B swizzle"): an operand of R rows and 32 f32
-// elements (128 bytes) along K is stored row after row, 128 bytes per row;
-// inside each group of 8 rows (1024 bytes) the sixteen-byte chunk c of row r
-// sits at chunk position c ^ (r % 8).  Wider K is stored as consecutive such
-// k-blocks of R*128 bytes.  Every k-block starts on a 1024-byte boundary.
+// Operand layout ("K-major, 128B swizzle"): an operand of R rows and 128
+// bytes along K (32 f32 / tf32 or 64 f16 elements) is stored row after row,
+// 128 bytes per row; inside each group of 8 rows (1024 bytes) the
+// sixteen-byte chunk c of row r sits at chunk position c ^ (r % 8).  Wider K
+// is stored as consecutive such k-blocks of R*128 bytes.  Every k-block
+// starts on a 1024-byte boundary.  One MMA k-step reads 32 bytes of each row
+// (8 tf32 or 16 f16 elements).
 #pragma once
 
 #include <cstdint>
@@ -47,6 +50,39 @@ __host__ __device__ constexpr uint32_t idesc_tf32(uint32_t M, uint32_t N) {
            | (2u << 10)         // B format tf32
            | ((N >> 3) << 17)   // N / 8
            | ((M >> 4) << 24);  // M / 16
+}
+
+// Instruction descriptor: D f32, A and B f16, both K-major, shape M x N.
+__host__ __device__ constexpr uint32_t idesc_f16(uint32_t M, uint32_t N) {
+    return (1u << 4)            // D format f32
+           | (0u << 7)          // A format f16
+           | (0u << 10)         // B format f16
+           | ((N >> 3) << 17)   // N / 8
+           | ((M >> 4) << 24);  // M / 16
+}
+
+// D[tmem] (+)= A[smem] * B[smem]^T, one K = 16 step of f16 (32 bytes of K).
+__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                        uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// D[tmem] (+)= A[tmem] * B[smem]^T, one K = 16 step of f16: A is M rows (TMEM
+// lanes) by 8 columns starting at a_tmem, each column two f16 elements (the
+// lower K index in the low half).
+__device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                           uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
 }
 
 // D[tmem] (+)= A[smem] * B[smem]^T, one K = 8 step (32 bytes of K).
@@ -249,6 +285,22 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) 
         "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])), "r"(__float_as_uint(v[26])),
         "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])),
         "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
+        : "memory");
+}
+
+// Store 8 / 16 consecutive 32-bit columns (raw bits) of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_st8u(uint32_t taddr, const uint32_t (&v)[8]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};\n" ::"r"(taddr),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+        : "memory");
+}
+__device__ __forceinline__ void tmem_st16u(uint32_t taddr, const uint32_t (&v)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};\n" ::"r"(taddr),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+        "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
         : "memory");
 }
 

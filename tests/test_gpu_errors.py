@@ -105,3 +105,18 @@ def test_tf32_probe_reports_rates_and_checks_arguments():
     for args in ((96, 1, 256), (64, 1, 100), (64, 1, 0)):
         with pytest.raises(pkv.PkvError):
             pkv.pkv_probe_tf32_mma(*args)
+
+
+@pytest.mark.gpu
+def test_f16_probe_reports_rates_and_checks_arguments():
+    """The same for the kind::f16 probe (the prefill kernel's instruction):
+    positive clocks and rates, and bad arguments rejected."""
+    for n, ts in ((64, True), (128, True), (64, False)):
+        clk, tf = pkv.pkv_probe_f16_mma(n, ts, 256)
+        assert clk > 0 and tf > 0, (n, ts, clk, tf)
+    c64, _ = pkv.pkv_probe_f16_mma(64, True, 1024)
+    c128, _ = pkv.pkv_probe_f16_mma(128, True, 1024)
+    assert c128 >= c64 * 0.9
+    for args in ((96, 1, 256), (64, 1, 100), (64, 1, 0)):
+        with pytest.raises(pkv.PkvError):
+            pkv.pkv_probe_f16_mma(*args)
