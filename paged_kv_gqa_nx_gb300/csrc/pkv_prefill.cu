@@ -59,7 +59,9 @@ constexpr int kHD = 128;
 constexpr int kKT = 64;  // keys per tile
 static_assert(kKT == kKeyTile, "one image per tile");
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColQ0 = 0, kColS = 64, kColP0 = 128, kColP1 = 160, kColD = 256;
+// TMEM columns: Q0 [0,64), S buffers [64,192) (64 each), P buffers [192,320)
+// (buffer b: piece 0 at 192 + 64b, piece 1 32 columns on), D [384,512)
+constexpr uint32_t kColQ0 = 0, kColS = 64, kColP = 192, kColD = 384;
 #ifndef PKV_PREFILL_COMPUTE_WARPS
 #define PKV_PREFILL_COMPUTE_WARPS 16
 #endif
@@ -123,6 +125,12 @@ __device__ __forceinline__ void split_chunk(const float (&x)[8], float sc, uint4
 }
 __device__ __forceinline__ float absmax4(float m, const float4 &x) {
     return fmaxf(fmaxf(m, fmaxf(fabsf(x.x), fabsf(x.y))), fmaxf(fabsf(x.z), fabsf(x.w)));
+}
+// 2^x to about 2^-22 relative (ex2.approx; 0 for -inf and below 2^-126).
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
+    return y;
 }
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
@@ -199,10 +207,11 @@ struct ContigRowsP {
 };
 
 constexpr uint32_t kSmemQ1 = 32 * 1024;  // Q1: 2 k-blocks of 128 rows x 64 f16
-constexpr uint32_t kSmemK = 16 * 1024;   // one of K0 / K1: 2 k-blocks of 64 rows x 64 f16
-constexpr uint32_t kSmemV = 16 * 1024;   // one of V0^T / V1^T: 1 k-block of 128 rows x 64 f16
-static_assert(kSmemK == kImagePlane && kSmemV == kImagePlane, "one image plane per buffer");
-constexpr size_t kSmemBytes = kSmemQ1 + 2 * kSmemK + 2 * kSmemV + 1024;  // + alignment slack
+// one K buffer: K0, K1 (each 2 k-blocks of 64 rows x 64 f16); one V buffer:
+// V0^T, V1^T (each 1 k-block of 128 rows x 64 f16); two of each
+constexpr uint32_t kSmemKV = 2 * kImagePlane;
+static_assert(kImagePlane == 16 * 1024, "a piece of a tile is 16 KiB");
+constexpr size_t kSmemBytes = kSmemQ1 + 4 * kSmemKV + 1024;  // + alignment slack
 
 // kBulk: the K/V operands come as images (the split pass) by bulk copy;
 // otherwise the compute warps load and split them.  kLoZero (images of a
@@ -211,6 +220,22 @@ constexpr size_t kSmemBytes = kSmemQ1 + 2 * kSmemK + 2 * kSmemV + 1024;  // + al
 // 2^28 below the tile's largest magnitude, where it is rounded to an f16
 // subnormal (an error below 2^-38 of that magnitude) -- so they are neither
 // copied nor used.
+//
+// Tile j of the CTA (key tile kt0 + j) uses buffer b = j & 1 of K, V (shared
+// memory), S and P (TMEM).  Per-buffer mbarriers, phase j >> 1 for tile j:
+//   qkready[b]  QK(j)'s operands: K_j in place (copy warp's bytes; register
+//               mode: the compute warps' stores) and S_{j-2} read (compute
+//               warps; for j < 2 their arrival after writing Q instead)
+//   pvready[b]  PV(j)'s operands: P_j written (compute warps) and V_j in place
+//               (copy warp's bytes; register mode: stored with P)
+//   qkdone[b]   QK(j) complete (commit)
+//   pvdone[b]   PV(j) complete (commit)
+// One warp issues the QKs and another the PVs, each waiting once per tile: a
+// thread's mbarrier test after its own MMAs waits for them to reach the tensor
+// core, so with one issuing thread the tensor pipe drained at every wait.
+// QK(j+1) runs while the compute warps do the softmax of tile j.  No waiter
+// is ever two phases behind: each next phase needs an arrival that follows
+// the wait.
 template <int G, class Rows, bool kBulk, bool kLoZero>
 __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs a, Rows rows_of) {
     constexpr int TQ = 128 / G;  // tokens per tile
@@ -218,18 +243,13 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs a, 
     unsigned char *sm = reinterpret_cast<unsigned char *>(
         (reinterpret_cast<uintptr_t>(smraw) + 1023) & ~static_cast<uintptr_t>(1023));
     unsigned char *Q1 = sm;
-    unsigned char *K0 = Q1 + kSmemQ1;
-    unsigned char *K1 = K0 + kSmemK;
-    unsigned char *V0 = K1 + kSmemK;
-    unsigned char *V1 = V0 + kSmemV;
-    // bar_qk / bar_pv: the MMAs of QK / PV completed (tcgen05.commit);
-    // bar_k / bar_p: the operands of QK / PV are in place.  Register mode: the
-    // compute warps stored them.  Image mode: the compute warps read S (or, the
-    // first time, wrote Q) / wrote P, and the copy warp's K / V image landed.
-    __shared__ uint64_t bar_qk, bar_pv, bar_k, bar_p;
+    unsigned char *Kbuf = Q1 + kSmemQ1;    // buffer b: pieces 0, 1 at b * kSmemKV + {0, kImagePlane}
+    unsigned char *Vbuf = Kbuf + 2 * kSmemKV;
+    __shared__ uint64_t bar_qkready[2], bar_pvready[2], bar_qkdone[2], bar_pvdone[2];
     __shared__ uint32_t tslot;
     __shared__ float red[2][kCompute];
     __shared__ float kpart[kComputeWarps], vpart[kComputeWarps];  // register mode: tile maxima
+    __shared__ int s_flag;
     static_assert(kSCols == 16, "16 scores per thread");
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -244,24 +264,30 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs a, 
     const int kbeg = tile.split * a.split_keys;
     const int kend = min(kbeg + a.split_keys, kend_tile);
     const int kt0 = kbeg / kKT, kt1 = (kend + kKT - 1) / kKT;
+    const int n = kt1 - kt0;  // key tiles of this CTA
+    auto ph = [](int j) { return static_cast<uint32_t>(j >> 1) & 1u; };
 
     if (warp == 0) {
         tmem_alloc(smem_u32(&tslot), kTmemCols);
         tmem_relinquish();
     }
     if (tid == 0) {
-        mbar_init(smem_u32(&bar_qk), 1);
-        mbar_init(smem_u32(&bar_pv), 1);
-        // with images the copy warp's expect-tx arrival joins each phase
-        mbar_init(smem_u32(&bar_k), kComputeWarps + (kBulk ? 1 : 0));
-        mbar_init(smem_u32(&bar_p), kComputeWarps + (kBulk ? 1 : 0));
+        for (int b = 0; b < 2; ++b) {
+            // per phase: the compute warps' arrivals, and the copy warp's
+            // expect-tx arrival (image mode) or a second arrival of the compute
+            // warps after storing K (register mode)
+            mbar_init(smem_u32(&bar_qkready[b]), kBulk ? kComputeWarps + 1 : 2 * kComputeWarps);
+            mbar_init(smem_u32(&bar_pvready[b]), kComputeWarps + (kBulk ? 1 : 0));
+            mbar_init(smem_u32(&bar_qkdone[b]), 1);
+            mbar_init(smem_u32(&bar_pvdone[b]), 1);
+        }
     }
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
     const uint32_t tbase = tslot;
     bool ok = true;
-    // image of key tile kt (image mode); slot_at reads the row's slot list
+    // image of key tile kt (image mode)
     const int32_t *slots = kBulk ? a.img_slot + a.img_tile0[tile.row] : nullptr;
     auto image = [&](int32_t slot) {
         return a.img + (static_cast<size_t>(slot) * a.n_kv + kvh) * kImageBytes;
@@ -272,149 +298,114 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs a, 
         // its second warp runs the bulk copies; the rest only give their
         // registers back
         setmaxnreg_dec<kBulk ? kIssueRegsBulk : kIssueRegs>();
+        // lane 0 waits (bounded), the warp learns the outcome
+        auto wait_w = [&](uint64_t *bar, uint32_t parity) {
+            return __shfl_sync(0xffffffffu, lane == 0 ? mbar_wait(smem_u32(bar), parity) : true, 0) != 0;
+        };
         if (kBulk && warp == kComputeWarps + 1) {
             // ---------------- copy warp (lane 0 copies) ----------------
-            // A K / V buffer is refilled as soon as the MMAs that read it are
-            // done, in the order the tensor core completes them: QK(kt0), then
-            // QK(kt+1), PV(kt), ...  Each copy arrives with its byte count on
-            // the operand barrier that the MMA warp waits on.
-            auto slot_at = [&](int kt) { return kt < kt1 ? __ldg(slots + kt) : 0; };
+            // Buffer b is refilled with tile j + 2 as soon as the MMAs of tile
+            // j that read it are done; each copy arrives with its byte count on
+            // the barrier that the MMA warp waits on.
             constexpr uint32_t planes = kLoZero ? 1u : 2u;  // pieces 0 (and 1) of K / V
-            auto copy_k = [&](int32_t slot) {
+            auto copy = [&](unsigned char *dst, uint64_t *bar, int j, uint32_t plane0) {
                 if (lane == 0) {
-                    const unsigned char *src = image(slot);
-                    mbar_expect_tx(smem_u32(&bar_k), planes * kImagePlane);
-                    bulk_g2s(smem_u32(K0), src, kImagePlane, smem_u32(&bar_k));
-                    if constexpr (planes == 2) bulk_g2s(smem_u32(K1), src + kImagePlane, kImagePlane, smem_u32(&bar_k));
+                    const unsigned char *src = image(__ldg(slots + kt0 + j)) + plane0 * kImagePlane;
+                    mbar_expect_tx(smem_u32(bar), planes * kImagePlane);
+                    bulk_g2s(smem_u32(dst), src, kImagePlane, smem_u32(bar));
+                    if constexpr (planes == 2)
+                        bulk_g2s(smem_u32(dst + kImagePlane), src + kImagePlane, kImagePlane, smem_u32(bar));
                 }
             };
-            auto copy_v = [&](int32_t slot) {
-                if (lane == 0) {
-                    const unsigned char *src = image(slot) + 2 * kImagePlane;
-                    mbar_expect_tx(smem_u32(&bar_p), planes * kImagePlane);
-                    bulk_g2s(smem_u32(V0), src, kImagePlane, smem_u32(&bar_p));
-                    if constexpr (planes == 2) bulk_g2s(smem_u32(V1), src + kImagePlane, kImagePlane, smem_u32(&bar_p));
-                }
-            };
-            auto wait_c = [&](uint64_t *bar, uint32_t &ph) {
-                const bool w = __shfl_sync(0xffffffffu, lane == 0 ? mbar_wait(smem_u32(bar), ph) : true, 0);
-                ph ^= 1;
-                return w;
-            };
-            uint32_t ph_qkd = 0, ph_pvd = 0;
+            auto copy_k = [&](int j) { copy(Kbuf + (j & 1) * kSmemKV, &bar_qkready[j & 1], j, 0); };
+            auto copy_v = [&](int j) { copy(Vbuf + (j & 1) * kSmemKV, &bar_pvready[j & 1], j, 2); };
+            for (int j = 0; j < min(n, 2); ++j) {
+                copy_k(j);
+                copy_v(j);
+            }
             bool cok = true;
-            int32_t s_v = 0, s_k = 0;  // slots of the next V copy (kt + 1) and K copy (kt + 2)
-            if (lane == 0 && kt0 < kt1) {
-                const int32_t s0 = slot_at(kt0);
-                s_v = slot_at(kt0 + 1);
-                s_k = slot_at(kt0 + 2);
-                copy_k(s0);
-                copy_v(s0);
-            }
-            if (kt0 + 1 < kt1) {
-                cok = wait_c(&bar_qk, ph_qkd);  // QK(kt0) done
-                if (cok) copy_k(s_v);
-            }
-            for (int kt = kt0; kt + 1 < kt1 && cok; ++kt) {
-                if (kt + 2 < kt1) {
-                    cok = wait_c(&bar_qk, ph_qkd);  // QK(kt+1) done: the K buffer is free
-                    if (!cok) break;
-                    copy_k(s_k);
-                }
-                cok = wait_c(&bar_pv, ph_pvd);  // PV(kt) done: the V buffer is free
+            for (int j = 0; j + 2 < n; ++j) {
+                cok = wait_w(&bar_qkdone[j & 1], ph(j));  // QK(j) done: K buffer free
                 if (!cok) break;
-                copy_v(s_v);
-                if (lane == 0) {
-                    s_v = s_k;
-                    s_k = slot_at(kt + 3);
-                }
+                copy_k(j + 2);
+                cok = wait_w(&bar_pvdone[j & 1], ph(j));  // PV(j) done: V buffer free
+                if (!cok) break;
+                copy_v(j + 2);
             }
             // let the last copies land before the CTA's shared memory is given
-            // up (their phases also need the compute warps; bounded if those
-            // gave up)
-            if (kt0 < kt1) {
-                uint32_t last = static_cast<uint32_t>(kt1 - 1 - kt0) & 1u;
-                wait_c(&bar_k, last);
-                last = static_cast<uint32_t>(kt1 - 1 - kt0) & 1u;
-                wait_c(&bar_p, last);
+            // up (bounded if the MMA side gave up)
+            for (int j = max(0, n - 2); j < n; ++j) {
+                wait_w(&bar_qkready[j & 1], ph(j));
+                wait_w(&bar_pvready[j & 1], ph(j));
             }
-        } else if (warp == kComputeWarps) {
-        // ---------------- MMA issue warp (lane 0 issues) ----------------
-        const uint64_t dK0 = desc_sw128(smem_u32(K0)), dK1 = desc_sw128(smem_u32(K1));
+        } else if (warp == kComputeWarps || warp == kComputeWarps + 2) {
+        // ---------- MMA issue warps (lane 0 issues): QK(j) / PV(j) ----------
         const uint64_t dQ1 = desc_sw128(smem_u32(Q1));
-        const uint64_t dV0 = desc_sw128(smem_u32(V0)), dV1 = desc_sw128(smem_u32(V1));
-        const uint32_t tS = tbase + kColS, tQ = tbase + kColQ0, tD = tbase + kColD;
-        const uint32_t tP0 = tbase + kColP0, tP1 = tbase + kColP1;
+        const uint32_t tQ = tbase + kColQ0, tD = tbase + kColD;
         const uint32_t idesc_s = idesc_f16(128, kKT), idesc_o = idesc_f16(128, kHD);
-        uint32_t ph_k = 0, ph_p = 0;
         // one k-step of QK (16 dims) / PV (16 keys): three products of the
         // pieces (products with the K / V piece-1 planes are left out when
         // those are zero)
         constexpr bool lo = !kLoZero;
-        auto qk_step = [&](int s) {
+        auto qk_step = [&](int s, uint32_t tS, uint64_t dK0, uint64_t dK1) {
             const uint64_t ko = ((s >> 2) * 8192u + (s & 3) * 32u) >> 4;
             const uint64_t qo = ((s >> 2) * 16384u + (s & 3) * 32u) >> 4;
             mma_f16_ts(tS, tQ + 8 * s, dK0 + ko, idesc_s, s > 0);
             if constexpr (lo) mma_f16_ts(tS, tQ + 8 * s, dK1 + ko, idesc_s, 1);
             mma_f16(tS, dQ1 + qo, dK0 + ko, idesc_s, 1);
         };
-        auto pv_step = [&](int s, bool first) {
+        auto pv_step = [&](int s, bool first, uint32_t tP, uint64_t dV0, uint64_t dV1) {
             const uint64_t vo = (s * 32u) >> 4;
-            mma_f16_ts(tD, tP0 + 8 * s, dV0 + vo, idesc_o, !first || s > 0);
-            if constexpr (lo) mma_f16_ts(tD, tP0 + 8 * s, dV1 + vo, idesc_o, 1);
-            mma_f16_ts(tD, tP1 + 8 * s, dV0 + vo, idesc_o, 1);
+            mma_f16_ts(tD, tP + 8 * s, dV0 + vo, idesc_o, !first || s > 0);
+            if constexpr (lo) mma_f16_ts(tD, tP + 8 * s, dV1 + vo, idesc_o, 1);
+            mma_f16_ts(tD, tP + 32 + 8 * s, dV0 + vo, idesc_o, 1);
         };
         // the MMAs of one tile (lane 0 issues, then commits); unrolled when the
         // issue warpgroup has the registers for it (image mode)
-        auto mma_qk = [&]() {
+        auto mma_qk = [&](int b) {
             fence_after_sync();
             if (lane == 0) {
+                const uint32_t tS = tbase + kColS + 64u * b;
+                const uint64_t dK0 = desc_sw128(smem_u32(Kbuf + b * kSmemKV));
+                const uint64_t dK1 = desc_sw128(smem_u32(Kbuf + b * kSmemKV + kImagePlane));
                 if constexpr (kBulk) {
 #pragma unroll
-                    for (int s = 0; s < kHD / 16; ++s) qk_step(s);
+                    for (int s = 0; s < kHD / 16; ++s) qk_step(s, tS, dK0, dK1);
                 } else {
 #pragma unroll 1
-                    for (int s = 0; s < kHD / 16; ++s) qk_step(s);
+                    for (int s = 0; s < kHD / 16; ++s) qk_step(s, tS, dK0, dK1);
                 }
-                mma_commit(smem_u32(&bar_qk));
+                mma_commit(smem_u32(&bar_qkdone[b]));
             }
             __syncwarp();
         };
-        auto mma_pv = [&](bool first) {
+        auto mma_pv = [&](int b, bool first) {
             fence_after_sync();
             if (lane == 0) {
+                const uint32_t tP = tbase + kColP + 64u * b;
+                const uint64_t dV0 = desc_sw128(smem_u32(Vbuf + b * kSmemKV));
+                const uint64_t dV1 = desc_sw128(smem_u32(Vbuf + b * kSmemKV + kImagePlane));
                 if constexpr (kBulk) {
 #pragma unroll
-                    for (int s = 0; s < kKT / 16; ++s) pv_step(s, first);
+                    for (int s = 0; s < kKT / 16; ++s) pv_step(s, first, tP, dV0, dV1);
                 } else {
 #pragma unroll 1
-                    for (int s = 0; s < kKT / 16; ++s) pv_step(s, first);
+                    for (int s = 0; s < kKT / 16; ++s) pv_step(s, first, tP, dV0, dV1);
                 }
-                mma_commit(smem_u32(&bar_pv));
+                mma_commit(smem_u32(&bar_pvdone[b]));
             }
             __syncwarp();
         };
-        // lane 0 waits (bounded), the warp learns the outcome
-        auto wait1 = [&](uint64_t *bar, uint32_t &ph) {
-            const bool w = __shfl_sync(0xffffffffu, lane == 0 ? mbar_wait(smem_u32(bar), ph) : true, 0);
-            ph ^= 1;
-            return w;
-        };
-        // order on the tensor core: QK(kt0), then per tile QK(kt+1) before
-        // PV(kt), so QK(kt+1) runs while the compute warps do the softmax
-        if (kt0 < kt1) {
-            ok = wait1(&bar_k, ph_k);  // K of the tile (and, the first time, Q) in place
-            if (ok) mma_qk();
-        }
-        for (int kt = kt0; kt < kt1 && ok; ++kt) {
-            if (kt + 1 < kt1) {
-                ok = wait1(&bar_k, ph_k);
-                if (!ok) break;
-                mma_qk();
+        if (warp == kComputeWarps) {
+            for (int j = 0; j < n && ok; ++j) {
+                ok = wait_w(&bar_qkready[j & 1], ph(j));
+                if (ok) mma_qk(j & 1);
             }
-            ok = wait1(&bar_p, ph_p);  // P and V of the tile in place
-            if (!ok) break;
-            mma_pv(kt == kt0);
+        } else {
+            for (int j = 0; j < n && ok; ++j) {
+                ok = wait_w(&bar_pvready[j & 1], ph(j));
+                if (ok) mma_pv(j & 1, j == 0);
+            }
         }
         if (!ok && lane == 0 && a.err) atomicOr(a.err, 2);
         }
@@ -429,8 +420,28 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs a, 
         const bool valid = qi < rd.n_q;
         const int q_pos = total_k - rd.n_q + qi;
         const int kend_row = valid ? (a.causal ? min(q_pos + 1, total_k) : total_k) : 1;
+        const int klim = min(kend_row, kend);  // keys below klim are visible to this row
         const uint32_t tlane = static_cast<uint32_t>(32 * wq) << 16;
         const int r0 = tid & 127;
+
+        // operands written: make them visible to the tensor core, then one lane
+        // per warp arrives on the barrier the issue warp waits on
+        auto arrive = [&](uint64_t *bar) {
+            tmem_st_wait();
+            fence_proxy_async();
+            fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(bar));
+        };
+        // Wait for an MMA commit: one thread polls the mbarrier and the others
+        // wait in the named barrier, so the polling takes no shared-memory
+        // bandwidth from the tensor core's operand reads.
+        auto wait_one = [&](uint64_t *bar, uint32_t parity) {
+            bool w = true;
+            if (tid == 0) w = mbar_wait(smem_u32(bar), parity);
+            __syncwarp();
+            return named_sync_and(1, kCompute, w);
+        };
 
         // Q row (pre-scaled to base-2 units, then by the row's power of two):
         // this thread's kDCols dims, piece 0 -> TMEM, piece 1 -> shared memory
@@ -479,6 +490,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs a, 
             }
             tmem_st16u(tbase + tlane + kColQ0 + 16 * qp, h0);
         }
+        // Q written: the arrival that stands for "S_{j-2} read" of tiles 0 and 1
+        arrive(&bar_qkready[0]);
+        arrive(&bar_qkready[1]);
 
         // Register mode.  Key rows of a tile: warp w owns keys kKPW*w ..
         // kKPW*w + kKPW-1 of both K and V (every key below total_k, zero
@@ -541,7 +555,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs a, 
             for (int w = 1; w < kComputeWarps; ++w) t = fmaxf(t, kpart[w]);
             return f16_scale_exp(t);
         };
-        auto store_k = [&](int kexp) {
+        auto store_k = [&](int b, int kexp) {
+            unsigned char *K0 = Kbuf + b * kSmemKV, *K1 = K0 + kImagePlane;
             const float ks = pow2f(kexp);
 #pragma unroll
             for (int i = 0; i < kKPW; ++i) {
@@ -565,7 +580,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs a, 
             mx = warp_max(mx);
             if (lane == 0) vpart[warp] = mx;
         };
-        auto store_v = [&](int vexp) {
+        auto store_v = [&](int b, int vexp) {
+            unsigned char *V0 = Vbuf + b * kSmemKV, *V1 = V0 + kImagePlane;
             const float vs = pow2f(vexp);
 #pragma unroll
             for (int g4 = 0; g4 < kKPW / 4; ++g4) {
@@ -582,24 +598,6 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs a, 
                 }
             }
         };
-        // Wait for an MMA commit: one thread polls the mbarrier and the others
-        // wait in the named barrier, so the polling takes no shared-memory
-        // bandwidth from the tensor core's operand reads.
-        auto wait_one = [&](uint64_t *bar, uint32_t ph) {
-            bool w = true;
-            if (tid == 0) w = mbar_wait(smem_u32(bar), ph);
-            __syncwarp();
-            return named_sync_and(1, kCompute, w);
-        };
-        // operands written: make them visible to the tensor core, then one lane
-        // per warp arrives on the barrier the issue warp waits on
-        auto arrive = [&](uint64_t *bar) {
-            tmem_st_wait();
-            fence_proxy_async();
-            fence_before_sync();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(bar));
-        };
 
         // The output accumulator lives in TMEM (D) and the P.V MMAs add into it.
         // p is taken relative to a reference max m_ref that moves only when a
@@ -607,77 +605,84 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs a, 
         // l are rescaled once.  The four threads of a row take the same decisions.
         float m_ref = -INFINITY, l_run = 0.f;
         int cexp = 0;  // C: D holds 2^C x the output's sum
-        uint32_t ph_qk = 0, ph_pv = 0;
 
-        // prologue: K_kt0 in place (QK(kt0) may start), V_kt0 and K_kt0+1 in
-        // registers, the page-table entries of K_kt0+2 and V_kt0+1 on their way.
-        // With images (kBulk) the copy warp brings K and V in: Q only, and the
+        // prologue.  Register mode: K_0 in place (QK(0) may start), V_0 and
+        // K_1 in registers.  Image mode: the copy warp brings K and V in; the
         // tile exponents are read from the images a tile ahead.
         int vblk = -1, kblk = -1;
         int kexp_cur = 0, kexp_next = 0;
         int2 ex_cur = make_int2(0, 0);
         int32_t slot_next = 0;
         if constexpr (kBulk) {
-            if (kt0 < kt1) ex_cur = __ldg(reinterpret_cast<const int2 *>(image(__ldg(slots + kt0)) + kImageExpOff));
-            if (kt0 + 1 < kt1) slot_next = __ldg(slots + kt0 + 1);
+            if (n > 0) ex_cur = __ldg(reinterpret_cast<const int2 *>(image(__ldg(slots + kt0)) + kImageExpOff));
+            if (n > 1) slot_next = __ldg(slots + kt0 + 1);
         } else {
             load_k(kt0, lookup_k(kt0));
             vblk = lookup_v(kt0);
             load_v(kt0, vblk);
             kexp_cur = k_exp();
-            store_k(kexp_cur);
-            kblk = kt0 + 1 < kt1 ? lookup_k(kt0 + 1) : -1;
-        }
-        arrive(&bar_k);
-        if constexpr (!kBulk) {
-            if (kt0 + 1 < kt1) load_k(kt0 + 1, kblk);
-            vblk = kt0 + 1 < kt1 ? lookup_v(kt0 + 1) : -1;
+            store_k(0, kexp_cur);
+            kblk = n > 1 ? lookup_k(kt0 + 1) : -1;
+            arrive(&bar_qkready[0]);
+            if (n > 1) load_k(kt0 + 1, kblk);
+            vblk = n > 1 ? lookup_v(kt0 + 1) : -1;
         }
 
-        for (int kt = kt0; kt < kt1; ++kt) {
-            // S_kt ready (QK(kt) done: the K buffer is free again)
-            ok = wait_one(&bar_qk, ph_qk);
-            ph_qk ^= 1;
+        for (int j = 0; j < n; ++j) {
+            const int kt = kt0 + j, b = j & 1;
+            // S_j ready (QK(j) done; so are all earlier MMAs)
+            ok = wait_one(&bar_qkdone[b], ph(j));
             if (!ok) break;
             fence_after_sync();
             float s[kSCols];
-            tmem_ldn<kSCols>(tbase + tlane + kColS + kSCols * qp, s);
+            tmem_ldn<kSCols>(tbase + tlane + kColS + 64u * b + kSCols * qp, s);
+            if (j + 2 < n) {
+                // S buffer b may be rewritten: QK(j+2) needs this arrival
+                fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&bar_qkready[b]));
+            }
             int kexp;
             if constexpr (kBulk) {
                 kexp = ex_cur.x;
-                // S read: QK(kt+1) may overwrite it
-                if (kt + 1 < kt1) arrive(&bar_k);
             } else {
                 kexp = kexp_cur;
-                if (kt + 1 < kt1) {
-                    // K_{kt+1} -> smem; the issue warp starts QK(kt+1) while we
-                    // do the softmax, and the K_{kt+2} loads overlap it too
+                if (j + 1 < n) {
+                    // K_{j+1} -> smem (its buffer was read by QK(j-1), done);
+                    // the issue warp starts QK(j+1) while we do the softmax,
+                    // and the K_{j+2} loads overlap it too
                     kexp_next = k_exp();
-                    store_k(kexp_next);
-                    kblk = kt + 2 < kt1 ? lookup_k(kt + 2) : -1;
-                    arrive(&bar_k);
+                    store_k((j + 1) & 1, kexp_next);
+                    kblk = j + 2 < n ? lookup_k(kt + 2) : -1;
+                    arrive(&bar_qkready[(j + 1) & 1]);
                 }
                 v_part();
             }
 
-            // scores back to base-2 units (exact), then the online softmax:
-            // this thread's kSCols scores; max and sum combined over the row's
-            // threads (tid + 128 k), in order of k
+            // scores to base-2 units: one exact factor 2^sn (two steps when
+            // 2^sn is not a normal f32); mask the keys this row does not see
             const int sn = -(qexp + kexp);
-            const float sa = pow2f(sn / 2), sb = pow2f(sn - sn / 2);
+            const bool one = sn >= -126 && sn <= 127;
+            const float fsc = one ? pow2f(sn) : 1.f;
+            if (!one) {
+                const float sa = pow2f(sn / 2), sb = pow2f(sn - sn / 2);
+#pragma unroll
+                for (int i = 0; i < kSCols; ++i) s[i] = (s[i] * sa) * sb;
+            }
             const int base = kt * kKT + kSCols * qp;
+            if (base + kSCols > klim) {
+#pragma unroll
+                for (int i = 0; i < kSCols; ++i) s[i] = base + i < klim ? s[i] : -INFINITY;
+            }
             float tmax = -INFINITY;
 #pragma unroll
-            for (int i = 0; i < kSCols; ++i) {
-                const bool vis = base + i < kend_row && base + i < kend;
-                s[i] = vis ? (s[i] * sa) * sb : -INFINITY;
-                tmax = fmaxf(tmax, s[i]);
-            }
+            for (int i = 0; i < kSCols; ++i) tmax = fmaxf(tmax, s[i]);
             red[0][tid] = tmax;
             named_sync(1, kCompute);
             float row_max = red[0][r0];
 #pragma unroll
             for (int k = 1; k < kTPR; ++k) row_max = fmaxf(row_max, red[0][r0 + 128 * k]);
+            row_max *= fsc;
             int vexp;
             if constexpr (kBulk) {
                 vexp = ex_cur.y;
@@ -689,41 +694,52 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs a, 
             }
             const bool rescale = m_ref != -INFINITY && row_max > m_ref + kRescale;
             const float m_use = (m_ref == -INFINITY || rescale) ? row_max : m_ref;
+            // p = 2^(s - m_use): one FFMA (exact scaling, one rounding) and ex2
+            const float nm = m_use == -INFINITY ? 0.f : -m_use;
             float psum = 0.f;
 #pragma unroll
             for (int i = 0; i < kSCols; ++i) {
-                s[i] = (s[i] == -INFINITY) ? 0.f : exp2f(s[i] - m_use);
+                s[i] = ex2_approx(fmaf(s[i], fsc, nm));
                 psum += s[i];
             }
+            // C for this tile (the same in every thread)
+            const int c_new = j == 0 ? kPExp + vexp : min(cexp, kPExp + vexp);
+            // P / V buffer b free: PV(j-2) done (thread 0 waits before the barrier)
+            if (tid == 0) s_flag = j >= 2 ? static_cast<int>(mbar_wait(smem_u32(&bar_pvdone[b]), ph(j - 2))) : 1;
             red[1][tid] = psum;
-            named_sync(1, kCompute);
+            const bool any_rescale = named_sync_or(1, kCompute, rescale);
+            if (!s_flag) {
+                ok = false;
+                break;
+            }
+            fence_after_sync();
             float rowsum = red[1][r0];
 #pragma unroll
             for (int k = 1; k < kTPR; ++k) rowsum += red[1][r0 + 128 * k];
-            // C for this tile (the same in every thread)
-            const int c_new = kt == kt0 ? kPExp + vexp : min(cexp, kPExp + vexp);
 
-            // PV(kt-1) done: D, the P columns and the V buffer are free
-            if (kt > kt0) {
-                ok = wait_one(&bar_pv, ph_pv);
-                ph_pv ^= 1;
-                if (!ok) break;
-                fence_after_sync();
-            }
-            // tcgen05.ld / st are warp-collective: the whole warp takes this branch
-            // when any of its rows rescales (the others multiply by 1) or C moves
-            const bool cmove = kt > kt0 && c_new != cexp;
-            if (cmove || __any_sync(0xffffffffu, rescale)) {
+            // D moves (a row's reference max, or C): every PV so far done first
+            const bool cmove = j > 0 && c_new != cexp;
+            if (any_rescale || cmove) {
+                if (j >= 1) {
+                    ok = wait_one(&bar_pvdone[(j - 1) & 1], ph(j - 1));
+                    if (!ok) break;
+                    fence_after_sync();
+                }
+                // tcgen05.ld / st are warp-collective: the whole warp takes this
+                // branch when any of its rows rescales (the others multiply by 1)
+                // or C moves
                 const float f = rescale ? exp2f(m_ref - m_use) : 1.f;
-                const float fd = mul_pow2(f, c_new - cexp);
+                if (cmove || __any_sync(0xffffffffu, rescale)) {
+                    const float fd = mul_pow2(f, c_new - cexp);
 #pragma unroll
-                for (int c = 0; c < kDCols / 32; ++c) {
-                    float dv[32];
-                    tmem_ld32(tbase + tlane + kColD + kDCols * qp + 32 * c, dv);
+                    for (int c = 0; c < kDCols / 32; ++c) {
+                        float dv[32];
+                        tmem_ld32(tbase + tlane + kColD + kDCols * qp + 32 * c, dv);
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) dv[i] *= fd;
-                    tmem_st32(tbase + tlane + kColD + kDCols * qp + 32 * c, dv);
-                    tmem_st_wait();
+                        for (int i = 0; i < 32; ++i) dv[i] *= fd;
+                        tmem_st32(tbase + tlane + kColD + kDCols * qp + 32 * c, dv);
+                        tmem_st_wait();
+                    }
                 }
                 l_run *= f;
             }
@@ -731,37 +747,38 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs a, 
             m_ref = m_use;
             cexp = c_new;
 
-            // P_kt * 2^(C - c) -> TMEM as two f16 pieces (and V_kt -> smem);
-            // the issue warp starts PV(kt)
+            // P_j * 2^(C - c) -> TMEM as two f16 pieces (and V_j -> smem); the
+            // issue warp starts PV(j)
             {
                 const int pe = cexp - vexp;  // <= kPExp
                 const float pf = pe >= -126 ? pow2f(pe) : 0.f;
                 uint32_t p0[kSCols / 2], p1[kSCols / 2];
 #pragma unroll
                 for (int i = 0; i < kSCols / 2; ++i) split_f16x2(s[2 * i] * pf, s[2 * i + 1] * pf, p0[i], p1[i]);
-                tmem_st8u(tbase + tlane + kColP0 + (kSCols / 2) * qp, p0);
-                tmem_st8u(tbase + tlane + kColP1 + (kSCols / 2) * qp, p1);
+                const uint32_t tp = tbase + tlane + kColP + 64u * b + (kSCols / 2) * qp;
+                tmem_st8u(tp, p0);
+                tmem_st8u(tp + 32, p1);
             }
-            if constexpr (!kBulk) store_v(vexp);
-            arrive(&bar_p);
+            if constexpr (!kBulk) store_v(b, vexp);
+            arrive(&bar_pvready[b]);
 
             // the next tile: its exponents (image mode) or its rows (register mode)
             if constexpr (kBulk) {
-                if (kt + 1 < kt1) {
+                if (j + 1 < n) {
                     ex_cur = __ldg(reinterpret_cast<const int2 *>(image(slot_next) + kImageExpOff));
-                    if (kt + 2 < kt1) slot_next = __ldg(slots + kt + 2);
+                    if (j + 2 < n) slot_next = __ldg(slots + kt + 2);
                 }
             } else {
                 kexp_cur = kexp_next;
-                if (kt + 1 < kt1) {
+                if (j + 1 < n) {
                     load_v(kt + 1, vblk);
-                    vblk = kt + 2 < kt1 ? lookup_v(kt + 2) : -1;
+                    vblk = j + 2 < n ? lookup_v(kt + 2) : -1;
                 }
-                if (kt + 2 < kt1) load_k(kt + 2, kblk);
+                if (j + 2 < n) load_k(kt + 2, kblk);
             }
         }
         // the last PV, then the result: D * 2^-C (exact), divided by l
-        if (ok) ok = wait_one(&bar_pv, ph_pv);
+        if (ok && n > 0) ok = wait_one(&bar_pvdone[(n - 1) & 1], ph(n - 1));
         if (!ok) {
             if (tid == 0 && a.err) atomicOr(a.err, 2);
         } else {
@@ -769,15 +786,15 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs a, 
             const int h = kvh * G + g;
             const bool direct = tile.part0 < 0;
             float *dst = nullptr;
-            size_t ph = 0;
+            size_t pidx = 0;
             if (direct) {
                 dst = a.out + static_cast<size_t>(rd.q_row0 + (valid ? qi : 0)) * (a.n_heads * kHD) +
                       static_cast<size_t>(h) * kHD + kDCols * qp;
             } else {
                 const int n_split = (kend_tile + a.split_keys - 1) / a.split_keys;
                 const int stride = tile.stride > 0 ? tile.stride : n_split;
-                ph = static_cast<size_t>(tile.part0 + (valid ? tq : 0) * stride + tile.split) * a.n_heads + h;
-                dst = a.pacc + ph * kHD + kDCols * qp;
+                pidx = static_cast<size_t>(tile.part0 + (valid ? tq : 0) * stride + tile.split) * a.n_heads + h;
+                dst = a.pacc + pidx * kHD + kDCols * qp;
             }
             const float scl = direct ? 1.f / l_run : 1.f;
 #pragma unroll
@@ -794,8 +811,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs a, 
             }
             if (valid) {
                 if (!direct && qp == 0) {
-                    a.pm[ph] = m_ref;
-                    a.pl[ph] = l_run;
+                    a.pm[pidx] = m_ref;
+                    a.pl[pidx] = l_run;
                 }
             }
         }

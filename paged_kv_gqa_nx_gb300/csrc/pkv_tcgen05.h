@@ -188,7 +188,7 @@ __device__ __forceinline__ void mbar_arrive(uint32_t mbar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(mbar) : "memory");
 }
 
-// Named barrier `id` over `count` threads (a multiple of 32), and its AND-reduction form.
+// Named barrier `id` over `count` threads (a multiple of 32), and its AND- / OR-reduction forms.
 __device__ __forceinline__ void named_sync(uint32_t id, uint32_t count) {
     asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(count) : "memory");
 }
@@ -198,6 +198,19 @@ __device__ __forceinline__ bool named_sync_and(uint32_t id, uint32_t count, bool
         "{\n\t.reg .pred p, q;\n\t"
         "setp.ne.u32 p, %3, 0;\n\t"
         "bar.red.and.pred q, %1, %2, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}\n"
+        : "=r"(r)
+        : "r"(id), "r"(count), "r"(static_cast<uint32_t>(v))
+        : "memory");
+    return r != 0;
+}
+
+__device__ __forceinline__ bool named_sync_or(uint32_t id, uint32_t count, bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %3, 0;\n\t"
+        "bar.red.or.pred q, %1, %2, p;\n\t"
         "selp.u32 %0, 1, 0, q;\n\t}\n"
         : "=r"(r)
         : "r"(id), "r"(count), "r"(static_cast<uint32_t>(v))
