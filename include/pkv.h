@@ -315,13 +315,18 @@ PKV_API int pkv_attn_contiguous(const float *Q, const float *Kc, const float *Vc
  * (a further cudaMalloc would fail or break its accounting), code running
  * inside an allocator or memory-pressure callback (allocating again would
  * re-enter that allocator), and latency-critical loops where cudaMalloc /
- * cudaFree may synchronise the device.  Same arguments, same kernels and the
- * same result as pkv_attn_contiguous, but it calls no cudaMalloc, cudaFree or
- * other allocating routine: its scratch (work list and split-K partials) is one
- * static device array of PKV_NOALLOC_SCRATCH_BYTES, held by every GPU that loads
- * the library until the process exits.  The caller still passes the inputs and
- * the output.  Requests whose scratch would exceed the array are rejected with
- * PKV_ERR_CAPACITY before any work is enqueued (pkv_last_error() names the sizes).
+ * cudaFree may synchronise the device.  Same arguments, kernels and result as
+ * pkv_attn_contiguous, but it calls no cudaMalloc, cudaFree or other
+ * allocating routine: its scratch (work list, split-K partials and, for a row
+ * that takes the tensor-core kernel, the operand images of its keys, 64 KiB per
+ * 64-key tile and kv head) is one static device array of
+ * PKV_NOALLOC_SCRATCH_BYTES, held by every GPU that loads the library until the
+ * process exits.  The caller still passes the inputs and the output.  When a
+ * tensor-core row's images do not fit in the array beside the rest, the row
+ * goes to the split-K decode kernels instead (the same attention within f32
+ * rounding, not the same bits as pkv_attn_contiguous).  Requests whose scratch
+ * would still exceed the array are rejected with PKV_ERR_CAPACITY before any
+ * work is enqueued (pkv_last_error() names the sizes).
  * The first call on a device does a one-time set-up with that device current:
  * it looks up the array's device address and clears the array's error word
  * (waiting for the device to finish the clear); make that first call before

@@ -589,10 +589,11 @@ int32_t unit_keys(const UnitDesc &u, const RowDesc &rd, int causal, int32_t S) {
 
 // S: keys per split-K decode unit; prefill_split: keys per split of the
 // tensor-core prefill rows (0: kPrefillSplitFactor * S); prefix_split: keys
-// per split of the shared-prefix pass (0: S).
+// per split of the shared-prefix pass (0: S); allow_tc false: every row to the
+// split-K decode kernels.
 void build_work(std::vector<RowDesc> &rows, int causal, int32_t S, int32_t head_dim,
                 int32_t group, WorkList &w, const std::vector<Cascade> &cas = {},
-                int32_t prefix_split = 0, int32_t prefill_split = 0) {
+                int32_t prefix_split = 0, int32_t prefill_split = 0, bool allow_tc = true) {
     std::vector<UnitDesc> tail;
     w.units.clear();
     w.tiles.clear();
@@ -603,7 +604,7 @@ void build_work(std::vector<RowDesc> &rows, int causal, int32_t S, int32_t head_
     const int32_t n_real = static_cast<int32_t>(rows.size());
     const std::vector<char> member =
         add_cascades(rows, cas, S, prefix_split > 0 ? prefix_split : S, group, w, tail);
-    const bool tc_shape = prefill_shape(head_dim, group);
+    const bool tc_shape = allow_tc && prefill_shape(head_dim, group);
     const int32_t TQ = tc_shape ? 128 / group : 0;
     const int32_t Sp = prefill_split > 0 ? prefill_split : S * kPrefillSplitFactor;
     for (int32_t r = 0; r < n_real; ++r) {
@@ -1663,14 +1664,30 @@ int pkv_attn_contiguous(const float *Q, const float *Kc, const float *Vc, int32_
     WorkList w;
     const int32_t S = g_split_keys.load();
     build_work(rows, causal, S, head_dim, n_heads / n_kv_heads, w);
+    // the tensor-core tiles' operand images: every 64-key tile of the row
+    std::vector<SplitItem> items;
+    std::vector<int32_t> img_tile0, img_slot;
+    if (!w.tiles.empty()) {
+        const int32_t nt = ceil_div(total_k, kKeyTile);
+        img_tile0.push_back(0);
+        for (int32_t kt = 0; kt < nt; ++kt) {
+            img_slot.push_back(kt);
+            items.push_back({0, kt, kt});
+        }
+    }
     Blob blob;
     const size_t rows_off = blob.put(rows.data(), 1);
     const size_t units_off = blob.put(w.units.data(), w.units.size());
     const size_t tiles_off = blob.put(w.tiles.data(), w.tiles.size());
     const size_t merges_off = blob.put(w.merges.data(), w.merges.size());
+    const size_t items_off = blob.put(items.data(), items.size());
+    const size_t tile0_off = blob.put(img_tile0.data(), img_tile0.size());
+    const size_t slot_off = blob.put(img_slot.data(), img_slot.size());
     const size_t desc_bytes = (blob.size() + 255) & ~static_cast<size_t>(255);
     const size_t pf = static_cast<size_t>(w.n_part) * n_heads;
-    const size_t total = desc_bytes + pf * (2 + head_dim) * sizeof(float);
+    const size_t part_bytes = (pf * (2 + head_dim) * sizeof(float) + 255) & ~static_cast<size_t>(255);
+    const size_t img_bytes = img_slot.size() * static_cast<size_t>(n_kv_heads) * kImageBytes;
+    const size_t total = desc_bytes + part_bytes + img_bytes;
 
     std::lock_guard<std::mutex> lk(g_contig_mu);
     int32_t *err_word = nullptr;
@@ -1710,11 +1727,19 @@ int pkv_attn_contiguous(const float *Q, const float *Kc, const float *Vc, int32_
     }
     const ContigAddr addr{Kc, Vc, n_kv_heads * head_dim};
     if (!w.tiles.empty()) {
-        const PrefillArgs pa{Q, out, a.rows, reinterpret_cast<const PrefillTile *>(base + tiles_off),
-                             static_cast<int32_t>(w.tiles.size()), a.pm, a.pl, a.pacc, n_heads,
-                             n_kv_heads, a.group, a.causal, S * kPrefillSplitFactor, a.scale_log2,
-                             a.err};
-        e = launch(PKV_KERNEL_PREFILL, st, [&] { return launch_prefill_contig(pa, addr, st); });
+        unsigned char *img = base + desc_bytes + part_bytes;
+        const SplitArgs sa{a.rows, reinterpret_cast<const SplitItem *>(base + items_off),
+                           static_cast<int32_t>(items.size()), n_kv_heads, img, a.err};
+        e = launch(PKV_KERNEL_SPLIT, st, [&] { return launch_split_contig(sa, addr, st); });
+        PrefillArgs pa{Q, out, a.rows, reinterpret_cast<const PrefillTile *>(base + tiles_off),
+                       static_cast<int32_t>(w.tiles.size()), a.pm, a.pl, a.pacc, n_heads,
+                       n_kv_heads, a.group, a.causal, S * kPrefillSplitFactor, a.scale_log2,
+                       a.err};
+        pa.img = img;
+        pa.img_tile0 = reinterpret_cast<const int32_t *>(base + tile0_off);
+        pa.img_slot = reinterpret_cast<const int32_t *>(base + slot_off);
+        if (e == cudaSuccess)
+            e = launch(PKV_KERNEL_PREFILL, st, [&] { return launch_prefill_contig(pa, addr, st); });
     }
     if (e == cudaSuccess && !w.units.empty())
         e = launch(PKV_KERNEL_DECODE, st, [&] { return launch_decode_contig(a, addr, st); });
@@ -1863,10 +1888,10 @@ namespace pkv {
 void build_contig_work(int32_t n_q, int32_t total_k, int32_t causal, int32_t split_keys,
                        int32_t head_dim, int32_t group, std::vector<UnitDesc> &units,
                        std::vector<PrefillTile> &tiles, std::vector<MergeDesc> &merges,
-                       int64_t *n_part) {
+                       int64_t *n_part, bool allow_tc) {
     WorkList w;
     std::vector<RowDesc> rows{{0, total_k - n_q, n_q, 0}};
-    build_work(rows, causal, split_keys, head_dim, group, w);
+    build_work(rows, causal, split_keys, head_dim, group, w, {}, 0, 0, allow_tc);
     units.swap(w.units);
     tiles.swap(w.tiles);
     merges.swap(w.merges);

@@ -220,11 +220,14 @@ __host__ __device__ constexpr bool decode_mma_shape(int head_dim, int group, boo
             (!fp8 && bf16 && (group == 1 || group == 2 || group == 4)));
 }
 cudaError_t launch_merge(const MergeArgs &a, cudaStream_t s);
-// Tensor-core prefill (pkv_prefill.cu): head_dim 128, group 1, 2, 4 or 8.
+// Tensor-core prefill (pkv_prefill.cu): head_dim 128, group 1, 2, 4 or 8; its
+// K/V operands are the images in PrefillArgs::img (made by the split pass).
 cudaError_t launch_prefill_paged(const PrefillArgs &a, const PagedAddr &addr, cudaStream_t s);
-// The split pass of the paged tensor-core launches: one image per item and kv head.
-cudaError_t launch_split_paged(const SplitArgs &a, const PagedAddr &addr, cudaStream_t s);
 cudaError_t launch_prefill_contig(const PrefillArgs &a, const ContigAddr &addr, cudaStream_t s);
+// The split pass of the tensor-core launches: one image per item and kv head,
+// from the pool's rows or from a contiguous K/V pair.
+cudaError_t launch_split_paged(const SplitArgs &a, const PagedAddr &addr, cudaStream_t s);
+cudaError_t launch_split_contig(const SplitArgs &a, const ContigAddr &addr, cudaStream_t s);
 
 // Rows with at least this many queries take the tensor-core prefill kernel
 // (when head_dim is 128 and the group is 1, 2, 4 or 8); its key split is
@@ -237,13 +240,14 @@ __host__ __device__ constexpr bool prefill_shape(int head_dim, int group) {
 
 // Host-core helpers for entry points defined in other translation units
 // (pkv_host.cpp).  build_contig_work: the split-K work list of one contiguous
-// row, as pkv_attn_contiguous builds it.  launch_counted: enqueue fn(ctx) with
+// row, as pkv_attn_contiguous builds it (allow_tc false: no tensor-core
+// tiles, every query to the split-K decode kernels).  launch_counted: enqueue fn(ctx) with
 // the library's launch accounting and optional event timing.  report_error:
 // record the calling thread's last error message and return code.
 void build_contig_work(int32_t n_q, int32_t total_k, int32_t causal, int32_t split_keys,
                        int32_t head_dim, int32_t group, std::vector<UnitDesc> &units,
                        std::vector<PrefillTile> &tiles, std::vector<MergeDesc> &merges,
-                       int64_t *n_part);
+                       int64_t *n_part, bool allow_tc = true);
 cudaError_t launch_counted(int kind, cudaStream_t s, cudaError_t (*fn)(void *), void *ctx);
 int32_t current_split_keys();
 int report_error(int code, const char *msg);

@@ -9,7 +9,9 @@
 // and latency-critical loops where cudaMalloc / cudaFree may synchronise the
 // device.  pkv_attn_contiguous_noalloc serves them: the same kernels, with the
 // scratch in one file-scope device array that every GPU loading the library
-// holds until the process exits.
+// holds until the process exits.  A row of 32 or more queries takes the
+// tensor-core kernel when its operand images (64 KiB per 64-key tile and kv
+// head) fit in the array beside the rest, else the split-K decode kernels.
 //
 // The array's name is a host-side stand-in in host code, not a device
 // address, so the entry point looks the address up once per device with
@@ -58,6 +60,15 @@ struct PrefillCtx {
 cudaError_t run_prefill(void *p) {
     auto *c = static_cast<PrefillCtx *>(p);
     return launch_prefill_contig(*c->a, *c->addr, c->s);
+}
+struct SplitCtx {
+    const SplitArgs *a;
+    const ContigAddr *addr;
+    cudaStream_t s;
+};
+cudaError_t run_split(void *p) {
+    auto *c = static_cast<SplitCtx *>(p);
+    return launch_split_contig(*c->a, *c->addr, c->s);
 }
 struct MergeCtx {
     const MergeArgs *m;
@@ -123,23 +134,47 @@ extern "C" int pkv_attn_contiguous_noalloc(const float *Q, const float *Kc, cons
         return err_arg(PKV_ERR_ARG, "device pointers must be 16-byte aligned (4-byte if head_dim % 4 != 0)");
 
     // work list and the scratch layout:
-    // [error word][rows][units][tiles][merges][partials]
+    // [error word][rows][units][tiles][merges][items][image lists][partials][images]
     const int32_t S = current_split_keys();
     std::vector<UnitDesc> units;
     std::vector<PrefillTile> tiles;
     std::vector<MergeDesc> merges;
+    std::vector<SplitItem> items;
+    std::vector<int32_t> img_tile0, img_slot;
     int64_t n_part = 0;
-    build_contig_work(n_q, total_k, causal, S, head_dim, n_heads / n_kv_heads, units, tiles,
-                      merges, &n_part);
     const RowDesc row{0, total_k - n_q, n_q, 0};
-    const size_t rows_off = 256;
-    const size_t units_off = round256(rows_off + sizeof(RowDesc));
-    const size_t tiles_off = round256(units_off + units.size() * sizeof(UnitDesc));
-    const size_t merges_off = round256(tiles_off + tiles.size() * sizeof(PrefillTile));
-    const size_t desc_end = round256(merges_off + merges.size() * sizeof(MergeDesc));
-    const size_t part_off = desc_end;
-    const size_t pf = static_cast<size_t>(n_part) * n_heads;
-    const size_t total = part_off + pf * (2 + static_cast<size_t>(head_dim)) * sizeof(float);
+    size_t rows_off = 0, units_off = 0, tiles_off = 0, merges_off = 0, items_off = 0, tile0_off = 0,
+           slot_off = 0, desc_end = 0, part_off = 0, img_off = 0, pf = 0, total = 0;
+    auto lay_out = [&](bool allow_tc) {
+        build_contig_work(n_q, total_k, causal, S, head_dim, n_heads / n_kv_heads, units, tiles, merges,
+                          &n_part, allow_tc);
+        items.clear();
+        img_tile0.clear();
+        img_slot.clear();
+        if (!tiles.empty()) {
+            // the tensor-core tiles' operand images: every 64-key tile of the row
+            const int32_t nt = (total_k + kKeyTile - 1) / kKeyTile;
+            img_tile0.push_back(0);
+            for (int32_t kt = 0; kt < nt; ++kt) {
+                img_slot.push_back(kt);
+                items.push_back({0, kt, kt});
+            }
+        }
+        rows_off = 256;
+        units_off = round256(rows_off + sizeof(RowDesc));
+        tiles_off = round256(units_off + units.size() * sizeof(UnitDesc));
+        merges_off = round256(tiles_off + tiles.size() * sizeof(PrefillTile));
+        items_off = round256(merges_off + merges.size() * sizeof(MergeDesc));
+        tile0_off = round256(items_off + items.size() * sizeof(SplitItem));
+        slot_off = round256(tile0_off + img_tile0.size() * sizeof(int32_t));
+        desc_end = round256(slot_off + img_slot.size() * sizeof(int32_t));
+        part_off = desc_end;
+        pf = static_cast<size_t>(n_part) * n_heads;
+        img_off = round256(part_off + pf * (2 + static_cast<size_t>(head_dim)) * sizeof(float));
+        total = img_off + img_slot.size() * static_cast<size_t>(n_kv_heads) * kImageBytes;
+    };
+    lay_out(true);
+    if (total > kScratchBytes && !tiles.empty()) lay_out(false);  // the images do not fit
     if (total > kScratchBytes) {
         char msg[256];
         snprintf(msg, sizeof msg,
@@ -174,6 +209,11 @@ extern "C" int pkv_attn_contiguous_noalloc(const float *Q, const float *Kc, cons
         std::memcpy(blob.data() + (tiles_off - rows_off), tiles.data(), tiles.size() * sizeof(PrefillTile));
     if (!merges.empty())
         std::memcpy(blob.data() + (merges_off - rows_off), merges.data(), merges.size() * sizeof(MergeDesc));
+    if (!items.empty()) {
+        std::memcpy(blob.data() + (items_off - rows_off), items.data(), items.size() * sizeof(SplitItem));
+        std::memcpy(blob.data() + (tile0_off - rows_off), img_tile0.data(), img_tile0.size() * sizeof(int32_t));
+        std::memcpy(blob.data() + (slot_off - rows_off), img_slot.data(), img_slot.size() * sizeof(int32_t));
+    }
     e = cudaMemcpyAsync(base + rows_off, blob.data(), blob.size(), cudaMemcpyHostToDevice, st);
     if (e != cudaSuccess) return err_arg(PKV_ERR_CUDA, cudaGetErrorString(e));
 
@@ -199,12 +239,19 @@ extern "C" int pkv_attn_contiguous_noalloc(const float *Q, const float *Kc, cons
     }
     const ContigAddr addr{Kc, Vc, n_kv_heads * head_dim};
     if (!tiles.empty()) {
-        const PrefillArgs pa{Q, out, a.rows, reinterpret_cast<const PrefillTile *>(base + tiles_off),
-                             static_cast<int32_t>(tiles.size()), a.pm, a.pl, a.pacc, n_heads,
-                             n_kv_heads, a.group, a.causal, S * kPrefillSplitFactor, a.scale_log2,
-                             a.err};
+        const SplitArgs sa{a.rows, reinterpret_cast<const SplitItem *>(base + items_off),
+                           static_cast<int32_t>(items.size()), n_kv_heads, base + img_off, a.err};
+        SplitCtx sc{&sa, &addr, st};
+        e = launch_counted(PKV_KERNEL_SPLIT, st, run_split, &sc);
+        PrefillArgs pa{Q, out, a.rows, reinterpret_cast<const PrefillTile *>(base + tiles_off),
+                       static_cast<int32_t>(tiles.size()), a.pm, a.pl, a.pacc, n_heads,
+                       n_kv_heads, a.group, a.causal, S * kPrefillSplitFactor, a.scale_log2,
+                       a.err};
+        pa.img = base + img_off;
+        pa.img_tile0 = reinterpret_cast<const int32_t *>(base + tile0_off);
+        pa.img_slot = reinterpret_cast<const int32_t *>(base + slot_off);
         PrefillCtx pc{&pa, &addr, st};
-        e = launch_counted(PKV_KERNEL_PREFILL, st, run_prefill, &pc);
+        if (e == cudaSuccess) e = launch_counted(PKV_KERNEL_PREFILL, st, run_prefill, &pc);
     }
     DecodeCtx dc{&a, &addr, st};
     if (e == cudaSuccess && !units.empty()) e = launch_counted(PKV_KERNEL_DECODE, st, run_decode, &dc);

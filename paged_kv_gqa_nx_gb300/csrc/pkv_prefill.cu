@@ -10,40 +10,35 @@
 // term is ~2^-22 relative.  The powers of two: one per query row, one per
 // 64-key tile of K and one of V per kv head (the largest magnitude over the
 // tile).  The scores are scaled back exactly before the softmax.  The
-// probabilities p (below 2^8, see the lazy rescale) of a tile whose V
+// probabilities p (at most 2^8, see the lazy rescale) of a tile whose V
 // exponent is c are multiplied by 2^(C - c), where C is a per-CTA exponent
 // that only decreases and stays at most 7 + c for every tile seen, so they
-// stay below 2^15; the accumulator then holds 2^C x the output's sum, is
+// stay at most 2^15; the accumulator then holds 2^C x the output's sum, is
 // rescaled exactly when C moves, and is scaled back by 2^-C at the end.
 //
+// The K/V operands of a tile come as an image made by the split pass (below)
+// from the pool's rows or from a contiguous K/V pair: the pieces already in
+// the kernel's shared-memory layout, then the tile's two exponents.  Paged
+// and contiguous launches read the same images of the same keys, so they
+// return the same bits.
+//
 // One CTA = one tile of 128 query rows -- (128 / G) consecutive tokens x the G
-// query heads that share kv head `kvh` -- and one key split.  16 compute
-// warps and one more warpgroup whose first warp issues the MMAs; that
-// warpgroup hands most of its registers to the compute warps (setmaxnreg).
-// Row m of the tile is token m / G, head m % G and TMEM lane m; the four
-// compute threads that share TMEM lane m (warps w, w + 4, w + 8, w + 12) each
-// own 16 of a key tile's scores and 32 of the row's output columns, and
-// combine the row max and sum through shared memory.  The compute warps
-// arrive on an mbarrier when the operands of QK or PV are in place; the issue
-// warp waits on it, issues, and commits to the mbarrier the compute warps
-// wait on.  Key tiles are 64 positions:
+// query heads that share kv head `kvh` -- and one key split.  Row m of the
+// tile is token m / G, head m % G, TMEM lane m and compute thread m (warps 0-3):
+// each thread reads its row's 64 scores of a key tile, so the softmax needs no
+// exchange between threads.  Warp 4 issues the QK MMAs, warp 6 the PV MMAs
+// (one thread each), warp 5 bulk-copies the images.  Key tiles are 64
+// positions; tile j of the CTA uses buffer j % 2 of K, V (shared memory), S
+// and P (TMEM):
 //   QK(j):  S[128 x 64]  = Q.K_j^T     A = Q0 (TMEM) / Q1 (smem), B = K_j (smem)
 //   PV(j):  D[128 x 128] = P_j.V_j     A = P0 / P1 (TMEM),        B = V_j^T (smem)
-// Loop j: wait S_j -> (K_{j+1} in place: QK(j+1) starts) -> online softmax
-// (offset-causal mask: key p visible iff p <= q_pos = total_k - n_q + i) ->
-// wait PV(j-1) -> write P_j (and V_j) (PV(j) starts, adding into the TMEM
-// accumulator D); QK(j+1) runs during the softmax of tile j.  p is relative
-// to a reference max that moves (and D is rescaled) only when a tile's max
-// exceeds it by more than 2^8, which keeps every p at most 256.
-// Shared memory: Q1 32 KiB, K0/K1 16 KiB each, V0^T/V1^T 16 KiB each.
+// QK(j+1) runs while the compute warps do the softmax of tile j (offset-causal
+// mask: key p visible iff p <= q_pos = total_k - n_q + i), PV(j) after it.  p
+// is relative to a reference max that moves (and D is rescaled) only when a
+// tile's max exceeds it by more than 2^8, which keeps every p at most 256.
+// Shared memory: Q1 32 KiB, two K and two V buffers of 32 KiB (pieces 0, 1).
 // TMEM (512 columns; two f16 per column for the A operands): Q0 [0,64),
-// S [64,128), P0 [128,160), P1 [160,192), D [256,384).
-//
-// The operands come either as images made by the split pass (paged launches)
-// or are loaded and split by the compute warps (contiguous launches); both
-// take the same tile exponents (over the tile's keys below total_k, zero
-// beyond) and the same pieces, so the paged and contiguous launches return
-// the same bits.
+// S buffers [64,192), P buffers [192,320), D [384,512).
 #include "pkv_elem.h"
 #include "pkv_internal.h"
 #include "pkv_tcgen05.h"
@@ -62,36 +57,12 @@ constexpr uint32_t kTmemCols = 512;
 // TMEM columns: Q0 [0,64), S buffers [64,192) (64 each), P buffers [192,320)
 // (buffer b: piece 0 at 192 + 64b, piece 1 32 columns on), D [384,512)
 constexpr uint32_t kColQ0 = 0, kColS = 64, kColP = 192, kColD = 384;
-#ifndef PKV_PREFILL_COMPUTE_WARPS
-#define PKV_PREFILL_COMPUTE_WARPS 16
-#endif
-constexpr int kComputeWarps = PKV_PREFILL_COMPUTE_WARPS;  // 8: two threads per tile row, 16: four
+constexpr int kComputeWarps = 4;          // one thread per tile row
 constexpr int kCompute = 32 * kComputeWarps;
-// + one warpgroup whose first warp issues the MMAs; it gives registers back
-// (setmaxnreg) so that the compute warps can hold more
-constexpr int kThreads = kCompute + 128;
-// per thread at launch: 65536 registers over the CTA, and 16384 over the at
-// most kThreads/128 warps of one SM sub-partition
-constexpr int kLaunchRegs = kComputeWarps == 16 ? 96 : 168;
-constexpr int kIssueRegs = 32;                                 // issue warpgroup after .dec
-constexpr int kComputeRegs = kComputeWarps == 16 ? 112 : 232;  // compute warps after .inc
-static_assert(kCompute * kComputeRegs + 128 * kIssueRegs <= kThreads * kLaunchRegs,
-              "register split exceeds the launch's registers");
-// with operand images the compute warps hold no prefetch registers and the
-// issue thread also runs the copies
-constexpr int kIssueRegsBulk = 80;
-constexpr int kComputeRegsBulk = kComputeWarps == 16 ? 96 : 184;
-static_assert(kCompute * kComputeRegsBulk + 128 * kIssueRegsBulk <= kThreads * kLaunchRegs,
-              "register split exceeds the launch's registers");
-static_assert(kComputeWarps != 16 || 4 * 32 * kComputeRegsBulk + 32 * kIssueRegsBulk <= 16384,
-              "register split exceeds one SM sub-partition");
-constexpr int kTPR = kComputeWarps / 4;                     // threads per tile row
-constexpr int kSCols = kKT / kTPR;                          // scores per thread per key tile
-constexpr int kDCols = kHD / kTPR;                          // output columns per thread
-constexpr int kKPW = kKT / kComputeWarps;                   // K rows per warp per key tile
-static_assert(kComputeWarps == 8 || kComputeWarps == 16, "8 or 16 compute warps");
-constexpr float kRescale = 8.f;               // lazy-rescale threshold (base 2)
-constexpr int kPExp = 7;                      // C <= kPExp + c: p * 2^(C - c) < 2^(8 + kPExp)
+constexpr int kWarpQK = 4, kWarpCopy = 5, kWarpPV = 6;
+constexpr int kThreads = 32 * 7;
+constexpr float kRescale = 8.f;           // lazy-rescale threshold (base 2)
+constexpr int kPExp = 7;                  // C <= kPExp + c: p * 2^(C - c) <= 2^(8 + kPExp)
 
 // The power of two that brings a largest magnitude m into [2^14, 2^15):
 // 14 - floor(log2 m), clamped to [-113, 126] (m = 0 or subnormal: 126).
@@ -116,7 +87,7 @@ __device__ __forceinline__ void split_f16x2(float a, float b, uint32_t &p0, uint
     p0 = *reinterpret_cast<const uint32_t *>(&h0);
     p1 = *reinterpret_cast<const uint32_t *>(&h1);
 }
-// Eight consecutive values times 2^e as one 16-byte chunk of each piece.
+// Eight consecutive values times sc as one 16-byte chunk of each piece.
 __device__ __forceinline__ void split_chunk(const float (&x)[8], float sc, uint4 &c0, uint4 &c1) {
     split_f16x2(x[0] * sc, x[1] * sc, c0.x, c1.x);
     split_f16x2(x[2] * sc, x[3] * sc, c0.y, c1.y);
@@ -137,30 +108,37 @@ __device__ __forceinline__ float warp_max(float v) {
     for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
     return v;
 }
+// max / sum of N values as a pairwise tree (N a power of two)
+template <int N>
+__device__ __forceinline__ float tree_max(const float (&v)[N]) {
+    float t[N / 2];
+#pragma unroll
+    for (int i = 0; i < N / 2; ++i) t[i] = fmaxf(v[2 * i], v[2 * i + 1]);
+#pragma unroll
+    for (int w = N / 4; w >= 1; w >>= 1)
+#pragma unroll
+        for (int i = 0; i < w; ++i) t[i] = fmaxf(t[2 * i], t[2 * i + 1]);
+    return t[0];
+}
+template <int N>
+__device__ __forceinline__ float tree_sum(const float (&v)[N]) {
+    float t[N / 2];
+#pragma unroll
+    for (int i = 0; i < N / 2; ++i) t[i] = v[2 * i] + v[2 * i + 1];
+#pragma unroll
+    for (int w = N / 4; w >= 1; w >>= 1)
+#pragma unroll
+        for (int i = 0; i < w; ++i) t[i] = t[2 * i] + t[2 * i + 1];
+    return t[0];
+}
 
+// Rows of the split pass: through the page table, or a contiguous K/V pair.
 template <class E>
 struct PagedRowsP {
     using Elem = E;
     PagedAddr a;
-    // Block id of (slot, pos), or -1 (and the error flag) when the page index
-    // or the id is out of range.
-    __device__ __forceinline__ int block(int slot, int pos, int32_t *err) const {
-        const int bi = a.bs_shift >= 0 ? (pos >> a.bs_shift) : (pos / a.bs);
-        if (bi >= a.max_blocks) {
-            if (err) atomicOr(err, 1);
-            return -1;
-        }
-        const int blk = __ldg(a.pt + static_cast<size_t>(slot) * a.max_blocks + bi);
-        if (static_cast<unsigned>(blk) >= static_cast<unsigned>(a.n_blocks)) {
-            if (err) atomicOr(err, 1);
-            return -1;
-        }
-        return blk;
-    }
-    // The page-table entry of (slot, pos) without waiting for it: -1 when the
-    // page index is out of range (error flag set), else the raw entry, which
-    // checked() validates where it is used, a tile later, so the lookup's
-    // latency stays off the critical path.
+    // The page-table entry of (slot, pos): -1 when the page index is out of
+    // range (error flag set), else the raw entry, which checked() validates.
     __device__ __forceinline__ int entry(int slot, int pos, int32_t *err) const {
         const int bi = a.bs_shift >= 0 ? (pos >> a.bs_shift) : (pos / a.bs);
         if (bi >= a.max_blocks) {
@@ -187,14 +165,12 @@ struct PagedRowsP {
     __device__ __forceinline__ const E *v_row(int blk, int pos, int kvh) const {
         return static_cast<const E *>(a.v) + offset(blk, pos, kvh);
     }
-    // groups of n positions starting at a multiple of n lie in one block
-    __device__ __forceinline__ bool whole(int n) const { return (a.bs % n) == 0; }
+    __device__ __forceinline__ float scale() const { return a.kv_scale; }
 };
 
 struct ContigRowsP {
     using Elem = float;
     ContigAddr a;
-    __device__ __forceinline__ int block(int, int, int32_t *) const { return 0; }
     __device__ __forceinline__ int entry(int, int, int32_t *) const { return 0; }
     __device__ __forceinline__ int checked(int blk, int32_t *) const { return blk; }
     __device__ __forceinline__ const float *k_row(int, int pos, int kvh) const {
@@ -203,7 +179,7 @@ struct ContigRowsP {
     __device__ __forceinline__ const float *v_row(int, int pos, int kvh) const {
         return a.v + static_cast<size_t>(pos) * a.kv_dim + static_cast<size_t>(kvh) * kHD;
     }
-    __device__ __forceinline__ bool whole(int) const { return true; }
+    __device__ __forceinline__ float scale() const { return 1.f; }
 };
 
 constexpr uint32_t kSmemQ1 = 32 * 1024;  // Q1: 2 k-blocks of 128 rows x 64 f16
@@ -213,31 +189,25 @@ constexpr uint32_t kSmemKV = 2 * kImagePlane;
 static_assert(kImagePlane == 16 * 1024, "a piece of a tile is 16 KiB");
 constexpr size_t kSmemBytes = kSmemQ1 + 4 * kSmemKV + 1024;  // + alignment slack
 
-// kBulk: the K/V operands come as images (the split pass) by bulk copy;
-// otherwise the compute warps load and split them.  kLoZero (images of a
-// bf16 or fp8 pool): the K / V piece-1 planes are left out -- a pool value
-// times the tile's power of two is exact in f16 unless it lies more than
-// 2^28 below the tile's largest magnitude, where it is rounded to an f16
-// subnormal (an error below 2^-38 of that magnitude) -- so they are neither
-// copied nor used.
+// kLoZero (images of a bf16 or fp8 pool): the K / V piece-1 planes are left
+// out -- a pool value times the tile's power of two is exact in f16 unless it
+// lies more than 2^28 below the tile's largest magnitude, where it is rounded
+// to an f16 subnormal (an error below 2^-38 of that magnitude) -- so they are
+// neither copied nor used.
 //
-// Tile j of the CTA (key tile kt0 + j) uses buffer b = j & 1 of K, V (shared
-// memory), S and P (TMEM).  Per-buffer mbarriers, phase j >> 1 for tile j:
-//   qkready[b]  QK(j)'s operands: K_j in place (copy warp's bytes; register
-//               mode: the compute warps' stores) and S_{j-2} read (compute
-//               warps; for j < 2 their arrival after writing Q instead)
-//   pvready[b]  PV(j)'s operands: P_j written (compute warps) and V_j in place
-//               (copy warp's bytes; register mode: stored with P)
+// Per-buffer mbarriers, phase j / 2 for tile j:
+//   qkready[b]  QK(j)'s operands: K_j landed (copy warp's bytes) and S_{j-2}
+//               read (compute warps; for j < 2 their arrival after writing Q)
+//   pvready[b]  PV(j)'s operands: P_j written (compute warps), V_j landed
 //   qkdone[b]   QK(j) complete (commit)
 //   pvdone[b]   PV(j) complete (commit)
-// One warp issues the QKs and another the PVs, each waiting once per tile: a
-// thread's mbarrier test after its own MMAs waits for them to reach the tensor
-// core, so with one issuing thread the tensor pipe drained at every wait.
-// QK(j+1) runs while the compute warps do the softmax of tile j.  No waiter
+// QK and PV are issued by two warps, each waiting once per tile: a thread's
+// mbarrier test after its own MMAs waits for them to reach the tensor core,
+// so with one issuing thread the tensor pipe drained at every wait.  No waiter
 // is ever two phases behind: each next phase needs an arrival that follows
 // the wait.
-template <int G, class Rows, bool kBulk, bool kLoZero>
-__global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs a, Rows rows_of) {
+template <int G, bool kLoZero>
+__global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs a) {
     constexpr int TQ = 128 / G;  // tokens per tile
     extern __shared__ __align__(1024) unsigned char smraw[];
     unsigned char *sm = reinterpret_cast<unsigned char *>(
@@ -247,10 +217,6 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs a, 
     unsigned char *Vbuf = Kbuf + 2 * kSmemKV;
     __shared__ uint64_t bar_qkready[2], bar_pvready[2], bar_qkdone[2], bar_pvdone[2];
     __shared__ uint32_t tslot;
-    __shared__ float red[2][kCompute];
-    __shared__ float kpart[kComputeWarps], vpart[kComputeWarps];  // register mode: tile maxima
-    __shared__ int s_flag;
-    static_assert(kSCols == 16, "16 scores per thread");
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int ti = blockIdx.x / a.n_kv;
@@ -266,6 +232,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs a, 
     const int kt0 = kbeg / kKT, kt1 = (kend + kKT - 1) / kKT;
     const int n = kt1 - kt0;  // key tiles of this CTA
     auto ph = [](int j) { return static_cast<uint32_t>(j >> 1) & 1u; };
+    // lane 0 waits (bounded), the warp learns the outcome
+    auto wait_w = [&](uint64_t *bar, uint32_t parity) {
+        return __shfl_sync(0xffffffffu, lane == 0 ? mbar_wait(smem_u32(bar), parity) : true, 0) != 0;
+    };
 
     if (warp == 0) {
         tmem_alloc(smem_u32(&tslot), kTmemCols);
@@ -273,11 +243,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs a, 
     }
     if (tid == 0) {
         for (int b = 0; b < 2; ++b) {
-            // per phase: the compute warps' arrivals, and the copy warp's
-            // expect-tx arrival (image mode) or a second arrival of the compute
-            // warps after storing K (register mode)
-            mbar_init(smem_u32(&bar_qkready[b]), kBulk ? kComputeWarps + 1 : 2 * kComputeWarps);
-            mbar_init(smem_u32(&bar_pvready[b]), kComputeWarps + (kBulk ? 1 : 0));
+            // per phase: the compute warps' arrivals and the copy warp's expect-tx arrival
+            mbar_init(smem_u32(&bar_qkready[b]), kComputeWarps + 1);
+            mbar_init(smem_u32(&bar_pvready[b]), kComputeWarps + 1);
             mbar_init(smem_u32(&bar_qkdone[b]), 1);
             mbar_init(smem_u32(&bar_pvdone[b]), 1);
         }
@@ -287,58 +255,48 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs a, 
     fence_after_sync();
     const uint32_t tbase = tslot;
     bool ok = true;
-    // image of key tile kt (image mode)
-    const int32_t *slots = kBulk ? a.img_slot + a.img_tile0[tile.row] : nullptr;
+    const int32_t *slots = a.img_slot + a.img_tile0[tile.row];  // images of the row's key tiles
     auto image = [&](int32_t slot) {
         return a.img + (static_cast<size_t>(slot) * a.n_kv + kvh) * kImageBytes;
     };
 
-    if (warp >= kComputeWarps) {
-        // the issue warpgroup: its first warp issues the MMAs, in image mode
-        // its second warp runs the bulk copies; the rest only give their
-        // registers back
-        setmaxnreg_dec<kBulk ? kIssueRegsBulk : kIssueRegs>();
-        // lane 0 waits (bounded), the warp learns the outcome
-        auto wait_w = [&](uint64_t *bar, uint32_t parity) {
-            return __shfl_sync(0xffffffffu, lane == 0 ? mbar_wait(smem_u32(bar), parity) : true, 0) != 0;
+    if (warp == kWarpCopy) {
+        // ---------------- copy warp (lane 0 copies) ----------------
+        // Buffer b is refilled with tile j + 2 as soon as the MMAs of tile j
+        // that read it are done; each copy arrives with its byte count on the
+        // barrier that the MMA warps wait on.
+        constexpr uint32_t planes = kLoZero ? 1u : 2u;  // pieces 0 (and 1) of K / V
+        auto copy = [&](unsigned char *dst, uint64_t *bar, int j, uint32_t plane0) {
+            if (lane == 0) {
+                const unsigned char *src = image(__ldg(slots + kt0 + j)) + plane0 * kImagePlane;
+                mbar_expect_tx(smem_u32(bar), planes * kImagePlane);
+                bulk_g2s(smem_u32(dst), src, kImagePlane, smem_u32(bar));
+                if constexpr (planes == 2)
+                    bulk_g2s(smem_u32(dst + kImagePlane), src + kImagePlane, kImagePlane, smem_u32(bar));
+            }
         };
-        if (kBulk && warp == kComputeWarps + 1) {
-            // ---------------- copy warp (lane 0 copies) ----------------
-            // Buffer b is refilled with tile j + 2 as soon as the MMAs of tile
-            // j that read it are done; each copy arrives with its byte count on
-            // the barrier that the MMA warp waits on.
-            constexpr uint32_t planes = kLoZero ? 1u : 2u;  // pieces 0 (and 1) of K / V
-            auto copy = [&](unsigned char *dst, uint64_t *bar, int j, uint32_t plane0) {
-                if (lane == 0) {
-                    const unsigned char *src = image(__ldg(slots + kt0 + j)) + plane0 * kImagePlane;
-                    mbar_expect_tx(smem_u32(bar), planes * kImagePlane);
-                    bulk_g2s(smem_u32(dst), src, kImagePlane, smem_u32(bar));
-                    if constexpr (planes == 2)
-                        bulk_g2s(smem_u32(dst + kImagePlane), src + kImagePlane, kImagePlane, smem_u32(bar));
-                }
-            };
-            auto copy_k = [&](int j) { copy(Kbuf + (j & 1) * kSmemKV, &bar_qkready[j & 1], j, 0); };
-            auto copy_v = [&](int j) { copy(Vbuf + (j & 1) * kSmemKV, &bar_pvready[j & 1], j, 2); };
-            for (int j = 0; j < min(n, 2); ++j) {
-                copy_k(j);
-                copy_v(j);
-            }
-            bool cok = true;
-            for (int j = 0; j + 2 < n; ++j) {
-                cok = wait_w(&bar_qkdone[j & 1], ph(j));  // QK(j) done: K buffer free
-                if (!cok) break;
-                copy_k(j + 2);
-                cok = wait_w(&bar_pvdone[j & 1], ph(j));  // PV(j) done: V buffer free
-                if (!cok) break;
-                copy_v(j + 2);
-            }
-            // let the last copies land before the CTA's shared memory is given
-            // up (bounded if the MMA side gave up)
-            for (int j = max(0, n - 2); j < n; ++j) {
-                wait_w(&bar_qkready[j & 1], ph(j));
-                wait_w(&bar_pvready[j & 1], ph(j));
-            }
-        } else if (warp == kComputeWarps || warp == kComputeWarps + 2) {
+        auto copy_k = [&](int j) { copy(Kbuf + (j & 1) * kSmemKV, &bar_qkready[j & 1], j, 0); };
+        auto copy_v = [&](int j) { copy(Vbuf + (j & 1) * kSmemKV, &bar_pvready[j & 1], j, 2); };
+        for (int j = 0; j < min(n, 2); ++j) {
+            copy_k(j);
+            copy_v(j);
+        }
+        bool cok = true;
+        for (int j = 0; j + 2 < n; ++j) {
+            cok = wait_w(&bar_qkdone[j & 1], ph(j));  // QK(j) done: K buffer free
+            if (!cok) break;
+            copy_k(j + 2);
+            cok = wait_w(&bar_pvdone[j & 1], ph(j));  // PV(j) done: V buffer free
+            if (!cok) break;
+            copy_v(j + 2);
+        }
+        // let the last copies land before the CTA's shared memory is given up
+        // (bounded if the other warps gave up)
+        for (int j = max(0, n - 2); j < n; ++j) {
+            wait_w(&bar_qkready[j & 1], ph(j));
+            wait_w(&bar_pvready[j & 1], ph(j));
+        }
+    } else if (warp == kWarpQK || warp == kWarpPV) {
         // ---------- MMA issue warps (lane 0 issues): QK(j) / PV(j) ----------
         const uint64_t dQ1 = desc_sw128(smem_u32(Q1));
         const uint32_t tQ = tbase + kColQ0, tD = tbase + kColD;
@@ -347,317 +305,152 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs a, 
         // pieces (products with the K / V piece-1 planes are left out when
         // those are zero)
         constexpr bool lo = !kLoZero;
-        auto qk_step = [&](int s, uint32_t tS, uint64_t dK0, uint64_t dK1) {
-            const uint64_t ko = ((s >> 2) * 8192u + (s & 3) * 32u) >> 4;
-            const uint64_t qo = ((s >> 2) * 16384u + (s & 3) * 32u) >> 4;
-            mma_f16_ts(tS, tQ + 8 * s, dK0 + ko, idesc_s, s > 0);
-            if constexpr (lo) mma_f16_ts(tS, tQ + 8 * s, dK1 + ko, idesc_s, 1);
-            mma_f16(tS, dQ1 + qo, dK0 + ko, idesc_s, 1);
-        };
-        auto pv_step = [&](int s, bool first, uint32_t tP, uint64_t dV0, uint64_t dV1) {
-            const uint64_t vo = (s * 32u) >> 4;
-            mma_f16_ts(tD, tP + 8 * s, dV0 + vo, idesc_o, !first || s > 0);
-            if constexpr (lo) mma_f16_ts(tD, tP + 8 * s, dV1 + vo, idesc_o, 1);
-            mma_f16_ts(tD, tP + 32 + 8 * s, dV0 + vo, idesc_o, 1);
-        };
-        // the MMAs of one tile (lane 0 issues, then commits); unrolled when the
-        // issue warpgroup has the registers for it (image mode)
-        auto mma_qk = [&](int b) {
-            fence_after_sync();
-            if (lane == 0) {
-                const uint32_t tS = tbase + kColS + 64u * b;
-                const uint64_t dK0 = desc_sw128(smem_u32(Kbuf + b * kSmemKV));
-                const uint64_t dK1 = desc_sw128(smem_u32(Kbuf + b * kSmemKV + kImagePlane));
-                if constexpr (kBulk) {
-#pragma unroll
-                    for (int s = 0; s < kHD / 16; ++s) qk_step(s, tS, dK0, dK1);
-                } else {
-#pragma unroll 1
-                    for (int s = 0; s < kHD / 16; ++s) qk_step(s, tS, dK0, dK1);
-                }
-                mma_commit(smem_u32(&bar_qkdone[b]));
-            }
-            __syncwarp();
-        };
-        auto mma_pv = [&](int b, bool first) {
-            fence_after_sync();
-            if (lane == 0) {
-                const uint32_t tP = tbase + kColP + 64u * b;
-                const uint64_t dV0 = desc_sw128(smem_u32(Vbuf + b * kSmemKV));
-                const uint64_t dV1 = desc_sw128(smem_u32(Vbuf + b * kSmemKV + kImagePlane));
-                if constexpr (kBulk) {
-#pragma unroll
-                    for (int s = 0; s < kKT / 16; ++s) pv_step(s, first, tP, dV0, dV1);
-                } else {
-#pragma unroll 1
-                    for (int s = 0; s < kKT / 16; ++s) pv_step(s, first, tP, dV0, dV1);
-                }
-                mma_commit(smem_u32(&bar_pvdone[b]));
-            }
-            __syncwarp();
-        };
-        if (warp == kComputeWarps) {
+        if (warp == kWarpQK) {
             for (int j = 0; j < n && ok; ++j) {
-                ok = wait_w(&bar_qkready[j & 1], ph(j));
-                if (ok) mma_qk(j & 1);
+                const int b = j & 1;
+                ok = wait_w(&bar_qkready[b], ph(j));
+                if (!ok) break;
+                fence_after_sync();
+                if (lane == 0) {
+                    const uint32_t tS = tbase + kColS + 64u * b;
+                    const uint64_t dK0 = desc_sw128(smem_u32(Kbuf + b * kSmemKV));
+                    const uint64_t dK1 = desc_sw128(smem_u32(Kbuf + b * kSmemKV + kImagePlane));
+#pragma unroll
+                    for (int s = 0; s < kHD / 16; ++s) {
+                        const uint64_t ko = ((s >> 2) * 8192u + (s & 3) * 32u) >> 4;
+                        const uint64_t qo = ((s >> 2) * 16384u + (s & 3) * 32u) >> 4;
+                        mma_f16_ts(tS, tQ + 8 * s, dK0 + ko, idesc_s, s > 0);
+                        if constexpr (lo) mma_f16_ts(tS, tQ + 8 * s, dK1 + ko, idesc_s, 1);
+                        mma_f16(tS, dQ1 + qo, dK0 + ko, idesc_s, 1);
+                    }
+                    mma_commit(smem_u32(&bar_qkdone[b]));
+                }
+                __syncwarp();
             }
         } else {
             for (int j = 0; j < n && ok; ++j) {
-                ok = wait_w(&bar_pvready[j & 1], ph(j));
-                if (ok) mma_pv(j & 1, j == 0);
+                const int b = j & 1;
+                ok = wait_w(&bar_pvready[b], ph(j));
+                if (!ok) break;
+                fence_after_sync();
+                if (lane == 0) {
+                    const uint32_t tP = tbase + kColP + 64u * b;
+                    const uint64_t dV0 = desc_sw128(smem_u32(Vbuf + b * kSmemKV));
+                    const uint64_t dV1 = desc_sw128(smem_u32(Vbuf + b * kSmemKV + kImagePlane));
+#pragma unroll
+                    for (int s = 0; s < kKT / 16; ++s) {
+                        const uint64_t vo = (s * 32u) >> 4;
+                        mma_f16_ts(tD, tP + 8 * s, dV0 + vo, idesc_o, j > 0 || s > 0);
+                        if constexpr (lo) mma_f16_ts(tD, tP + 8 * s, dV1 + vo, idesc_o, 1);
+                        mma_f16_ts(tD, tP + 32 + 8 * s, dV0 + vo, idesc_o, 1);
+                    }
+                    mma_commit(smem_u32(&bar_pvdone[b]));
+                }
+                __syncwarp();
             }
         }
         if (!ok && lane == 0 && a.err) atomicOr(a.err, 2);
-        }
-    } else {
-        setmaxnreg_inc<kBulk ? kComputeRegsBulk : kComputeRegs>();
-        // ---------------- compute warps: 4 threads per tile row ----------------
-        const int wq = warp & 3;               // TMEM lane quadrant
-        const int qp = warp >> 2;              // which quarter of the row this thread owns
-        const int m = 32 * wq + lane;          // this thread's row of the tile
+    } else if (warp < kComputeWarps) {
+        // ---------------- compute warps: one thread per tile row ----------------
+        const int m = tid;                     // this thread's row of the tile (TMEM lane)
         const int tq = m / G, g = m - (m / G) * G;
         const int qi = tile.q0 + tq;
         const bool valid = qi < rd.n_q;
         const int q_pos = total_k - rd.n_q + qi;
         const int kend_row = valid ? (a.causal ? min(q_pos + 1, total_k) : total_k) : 1;
         const int klim = min(kend_row, kend);  // keys below klim are visible to this row
-        const uint32_t tlane = static_cast<uint32_t>(32 * wq) << 16;
-        const int r0 = tid & 127;
-
-        // operands written: make them visible to the tensor core, then one lane
-        // per warp arrives on the barrier the issue warp waits on
+        const uint32_t tlane = static_cast<uint32_t>(32 * warp) << 16;
+        // this warp's arrival on an operand barrier, after its TMEM stores
         auto arrive = [&](uint64_t *bar) {
             tmem_st_wait();
-            fence_proxy_async();
             fence_before_sync();
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(bar));
         };
-        // Wait for an MMA commit: one thread polls the mbarrier and the others
-        // wait in the named barrier, so the polling takes no shared-memory
-        // bandwidth from the tensor core's operand reads.
-        auto wait_one = [&](uint64_t *bar, uint32_t parity) {
-            bool w = true;
-            if (tid == 0) w = mbar_wait(smem_u32(bar), parity);
-            __syncwarp();
-            return named_sync_and(1, kCompute, w);
-        };
 
         // Q row (pre-scaled to base-2 units, then by the row's power of two):
-        // this thread's kDCols dims, piece 0 -> TMEM, piece 1 -> shared memory
+        // piece 0 -> TMEM, piece 1 -> shared memory.  All 32 loads of the row
+        // are issued together (one memory latency), then its largest
+        // magnitude, then the pieces.
         int qexp;
         {
-            static_assert(kDCols == 32, "32 dims per thread");
-            const float *qrow = a.Q + static_cast<size_t>(rd.q_row0 + (valid ? qi : 0)) * (a.n_heads * kHD) +
-                                static_cast<size_t>(kvh * G + g) * kHD + kDCols * qp;
-            float x[32];
+            const float4 *qrow = reinterpret_cast<const float4 *>(
+                a.Q + static_cast<size_t>(rd.q_row0 + (valid ? qi : 0)) * (a.n_heads * kHD) +
+                static_cast<size_t>(kvh * G + g) * kHD);
+            float4 q[kHD / 4];
+#pragma unroll
+            for (int j4 = 0; j4 < kHD / 4; ++j4) q[j4] = valid ? __ldg(qrow + j4) : make_float4(0.f, 0.f, 0.f, 0.f);
             float mx = 0.f;
 #pragma unroll
-            for (int j4 = 0; j4 < 8; ++j4) {
-                float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (valid) v = __ldg(reinterpret_cast<const float4 *>(qrow) + j4);
-                v.x *= a.scale_log2;
-                v.y *= a.scale_log2;
-                v.z *= a.scale_log2;
-                v.w *= a.scale_log2;
-                x[4 * j4] = v.x;
-                x[4 * j4 + 1] = v.y;
-                x[4 * j4 + 2] = v.z;
-                x[4 * j4 + 3] = v.w;
-                mx = absmax4(mx, v);
+            for (int j4 = 0; j4 < kHD / 4; ++j4) {
+                q[j4].x *= a.scale_log2;
+                q[j4].y *= a.scale_log2;
+                q[j4].z *= a.scale_log2;
+                q[j4].w *= a.scale_log2;
+                mx = absmax4(mx, q[j4]);
             }
-            red[0][tid] = mx;
-            named_sync(1, kCompute);
-            float rmax = red[0][r0];
-#pragma unroll
-            for (int k = 1; k < kTPR; ++k) rmax = fmaxf(rmax, red[0][r0 + 128 * k]);
-            qexp = f16_scale_exp(rmax);
+            qexp = f16_scale_exp(mx);
             const float qs = pow2f(qexp);
-            uint32_t h0[16];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                float c8[8];
+            for (int c4 = 0; c4 < 4; ++c4) {  // 32 dims: 16 TMEM columns, 4 chunks of Q1
+                uint32_t h0[16];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) c8[i] = x[8 * j + i];
-                uint4 c0, c1;
-                split_chunk(c8, qs, c0, c1);
-                h0[4 * j] = c0.x;
-                h0[4 * j + 1] = c0.y;
-                h0[4 * j + 2] = c0.z;
-                h0[4 * j + 3] = c0.w;
-                // dims 32 qp + 8 j: k-block qp / 2, chunk 4 (qp % 2) + j of row m
-                *reinterpret_cast<uint4 *>(Q1 + (qp >> 1) * 16384u + sw128_chunk(m, 4 * (qp & 1) + j)) = c1;
+                for (int j = 0; j < 4; ++j) {
+                    const int c = 4 * c4 + j;  // dims 8c .. 8c + 7
+                    const float x[8] = {q[2 * c].x,     q[2 * c].y,     q[2 * c].z,     q[2 * c].w,
+                                        q[2 * c + 1].x, q[2 * c + 1].y, q[2 * c + 1].z, q[2 * c + 1].w};
+                    uint4 c0, c1;
+                    split_chunk(x, qs, c0, c1);
+                    h0[4 * j] = c0.x;
+                    h0[4 * j + 1] = c0.y;
+                    h0[4 * j + 2] = c0.z;
+                    h0[4 * j + 3] = c0.w;
+                    // k-block c / 8, chunk c % 8 of row m
+                    *reinterpret_cast<uint4 *>(Q1 + (c >> 3) * 16384u + sw128_chunk(m, c & 7)) = c1;
+                }
+                tmem_st16u(tbase + tlane + kColQ0 + 16 * c4, h0);
             }
-            tmem_st16u(tbase + tlane + kColQ0 + 16 * qp, h0);
         }
         // Q written: the arrival that stands for "S_{j-2} read" of tiles 0 and 1
+        fence_proxy_async();
         arrive(&bar_qkready[0]);
         arrive(&bar_qkready[1]);
-
-        // Register mode.  Key rows of a tile: warp w owns keys kKPW*w ..
-        // kKPW*w + kKPW-1 of both K and V (every key below total_k, zero
-        // beyond, as in an image).  K: lane l holds dims 4l .. 4l+3 of each
-        // row, stored as 8-byte halves of the K-major chunks.  V: lane l holds
-        // dims l + 32c (c < 4) of each row and writes 4 keys of rows
-        // d = l + 32c of V^T.
-        float4 kreg[kKPW], vq[kKPW / 4][4];
-        const bool k_whole = rows_of.whole(kKPW);
-        auto k_pos = [&](int kt) { return kt * kKT + warp * kKPW; };
-        using E = typename Rows::Elem;
-        auto row_of = [&](int pos, int blk0, bool is_v) -> const E * {
-            if (pos >= total_k) return nullptr;
-            int b = blk0;
-            if (!k_whole) b = rows_of.block(rd.slot, pos, a.err);
-            if (b < 0) return nullptr;
-            return is_v ? rows_of.v_row(b, pos, kvh) : rows_of.k_row(b, pos, kvh);
-        };
-        auto load_k = [&](int kt, int blk0) {
-            const int pos0 = k_pos(kt);
-            if (k_whole && pos0 < total_k) blk0 = rows_of.checked(blk0, a.err);
-#pragma unroll
-            for (int i = 0; i < kKPW; ++i) {
-                const E *kr = row_of(pos0 + i, blk0, false);
-                kreg[i] = kr ? ldg4(kr + 4 * lane) : make_float4(0.f, 0.f, 0.f, 0.f);
-            }
-        };
-        auto load_v = [&](int kt, int blk0) {
-            const int pos0 = k_pos(kt);
-            if (k_whole && pos0 < total_k) blk0 = rows_of.checked(blk0, a.err);
-#pragma unroll
-            for (int g4 = 0; g4 < kKPW / 4; ++g4) {
-                float v[4][4];  // [key][c]
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const E *vr = row_of(pos0 + 4 * g4 + i, blk0, true);
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) v[i][c] = vr ? ldg1(vr + lane + 32 * c) : 0.f;
-                }
-#pragma unroll
-                for (int c = 0; c < 4; ++c) vq[g4][c] = make_float4(v[0][c], v[1][c], v[2][c], v[3][c]);
-            }
-        };
-        auto lookup_k = [&](int kt) {
-            const int pos0 = k_pos(kt);
-            return (k_whole && pos0 < total_k) ? rows_of.entry(rd.slot, pos0, a.err) : -1;
-        };
-        auto lookup_v = lookup_k;
-        // the K tile's exponent: this warp's maximum, then all warps' (a
-        // barrier of the compute warps)
-        auto k_exp = [&]() {
-            float mx = 0.f;
-#pragma unroll
-            for (int i = 0; i < kKPW; ++i) mx = absmax4(mx, kreg[i]);
-            mx = warp_max(mx);
-            if (lane == 0) kpart[warp] = mx;
-            named_sync(2, kCompute);
-            float t = kpart[0];
-#pragma unroll
-            for (int w = 1; w < kComputeWarps; ++w) t = fmaxf(t, kpart[w]);
-            return f16_scale_exp(t);
-        };
-        auto store_k = [&](int b, int kexp) {
-            unsigned char *K0 = Kbuf + b * kSmemKV, *K1 = K0 + kImagePlane;
-            const float ks = pow2f(kexp);
-#pragma unroll
-            for (int i = 0; i < kKPW; ++i) {
-                uint32_t a0, a1, b0, b1;
-                split_f16x2(kreg[i].x * ks, kreg[i].y * ks, a0, a1);
-                split_f16x2(kreg[i].z * ks, kreg[i].w * ks, b0, b1);
-                // dims 4 lane .. 4 lane + 3: k-block lane / 16, chunk (lane % 16) / 2, half lane % 2
-                const uint32_t off = (lane >> 4) * 8192u + sw128_chunk(warp * kKPW + i, (lane & 15) >> 1) +
-                                     8u * (lane & 1);
-                *reinterpret_cast<uint2 *>(K0 + off) = make_uint2(a0, b0);
-                *reinterpret_cast<uint2 *>(K1 + off) = make_uint2(a1, b1);
-            }
-        };
-        // this warp's part of the V tile's maximum (read after the next barrier)
-        auto v_part = [&]() {
-            float mx = 0.f;
-#pragma unroll
-            for (int g4 = 0; g4 < kKPW / 4; ++g4)
-#pragma unroll
-                for (int c = 0; c < 4; ++c) mx = absmax4(mx, vq[g4][c]);
-            mx = warp_max(mx);
-            if (lane == 0) vpart[warp] = mx;
-        };
-        auto store_v = [&](int b, int vexp) {
-            unsigned char *V0 = Vbuf + b * kSmemKV, *V1 = V0 + kImagePlane;
-            const float vs = pow2f(vexp);
-#pragma unroll
-            for (int g4 = 0; g4 < kKPW / 4; ++g4) {
-                const int key0 = warp * kKPW + 4 * g4;
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    uint32_t a0, a1, b0, b1;
-                    split_f16x2(vq[g4][c].x * vs, vq[g4][c].y * vs, a0, a1);
-                    split_f16x2(vq[g4][c].z * vs, vq[g4][c].w * vs, b0, b1);
-                    // keys key0 .. key0 + 3 of row d: chunk key0 / 8, half (key0 / 4) % 2
-                    const uint32_t off = sw128_chunk(lane + 32 * c, key0 >> 3) + 8u * ((key0 >> 2) & 1);
-                    *reinterpret_cast<uint2 *>(V0 + off) = make_uint2(a0, b0);
-                    *reinterpret_cast<uint2 *>(V1 + off) = make_uint2(a1, b1);
-                }
-            }
-        };
 
         // The output accumulator lives in TMEM (D) and the P.V MMAs add into it.
         // p is taken relative to a reference max m_ref that moves only when a
         // tile's max exceeds it by more than kRescale (base-2 units); then D and
-        // l are rescaled once.  The four threads of a row take the same decisions.
+        // l are rescaled once.
         float m_ref = -INFINITY, l_run = 0.f;
         int cexp = 0;  // C: D holds 2^C x the output's sum
-
-        // prologue.  Register mode: K_0 in place (QK(0) may start), V_0 and
-        // K_1 in registers.  Image mode: the copy warp brings K and V in; the
-        // tile exponents are read from the images a tile ahead.
-        int vblk = -1, kblk = -1;
-        int kexp_cur = 0, kexp_next = 0;
+        // the tile exponents (K, V), read from the images a tile ahead
         int2 ex_cur = make_int2(0, 0);
         int32_t slot_next = 0;
-        if constexpr (kBulk) {
-            if (n > 0) ex_cur = __ldg(reinterpret_cast<const int2 *>(image(__ldg(slots + kt0)) + kImageExpOff));
-            if (n > 1) slot_next = __ldg(slots + kt0 + 1);
-        } else {
-            load_k(kt0, lookup_k(kt0));
-            vblk = lookup_v(kt0);
-            load_v(kt0, vblk);
-            kexp_cur = k_exp();
-            store_k(0, kexp_cur);
-            kblk = n > 1 ? lookup_k(kt0 + 1) : -1;
-            arrive(&bar_qkready[0]);
-            if (n > 1) load_k(kt0 + 1, kblk);
-            vblk = n > 1 ? lookup_v(kt0 + 1) : -1;
-        }
+        if (n > 0) ex_cur = __ldg(reinterpret_cast<const int2 *>(image(__ldg(slots + kt0)) + kImageExpOff));
+        if (n > 1) slot_next = __ldg(slots + kt0 + 1);
 
         for (int j = 0; j < n; ++j) {
             const int kt = kt0 + j, b = j & 1;
-            // S_j ready (QK(j) done; so are all earlier MMAs)
-            ok = wait_one(&bar_qkdone[b], ph(j));
+            // S_j ready (QK(j) done)
+            ok = wait_w(&bar_qkdone[b], ph(j));
             if (!ok) break;
             fence_after_sync();
-            float s[kSCols];
-            tmem_ldn<kSCols>(tbase + tlane + kColS + 64u * b + kSCols * qp, s);
+            float s[kKT];
+            {
+                float h[32];
+                tmem_ld32(tbase + tlane + kColS + 64u * b, h);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) s[i] = h[i];
+                tmem_ld32(tbase + tlane + kColS + 64u * b + 32, h);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) s[32 + i] = h[i];
+            }
             if (j + 2 < n) {
                 // S buffer b may be rewritten: QK(j+2) needs this arrival
                 fence_before_sync();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_u32(&bar_qkready[b]));
             }
-            int kexp;
-            if constexpr (kBulk) {
-                kexp = ex_cur.x;
-            } else {
-                kexp = kexp_cur;
-                if (j + 1 < n) {
-                    // K_{j+1} -> smem (its buffer was read by QK(j-1), done);
-                    // the issue warp starts QK(j+1) while we do the softmax,
-                    // and the K_{j+2} loads overlap it too
-                    kexp_next = k_exp();
-                    store_k((j + 1) & 1, kexp_next);
-                    kblk = j + 2 < n ? lookup_k(kt + 2) : -1;
-                    arrive(&bar_qkready[(j + 1) & 1]);
-                }
-                v_part();
-            }
+            const int kexp = ex_cur.x, vexp = ex_cur.y;
 
             // scores to base-2 units: one exact factor 2^sn (two steps when
             // 2^sn is not a normal f32); mask the keys this row does not see
@@ -667,120 +460,77 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs a, 
             if (!one) {
                 const float sa = pow2f(sn / 2), sb = pow2f(sn - sn / 2);
 #pragma unroll
-                for (int i = 0; i < kSCols; ++i) s[i] = (s[i] * sa) * sb;
+                for (int i = 0; i < kKT; ++i) s[i] = (s[i] * sa) * sb;
             }
-            const int base = kt * kKT + kSCols * qp;
-            if (base + kSCols > klim) {
+            const int base = kt * kKT;
+            if (base + kKT > klim) {
 #pragma unroll
-                for (int i = 0; i < kSCols; ++i) s[i] = base + i < klim ? s[i] : -INFINITY;
+                for (int i = 0; i < kKT; ++i) s[i] = base + i < klim ? s[i] : -INFINITY;
             }
-            float tmax = -INFINITY;
-#pragma unroll
-            for (int i = 0; i < kSCols; ++i) tmax = fmaxf(tmax, s[i]);
-            red[0][tid] = tmax;
-            named_sync(1, kCompute);
-            float row_max = red[0][r0];
-#pragma unroll
-            for (int k = 1; k < kTPR; ++k) row_max = fmaxf(row_max, red[0][r0 + 128 * k]);
-            row_max *= fsc;
-            int vexp;
-            if constexpr (kBulk) {
-                vexp = ex_cur.y;
-            } else {
-                float t = vpart[0];
-#pragma unroll
-                for (int w = 1; w < kComputeWarps; ++w) t = fmaxf(t, vpart[w]);
-                vexp = f16_scale_exp(t);
-            }
+            const float row_max = tree_max(s) * fsc;
             const bool rescale = m_ref != -INFINITY && row_max > m_ref + kRescale;
             const float m_use = (m_ref == -INFINITY || rescale) ? row_max : m_ref;
             // p = 2^(s - m_use): one FFMA (exact scaling, one rounding) and ex2
             const float nm = m_use == -INFINITY ? 0.f : -m_use;
-            float psum = 0.f;
 #pragma unroll
-            for (int i = 0; i < kSCols; ++i) {
-                s[i] = ex2_approx(fmaf(s[i], fsc, nm));
-                psum += s[i];
-            }
+            for (int i = 0; i < kKT; ++i) s[i] = ex2_approx(fmaf(s[i], fsc, nm));
+            const float rowsum = tree_sum(s);
             // C for this tile (the same in every thread)
             const int c_new = j == 0 ? kPExp + vexp : min(cexp, kPExp + vexp);
-            // P / V buffer b free: PV(j-2) done (thread 0 waits before the barrier)
-            if (tid == 0) s_flag = j >= 2 ? static_cast<int>(mbar_wait(smem_u32(&bar_pvdone[b]), ph(j - 2))) : 1;
-            red[1][tid] = psum;
-            const bool any_rescale = named_sync_or(1, kCompute, rescale);
-            if (!s_flag) {
-                ok = false;
-                break;
-            }
-            fence_after_sync();
-            float rowsum = red[1][r0];
-#pragma unroll
-            for (int k = 1; k < kTPR; ++k) rowsum += red[1][r0 + 128 * k];
 
-            // D moves (a row's reference max, or C): every PV so far done first
-            const bool cmove = j > 0 && c_new != cexp;
-            if (any_rescale || cmove) {
-                if (j >= 1) {
-                    ok = wait_one(&bar_pvdone[(j - 1) & 1], ph(j - 1));
-                    if (!ok) break;
-                    fence_after_sync();
-                }
-                // tcgen05.ld / st are warp-collective: the whole warp takes this
-                // branch when any of its rows rescales (the others multiply by 1)
-                // or C moves
-                const float f = rescale ? exp2f(m_ref - m_use) : 1.f;
-                if (cmove || __any_sync(0xffffffffu, rescale)) {
-                    const float fd = mul_pow2(f, c_new - cexp);
-#pragma unroll
-                    for (int c = 0; c < kDCols / 32; ++c) {
-                        float dv[32];
-                        tmem_ld32(tbase + tlane + kColD + kDCols * qp + 32 * c, dv);
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) dv[i] *= fd;
-                        tmem_st32(tbase + tlane + kColD + kDCols * qp + 32 * c, dv);
-                        tmem_st_wait();
-                    }
-                }
-                l_run *= f;
+            // P buffer b free: PV(j-2) done
+            if (j >= 2) {
+                ok = wait_w(&bar_pvdone[b], ph(j - 2));
+                if (!ok) break;
+                fence_after_sync();
             }
-            l_run += rowsum;
+            // D moves (a row's reference max, or C): every PV so far done
+            // first; tcgen05.ld / st are warp-collective, so the whole warp
+            // takes the branch (rows that do not rescale multiply by 2^(C'-C))
+            const bool cmove = j > 0 && c_new != cexp;
+            const float f = rescale ? exp2f(m_ref - m_use) : 1.f;
+            if (cmove || __any_sync(0xffffffffu, rescale)) {
+                ok = wait_w(&bar_pvdone[b ^ 1], ph(j - 1));
+                if (!ok) break;
+                fence_after_sync();
+                const float fd = mul_pow2(f, c_new - cexp);
+#pragma unroll
+                for (int c = 0; c < kHD / 32; ++c) {
+                    float dv[32];
+                    tmem_ld32(tbase + tlane + kColD + 32 * c, dv);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) dv[i] *= fd;
+                    tmem_st32(tbase + tlane + kColD + 32 * c, dv);
+                }
+                tmem_st_wait();
+            }
+            l_run = l_run * f + rowsum;
             m_ref = m_use;
             cexp = c_new;
 
-            // P_j * 2^(C - c) -> TMEM as two f16 pieces (and V_j -> smem); the
-            // issue warp starts PV(j)
+            // P_j * 2^(C - c) -> TMEM as two f16 pieces; the PV warp starts PV(j)
             {
                 const int pe = cexp - vexp;  // <= kPExp
                 const float pf = pe >= -126 ? pow2f(pe) : 0.f;
-                uint32_t p0[kSCols / 2], p1[kSCols / 2];
+                uint32_t p0[32], p1[32];
 #pragma unroll
-                for (int i = 0; i < kSCols / 2; ++i) split_f16x2(s[2 * i] * pf, s[2 * i + 1] * pf, p0[i], p1[i]);
-                const uint32_t tp = tbase + tlane + kColP + 64u * b + (kSCols / 2) * qp;
-                tmem_st8u(tp, p0);
-                tmem_st8u(tp + 32, p1);
+                for (int i = 0; i < 32; ++i) split_f16x2(s[2 * i] * pf, s[2 * i + 1] * pf, p0[i], p1[i]);
+                const uint32_t tp = tbase + tlane + kColP + 64u * b;
+                tmem_st32u(tp, p0);
+                tmem_st32u(tp + 32, p1);
             }
-            if constexpr (!kBulk) store_v(b, vexp);
             arrive(&bar_pvready[b]);
 
-            // the next tile: its exponents (image mode) or its rows (register mode)
-            if constexpr (kBulk) {
-                if (j + 1 < n) {
-                    ex_cur = __ldg(reinterpret_cast<const int2 *>(image(slot_next) + kImageExpOff));
-                    if (j + 2 < n) slot_next = __ldg(slots + kt + 2);
-                }
-            } else {
-                kexp_cur = kexp_next;
-                if (j + 1 < n) {
-                    load_v(kt + 1, vblk);
-                    vblk = j + 2 < n ? lookup_v(kt + 2) : -1;
-                }
-                if (j + 2 < n) load_k(kt + 2, kblk);
+            // the next tile's exponents
+            if (j + 1 < n) {
+                ex_cur = __ldg(reinterpret_cast<const int2 *>(image(slot_next) + kImageExpOff));
+                if (j + 2 < n) slot_next = __ldg(slots + kt + 2);
             }
         }
         // the last PV, then the result: D * 2^-C (exact), divided by l
-        if (ok && n > 0) ok = wait_one(&bar_pvdone[(n - 1) & 1], ph(n - 1));
+        if (ok && n > 0) ok = wait_w(&bar_pvdone[(n - 1) & 1], ph(n - 1));
         if (!ok) {
-            if (tid == 0 && a.err) atomicOr(a.err, 2);
+            if (lane == 0 && a.err) atomicOr(a.err, 2);
         } else {
             fence_after_sync();
             const int h = kvh * G + g;
@@ -789,18 +539,18 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs a, 
             size_t pidx = 0;
             if (direct) {
                 dst = a.out + static_cast<size_t>(rd.q_row0 + (valid ? qi : 0)) * (a.n_heads * kHD) +
-                      static_cast<size_t>(h) * kHD + kDCols * qp;
+                      static_cast<size_t>(h) * kHD;
             } else {
                 const int n_split = (kend_tile + a.split_keys - 1) / a.split_keys;
                 const int stride = tile.stride > 0 ? tile.stride : n_split;
                 pidx = static_cast<size_t>(tile.part0 + (valid ? tq : 0) * stride + tile.split) * a.n_heads + h;
-                dst = a.pacc + pidx * kHD + kDCols * qp;
+                dst = a.pacc + pidx * kHD;
             }
             const float scl = direct ? 1.f / l_run : 1.f;
 #pragma unroll
-            for (int c = 0; c < kDCols / 32; ++c) {
+            for (int c = 0; c < kHD / 32; ++c) {
                 float dv[32];
-                tmem_ld32(tbase + tlane + kColD + kDCols * qp + 32 * c, dv);
+                tmem_ld32(tbase + tlane + kColD + 32 * c, dv);
                 if (valid) {
 #pragma unroll
                     for (int i = 0; i < 32; i += 4)
@@ -809,11 +559,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs a, 
                                         mul_pow2(dv[i + 2], -cexp) * scl, mul_pow2(dv[i + 3], -cexp) * scl);
                 }
             }
-            if (valid) {
-                if (!direct && qp == 0) {
-                    a.pm[pidx] = m_ref;
-                    a.pl[pidx] = l_run;
-                }
+            if (valid && !direct) {
+                a.pm[pidx] = m_ref;
+                a.pl[pidx] = l_run;
             }
         }
     }
@@ -822,61 +570,52 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs a, 
     if (warp == 0) tmem_dealloc(tbase, kTmemCols);
 }
 
-template <int G, class Rows, bool kBulk, bool kLoZero>
-cudaError_t launch_prefill_g(const PrefillArgs &a, const Rows &r, cudaStream_t s) {
+template <int G, bool kLoZero>
+cudaError_t launch_prefill_g(const PrefillArgs &a, cudaStream_t s) {
     static PerDeviceOnce configured;  // the attribute is per function and device
     const cudaError_t ce = configured.run([&]() -> cudaError_t {
-        // setmaxnreg.inc waits until the CTA's pool holds the registers it asks
-        // for, so launch only if the compiled kernel starts with the registers
-        // the split was sized for
-        cudaFuncAttributes fa{};
-        cudaError_t e = cudaFuncGetAttributes(&fa, prefill_tc_kernel<G, Rows, kBulk, kLoZero>);
-        if (e != cudaSuccess) return e;
-        if (fa.numRegs < kLaunchRegs || fa.maxThreadsPerBlock < kThreads)
-            return cudaErrorInvalidConfiguration;
-        e = cudaFuncSetAttribute(prefill_tc_kernel<G, Rows, kBulk, kLoZero>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(kSmemBytes));
-        if (e != cudaSuccess) return e;
-        return cudaSuccess;
+        return cudaFuncSetAttribute(prefill_tc_kernel<G, kLoZero>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    static_cast<int>(kSmemBytes));
     });
     if (ce != cudaSuccess) return ce;
     const long long grid = static_cast<long long>(a.n_tiles) * a.n_kv;
     if (grid <= 0 || grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    prefill_tc_kernel<G, Rows, kBulk, kLoZero><<<static_cast<unsigned>(grid), kThreads, kSmemBytes, s>>>(a, r);
+    prefill_tc_kernel<G, kLoZero><<<static_cast<unsigned>(grid), kThreads, kSmemBytes, s>>>(a);
     return cudaGetLastError();
 }
 
-template <class Rows, bool kBulk, bool kLoZero = false>
-cudaError_t launch_prefill(const PrefillArgs &a, const Rows &r, cudaStream_t s) {
+template <bool kLoZero>
+cudaError_t launch_prefill(const PrefillArgs &a, cudaStream_t s) {
+    if (!a.img || !a.img_tile0 || !a.img_slot) return cudaErrorInvalidValue;
     switch (a.group) {
-        case 1: return launch_prefill_g<1, Rows, kBulk, kLoZero>(a, r, s);
-        case 2: return launch_prefill_g<2, Rows, kBulk, kLoZero>(a, r, s);
-        case 4: return launch_prefill_g<4, Rows, kBulk, kLoZero>(a, r, s);
-        case 8: return launch_prefill_g<8, Rows, kBulk, kLoZero>(a, r, s);
+        case 1: return launch_prefill_g<1, kLoZero>(a, s);
+        case 2: return launch_prefill_g<2, kLoZero>(a, s);
+        case 4: return launch_prefill_g<4, kLoZero>(a, s);
+        case 8: return launch_prefill_g<8, kLoZero>(a, s);
         default: return cudaErrorInvalidValue;
     }
 }
 
 // ----------------------------------------------------------- split pass ----
 //
-// One CTA per (row, 64-key tile, kv head): the tile's K and V rows (read once
-// through the page table, widened to f32, an fp8 pool's scale applied; zero
-// past the row's keys) go to shared memory, and the block finds the largest
-// magnitude of each; then every 16-byte chunk of the four planes is written in
-// the prefill kernel's shared-memory order, chunk by chunk (coalesced): eight
-// values times the tile's power of two, split into their two f16 pieces.  The
-// two tile exponents (K, V) follow the planes.  The V rows are kept 129
-// floats apart so that reading them transposed has no bank conflicts.
+// One CTA per (row, 64-key tile, kv head): the tile's K and V rows (read once,
+// through the page table or from a contiguous pair, widened to f32, an fp8
+// pool's scale applied; zero past the row's keys) go to shared memory, and
+// the block finds the largest magnitude of each; then every 16-byte chunk of
+// the four planes is written in the prefill kernel's shared-memory order,
+// chunk by chunk (coalesced): eight values times the tile's power of two,
+// split into their two f16 pieces.  The two tile exponents (K, V) follow the
+// planes.  The V rows are kept 129 floats apart so that reading them
+// transposed has no bank conflicts.
 constexpr int kSplitRawFloats = kKT * kHD + kKT * (kHD + 1);
 
-template <class E>
-__global__ void __launch_bounds__(256) split_kernel(SplitArgs p, PagedRowsP<E> rows_of) {
+template <class Rows>
+__global__ void __launch_bounds__(256) split_kernel(SplitArgs p, Rows rows_of) {
+    using E = typename Rows::Elem;
     // a bf16 / fp8 value times a power of two is exact in f16 (but for
     // values more than 2^28 below the tile's largest): the piece-1 planes are
     // not written
     constexpr bool kLoZero = !std::is_same<E, float>::value;
-    const float p_scale = rows_of.a.kv_scale;
     extern __shared__ __align__(16) float raw[];
     __shared__ float wmax[2][8];
     float *rk = raw;              // [64][128]
@@ -902,7 +641,7 @@ __global__ void __launch_bounds__(256) split_kernel(SplitArgs p, PagedRowsP<E> r
                 kx = ldg4(rows_of.k_row(b, pos, kvh) + 4 * ch);
                 vx = ldg4(rows_of.v_row(b, pos, kvh) + 4 * ch);
                 if constexpr (std::is_same<E, fp8>::value) {
-                    const float sc = p_scale;  // power of two: exact
+                    const float sc = rows_of.scale();  // power of two: exact
                     kx = make_float4(kx.x * sc, kx.y * sc, kx.z * sc, kx.w * sc);
                     vx = make_float4(vx.x * sc, vx.y * sc, vx.z * sc, vx.w * sc);
                 }
@@ -943,8 +682,14 @@ __global__ void __launch_bounds__(256) split_kernel(SplitArgs p, PagedRowsP<E> r
             const float *src = rk + r * kHD + kb * 64 + lc * 8;
             const float4 a0 = *reinterpret_cast<const float4 *>(src);
             const float4 a1 = *reinterpret_cast<const float4 *>(src + 4);
-            x[0] = a0.x; x[1] = a0.y; x[2] = a0.z; x[3] = a0.w;
-            x[4] = a1.x; x[5] = a1.y; x[6] = a1.z; x[7] = a1.w;
+            x[0] = a0.x;
+            x[1] = a0.y;
+            x[2] = a0.z;
+            x[3] = a0.w;
+            x[4] = a1.x;
+            x[5] = a1.y;
+            x[6] = a1.z;
+            x[7] = a1.w;
             split_chunk(x, ks, c0, c1);
             *reinterpret_cast<uint4 *>(out + q * 16) = c0;
             if constexpr (!kLoZero) *reinterpret_cast<uint4 *>(out + kImagePlane + q * 16) = c1;
@@ -962,40 +707,39 @@ __global__ void __launch_bounds__(256) split_kernel(SplitArgs p, PagedRowsP<E> r
     if (threadIdx.x == 0) *reinterpret_cast<int2 *>(out + kImageExpOff) = make_int2(kexp, vexp);
 }
 
-template <class E>
-cudaError_t launch_split(const SplitArgs &a, const PagedRowsP<E> &r, cudaStream_t s) {
+template <class Rows>
+cudaError_t launch_split(const SplitArgs &a, const Rows &r, cudaStream_t s) {
     constexpr size_t smem = kSplitRawFloats * sizeof(float);
     static PerDeviceOnce configured;  // the attribute is per function and device
     const cudaError_t ce = configured.run([&]() -> cudaError_t {
-        cudaError_t e = cudaFuncSetAttribute(split_kernel<E>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(smem));
-        if (e != cudaSuccess) return e;
-        return cudaSuccess;
+        return cudaFuncSetAttribute(split_kernel<Rows>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    static_cast<int>(smem));
     });
     if (ce != cudaSuccess) return ce;
     const long long grid = static_cast<long long>(a.n_items) * a.n_kv;
     if (grid <= 0 || grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    split_kernel<E><<<static_cast<unsigned>(grid), 256, smem, s>>>(a, r);
+    split_kernel<Rows><<<static_cast<unsigned>(grid), 256, smem, s>>>(a, r);
     return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_prefill_paged(const PrefillArgs &a, const PagedAddr &addr, cudaStream_t s) {
-    // the operands come as images (whatever the pool element): one instantiation
-    if (!a.img || !a.img_tile0) return cudaErrorInvalidValue;
-    if (a.lo_zero) return launch_prefill<PagedRowsP<float>, true, true>(a, PagedRowsP<float>{addr}, s);
-    return launch_prefill<PagedRowsP<float>, true, false>(a, PagedRowsP<float>{addr}, s);
+cudaError_t launch_prefill_paged(const PrefillArgs &a, const PagedAddr &, cudaStream_t s) {
+    return a.lo_zero ? launch_prefill<true>(a, s) : launch_prefill<false>(a, s);
 }
 
-cudaError_t launch_prefill_contig(const PrefillArgs &a, const ContigAddr &addr, cudaStream_t s) {
-    return launch_prefill<ContigRowsP, false>(a, ContigRowsP{addr}, s);
+cudaError_t launch_prefill_contig(const PrefillArgs &a, const ContigAddr &, cudaStream_t s) {
+    return launch_prefill<false>(a, s);
 }
 
 cudaError_t launch_split_paged(const SplitArgs &a, const PagedAddr &addr, cudaStream_t s) {
     if (addr.fp8) return launch_split(a, PagedRowsP<fp8>{addr}, s);
     if (addr.bf16) return launch_split(a, PagedRowsP<bf16>{addr}, s);
     return launch_split(a, PagedRowsP<float>{addr}, s);
+}
+
+cudaError_t launch_split_contig(const SplitArgs &a, const ContigAddr &addr, cudaStream_t s) {
+    return launch_split(a, ContigRowsP{addr}, s);
 }
 
 }  // namespace pkv

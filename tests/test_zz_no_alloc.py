@@ -8,8 +8,10 @@ in a row (each finds the previous call's contents in the array), and the
 oracle within the same tolerance.  The calls cover both kernels the entry
 point dispatches: split-K decode (with split partials and their merge in the
 array) and the tensor-core kernel for rows of 32 or more queries (its tiles'
-descriptors and, past 16 384 keys, its split partials in the array), the
-latter both before and after a call that left other partials behind.
+descriptors, the split pass's operand images and the kernel's reads of them
+in the array), the latter both before and after a call that left other
+partials behind; and a 32-query row whose images would not fit in the array,
+which goes to split-K decode instead.
 
 This file is collected last so that a run stopping at the first failure has
 run every other test before it; it also passes alone in a fresh process.
@@ -40,10 +42,11 @@ def _case(n_q, past, H, KV, hd, causal, seed):
 def test_no_alloc_matches_allocating_entry_point_on_two_calls():
     stream = torch.cuda.current_stream()
     cases = [
-        _case(32, 16500, 32, 8, 128, 1, 4),  # tensor-core kernel, 2 key splits + merge
+        _case(32, 16500, 32, 8, 128, 1, 4),  # images would not fit: split-K decode, splits + merge
         _case(1, 3000, 32, 8, 128, 1, 1),    # several splits + merge on the head_dim-128 kernel
         _case(64, 1024, 32, 8, 128, 1, 5),   # tensor-core kernel after stale decode partials
         _case(3, 40, 4, 2, 8, 1, 2),         # one split, generic kernel, stale scratch from call 1
+        _case(40, 1500, 32, 8, 128, 0, 6),   # tensor-core kernel, non-causal, ragged tail, 12.6 MB of images
     ]
     for i, (Q, Kc, Vc, n_q, tk, H, KV, hd, causal, scale) in enumerate(cases):
         ref = torch.empty(n_q, H * hd, device="cuda")
