@@ -87,8 +87,9 @@ typedef void *pkv_stream_t; /* cudaStream_t */
 /* fp8 e4m3 storage (no counterpart on the pages): every K/V row is stored as
  * e4m3(x / scale) -- nearest, ties to even, saturated to +-448 -- and read as
  * that value times scale; scale is a power of two (pkv_pool_set_kv_scale,
- * default 1), so the read values are exact in f32 and tf32 and only the
- * storage rounding differs from f32.  Quarters the pool's bytes.  Needs kv_dim
+ * default 1), so the read values are exact in f32 (and, times a tile's
+ * power of two, in the tensor-core kernel's f16) and only the storage
+ * rounding differs from f32.  Quarters the pool's bytes.  Needs kv_dim
  * % 4 == 0 (% 16 with head_dim 128).  As for bf16, the fused append rounds
  * the new rows the same way, and the contiguous twin stays f32. */
 #define PKV_POOL_FP8 4u
@@ -145,8 +146,9 @@ PKV_API int pkv_pool_last_work(const pkv_pool *pool, int64_t *out, int32_t cap);
 
 /* Operand-image cache (no counterpart on the pages; off by default).  The
  * tensor-core launches read every 64-key tile they attend as an image of
- * tf32 hi/lo planes (n_kv_heads x 128 KiB per tile, head_dim 128), which a
- * split pass builds from the pool.  With the cache on, images of tiles whose
+ * f16 pieces (the tile's values times a power of two, split into two f16
+ * planes; n_kv_heads x 64 KiB per tile, head_dim 128), which a split pass
+ * builds from the pool.  With the cache on, images of tiles whose
  * pages have not been written since are kept across calls in up to
  * max_bytes of device memory (least recently used first out) instead of
  * being rebuilt: a chunked prefill then splits each key tile once rather

@@ -58,7 +58,6 @@ constexpr uint32_t kTmemCols = 512;
 // (buffer b: piece 0 at 192 + 64b, piece 1 32 columns on), D [384,512)
 constexpr uint32_t kColQ0 = 0, kColS = 64, kColP = 192, kColD = 384;
 constexpr int kComputeWarps = 4;          // one thread per tile row
-constexpr int kCompute = 32 * kComputeWarps;
 constexpr int kWarpQK = 4, kWarpCopy = 5, kWarpPV = 6;
 constexpr int kThreads = 32 * 7;
 constexpr float kRescale = 8.f;           // lazy-rescale threshold (base 2)

@@ -320,7 +320,7 @@ def test_launch_accounting_and_profiling():
 @pytest.mark.gpu
 @pytest.mark.parametrize("H,KV", [(32, 8), (16, 8), (8, 8), (64, 8)], ids=["g4", "g2", "g1", "g8"])
 def test_prefill_tensor_core_rows(H, KV, split_keys):
-    """Rows with n_q >= 32 take the tcgen05 3xTF32 kernel: tiles of 128/G
+    """Rows with n_q >= 32 take the tcgen05 kind::f16 kernel: tiles of 128/G
     tokens, ragged last tiles, an empty history, and rows long enough to be
     cut into several key splits (split size 16 x 32 = 512 keys) and merged."""
     split_keys(32)
