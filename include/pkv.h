@@ -253,7 +253,10 @@ PKV_API int pkv_append_layer(pkv_seq *seq, int32_t layer, const float *K_new, co
  * Q, out: device [n_tokens, n_heads*head_dim]; K_new, V_new: device
  * [n_tokens, n_kv_heads*head_dim]; n_kv_heads*head_dim must equal the pool's
  * kv_dim, head_dim <= 256.  Checks, in order: sizes <= 0 -> PKV_ERR_BAD_DIM;
- * grouping -> PKV_ERR_BAD_GQA; NULL seq or rows not ensured -> PKV_ERR_SEQ. */
+ * grouping -> PKV_ERR_BAD_GQA; NULL seq or rows not ensured -> PKV_ERR_SEQ.
+ * Range: the kernels sum p * V in f32 with p taken relative to a running
+ * maximum (each p at most 256), so results are finite while 256 x (visible
+ * keys) x max|V| < 3.4e38: max|V| up to about 1e30 for a million keys. */
 PKV_API int pkv_attn_with_paged(const float *Q, const float *K_new, const float *V_new,
                         int32_t n_tokens, int32_t n_heads, int32_t n_kv_heads, int32_t head_dim,
                         pkv_seq *seq, int32_t layer, int32_t causal, float scale, float *out);

@@ -526,7 +526,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs a) 
                 if (j + 2 < n) slot_next = __ldg(slots + kt + 2);
             }
         }
-        // the last PV, then the result: D * 2^-C (exact), divided by l
+        // the last PV, then the result: D / l, then * 2^-C (exact); in that
+        // order the output does not overflow where D * 2^-C (up to l times it)
+        // would
         if (ok && n > 0) ok = wait_w(&bar_pvdone[(n - 1) & 1], ph(n - 1));
         if (!ok) {
             if (lane == 0 && a.err) atomicOr(a.err, 2);
@@ -554,8 +556,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs a) 
 #pragma unroll
                     for (int i = 0; i < 32; i += 4)
                         *reinterpret_cast<float4 *>(dst + 32 * c + i) =
-                            make_float4(mul_pow2(dv[i], -cexp) * scl, mul_pow2(dv[i + 1], -cexp) * scl,
-                                        mul_pow2(dv[i + 2], -cexp) * scl, mul_pow2(dv[i + 3], -cexp) * scl);
+                            make_float4(mul_pow2(dv[i] * scl, -cexp), mul_pow2(dv[i + 1] * scl, -cexp),
+                                        mul_pow2(dv[i + 2] * scl, -cexp), mul_pow2(dv[i + 3] * scl, -cexp));
                 }
             }
             if (valid && !direct) {
