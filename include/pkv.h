@@ -308,8 +308,13 @@ PKV_API int pkv_attn_batch_host(pkv_seq *const *seqs, int32_t M, const int32_t *
  * gate in "nx_paged_kv_gate.nx source"): the same kernels over a contiguous
  * history.  Kc, Vc: device [total_k, n_kv_heads*head_dim], already holding the
  * n_q new rows at the end; Q, out: device [n_q, n_heads*head_dim].  For the
- * same history it returns the paged path's output bit for bit.  Failures the
- * kernels find on the device are read by pkv_contiguous_sync_error. */
+ * same history it returns the paged path's output bit for bit.  Its scratch
+ * (work list, split-K partials and, when the row takes the tensor-core kernel
+ * (n_q >= 32, head_dim 128), the operand images of its keys: 64 KiB per
+ * 64-key tile and kv head) comes from a stream-ordered memory pool and is
+ * released on the stream after the launches; PKV_ERR_CUDA if it cannot be
+ * allocated.  Failures the kernels find on the device are read by
+ * pkv_contiguous_sync_error. */
 PKV_API int pkv_attn_contiguous(const float *Q, const float *Kc, const float *Vc, int32_t n_q,
                         int32_t total_k, int32_t n_heads, int32_t n_kv_heads, int32_t head_dim,
                         int32_t causal, float scale, float *out, pkv_stream_t stream);
