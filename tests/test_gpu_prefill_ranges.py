@@ -13,7 +13,9 @@ spread over 2^-20 .. 2^2 (near-uniform rows beside sharp ones, lazy max
 rescales); all-zero K and V tiles and query rows; and tiles whose largest
 magnitudes sit far out in f32's range, subnormals included (the
 exponents' clamps).  Each case also runs through a pool, which must return the
-contiguous entry point's bits.
+contiguous entry point's bits.  On bf16 / fp8 pools (the kernel's one-piece
+K/V images) K and V tiles spread over 2^-6 .. 2^2 and 2^-8 .. 2^8 per kv
+head, against the oracle over the rounded history.
 """
 import math
 import zlib
@@ -120,3 +122,55 @@ def test_prefill_far_from_unit_scale(name, n_q, total_k, causal):
     assert_close(out.cpu().numpy(), exp, np.abs(V).max(), name)
     out_p = _paged(Q, K, V, n_q, total_k, causal, scale)
     assert bits_equal(out_p, out), name + ": paged != contiguous"
+
+
+NARROW = {
+    "bf16": (torch.bfloat16, 1.0, lambda x, s: oracle.round_bf16(x)),
+    "fp8": (torch.float8_e4m3fn, 1.0, lambda x, s: oracle.round_e4m3(x, s)),
+    "fp8s": (torch.float8_e4m3fn, 0.25, lambda x, s: oracle.round_e4m3(x, s)),
+}
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("fmt", ["bf16", "fp8", "fp8s"])
+def test_prefill_narrow_pool_ranges(fmt):
+    """bf16 / fp8 pools take the kernel's one-piece K/V images (a pool value
+    times its tile's power of two is an f16 value); here K tiles spread over
+    2^-6 .. 2^2 and V tiles over 2^-8 .. 2^8 per kv head (on fp8 pools the
+    largest saturate and the smallest fall into e4m3's subnormals, exactly as
+    the oracle's rounding has them), against the oracle over the rounded
+    history at the tests' tolerance."""
+    dtype, kv_scale, rnd = NARROW[fmt]
+    rng = np.random.default_rng(zlib.crc32(fmt.encode()) + 7)
+    past, n_q, bs = 1000, 96, 16
+    total_k = past + n_q
+    kv_dim = KV * HD
+    scale = float(np.float32(1.0 / math.sqrt(HD)))
+    K = rng.standard_normal((total_k, kv_dim)).astype(np.float32)
+    V = rng.standard_normal((total_k, kv_dim)).astype(np.float32)
+    for a, b in _tiles(total_k):
+        for h in range(KV):
+            K[a:b, h * HD:(h + 1) * HD] *= np.float32(2.0 ** rng.integers(-6, 3))
+            V[a:b, h * HD:(h + 1) * HD] *= np.float32(2.0 ** rng.integers(-8, 9))
+    Q = rng.standard_normal((n_q, H * HD)).astype(np.float32)
+    # the oracle's rounding (saturating at +-448 x scale on fp8 pools, as the
+    # library's store does); the history is written as those exact values,
+    # since torch's e4m3fn cast turns magnitudes beyond 448 into NaN
+    Kr, Vr = rnd(K, kv_scale), rnd(V, kv_scale)
+    blocks = -(-total_k // bs)
+    pool = GpuPool(blocks + 4, 1, kv_dim, bs, max_seqs=2, max_blocks=blocks + 1, shuffle_seed=3,
+                   dtype=dtype, kv_scale=kv_scale)
+    try:
+        s = pool.new_seq(total_k)
+        pool.grow(s, past)
+        pool.write_history(s, 0, torch.from_numpy(Kr[:past]), torch.from_numpy(Vr[:past]))
+        pkv.check(pkv.pkv_ensure_append_batch([s], [n_q]))
+        out = torch.empty(n_q, H * HD, device="cuda")
+        Qd, Kd, Vd = (torch.from_numpy(np.ascontiguousarray(x)).cuda() for x in (Q, K[past:], V[past:]))
+        pkv.check(pkv.pkv_attn_batch([s], [n_q], Qd, Kd, Vd, H, KV, HD, 0, 1, scale, out))
+        pool.check_no_device_error()
+        rc, exp = oracle.attend(Q, Kr, Vr, n_q, total_k, H, KV, HD, 1, scale)
+        assert rc == 0
+        assert_close(out.cpu().numpy(), exp, np.abs(Vr).max(), fmt)
+    finally:
+        pool.close()
