@@ -599,16 +599,17 @@ cudaError_t launch_prefill(const PrefillArgs &a, cudaStream_t s) {
 
 // ----------------------------------------------------------- split pass ----
 //
-// One CTA per (row, 64-key tile, kv head): the tile's K and V rows (read once,
-// through the page table or from a contiguous pair, widened to f32, an fp8
-// pool's scale applied; zero past the row's keys) go to shared memory, and
-// the block finds the largest magnitude of each; then every 16-byte chunk of
-// the four planes is written in the prefill kernel's shared-memory order,
-// chunk by chunk (coalesced): eight values times the tile's power of two,
-// split into their two f16 pieces.  The two tile exponents (K, V) follow the
-// planes.  The V rows are kept 129 floats apart so that reading them
-// transposed has no bank conflicts.
-constexpr int kSplitRawFloats = kKT * kHD + kKT * (kHD + 1);
+// Two CTAs per (row, 64-key tile, kv head), one for K and one for V: the
+// tile's rows of that operand (read once, through the page table or from a
+// contiguous pair, widened to f32, an fp8 pool's scale applied; zero past the
+// row's keys) go to shared memory, and the block finds their largest
+// magnitude; then every 16-byte chunk of the operand's two planes is written
+// in the prefill kernel's shared-memory order, chunk by chunk (coalesced):
+// eight values times the tile's power of two, split into their two f16
+// pieces, and the operand's exponent after the planes.  V rows are kept 129
+// floats apart so that reading them transposed has no bank conflicts.  One
+// operand per CTA halves the staging, so twice as many CTAs share an SM.
+constexpr int kSplitRawFloats = kKT * (kHD + 1);
 
 template <class Rows>
 __global__ void __launch_bounds__(256) split_kernel(SplitArgs p, Rows rows_of) {
@@ -618,69 +619,63 @@ __global__ void __launch_bounds__(256) split_kernel(SplitArgs p, Rows rows_of) {
     // not written
     constexpr bool kLoZero = !std::is_same<E, float>::value;
     extern __shared__ __align__(16) float raw[];
-    __shared__ float wmax[2][8];
-    float *rk = raw;              // [64][128]
-    float *rv = raw + kKT * kHD;  // [64][129]
-    const int it = blockIdx.x / p.n_kv;
-    const int kvh = blockIdx.x - it * p.n_kv;
+    __shared__ float wmax[8];
+    const int part = blockIdx.x & 1;  // 0: K, 1: V
+    const int ik = blockIdx.x >> 1;
+    const int it = ik / p.n_kv;
+    const int kvh = ik - it * p.n_kv;
     const SplitItem t = p.items[it];
     const RowDesc rd = p.rows[t.row];
     const int total_k = rd.past_len + rd.n_q;
     const int key0 = t.kt * kKT;
-    float km = 0.f, vm = 0.f;
+    const int ld = part ? kHD + 1 : kHD;  // row pitch in shared memory
+    float mx = 0.f;
     // 256 threads x 8 passes = 64 keys x 32 float4 chunks; unrolled, so that
-    // a thread's 16 row loads are in flight together
+    // a thread's 8 row loads are in flight together
     static_assert(kKT * (kHD / 4) == 256 * 8, "one tile per 8 passes of 256 threads");
 #pragma unroll
     for (int pass = 0; pass < 8; ++pass) {
         const int i = threadIdx.x + 256 * pass;
         const int key = i >> 5, ch = i & 31, pos = key0 + key;
-        float4 kx = make_float4(0.f, 0.f, 0.f, 0.f), vx = kx;
+        float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
         if (pos < total_k) {
             const int b = rows_of.checked(rows_of.entry(rd.slot, pos, p.err), p.err);
             if (b >= 0) {
-                kx = ldg4(rows_of.k_row(b, pos, kvh) + 4 * ch);
-                vx = ldg4(rows_of.v_row(b, pos, kvh) + 4 * ch);
+                x = ldg4((part ? rows_of.v_row(b, pos, kvh) : rows_of.k_row(b, pos, kvh)) + 4 * ch);
                 if constexpr (std::is_same<E, fp8>::value) {
                     const float sc = rows_of.scale();  // power of two: exact
-                    kx = make_float4(kx.x * sc, kx.y * sc, kx.z * sc, kx.w * sc);
-                    vx = make_float4(vx.x * sc, vx.y * sc, vx.z * sc, vx.w * sc);
+                    x = make_float4(x.x * sc, x.y * sc, x.z * sc, x.w * sc);
                 }
             }
         }
-        km = absmax4(km, kx);
-        vm = absmax4(vm, vx);
-        *reinterpret_cast<float4 *>(rk + key * kHD + 4 * ch) = kx;
-        float *vd = rv + key * (kHD + 1) + 4 * ch;
-        vd[0] = vx.x;
-        vd[1] = vx.y;
-        vd[2] = vx.z;
-        vd[3] = vx.w;
+        mx = absmax4(mx, x);
+        float *d = raw + key * ld + 4 * ch;
+        if (part) {
+            d[0] = x.x;
+            d[1] = x.y;
+            d[2] = x.z;
+            d[3] = x.w;
+        } else {
+            *reinterpret_cast<float4 *>(d) = x;
+        }
     }
-    km = warp_max(km);
-    vm = warp_max(vm);
-    if ((threadIdx.x & 31) == 0) {
-        wmax[0][threadIdx.x >> 5] = km;
-        wmax[1][threadIdx.x >> 5] = vm;
-    }
+    mx = warp_max(mx);
+    if ((threadIdx.x & 31) == 0) wmax[threadIdx.x >> 5] = mx;
     __syncthreads();
-    km = wmax[0][0];
-    vm = wmax[1][0];
+    mx = wmax[0];
 #pragma unroll
-    for (int w = 1; w < 8; ++w) {
-        km = fmaxf(km, wmax[0][w]);
-        vm = fmaxf(vm, wmax[1][w]);
-    }
-    const int kexp = f16_scale_exp(km), vexp = f16_scale_exp(vm);
-    const float ks = pow2f(kexp), vs = pow2f(vexp);
-    unsigned char *out = p.img + (static_cast<size_t>(t.slot) * p.n_kv + kvh) * kImageBytes;
+    for (int w = 1; w < 8; ++w) mx = fmaxf(mx, wmax[w]);
+    const int ex = f16_scale_exp(mx);
+    const float sc = pow2f(ex);
+    unsigned char *out = p.img + (static_cast<size_t>(t.slot) * p.n_kv + kvh) * kImageBytes +
+                         static_cast<size_t>(part) * 2 * kImagePlane;
     for (int q = threadIdx.x; q < static_cast<int>(kImagePlane / 16); q += blockDim.x) {
         uint4 c0, c1;
         float x[8];
-        {
+        if (part == 0) {
             // K: k-block q >> 9 (64 dims), key row (q >> 3) & 63, swizzled chunk q & 7
             const int kb = q >> 9, r = (q >> 3) & 63, lc = (q & 7) ^ (r & 7);
-            const float *src = rk + r * kHD + kb * 64 + lc * 8;
+            const float *src = raw + r * kHD + kb * 64 + lc * 8;
             const float4 a0 = *reinterpret_cast<const float4 *>(src);
             const float4 a1 = *reinterpret_cast<const float4 *>(src + 4);
             x[0] = a0.x;
@@ -691,21 +686,21 @@ __global__ void __launch_bounds__(256) split_kernel(SplitArgs p, Rows rows_of) {
             x[5] = a1.y;
             x[6] = a1.z;
             x[7] = a1.w;
-            split_chunk(x, ks, c0, c1);
-            *reinterpret_cast<uint4 *>(out + q * 16) = c0;
-            if constexpr (!kLoZero) *reinterpret_cast<uint4 *>(out + kImagePlane + q * 16) = c1;
-        }
-        {
+        } else {
             // V^T: dim row q >> 3, swizzled chunk q & 7 (8 keys)
             const int d = q >> 3, k0 = ((q & 7) ^ (d & 7)) * 8;
 #pragma unroll
-            for (int j = 0; j < 8; ++j) x[j] = rv[(k0 + j) * (kHD + 1) + d];
-            split_chunk(x, vs, c0, c1);
-            *reinterpret_cast<uint4 *>(out + 2 * kImagePlane + q * 16) = c0;
-            if constexpr (!kLoZero) *reinterpret_cast<uint4 *>(out + 3 * kImagePlane + q * 16) = c1;
+            for (int j = 0; j < 8; ++j) x[j] = raw[(k0 + j) * (kHD + 1) + d];
         }
+        split_chunk(x, sc, c0, c1);
+        *reinterpret_cast<uint4 *>(out + q * 16) = c0;
+        if constexpr (!kLoZero) *reinterpret_cast<uint4 *>(out + kImagePlane + q * 16) = c1;
     }
-    if (threadIdx.x == 0) *reinterpret_cast<int2 *>(out + kImageExpOff) = make_int2(kexp, vexp);
+    if (threadIdx.x == 0) {
+        int32_t *e = reinterpret_cast<int32_t *>(p.img + (static_cast<size_t>(t.slot) * p.n_kv + kvh) * kImageBytes +
+                                                 kImageExpOff);
+        e[part] = ex;
+    }
 }
 
 template <class Rows>
@@ -717,7 +712,7 @@ cudaError_t launch_split(const SplitArgs &a, const Rows &r, cudaStream_t s) {
                                     static_cast<int>(smem));
     });
     if (ce != cudaSuccess) return ce;
-    const long long grid = static_cast<long long>(a.n_items) * a.n_kv;
+    const long long grid = static_cast<long long>(a.n_items) * a.n_kv * 2;
     if (grid <= 0 || grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     split_kernel<Rows><<<static_cast<unsigned>(grid), 256, smem, s>>>(a, r);
     return cudaGetLastError();
