@@ -439,10 +439,17 @@ bool can_append(const pkv_seq *s, int32_t n) {
     return true;
 }
 
+// The second tile of a CTA that has only one.
+constexpr PrefillTile kNoTile{-1, 0, 0, -1, 0};
+
+int64_t count_tiles(const std::vector<PrefillTile> &v) {
+    return std::count_if(v.begin(), v.end(), [](const PrefillTile &t) { return t.row >= 0; });
+}
+
 // Work list for a set of rows.  Rows with many queries (and a supported
 // shape) become tensor-core prefill tiles; every other query becomes split-K
 // decode units, listed longest first; prefill tiles are listed latest-first
-// (the latest queries see the most keys).
+// (the latest queries see the most keys), two per tensor-core CTA.
 struct WorkList {
     std::vector<UnitDesc> units;
     std::vector<PrefillTile> tiles;
@@ -515,7 +522,7 @@ int32_t prefix_split_keys(const std::vector<Cascade> &cas, int32_t group, int32_
     int64_t per_split = 0;  // CTAs per split, all runs
     int32_t lp = 0;
     for (const Cascade &c : cas) {
-        per_split += static_cast<int64_t>(ceil_div(c.n, TQ)) * n_kv;
+        per_split += static_cast<int64_t>(ceil_div(ceil_div(c.n, TQ), 2)) * n_kv;  // tile pairs
         lp = std::max(lp, c.Lp);
     }
     const int32_t tiles = ceil_div(lp, kKeyTile);
@@ -559,10 +566,14 @@ std::vector<char> add_cascades(std::vector<RowDesc> &rows, const std::vector<Cas
         rows.push_back(vr);
         // split-major: the query tiles that read the same prefix keys (the
         // same operand images) are neighbours in the grid, so they run
-        // together and share those images in L2
+        // together and share those images in L2; two neighbouring tiles per
+        // CTA (the second absent past the last tile)
         for (int32_t sp = 0; sp < n_pref; ++sp)
-            for (int32_t q0 = 0; q0 < c.n; q0 += TQ)
+            for (int32_t q0 = 0; q0 < c.n; q0 += 2 * TQ) {
                 w.ctiles.push_back({vi, q0, sp, part0 + q0 * stride, stride});
+                const int32_t q1 = q0 + TQ;
+                w.ctiles.push_back(q1 < c.n ? PrefillTile{vi, q1, sp, part0 + q1 * stride, stride} : kNoTile);
+            }
         for (int32_t t = 0; t < c.n; ++t) {
             const int32_t r = c.r0 + t;
             RowDesc &rd = rows[r];
@@ -612,17 +623,36 @@ void build_work(std::vector<RowDesc> &rows, int causal, int32_t S, int32_t head_
         const RowDesc &rd = rows[r];
         const int32_t total_k = rd.past_len + rd.n_q;
         if (tc_shape && rd.n_q >= kPrefillMinQueries) {
+            // query tiles latest first (part0 -1: one split, written directly)
+            struct QTile {
+                int32_t q0, ns, part0;
+            };
+            std::vector<QTile> qt;
             for (int32_t q0 = ((rd.n_q - 1) / TQ) * TQ; q0 >= 0; q0 -= TQ) {
                 const int32_t nv = std::min(TQ, rd.n_q - q0);
                 const int32_t kend = causal ? total_k - rd.n_q + q0 + nv : total_k;
                 const int32_t ns = ceil_div(kend, Sp);
-                if (ns == 1) {
-                    w.tiles.push_back({r, q0, 0, -1});
-                } else {
-                    const int32_t part0 = static_cast<int32_t>(w.n_part);
+                int32_t part0 = -1;
+                if (ns > 1) {
+                    part0 = static_cast<int32_t>(w.n_part);
                     w.n_part += static_cast<int64_t>(nv) * ns;
-                    for (int32_t s = 0; s < ns; ++s) w.tiles.push_back({r, q0, s, part0});
                     for (int32_t t = 0; t < nv; ++t) w.pmerges.push_back({r, q0 + t, part0 + t * ns, ns});
+                }
+                qt.push_back({q0, ns, part0});
+            }
+            // neighbouring tiles in pairs, one CTA per pair and split (the
+            // pair's tiles of one split share every key tile); a present tile
+            // first, the second absent where a tile has no partner
+            for (size_t i = 0; i < qt.size(); i += 2) {
+                const QTile &x = qt[i];
+                const QTile *y = i + 1 < qt.size() ? &qt[i + 1] : nullptr;
+                const int32_t ns = std::max(x.ns, y ? y->ns : 0);
+                for (int32_t sp = 0; sp < ns; ++sp) {
+                    PrefillTile u = sp < x.ns ? PrefillTile{r, x.q0, sp, x.part0} : kNoTile;
+                    PrefillTile v = y && sp < y->ns ? PrefillTile{r, y->q0, sp, y->part0} : kNoTile;
+                    if (u.row < 0) std::swap(u, v);
+                    w.tiles.push_back(u);
+                    w.tiles.push_back(v);
                 }
             }
             continue;
@@ -839,8 +869,8 @@ int run_layer(pkv_seq *const *seqs, int32_t M, const int32_t *n_q, const float *
         }
         for (const Cascade &c : cas) ppairs += static_cast<int64_t>(c.n) * c.Lp;
         const int64_t vals[PKV_WORK_FIELDS] = {static_cast<int64_t>(w.units.size()),
-                                               static_cast<int64_t>(w.tiles.size()),
-                                               static_cast<int64_t>(w.ctiles.size()),
+                                               count_tiles(w.tiles),
+                                               count_tiles(w.ctiles),
                                                static_cast<int64_t>(w.merges.size()),
                                                pairs, ppairs, fuse ? 1 : 0, 0, 0, Sp};
         std::copy(vals, vals + PKV_WORK_FIELDS, p->last_work);
@@ -868,8 +898,10 @@ int run_layer(pkv_seq *const *seqs, int32_t M, const int32_t *n_q, const float *
             next += ceil_div(rows[r].past_len + rows[r].n_q, kKeyTile);
             order.push_back(r);
         };
-        for (const PrefillTile &t : w.tiles) need(t.row);
-        for (const PrefillTile &t : w.ctiles) need(t.row);
+        for (const PrefillTile &t : w.tiles)
+            if (t.row >= 0) need(t.row);
+        for (const PrefillTile &t : w.ctiles)
+            if (t.row >= 0) need(t.row);
         img_slot.resize(next);
         ImageCache &ic = p->icache;
         cached = ic.n_slots >= next && ic.slot_bytes == static_cast<size_t>(n_kv_heads) * kImageBytes;

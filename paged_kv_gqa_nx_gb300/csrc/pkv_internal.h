@@ -100,6 +100,8 @@ struct AttnArgs {
 // otherwise query q0 + t's partial for split s is record
 // part0 + t*stride + s, stride = n_split unless the tile sets it (a prefix
 // pass leaves room for the decode splits that follow each query's prefix).
+// The kernel takes tiles in pairs, one pair per CTA: tiles 2i and 2i + 1 share
+// the row and the split; row < 0 marks an absent second tile.
 struct PrefillTile {
     int32_t row, q0, split, part0;
     int32_t stride = 0;
@@ -110,7 +112,7 @@ struct PrefillArgs {
     float *out;
     const RowDesc *rows;
     const PrefillTile *tiles;
-    int32_t n_tiles;
+    int32_t n_tiles;  // even: two per CTA
     float *pm, *pl, *pacc;  // same partial layout as AttnArgs
     int32_t n_heads, n_kv, group, causal, split_keys;
     float scale_log2;

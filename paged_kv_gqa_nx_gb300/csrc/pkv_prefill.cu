@@ -22,23 +22,28 @@
 // and contiguous launches read the same images of the same keys, so they
 // return the same bits.
 //
-// One CTA = one tile of 128 query rows -- (128 / G) consecutive tokens x the G
-// query heads that share kv head `kvh` -- and one key split.  Row m of the
-// tile is token m / G, head m % G, TMEM lane m and compute thread m (warps 0-3):
-// each thread reads its row's 64 scores of a key tile, so the softmax needs no
-// exchange between threads.  Warp 4 issues the QK MMAs, warp 6 the PV MMAs
-// (one thread each), warp 5 bulk-copies the images.  Key tiles are 64
-// positions; tile j of the CTA uses buffer j % 2 of K, V (shared memory), S
-// and P (TMEM):
-//   QK(j):  S[128 x 64]  = Q.K_j^T     A = Q0 (TMEM) / Q1 (smem), B = K_j (smem)
-//   PV(j):  D[128 x 128] = P_j.V_j     A = P0 / P1 (TMEM),        B = V_j^T (smem)
-// QK(j+1) runs while the compute warps do the softmax of tile j (offset-causal
-// mask: key p visible iff p <= q_pos = total_k - n_q + i), PV(j) after it.  p
-// is relative to a reference max that moves (and D is rescaled) only when a
+// One CTA = two tiles of 128 query rows of one row and one key split (two
+// softmax chains that share every K/V tile); a tile is (128 / G) consecutive
+// tokens x the G query heads that share kv head `kvh`.  Row m of chain c's
+// tile is token m / G, head m % G, TMEM lane m and compute thread m of warps
+// 4c .. 4c+3: each thread reads its row's 64 scores of a key tile, so the
+// softmax needs no exchange between threads.  Warps 8 and 11 issue chain 0's
+// and chain 1's QK MMAs, warp 10 the PV MMAs of both (one thread each), warp 9
+// bulk-copies the images.  Key tiles are 64 positions; tile j of chain c uses
+// S / P buffer j % 2 of the chain (TMEM), and K_j, V_j^T come through a ring
+// of three shared-memory slots, K one tile ahead of V (K_0, K_1, V_0, K_2,
+// V_1, ...):
+//   QK_c(j):  S_c[128 x 64]  = Q_c.K_j^T   A = Q0_c / Q1_c (smem), B = K_j
+//   PV_c(j):  D_c[128 x 128] = P_c.V_j     A = P0_c / P1_c (TMEM),  B = V_j^T
+// P_c(j) is written over S_c(j) (two f16 pieces take the columns of one f32).
+// QK_c(j+1) runs while the compute warps do the softmax of tile j, PV_c(j)
+// after it, and the two chains' MMAs interleave on the tensor core.
+// Offset-causal mask: key p visible iff p <= q_pos = total_k - n_q + i.  p is
+// relative to a reference max that moves (and D is rescaled) only when a
 // tile's max exceeds it by more than 2^8, which keeps every p at most 256.
-// Shared memory: Q1 32 KiB, two K and two V buffers of 32 KiB (pieces 0, 1).
-// TMEM (512 columns; two f16 per column for the A operands): Q0 [0,64),
-// S buffers [64,192), P buffers [192,320), D [384,512).
+// Shared memory: Q0 and Q1 of each chain (32 KiB each), three ring slots of
+// 32 KiB (pieces 0, 1).  TMEM (512 columns; two f16 per column for the A
+// operands): chain c's D at 128c, its S / P buffers at 256 + 128c + {0, 64}.
 #include "pkv_elem.h"
 #include "pkv_internal.h"
 #include "pkv_tcgen05.h"
@@ -54,12 +59,21 @@ constexpr int kHD = 128;
 constexpr int kKT = 64;  // keys per tile
 static_assert(kKT == kKeyTile, "one image per tile");
 constexpr uint32_t kTmemCols = 512;
-// TMEM columns: Q0 [0,64), S buffers [64,192) (64 each), P buffers [192,320)
-// (buffer b: piece 0 at 192 + 64b, piece 1 32 columns on), D [384,512)
-constexpr uint32_t kColQ0 = 0, kColS = 64, kColP = 192, kColD = 384;
-constexpr int kComputeWarps = 4;          // one thread per tile row
-constexpr int kWarpQK = 4, kWarpCopy = 5, kWarpPV = 6;
-constexpr int kThreads = 32 * 7;
+// TMEM columns: chain c's D at kColD + 128c; its S / P buffer b at
+// kColSP + 128c + 64b (P piece 0 in the first 32 columns, piece 1 in the next 32)
+constexpr uint32_t kColD = 0, kColSP = 256;
+constexpr int kChains = 2;
+constexpr int kComputeWarps = 4 * kChains;  // one thread per tile row and chain
+constexpr int kWarpQK0 = 8, kWarpCopy = 9, kWarpPV = 10, kWarpQK1 = 11;
+constexpr int kThreads = 32 * 12;
+// registers per thread: at launch (the whole register file over the CTA),
+// then the issue warpgroup (warps 8-11) after setmaxnreg.dec and the compute
+// warpgroups after setmaxnreg.inc; .inc waits until the pool holds its
+// registers, so the shares must add up to no more than the launch's
+constexpr int kLaunchRegs = 168, kIssueRegs = 88, kComputeRegs = 208;
+static_assert(kThreads * kLaunchRegs <= 65536, "launch registers exceed the register file");
+static_assert(32 * kComputeWarps * kComputeRegs + 128 * kIssueRegs <= kThreads * kLaunchRegs,
+              "register split exceeds the launch's registers");
 constexpr float kRescale = 8.f;           // lazy-rescale threshold (base 2)
 constexpr int kPExp = 7;                  // C <= kPExp + c: p * 2^(C - c) <= 2^(8 + kPExp)
 
@@ -181,12 +195,13 @@ struct ContigRowsP {
     __device__ __forceinline__ float scale() const { return 1.f; }
 };
 
-constexpr uint32_t kSmemQ1 = 32 * 1024;  // Q1: 2 k-blocks of 128 rows x 64 f16
-// one K buffer: K0, K1 (each 2 k-blocks of 64 rows x 64 f16); one V buffer:
-// V0^T, V1^T (each 1 k-block of 128 rows x 64 f16); two of each
+constexpr uint32_t kSmemQ = 64 * 1024;  // one chain's Q0, Q1: each 2 k-blocks of 128 rows x 64 f16
+// one ring slot: pieces 0, 1 of K_j (each 2 k-blocks of 64 rows x 64 f16) or
+// of V_j^T (each 1 k-block of 128 rows x 64 f16)
 constexpr uint32_t kSmemKV = 2 * kImagePlane;
 static_assert(kImagePlane == 16 * 1024, "a piece of a tile is 16 KiB");
-constexpr size_t kSmemBytes = kSmemQ1 + 4 * kSmemKV + 1024;  // + alignment slack
+constexpr int kSlots = 3;
+constexpr size_t kSmemBytes = kChains * kSmemQ + kSlots * kSmemKV + 1024;  // + alignment slack
 
 // kLoZero (images of a bf16 or fp8 pool): the K / V piece-1 planes are left
 // out -- a pool value times the tile's power of two is exact in f16 unless it
@@ -194,43 +209,65 @@ constexpr size_t kSmemBytes = kSmemQ1 + 4 * kSmemKV + 1024;  // + alignment slac
 // to an f16 subnormal (an error below 2^-38 of that magnitude) -- so they are
 // neither copied nor used.
 //
-// Per-buffer mbarriers, phase j / 2 for tile j:
-//   qkready[b]  QK(j)'s operands: K_j landed (copy warp's bytes) and S_{j-2}
-//               read (compute warps; for j < 2 their arrival after writing Q)
-//   pvready[b]  PV(j)'s operands: P_j written (compute warps), V_j landed
-//   qkdone[b]   QK(j) complete (commit)
-//   pvdone[b]   PV(j) complete (commit)
-// QK and PV are issued by two warps, each waiting once per tile: a thread's
-// mbarrier test after its own MMAs waits for them to reach the tensor core,
-// so with one issuing thread the tensor pipe drained at every wait.  No waiter
-// is ever two phases behind: each next phase needs an arrival that follows
-// the wait.
+// mbarriers.  Ring item i sits in slot i % 3, phase (i / 3) % 2:
+//   full[s]    the item's bytes landed (the copy warp's expect-tx arrival)
+//   free[s]    every MMA that reads the item complete: two commits, one per
+//              QK warp for a K item, both from the PV warp for a V item
+// Per chain c and S / P buffer b, phase (j / 2) % 2 for tile j (qready: once):
+//   qready[c]     Q_c written (compute warps of chain c)
+//   sdone[c][b]   QK_c(j) complete (commit): S_c(j) readable
+//   pready[c][b]  P_c(j) written over S_c(j) (compute warps)
+//   pvdone[c][b]  PV_c(j) complete (commit): the buffer free for QK_c(j+2)
+// The MMAs are issued by three warps, and a QK warp takes every wait of a
+// tile before its first MMA: a thread's mbarrier test after its own MMAs
+// waits for them to reach the tensor core, so a wait between MMAs drains the
+// tensor pipe unless another warp's MMAs are queued.  No waiter is ever two phases behind: each next phase needs an
+// arrival that follows the wait.
 template <int G, bool kLoZero>
 __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs a) {
     constexpr int TQ = 128 / G;  // tokens per tile
     extern __shared__ __align__(1024) unsigned char smraw[];
     unsigned char *sm = reinterpret_cast<unsigned char *>(
         (reinterpret_cast<uintptr_t>(smraw) + 1023) & ~static_cast<uintptr_t>(1023));
-    unsigned char *Q1 = sm;
-    unsigned char *Kbuf = Q1 + kSmemQ1;    // buffer b: pieces 0, 1 at b * kSmemKV + {0, kImagePlane}
-    unsigned char *Vbuf = Kbuf + 2 * kSmemKV;
-    __shared__ uint64_t bar_qkready[2], bar_pvready[2], bar_qkdone[2], bar_pvdone[2];
+    unsigned char *Qs = sm;                       // chain c: Q0 at c * kSmemQ, Q1 32 KiB on
+    unsigned char *ring = Qs + kChains * kSmemQ;  // slot s at s * kSmemKV: pieces 0, 1 (+ kImagePlane)
+    __shared__ uint64_t bar_full[kSlots], bar_free[kSlots];
+    __shared__ uint64_t bar_qready[kChains], bar_sdone[kChains][2], bar_pready[kChains][2], bar_pvdone[kChains][2];
     __shared__ uint32_t tslot;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int ti = blockIdx.x / a.n_kv;
-    const int kvh = blockIdx.x - ti * a.n_kv;
-    const PrefillTile tile = a.tiles[ti];
-    const RowDesc rd = a.rows[tile.row];
+    const int pi = blockIdx.x / a.n_kv;
+    const int kvh = blockIdx.x - pi * a.n_kv;
+    // the pair's tiles: one row and one split; the second may be absent
+    const PrefillTile t0 = a.tiles[2 * pi], t1 = a.tiles[2 * pi + 1];
+    const RowDesc rd = a.rows[t0.row];
     const int total_k = rd.past_len + rd.n_q;
-    const int n_valid_q = min(TQ, rd.n_q - tile.q0);
-    const int kend_tile =
-        a.causal ? min(total_k, total_k - rd.n_q + tile.q0 + n_valid_q) : total_k;
-    const int kbeg = tile.split * a.split_keys;
-    const int kend = min(kbeg + a.split_keys, kend_tile);
-    const int kt0 = kbeg / kKT, kt1 = (kend + kKT - 1) / kKT;
-    const int n = kt1 - kt0;  // key tiles of this CTA
-    auto ph = [](int j) { return static_cast<uint32_t>(j >> 1) & 1u; };
+    const int kbeg = t0.split * a.split_keys;
+    const int kt0 = kbeg / kKT;
+    // a tile's end within the split (kend: its last visible key + 1, at
+    // most the split's end) and its key tiles
+    auto tile_keys = [&](const PrefillTile &t, int &kend) {
+        const int n_valid_q = min(TQ, rd.n_q - t.q0);
+        const int kend_tile = a.causal ? min(total_k, total_k - rd.n_q + t.q0 + n_valid_q) : total_k;
+        kend = min(kbeg + a.split_keys, kend_tile);
+        return max(0, (kend + kKT - 1) / kKT - kt0);
+    };
+    int kend0, kend1 = 0;
+    const int n0 = tile_keys(t0, kend0);
+    int n1 = 0;
+    if (t1.row >= 0) {
+        if (t1.row == t0.row && t1.split == t0.split) {
+            n1 = tile_keys(t1, kend1);
+        } else if (tid == 0 && a.err) {
+            atomicOr(a.err, 1);  // not a pair: the second tile is dropped
+        }
+    }
+    const int n_max = max(n0, n1);  // key tiles loaded
+    auto ph = [](int j) { return static_cast<uint32_t>(j >> 1) & 1u; };        // buffer j % 2
+    auto rph = [](int i) { return static_cast<uint32_t>(i / kSlots) & 1u; };  // ring item i
+    // ring items: K_0, K_1, V_0, K_2, V_1, ..., K_{n-1}, V_{n-2}, V_{n-1}
+    auto k_item = [](int j) { return j == 0 ? 0 : 2 * j - 1; };
+    auto v_item = [&](int j) { return j + 1 < n_max ? 2 * j + 2 : 2 * j + 1; };
     // lane 0 waits (bounded), the warp learns the outcome
     auto wait_w = [&](uint64_t *bar, uint32_t parity) {
         return __shfl_sync(0xffffffffu, lane == 0 ? mbar_wait(smem_u32(bar), parity) : true, 0) != 0;
@@ -241,12 +278,17 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs a) 
         tmem_relinquish();
     }
     if (tid == 0) {
-        for (int b = 0; b < 2; ++b) {
-            // per phase: the compute warps' arrivals and the copy warp's expect-tx arrival
-            mbar_init(smem_u32(&bar_qkready[b]), kComputeWarps + 1);
-            mbar_init(smem_u32(&bar_pvready[b]), kComputeWarps + 1);
-            mbar_init(smem_u32(&bar_qkdone[b]), 1);
-            mbar_init(smem_u32(&bar_pvdone[b]), 1);
+        for (int sl = 0; sl < kSlots; ++sl) {
+            mbar_init(smem_u32(&bar_full[sl]), 1);  // the copy warp's expect-tx arrival
+            mbar_init(smem_u32(&bar_free[sl]), 2);
+        }
+        for (int c = 0; c < kChains; ++c) {
+            mbar_init(smem_u32(&bar_qready[c]), 4);  // the chain's four compute warps
+            for (int b = 0; b < 2; ++b) {
+                mbar_init(smem_u32(&bar_sdone[c][b]), 1);
+                mbar_init(smem_u32(&bar_pready[c][b]), 4);
+                mbar_init(smem_u32(&bar_pvdone[c][b]), 1);
+            }
         }
     }
     fence_before_sync();
@@ -254,112 +296,141 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs a) 
     fence_after_sync();
     const uint32_t tbase = tslot;
     bool ok = true;
-    const int32_t *slots = a.img_slot + a.img_tile0[tile.row];  // images of the row's key tiles
+    const int32_t *slots = a.img_slot + a.img_tile0[t0.row];  // images of the row's key tiles
     auto image = [&](int32_t slot) {
         return a.img + (static_cast<size_t>(slot) * a.n_kv + kvh) * kImageBytes;
     };
 
-    if (warp == kWarpCopy) {
-        // ---------------- copy warp (lane 0 copies) ----------------
-        // Buffer b is refilled with tile j + 2 as soon as the MMAs of tile j
-        // that read it are done; each copy arrives with its byte count on the
-        // barrier that the MMA warps wait on.
-        constexpr uint32_t planes = kLoZero ? 1u : 2u;  // pieces 0 (and 1) of K / V
-        auto copy = [&](unsigned char *dst, uint64_t *bar, int j, uint32_t plane0) {
-            if (lane == 0) {
-                const unsigned char *src = image(__ldg(slots + kt0 + j)) + plane0 * kImagePlane;
-                mbar_expect_tx(smem_u32(bar), planes * kImagePlane);
-                bulk_g2s(smem_u32(dst), src, kImagePlane, smem_u32(bar));
-                if constexpr (planes == 2)
-                    bulk_g2s(smem_u32(dst + kImagePlane), src + kImagePlane, kImagePlane, smem_u32(bar));
+    if (warp >= kComputeWarps) {
+        setmaxnreg_dec<kIssueRegs>();
+        if (warp == kWarpCopy) {
+            // ---------------- copy warp (lane 0 copies) ----------------
+            // Ring item i is copied as soon as the MMAs that read item i - 3
+            // (the slot's previous item) are done; each copy arrives with its
+            // byte count on the slot's full barrier.  Item i: K_0 (i = 0),
+            // V_{n-1} (the last), else K_{(i+1)/2} (odd i) or V_{(i-2)/2}.
+            constexpr uint32_t planes = kLoZero ? 1u : 2u;  // pieces 0 (and 1) of K / V
+            int issued = 0;
+            for (int i = 0; i < 2 * n_max; ++i) {
+                const int sl = i % kSlots;
+                if (i >= kSlots && !wait_w(&bar_free[sl], rph(i - kSlots))) break;
+                const bool is_v = i > 0 && ((i & 1) == 0 || i == 2 * n_max - 1);
+                const int jt = i == 0 ? 0 : (i == 2 * n_max - 1 ? n_max - 1 : ((i & 1) ? (i + 1) >> 1 : (i - 2) >> 1));
+                if (lane == 0) {
+                    // K_j: planes 0, 1 of the image; V_j^T: planes 2, 3
+                    const unsigned char *src = image(__ldg(slots + kt0 + jt)) + (is_v ? 2 : 0) * kImagePlane;
+                    unsigned char *dst = ring + sl * kSmemKV;
+                    mbar_expect_tx(smem_u32(&bar_full[sl]), planes * kImagePlane);
+                    bulk_g2s(smem_u32(dst), src, kImagePlane, smem_u32(&bar_full[sl]));
+                    if constexpr (planes == 2)
+                        bulk_g2s(smem_u32(dst + kImagePlane), src + kImagePlane, kImagePlane,
+                                 smem_u32(&bar_full[sl]));
+                }
+                issued = i + 1;
             }
-        };
-        auto copy_k = [&](int j) { copy(Kbuf + (j & 1) * kSmemKV, &bar_qkready[j & 1], j, 0); };
-        auto copy_v = [&](int j) { copy(Vbuf + (j & 1) * kSmemKV, &bar_pvready[j & 1], j, 2); };
-        for (int j = 0; j < min(n, 2); ++j) {
-            copy_k(j);
-            copy_v(j);
-        }
-        bool cok = true;
-        for (int j = 0; j + 2 < n; ++j) {
-            cok = wait_w(&bar_qkdone[j & 1], ph(j));  // QK(j) done: K buffer free
-            if (!cok) break;
-            copy_k(j + 2);
-            cok = wait_w(&bar_pvdone[j & 1], ph(j));  // PV(j) done: V buffer free
-            if (!cok) break;
-            copy_v(j + 2);
-        }
-        // let the last copies land before the CTA's shared memory is given up
-        // (bounded if the other warps gave up)
-        for (int j = max(0, n - 2); j < n; ++j) {
-            wait_w(&bar_qkready[j & 1], ph(j));
-            wait_w(&bar_pvready[j & 1], ph(j));
-        }
-    } else if (warp == kWarpQK || warp == kWarpPV) {
-        // ---------- MMA issue warps (lane 0 issues): QK(j) / PV(j) ----------
-        const uint64_t dQ1 = desc_sw128(smem_u32(Q1));
-        const uint32_t tQ = tbase + kColQ0, tD = tbase + kColD;
-        const uint32_t idesc_s = idesc_f16(128, kKT), idesc_o = idesc_f16(128, kHD);
-        // one k-step of QK (16 dims) / PV (16 keys): three products of the
-        // pieces (products with the K / V piece-1 planes are left out when
-        // those are zero)
-        constexpr bool lo = !kLoZero;
-        if (warp == kWarpQK) {
-            for (int j = 0; j < n && ok; ++j) {
-                const int b = j & 1;
-                ok = wait_w(&bar_qkready[b], ph(j));
+            // let the last copies land before the CTA's shared memory is given
+            // up (every earlier one was waited for before its slot was
+            // refilled; bounded if the other warps gave up)
+            for (int i = max(0, issued - kSlots); i < issued; ++i) wait_w(&bar_full[i % kSlots], rph(i));
+        } else if (warp == kWarpQK0 || warp == kWarpQK1) {
+            // ---------- QK issue warps (lane 0 issues): QK_c(j) ----------
+            // one k-step (16 dims): three products of the pieces (the one with
+            // the K piece-1 plane is left out when that plane is zero).  Every
+            // K item gets one commit from each QK warp, also past the chain's
+            // last tile (after the item landed, so that it counts for its
+            // own phase).
+            constexpr bool lo = !kLoZero;
+            const int c = warp == kWarpQK1 ? 1 : 0;
+            const int n = c ? n1 : n0;
+            const uint32_t idesc_s = idesc_f16(128, kKT);
+            const uint64_t dQ0 = desc_sw128(smem_u32(Qs + c * kSmemQ));
+            const uint64_t dQ1 = desc_sw128(smem_u32(Qs + c * kSmemQ + kSmemQ / 2));
+            for (int j = 0; j < n_max && ok; ++j) {
+                const int b = j & 1, i = k_item(j), sl = i % kSlots;
+                // every wait of the tile first: K_j landed, the chain's S / P
+                // buffer free (PV_c(j-2) done) and, for tile 0, its Q written
+                ok = wait_w(&bar_full[sl], rph(i));
+                if (ok && j < n) {
+                    if (j == 0) ok = wait_w(&bar_qready[c], 0);
+                    else if (j >= 2) ok = wait_w(&bar_pvdone[c][b], ph(j - 2));
+                }
                 if (!ok) break;
                 fence_after_sync();
                 if (lane == 0) {
-                    const uint32_t tS = tbase + kColS + 64u * b;
-                    const uint64_t dK0 = desc_sw128(smem_u32(Kbuf + b * kSmemKV));
-                    const uint64_t dK1 = desc_sw128(smem_u32(Kbuf + b * kSmemKV + kImagePlane));
+                    if (j < n) {
+                        const uint64_t dK0 = desc_sw128(smem_u32(ring + sl * kSmemKV));
+                        const uint64_t dK1 = desc_sw128(smem_u32(ring + sl * kSmemKV + kImagePlane));
+                        const uint32_t tS = tbase + kColSP + 128u * c + 64u * b;
 #pragma unroll
-                    for (int s = 0; s < kHD / 16; ++s) {
-                        const uint64_t ko = ((s >> 2) * 8192u + (s & 3) * 32u) >> 4;
-                        const uint64_t qo = ((s >> 2) * 16384u + (s & 3) * 32u) >> 4;
-                        mma_f16_ts(tS, tQ + 8 * s, dK0 + ko, idesc_s, s > 0);
-                        if constexpr (lo) mma_f16_ts(tS, tQ + 8 * s, dK1 + ko, idesc_s, 1);
-                        mma_f16(tS, dQ1 + qo, dK0 + ko, idesc_s, 1);
+                        for (int s = 0; s < kHD / 16; ++s) {
+                            const uint64_t ko = ((s >> 2) * 8192u + (s & 3) * 32u) >> 4;
+                            const uint64_t qo = ((s >> 2) * 16384u + (s & 3) * 32u) >> 4;
+                            mma_f16(tS, dQ0 + qo, dK0 + ko, idesc_s, s > 0);
+                            if constexpr (lo) mma_f16(tS, dQ0 + qo, dK1 + ko, idesc_s, 1);
+                            mma_f16(tS, dQ1 + qo, dK0 + ko, idesc_s, 1);
+                        }
+                        mma_commit(smem_u32(&bar_sdone[c][b]));
                     }
-                    mma_commit(smem_u32(&bar_qkdone[b]));
+                    mma_commit(smem_u32(&bar_free[sl]));
                 }
                 __syncwarp();
             }
-        } else {
-            for (int j = 0; j < n && ok; ++j) {
-                const int b = j & 1;
-                ok = wait_w(&bar_pvready[b], ph(j));
+            if (!ok && lane == 0 && a.err) atomicOr(a.err, 2);
+        } else if (warp == kWarpPV) {
+            // ---------- PV issue warp (lane 0 issues): PV_0(j), PV_1(j) ----------
+            constexpr bool lo = !kLoZero;
+            const uint32_t idesc_o = idesc_f16(128, kHD);
+            for (int j = 0; j < n_max && ok; ++j) {
+                const int b = j & 1, i = v_item(j), sl = i % kSlots;
+                ok = wait_w(&bar_full[sl], rph(i));
                 if (!ok) break;
-                fence_after_sync();
-                if (lane == 0) {
-                    const uint32_t tP = tbase + kColP + 64u * b;
-                    const uint64_t dV0 = desc_sw128(smem_u32(Vbuf + b * kSmemKV));
-                    const uint64_t dV1 = desc_sw128(smem_u32(Vbuf + b * kSmemKV + kImagePlane));
+                const uint64_t dV0 = desc_sw128(smem_u32(ring + sl * kSmemKV));
+                const uint64_t dV1 = desc_sw128(smem_u32(ring + sl * kSmemKV + kImagePlane));
+#pragma unroll 1
+                for (int c = 0; c < kChains; ++c) {
+                    if (j >= (c ? n1 : n0)) continue;
+                    ok = wait_w(&bar_pready[c][b], ph(j));
+                    if (!ok) break;
+                    fence_after_sync();
+                    if (lane == 0) {
+                        const uint32_t tP = tbase + kColSP + 128u * c + 64u * b, tD = tbase + kColD + 128u * c;
 #pragma unroll
-                    for (int s = 0; s < kKT / 16; ++s) {
-                        const uint64_t vo = (s * 32u) >> 4;
-                        mma_f16_ts(tD, tP + 8 * s, dV0 + vo, idesc_o, j > 0 || s > 0);
-                        if constexpr (lo) mma_f16_ts(tD, tP + 8 * s, dV1 + vo, idesc_o, 1);
-                        mma_f16_ts(tD, tP + 32 + 8 * s, dV0 + vo, idesc_o, 1);
+                        for (int s = 0; s < kKT / 16; ++s) {
+                            const uint64_t vo = (s * 32u) >> 4;
+                            mma_f16_ts(tD, tP + 8 * s, dV0 + vo, idesc_o, j > 0 || s > 0);
+                            if constexpr (lo) mma_f16_ts(tD, tP + 8 * s, dV1 + vo, idesc_o, 1);
+                            mma_f16_ts(tD, tP + 32 + 8 * s, dV0 + vo, idesc_o, 1);
+                        }
+                        mma_commit(smem_u32(&bar_pvdone[c][b]));
                     }
-                    mma_commit(smem_u32(&bar_pvdone[b]));
+                    __syncwarp();
+                }
+                if (!ok) break;
+                if (lane == 0) {  // the V item's two arrivals
+                    mma_commit(smem_u32(&bar_free[sl]));
+                    mma_commit(smem_u32(&bar_free[sl]));
                 }
                 __syncwarp();
             }
+            if (!ok && lane == 0 && a.err) atomicOr(a.err, 2);
         }
-        if (!ok && lane == 0 && a.err) atomicOr(a.err, 2);
-    } else if (warp < kComputeWarps) {
-        // ---------------- compute warps: one thread per tile row ----------------
-        const int m = tid;                     // this thread's row of the tile (TMEM lane)
+    } else {
+        // -------------- compute warps: one thread per tile row and chain --------------
+        setmaxnreg_inc<kComputeRegs>();
+        const int c = warp >> 2;  // chain
+        const int n = c ? n1 : n0;
+        const int q0 = c ? t1.q0 : t0.q0, kend = c ? kend1 : kend0;
+        const uint32_t cD = kColD + 128u * c, cSP = kColSP + 128u * c;
+        unsigned char *Q0 = Qs + c * kSmemQ, *Q1 = Q0 + kSmemQ / 2;
+        const int m = tid & 127;  // this thread's row of the tile (TMEM lane)
         const int tq = m / G, g = m - (m / G) * G;
-        const int qi = tile.q0 + tq;
+        const int qi = q0 + tq;
         const bool valid = qi < rd.n_q;
         const int q_pos = total_k - rd.n_q + qi;
         const int kend_row = valid ? (a.causal ? min(q_pos + 1, total_k) : total_k) : 1;
         const int klim = min(kend_row, kend);  // keys below klim are visible to this row
-        const uint32_t tlane = static_cast<uint32_t>(32 * warp) << 16;
-        // this warp's arrival on an operand barrier, after its TMEM stores
+        const uint32_t tlane = static_cast<uint32_t>(32 * (warp & 3)) << 16;
+        // this warp's arrival on a barrier, after its TMEM stores
         auto arrive = [&](uint64_t *bar) {
             tmem_st_wait();
             fence_before_sync();
@@ -367,202 +438,185 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs a) 
             if (lane == 0) mbar_arrive(smem_u32(bar));
         };
 
-        // Q row (pre-scaled to base-2 units, then by the row's power of two):
-        // piece 0 -> TMEM, piece 1 -> shared memory.  All 32 loads of the row
-        // are issued together (one memory latency), then its largest
-        // magnitude, then the pieces.
-        int qexp;
-        {
-            const float4 *qrow = reinterpret_cast<const float4 *>(
-                a.Q + static_cast<size_t>(rd.q_row0 + (valid ? qi : 0)) * (a.n_heads * kHD) +
-                static_cast<size_t>(kvh * G + g) * kHD);
-            float4 q[kHD / 4];
+        if (n > 0) {
+            // Q row (pre-scaled to base-2 units, then by the row's power of
+            // two) -> its two pieces in shared memory.  All 32 loads of the row
+            // are issued together (one memory latency), then its largest
+            // magnitude, then the pieces.
+            int qexp;
+            {
+                const float4 *qrow = reinterpret_cast<const float4 *>(
+                    a.Q + static_cast<size_t>(rd.q_row0 + (valid ? qi : 0)) * (a.n_heads * kHD) +
+                    static_cast<size_t>(kvh * G + g) * kHD);
+                float4 q[kHD / 4];
 #pragma unroll
-            for (int j4 = 0; j4 < kHD / 4; ++j4) q[j4] = valid ? __ldg(qrow + j4) : make_float4(0.f, 0.f, 0.f, 0.f);
-            float mx = 0.f;
+                for (int j4 = 0; j4 < kHD / 4; ++j4)
+                    q[j4] = valid ? __ldg(qrow + j4) : make_float4(0.f, 0.f, 0.f, 0.f);
+                float mx = 0.f;
 #pragma unroll
-            for (int j4 = 0; j4 < kHD / 4; ++j4) {
-                q[j4].x *= a.scale_log2;
-                q[j4].y *= a.scale_log2;
-                q[j4].z *= a.scale_log2;
-                q[j4].w *= a.scale_log2;
-                mx = absmax4(mx, q[j4]);
-            }
-            qexp = f16_scale_exp(mx);
-            const float qs = pow2f(qexp);
+                for (int j4 = 0; j4 < kHD / 4; ++j4) {
+                    q[j4].x *= a.scale_log2;
+                    q[j4].y *= a.scale_log2;
+                    q[j4].z *= a.scale_log2;
+                    q[j4].w *= a.scale_log2;
+                    mx = absmax4(mx, q[j4]);
+                }
+                qexp = f16_scale_exp(mx);
+                const float qs = pow2f(qexp);
 #pragma unroll
-            for (int c4 = 0; c4 < 4; ++c4) {  // 32 dims: 16 TMEM columns, 4 chunks of Q1
-                uint32_t h0[16];
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const int c = 4 * c4 + j;  // dims 8c .. 8c + 7
-                    const float x[8] = {q[2 * c].x,     q[2 * c].y,     q[2 * c].z,     q[2 * c].w,
-                                        q[2 * c + 1].x, q[2 * c + 1].y, q[2 * c + 1].z, q[2 * c + 1].w};
+                for (int cc = 0; cc < kHD / 8; ++cc) {  // dims 8cc .. 8cc + 7: k-block cc / 8, chunk cc % 8
+                    const float x[8] = {q[2 * cc].x,     q[2 * cc].y,     q[2 * cc].z,     q[2 * cc].w,
+                                        q[2 * cc + 1].x, q[2 * cc + 1].y, q[2 * cc + 1].z, q[2 * cc + 1].w};
                     uint4 c0, c1;
                     split_chunk(x, qs, c0, c1);
-                    h0[4 * j] = c0.x;
-                    h0[4 * j + 1] = c0.y;
-                    h0[4 * j + 2] = c0.z;
-                    h0[4 * j + 3] = c0.w;
-                    // k-block c / 8, chunk c % 8 of row m
-                    *reinterpret_cast<uint4 *>(Q1 + (c >> 3) * 16384u + sw128_chunk(m, c & 7)) = c1;
+                    const uint32_t off = (cc >> 3) * 16384u + sw128_chunk(m, cc & 7);
+                    *reinterpret_cast<uint4 *>(Q0 + off) = c0;
+                    *reinterpret_cast<uint4 *>(Q1 + off) = c1;
                 }
-                tmem_st16u(tbase + tlane + kColQ0 + 16 * c4, h0);
             }
-        }
-        // Q written: the arrival that stands for "S_{j-2} read" of tiles 0 and 1
-        fence_proxy_async();
-        arrive(&bar_qkready[0]);
-        arrive(&bar_qkready[1]);
+            fence_proxy_async();  // generic-proxy writes, before the MMAs read them
+            arrive(&bar_qready[c]);
 
-        // The output accumulator lives in TMEM (D) and the P.V MMAs add into it.
-        // p is taken relative to a reference max m_ref that moves only when a
-        // tile's max exceeds it by more than kRescale (base-2 units); then D and
-        // l are rescaled once.
-        float m_ref = -INFINITY, l_run = 0.f;
-        int cexp = 0;  // C: D holds 2^C x the output's sum
-        // the tile exponents (K, V), read from the images a tile ahead
-        int2 ex_cur = make_int2(0, 0);
-        int32_t slot_next = 0;
-        if (n > 0) ex_cur = __ldg(reinterpret_cast<const int2 *>(image(__ldg(slots + kt0)) + kImageExpOff));
-        if (n > 1) slot_next = __ldg(slots + kt0 + 1);
+            // The output accumulator lives in TMEM (D) and the P.V MMAs add into
+            // it.  p is taken relative to a reference max m_ref that moves only
+            // when a tile's max exceeds it by more than kRescale (base-2 units);
+            // then D and l are rescaled once.
+            float m_ref = -INFINITY, l_run = 0.f;
+            int cexp = 0;  // C: D holds 2^C x the output's sum
+            // the tile exponents (K, V), read from the images a tile ahead
+            int2 ex_cur = __ldg(reinterpret_cast<const int2 *>(image(__ldg(slots + kt0)) + kImageExpOff));
+            int32_t slot_next = n > 1 ? __ldg(slots + kt0 + 1) : 0;
 
-        for (int j = 0; j < n; ++j) {
-            const int kt = kt0 + j, b = j & 1;
-            // S_j ready (QK(j) done)
-            ok = wait_w(&bar_qkdone[b], ph(j));
-            if (!ok) break;
-            fence_after_sync();
-            float s[kKT];
-            {
-                float h[32];
-                tmem_ld32(tbase + tlane + kColS + 64u * b, h);
-#pragma unroll
-                for (int i = 0; i < 32; ++i) s[i] = h[i];
-                tmem_ld32(tbase + tlane + kColS + 64u * b + 32, h);
-#pragma unroll
-                for (int i = 0; i < 32; ++i) s[32 + i] = h[i];
-            }
-            if (j + 2 < n) {
-                // S buffer b may be rewritten: QK(j+2) needs this arrival
-                fence_before_sync();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(smem_u32(&bar_qkready[b]));
-            }
-            const int kexp = ex_cur.x, vexp = ex_cur.y;
-
-            // scores to base-2 units: one exact factor 2^sn (two steps when
-            // 2^sn is not a normal f32); mask the keys this row does not see
-            const int sn = -(qexp + kexp);
-            const bool one = sn >= -126 && sn <= 127;
-            const float fsc = one ? pow2f(sn) : 1.f;
-            if (!one) {
-                const float sa = pow2f(sn / 2), sb = pow2f(sn - sn / 2);
-#pragma unroll
-                for (int i = 0; i < kKT; ++i) s[i] = (s[i] * sa) * sb;
-            }
-            const int base = kt * kKT;
-            if (base + kKT > klim) {
-#pragma unroll
-                for (int i = 0; i < kKT; ++i) s[i] = base + i < klim ? s[i] : -INFINITY;
-            }
-            const float row_max = tree_max(s) * fsc;
-            const bool rescale = m_ref != -INFINITY && row_max > m_ref + kRescale;
-            const float m_use = (m_ref == -INFINITY || rescale) ? row_max : m_ref;
-            // p = 2^(s - m_use): one FFMA (exact scaling, one rounding) and ex2
-            const float nm = m_use == -INFINITY ? 0.f : -m_use;
-#pragma unroll
-            for (int i = 0; i < kKT; ++i) s[i] = ex2_approx(fmaf(s[i], fsc, nm));
-            const float rowsum = tree_sum(s);
-            // C for this tile (the same in every thread)
-            const int c_new = j == 0 ? kPExp + vexp : min(cexp, kPExp + vexp);
-
-            // P buffer b free: PV(j-2) done
-            if (j >= 2) {
-                ok = wait_w(&bar_pvdone[b], ph(j - 2));
+            for (int j = 0; j < n; ++j) {
+                const int kt = kt0 + j, b = j & 1;
+                const uint32_t tSP = tbase + tlane + cSP + 64u * b;
+                // S_c(j) ready (QK_c(j) done)
+                ok = wait_w(&bar_sdone[c][b], ph(j));
                 if (!ok) break;
                 fence_after_sync();
-            }
-            // D moves (a row's reference max, or C): every PV so far done
-            // first; tcgen05.ld / st are warp-collective, so the whole warp
-            // takes the branch (rows that do not rescale multiply by 2^(C'-C))
-            const bool cmove = j > 0 && c_new != cexp;
-            const float f = rescale ? exp2f(m_ref - m_use) : 1.f;
-            if (cmove || __any_sync(0xffffffffu, rescale)) {
-                ok = wait_w(&bar_pvdone[b ^ 1], ph(j - 1));
-                if (!ok) break;
-                fence_after_sync();
-                const float fd = mul_pow2(f, c_new - cexp);
+                float s[kKT];
+                {
+                    float h[32];
+                    tmem_ld32(tSP, h);
 #pragma unroll
-                for (int c = 0; c < kHD / 32; ++c) {
-                    float dv[32];
-                    tmem_ld32(tbase + tlane + kColD + 32 * c, dv);
+                    for (int i = 0; i < 32; ++i) s[i] = h[i];
+                    tmem_ld32(tSP + 32, h);
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) dv[i] *= fd;
-                    tmem_st32(tbase + tlane + kColD + 32 * c, dv);
+                    for (int i = 0; i < 32; ++i) s[32 + i] = h[i];
                 }
-                tmem_st_wait();
-            }
-            l_run = l_run * f + rowsum;
-            m_ref = m_use;
-            cexp = c_new;
+                const int kexp = ex_cur.x, vexp = ex_cur.y;
 
-            // P_j * 2^(C - c) -> TMEM as two f16 pieces; the PV warp starts PV(j)
-            {
-                const int pe = cexp - vexp;  // <= kPExp
-                const float pf = pe >= -126 ? pow2f(pe) : 0.f;
-                uint32_t p0[32], p1[32];
+                // scores to base-2 units: one exact factor 2^sn (two steps when
+                // 2^sn is not a normal f32); mask the keys this row does not see
+                const int sn = -(qexp + kexp);
+                const bool one = sn >= -126 && sn <= 127;
+                const float fsc = one ? pow2f(sn) : 1.f;
+                if (!one) {
+                    const float sa = pow2f(sn / 2), sb = pow2f(sn - sn / 2);
 #pragma unroll
-                for (int i = 0; i < 32; ++i) split_f16x2(s[2 * i] * pf, s[2 * i + 1] * pf, p0[i], p1[i]);
-                const uint32_t tp = tbase + tlane + kColP + 64u * b;
-                tmem_st32u(tp, p0);
-                tmem_st32u(tp + 32, p1);
-            }
-            arrive(&bar_pvready[b]);
+                    for (int i = 0; i < kKT; ++i) s[i] = (s[i] * sa) * sb;
+                }
+                const int base = kt * kKT;
+                if (base + kKT > klim) {
+#pragma unroll
+                    for (int i = 0; i < kKT; ++i) s[i] = base + i < klim ? s[i] : -INFINITY;
+                }
+                const float row_max = tree_max(s) * fsc;
+                const bool rescale = m_ref != -INFINITY && row_max > m_ref + kRescale;
+                const float m_use = (m_ref == -INFINITY || rescale) ? row_max : m_ref;
+                // p = 2^(s - m_use): one FFMA (exact scaling, one rounding) and ex2
+                const float nm = m_use == -INFINITY ? 0.f : -m_use;
+#pragma unroll
+                for (int i = 0; i < kKT; ++i) s[i] = ex2_approx(fmaf(s[i], fsc, nm));
+                const float rowsum = tree_sum(s);
+                // C for this tile (the same in every thread of the chain)
+                const int c_new = j == 0 ? kPExp + vexp : min(cexp, kPExp + vexp);
 
-            // the next tile's exponents
-            if (j + 1 < n) {
-                ex_cur = __ldg(reinterpret_cast<const int2 *>(image(slot_next) + kImageExpOff));
-                if (j + 2 < n) slot_next = __ldg(slots + kt + 2);
+                // D moves (a row's reference max, or C): PV_c(j-1) done first;
+                // tcgen05.ld / st are warp-collective, so the whole warp takes
+                // the branch (rows that do not rescale multiply by 2^(C'-C))
+                const bool cmove = j > 0 && c_new != cexp;
+                const float f = rescale ? exp2f(m_ref - m_use) : 1.f;
+                if (cmove || __any_sync(0xffffffffu, rescale)) {
+                    ok = wait_w(&bar_pvdone[c][b ^ 1], ph(j - 1));
+                    if (!ok) break;
+                    fence_after_sync();
+                    const float fd = mul_pow2(f, c_new - cexp);
+#pragma unroll
+                    for (int cc = 0; cc < kHD / 16; ++cc) {  // 16 columns at a time: the scores are live
+                        float dv[16];
+                        tmem_ld16(tbase + tlane + cD + 16 * cc, dv);
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) dv[i] *= fd;
+                        tmem_st16(tbase + tlane + cD + 16 * cc, dv);
+                    }
+                }
+                l_run = l_run * f + rowsum;
+                m_ref = m_use;
+                cexp = c_new;
+
+                // P_j * 2^(C - c) over S as two f16 pieces; the PV warp starts PV_c(j)
+                {
+                    const int pe = cexp - vexp;  // <= kPExp
+                    const float pf = pe >= -126 ? pow2f(pe) : 0.f;
+                    uint32_t p0[32], p1[32];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) split_f16x2(s[2 * i] * pf, s[2 * i + 1] * pf, p0[i], p1[i]);
+                    tmem_st32u(tSP, p0);
+                    tmem_st32u(tSP + 32, p1);
+                }
+                arrive(&bar_pready[c][b]);
+
+                // the next tile's exponents
+                if (j + 1 < n) {
+                    ex_cur = __ldg(reinterpret_cast<const int2 *>(image(slot_next) + kImageExpOff));
+                    if (j + 2 < n) slot_next = __ldg(slots + kt + 2);
+                }
             }
-        }
-        // the last PV, then the result: D / l, then * 2^-C (exact); in that
-        // order the output does not overflow where D * 2^-C (up to l times it)
-        // would
-        if (ok && n > 0) ok = wait_w(&bar_pvdone[(n - 1) & 1], ph(n - 1));
-        if (!ok) {
-            if (lane == 0 && a.err) atomicOr(a.err, 2);
-        } else {
-            fence_after_sync();
-            const int h = kvh * G + g;
-            const bool direct = tile.part0 < 0;
-            float *dst = nullptr;
-            size_t pidx = 0;
-            if (direct) {
-                dst = a.out + static_cast<size_t>(rd.q_row0 + (valid ? qi : 0)) * (a.n_heads * kHD) +
-                      static_cast<size_t>(h) * kHD;
+            // the last PV, then the result: D / l, then * 2^-C (exact); in that
+            // order the output does not overflow where D * 2^-C (up to l times
+            // it) would
+            if (ok) ok = wait_w(&bar_pvdone[c][(n - 1) & 1], ph(n - 1));
+            if (!ok) {
+                if (lane == 0 && a.err) atomicOr(a.err, 2);
             } else {
-                const int n_split = (kend_tile + a.split_keys - 1) / a.split_keys;
-                const int stride = tile.stride > 0 ? tile.stride : n_split;
-                pidx = static_cast<size_t>(tile.part0 + (valid ? tq : 0) * stride + tile.split) * a.n_heads + h;
-                dst = a.pacc + pidx * kHD;
-            }
-            const float scl = direct ? 1.f / l_run : 1.f;
-#pragma unroll
-            for (int c = 0; c < kHD / 32; ++c) {
-                float dv[32];
-                tmem_ld32(tbase + tlane + kColD + 32 * c, dv);
-                if (valid) {
-#pragma unroll
-                    for (int i = 0; i < 32; i += 4)
-                        *reinterpret_cast<float4 *>(dst + 32 * c + i) =
-                            make_float4(mul_pow2(dv[i] * scl, -cexp), mul_pow2(dv[i + 1] * scl, -cexp),
-                                        mul_pow2(dv[i + 2] * scl, -cexp), mul_pow2(dv[i + 3] * scl, -cexp));
+                fence_after_sync();
+                // the tile's output placement, read again here rather than
+                // held through the loop
+                const PrefillTile tile = a.tiles[2 * pi + c];
+                const int h = kvh * G + g;
+                const bool direct = tile.part0 < 0;
+                float *dst = nullptr;
+                size_t pidx = 0;
+                if (direct) {
+                    dst = a.out + static_cast<size_t>(rd.q_row0 + (valid ? qi : 0)) * (a.n_heads * kHD) +
+                          static_cast<size_t>(h) * kHD;
+                } else {
+                    const int n_valid_q = min(TQ, rd.n_q - tile.q0);
+                    const int kend_tile =
+                        a.causal ? min(total_k, total_k - rd.n_q + tile.q0 + n_valid_q) : total_k;
+                    const int n_split = (kend_tile + a.split_keys - 1) / a.split_keys;
+                    const int stride = tile.stride > 0 ? tile.stride : n_split;
+                    pidx = static_cast<size_t>(tile.part0 + (valid ? tq : 0) * stride + tile.split) * a.n_heads + h;
+                    dst = a.pacc + pidx * kHD;
                 }
-            }
-            if (valid && !direct) {
-                a.pm[pidx] = m_ref;
-                a.pl[pidx] = l_run;
+                const float scl = direct ? 1.f / l_run : 1.f;
+#pragma unroll
+                for (int cc = 0; cc < kHD / 32; ++cc) {
+                    float dv[32];
+                    tmem_ld32(tbase + tlane + cD + 32 * cc, dv);
+                    if (valid) {
+#pragma unroll
+                        for (int i = 0; i < 32; i += 4)
+                            *reinterpret_cast<float4 *>(dst + 32 * cc + i) =
+                                make_float4(mul_pow2(dv[i] * scl, -cexp), mul_pow2(dv[i + 1] * scl, -cexp),
+                                            mul_pow2(dv[i + 2] * scl, -cexp), mul_pow2(dv[i + 3] * scl, -cexp));
+                    }
+                }
+                if (valid && !direct) {
+                    a.pm[pidx] = m_ref;
+                    a.pl[pidx] = l_run;
+                }
             }
         }
     }
@@ -573,13 +627,22 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(PrefillArgs a) 
 
 template <int G, bool kLoZero>
 cudaError_t launch_prefill_g(const PrefillArgs &a, cudaStream_t s) {
-    static PerDeviceOnce configured;  // the attribute is per function and device
+    static PerDeviceOnce configured;  // the attributes are per function and device
     const cudaError_t ce = configured.run([&]() -> cudaError_t {
+        // setmaxnreg.inc waits until the CTA's pool holds the registers asked
+        // for, so launch only if the compiled kernel starts with the registers
+        // the split was sized for
+        cudaFuncAttributes fa{};
+        cudaError_t e = cudaFuncGetAttributes(&fa, prefill_tc_kernel<G, kLoZero>);
+        if (e != cudaSuccess) return e;
+        if (fa.numRegs < kLaunchRegs || fa.maxThreadsPerBlock < kThreads) return cudaErrorInvalidConfiguration;
         return cudaFuncSetAttribute(prefill_tc_kernel<G, kLoZero>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     static_cast<int>(kSmemBytes));
     });
     if (ce != cudaSuccess) return ce;
-    const long long grid = static_cast<long long>(a.n_tiles) * a.n_kv;
+    // two tiles per CTA
+    if (a.n_tiles <= 0 || (a.n_tiles & 1)) return cudaErrorInvalidValue;
+    const long long grid = static_cast<long long>(a.n_tiles / 2) * a.n_kv;
     if (grid <= 0 || grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     prefill_tc_kernel<G, kLoZero><<<static_cast<unsigned>(grid), kThreads, kSmemBytes, s>>>(a);
     return cudaGetLastError();
