@@ -140,8 +140,9 @@ PKV_API int32_t pkv_pool_free_blocks(const pkv_pool *pool);
  *   [5] (query, key) pairs of the shared-prefix pass, [6] 1 if the call ran
  *   with the fused append, [7] operand images (64-key tile x kv heads) the
  *   call took from the image cache, [8] operand images it built, [9] keys per
- *   split of the shared-prefix pass (0 without one). */
-#define PKV_WORK_FIELDS 10
+ *   split of the shared-prefix pass (0 without one), [10] CTAs of the
+ *   tensor-core prefill launch (see pkv_set_prefill_pairing). */
+#define PKV_WORK_FIELDS 11
 PKV_API int pkv_pool_last_work(const pkv_pool *pool, int64_t *out, int32_t cap);
 
 /* Operand-image cache (no counterpart on the pages; off by default).  The
@@ -428,6 +429,18 @@ PKV_API int32_t pkv_get_fused_append(void);
  * process-wide. */
 PKV_API int pkv_set_cascade(int32_t on);
 PKV_API int32_t pkv_get_cascade(void);
+
+/* Placement of the tensor-core prefill tiles (no counterpart on the pages).
+ * A CTA of the tensor-core kernel runs two tiles of 128 query rows of one row
+ * and key split side by side, sharing every K/V tile.  mode 0: one tile per
+ * CTA; 1: neighbouring tiles in pairs; 2 (default): pairs, with the shortest
+ * pairs split into one-tile CTAs where a cost model says the launch then ends
+ * sooner on the device's SMs (paged calls; the contiguous entry points use
+ * mode 1 there).  Each tile's arithmetic is the same whatever its CTA holds,
+ * so results are bit-identical in every mode.  Returns PKV_OK, or
+ * PKV_ERR_ARG for a mode outside 0-2; process-wide. */
+PKV_API int pkv_set_prefill_pairing(int32_t mode);
+PKV_API int32_t pkv_get_prefill_pairing(void);
 
 /* Kernel launch accounting.  pkv_launch_count: kernels launched by the library
  * so far (all kinds).  When profiling is on, every launch is bracketed by CUDA

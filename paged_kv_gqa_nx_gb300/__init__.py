@@ -114,6 +114,8 @@ _SIGS = {
     "pkv_pool_set_image_cache": (_int, [_vp, ctypes.c_int64]),
     "pkv_pool_set_kv_scale": (_int, [_vp, _f32]),
     "pkv_get_cascade": (_i32, []),
+    "pkv_set_prefill_pairing": (_int, [_i32]),
+    "pkv_get_prefill_pairing": (_i32, []),
     "pkv_launch_count": (_i64, []),
     "pkv_profile_enable": (_int, [_i32]),
     "pkv_profile_reset": (_int, []),
@@ -384,10 +386,10 @@ def pkv_get_fused_append():
     return bool(_lib.pkv_get_fused_append())
 
 
-PKV_WORK_FIELDS = 10
+PKV_WORK_FIELDS = 11
 WORK_FIELD_NAMES = ("decode_units", "prefill_tiles", "prefix_tiles", "merge_items",
                     "prefill_pairs", "prefix_pairs", "fused_append", "image_hits", "image_builds",
-                    "prefix_split_keys")
+                    "prefix_split_keys", "prefill_ctas")
 
 
 def pkv_pool_last_work(pool):
@@ -411,6 +413,14 @@ def pkv_set_cascade(on):
 
 def pkv_get_cascade():
     return bool(_lib.pkv_get_cascade())
+
+
+def pkv_set_prefill_pairing(mode):
+    return _lib.pkv_set_prefill_pairing(int(mode))
+
+
+def pkv_get_prefill_pairing():
+    return _lib.pkv_get_prefill_pairing()
 
 
 def pkv_launch_count():

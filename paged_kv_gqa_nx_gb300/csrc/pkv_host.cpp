@@ -16,11 +16,13 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <array>
 #include <cmath>
 #include <atomic>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <functional>
 #include <list>
 #include <mutex>
 #include <string>
@@ -51,6 +53,7 @@ int cuda_fail(cudaError_t e, const char *what) {
 std::atomic<int32_t> g_split_keys{1024};
 std::atomic<int32_t> g_fused_append{1};
 std::atomic<int32_t> g_cascade{1};
+std::atomic<int32_t> g_prefill_pairing{2};
 std::atomic<int64_t> g_launches{0};
 
 // Optional per-launch CUDA-event timing.
@@ -598,13 +601,103 @@ int32_t unit_keys(const UnitDesc &u, const RowDesc &rd, int causal, int32_t S) {
     return std::max(0, std::min(kbeg + S, lim) - kbeg);
 }
 
+// Cost of a tensor-core prefill CTA in units of ~100 SM clocks, from clock64
+// timelines of the kernel: ~3.9k clocks per 64-key tile with two chains,
+// ~2.7k with one, ~15k per CTA besides (query rows, first copies, output).
+constexpr int64_t kPairTileCost = 39, kSingleTileCost = 27, kCtaCost = 150;
+
+// Tile pairs -> the CTA list (two entries per CTA, the second may be absent).
+// mode 0: one tile per CTA; 1: every pair; 2: pairs, with the k shortest
+// split into two one-tile CTAs where that ends the launch sooner on n_sm SMs
+// (the hardware hands CTAs to free SMs in order; every entry is n_kv CTAs).
+// A chain's arithmetic does not depend on its partner, so the outputs are the
+// same bits in every mode.
+void place_pairs(const std::vector<std::array<PrefillTile, 2>> &pairs, const std::vector<int32_t> &len0,
+                 const std::vector<int32_t> &len1, int32_t mode, int32_t n_kv, int32_t n_sm,
+                 std::vector<PrefillTile> &out) {
+    const size_t np = pairs.size();
+    if (mode == 0) {
+        for (const auto &pr : pairs)
+            for (const PrefillTile &t : pr)
+                if (t.row >= 0) {
+                    out.push_back(t);
+                    out.push_back(kNoTile);
+                }
+        return;
+    }
+    std::vector<size_t> full;  // pairs with both tiles, cheapest first
+    for (size_t i = 0; i < np; ++i)
+        if (pairs[i][1].row >= 0) full.push_back(i);
+    std::stable_sort(full.begin(), full.end(), [&](size_t x, size_t y) {
+        return std::max(len0[x], len1[x]) < std::max(len0[y], len1[y]);
+    });
+    const int64_t ctas = static_cast<int64_t>(np) * std::max(1, n_kv);
+    const int64_t rounds = n_sm > 0 ? (ctas + n_sm - 1) / n_sm : 0;
+    int32_t best_k = 0;
+    if (mode == 2 && n_sm > 0 && n_kv > 0 && !full.empty() && rounds <= 16) {
+        std::vector<char> split(np, 0);
+        std::vector<int64_t> heap;
+        // finish time of the launch with the k cheapest pairs split: pairs (and
+        // one-tile entries) in list order, then the split tiles, longest first
+        auto makespan = [&](int32_t k) {
+            std::fill(split.begin(), split.end(), 0);
+            for (int32_t i = 0; i < k; ++i) split[full[i]] = 1;
+            heap.assign(static_cast<size_t>(n_sm), 0);
+            auto put = [&](int64_t cost) {
+                for (int32_t h = 0; h < n_kv; ++h) {
+                    std::pop_heap(heap.begin(), heap.end(), std::greater<int64_t>());
+                    heap.back() += cost;
+                    std::push_heap(heap.begin(), heap.end(), std::greater<int64_t>());
+                }
+            };
+            for (size_t i = 0; i < np; ++i) {
+                if (split[i]) continue;
+                const bool two = pairs[i][1].row >= 0;
+                put(two ? kPairTileCost * std::max(len0[i], len1[i]) + kCtaCost
+                        : kSingleTileCost * len0[i] + kCtaCost);
+            }
+            for (int32_t i = k - 1; i >= 0; --i) {
+                put(kSingleTileCost * len0[full[i]] + kCtaCost);
+                put(kSingleTileCost * len1[full[i]] + kCtaCost);
+            }
+            return *std::max_element(heap.begin(), heap.end());
+        };
+        int64_t best = makespan(0);
+        for (int64_t r = 1; r <= rounds; ++r) {
+            const int64_t keep = r * n_sm / n_kv;  // pair entries that fill r rounds
+            const int32_t k = static_cast<int32_t>(std::max<int64_t>(0, std::min<int64_t>(
+                static_cast<int64_t>(full.size()), static_cast<int64_t>(np) - keep)));
+            if (k == 0) continue;
+            const int64_t t = makespan(k);
+            if (t < best) {
+                best = t;
+                best_k = k;
+            }
+        }
+    }
+    std::vector<char> split(np, 0);
+    for (int32_t i = 0; i < best_k; ++i) split[full[i]] = 1;
+    for (size_t i = 0; i < np; ++i)
+        if (!split[i]) {
+            out.push_back(pairs[i][0]);
+            out.push_back(pairs[i][1]);
+        }
+    for (int32_t i = best_k - 1; i >= 0; --i)
+        for (const PrefillTile &t : pairs[full[i]]) {
+            out.push_back(t);
+            out.push_back(kNoTile);
+        }
+}
+
 // S: keys per split-K decode unit; prefill_split: keys per split of the
 // tensor-core prefill rows (0: kPrefillSplitFactor * S); prefix_split: keys
 // per split of the shared-prefix pass (0: S); allow_tc false: every row to the
-// split-K decode kernels.
+// split-K decode kernels; n_kv, n_sm: kv heads and the device's SMs, for the
+// placement of the prefill tiles (0: not known).
 void build_work(std::vector<RowDesc> &rows, int causal, int32_t S, int32_t head_dim,
                 int32_t group, WorkList &w, const std::vector<Cascade> &cas = {},
-                int32_t prefix_split = 0, int32_t prefill_split = 0, bool allow_tc = true) {
+                int32_t prefix_split = 0, int32_t prefill_split = 0, bool allow_tc = true,
+                int32_t n_kv = 0, int32_t n_sm = 0) {
     std::vector<UnitDesc> tail;
     w.units.clear();
     w.tiles.clear();
@@ -618,6 +711,16 @@ void build_work(std::vector<RowDesc> &rows, int causal, int32_t S, int32_t head_
     const bool tc_shape = allow_tc && prefill_shape(head_dim, group);
     const int32_t TQ = tc_shape ? 128 / group : 0;
     const int32_t Sp = prefill_split > 0 ? prefill_split : S * kPrefillSplitFactor;
+    std::vector<std::array<PrefillTile, 2>> pairs;
+    std::vector<int32_t> len0, len1;  // key tiles of each pair's tiles
+    auto key_tiles = [&](const PrefillTile &t) {
+        if (t.row < 0) return 0;
+        const RowDesc &rd = rows[t.row];
+        const int32_t total_k = rd.past_len + rd.n_q, nv = std::min(TQ, rd.n_q - t.q0);
+        const int32_t kend_tile = causal ? std::min(total_k, total_k - rd.n_q + t.q0 + nv) : total_k;
+        const int32_t kbeg = t.split * Sp, kend = std::min(kbeg + Sp, kend_tile);
+        return std::max(0, ceil_div(kend, kKeyTile) - kbeg / kKeyTile);
+    };
     for (int32_t r = 0; r < n_real; ++r) {
         if (member[r]) continue;
         const RowDesc &rd = rows[r];
@@ -651,8 +754,9 @@ void build_work(std::vector<RowDesc> &rows, int causal, int32_t S, int32_t head_
                     PrefillTile u = sp < x.ns ? PrefillTile{r, x.q0, sp, x.part0} : kNoTile;
                     PrefillTile v = y && sp < y->ns ? PrefillTile{r, y->q0, sp, y->part0} : kNoTile;
                     if (u.row < 0) std::swap(u, v);
-                    w.tiles.push_back(u);
-                    w.tiles.push_back(v);
+                    pairs.push_back({u, v});
+                    len0.push_back(key_tiles(u));
+                    len1.push_back(key_tiles(v));
                 }
             }
             continue;
@@ -673,6 +777,7 @@ void build_work(std::vector<RowDesc> &rows, int causal, int32_t S, int32_t head_
             }
         }
     }
+    place_pairs(pairs, len0, len1, g_prefill_pairing.load(), n_kv, n_sm, w.tiles);
     w.units.insert(w.units.end(), tail.begin(), tail.end());
     // longest units first, so that the grid's last CTAs are its shortest and
     // the launch drains quickly (the order changes no result)
@@ -849,7 +954,9 @@ int run_layer(pkv_seq *const *seqs, int32_t M, const int32_t *n_q, const float *
     if (attend && g_cascade.load() != 0 && prefill_shape(head_dim, group))
         cas = find_cascades(seqs, M, n_q, p->bs);
     const int32_t Sp = cas.empty() ? 0 : prefix_split_keys(cas, group, n_kv_heads, p->n_sm);
-    if (attend) build_work(rows, causal, S_dec, head_dim, group, w, cas, Sp, S * kPrefillSplitFactor);
+    if (attend)
+        build_work(rows, causal, S_dec, head_dim, group, w, cas, Sp, S * kPrefillSplitFactor, true, n_kv_heads,
+                   p->n_sm);
     // the decode kernels that take the append themselves: the f32 kernel for
     // groups 1, 2, 4 and the narrow-pool kernel for its shapes (head_dim 128)
     const bool fuse_shape = head_dim == 128 &&
@@ -872,7 +979,8 @@ int run_layer(pkv_seq *const *seqs, int32_t M, const int32_t *n_q, const float *
                                                count_tiles(w.tiles),
                                                count_tiles(w.ctiles),
                                                static_cast<int64_t>(w.merges.size()),
-                                               pairs, ppairs, fuse ? 1 : 0, 0, 0, Sp};
+                                               pairs, ppairs, fuse ? 1 : 0, 0, 0, Sp,
+                                               static_cast<int64_t>(w.tiles.size() / 2) * n_kv_heads};
         std::copy(vals, vals + PKV_WORK_FIELDS, p->last_work);
     }
 
@@ -1884,6 +1992,13 @@ int pkv_set_cascade(int32_t on) {
     return PKV_OK;
 }
 int32_t pkv_get_cascade(void) { return g_cascade.load(); }
+
+int pkv_set_prefill_pairing(int32_t mode) {
+    if (mode < 0 || mode > 2) return fail(PKV_ERR_ARG, "prefill pairing mode must be 0, 1 or 2");
+    g_prefill_pairing.store(mode);
+    return PKV_OK;
+}
+int32_t pkv_get_prefill_pairing(void) { return g_prefill_pairing.load(); }
 
 int64_t pkv_launch_count(void) { return g_launches.load(); }
 
