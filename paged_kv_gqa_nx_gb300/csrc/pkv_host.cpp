@@ -607,9 +607,11 @@ int32_t unit_keys(const UnitDesc &u, const RowDesc &rd, int causal, int32_t S) {
 constexpr int64_t kPairTileCost = 39, kSingleTileCost = 27, kCtaCost = 150;
 
 // Tile pairs -> the CTA list (two entries per CTA, the second may be absent).
-// mode 0: one tile per CTA; 1: every pair; 2: pairs, with the k shortest
-// split into two one-tile CTAs where that ends the launch sooner on n_sm SMs
-// (the hardware hands CTAs to free SMs in order; every entry is n_kv CTAs).
+// mode 0: one tile per CTA; 1: every pair; 2: pairs, with the last k of the
+// list split into two one-tile CTAs (which then run last, beside the pairs
+// that read the same rows' images, so those are still in L2) where that ends
+// the launch sooner on n_sm SMs (the hardware hands CTAs to free SMs in
+// order; every entry is n_kv CTAs).
 // A chain's arithmetic does not depend on its partner, so the outputs are the
 // same bits in every mode.
 void place_pairs(const std::vector<std::array<PrefillTile, 2>> &pairs, const std::vector<int32_t> &len0,
@@ -625,20 +627,17 @@ void place_pairs(const std::vector<std::array<PrefillTile, 2>> &pairs, const std
                 }
         return;
     }
-    std::vector<size_t> full;  // pairs with both tiles, cheapest first
-    for (size_t i = 0; i < np; ++i)
+    std::vector<size_t> full;  // pairs with both tiles, last in the list first
+    for (size_t i = np; i-- > 0;)
         if (pairs[i][1].row >= 0) full.push_back(i);
-    std::stable_sort(full.begin(), full.end(), [&](size_t x, size_t y) {
-        return std::max(len0[x], len1[x]) < std::max(len0[y], len1[y]);
-    });
     const int64_t ctas = static_cast<int64_t>(np) * std::max(1, n_kv);
     const int64_t rounds = n_sm > 0 ? (ctas + n_sm - 1) / n_sm : 0;
     int32_t best_k = 0;
     if (mode == 2 && n_sm > 0 && n_kv > 0 && !full.empty() && rounds <= 16) {
         std::vector<char> split(np, 0);
         std::vector<int64_t> heap;
-        // finish time of the launch with the k cheapest pairs split: pairs (and
-        // one-tile entries) in list order, then the split tiles, longest first
+        // finish time of the launch with the last k pairs split: pairs (and
+        // one-tile entries) in list order, then the split tiles in list order
         auto makespan = [&](int32_t k) {
             std::fill(split.begin(), split.end(), 0);
             for (int32_t i = 0; i < k; ++i) split[full[i]] = 1;
