@@ -512,13 +512,13 @@ std::vector<Cascade> find_cascades(pkv_seq *const *seqs, int32_t M, const int32_
     return out;
 }
 
-// Keys per split of the shared-prefix pass.  Its CTAs (query tile x kv head
-// x split) each pay a fixed cost -- loading and splitting 128 query rows,
-// writing 128 partial rows -- worth about kPrefixCtaTiles 64-key tiles of
-// work, so the split count of the longest prefix is the one that minimises
+// Keys per split of the shared-prefix pass.  Its CTAs (pair of query tiles x
+// kv head x split) each pay a fixed cost -- loading and splitting the query
+// rows, writing the partial rows -- worth about kPrefixCtaTiles 64-key tiles
+// of work, so the split count of the longest prefix is the one that minimises
 // rounds x (tiles per CTA + that cost) on the device's SMs: for 128 forks of
-// an 8192-token prefix (32 CTAs per split on 152 SMs), 4 splits of 2048 keys
-// in one round rather than 8 of 1024 in 1.7.
+// an 8192-token prefix (16 CTAs per split on 152 SMs), 9 splits of 960 keys
+// in one round.
 constexpr int32_t kPrefixCtaTiles = 7;
 int32_t prefix_split_keys(const std::vector<Cascade> &cas, int32_t group, int32_t n_kv, int32_t n_sm) {
     const int32_t TQ = 128 / group;
