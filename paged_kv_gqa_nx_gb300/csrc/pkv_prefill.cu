@@ -11,10 +11,11 @@
 // 64-key tile of K and one of V per kv head (the largest magnitude over the
 // tile).  The scores are scaled back exactly before the softmax.  The
 // probabilities p (at most 2^8, see the lazy rescale) of a tile whose V
-// exponent is c are multiplied by 2^(C - c), where C is a per-CTA exponent
-// that only decreases and stays at most 7 + c for every tile seen, so they
-// stay at most 2^15; the accumulator then holds 2^C x the output's sum, is
-// rescaled exactly when C moves, and is scaled back by 2^-C at the end.
+// exponent is c are multiplied by 2^(C - c), where C is an exponent of the
+// query tile (one per softmax chain) that only decreases and stays at most
+// 7 + c for every key tile seen, so they stay at most 2^15; the accumulator
+// then holds 2^C x the output's sum, is rescaled exactly when C moves, and is
+// scaled back by 2^-C at the end.
 //
 // The K/V operands of a tile come as an image made by the split pass (below)
 // from the pool's rows or from a contiguous K/V pair: the pieces already in
