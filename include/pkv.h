@@ -433,12 +433,14 @@ PKV_API int32_t pkv_get_cascade(void);
 /* Placement of the tensor-core prefill tiles (no counterpart on the pages).
  * A CTA of the tensor-core kernel runs two tiles of 128 query rows of one row
  * and key split side by side, sharing every K/V tile.  mode 0: one tile per
- * CTA; 1: neighbouring tiles in pairs; 2 (default): pairs, with the shortest
- * pairs split into one-tile CTAs where a cost model says the launch then ends
- * sooner on the device's SMs (paged calls; the contiguous entry points use
- * mode 1 there).  Each tile's arithmetic is the same whatever its CTA holds,
- * so results are bit-identical in every mode.  Returns PKV_OK, or
- * PKV_ERR_ARG for a mode outside 0-2; process-wide. */
+ * CTA; 1: neighbouring tiles in pairs; 2 (default): pairs, with the last
+ * pairs of the launch split into one-tile CTAs where a cost model says the
+ * launch then ends sooner on the device's SMs (paged calls; the contiguous
+ * entry points use mode 1 there).  The shared-prefix pass pairs its tiles in
+ * every mode (its split size is chosen for pairs).  Each tile's arithmetic is
+ * the same whatever its CTA holds, so results are bit-identical in every
+ * mode.  Returns PKV_OK, or PKV_ERR_ARG for a mode outside 0-2;
+ * process-wide. */
 PKV_API int pkv_set_prefill_pairing(int32_t mode);
 PKV_API int32_t pkv_get_prefill_pairing(void);
 
